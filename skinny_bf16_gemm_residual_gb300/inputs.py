@@ -1,0 +1,96 @@
+"""Seeded synthetic inputs for the skinny BF16 projection GEMM + residual.
+
+This module only draws random numbers; it holds none of the operation's
+arithmetic, so both the CUDA path's tests/benchmark and the CPU oracle's
+checks can take their inputs from it.
+
+Shapes and distributions follow the decode-sized latent-MoE projection of the
+vLLM "benchmark_k3_cutedsl_residual.py" page (module docstring and the N / K
+constants: BF16[M,3584] @ BF16[7168,3584].T + BF16[M,7168]).  That page draws
+every operand from a unit normal on the device; here W is scaled by 1/sqrt(K)
+so that A.W^T has unit variance like R, which keeps Y ~ N(0, 2) and makes the
+BF16 rounding of the output a relative 2^-9 effect.  Values are drawn on the
+host (torch CPU generator, one per seed) in the order A, W, R and then copied
+wherever they are needed, so every consumer sees the same bits.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+
+import torch
+
+N_LATENT_MOE = 7168
+K_LATENT_MOE = 3584
+
+
+@dataclass
+class Problem:
+    """One synthetic problem: A [M,K], W [N,K], R [M,N], all torch.bfloat16 (CPU)."""
+
+    A: torch.Tensor
+    W: torch.Tensor
+    R: torch.Tensor
+    seed: int
+
+    @property
+    def M(self) -> int:
+        return self.A.shape[0]
+
+    @property
+    def N(self) -> int:
+        return self.W.shape[0]
+
+    @property
+    def K(self) -> int:
+        return self.A.shape[1]
+
+
+def make_problem(M: int, N: int = N_LATENT_MOE, K: int = K_LATENT_MOE, seed: int = 0,
+                 w_scale: float | None = None) -> Problem:
+    """A ~ N(0,1), W ~ N(0,1) * w_scale (default 1/sqrt(K)), R ~ N(0,1), BF16.
+
+    Draw order A, W, R from ``torch.Generator().manual_seed(seed)``."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    if w_scale is None:
+        w_scale = 1.0 / math.sqrt(K) if K > 0 else 1.0
+    A = torch.randn((M, K), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    W = (torch.randn((N, K), generator=g, dtype=torch.float32) * w_scale).to(torch.bfloat16)
+    R = torch.randn((M, N), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    return Problem(A, W, R, seed)
+
+
+def make_weights(N: int, K: int, seed: int, w_scale: float | None = None) -> torch.Tensor:
+    """One W [N,K] BF16 ~ N(0,1)/sqrt(K) from its own seed (CPU)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    if w_scale is None:
+        w_scale = 1.0 / math.sqrt(K) if K > 0 else 1.0
+    return (torch.randn((N, K), generator=g, dtype=torch.float32) * w_scale).to(torch.bfloat16)
+
+
+def make_rows(M: int, cols: int, seed: int) -> torch.Tensor:
+    """[M, cols] BF16 ~ N(0,1) from its own seed (CPU): activations or residuals."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    return torch.randn((M, cols), generator=g, dtype=torch.float32).to(torch.bfloat16)
+
+
+def random_bf16_bits(shape, seed: int, lo_exp: int = -12, hi_exp: int = 6) -> torch.Tensor:
+    """BF16 values with random sign, a random exponent in [lo_exp, hi_exp] and a
+    random 7-bit fraction (CPU).  A wide exponent spread makes rounding matter."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    sign = torch.randint(0, 2, shape, generator=g) * 2 - 1
+    expo = torch.randint(lo_exp, hi_exp + 1, shape, generator=g).to(torch.float64)
+    frac = torch.randint(0, 128, shape, generator=g).to(torch.float64)
+    vals = sign * (1.0 + frac / 128.0) * torch.pow(2.0, expo)
+    return vals.to(torch.bfloat16)  # exactly representable: 8 significant bits
+
+
+def integer_bf16(shape, lo: int, hi: int, seed: int) -> torch.Tensor:
+    """Integer values in [lo, hi] stored as BF16 (exact for |v| <= 256) (CPU)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    return torch.randint(lo, hi + 1, shape, generator=g).to(torch.bfloat16)

@@ -1,0 +1,280 @@
+"""Pins for the CPU oracle: checks that tie it to the definition of the
+operation and to the mathematics, not to itself.
+
+Each ``check_*`` takes a loaded oracle (``oracle.Oracle``) and raises
+AssertionError on a mismatch.  ``test_oracle_pins.py`` runs them on the real
+oracle; ``test_oracle_mutants.py`` runs them on builds with one planted
+mistake each and expects at least one to fail.
+
+Independent formulations used here:
+  * exact rational arithmetic (fractions.Fraction) and a rounding to BF16 by
+    bisection over the ordered BF16 grid (no frexp/ldexp, unlike the oracle);
+  * hand-worked fixtures under tests/golden/;
+  * special cases whose answer is a library rounding (torch float32 -> bf16,
+    IEEE round-to-nearest-even) or an exact integer (numpy int64 matmul).
+"""
+from __future__ import annotations
+
+import os
+import struct
+from fractions import Fraction
+
+import numpy as np
+import torch
+
+from skinny_bf16_gemm_residual_gb300 import inputs
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+# ---------------------------------------------------------------- helpers
+def bits(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def bf16_value(pattern: int) -> Fraction:
+    """Exact value of a finite BF16 bit pattern."""
+    f = struct.unpack("<f", struct.pack("<I", (pattern & 0xFFFF) << 16))[0]
+    return Fraction(f)
+
+
+_POS_MAX = 0x7F7F
+
+
+def rne_bf16_exact(x: Fraction) -> int:
+    """Round an exact rational to BF16 (ties to even) by bisection on the grid.
+
+    Positive finite patterns 0x0000..0x7F7F are ordered by value, so the two
+    neighbours of |x| are found by binary search; the nearer wins, and a tie
+    goes to the pattern with a zero last bit.  Above the largest finite value,
+    the next grid point is 2^128 (infinity)."""
+    if x == 0:
+        return 0x0000
+    sign = 0x8000 if x < 0 else 0x0000
+    ax = abs(x)
+    top = bf16_value(_POS_MAX)
+    if ax >= top:
+        nxt = Fraction(2) ** 128
+        if ax - top < nxt - ax:
+            return sign | _POS_MAX
+        return sign | 0x7F80  # tie or above: the even neighbour is infinity
+    lo, hi = 0, _POS_MAX  # invariant: value(lo) <= ax < value(hi)
+    while hi - lo > 1:
+        mid = (lo + hi) // 2
+        if bf16_value(mid) <= ax:
+            lo = mid
+        else:
+            hi = mid
+    dlo, dhi = ax - bf16_value(lo), bf16_value(hi) - ax
+    if dlo < dhi:
+        p = lo
+    elif dhi < dlo:
+        p = hi
+    else:
+        p = lo if lo % 2 == 0 else hi
+    return sign | p
+
+
+def exact_reference(A: np.ndarray, W: np.ndarray, R: np.ndarray) -> np.ndarray:
+    """Brute force: Y[m,n] = rne(sum_k A[m,k] W[n,k] + R[m,n]) in exact rationals."""
+    M, K = A.shape
+    N = W.shape[0]
+    a = [[bf16_value(int(v)) for v in row] for row in A]
+    w = [[bf16_value(int(v)) for v in row] for row in W]
+    out = np.empty((M, N), dtype=np.uint16)
+    for m in range(M):
+        for n in range(N):
+            s = sum((a[m][k] * w[n][k] for k in range(K)), Fraction(0))
+            out[m, n] = rne_bf16_exact(s + bf16_value(int(R[m, n])))
+    return out
+
+
+def load_rounding_fixture():
+    rows = []
+    with open(os.path.join(GOLDEN, "bf16_rne.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            x, y = line.split()
+            rows.append((float.fromhex(x), int(y, 16)))
+    return rows
+
+
+def load_crafted_fixture():
+    cases, cur = [], None
+    with open(os.path.join(GOLDEN, "crafted_gemm.txt")) as f:
+        for raw in f:
+            line = raw.strip()
+            if not line or line.startswith("#"):
+                continue
+            if line.startswith("case "):
+                cur = {"name": line[5:].split(":", 1)[0]}
+                cases.append(cur)
+            elif ":" not in line:
+                cur["M"], cur["N"], cur["K"] = (int(v) for v in line.split())
+            else:
+                key, vals = line.split(":", 1)
+                vals = vals.split()
+                if key == "Y":
+                    cur["Y"] = np.array([int(v, 16) for v in vals], dtype=np.uint16)
+                else:
+                    f32 = np.array([float.fromhex(v) for v in vals], dtype=np.float32)
+                    cur[key] = bits(torch.from_numpy(f32).to(torch.bfloat16))
+    for c in cases:
+        c["A"] = c["A"].reshape(c["M"], c["K"])
+        c["W"] = c["W"].reshape(c["N"], c["K"])
+        c["R"] = c["R"].reshape(c["M"], c["N"])
+        c["Y"] = c["Y"].reshape(c["M"], c["N"])
+    return cases
+
+
+def _eq(got: np.ndarray, want: np.ndarray, what: str):
+    if not np.array_equal(got, want):
+        bad = np.argwhere(got != want)
+        i = tuple(bad[0])
+        raise AssertionError(f"{what}: {len(bad)} mismatches, first at {i}: "
+                             f"got 0x{int(got[i]):04X} want 0x{int(want[i]):04X}")
+
+
+def _library_round_f32(x: np.ndarray) -> np.ndarray:
+    """float64 values that are exact in float32 -> BF16 via torch's float32
+    conversion (IEEE round-to-nearest-even)."""
+    f32 = x.astype(np.float32)
+    assert np.array_equal(f32.astype(np.float64), x), "value not exact in float32"
+    return bits(torch.from_numpy(f32).to(torch.bfloat16))
+
+
+def _f64(b: np.ndarray) -> np.ndarray:
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+# ---------------------------------------------------------------- pins
+def check_rounding_fixture(orc):
+    rows = load_rounding_fixture()
+    got = orc.round_bf16(np.array([x for x, _ in rows]))
+    want = np.array([y for _, y in rows], dtype=np.uint16)
+    _eq(got, want, "BF16 round-to-nearest-even fixture")
+
+
+def check_rounding_vs_exact_bisection(orc):
+    """Random doubles near grid points and midpoints, checked against the
+    bisection rounding on exact rationals."""
+    rng = np.random.default_rng(1234)
+    base = rng.integers(0x0001, 0x7F7F, 400)
+    vals = []
+    for p in base:
+        v = float(bf16_value(int(p)))
+        nxt = float(bf16_value(int(p) + 1))
+        mid = (v + nxt) / 2
+        for x in (v, mid, np.nextafter(mid, 0), np.nextafter(mid, np.inf), (v + mid) / 2):
+            vals.append(x)
+            vals.append(-x)
+    vals = np.array(vals, dtype=np.float64)
+    got = orc.round_bf16(vals)
+    want = np.array([rne_bf16_exact(Fraction(float(x))) for x in vals], dtype=np.uint16)
+    _eq(got, want, "rounding vs exact bisection")
+
+
+def check_crafted_fixture(orc):
+    for c in load_crafted_fixture():
+        _eq(orc.gemm_residual(c["A"], c["W"], c["R"], threads=1), c["Y"], f"crafted case {c['name']}")
+
+
+def check_brute_force_exact(orc):
+    """4x8x16 and a few other tiny shapes: oracle == exact rational brute force."""
+    for (M, N, K, seed) in ((4, 8, 16, 1), (3, 5, 7, 2), (1, 1, 1, 3), (2, 9, 33, 4), (5, 3, 64, 5)):
+        A = bits(inputs.random_bf16_bits((M, K), seed))
+        W = bits(inputs.random_bf16_bits((N, K), seed + 100))
+        R = bits(inputs.random_bf16_bits((M, N), seed + 200))
+        _eq(orc.gemm_residual(A, W, R, threads=2), exact_reference(A, W, R),
+            f"brute force {M}x{N}x{K}")
+
+
+def check_identity_weight(orc):
+    """N = K and W = I: Y = bf16(A + R), a single library rounding."""
+    K = 24
+    A = bits(inputs.random_bf16_bits((5, K), 11, lo_exp=-4, hi_exp=4))
+    R = bits(inputs.random_bf16_bits((5, K), 12, lo_exp=-4, hi_exp=4))
+    W = bits(torch.eye(K, dtype=torch.bfloat16))
+    want = _library_round_f32(_f64(A) + _f64(R))
+    _eq(orc.gemm_residual(A, W, R), want, "identity W")
+
+
+def check_one_hot_activation(orc):
+    """A[m,:] = e_j(m): Y[m,n] = bf16(W[n, j(m)] + R[m,n])."""
+    M, N, K = 6, 10, 12
+    W = bits(inputs.random_bf16_bits((N, K), 21, lo_exp=-4, hi_exp=4))
+    R = bits(inputs.random_bf16_bits((M, N), 22, lo_exp=-4, hi_exp=4))
+    js = [(3 * m + 1) % K for m in range(M)]
+    A_t = torch.zeros((M, K), dtype=torch.bfloat16)
+    for m, j in enumerate(js):
+        A_t[m, j] = 1.0
+    A = bits(A_t)
+    want = _library_round_f32(_f64(W)[:, js].T + _f64(R))
+    _eq(orc.gemm_residual(A, W, R), want, "one-hot A")
+
+
+def check_zero_operands(orc):
+    """W = 0 or A = 0 leaves Y == R (R has no zeros, so no -0 question);
+    R = 0 with integer A, W gives the exact integer product."""
+    M, N, K = 3, 7, 9
+    A = bits(inputs.random_bf16_bits((M, K), 31))
+    W = bits(inputs.random_bf16_bits((N, K), 32))
+    R = bits(inputs.random_bf16_bits((M, N), 33))
+    zA = np.zeros_like(A)
+    zW = np.zeros_like(W)
+    _eq(orc.gemm_residual(A, zW, R), R, "W = 0")
+    _eq(orc.gemm_residual(zA, W, R), R, "A = 0")
+    Ai = inputs.integer_bf16((M, K), -3, 3, 34)
+    Wi = inputs.integer_bf16((N, K), -3, 3, 35)
+    prod = Ai.to(torch.int64) @ Wi.to(torch.int64).T
+    want = bits(prod.to(torch.bfloat16))  # |prod| <= 81: exact
+    _eq(orc.gemm_residual(bits(Ai), bits(Wi), np.zeros((M, N), np.uint16)), want, "R = 0")
+
+
+def check_integer_exact(orc):
+    """A, W in [-2,2], R in [-8,8], K <= 32: |y| <= 136, every step exact."""
+    for (M, N, K, s) in ((16, 40, 32, 41), (1, 128, 32, 42), (7, 9, 5, 43)):
+        Ai = inputs.integer_bf16((M, K), -2, 2, s)
+        Wi = inputs.integer_bf16((N, K), -2, 2, s + 1)
+        Ri = inputs.integer_bf16((M, N), -8, 8, s + 2)
+        y = Ai.to(torch.int64) @ Wi.to(torch.int64).T + Ri.to(torch.int64)
+        _eq(orc.gemm_residual(bits(Ai), bits(Wi), bits(Ri)), bits(y.to(torch.bfloat16)),
+            f"integer-valued {M}x{N}x{K}")
+
+
+def check_transpose_symmetry(orc):
+    """With R = 0, swapping the roles of A and W transposes Y."""
+    M, N, K = 4, 6, 20
+    A = bits(inputs.random_bf16_bits((M, K), 51))
+    W = bits(inputs.random_bf16_bits((N, K), 52))
+    y1 = orc.gemm_residual(A, W, np.zeros((M, N), np.uint16))
+    y2 = orc.gemm_residual(W, A, np.zeros((N, M), np.uint16))
+    _eq(y1, np.ascontiguousarray(y2.T), "transpose symmetry")
+
+
+def check_strided_rows(orc):
+    """Row strides larger than the row width give the same result as a
+    contiguous copy (the operand view is what is multiplied)."""
+    M, N, K = 3, 5, 8
+    A = bits(inputs.random_bf16_bits((M, 2 * K), 61))
+    W = bits(inputs.random_bf16_bits((N, K), 62))
+    R = bits(inputs.random_bf16_bits((M, 3 * N), 63))
+    a_view, r_view = A[:, K:], R[:, N:2 * N]
+    want = exact_reference(np.ascontiguousarray(a_view), W, np.ascontiguousarray(r_view))
+    _eq(orc.gemm_residual(a_view, W, r_view), want, "strided operands")
+
+
+ALL_CHECKS = [
+    check_rounding_fixture,
+    check_rounding_vs_exact_bisection,
+    check_crafted_fixture,
+    check_brute_force_exact,
+    check_identity_weight,
+    check_one_hot_activation,
+    check_zero_operands,
+    check_integer_exact,
+    check_transpose_symmetry,
+    check_strided_rows,
+]
