@@ -1,0 +1,517 @@
+"""Benchmark: skinny BF16 GEMM + fused residual on GB300.
+
+Workload (the decode-sized latent-MoE projection of the vLLM
+"benchmark_k3_cutedsl_residual.py" page): Y = bf16(A . W^T + R) with
+N = 7168, K = 3584, for each M in {1, 2, 4, 8, 16}, with 4 rotating copies of
+W (~205 MB together, more than the 126 MB L2) so every call streams W from
+HBM.  One step = one call per (M, copy) pair = 20 calls, captured once in a
+CUDA graph and replayed (the page's graph-replay method).  Synthetic inputs:
+A, R ~ N(0,1), W ~ N(0,1)/sqrt(K), BF16, seeded.
+
+Prints ONE JSON line (rank 0).  `value` is achieved HBM GB/s over the whole
+step: algorithmic bytes 2*(N*K + M*K + 2*M*N) per call, summed over the
+step's calls, divided by the device time per step (CUDA events).
+Per-M microseconds per call (median of repeats, the page's summary) are in
+`per_m`.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (FP64 C loop) on the host cores on a
+bounded sample of the same workload, as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "µs/call and achieved HBM GB/s, BF16 skinny GEMM+residual, M=1..16, N7168 K3584"
+N_DIM, K_DIM = 7168, 3584
+M_LIST = (1, 2, 4, 8, 16)
+COPIES = 4
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def alg_bytes(M: int, N: int = N_DIM, K: int = K_DIM) -> int:
+    return 2 * (N * K + M * K + 2 * M * N)
+
+
+def alg_flops(M: int, N: int = N_DIM, K: int = K_DIM) -> int:
+    return 2 * M * N * K
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"]))}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "skinny_bf16_gemm_residual_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel: str):
+    """dram bytes per launch from the committed ncu summary for `kernel`, if it
+    was taken on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_traffic.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    vals = {}
+    for line in text.splitlines():
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("source_digest") != kernel_source_digest():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+        self._t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self._t:
+            self._t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": sorted(reasons), "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ stats
+def summarize(samples):
+    """Median, p10, p90 (linear interpolation), mean and cv% of samples (the
+    vLLM benchmark page's summary statistics)."""
+    ordered = sorted(samples)
+
+    def pct(f):
+        pos = f * (len(ordered) - 1)
+        lo, hi = math.floor(pos), math.ceil(pos)
+        if lo == hi:
+            return ordered[lo]
+        w = pos - lo
+        return ordered[lo] * (1 - w) + ordered[hi] * w
+
+    mean = statistics.mean(samples)
+    return {"median_us": statistics.median(samples), "p10_us": pct(0.1), "p90_us": pct(0.9),
+            "mean_us": mean, "cv_pct": statistics.pstdev(samples) / mean * 100.0 if mean else 0.0}
+
+
+# ------------------------------------------------------------------ dist
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def dist_max(value: float, ws: int, device=None) -> float:
+    """Max of a host float over ranks (timing aggregation; no data-path collective)."""
+    if ws == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def dist_barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ workload
+def make_workload(device, m_list=M_LIST, copies=COPIES):
+    """Rotating W copies (seed s) shared by every M; per-M activation and
+    per-(M, copy) residuals.  Generated on the host, copied to the device."""
+    import torch
+
+    from skinny_bf16_gemm_residual_gb300 import inputs
+
+    Ws_cpu = [inputs.make_weights(N_DIM, K_DIM, seed=s) for s in range(copies)]
+    Ws = [w.to(device) for w in Ws_cpu]
+    per_m = {}
+    for M in m_list:
+        A_cpu = inputs.make_rows(M, K_DIM, seed=10_000 + M)
+        Rs_cpu = [inputs.make_rows(M, N_DIM, seed=20_000 + 100 * M + s) for s in range(copies)]
+        per_m[M] = {
+            "A_cpu": A_cpu, "R_cpu": Rs_cpu,
+            "A": A_cpu.to(device), "R": [r.to(device) for r in Rs_cpu],
+            "Y": [torch.empty((M, N_DIM), dtype=torch.bfloat16, device=device) for _ in range(copies)],
+        }
+    return Ws_cpu, Ws, per_m
+
+
+def capture(calls, stream):
+    """Eager warm-up of every call, then one CUDA graph holding all of them."""
+    import torch
+
+    with torch.cuda.stream(stream):
+        for fn in calls:
+            fn()
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for fn in calls:
+            fn()
+    return g
+
+
+def time_graph(g, stream, replays: int, repeats: int):
+    import torch
+
+    out = []
+    for _ in range(repeats):
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for _ in range(replays):
+            g.replay()
+        e.record(stream)
+        e.synchronize()
+        out.append(s.elapsed_time(e) * 1000.0 / replays)  # us per replay
+    return out
+
+
+# ------------------------------------------------------------------ CPU arms
+def cpu_oracle_rate(Ws_cpu, per_m_cpu, m_list, budget_s: float, n_rows: int | None = None):
+    """Time the oracle (all host cores) on the workload, bounded by budget_s.
+    Returns (GB/s of algorithmic bytes, threads, sample description, seconds)."""
+    import oracle
+
+    threads = os.cpu_count() or 1
+    lib = oracle.load()
+    n_rows = n_rows or N_DIM
+    done_bytes, t0, calls = 0, time.perf_counter(), 0
+    while True:
+        for M in m_list:
+            A = per_m_cpu[M]["A_cpu"]
+            R = per_m_cpu[M]["R_cpu"][calls % len(Ws_cpu)][:, :n_rows]
+            W = Ws_cpu[calls % len(Ws_cpu)][:n_rows]
+            lib.gemm_residual(A, W, R, threads=threads)
+            done_bytes += alg_bytes(M, n_rows, K_DIM)
+        calls += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    desc = (f"{calls} pass(es) over M in {list(m_list)} with the first {n_rows} of {N_DIM} "
+            f"output columns (K={K_DIM}), FP64 C oracle, {threads} threads")
+    return done_bytes / el / 1e9, threads, desc, el
+
+
+def run_reference(args):
+    """Reference arm: the CPU oracle as it stands, on the host cores."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    from skinny_bf16_gemm_residual_gb300 import inputs
+
+    m_list = tuple(int(x) for x in args.m_list.split(","))
+    Ws_cpu = [inputs.make_weights(N_DIM, K_DIM, seed=s) for s in range(COPIES)]
+    per_m = {M: {"A_cpu": inputs.make_rows(M, K_DIM, seed=10_000 + M),
+                 "R_cpu": [inputs.make_rows(M, N_DIM, seed=20_000 + 100 * M + s) for s in range(COPIES)]}
+             for M in m_list}
+    import oracle
+
+    lib = oracle.load()
+    threads = os.cpu_count() or 1
+    # Size one step so that warmup + steps fit in about args.ref_budget seconds.
+    t0 = time.perf_counter()
+    probe_rows = 256
+    for M in m_list:
+        lib.gemm_residual(per_m[M]["A_cpu"], Ws_cpu[0][:probe_rows], per_m[M]["R_cpu"][0][:, :probe_rows],
+                          threads=threads)
+    per_row = (time.perf_counter() - t0) / probe_rows
+    total_steps = args.steps + args.warmup
+    rows = int(args.ref_budget / max(total_steps, 1) / max(per_row, 1e-9))
+    rows = max(8, min(N_DIM, rows // 8 * 8))
+    times, nbytes = [], sum(alg_bytes(M, rows, K_DIM) for M in m_list)
+    for i in range(total_steps):
+        c = i % COPIES
+        t0 = time.perf_counter()
+        for M in m_list:
+            lib.gemm_residual(per_m[M]["A_cpu"], Ws_cpu[c][:rows], per_m[M]["R_cpu"][c][:, :rows],
+                              threads=threads)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = nbytes * len(times) / total / 1e9
+    sample = (f"each step: one call per M in {list(m_list)} on the first {rows} of {N_DIM} output "
+              f"columns (W rows), K={K_DIM}, rotating 4 W copies; FP64 C oracle")
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "impl": "reference",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total / len(times) * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"M sweep {list(m_list)}, N={N_DIM}, K={K_DIM}, 4 rotating W/R copies "
+                               f"(bounded CPU sample: {rows} output columns per call)"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_ours(args):
+    import torch
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    device = torch.device("cuda", torch.cuda.current_device())
+    import skinny_bf16_gemm_residual_gb300 as sgr
+
+    sgr.sgr_init(device.index)
+    m_list = tuple(int(x) for x in args.m_list.split(","))
+    Ws_cpu, Ws, per_m = make_workload(device, m_list)
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    w_total = COPIES * N_DIM * K_DIM * 2
+    assert w_total > 1.5 * l2, "rotating W copies must exceed L2"
+    stream = torch.cuda.Stream(device=device)
+
+    def call(M, c):
+        d = per_m[M]
+        return lambda: sgr.skinny_gemm_residual(d["A"], Ws[c], d["R"][c], d["Y"][c], stream=stream)
+
+    step_calls = [call(M, c) for M in m_list for c in range(COPIES)]
+    launches_per_step = len(step_calls)
+    bytes_per_step = sum(alg_bytes(M) for M in m_list for _ in range(COPIES))
+    g_step = capture(step_calls, stream)
+
+    # per-M microseconds per call: one graph of the 4 copies, repeats x replays
+    per_m_out = {}
+    peaks, peak_src = load_peaks()
+    for M in m_list:
+        g = capture([call(M, c) for c in range(COPIES)], stream)
+        for _ in range(20):
+            g.replay()
+        stream.synchronize()
+        samples = [t / COPIES for t in time_graph(g, stream, args.replays, args.repeats)]
+        s = summarize(samples)
+        gbs = alg_bytes(M) / (s["median_us"] * 1e-6) / 1e9
+        per_m_out[str(M)] = {
+            "us_per_call": s["median_us"], "p10_us": s["p10_us"], "p90_us": s["p90_us"],
+            "cv_pct": s["cv_pct"], "gbs": gbs, "frac_of_hbm_peak": gbs / peaks["hbm_gbs"],
+            "path": {1: "simt", 2: "tc"}.get(sgr.sgr_select_path(M, N_DIM, K_DIM), "?"),
+        }
+        del g
+
+    # headline: K timed steps of the whole M sweep
+    clocks = ClockSampler(device.index)
+    clocks.start()
+    for _ in range(args.warmup):
+        g_step.replay()
+    stream.synchronize()
+    dist_barrier(ws)
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        g_step.replay()
+    ev1.record(stream)
+    ev1.synchronize()
+    torch.cuda.synchronize()
+    dist_barrier(ws)
+    clk = clocks.stop()
+    elapsed_ms = ev0.elapsed_time(ev1)
+    elapsed_ms = dist_max(elapsed_ms, ws, device)
+    ms_per_step = elapsed_ms / args.steps
+    value = bytes_per_step * ws * args.steps / (elapsed_ms * 1e-3) / 1e9
+
+    # end to end through the public call with host buffers (pinned), W resident
+    e2e = run_e2e(sgr, per_m, Ws, m_list, device, stream, max(3, min(args.steps, args.e2e_steps)))
+    e2e_seconds = dist_max(e2e["seconds"], ws, device)  # slowest rank
+    e2e_value = bytes_per_step * ws * e2e["steps"] / e2e_seconds / 1e9
+
+    if rank != 0:
+        return 0
+
+    avg_launch_s = elapsed_ms * 1e-3 / (args.steps * launches_per_step)
+    achieved = bytes_per_step / launches_per_step / avg_launch_s / 1e9
+    kernels = sorted({v["path"] for v in per_m_out.values()})
+    dominant = "simt_skinny_kernel" if kernels == ["simt"] else "tc_skinny_kernel" if kernels == ["tc"] else "mixed"
+    traffic = committed_traffic(dominant)
+    roofline = {
+        "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+        "frac": achieved / peaks["hbm_gbs"], "traffic": traffic, "peak_source": peak_src,
+        "kernel": dominant,
+        "bytes_per_launch": bytes_per_step / launches_per_step,
+        "note": "algorithmic bytes 2*(N*K + M*K + 2*M*N) per call averaged over the step's calls / "
+                "average launch duration over the timed region (CUDA events on the launch stream)",
+    }
+    cpu = None
+    if ws == 1 and not args.no_cpu_baseline:
+        rate, threads, desc, secs = cpu_oracle_rate(Ws_cpu, per_m, m_list, args.cpu_budget)
+        cpu = {"value": rate, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": desc,
+               "seconds": secs}
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {
+            "workload": f"M sweep {list(m_list)} x {COPIES} rotating W/R copies, N={N_DIM}, K={K_DIM}",
+            "calls_per_step": launches_per_step, "l2": "inputs larger than L2 (4 W copies = "
+            f"{w_total / 1e6:.0f} MB vs L2 {l2 / 1e6:.0f} MB); no flush",
+            "launch": "one CUDA graph per step, PDL on", "parallelism": "replicas" if ws > 1 else "single GPU",
+        },
+        "per_m": per_m_out,
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": e2e["h2d"],
+                "d2h_bytes_per_step": e2e["d2h"], "steps": e2e["steps"]},
+        "gpu_launches": args.steps * launches_per_step,
+        "clocks": clk,
+        "peaks": {"hbm_gbs": peaks["hbm_gbs"], "source": peak_src},
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+def run_e2e(sgr, per_m, Ws, m_list, device, stream, steps: int):
+    """Each step: for every (M, copy) call, copy A and R from pinned host
+    memory, run the public call, copy Y back; W stays resident (weights)."""
+    import torch
+
+    host = {}
+    h2d = d2h = 0
+    for M in m_list:
+        d = per_m[M]
+        host[M] = {"A": d["A_cpu"].pin_memory(), "R": [r.pin_memory() for r in d["R_cpu"]],
+                   "Y": [torch.empty((M, N_DIM), dtype=torch.bfloat16).pin_memory() for _ in range(COPIES)],
+                   "Ad": torch.empty_like(d["A"]), "Rd": [torch.empty_like(r) for r in d["R"]],
+                   "Yd": [torch.empty_like(y) for y in d["Y"]]}
+        h2d += COPIES * (M * K_DIM + M * N_DIM) * 2
+        d2h += COPIES * M * N_DIM * 2
+
+    def one_step():
+        with torch.cuda.stream(stream):
+            for M in m_list:
+                h = host[M]
+                for c in range(COPIES):
+                    h["Ad"].copy_(h["A"], non_blocking=True)
+                    h["Rd"][c].copy_(h["R"][c], non_blocking=True)
+                    sgr.skinny_gemm_residual(h["Ad"], Ws[c], h["Rd"][c], h["Yd"][c], stream=stream)
+                    h["Y"][c].copy_(h["Yd"][c], non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(3):
+        one_step()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one_step()
+    secs = time.perf_counter() - t0
+    return {"seconds": secs, "steps": steps, "h2d": h2d, "d2h": d2h}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--m-list", default=",".join(str(m) for m in M_LIST))
+    ap.add_argument("--repeats", type=int, default=21)
+    ap.add_argument("--replays", type=int, default=200)
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--ref-budget", type=float, default=90.0, help="seconds for the reference arm")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,192 @@
+/*
+ * skinny_gemm_residual.h -- C ABI of the GB300 (sm_103a) skinny BF16
+ * projection GEMM with a fused residual add.
+ *
+ * Operation (vLLM "benchmark_k3_cutedsl_residual.py", module docstring and
+ * its correctness() reference; shape constants N = 7168, K = 3584):
+ *
+ *     Y[m,n] = bf16( sum_k A[m,k] * W[n,k] + R[m,n] ),  0 <= m < M, 0 <= n < N
+ *
+ * with FP32 accumulation and a single round-to-nearest-even to BF16 in the
+ * epilogue.  The vLLM "fused_add_multicast_skinny_gemm" page rounds the FP32
+ * product to BF16 before adding the residual; this library rounds once.
+ *
+ * Types and layouts.  A, W, R, Y hold IEEE bfloat16 values, row-major with
+ * unit inner stride:
+ *     A  [M, K]  row stride lda >= K      (activations)
+ *     W  [N, K]  row stride K (contiguous) (nn.Linear weight layout)
+ *     R  [M, N]  row stride ldr >= N      (residual)
+ *     Y  [M, N]  row stride ldy >= N      (output)
+ * Strides are in elements.  The plain entry point uses lda = K, ldr = ldy = N.
+ * The row-strided forms cover the case on the "fused_add_multicast_skinny_gemm"
+ * page where the residual is a column slice of a wider [M, hidden_dim] buffer,
+ * and a chain where the next layer's A is a column slice of this layer's Y.
+ *
+ * Ownership.  Every pointer is a DEVICE pointer owned by the caller and must
+ * stay valid until the work queued on `stream` has finished.  The library keeps
+ * no reference to them after the call returns.  A per-device workspace used by
+ * the tensor-core split-K path is owned by the library, allocated once per
+ * device by sgr_init() (or lazily on first use) and released at process exit.
+ *
+ * Asynchrony.  Calls enqueue work on `stream` (a cudaStream_t; NULL is the
+ * legacy default stream) and return without synchronising.  Kernels launch
+ * with programmatic dependent launch (PDL) unless SGR_FLAG_NO_PDL is given:
+ * a kernel starts streaming W while the previous kernel on the stream is still
+ * finishing, and reads A and R and writes Y only after that kernel completes.
+ * Contract that follows: W must not be written by the kernel queued
+ * immediately before on the same stream.  A and R may be.
+ *
+ * CUDA graphs.  Calls may be captured into a CUDA graph after sgr_init() has
+ * run for the device (the first call does it otherwise, and that first call
+ * must not be inside a capture).
+ *
+ * Errors.  Every entry point returns an sgr_status.  Argument errors are
+ * detected on the host before anything is enqueued, so nothing runs and the
+ * output is untouched:
+ *   SGR_ERR_NULL        a required pointer is NULL
+ *   SGR_ERR_SHAPE       M, N or K negative; N or K not a multiple of 8;
+ *                       a row stride smaller than its row width
+ *   SGR_ERR_ALIGN       a pointer not 16-byte aligned, or a row stride that is
+ *                       not a multiple of 8 elements (16 bytes)
+ *   SGR_ERR_ALIAS       Y overlaps A or W, or overlaps R other than being
+ *                       exactly R (Y == R with ldy == ldr, an in-place residual
+ *                       update, is allowed: each element of R is read before
+ *                       the same thread writes it)
+ *   SGR_ERR_UNSUPPORTED a size beyond the library's limits, or a forced
+ *                       path/config that cannot run this shape
+ *   SGR_ERR_LAUNCH      the CUDA launch itself failed (cudaGetLastError)
+ *   SGR_ERR_DEVICE      no usable device, or device set-up failed
+ * Empty problems (M == 0 or N == 0) return SGR_OK and enqueue nothing.
+ * K == 0 makes the product an empty sum, so Y = R (a device copy).
+ * Device-side waits are bounded (about one second); a wait that runs out
+ * records a code readable with sgr_device_error() instead of hanging.
+ */
+#ifndef SKINNY_GEMM_RESIDUAL_H
+#define SKINNY_GEMM_RESIDUAL_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SGR_ABI_VERSION 1
+
+typedef enum {
+  SGR_OK = 0,
+  SGR_ERR_NULL = 1,
+  SGR_ERR_SHAPE = 2,
+  SGR_ERR_ALIGN = 3,
+  SGR_ERR_ALIAS = 4,
+  SGR_ERR_UNSUPPORTED = 5,
+  SGR_ERR_LAUNCH = 6,
+  SGR_ERR_DEVICE = 7
+} sgr_status;
+
+/* Flags for the _ex / _config entry points. */
+#define SGR_FLAG_NO_PDL 0x1u /* launch without programmatic dependent launch */
+
+/* Kernel paths. */
+#define SGR_PATH_AUTO 0 /* per-M table */
+#define SGR_PATH_SIMT 1 /* CUDA-core streaming kernel, M <= 16 */
+#define SGR_PATH_TC 2   /* tcgen05 / tensor-memory kernel */
+
+/*
+ * Y = bf16(A . W^T + R) with contiguous operands (lda = K, ldr = ldy = N).
+ * The operation of the vLLM "benchmark_k3_cutedsl_residual.py" page
+ * (module docstring), at any M >= 0 and N, K multiples of 8.
+ * `stream` is a cudaStream_t.  Returns an sgr_status.
+ */
+int skinny_gemm_residual(const void* A, const void* W, const void* R, void* Y,
+                         int M, int N, int K, void* stream);
+
+/*
+ * Same operation with row strides (elements) for A, R and Y and launch flags
+ * (SGR_FLAG_*).  Row-strided residual as on the vLLM
+ * "fused_add_multicast_skinny_gemm" page (its shared_shard operand has row
+ * stride hidden_dim).  Returns an sgr_status.
+ */
+int skinny_gemm_residual_ex(const void* A, int64_t lda, const void* W,
+                            const void* R, int64_t ldr, void* Y, int64_t ldy,
+                            int M, int N, int K, unsigned flags, void* stream);
+
+/*
+ * Launch configuration, the analogue of the Config(block_size,
+ * outputs_per_block, k_unroll, vector_width) record that the
+ * "benchmark_k3_cutedsl_residual.py" page sweeps.  Zero in any field means
+ * "the library's choice for this M".
+ */
+typedef struct {
+  int path;           /* SGR_PATH_* */
+  int ctas_per_sm;    /* persistent grid = SM count x ctas_per_sm (SIMT, TC) */
+  int rows_per_stage; /* SIMT: W rows per shared-memory ring stage */
+  int stages;         /* ring depth (SIMT, TC) */
+  int split_units;    /* TC: K blocks (of 64) per work unit; 0 = balanced stream-K */
+  int reserved[3];    /* must be zero */
+} sgr_config;
+
+/*
+ * As skinny_gemm_residual_ex with an explicit configuration (for sweeps and
+ * tests).  A configuration that cannot run the shape returns
+ * SGR_ERR_UNSUPPORTED without launching.  `cfg` may be NULL (library choice).
+ */
+int skinny_gemm_residual_config(const void* A, int64_t lda, const void* W,
+                                const void* R, int64_t ldr, void* Y, int64_t ldy,
+                                int M, int N, int K, const sgr_config* cfg,
+                                unsigned flags, void* stream);
+
+/*
+ * Host-only argument check with exactly the rules the entry points apply.
+ * Never touches the GPU or dereferences a pointer.  Returns an sgr_status.
+ */
+int sgr_validate(const void* A, int64_t lda, const void* W, const void* R,
+                 int64_t ldr, const void* Y, int64_t ldy, int M, int N, int K);
+
+/*
+ * Kernel path the library chooses for this shape with SGR_PATH_AUTO
+ * (SGR_PATH_SIMT or SGR_PATH_TC), or a negative sgr_status if none can run
+ * it.  Host-only.
+ */
+int sgr_select_path(int M, int N, int K);
+
+/*
+ * The configuration the library uses for this shape on the given path
+ * (SGR_PATH_AUTO resolves first).  Writes *cfg.  Host-only apart from a
+ * device-attribute query for the SM count of `device`.  Returns an sgr_status.
+ */
+int sgr_default_config(int device, int M, int N, int K, int path, sgr_config* cfg);
+
+/*
+ * One-time per-device set-up: SM count, kernel attributes, split-K workspace
+ * and counters, device error word.  Idempotent and thread-safe.  Call before
+ * capturing calls into a CUDA graph.  Returns an sgr_status.
+ */
+int sgr_init(int device);
+
+/*
+ * Read (and with clear != 0, reset) the device error word of `device`, which
+ * a kernel sets when one of its bounded waits runs out (0 = no error).
+ * Synchronises with the device.  Returns an sgr_status.
+ */
+int sgr_device_error(int device, unsigned* code, int clear);
+
+/*
+ * Resource usage of the kernel the library would launch for (path, M, K):
+ * registers per thread, local (spill) bytes per thread, dynamic shared
+ * memory per CTA and threads per CTA.  Like the register/spill query on the
+ * "benchmark_k3_cutedsl_residual.py" page (resource_usage).  Host query.
+ */
+int sgr_kernel_resources(int device, int path, int M, int N, int K, int* regs,
+                         int* local_bytes, int* smem_bytes, int* threads);
+
+/* Static text for an sgr_status value. */
+const char* sgr_status_string(int status);
+
+/* SGR_ABI_VERSION of the built library; bindings compare it with their own. */
+int sgr_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SKINNY_GEMM_RESIDUAL_H */

@@ -1,0 +1,43 @@
+"""Skinny BF16 projection GEMM with a fused residual add, for GB300 (sm_103a).
+
+    Y[M,N] = bf16( A[M,K] . W[N,K]^T  (FP32 accumulate)  +  R[M,N] )
+
+The work runs in hand-written CUDA kernels behind the C ABI declared in
+include/skinny_gemm_residual.h; this package is a ctypes binding with the
+same function names (see ``binding``), the build step (``build``) and the
+seeded synthetic input generators (``inputs``).  The library is loaded on
+first use; there is no CPU fallback.
+"""
+from .binding import (  # noqa: F401
+    ABI_VERSION,
+    SGR_ERR_ALIAS,
+    SGR_ERR_ALIGN,
+    SGR_ERR_DEVICE,
+    SGR_ERR_LAUNCH,
+    SGR_ERR_NULL,
+    SGR_ERR_SHAPE,
+    SGR_ERR_UNSUPPORTED,
+    SGR_FLAG_NO_PDL,
+    SGR_OK,
+    SGR_PATH_AUTO,
+    SGR_PATH_SIMT,
+    SGR_PATH_TC,
+    SgrError,
+    load,
+    make_config,
+    sgr_abi_version,
+    sgr_config,
+    sgr_default_config,
+    sgr_device_error,
+    sgr_init,
+    sgr_kernel_resources,
+    sgr_select_path,
+    sgr_status_string,
+    sgr_validate_ptr,
+    skinny_gemm_residual,
+    skinny_gemm_residual_config,
+    skinny_gemm_residual_config_ptr,
+    skinny_gemm_residual_ex,
+    skinny_gemm_residual_ex_ptr,
+    skinny_gemm_residual_ptr,
+)

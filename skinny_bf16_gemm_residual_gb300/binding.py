@@ -1,0 +1,282 @@
+"""ctypes binding of the C ABI in include/skinny_gemm_residual.h.
+
+Argument marshalling only: every step of the operation runs in the CUDA
+library.  Functions carry the C names.  Tensor arguments are torch CUDA
+tensors of dtype bfloat16 (2-D, unit inner stride); raw-pointer forms
+(``*_ptr``) take integers.  There is no CPU fallback: if the library is not
+built or does not load, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+ABI_VERSION = 1  # must equal SGR_ABI_VERSION of the loaded library
+
+SGR_OK = 0
+SGR_ERR_NULL = 1
+SGR_ERR_SHAPE = 2
+SGR_ERR_ALIGN = 3
+SGR_ERR_ALIAS = 4
+SGR_ERR_UNSUPPORTED = 5
+SGR_ERR_LAUNCH = 6
+SGR_ERR_DEVICE = 7
+
+SGR_FLAG_NO_PDL = 0x1
+
+SGR_PATH_AUTO = 0
+SGR_PATH_SIMT = 1
+SGR_PATH_TC = 2
+
+
+class SgrError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: status {status} ({sgr_status_string(status)})")
+
+
+class sgr_config(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int), ("ctas_per_sm", ctypes.c_int),
+                ("rows_per_stage", ctypes.c_int), ("stages", ctypes.c_int),
+                ("split_units", ctypes.c_int), ("reserved", ctypes.c_int * 3)]
+
+    def as_dict(self) -> dict:
+        return {"path": self.path, "ctas_per_sm": self.ctas_per_sm,
+                "rows_per_stage": self.rows_per_stage, "stages": self.stages,
+                "split_units": self.split_units}
+
+
+_lock = threading.Lock()
+_lib = None
+
+# Entry points declared in include/skinny_gemm_residual.h.
+EXPORTS = (
+    "skinny_gemm_residual",
+    "skinny_gemm_residual_ex",
+    "skinny_gemm_residual_config",
+    "sgr_validate",
+    "sgr_select_path",
+    "sgr_default_config",
+    "sgr_init",
+    "sgr_device_error",
+    "sgr_kernel_resources",
+    "sgr_status_string",
+    "sgr_abi_version",
+)
+
+
+def library_path() -> str:
+    return os.environ.get("SGR_LIBRARY", _build.LIB_PATH)
+
+
+def load(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load (building first if needed) the CUDA library; raise if impossible."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if build_if_missing and path == _build.LIB_PATH and _build.is_stale(path):
+            _build.build_library()
+        if not os.path.exists(path):
+            raise RuntimeError(f"CUDA library not found at {path}; run the build step")
+        lib = ctypes.CDLL(path)
+        vp, i64, I, U = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint
+        ip = ctypes.POINTER(ctypes.c_int)
+        lib.skinny_gemm_residual.argtypes = [vp, vp, vp, vp, I, I, I, vp]
+        lib.skinny_gemm_residual_ex.argtypes = [vp, i64, vp, vp, i64, vp, i64, I, I, I, U, vp]
+        lib.skinny_gemm_residual_config.argtypes = [vp, i64, vp, vp, i64, vp, i64, I, I, I,
+                                                    ctypes.POINTER(sgr_config), U, vp]
+        lib.sgr_validate.argtypes = [vp, i64, vp, vp, i64, vp, i64, I, I, I]
+        lib.sgr_select_path.argtypes = [I, I, I]
+        lib.sgr_default_config.argtypes = [I, I, I, I, I, ctypes.POINTER(sgr_config)]
+        lib.sgr_init.argtypes = [I]
+        lib.sgr_device_error.argtypes = [I, ctypes.POINTER(ctypes.c_uint), I]
+        lib.sgr_kernel_resources.argtypes = [I, I, I, I, I, ip, ip, ip, ip]
+        lib.sgr_status_string.argtypes = [I]
+        lib.sgr_status_string.restype = ctypes.c_char_p
+        lib.sgr_abi_version.argtypes = []
+        for name in EXPORTS:
+            if name != "sgr_status_string":
+                getattr(lib, name).restype = ctypes.c_int
+        v = lib.sgr_abi_version()
+        if v != ABI_VERSION:
+            raise RuntimeError(f"library ABI version {v} != binding ABI version {ABI_VERSION}; rebuild")
+        _lib = lib
+        return lib
+
+
+# ---------------------------------------------------------------- host-only
+def sgr_status_string(status: int) -> str:
+    return load().sgr_status_string(int(status)).decode()
+
+
+def sgr_abi_version() -> int:
+    return load().sgr_abi_version()
+
+
+def sgr_validate_ptr(A: int, lda: int, W: int, R: int, ldr: int, Y: int, ldy: int,
+                     M: int, N: int, K: int) -> int:
+    """Host-only argument check on raw addresses; returns the status."""
+    return load().sgr_validate(A, lda, W, R, ldr, Y, ldy, M, N, K)
+
+
+def sgr_select_path(M: int, N: int, K: int) -> int:
+    return load().sgr_select_path(M, N, K)
+
+
+def sgr_default_config(M: int, N: int, K: int, path: int = SGR_PATH_AUTO, device: int | None = None) -> sgr_config:
+    import torch
+
+    dev = torch.cuda.current_device() if device is None else device
+    c = sgr_config()
+    rc = load().sgr_default_config(dev, M, N, K, path, ctypes.byref(c))
+    if rc != SGR_OK:
+        raise SgrError(rc, "sgr_default_config")
+    return c
+
+
+def sgr_init(device: int | None = None) -> None:
+    import torch
+
+    dev = torch.cuda.current_device() if device is None else device
+    rc = load().sgr_init(dev)
+    if rc != SGR_OK:
+        raise SgrError(rc, "sgr_init")
+
+
+def sgr_device_error(device: int | None = None, clear: bool = True) -> int:
+    import torch
+
+    dev = torch.cuda.current_device() if device is None else device
+    code = ctypes.c_uint(0)
+    rc = load().sgr_device_error(dev, ctypes.byref(code), 1 if clear else 0)
+    if rc != SGR_OK:
+        raise SgrError(rc, "sgr_device_error")
+    return code.value
+
+
+def sgr_kernel_resources(M: int, N: int, K: int, path: int = SGR_PATH_AUTO,
+                         device: int | None = None) -> dict:
+    import torch
+
+    dev = torch.cuda.current_device() if device is None else device
+    vals = [ctypes.c_int(0) for _ in range(4)]
+    rc = load().sgr_kernel_resources(dev, path, M, N, K, *(ctypes.byref(v) for v in vals))
+    if rc != SGR_OK:
+        raise SgrError(rc, "sgr_kernel_resources")
+    return dict(zip(("registers_per_thread", "spill_bytes", "smem_bytes", "threads"),
+                    (v.value for v in vals)))
+
+
+# ---------------------------------------------------------------- launches
+def _stream_handle(stream) -> int:
+    import torch
+
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check_tensor(t, name: str):
+    import torch
+
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be torch.bfloat16, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dim() != 2:
+        raise ValueError(f"{name} must be 2-D")
+    if t.shape[0] > 1 and t.shape[1] > 0 and t.stride(1) != 1:
+        raise ValueError(f"{name} must have unit inner stride")
+
+
+def _ld(t) -> int:
+    return t.stride(0) if t.shape[0] > 1 else t.shape[1]
+
+
+def skinny_gemm_residual_ptr(A: int, W: int, R: int, Y: int, M: int, N: int, K: int, stream: int) -> int:
+    return load().skinny_gemm_residual(A, W, R, Y, M, N, K, stream)
+
+
+def skinny_gemm_residual_ex_ptr(A: int, lda: int, W: int, R: int, ldr: int, Y: int, ldy: int,
+                                M: int, N: int, K: int, flags: int, stream: int) -> int:
+    return load().skinny_gemm_residual_ex(A, lda, W, R, ldr, Y, ldy, M, N, K, flags, stream)
+
+
+def skinny_gemm_residual_config_ptr(A: int, lda: int, W: int, R: int, ldr: int, Y: int, ldy: int,
+                                    M: int, N: int, K: int, cfg: sgr_config | None, flags: int,
+                                    stream: int) -> int:
+    return load().skinny_gemm_residual_config(A, lda, W, R, ldr, Y, ldy, M, N, K,
+                                              ctypes.byref(cfg) if cfg is not None else None,
+                                              flags, stream)
+
+
+def skinny_gemm_residual(A, W, R, Y=None, stream=None):
+    """Y = bf16(A . W^T + R) for contiguous CUDA bf16 tensors; returns Y."""
+    import torch
+
+    for t, n in ((A, "A"), (W, "W"), (R, "R")):
+        _check_tensor(t, n)
+    if Y is None:
+        Y = torch.empty_like(R, memory_format=torch.contiguous_format)
+    _check_tensor(Y, "Y")
+    M, K = A.shape
+    N = W.shape[0]
+    if W.shape[1] != K or tuple(R.shape) != (M, N) or tuple(Y.shape) != (M, N):
+        raise ValueError(f"shape mismatch A{tuple(A.shape)} W{tuple(W.shape)} R{tuple(R.shape)} Y{tuple(Y.shape)}")
+    if not (A.is_contiguous() and W.is_contiguous() and R.is_contiguous() and Y.is_contiguous()):
+        raise ValueError("skinny_gemm_residual takes contiguous tensors; use skinny_gemm_residual_ex")
+    rc = load().skinny_gemm_residual(A.data_ptr(), W.data_ptr(), R.data_ptr(), Y.data_ptr(),
+                                     M, N, K, _stream_handle(stream))
+    if rc != SGR_OK:
+        raise SgrError(rc, "skinny_gemm_residual")
+    return Y
+
+
+def skinny_gemm_residual_ex(A, W, R, Y=None, flags: int = 0, stream=None, config: sgr_config | None = None):
+    """Row-strided form: A, R, Y may be row slices/column slices with unit inner stride."""
+    import torch
+
+    for t, n in ((A, "A"), (W, "W"), (R, "R")):
+        _check_tensor(t, n)
+    if Y is None:
+        Y = torch.empty(R.shape, dtype=R.dtype, device=R.device)
+    _check_tensor(Y, "Y")
+    M, K = A.shape
+    N = W.shape[0]
+    if W.shape[1] != K or tuple(R.shape) != (M, N) or tuple(Y.shape) != (M, N):
+        raise ValueError(f"shape mismatch A{tuple(A.shape)} W{tuple(W.shape)} R{tuple(R.shape)} Y{tuple(Y.shape)}")
+    if not W.is_contiguous():
+        raise ValueError("W must be contiguous [N, K]")
+    if config is None:
+        rc = load().skinny_gemm_residual_ex(A.data_ptr(), _ld(A), W.data_ptr(), R.data_ptr(), _ld(R),
+                                            Y.data_ptr(), _ld(Y), M, N, K, flags, _stream_handle(stream))
+        what = "skinny_gemm_residual_ex"
+    else:
+        rc = skinny_gemm_residual_config_ptr(A.data_ptr(), _ld(A), W.data_ptr(), R.data_ptr(), _ld(R),
+                                             Y.data_ptr(), _ld(Y), M, N, K, config, flags,
+                                             _stream_handle(stream))
+        what = "skinny_gemm_residual_config"
+    if rc != SGR_OK:
+        raise SgrError(rc, what)
+    return Y
+
+
+def skinny_gemm_residual_config(A, W, R, Y=None, config: sgr_config | None = None, flags: int = 0, stream=None):
+    """Explicit launch configuration (sweeps, tests)."""
+    return skinny_gemm_residual_ex(A, W, R, Y, flags=flags, stream=stream,
+                                   config=config if config is not None else sgr_config())
+
+
+def make_config(path: int = SGR_PATH_AUTO, ctas_per_sm: int = 0, rows_per_stage: int = 0,
+                stages: int = 0, split_units: int = 0) -> sgr_config:
+    c = sgr_config()
+    c.path, c.ctas_per_sm, c.rows_per_stage, c.stages, c.split_units = (
+        path, ctas_per_sm, rows_per_stage, stages, split_units)
+    return c

@@ -1,0 +1,398 @@
+// sgr_api.cu -- C ABI of the skinny BF16 GEMM + residual library: argument
+// validation, per-device set-up, path/config selection and kernel launch.
+// The operation and its argument rules are documented in
+// include/skinny_gemm_residual.h.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "skinny_gemm_residual.h"
+#include "sgr_simt.cuh"
+#include "sgr_tc.cuh"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxDynSmem = 232448;  // 227 KB, the per-CTA opt-in limit on sm_100-class GPUs
+constexpr long long kMaxN = 1 << 24;
+constexpr long long kMaxK = 1 << 20;
+constexpr long long kMaxM = 1 << 20;
+
+__device__ unsigned g_sgr_error_word;
+
+struct DeviceState {
+  std::once_flag once;
+  int status = SGR_ERR_DEVICE;
+  int sms = 0;
+  unsigned* err = nullptr;
+  sgr::TcWorkspace ws{};
+};
+DeviceState g_dev[kMaxDevices];
+
+// ------------------------------------------------------------ SIMT kernels
+using SimtFn = void (*)(const sgr::SimtParams);
+
+template <int MT>
+SimtFn simt_fn_vpt(int vpt) {
+  switch (vpt) {
+    case 1: return sgr::simt_skinny_kernel<MT, 1>;
+    case 2: return sgr::simt_skinny_kernel<MT, 2>;
+    case 4: return sgr::simt_skinny_kernel<MT, 4>;
+    default: return nullptr;
+  }
+}
+
+SimtFn simt_fn(int mt, int vpt) {
+  switch (mt) {
+    case 1: return simt_fn_vpt<1>(vpt);
+    case 2: return simt_fn_vpt<2>(vpt);
+    case 4: return simt_fn_vpt<4>(vpt);
+    case 8: return simt_fn_vpt<8>(vpt);
+    case 16: return simt_fn_vpt<16>(vpt);
+    default: return nullptr;
+  }
+}
+
+int simt_mt(int M) {
+  if (M <= 1) return 1;
+  if (M <= 2) return 2;
+  if (M <= 4) return 4;
+  if (M <= 8) return 8;
+  if (M <= 16) return 16;
+  return 0;
+}
+
+int simt_vpt(int K) {
+  const int kv = K / 8;
+  if (kv <= sgr::kSimtConsumers) return 1;
+  if (kv <= 2 * sgr::kSimtConsumers) return 2;
+  if (kv <= 4 * sgr::kSimtConsumers) return 4;
+  return 0;
+}
+
+// ------------------------------------------------------------ helpers
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Extent {
+  uintptr_t lo, hi;  // [lo, hi) bytes
+};
+
+Extent extent(const void* p, long long rows, long long ld, long long cols) {
+  const uintptr_t b = reinterpret_cast<uintptr_t>(p);
+  if (rows <= 0 || cols <= 0) return {b, b};
+  return {b, b + static_cast<uintptr_t>(((rows - 1) * ld + cols) * 2)};
+}
+
+bool overlap(Extent a, Extent b) { return a.lo < b.hi && b.lo < a.hi && a.lo < a.hi && b.lo < b.hi; }
+
+int validate(const void* A, long long lda, const void* W, const void* R, long long ldr,
+             const void* Y, long long ldy, int M, int N, int K) {
+  if (M < 0 || N < 0 || K < 0) return SGR_ERR_SHAPE;
+  if (M == 0 || N == 0) return SGR_OK;  // empty: nothing is read or written
+  if (M > kMaxM || N > kMaxN || K > kMaxK) return SGR_ERR_UNSUPPORTED;
+  if (N % 8 != 0 || K % 8 != 0) return SGR_ERR_SHAPE;
+  if (!R || !Y) return SGR_ERR_NULL;
+  if (K > 0 && (!A || !W)) return SGR_ERR_NULL;
+  if (ldr < N || ldy < N) return SGR_ERR_SHAPE;
+  if (K > 0 && lda < K) return SGR_ERR_SHAPE;
+  if (ldr % 8 != 0 || ldy % 8 != 0 || (K > 0 && lda % 8 != 0)) return SGR_ERR_ALIGN;
+  if (!aligned16(R) || !aligned16(Y)) return SGR_ERR_ALIGN;
+  if (K > 0 && (!aligned16(A) || !aligned16(W))) return SGR_ERR_ALIGN;
+  const Extent ey = extent(Y, M, ldy, N);
+  if (K > 0) {
+    if (overlap(ey, extent(A, M, lda, K))) return SGR_ERR_ALIAS;
+    if (overlap(ey, extent(W, N, K, K))) return SGR_ERR_ALIAS;
+  }
+  const bool in_place = (Y == R) && (ldy == ldr);
+  if (!in_place && overlap(ey, extent(R, M, ldr, N))) return SGR_ERR_ALIAS;
+  return SGR_OK;
+}
+
+int current_device(int* dev) {
+  if (cudaGetDevice(dev) != cudaSuccess) {
+    cudaGetLastError();
+    return SGR_ERR_DEVICE;
+  }
+  if (*dev < 0 || *dev >= kMaxDevices) return SGR_ERR_DEVICE;
+  return SGR_OK;
+}
+
+int init_device(int dev) {
+  if (dev < 0 || dev >= kMaxDevices) return SGR_ERR_DEVICE;
+  DeviceState& st = g_dev[dev];
+  std::call_once(st.once, [&] {
+    int prev = -1;
+    if (cudaGetDevice(&prev) != cudaSuccess) {
+      cudaGetLastError();
+      st.status = SGR_ERR_DEVICE;
+      return;
+    }
+    if (prev != dev && cudaSetDevice(dev) != cudaSuccess) {
+      cudaGetLastError();
+      st.status = SGR_ERR_DEVICE;
+      return;
+    }
+    int ok = SGR_OK;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+      ok = SGR_ERR_DEVICE;
+    void* errp = nullptr;
+    if (ok == SGR_OK && cudaGetSymbolAddress(&errp, g_sgr_error_word) != cudaSuccess) ok = SGR_ERR_DEVICE;
+    if (ok == SGR_OK && cudaMemset(errp, 0, sizeof(unsigned)) != cudaSuccess) ok = SGR_ERR_DEVICE;
+    const int mts[5] = {1, 2, 4, 8, 16};
+    const int vpts[3] = {1, 2, 4};
+    for (int mt : mts)
+      for (int v : vpts)
+        if (ok == SGR_OK &&
+            cudaFuncSetAttribute(simt_fn(mt, v), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kMaxDynSmem) != cudaSuccess)
+          ok = SGR_ERR_DEVICE;
+    if (ok == SGR_OK && sgr::tc_init_device(sms, &st.ws) != cudaSuccess) ok = SGR_ERR_DEVICE;
+    if (ok != SGR_OK) cudaGetLastError();
+    st.sms = sms;
+    st.err = static_cast<unsigned*>(errp);
+    st.status = ok;
+    if (prev != dev) cudaSetDevice(prev);
+  });
+  return st.status;
+}
+
+// Library choice for a shape.  The SIMT kernel serves small M on CUDA cores;
+// larger M needs the tensor-core kernel.
+int select_path(int M, int N, int K) {
+  (void)N;
+  if (M <= 16 && simt_vpt(K) > 0) return SGR_PATH_SIMT;
+  if (sgr::tc_supported(M, N, K)) return SGR_PATH_TC;
+  return -SGR_ERR_UNSUPPORTED;
+}
+
+void default_simt_config(int sms, int M, int K, sgr_config* c) {
+  (void)sms;
+  (void)M;
+  c->path = SGR_PATH_SIMT;
+  c->ctas_per_sm = 1;
+  const int row_bytes = K * 2;
+  c->rows_per_stage = row_bytes >= 16384 ? 1 : 16384 / row_bytes;
+  const size_t stage = (size_t)c->rows_per_stage * row_bytes;
+  const size_t budget = 200 * 1024 - sgr::simt_ring_offset(16);
+  int s = (int)(budget / stage);
+  c->stages = s > 16 ? 16 : (s < 2 ? 2 : s);
+  c->split_units = 0;
+}
+
+int resolve_config(int dev_sms, int M, int N, int K, const sgr_config* in, sgr_config* out) {
+  std::memset(out, 0, sizeof *out);
+  int path = in ? in->path : SGR_PATH_AUTO;
+  if (path == SGR_PATH_AUTO) {
+    path = select_path(M, N, K);
+    if (path < 0) return -path;
+  }
+  if (path == SGR_PATH_SIMT) {
+    if (M > 16 || simt_vpt(K) == 0) return SGR_ERR_UNSUPPORTED;
+    default_simt_config(dev_sms, M, K, out);
+  } else if (path == SGR_PATH_TC) {
+    if (!sgr::tc_supported(M, N, K)) return SGR_ERR_UNSUPPORTED;
+    sgr::tc_default_config(dev_sms, M, N, K, out);
+  } else {
+    return SGR_ERR_UNSUPPORTED;
+  }
+  if (in) {
+    for (int r : in->reserved)
+      if (r != 0) return SGR_ERR_UNSUPPORTED;
+    if (in->ctas_per_sm) out->ctas_per_sm = in->ctas_per_sm;
+    if (in->rows_per_stage) out->rows_per_stage = in->rows_per_stage;
+    if (in->stages) out->stages = in->stages;
+    if (in->split_units) out->split_units = in->split_units;
+  }
+  if (out->ctas_per_sm < 1 || out->ctas_per_sm > 8 || out->stages < 1 || out->stages > 64)
+    return SGR_ERR_UNSUPPORTED;
+  if (path == SGR_PATH_SIMT) {
+    if (out->rows_per_stage < 1 || out->rows_per_stage > 64) return SGR_ERR_UNSUPPORTED;
+    if (sgr::simt_smem_bytes(out->stages, out->rows_per_stage, K) > (size_t)kMaxDynSmem)
+      return SGR_ERR_UNSUPPORTED;
+    if ((size_t)out->rows_per_stage * K * 2 >= (1u << 31)) return SGR_ERR_UNSUPPORTED;
+  }
+  return SGR_OK;
+}
+
+int launch_simt(const sgr_config& c, int sms, unsigned* err, const void* A, long long lda,
+                const void* W, const void* R, long long ldr, void* Y, long long ldy, int M, int N,
+                int K, unsigned flags, cudaStream_t stream) {
+  SimtFn fn = simt_fn(simt_mt(M), simt_vpt(K));
+  if (!fn) return SGR_ERR_UNSUPPORTED;
+  sgr::SimtParams p;
+  p.A = static_cast<const __nv_bfloat16*>(A);
+  p.W = static_cast<const __nv_bfloat16*>(W);
+  p.R = static_cast<const __nv_bfloat16*>(R);
+  p.Y = static_cast<__nv_bfloat16*>(Y);
+  p.lda = lda;
+  p.ldr = ldr;
+  p.ldy = ldy;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.rows_per_stage = c.rows_per_stage;
+  p.stages = c.stages;
+  p.err = err;
+  long long grid = (long long)sms * c.ctas_per_sm;
+  if (grid > N) grid = N;
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3((unsigned)grid, 1, 1);
+  lc.blockDim = dim3(sgr::kSimtThreads, 1, 1);
+  lc.dynamicSmemBytes = sgr::simt_smem_bytes(c.stages, c.rows_per_stage, K);
+  lc.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = (flags & SGR_FLAG_NO_PDL) ? 0 : 1;
+  if (cudaLaunchKernelEx(&lc, fn, p) != cudaSuccess) {
+    cudaGetLastError();
+    return SGR_ERR_LAUNCH;
+  }
+  return SGR_OK;
+}
+
+int run(const void* A, long long lda, const void* W, const void* R, long long ldr, void* Y,
+        long long ldy, int M, int N, int K, const sgr_config* cfg, unsigned flags,
+        void* stream_ptr) {
+  int rc = validate(A, lda, W, R, ldr, Y, ldy, M, N, K);
+  if (rc != SGR_OK) return rc;
+  if (M == 0 || N == 0) return SGR_OK;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  if (K == 0) {  // empty sum: Y = R
+    if (Y == R) return SGR_OK;
+    if (cudaMemcpy2DAsync(Y, (size_t)ldy * 2, R, (size_t)ldr * 2, (size_t)N * 2, (size_t)M,
+                          cudaMemcpyDeviceToDevice, stream) != cudaSuccess) {
+      cudaGetLastError();
+      return SGR_ERR_LAUNCH;
+    }
+    return SGR_OK;
+  }
+  int dev;
+  if ((rc = current_device(&dev)) != SGR_OK) return rc;
+  if ((rc = init_device(dev)) != SGR_OK) return rc;
+  DeviceState& st = g_dev[dev];
+  sgr_config c;
+  if ((rc = resolve_config(st.sms, M, N, K, cfg, &c)) != SGR_OK) return rc;
+  if (c.path == SGR_PATH_SIMT)
+    return launch_simt(c, st.sms, st.err, A, lda, W, R, ldr, Y, ldy, M, N, K, flags, stream);
+  return sgr::tc_launch(c, st.sms, st.err, &st.ws, A, lda, W, R, ldr, Y, ldy, M, N, K,
+                        (flags & SGR_FLAG_NO_PDL) == 0, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+int skinny_gemm_residual(const void* A, const void* W, const void* R, void* Y, int M, int N,
+                         int K, void* stream) {
+  return run(A, K, W, R, N, Y, N, M, N, K, nullptr, 0u, stream);
+}
+
+int skinny_gemm_residual_ex(const void* A, int64_t lda, const void* W, const void* R,
+                            int64_t ldr, void* Y, int64_t ldy, int M, int N, int K,
+                            unsigned flags, void* stream) {
+  return run(A, lda, W, R, ldr, Y, ldy, M, N, K, nullptr, flags, stream);
+}
+
+int skinny_gemm_residual_config(const void* A, int64_t lda, const void* W, const void* R,
+                                int64_t ldr, void* Y, int64_t ldy, int M, int N, int K,
+                                const sgr_config* cfg, unsigned flags, void* stream) {
+  return run(A, lda, W, R, ldr, Y, ldy, M, N, K, cfg, flags, stream);
+}
+
+int sgr_validate(const void* A, int64_t lda, const void* W, const void* R, int64_t ldr,
+                 const void* Y, int64_t ldy, int M, int N, int K) {
+  return validate(A, lda, W, R, ldr, Y, ldy, M, N, K);
+}
+
+int sgr_select_path(int M, int N, int K) {
+  if (M < 1 || N < 1 || K < 8 || N % 8 || K % 8) return -SGR_ERR_SHAPE;
+  return select_path(M, N, K);
+}
+
+int sgr_default_config(int device, int M, int N, int K, int path, sgr_config* cfg) {
+  if (!cfg) return SGR_ERR_NULL;
+  if (M < 1 || N < 8 || K < 8 || N % 8 || K % 8) return SGR_ERR_SHAPE;
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) {
+    cudaGetLastError();
+    return SGR_ERR_DEVICE;
+  }
+  sgr_config in = {};
+  in.path = path;
+  return resolve_config(sms, M, N, K, &in, cfg);
+}
+
+int sgr_init(int device) { return init_device(device); }
+
+int sgr_device_error(int device, unsigned* code, int clear) {
+  if (!code) return SGR_ERR_NULL;
+  int rc = init_device(device);
+  if (rc != SGR_OK) return rc;
+  int prev = -1;
+  if (cudaGetDevice(&prev) != cudaSuccess) return SGR_ERR_DEVICE;
+  if (prev != device && cudaSetDevice(device) != cudaSuccess) return SGR_ERR_DEVICE;
+  unsigned v = 0;
+  cudaError_t e = cudaMemcpy(&v, g_dev[device].err, sizeof v, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && clear) e = cudaMemset(g_dev[device].err, 0, sizeof v);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (prev != device) cudaSetDevice(prev);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return SGR_ERR_DEVICE;
+  }
+  *code = v;
+  return SGR_OK;
+}
+
+int sgr_kernel_resources(int device, int path, int M, int N, int K, int* regs, int* local_bytes,
+                         int* smem_bytes, int* threads) {
+  if (!regs || !local_bytes || !smem_bytes || !threads) return SGR_ERR_NULL;
+  sgr_config c;
+  int rc = sgr_default_config(device, M, N, K, path, &c);
+  if (rc != SGR_OK) return rc;
+  cudaFuncAttributes fa;
+  if (c.path == SGR_PATH_SIMT) {
+    if (cudaFuncGetAttributes(&fa, simt_fn(simt_mt(M), simt_vpt(K))) != cudaSuccess) {
+      cudaGetLastError();
+      return SGR_ERR_DEVICE;
+    }
+    *smem_bytes = (int)sgr::simt_smem_bytes(c.stages, c.rows_per_stage, K);
+    *threads = sgr::kSimtThreads;
+  } else {
+    int s = 0, t = 0;
+    const void* fn = sgr::tc_kernel_for(M, N, K, &c, &s, &t);
+    if (!fn || cudaFuncGetAttributes(&fa, fn) != cudaSuccess) {
+      cudaGetLastError();
+      return SGR_ERR_DEVICE;
+    }
+    *smem_bytes = s;
+    *threads = t;
+  }
+  *regs = fa.numRegs;
+  *local_bytes = (int)fa.localSizeBytes;
+  return SGR_OK;
+}
+
+const char* sgr_status_string(int status) {
+  switch (status) {
+    case SGR_OK: return "ok";
+    case SGR_ERR_NULL: return "a required pointer is NULL";
+    case SGR_ERR_SHAPE: return "bad shape: negative size, N or K not a multiple of 8, or row stride below row width";
+    case SGR_ERR_ALIGN: return "misaligned: pointers must be 16-byte aligned and row strides multiples of 8 elements";
+    case SGR_ERR_ALIAS: return "Y overlaps A, W, or R (other than Y == R exactly)";
+    case SGR_ERR_UNSUPPORTED: return "unsupported size or configuration";
+    case SGR_ERR_LAUNCH: return "CUDA launch failed";
+    case SGR_ERR_DEVICE: return "no usable CUDA device or device set-up failed";
+    default: return "unknown status";
+  }
+}
+
+int sgr_abi_version(void) { return SGR_ABI_VERSION; }
+
+}  // extern "C"

@@ -1,0 +1,258 @@
+// sgr_simt.cuh -- bandwidth-bound SIMT path for small M (decode-sized batches).
+//
+// Computes Y[m,n] = bf16_rn( sum_k A[m,k] * W[n,k] + R[m,n] ) for m < M <= MT,
+// accumulating in FP32 and rounding once in the epilogue.  The operation is
+// the one benchmarked on the vLLM "benchmark_k3_cutedsl_residual.py" page
+// (BF16[M,3584] @ BF16[7168,3584].T + BF16[M,7168], FP32 accumulation, BF16
+// out); the SIMT structure follows the main loop of the vLLM
+// "fused_add_multicast_skinny_gemm" kernel (vectorised 16-byte W loads,
+// FP32 register accumulators, warp-shuffle then shared-memory K reduction,
+// residual fused into the epilogue), re-planned for GB300:
+//
+//  * Persistent grid: CTA c owns the contiguous W rows [N*c/G, N*(c+1)/G),
+//    i.e. one contiguous slab of HBM, so the grid is sized to the SM count
+//    instead of N/outputs_per_block CTAs.
+//  * W is streamed exactly once by one producer thread issuing 1-D bulk
+//    copies (cp.async.bulk, L2 evict-first) of `rows_per_stage` whole rows
+//    into a `stages`-deep shared-memory ring guarded by mbarriers.  The first
+//    stages are requested before griddepcontrol.wait, so with programmatic
+//    dependent launch the weight stream overlaps the previous kernel's tail.
+//  * 7 consumer warps (224 threads) own a fixed K slice each: thread t owns
+//    the 16-byte vectors t, t+224, ... of every row, so its slice of A is
+//    loaded once (after griddepcontrol.wait) and stays in registers.
+//  * Rows are reduced in batches of 32/MT rows so that each lane holds 32
+//    partial sums; one transposing butterfly (31 shuffles) leaves lane l
+//    with the warp's total for output l, the 7 warps' totals meet in shared
+//    memory, and warp 0 adds R, rounds once and stores.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "sgr_ptx.cuh"
+
+namespace sgr {
+
+constexpr int kSimtConsumerWarps = 7;
+constexpr int kSimtConsumers = kSimtConsumerWarps * 32;  // 224 threads
+constexpr int kSimtThreads = kSimtConsumers + 32;        // + one producer warp
+
+struct SimtParams {
+  const __nv_bfloat16* A;  // [M, K], row stride lda (elements)
+  const __nv_bfloat16* W;  // [N, K], contiguous rows
+  const __nv_bfloat16* R;  // [M, N], row stride ldr
+  __nv_bfloat16* Y;        // [M, N], row stride ldy
+  long long lda, ldr, ldy;
+  int M, N, K;
+  int rows_per_stage;  // W rows per ring stage
+  int stages;          // ring depth
+  unsigned* err;       // device error word
+};
+
+// Shared-memory layout (dynamic): [full bars][empty bars][partials 2x7x32 f32][pad][ring]
+__host__ __device__ constexpr size_t simt_ring_offset(int stages) {
+  return ((size_t)stages * 16 + 2 * kSimtConsumerWarps * 32 * 4 + 127) / 128 * 128;
+}
+
+__host__ __device__ constexpr size_t simt_smem_bytes(int stages, int rows_per_stage, int K) {
+  return simt_ring_offset(stages) + (size_t)stages * rows_per_stage * K * 2;
+}
+
+// Butterfly over 32 lanes that also transposes: on entry each lane holds 32
+// partial sums x[0..31]; on exit lane l returns the sum over all lanes of x[l].
+template <int CNT>
+__device__ __forceinline__ void transpose_reduce_step(float (&x)[32], int lane) {
+  const bool upper = (lane & CNT) != 0;
+#pragma unroll
+  for (int i = 0; i < CNT; ++i) {
+    const float send = upper ? x[i] : x[i + CNT];
+    const float keep = upper ? x[i + CNT] : x[i];
+    x[i] = keep + __shfl_xor_sync(0xffffffffu, send, CNT);
+  }
+}
+
+__device__ __forceinline__ float transpose_reduce32(float (&x)[32], int lane) {
+  transpose_reduce_step<16>(x, lane);
+  transpose_reduce_step<8>(x, lane);
+  transpose_reduce_step<4>(x, lane);
+  transpose_reduce_step<2>(x, lane);
+  transpose_reduce_step<1>(x, lane);
+  return x[0];
+}
+
+// MT: rows of A handled (M <= MT, rows >= M masked); VPT: 16-byte K vectors
+// per consumer thread (K <= 224 * 8 * VPT).
+template <int MT, int VPT>
+__global__ void __launch_bounds__(kSimtThreads, (MT <= 4 ? 2 : 1))
+    simt_skinny_kernel(const SimtParams p) {
+  constexpr int B = 32 / MT;                    // rows per reduction batch
+  constexpr bool kPackedA = MT * VPT * 8 > 64;  // keep A as bf16x2 when large
+  extern __shared__ __align__(128) unsigned char smem[];
+
+  const int S = p.stages;
+  const int RS = p.rows_per_stage;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* empty = full + S;
+  float* partial = reinterpret_cast<float*>(empty + S);  // [2][7][32]
+  const __nv_bfloat16* ring =
+      reinterpret_cast<const __nv_bfloat16*>(smem + simt_ring_offset(S));
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = gridDim.x, c = blockIdx.x;
+  const int n0 = (int)((long long)p.N * c / G);
+  const int n1 = (int)((long long)p.N * (c + 1) / G);
+  const int nrows = n1 - n0;
+  const int nstages = (nrows + RS - 1) / RS;
+  const int KV = p.K >> 3;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), kSimtConsumerWarps);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kSimtConsumerWarps) {
+    // ---------------- producer: stream this CTA's W slab through the ring
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      const uint32_t row_bytes = (uint32_t)p.K * 2u;
+      const char* wbase = reinterpret_cast<const char*>(p.W) + (size_t)n0 * row_bytes;
+      int issued = 0;
+      for (int s = 0; s < nstages; ++s) {
+        const int slot = s % S;
+        if (s >= S && !mbar_wait(smem_u32(&empty[slot]), ((s / S) - 1) & 1)) {
+          report_error(p.err, kErrWaitEmpty);
+          break;
+        }
+        const int rows = min(RS, nrows - s * RS);
+        const uint32_t bytes = (uint32_t)rows * row_bytes;
+        const uint32_t fb = smem_u32(&full[slot]);
+        mbar_arrive_expect_tx(fb, bytes);
+        bulk_g2s(smem_u32(ring + (size_t)slot * RS * p.K), wbase + (size_t)s * RS * row_bytes,
+                 bytes, fb, pol);
+        issued = s + 1;
+      }
+      pdl_launch_dependents();
+      // Before this CTA can exit, every copy it issued must have landed.
+      for (int t = max(0, issued - S); t < issued; ++t) {
+        if (!mbar_wait(smem_u32(&full[t % S]), (t / S) & 1)) {
+          report_error(p.err, kErrDrain);
+          break;
+        }
+      }
+    }
+    return;
+  }
+
+  // ---------------- consumers
+  pdl_wait();  // A and R may be produced by the preceding kernel; Y may be read by it
+
+  // This thread's K slice of A, loaded once.
+  float af[kPackedA ? 1 : MT][kPackedA ? 1 : VPT][8];
+  uint32_t ap[kPackedA ? MT : 1][kPackedA ? VPT : 1][4];
+#pragma unroll
+  for (int m = 0; m < MT; ++m) {
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      const int vid = threadIdx.x + v * kSimtConsumers;
+      uint4 q = make_uint4(0u, 0u, 0u, 0u);
+      if (m < p.M && vid < KV)
+        q = *reinterpret_cast<const uint4*>(p.A + (size_t)m * p.lda + (size_t)vid * 8);
+      if constexpr (kPackedA) {
+        ap[m][v][0] = q.x; ap[m][v][1] = q.y; ap[m][v][2] = q.z; ap[m][v][3] = q.w;
+      } else {
+        af[m][v][0] = bf16lo(q.x); af[m][v][1] = bf16hi(q.x);
+        af[m][v][2] = bf16lo(q.y); af[m][v][3] = bf16hi(q.y);
+        af[m][v][4] = bf16lo(q.z); af[m][v][5] = bf16hi(q.z);
+        af[m][v][6] = bf16lo(q.w); af[m][v][7] = bf16hi(q.w);
+      }
+    }
+  }
+
+  bool ok = true;
+  int buf = 0;
+  int slot = 0, rr = 0;   // ring slot of the current stage, row within the stage
+  uint32_t phase = 0;     // parity of the current stage's fill of that slot
+  const uint32_t ring_base = smem_u32(ring);
+  const uint32_t row_bytes = (uint32_t)p.K * 2u;
+  uint32_t row_addr = ring_base;
+  for (int base = 0; base < nrows; base += B) {
+    float acc[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+
+#pragma unroll
+    for (int j = 0; j < B; ++j) {
+      if (base + j < nrows) {
+        if (rr == 0 && ok && !mbar_wait(smem_u32(&full[slot]), phase)) {
+          report_error(p.err, kErrWaitFull);
+          ok = false;
+        }
+        if (ok) {
+#pragma unroll
+          for (int v = 0; v < VPT; ++v) {
+            const int vid = threadIdx.x + v * kSimtConsumers;
+            if (vid < KV) {
+              const uint4 q = lds128(row_addr + (uint32_t)vid * 16u);
+              float w[8];
+              w[0] = bf16lo(q.x); w[1] = bf16hi(q.x); w[2] = bf16lo(q.y); w[3] = bf16hi(q.y);
+              w[4] = bf16lo(q.z); w[5] = bf16hi(q.z); w[6] = bf16lo(q.w); w[7] = bf16hi(q.w);
+#pragma unroll
+              for (int m = 0; m < MT; ++m) {
+                float t = acc[j * MT + m];
+                if constexpr (kPackedA) {
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) {
+                    t = fmaf(bf16lo(ap[m][v][e]), w[2 * e], t);
+                    t = fmaf(bf16hi(ap[m][v][e]), w[2 * e + 1], t);
+                  }
+                } else {
+#pragma unroll
+                  for (int e = 0; e < 8; ++e) t = fmaf(af[m][v][e], w[e], t);
+                }
+                acc[j * MT + m] = t;
+              }
+            }
+          }
+        }
+        // Release the stage after its last row.
+        if (rr == RS - 1 || base + j == nrows - 1) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&empty[slot]));
+        }
+        row_addr += row_bytes;
+        if (++rr == RS) {
+          rr = 0;
+          if (++slot == S) {
+            slot = 0;
+            phase ^= 1u;
+            row_addr = ring_base;
+          }
+        }
+      }
+    }
+
+    // K reduction: within the warp, then across the 7 consumer warps.
+    const float mine = transpose_reduce32(acc, lane);
+    partial[(buf * kSimtConsumerWarps + warp) * 32 + lane] = mine;
+    named_bar_sync(1, kSimtConsumers);
+    if (warp == 0) {
+      float total = 0.f;
+#pragma unroll
+      for (int w = 0; w < kSimtConsumerWarps; ++w)
+        total += partial[(buf * kSimtConsumerWarps + w) * 32 + lane];
+      const int j = lane / MT, m = lane % MT;
+      if (base + j < nrows && m < p.M) {
+        const int n = n0 + base + j;
+        const float r = __bfloat162float(p.R[(size_t)m * p.ldr + n]);
+        p.Y[(size_t)m * p.ldy + n] = __float2bfloat16_rn(total + r);
+      }
+    }
+    buf ^= 1;
+  }
+  pdl_launch_dependents();
+}
+
+}  // namespace sgr

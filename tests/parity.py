@@ -1,0 +1,53 @@
+"""Shared helpers for the GPU parity tests: run the CUDA path, run the CPU
+oracle on the same seeded inputs, compare element by element.
+
+Tolerance (per element): |y - y_ref| <= 1e-2 * |y_ref| + 2e-2, where y_ref
+is the oracle's correctly rounded BF16 result.  Derivation: the kernel
+accumulates in FP32 (error about sqrt(K) * 2^-24 * sum|a*w|, ~1e-5 here) and
+rounds once to BF16 (half an ulp, 2^-9 relative); the oracle's own rounding
+adds another half ulp; 1e-2 relative covers both BF16 roundings with a 2.5x
+margin and 2e-2 absolute covers outputs near zero, where relative error is
+meaningless.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+
+RTOL = 1e-2
+ATOL = 2e-2
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def f64(b: np.ndarray) -> np.ndarray:
+    return (np.ascontiguousarray(b).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def compare(got_bits: np.ndarray, ref_bits: np.ndarray, what: str = "") -> dict:
+    """Elementwise gate plus the informative metrics of the vLLM benchmark
+    page's correctness() check (cosine, max abs error, max scaled error)."""
+    assert got_bits.shape == ref_bits.shape, (got_bits.shape, ref_bits.shape)
+    g, r = f64(got_bits), f64(ref_bits)
+    assert np.all(np.isfinite(g)), f"{what}: non-finite output"
+    err = np.abs(g - r)
+    bad = err > RTOL * np.abs(r) + ATOL
+    if bad.any():
+        i = tuple(np.argwhere(bad)[0])
+        raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} elements out of tolerance; "
+                             f"first at {i}: got {g[i]!r} want {r[i]!r}")
+    denom = np.linalg.norm(g) * np.linalg.norm(r)
+    return {
+        "max_abs_error": float(err.max()) if err.size else 0.0,
+        "max_scaled_error": float((err / (np.abs(r) + 1.0)).max()) if err.size else 0.0,
+        "cosine": float((g * r).sum() / denom) if denom > 0 else 1.0,
+        "exact_fraction": float((got_bits == ref_bits).mean()) if err.size else 1.0,
+    }
+
+
+def oracle_full(A, W, R) -> np.ndarray:
+    return oracle.load().gemm_residual(A, W, R)

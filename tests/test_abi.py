@@ -1,0 +1,103 @@
+"""The C-ABI library builds, loads and exports every symbol the public header
+declares; host-only argument checks (no GPU needed, nothing is launched)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import skinny_bf16_gemm_residual_gb300 as sgr
+from skinny_bf16_gemm_residual_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(\w+)\s*\(", text, flags=re.M):
+            if m.group(1) not in ("defined",):
+                names.add(m.group(1))
+    return sorted(names)
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    assert "skinny_gemm_residual" in names
+    assert set(binding.EXPORTS) <= set(names), set(binding.EXPORTS) - set(names)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = sgr.load()
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+        ctypes.cast(getattr(lib, name), ctypes.c_void_p)
+
+
+def test_abi_version_and_status_strings():
+    assert sgr.sgr_abi_version() == sgr.ABI_VERSION
+    for s in range(0, 8):
+        assert sgr.sgr_status_string(s)
+    assert sgr.sgr_status_string(99) == "unknown status"
+
+
+# Fake, never-dereferenced addresses for the host-only validator.
+BASE = 1 << 40
+A_, W_, R_, Y_ = BASE, BASE + (1 << 32), BASE + (2 << 32), BASE + (3 << 32)
+
+
+def v(A=A_, lda=3584, W=W_, R=R_, ldr=7168, Y=Y_, ldy=7168, M=4, N=7168, K=3584):
+    return sgr.sgr_validate_ptr(A, lda, W, R, ldr, Y, ldy, M, N, K)
+
+
+def test_validate_accepts_good_arguments():
+    assert v() == sgr.SGR_OK
+    assert v(M=1) == sgr.SGR_OK
+    assert v(M=1024) == sgr.SGR_OK
+    assert v(lda=7168, ldr=7168 * 2, ldy=7168 * 3) == sgr.SGR_OK
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(M=-1), sgr.SGR_ERR_SHAPE),
+    (dict(N=-8), sgr.SGR_ERR_SHAPE),
+    (dict(K=-8), sgr.SGR_ERR_SHAPE),
+    (dict(N=7170, ldr=7176, ldy=7176), sgr.SGR_ERR_SHAPE),
+    (dict(K=3585, lda=3592), sgr.SGR_ERR_SHAPE),
+    (dict(A=0), sgr.SGR_ERR_NULL),
+    (dict(W=0), sgr.SGR_ERR_NULL),
+    (dict(R=0), sgr.SGR_ERR_NULL),
+    (dict(Y=0), sgr.SGR_ERR_NULL),
+    (dict(lda=3576), sgr.SGR_ERR_SHAPE),
+    (dict(ldr=7160), sgr.SGR_ERR_SHAPE),
+    (dict(ldy=7000), sgr.SGR_ERR_SHAPE),
+    (dict(lda=3588), sgr.SGR_ERR_ALIGN),
+    (dict(ldy=7172), sgr.SGR_ERR_ALIGN),
+    (dict(A=A_ + 2), sgr.SGR_ERR_ALIGN),
+    (dict(W=W_ + 8), sgr.SGR_ERR_ALIGN),
+    (dict(R=R_ + 4), sgr.SGR_ERR_ALIGN),
+    (dict(Y=Y_ + 2), sgr.SGR_ERR_ALIGN),
+    (dict(Y=A_), sgr.SGR_ERR_ALIAS),
+    (dict(Y=W_ + 4096), sgr.SGR_ERR_ALIAS),
+    (dict(Y=R_ + 16), sgr.SGR_ERR_ALIAS),
+    (dict(Y=R_, ldy=7176), sgr.SGR_ERR_ALIAS),
+    (dict(M=(1 << 20) + 1), sgr.SGR_ERR_UNSUPPORTED),
+])
+def test_validate_rejects(kw, status):
+    assert v(**kw) == status
+
+
+def test_validate_in_place_and_empty():
+    assert v(Y=R_) == sgr.SGR_OK                       # Y == R exactly: in-place residual
+    assert v(M=0, A=0, W=0, R=0, Y=0) == sgr.SGR_OK    # empty problem
+    assert v(N=0, A=0, W=0, R=0, Y=0) == sgr.SGR_OK
+    assert v(K=0, A=0, W=0) == sgr.SGR_OK              # empty sum: Y = R
+
+
+def test_select_path():
+    for M in (1, 2, 3, 4, 8, 16):
+        assert sgr.sgr_select_path(M, 7168, 3584) in (sgr.SGR_PATH_SIMT, sgr.SGR_PATH_TC)
+    assert sgr.sgr_select_path(0, 7168, 3584) < 0
+    assert sgr.sgr_select_path(4, 7170, 3584) < 0
