@@ -239,15 +239,16 @@ def time_graph(g, stream, replays: int, repeats: int):
     import torch
 
     out = []
-    for _ in range(repeats):
-        s = torch.cuda.Event(enable_timing=True)
-        e = torch.cuda.Event(enable_timing=True)
-        s.record(stream)
-        for _ in range(replays):
-            g.replay()
-        e.record(stream)
-        e.synchronize()
-        out.append(s.elapsed_time(e) * 1000.0 / replays)  # us per replay
+    with torch.cuda.stream(stream):  # replay() launches on the current stream
+        for _ in range(repeats):
+            s = torch.cuda.Event(enable_timing=True)
+            e = torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            for _ in range(replays):
+                g.replay()
+            e.record(stream)
+            e.synchronize()
+            out.append(s.elapsed_time(e) * 1000.0 / replays)  # us per replay
     return out
 
 
@@ -365,10 +366,11 @@ def run_ours(args):
     # per-M microseconds per call: one graph of the 4 copies, repeats x replays
     per_m_out = {}
     peaks, peak_src = load_peaks()
-    for M in m_list:
+    for M in (() if args.skip_per_m else m_list):
         g = capture([call(M, c) for c in range(COPIES)], stream)
-        for _ in range(20):
-            g.replay()
+        with torch.cuda.stream(stream):
+            for _ in range(20):
+                g.replay()
         stream.synchronize()
         samples = [t / COPIES for t in time_graph(g, stream, args.replays, args.repeats)]
         s = summarize(samples)
@@ -383,17 +385,19 @@ def run_ours(args):
     # headline: K timed steps of the whole M sweep
     clocks = ClockSampler(device.index)
     clocks.start()
-    for _ in range(args.warmup):
-        g_step.replay()
+    with torch.cuda.stream(stream):  # replay() launches on the current stream
+        for _ in range(args.warmup):
+            g_step.replay()
     stream.synchronize()
     dist_barrier(ws)
     torch.cuda.synchronize()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for _ in range(args.steps):
-        g_step.replay()
-    ev1.record(stream)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(args.steps):
+            g_step.replay()
+        ev1.record(stream)
     ev1.synchronize()
     torch.cuda.synchronize()
     dist_barrier(ws)
@@ -404,16 +408,20 @@ def run_ours(args):
     value = bytes_per_step * ws * args.steps / (elapsed_ms * 1e-3) / 1e9
 
     # end to end through the public call with host buffers (pinned), W resident
-    e2e = run_e2e(sgr, per_m, Ws, m_list, device, stream, max(3, min(args.steps, args.e2e_steps)))
-    e2e_seconds = dist_max(e2e["seconds"], ws, device)  # slowest rank
-    e2e_value = bytes_per_step * ws * e2e["steps"] / e2e_seconds / 1e9
+    e2e_out = None
+    if not args.skip_e2e:
+        e2e = run_e2e(sgr, per_m, Ws, m_list, device, stream, max(3, min(args.steps, args.e2e_steps)))
+        e2e_seconds = dist_max(e2e["seconds"], ws, device)  # slowest rank
+        e2e_out = {"value": bytes_per_step * ws * e2e["steps"] / e2e_seconds / 1e9, "unit": "GB/s",
+                   "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+                   "steps": e2e["steps"]}
 
     if rank != 0:
         return 0
 
     avg_launch_s = elapsed_ms * 1e-3 / (args.steps * launches_per_step)
     achieved = bytes_per_step / launches_per_step / avg_launch_s / 1e9
-    kernels = sorted({v["path"] for v in per_m_out.values()})
+    kernels = sorted({{1: "simt", 2: "tc"}.get(sgr.sgr_select_path(M, N_DIM, K_DIM), "?") for M in m_list})
     dominant = "simt_skinny_kernel" if kernels == ["simt"] else "tc_skinny_kernel" if kernels == ["tc"] else "mixed"
     traffic = committed_traffic(dominant)
     roofline = {
@@ -442,8 +450,7 @@ def run_ours(args):
         "per_m": per_m_out,
         "roofline": roofline,
         "cpu_baseline": cpu,
-        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": e2e["h2d"],
-                "d2h_bytes_per_step": e2e["d2h"], "steps": e2e["steps"]},
+        "e2e": e2e_out,
         "gpu_launches": args.steps * launches_per_step,
         "clocks": clk,
         "peaks": {"hbm_gbs": peaks["hbm_gbs"], "source": peak_src},
@@ -505,6 +512,8 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--ref-budget", type=float, default=90.0, help="seconds for the reference arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--skip-per-m", action="store_true", help="skip the per-M repeat/replay timing")
+    ap.add_argument("--skip-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -175,7 +175,7 @@ void default_simt_config(int sms, int M, int K, sgr_config* c) {
   c->path = SGR_PATH_SIMT;
   c->ctas_per_sm = 1;
   const int row_bytes = K * 2;
-  c->rows_per_stage = row_bytes >= 16384 ? 1 : 16384 / row_bytes;
+  c->rows_per_stage = row_bytes >= 16384 ? 1 : (16384 / row_bytes > 64 ? 64 : 16384 / row_bytes);
   const size_t stage = (size_t)c->rows_per_stage * row_bytes;
   const size_t budget = 200 * 1024 - sgr::simt_ring_offset(16);
   int s = (int)(budget / stage);
