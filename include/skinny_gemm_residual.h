@@ -117,12 +117,13 @@ int skinny_gemm_residual_ex(const void* A, int64_t lda, const void* W,
  * "the library's choice for this M".
  */
 typedef struct {
-  int path;           /* SGR_PATH_* */
-  int ctas_per_sm;    /* persistent grid = SM count x ctas_per_sm (SIMT, TC) */
-  int rows_per_stage; /* SIMT: W rows per shared-memory ring stage */
-  int stages;         /* ring depth (SIMT, TC) */
-  int split_units;    /* TC: K blocks (of 64) per work unit; 0 = balanced stream-K */
-  int reserved[3];    /* must be zero */
+  int path;               /* SGR_PATH_* */
+  int ctas_per_sm;        /* persistent grid = SM count x ctas_per_sm */
+  int stages;             /* shared-memory ring depth */
+  int rows_per_stage;     /* SIMT: W rows per ring stage */
+  int k_blocks_per_stage; /* TC: 64-wide K blocks per ring stage */
+  int token_tile;         /* TC: activation rows per MMA (multiple of 16, <= 256) */
+  int reserved[2];        /* must be zero */
 } sgr_config;
 
 /*

@@ -40,13 +40,14 @@ class SgrError(RuntimeError):
 
 class sgr_config(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int), ("ctas_per_sm", ctypes.c_int),
-                ("rows_per_stage", ctypes.c_int), ("stages", ctypes.c_int),
-                ("split_units", ctypes.c_int), ("reserved", ctypes.c_int * 3)]
+                ("stages", ctypes.c_int), ("rows_per_stage", ctypes.c_int),
+                ("k_blocks_per_stage", ctypes.c_int), ("token_tile", ctypes.c_int),
+                ("reserved", ctypes.c_int * 2)]
 
     def as_dict(self) -> dict:
-        return {"path": self.path, "ctas_per_sm": self.ctas_per_sm,
-                "rows_per_stage": self.rows_per_stage, "stages": self.stages,
-                "split_units": self.split_units}
+        return {"path": self.path, "ctas_per_sm": self.ctas_per_sm, "stages": self.stages,
+                "rows_per_stage": self.rows_per_stage,
+                "k_blocks_per_stage": self.k_blocks_per_stage, "token_tile": self.token_tile}
 
 
 _lock = threading.Lock()
@@ -274,9 +275,9 @@ def skinny_gemm_residual_config(A, W, R, Y=None, config: sgr_config | None = Non
                                    config=config if config is not None else sgr_config())
 
 
-def make_config(path: int = SGR_PATH_AUTO, ctas_per_sm: int = 0, rows_per_stage: int = 0,
-                stages: int = 0, split_units: int = 0) -> sgr_config:
+def make_config(path: int = SGR_PATH_AUTO, ctas_per_sm: int = 0, stages: int = 0,
+                rows_per_stage: int = 0, k_blocks_per_stage: int = 0, token_tile: int = 0) -> sgr_config:
     c = sgr_config()
-    c.path, c.ctas_per_sm, c.rows_per_stage, c.stages, c.split_units = (
-        path, ctas_per_sm, rows_per_stage, stages, split_units)
+    c.path, c.ctas_per_sm, c.stages = path, ctas_per_sm, stages
+    c.rows_per_stage, c.k_blocks_per_stage, c.token_tile = rows_per_stage, k_blocks_per_stage, token_tile
     return c

@@ -180,7 +180,8 @@ void default_simt_config(int sms, int M, int K, sgr_config* c) {
   const size_t budget = 200 * 1024 - sgr::simt_ring_offset(16);
   int s = (int)(budget / stage);
   c->stages = s > 16 ? 16 : (s < 2 ? 2 : s);
-  c->split_units = 0;
+  c->k_blocks_per_stage = 0;
+  c->token_tile = 0;
 }
 
 int resolve_config(int dev_sms, int M, int N, int K, const sgr_config* in, sgr_config* out) {
@@ -205,10 +206,18 @@ int resolve_config(int dev_sms, int M, int N, int K, const sgr_config* in, sgr_c
     if (in->ctas_per_sm) out->ctas_per_sm = in->ctas_per_sm;
     if (in->rows_per_stage) out->rows_per_stage = in->rows_per_stage;
     if (in->stages) out->stages = in->stages;
-    if (in->split_units) out->split_units = in->split_units;
+    if (in->k_blocks_per_stage) out->k_blocks_per_stage = in->k_blocks_per_stage;
+    if (in->token_tile) out->token_tile = in->token_tile;
   }
   if (out->ctas_per_sm < 1 || out->ctas_per_sm > 8 || out->stages < 1 || out->stages > 64)
     return SGR_ERR_UNSUPPORTED;
+  if (path == SGR_PATH_TC) {
+    sgr::TcParams tp;
+    int grid = 0;
+    size_t smem = 0;
+    int rc = sgr::tc_plan(*out, dev_sms > 0 ? dev_sms : 1, M, N, K, &tp, &grid, &smem);
+    if (rc != SGR_OK) return rc;
+  }
   if (path == SGR_PATH_SIMT) {
     if (out->rows_per_stage < 1 || out->rows_per_stage > 64) return SGR_ERR_UNSUPPORTED;
     if (sgr::simt_smem_bytes(out->stages, out->rows_per_stage, K) > (size_t)kMaxDynSmem)

@@ -1,0 +1,165 @@
+"""Configuration sweep for the skinny GEMM + residual kernels (GPU).
+
+The analogue of the sweep mode of the vLLM "benchmark_k3_cutedsl_residual.py"
+page: for each M, every candidate launch configuration of each kernel path is
+timed by batched CUDA-graph replay over rotating weight/residual copies that
+together exceed L2, and one JSON row per (M, path, config) is written.  A
+`torch.addmm` (cuBLAS) row under the same protocol is included as context.
+The per-M table compiled into the library is generated from these rows by
+``gen_table.py``.
+
+    python -m skinny_bf16_gemm_residual_gb300.sweep --m 1 2 4 8 16 --output sweep.jsonl
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import statistics
+import sys
+
+import torch
+
+from . import binding as sgr
+from . import inputs
+
+
+def candidate_configs(path: int, M: int, K: int, grid: str) -> list[dict]:
+    out = []
+    if path == sgr.SGR_PATH_SIMT:
+        if M > 16:
+            return []
+        for cps in (1, 2):
+            for rps in (1, 2, 4):
+                for st in (2, 3, 4, 6, 8, 12, 16):
+                    smem = 2048 + st * rps * K * 2
+                    if smem * cps > 228 * 1024 or smem > 232448:
+                        continue
+                    if grid == "small" and st not in (4, 8, 12):
+                        continue
+                    out.append(dict(path=path, ctas_per_sm=cps, rows_per_stage=rps, stages=st))
+    else:
+        tiles = (M + 255) // 256
+        nt = ((M + tiles - 1) // tiles + 15) // 16 * 16  # the library's token tile
+        for kb in (1, 2, 4):
+            for st in (2, 3, 4, 5, 6, 8, 12):
+                for cps in (1, 2):
+                    smem = 2048 + st * kb * (16384 + nt * 128)
+                    if smem * cps > 228 * 1024 or smem > 232448:
+                        continue
+                    if grid == "small" and st not in (2, 4, 6):
+                        continue
+                    out.append(dict(path=path, ctas_per_sm=cps, k_blocks_per_stage=kb, stages=st))
+    return out
+
+
+def summarize(samples):
+    ordered = sorted(samples)
+
+    def pct(f):
+        pos = f * (len(ordered) - 1)
+        lo, hi = math.floor(pos), math.ceil(pos)
+        if lo == hi:
+            return ordered[lo]
+        return ordered[lo] * (1 - (pos - lo)) + ordered[hi] * (pos - lo)
+
+    mean = statistics.mean(samples)
+    return {"median_us": statistics.median(samples), "p10_us": pct(0.1), "p90_us": pct(0.9),
+            "mean_us": mean, "cv_pct": statistics.pstdev(samples) / mean * 100.0}
+
+
+def graph_samples(launch, copies, stream, repeats: int, replays: int):
+    """Eager call per copy, one graph holding all copies, warm replays, then
+    `repeats` event-timed batches of `replays` replays: us per call."""
+    with torch.cuda.stream(stream):
+        for c in range(copies):
+            launch(c)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for c in range(copies):
+            launch(c)
+    out = []
+    with torch.cuda.stream(stream):
+        for _ in range(10):
+            g.replay()
+        for _ in range(repeats):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(replays):
+                g.replay()
+            e1.record(stream)
+            e1.synchronize()
+            out.append(e0.elapsed_time(e1) * 1000.0 / (replays * copies))
+    del g
+    return out
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--m", type=int, nargs="+", default=[1, 2, 4, 8, 16])
+    ap.add_argument("--n", type=int, default=inputs.N_LATENT_MOE)
+    ap.add_argument("--k", type=int, default=inputs.K_LATENT_MOE)
+    ap.add_argument("--paths", default="simt,tc")
+    ap.add_argument("--grid", choices=("small", "full"), default="full")
+    ap.add_argument("--copies", type=int, default=4)
+    ap.add_argument("--repeats", type=int, default=7)
+    ap.add_argument("--replays", type=int, default=50)
+    ap.add_argument("--no-cublas", action="store_true")
+    ap.add_argument("--output", default=None)
+    args = ap.parse_args(argv)
+    torch.cuda.set_device(0)
+    sgr.sgr_init(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.Stream(device=dev)
+    N, K = args.n, args.k
+    Ws = [inputs.make_weights(N, K, seed=s).to(dev) for s in range(args.copies)]
+    props = torch.cuda.get_device_properties(dev)
+    meta = {"device": props.name, "sms": props.multi_processor_count,
+            "l2_bytes": props.L2_cache_size, "torch": torch.__version__}
+    out = open(args.output, "w") if args.output else None
+    paths = {"simt": sgr.SGR_PATH_SIMT, "tc": sgr.SGR_PATH_TC}
+    for M in args.m:
+        A = inputs.make_rows(M, K, seed=10_000 + M).to(dev)
+        Rs = [inputs.make_rows(M, N, seed=20_000 + 100 * M + s).to(dev) for s in range(args.copies)]
+        Ys = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for _ in range(args.copies)]
+        nbytes = 2 * (N * K + M * K + 2 * M * N)
+        rows = []
+        if not args.no_cublas:
+            launch = lambda c: torch.addmm(Rs[c], A, Ws[c].t(), out=Ys[c])
+            rows.append(("cublas_addmm", {}, graph_samples(launch, args.copies, stream, args.repeats, args.replays)))
+        for name in args.paths.split(","):
+            for cfg in candidate_configs(paths[name], M, K, args.grid):
+                c = sgr.make_config(**cfg)
+                launch = lambda i, c=c: sgr.skinny_gemm_residual_ex(A, Ws[i], Rs[i], Ys[i], stream=stream, config=c)
+                try:
+                    rows.append((name, cfg, graph_samples(launch, args.copies, stream, args.repeats, args.replays)))
+                except sgr.SgrError as e:
+                    rows.append((name, cfg, str(e)))
+        for backend, cfg, samples in rows:
+            row = {"m": M, "n": N, "k": K, "backend": backend, "config": cfg, "num_buffers": args.copies, **meta}
+            if isinstance(samples, str):
+                row.update({"valid": False, "error": samples})
+            else:
+                s = summarize(samples)
+                row.update(s)
+                row["gbs"] = nbytes / (s["median_us"] * 1e-6) / 1e9
+            line = json.dumps(row, sort_keys=True)
+            if out:
+                out.write(line + "\n")
+                out.flush()
+        best = {}
+        for backend, cfg, samples in rows:
+            if isinstance(samples, str):
+                continue
+            med = statistics.median(samples)
+            if backend not in best or med < best[backend][0]:
+                best[backend] = (med, cfg)
+        print(f"M={M}: " + "; ".join(f"{b} {v[0]:.2f} us {v[1]}" for b, v in best.items()), flush=True)
+    assert sgr.sgr_device_error() == 0
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -75,13 +75,14 @@ def test_parity_unit_normal_weights():
 
 def test_integer_inputs_are_exact():
     """Integer inputs keep every FP32 partial sum exact, so any summation
-    order gives the oracle's bits exactly."""
+    order gives the exact integer, and one rounding of it gives the
+    oracle's bits."""
     M, N, K = 16, 2048, 512
     A = inputs.integer_bf16((M, K), -2, 2, 1)
     W = inputs.integer_bf16((N, K), -2, 2, 2)
     R = inputs.integer_bf16((M, N), -8, 8, 3)
     want = (A.to(torch.int64) @ W.to(torch.int64).T + R.to(torch.int64))
-    assert want.abs().max() <= 256
+    assert want.abs().max() < 2 ** 24  # every FP32 partial sum is an exact integer
     Y = sgr.skinny_gemm_residual(A.cuda(), W.cuda(), R.cuda())
     torch.cuda.synchronize()
     assert np.array_equal(bits(Y), bits(want.to(torch.bfloat16)))
