@@ -40,6 +40,8 @@ METRIC = "µs/call and achieved HBM GB/s, BF16 skinny GEMM+residual, M=1..16, N7
 N_DIM, K_DIM = 7168, 3584
 M_LIST = (1, 2, 4, 8, 16)
 COPIES = 4
+PATH_NAMES = {1: "simt", 2: "tc", 3: "rows"}
+KERNEL_NAMES = {"simt": "simt_skinny_kernel", "tc": "tc_skinny_kernel", "rows": "rows_skinny_kernel"}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -378,7 +380,7 @@ def run_ours(args):
         per_m_out[str(M)] = {
             "us_per_call": s["median_us"], "p10_us": s["p10_us"], "p90_us": s["p90_us"],
             "cv_pct": s["cv_pct"], "gbs": gbs, "frac_of_hbm_peak": gbs / peaks["hbm_gbs"],
-            "path": {1: "simt", 2: "tc"}.get(sgr.sgr_select_path(M, N_DIM, K_DIM), "?"),
+            "path": PATH_NAMES.get(sgr.sgr_select_path(M, N_DIM, K_DIM), "?"),
         }
         del g
 
@@ -421,13 +423,20 @@ def run_ours(args):
 
     avg_launch_s = elapsed_ms * 1e-3 / (args.steps * launches_per_step)
     achieved = bytes_per_step / launches_per_step / avg_launch_s / 1e9
-    kernels = sorted({{1: "simt", 2: "tc"}.get(sgr.sgr_select_path(M, N_DIM, K_DIM), "?") for M in m_list})
-    dominant = "simt_skinny_kernel" if kernels == ["simt"] else "tc_skinny_kernel" if kernels == ["tc"] else "mixed"
+    # dominant kernel: the path with the largest share of the step's time
+    share = {}
+    for M in m_list:
+        path = PATH_NAMES.get(sgr.sgr_select_path(M, N_DIM, K_DIM), "?")
+        us = per_m_out[str(M)]["us_per_call"] if str(M) in per_m_out else 1.0
+        share[path] = share.get(path, 0.0) + us
+    dominant_path = max(share, key=share.get)
+    dominant = KERNEL_NAMES.get(dominant_path, dominant_path)
     traffic = committed_traffic(dominant)
     roofline = {
         "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
         "frac": achieved / peaks["hbm_gbs"], "traffic": traffic, "peak_source": peak_src,
         "kernel": dominant,
+        "kernels_in_step": {KERNEL_NAMES.get(k, k): round(v / sum(share.values()), 3) for k, v in share.items()},
         "bytes_per_launch": bytes_per_step / launches_per_step,
         "note": "algorithmic bytes 2*(N*K + M*K + 2*M*N) per call averaged over the step's calls / "
                 "average launch duration over the timed region (CUDA events on the launch stream)",

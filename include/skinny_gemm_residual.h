@@ -89,7 +89,8 @@ typedef enum {
 /* Kernel paths. */
 #define SGR_PATH_AUTO 0 /* per-M table */
 #define SGR_PATH_SIMT 1 /* CUDA-core streaming kernel, M <= 16 */
-#define SGR_PATH_TC 2   /* tcgen05 / tensor-memory kernel */
+#define SGR_PATH_TC 2      /* tcgen05 kernel, persistent stream-K with split-K fixup */
+#define SGR_PATH_TC_ROWS 3 /* tcgen05 kernel, one contiguous W row slab per CTA (M <= 256) */
 
 /*
  * Y = bf16(A . W^T + R) with contiguous operands (lda = K, ldr = ldy = N).
@@ -121,8 +122,8 @@ typedef struct {
   int ctas_per_sm;        /* persistent grid = SM count x ctas_per_sm */
   int stages;             /* shared-memory ring depth */
   int rows_per_stage;     /* SIMT: W rows per ring stage */
-  int k_blocks_per_stage; /* TC: 64-wide K blocks per ring stage */
-  int token_tile;         /* TC: activation rows per MMA (multiple of 16, <= 256) */
+  int k_blocks_per_stage; /* TC, TC_ROWS: 64-wide K blocks per ring stage */
+  int token_tile;         /* TC, TC_ROWS: activation rows per MMA (multiple of 16, <= 256) */
   int reserved[2];        /* must be zero */
 } sgr_config;
 
@@ -145,8 +146,8 @@ int sgr_validate(const void* A, int64_t lda, const void* W, const void* R,
 
 /*
  * Kernel path the library chooses for this shape with SGR_PATH_AUTO
- * (SGR_PATH_SIMT or SGR_PATH_TC), or a negative sgr_status if none can run
- * it.  Host-only.
+ * (SGR_PATH_SIMT, SGR_PATH_TC or SGR_PATH_TC_ROWS), or a negative sgr_status
+ * if none can run it.  Host-only.
  */
 int sgr_select_path(int M, int N, int K);
 

@@ -22,6 +22,7 @@ from .binding import (  # noqa: F401
     SGR_PATH_AUTO,
     SGR_PATH_SIMT,
     SGR_PATH_TC,
+    SGR_PATH_TC_ROWS,
     SgrError,
     load,
     make_config,

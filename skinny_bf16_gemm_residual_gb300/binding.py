@@ -30,6 +30,7 @@ SGR_FLAG_NO_PDL = 0x1
 SGR_PATH_AUTO = 0
 SGR_PATH_SIMT = 1
 SGR_PATH_TC = 2
+SGR_PATH_TC_ROWS = 3
 
 
 class SgrError(RuntimeError):

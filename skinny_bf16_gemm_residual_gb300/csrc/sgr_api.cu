@@ -12,6 +12,8 @@
 #include "skinny_gemm_residual.h"
 #include "sgr_simt.cuh"
 #include "sgr_tc.cuh"
+#include "sgr_rows.cuh"
+#include "sgr_table.h"
 
 namespace {
 
@@ -146,11 +148,10 @@ int init_device(int dev) {
     const int vpts[3] = {1, 2, 4};
     for (int mt : mts)
       for (int v : vpts)
-        if (ok == SGR_OK &&
-            cudaFuncSetAttribute(simt_fn(mt, v), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kMaxDynSmem) != cudaSuccess)
+        if (ok == SGR_OK && sgr::set_kernel_smem_attrs(reinterpret_cast<const void*>(simt_fn(mt, v))) != cudaSuccess)
           ok = SGR_ERR_DEVICE;
     if (ok == SGR_OK && sgr::tc_init_device(sms, &st.ws) != cudaSuccess) ok = SGR_ERR_DEVICE;
+    if (ok == SGR_OK && sgr::rows_init_device() != cudaSuccess) ok = SGR_ERR_DEVICE;
     if (ok != SGR_OK) cudaGetLastError();
     st.sms = sms;
     st.err = static_cast<unsigned*>(errp);
@@ -160,12 +161,29 @@ int init_device(int dev) {
   return st.status;
 }
 
-// Library choice for a shape.  The SIMT kernel serves small M on CUDA cores;
-// larger M needs the tensor-core kernel.
-int select_path(int M, int N, int K) {
-  (void)N;
-  if (M <= 16 && simt_vpt(K) > 0) return SGR_PATH_SIMT;
+// The measured table entry for (N, K) that covers M: the first entry whose M
+// is >= the call's M (entries are sorted by M), or nullptr.
+const sgr::TableEntry* table_lookup(int M, int N, int K) {
+  for (int i = 0; i < sgr::kTableSize; ++i) {
+    const sgr::TableEntry& e = sgr::kTable[i];
+    if (e.n == N && e.k == K && e.m >= M) return &e;
+  }
+  return nullptr;
+}
+
+// Library choice for a shape: the measured per-M table where it covers the
+// shape; otherwise the SIMT kernel for M <= 2, the row-slab tensor-core
+// kernel up to 256 tokens, and the stream-K tensor-core kernel beyond.
+int select_path(int M, int N, int K, int sms) {
+  if (const sgr::TableEntry* e = table_lookup(M, N, K)) {
+    if (e->path == SGR_PATH_SIMT && M <= 16 && simt_vpt(K) > 0) return SGR_PATH_SIMT;
+    if (e->path == SGR_PATH_TC_ROWS && sgr::rows_supported(sms, M, N, K)) return SGR_PATH_TC_ROWS;
+    if (e->path == SGR_PATH_TC && sgr::tc_supported(M, N, K)) return SGR_PATH_TC;
+  }
+  if (M <= 2 && simt_vpt(K) > 0) return SGR_PATH_SIMT;
+  if (sgr::rows_supported(sms, M, N, K)) return SGR_PATH_TC_ROWS;
   if (sgr::tc_supported(M, N, K)) return SGR_PATH_TC;
+  if (M <= 16 && simt_vpt(K) > 0) return SGR_PATH_SIMT;
   return -SGR_ERR_UNSUPPORTED;
 }
 
@@ -187,8 +205,9 @@ void default_simt_config(int sms, int M, int K, sgr_config* c) {
 int resolve_config(int dev_sms, int M, int N, int K, const sgr_config* in, sgr_config* out) {
   std::memset(out, 0, sizeof *out);
   int path = in ? in->path : SGR_PATH_AUTO;
-  if (path == SGR_PATH_AUTO) {
-    path = select_path(M, N, K);
+  const bool automatic = (path == SGR_PATH_AUTO);
+  if (automatic) {
+    path = select_path(M, N, K, dev_sms);
     if (path < 0) return -path;
   }
   if (path == SGR_PATH_SIMT) {
@@ -197,8 +216,20 @@ int resolve_config(int dev_sms, int M, int N, int K, const sgr_config* in, sgr_c
   } else if (path == SGR_PATH_TC) {
     if (!sgr::tc_supported(M, N, K)) return SGR_ERR_UNSUPPORTED;
     sgr::tc_default_config(dev_sms, M, N, K, out);
+  } else if (path == SGR_PATH_TC_ROWS) {
+    if (!sgr::rows_supported(dev_sms, M, N, K)) return SGR_ERR_UNSUPPORTED;
+    sgr::rows_default_config(dev_sms, M, N, K, out);
   } else {
     return SGR_ERR_UNSUPPORTED;
+  }
+  if (automatic) {  // measured configuration for this shape, if the table has one
+    const sgr::TableEntry* e = table_lookup(M, N, K);
+    if (e && e->path == path) {
+      out->ctas_per_sm = e->ctas_per_sm;
+      out->stages = e->stages;
+      if (path == SGR_PATH_SIMT) out->rows_per_stage = e->rows_per_stage;
+      else out->k_blocks_per_stage = e->k_blocks_per_stage;
+    }
   }
   if (in) {
     for (int r : in->reserved)
@@ -216,6 +247,13 @@ int resolve_config(int dev_sms, int M, int N, int K, const sgr_config* in, sgr_c
     int grid = 0;
     size_t smem = 0;
     int rc = sgr::tc_plan(*out, dev_sms > 0 ? dev_sms : 1, M, N, K, &tp, &grid, &smem);
+    if (rc != SGR_OK) return rc;
+  }
+  if (path == SGR_PATH_TC_ROWS) {
+    sgr::RowsParams rp;
+    int grid = 0;
+    size_t smem = 0;
+    int rc = sgr::rows_plan(*out, dev_sms > 0 ? dev_sms : 1, M, N, K, &rp, &grid, &smem);
     if (rc != SGR_OK) return rc;
   }
   if (path == SGR_PATH_SIMT) {
@@ -289,6 +327,9 @@ int run(const void* A, long long lda, const void* W, const void* R, long long ld
   if ((rc = resolve_config(st.sms, M, N, K, cfg, &c)) != SGR_OK) return rc;
   if (c.path == SGR_PATH_SIMT)
     return launch_simt(c, st.sms, st.err, A, lda, W, R, ldr, Y, ldy, M, N, K, flags, stream);
+  if (c.path == SGR_PATH_TC_ROWS)
+    return sgr::rows_launch(c, st.sms, st.err, A, lda, W, R, ldr, Y, ldy, M, N, K,
+                            (flags & SGR_FLAG_NO_PDL) == 0, stream);
   return sgr::tc_launch(c, st.sms, st.err, &st.ws, A, lda, W, R, ldr, Y, ldy, M, N, K,
                         (flags & SGR_FLAG_NO_PDL) == 0, stream);
 }
@@ -321,7 +362,13 @@ int sgr_validate(const void* A, int64_t lda, const void* W, const void* R, int64
 
 int sgr_select_path(int M, int N, int K) {
   if (M < 1 || N < 1 || K < 8 || N % 8 || K % 8) return -SGR_ERR_SHAPE;
-  return select_path(M, N, K);
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
+    cudaGetLastError();
+    sms = 148;  // no device visible: plan for a GB300-class part
+  }
+  return select_path(M, N, K, sms);
 }
 
 int sgr_default_config(int device, int M, int N, int K, int path, sgr_config* cfg) {
@@ -373,6 +420,19 @@ int sgr_kernel_resources(int device, int path, int M, int N, int K, int* regs, i
     }
     *smem_bytes = (int)sgr::simt_smem_bytes(c.stages, c.rows_per_stage, K);
     *threads = sgr::kSimtThreads;
+  } else if (c.path == SGR_PATH_TC_ROWS) {
+    if (cudaFuncGetAttributes(&fa, sgr::rows_skinny_kernel) != cudaSuccess) {
+      cudaGetLastError();
+      return SGR_ERR_DEVICE;
+    }
+    sgr::RowsParams rp;
+    int grid = 0;
+    size_t smem = 0;
+    int sms = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+    if (sgr::rows_plan(c, sms, M, N, K, &rp, &grid, &smem) != SGR_OK) return SGR_ERR_UNSUPPORTED;
+    *smem_bytes = (int)smem;
+    *threads = sgr::kRowsThreads;
   } else {
     int s = 0, t = 0;
     const void* fn = sgr::tc_kernel_for(M, N, K, &c, &s, &t);

@@ -111,7 +111,11 @@ __global__ void __launch_bounds__(kSimtThreads, (MT <= 4 ? 2 : 1))
     }
     fence_mbar_init();
   }
+  __syncwarp();
   __syncthreads();
+  // The dependent grid may be scheduled now: its own griddepcontrol.wait
+  // still orders its reads of our outputs after this grid completes.
+  pdl_launch_dependents();
 
   if (warp == kSimtConsumerWarps) {
     // ---------------- producer: stream this CTA's W slab through the ring
@@ -134,7 +138,6 @@ __global__ void __launch_bounds__(kSimtThreads, (MT <= 4 ? 2 : 1))
                  bytes, fb, pol);
         issued = s + 1;
       }
-      pdl_launch_dependents();
       // Before this CTA can exit, every copy it issued must have landed.
       for (int t = max(0, issued - S); t < issued; ++t) {
         if (!mbar_wait(smem_u32(&full[t % S]), (t / S) & 1)) {
@@ -252,7 +255,6 @@ __global__ void __launch_bounds__(kSimtThreads, (MT <= 4 ? 2 : 1))
     }
     buf ^= 1;
   }
-  pdl_launch_dependents();
 }
 
 }  // namespace sgr

@@ -70,6 +70,7 @@ struct TcParams {
   int k_stages;  // ceil(K / (64 * kbps))
   int kbps;      // 64-wide K blocks per stage
   int stages;    // ring depth
+  int chains;    // independent TMEM accumulators per buffer (1, 2 or 4)
   int tmem_cols;
 };
 
@@ -93,14 +94,25 @@ __device__ __forceinline__ int tc_cta_of(long long U, int G, long long u) {
 // Wait that also returns (false) as soon as another role of the CTA aborted.
 __device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity,
                                                    volatile int* abort_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_test_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
 #pragma unroll 1
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    for (int i = 0; i < 64; ++i)
+      if (mbar_test_wait(bar, parity)) return true;
     if (*abort_flag) return false;
     if (globaltimer_ns() - t0 > SGR_WAIT_LIMIT_NS) return false;
+  }
+}
+
+// 16 accumulator columns summed over the chains, chain 0 first (fixed order).
+__device__ __forceinline__ void tc_ld_chains(uint32_t taddr, int nt, int chains, float (&v)[16]) {
+  tmem_ld16(taddr, v);
+  for (int c = 1; c < chains; ++c) {
+    float w[16];
+    tmem_ld16(taddr + (uint32_t)(c * nt), w);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] += w[i];
   }
 }
 
@@ -145,6 +157,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     *bcast = 0;
     fence_mbar_init();
   }
+  __syncwarp();
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), (uint32_t)p.tmem_cols);
     tmem_relinquish();
@@ -237,8 +250,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t d = tmem + (uint32_t)(buf * p.NT);
-        bool first = true;
+        const uint32_t d = tmem + (uint32_t)(buf * p.chains * p.NT);
+        bool seg_start = true;
         for (; u < seg_end; ++u, ++i) {
           const int slot = i % S;
           if (!mbar_wait_or_abort(smem_u32(&full[slot]), (i / S) & 1, abort_flag)) {
@@ -250,12 +263,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           for (int j = 0; j < p.kbps; ++j) {
 #pragma unroll
             for (int kk = 0; kk < kTcKBlock / 16; ++kk) {
+              // K step kk accumulates into chain kk % chains (independent MMAs pipeline).
+              const int chain = kk & (p.chains - 1);
               const uint64_t ad = smem_desc_sw128(st + (uint32_t)j * (kTcTileRows * 128u) + kk * 32u);
               const uint64_t bd = smem_desc_sw128(st + w_bytes + (uint32_t)(j * p.NT * 128) + kk * 32u);
-              mma_bf16(d, ad, bd, idesc, first ? 0u : 1u);
-              first = false;
+              const bool first = seg_start && j == 0 && kk < p.chains;
+              mma_bf16(d + (uint32_t)(chain * p.NT), ad, bd, idesc, first ? 0u : 1u);
             }
           }
+          seg_start = false;
           mma_commit(smem_u32(&empty[slot]));  // stage free once these MMAs finish
         }
         if (!ok) break;
@@ -298,25 +314,33 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld below is warp-collective
       tc_fence_after();
-      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * p.NT);
+      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * p.chains * p.NT);
       float* part = p.ws + (size_t)(c * 2 + (first_seg ? 0 : 1)) * p.NT * kTcTileRows;
       if (ok) {
         for (int col0 = 0; col0 < p.NT; col0 += 16) {
           float v[16];
-          tmem_ld16(taddr + (uint32_t)col0, v);
           if (complete) {
+            // Residual loads first (independent of the accumulator), then one
+            // rounding per element.
+            float r[16];
+#pragma unroll
+            for (int cc = 0; cc < 16; ++cc) {
+              const int m = col0 + cc;
+              r[cc] = (m < m_count && n < p.N)
+                          ? __bfloat162float(p.R[(size_t)(m_base + m) * p.ldr + n])
+                          : 0.f;
+            }
+            tc_ld_chains(taddr + (uint32_t)col0, p.NT, p.chains, v);
             if (n < p.N) {
 #pragma unroll
               for (int cc = 0; cc < 16; ++cc) {
                 const int m = col0 + cc;
-                if (m < m_count) {
-                  const size_t gm = (size_t)(m_base + m);
-                  const float r = __bfloat162float(p.R[gm * p.ldr + n]);
-                  p.Y[gm * p.ldy + n] = __float2bfloat16_rn(v[cc] + r);
-                }
+                if (m < m_count)
+                  p.Y[(size_t)(m_base + m) * p.ldy + n] = __float2bfloat16_rn(v[cc] + r[cc]);
               }
             }
           } else {
+            tc_ld_chains(taddr + (uint32_t)col0, p.NT, p.chains, v);
 #pragma unroll
             for (int cc = 0; cc < 16; ++cc) part[(size_t)(col0 + cc) * kTcTileRows + row] = v[cc];
           }
@@ -346,15 +370,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         named_bar_sync(1, 128);
         if (*bcast && n < p.N) {
-          for (int m = 0; m < m_count; ++m) {
-            float acc = 0.f;
+          // Sum the partials in K order (contributor order), 16 tokens at a
+          // time with all loads of a group in flight together.
+          for (int mc = 0; mc < m_count; mc += 16) {
+            float acc[16], r[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              acc[i] = 0.f;
+              r[i] = (mc + i < m_count) ? __bfloat162float(p.R[(size_t)(m_base + mc + i) * p.ldr + n]) : 0.f;
+            }
             for (int cc = c_first; cc <= c_last; ++cc) {
               const int h = (cc == c_first && tc_unit_begin(U, G, cc) < t_begin) ? 1 : 0;
-              acc += __ldcg(p.ws + (size_t)(cc * 2 + h) * p.NT * kTcTileRows + (size_t)m * kTcTileRows + row);
+              const float* src = p.ws + (size_t)(cc * 2 + h) * p.NT * kTcTileRows + (size_t)mc * kTcTileRows + row;
+              float v[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) v[i] = (mc + i < m_count) ? __ldcg(src + (size_t)i * kTcTileRows) : 0.f;
+#pragma unroll
+              for (int i = 0; i < 16; ++i) acc[i] += v[i];
             }
-            const size_t gm = (size_t)(m_base + m);
-            const float r = __bfloat162float(p.R[gm * p.ldr + n]);
-            p.Y[gm * p.ldy + n] = __float2bfloat16_rn(acc + r);
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              if (mc + i < m_count)
+                p.Y[(size_t)(m_base + mc + i) * p.ldy + n] = __float2bfloat16_rn(acc[i] + r[i]);
           }
         }
       }
@@ -362,6 +399,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   }
 
+  __syncwarp();  // lane-0 roles rejoin their warp before the CTA-wide barrier
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -454,8 +492,7 @@ inline cudaError_t tc_init_device(int sms, TcWorkspace* ws) {
   ws->counter_count = kTcMaxCounters;
   e = cudaMemset(ws->counters, 0, (size_t)kTcMaxCounters * sizeof(unsigned));
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(tc_skinny_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
-  return e;
+  return set_kernel_smem_attrs(reinterpret_cast<const void*>(tc_skinny_kernel));
 }
 
 // Checks a resolved TC configuration for this shape; fills the kernel params.
@@ -485,7 +522,8 @@ inline int tc_plan(const sgr_config& c, int sms, int M, int N, int K, TcParams* 
   p->kbps = c.k_blocks_per_stage;
   p->stages = c.stages;
   p->units = units;
-  p->tmem_cols = detail::pow2_at_least(2 * nt);
+  p->chains = nt <= 64 ? 4 : (nt <= 128 ? 2 : 1);  // 2 buffers * chains * NT <= 512 TMEM columns
+  p->tmem_cols = detail::pow2_at_least(2 * p->chains * nt);
   *grid = (int)g;
   *smem = sm;
   return SGR_OK;

@@ -38,6 +38,20 @@ def candidate_configs(path: int, M: int, K: int, grid: str) -> list[dict]:
                     if grid == "small" and st not in (4, 8, 12):
                         continue
                     out.append(dict(path=path, ctas_per_sm=cps, rows_per_stage=rps, stages=st))
+    elif path == sgr.SGR_PATH_TC_ROWS:
+        if M > 256:
+            return []
+        nt = (M + 15) // 16 * 16
+        rb = 48
+        for kb in (1, 2, 4, 8):
+            for st in (2, 3, 4, 5, 6, 8, 10, 12):
+                slack = max(0, 16384 - rb * 128 - st * kb * nt * 128)
+                smem = 2048 + st * kb * (rb * 128 + nt * 128) + slack
+                if smem > 232448:
+                    continue
+                if grid == "small" and st not in (3, 4, 6):
+                    continue
+                out.append(dict(path=path, ctas_per_sm=1, k_blocks_per_stage=kb, stages=st))
     else:
         tiles = (M + 255) // 256
         nt = ((M + tiles - 1) // tiles + 15) // 16 * 16  # the library's token tile
@@ -101,7 +115,7 @@ def main(argv=None):
     ap.add_argument("--m", type=int, nargs="+", default=[1, 2, 4, 8, 16])
     ap.add_argument("--n", type=int, default=inputs.N_LATENT_MOE)
     ap.add_argument("--k", type=int, default=inputs.K_LATENT_MOE)
-    ap.add_argument("--paths", default="simt,tc")
+    ap.add_argument("--paths", default="simt,tc,rows")
     ap.add_argument("--grid", choices=("small", "full"), default="full")
     ap.add_argument("--copies", type=int, default=4)
     ap.add_argument("--repeats", type=int, default=7)
@@ -119,7 +133,7 @@ def main(argv=None):
     meta = {"device": props.name, "sms": props.multi_processor_count,
             "l2_bytes": props.L2_cache_size, "torch": torch.__version__}
     out = open(args.output, "w") if args.output else None
-    paths = {"simt": sgr.SGR_PATH_SIMT, "tc": sgr.SGR_PATH_TC}
+    paths = {"simt": sgr.SGR_PATH_SIMT, "tc": sgr.SGR_PATH_TC, "rows": sgr.SGR_PATH_TC_ROWS}
     for M in args.m:
         A = inputs.make_rows(M, K, seed=10_000 + M).to(dev)
         Rs = [inputs.make_rows(M, N, seed=20_000 + 100 * M + s).to(dev) for s in range(args.copies)]

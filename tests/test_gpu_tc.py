@@ -28,10 +28,13 @@ def _device():
     assert sgr.sgr_device_error(0) == 0, "a kernel reported a timed-out wait"
 
 
-def run_tc(p, **cfg):
+ROWS = sgr.SGR_PATH_TC_ROWS
+
+
+def run_tc(p, path=TC, **cfg):
     A, W, R = (t.cuda() for t in (p.A, p.W, p.R))
     Y = torch.full_like(R, float("nan"))
-    sgr.skinny_gemm_residual_ex(A, W, R, Y, config=sgr.make_config(path=TC, **cfg))
+    sgr.skinny_gemm_residual_ex(A, W, R, Y, config=sgr.make_config(path=path, **cfg))
     torch.cuda.synchronize()
     return bits(Y)
 
@@ -41,23 +44,61 @@ SMALL = [(1, 520, 264), (3, 7168, 64), (4, 2056, 3584), (5, 304, 8), (7, 1512, 1
          (40, 1000, 1032), (100, 1024, 520), (250, 264, 1000), (300, 392, 264)]
 
 
+PATHS = pytest.mark.parametrize("path", [TC, ROWS], ids=["streamk", "rows"])
+
+
+@PATHS
 @pytest.mark.parametrize("M,N,K", SMALL)
-def test_tc_small_shapes(M, N, K):
+def test_tc_small_shapes(M, N, K, path):
     p = inputs.make_problem(M, N, K, seed=M * 7 + N + K)
-    compare(run_tc(p), oracle_full(p.A, p.W, p.R), f"tc {M}x{N}x{K}")
+    if path == ROWS and M > 256:  # the row-slab kernel holds at most 256 tokens
+        with pytest.raises(sgr.SgrError) as e:
+            run_tc(p, path)
+        assert e.value.status == sgr.SGR_ERR_UNSUPPORTED
+        return
+    compare(run_tc(p, path), oracle_full(p.A, p.W, p.R), f"path {path} {M}x{N}x{K}")
 
 
+@PATHS
 @pytest.mark.parametrize("M", [1, 2, 4, 8, 16])
 @pytest.mark.parametrize("seed", [0, 1, 2, 3])
-def test_tc_full_size_m_sweep(M, seed):
+def test_tc_full_size_m_sweep(M, seed, path):
     p = inputs.make_problem(M, N_FULL, K_FULL, seed=seed)
-    compare(run_tc(p), oracle_full(p.A, p.W, p.R), f"tc M={M} seed={seed}")
+    compare(run_tc(p, path), oracle_full(p.A, p.W, p.R), f"path {path} M={M} seed={seed}")
 
 
+@PATHS
 @pytest.mark.parametrize("M", [32, 64, 128])
-def test_tc_full_size_transition(M):
+def test_tc_full_size_transition(M, path):
     p = inputs.make_problem(M, N_FULL, K_FULL, seed=M)
-    compare(run_tc(p), oracle_full(p.A, p.W, p.R), f"tc M={M}")
+    compare(run_tc(p, path), oracle_full(p.A, p.W, p.R), f"path {path} M={M}")
+
+
+ROWS_CONFIGS = [
+    dict(k_blocks_per_stage=1, stages=2),
+    dict(k_blocks_per_stage=1, stages=8),
+    dict(k_blocks_per_stage=2, stages=5),
+    dict(k_blocks_per_stage=4, stages=3),
+    dict(k_blocks_per_stage=8, stages=2),
+    dict(k_blocks_per_stage=3, stages=4),
+    dict(k_blocks_per_stage=2, stages=3, token_tile=64),
+]
+
+
+@pytest.mark.parametrize("cfg", ROWS_CONFIGS, ids=lambda c: "-".join(f"{k}{v}" for k, v in c.items()))
+@pytest.mark.parametrize("M", [1, 9, 16])
+def test_rows_configs(cfg, M):
+    p = inputs.make_problem(M, N_FULL, K_FULL, seed=71 + M)
+    compare(run_tc(p, ROWS, **cfg), oracle_full(p.A, p.W, p.R), f"rows M={M} {cfg}")
+
+
+def test_rows_rejects_bad_config():
+    p = inputs.make_problem(20, 256, 256, seed=1)
+    A, W, R = (t.cuda() for t in (p.A, p.W, p.R))
+    for cfg in (dict(token_tile=16), dict(ctas_per_sm=2), dict(k_blocks_per_stage=8, stages=12)):
+        with pytest.raises(sgr.SgrError) as e:
+            sgr.skinny_gemm_residual_ex(A, W, R, config=sgr.make_config(path=ROWS, **cfg))
+        assert e.value.status == sgr.SGR_ERR_UNSUPPORTED
 
 
 @pytest.mark.parametrize("M", [256, 512, 1024])
