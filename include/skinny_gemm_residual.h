@@ -187,6 +187,37 @@ const char* sgr_status_string(int status);
 /* SGR_ABI_VERSION of the built library; bindings compare it with their own. */
 int sgr_abi_version(void);
 
+/*
+ * Allocation-free variant (no counterpart on the pages; added for callers
+ * that must not allocate device memory).  Same operation, arguments, errors
+ * and PDL contract as skinny_gemm_residual_ex, computed by the stream-K
+ * tensor-core kernel, with its split-K scratch taken from a fixed array
+ * inside this library instead of the workspace that sgr_init() allocates.
+ * Who needs it: code that runs while a stream is being captured in a mode
+ * that forbids cudaMalloc, engines that reserve all device memory up front
+ * and allow no further allocation, and callers on latency-critical paths that
+ * cannot risk the implicit device synchronisation an allocation may cause.
+ * This entry point calls no cudaMalloc, cudaFree or allocating library
+ * routine; sgr_init() is not needed and is not called.
+ *
+ * Limits: the scratch array is 16 KiB of tile counters plus 4 MiB of FP32
+ * partial tiles, held by every GPU that loads the library until the process
+ * exits.  A shape needing more (more than 4096 output tiles of 128 W rows x
+ * one token tile, or more than 4 MiB of partials, which is grid x 2 x token
+ * tile x 128 floats; in practice M above 16 on a 152-SM GPU) returns
+ * SGR_ERR_UNSUPPORTED without launching.
+ *
+ * The first call on a device resolves the array's device address (with that
+ * device current) and sets kernel attributes; make that first call before
+ * any stream capture.  Every call on a device shares the one array: it clears
+ * the counters it uses before its kernel runs, and calls whose work may
+ * overlap on the GPU (different streams, or graphs replayed concurrently)
+ * race on the array and must be serialised by the caller.
+ */
+int skinny_gemm_residual_noalloc(const void* A, int64_t lda, const void* W,
+                                 const void* R, int64_t ldr, void* Y, int64_t ldy,
+                                 int M, int N, int K, unsigned flags, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -40,5 +40,7 @@ from .binding import (  # noqa: F401
     skinny_gemm_residual_config_ptr,
     skinny_gemm_residual_ex,
     skinny_gemm_residual_ex_ptr,
+    skinny_gemm_residual_noalloc,
+    skinny_gemm_residual_noalloc_ptr,
     skinny_gemm_residual_ptr,
 )

@@ -67,6 +67,7 @@ EXPORTS = (
     "sgr_kernel_resources",
     "sgr_status_string",
     "sgr_abi_version",
+    "skinny_gemm_residual_noalloc",
 )
 
 
@@ -101,6 +102,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.sgr_status_string.argtypes = [I]
         lib.sgr_status_string.restype = ctypes.c_char_p
         lib.sgr_abi_version.argtypes = []
+        lib.skinny_gemm_residual_noalloc.argtypes = [vp, i64, vp, vp, i64, vp, i64, I, I, I, U, vp]
         for name in EXPORTS:
             if name != "sgr_status_string":
                 getattr(lib, name).restype = ctypes.c_int
@@ -274,6 +276,31 @@ def skinny_gemm_residual_config(A, W, R, Y=None, config: sgr_config | None = Non
     """Explicit launch configuration (sweeps, tests)."""
     return skinny_gemm_residual_ex(A, W, R, Y, flags=flags, stream=stream,
                                    config=config if config is not None else sgr_config())
+
+
+def skinny_gemm_residual_noalloc_ptr(A: int, lda: int, W: int, R: int, ldr: int, Y: int, ldy: int,
+                                    M: int, N: int, K: int, flags: int, stream: int) -> int:
+    """Allocation-free entry point on raw device addresses; returns the status."""
+    return load().skinny_gemm_residual_noalloc(A, lda, W, R, ldr, Y, ldy, M, N, K, flags, stream)
+
+
+def skinny_gemm_residual_noalloc(A, W, R, Y, flags: int = 0, stream=None):
+    """Y = bf16(A . W^T + R) without any device allocation (fixed scratch
+    inside the library; see include/skinny_gemm_residual.h).  Y is required:
+    this call allocates nothing, not even its output."""
+    for t, n in ((A, "A"), (W, "W"), (R, "R"), (Y, "Y")):
+        _check_tensor(t, n)
+    M, K = A.shape
+    N = W.shape[0]
+    if W.shape[1] != K or tuple(R.shape) != (M, N) or tuple(Y.shape) != (M, N):
+        raise ValueError(f"shape mismatch A{tuple(A.shape)} W{tuple(W.shape)} R{tuple(R.shape)} Y{tuple(Y.shape)}")
+    if not W.is_contiguous():
+        raise ValueError("W must be contiguous [N, K]")
+    rc = skinny_gemm_residual_noalloc_ptr(A.data_ptr(), _ld(A), W.data_ptr(), R.data_ptr(), _ld(R),
+                                          Y.data_ptr(), _ld(Y), M, N, K, flags, _stream_handle(stream))
+    if rc != SGR_OK:
+        raise SgrError(rc, "skinny_gemm_residual_noalloc")
+    return Y
 
 
 def make_config(path: int = SGR_PATH_AUTO, ctas_per_sm: int = 0, stages: int = 0,

@@ -334,6 +334,97 @@ int run(const void* A, long long lda, const void* W, const void* R, long long ld
                         (flags & SGR_FLAG_NO_PDL) == 0, stream);
 }
 
+// ------------------------------------------------------------ no-allocation variant
+// Scratch for skinny_gemm_residual_noalloc: split-K tile counters followed by
+// FP32 partial tiles, in one file-scope device array.  Every GPU that loads
+// this library holds it (4 MiB + 16 KiB) until the process exits.  Host code
+// must not use the symbol itself as a pointer: it is a host-side stand-in, and
+// the device address comes from cudaGetSymbolAddress (once per device).
+constexpr int kNoallocCounters = 4096;              // W tiles x token tiles
+constexpr size_t kNoallocPartialFloats = 1u << 20;  // 4 MiB of FP32 partials
+constexpr size_t kNoallocBytes = kNoallocCounters * sizeof(unsigned) + kNoallocPartialFloats * sizeof(float);
+static __device__ __align__(256) unsigned char g_sgr_noalloc_scratch[kNoallocBytes];
+
+struct NoallocState {
+  std::once_flag once;
+  int status = SGR_ERR_DEVICE;
+  int sms = 0;
+  unsigned char* scratch = nullptr;  // device address of g_sgr_noalloc_scratch
+  unsigned* err = nullptr;           // device address of g_sgr_error_word
+};
+NoallocState g_noalloc[kMaxDevices];
+
+// One-time set-up for the current device (which must be `dev`): resolve the
+// device addresses of the scratch array and of the error word, and set the
+// kernel's shared-memory attributes.  Allocates nothing.
+int noalloc_setup(int dev) {
+  NoallocState& st = g_noalloc[dev];
+  std::call_once(st.once, [&] {
+    int ok = SGR_OK;
+    int sms = 0;
+    void* scratch = nullptr;
+    void* errp = nullptr;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+      ok = SGR_ERR_DEVICE;
+    if (ok == SGR_OK && cudaGetSymbolAddress(&scratch, g_sgr_noalloc_scratch) != cudaSuccess)
+      ok = SGR_ERR_DEVICE;
+    if (ok == SGR_OK && cudaGetSymbolAddress(&errp, g_sgr_error_word) != cudaSuccess) ok = SGR_ERR_DEVICE;
+    if (ok == SGR_OK &&
+        sgr::set_kernel_smem_attrs(reinterpret_cast<const void*>(sgr::tc_skinny_kernel)) != cudaSuccess)
+      ok = SGR_ERR_DEVICE;
+    if (ok != SGR_OK) cudaGetLastError();
+    st.sms = sms;
+    st.scratch = static_cast<unsigned char*>(scratch);
+    st.err = static_cast<unsigned*>(errp);
+    st.status = ok;
+  });
+  return st.status;
+}
+
+int run_noalloc(const void* A, long long lda, const void* W, const void* R, long long ldr, void* Y,
+                long long ldy, int M, int N, int K, unsigned flags, void* stream_ptr) {
+  int rc = validate(A, lda, W, R, ldr, Y, ldy, M, N, K);
+  if (rc != SGR_OK) return rc;
+  if (M == 0 || N == 0) return SGR_OK;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  if (K == 0) {  // empty sum: Y = R
+    if (Y == R) return SGR_OK;
+    if (cudaMemcpy2DAsync(Y, (size_t)ldy * 2, R, (size_t)ldr * 2, (size_t)N * 2, (size_t)M,
+                          cudaMemcpyDeviceToDevice, stream) != cudaSuccess) {
+      cudaGetLastError();
+      return SGR_ERR_LAUNCH;
+    }
+    return SGR_OK;
+  }
+  if (!sgr::tc_supported(M, N, K)) return SGR_ERR_UNSUPPORTED;
+  int dev;
+  if ((rc = current_device(&dev)) != SGR_OK) return rc;
+  if ((rc = noalloc_setup(dev)) != SGR_OK) return rc;
+  NoallocState& st = g_noalloc[dev];
+  sgr_config c;
+  std::memset(&c, 0, sizeof c);
+  sgr::tc_default_config(st.sms, M, N, K, &c);
+  sgr::TcParams plan;
+  int grid = 0;
+  size_t smem = 0;
+  if ((rc = sgr::tc_plan(c, st.sms, M, N, K, &plan, &grid, &smem)) != SGR_OK) return rc;
+  const long long tiles = (long long)((N + sgr::kTcTileRows - 1) / sgr::kTcTileRows) * plan.m_tiles;
+  const size_t partials = (size_t)grid * 2 * plan.NT * sgr::kTcTileRows;
+  if (tiles > kNoallocCounters || partials > kNoallocPartialFloats) return SGR_ERR_UNSUPPORTED;
+  sgr::TcWorkspace ws;
+  ws.counters = reinterpret_cast<unsigned*>(st.scratch);
+  ws.counter_count = kNoallocCounters;
+  ws.partials = reinterpret_cast<float*>(st.scratch + kNoallocCounters * sizeof(unsigned));
+  ws.partial_floats = kNoallocPartialFloats;
+  // The array keeps the previous call's contents: counters must start at zero.
+  if (cudaMemsetAsync(ws.counters, 0, (size_t)tiles * sizeof(unsigned), stream) != cudaSuccess) {
+    cudaGetLastError();
+    return SGR_ERR_LAUNCH;
+  }
+  return sgr::tc_launch(c, st.sms, st.err, &ws, A, lda, W, R, ldr, Y, ldy, M, N, K,
+                        (flags & SGR_FLAG_NO_PDL) == 0, stream);
+}
+
 }  // namespace
 
 extern "C" {
@@ -463,5 +554,11 @@ const char* sgr_status_string(int status) {
 }
 
 int sgr_abi_version(void) { return SGR_ABI_VERSION; }
+
+int skinny_gemm_residual_noalloc(const void* A, int64_t lda, const void* W, const void* R,
+                                 int64_t ldr, void* Y, int64_t ldy, int M, int N, int K,
+                                 unsigned flags, void* stream) {
+  return run_noalloc(A, lda, W, R, ldr, Y, ldy, M, N, K, flags, stream);
+}
 
 }  // extern "C"
