@@ -10,7 +10,17 @@
 // element is split across CTAs: no workspace, no counters, no fixup tail.
 // The slab is streamed once with 2-D TMA boxes of RB rows x 64 K into a
 // shared-memory ring and multiplied on the tensor core with
-// tcgen05.mma M=128 (W rows) x N=NT (tokens) x K=16.  The ring stores only
+// tcgen05.mma M=128 (W rows) x N=G*NT (tokens) x K=16.
+//
+// Diagonal packing: the W boxes of consecutive K blocks sit back to back in
+// the ring, so a 128-row MMA window starting at block j holds block j in rows
+// [0, RB), block j+1 in rows [RB, 2 RB), ...; the activation boxes sit back to
+// back too, so an N = G*NT window holds the tokens of blocks j .. j+G-1.  One
+// MMA then computes G useful diagonal blocks D[g RB + r, g NT + t] (block
+// j+g of W against block j+g of A) plus cross terms that are never read.
+// With RB = 48 this is G = 2: half the MMAs and half the shared-memory reads
+// of the W operand, which is what bounds a 16-token MMA.  The epilogue sums
+// the G diagonal blocks (in g order) through shared memory.  The ring stores only
 // the RB loaded rows per K block; the MMA's 128-row window over-reads into the
 // following bytes of shared memory (the next W blocks, then the A ring that
 // follows the W ring, then slack if needed), and those extra rows only feed
@@ -37,7 +47,7 @@ namespace sgr {
 
 constexpr int kRowsThreads = 192;
 constexpr int kRowsMaxTokens = 256;
-constexpr int kRowsPrefetchTokens = 32;  // residual values held in registers before the MMAs end
+constexpr int kRowsPrefetchTokens = 16;  // residual values held in registers before the MMAs end
 constexpr uint32_t kRowsSlack = kTcTileRows * 128u;  // MMA window over-read past the ring
 
 struct RowsParams {
@@ -51,7 +61,7 @@ struct RowsParams {
   int k_stages;  // ceil(K / (64 * kbps))
   int kbps;      // 64-wide K blocks per stage
   int stages;    // ring depth
-  int chains;    // independent TMEM accumulators (1, 2 or 4), summed in the epilogue
+  int groups;    // K blocks packed into one MMA along its diagonal (1, 2 or 4)
   int tmem_cols;
 };
 
@@ -72,15 +82,10 @@ __host__ __device__ inline size_t rows_smem_bytes(int stages, int kbps, int rb, 
          (size_t)stages * rows_stage_bytes(kbps, rb, nt) + rows_tail_slack(stages, kbps, rb, nt);
 }
 
-// 16 accumulator columns summed over the chains, chain 0 first (fixed order).
-__device__ __forceinline__ void rows_ld_chains(uint32_t taddr, int nt, int chains, float (&v)[16]) {
-  tmem_ld16(taddr, v);
-  for (int c = 1; c < chains; ++c) {
-    float w[16];
-    tmem_ld16(taddr + (uint32_t)(c * nt), w);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] += w[i];
-  }
+// Shared-memory staging for the epilogue's sum over packed groups:
+// [groups][RB][NT + 4] floats (the +4 spreads rows over banks).
+__host__ __device__ inline size_t rows_stage_floats(int groups, int rb, int nt) {
+  return (size_t)groups * rb * (nt + 4);
 }
 
 __global__ void __launch_bounds__(kRowsThreads, 1)
@@ -181,7 +186,7 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(kTcTileRows, p.NT);
+      const uint32_t idesc = idesc_bf16_f32(kTcTileRows, p.groups * p.NT);
       // Descriptors differ only in their start-address field (address >> 4):
       // build the ring bases once and add offsets.
       const uint64_t wdesc0 = smem_desc_sw128(w_ring);
@@ -196,14 +201,12 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
         tc_fence_after();
         const uint64_t wd = wdesc0 + ((uint64_t)(slot * w_stage) >> 4);
         const uint64_t ad = adesc0 + ((uint64_t)(slot * a_stage) >> 4);
-        for (int j = 0; j < p.kbps; ++j) {
+        for (int j = 0; j < p.kbps; j += p.groups) {
 #pragma unroll
           for (int kk = 0; kk < kTcKBlock / 16; ++kk) {
-            // K step kk goes to accumulator chain kk % chains.
-            const int chain = kk & (p.chains - 1);
-            const bool first = (s == 0) && (j == 0) && (kk < p.chains);
-            mma_bf16(tmem + (uint32_t)(chain * p.NT), wd + ((j * wblk + kk * 32u) >> 4),
-                     ad + ((j * ablk + kk * 32u) >> 4), idesc, first ? 0u : 1u);
+            const bool first = (s == 0) && (j == 0) && (kk == 0);
+            mma_bf16(tmem, wd + ((j * wblk + kk * 32u) >> 4), ad + ((j * ablk + kk * 32u) >> 4), idesc,
+                     first ? 0u : 1u);
           }
         }
         mma_commit(smem_u32(&empty[slot]));
@@ -219,52 +222,76 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;
-    const int row = q * 32 + lane;
-    if (q * 32 < p.RB) {  // warp-uniform: this quarter holds loaded rows
-      pdl_wait();
-      const int n = n0 + row;
-      const bool live = row < p.RB && n < p.N;
-      float r[kRowsPrefetchTokens];
+    pdl_wait();  // R may come from the preceding kernel; Y may be read by it
+    const int q = warp & 3;       // TMEM lane quarter this warp may access
+    const int etid = threadIdx.x - 64;
+    const int L = q * 32 + lane;  // TMEM lane = row of the MMA window
+    const int g = L / p.RB, r = L % p.RB;
+    const int G = p.groups;
+    const int chunks = p.NT / 16;  // 16-column groups per token tile
+    const int ldp = p.NT + 4;      // staging row stride (floats)
+    float* part = reinterpret_cast<float*>(sb + 1024);  // reuses the drained ring
+    // Residuals for the combine step (one row per thread when NT == 16).
+    float rpre[kRowsPrefetchTokens];
+    const bool pre = (p.NT == kRowsPrefetchTokens) && etid < p.RB && n0 + etid < p.N;
 #pragma unroll
-      for (int i = 0; i < kRowsPrefetchTokens; ++i)
-        r[i] = (live && i < p.M) ? __bfloat162float(p.R[(size_t)i * p.ldr + n]) : 0.f;
-      bool ok = mbar_wait_or_abort(smem_u32(acc_full), 0, abort_flag);
-      if (!ok) {
-        if (!*abort_flag) report_error(p.err, kErrWaitMma);
-        *abort_flag = 1;
+    for (int i = 0; i < kRowsPrefetchTokens; ++i)
+      rpre[i] = (pre && i < p.M) ? __bfloat162float(p.R[(size_t)i * p.ldr + n0 + etid]) : 0.f;
+    bool ok = mbar_wait_or_abort(smem_u32(acc_full), 0, abort_flag);
+    if (!ok) {
+      if (!*abort_flag) report_error(p.err, kErrWaitMma);
+      *abort_flag = 1;
+    }
+    ok = __all_sync(0xffffffffu, ok);
+    tc_fence_after();
+    // Step 1: each lane copies its diagonal block row (group g, row r) to shared memory.
+    if (ok) {
+      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16);
+      for (int c = 0; c < G * chunks; ++c) {
+        float v[16];
+        tmem_ld16(taddr + (uint32_t)(c * 16), v);  // warp-collective: every lane loads
+        if (g < G && c / chunks == g) {
+          float* dst = part + ((size_t)g * p.RB + r) * ldp + (c % chunks) * 16;
+#pragma unroll
+          for (int i = 0; i < 16; i += 4)
+            *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+        }
       }
-      ok = __all_sync(0xffffffffu, ok);
-      tc_fence_after();
-      if (ok) {
-        const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16);
-        // Tokens [0, 32): residuals already in registers (static indices).
+    }
+    named_bar_sync(1, 128);
+    // Step 2: sum the groups (g order), add the residual, round once, store.
+    if (ok) {
+      for (int item = etid; item < p.RB * chunks; item += 128) {
+        const int rr = item % p.RB, c16 = item / p.RB;
+        const int n = n0 + rr;
+        if (n >= p.N) continue;
+        float acc[16];
 #pragma unroll
-        for (int half = 0; half < kRowsPrefetchTokens / 16; ++half) {
-          const int col0 = half * 16;
-          if (col0 < p.NT) {
-            float v[16];
-            rows_ld_chains(taddr + (uint32_t)col0, p.NT, p.chains, v);
-            if (live) {
+        for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+        for (int gg = 0; gg < G; ++gg) {
+          const float* src = part + ((size_t)gg * p.RB + rr) * ldp + c16 * 16;
 #pragma unroll
-              for (int i = 0; i < 16; ++i)
-                if (col0 + i < p.M)
-                  p.Y[(size_t)(col0 + i) * p.ldy + n] = __float2bfloat16_rn(v[i] + r[col0 + i]);
-            }
+          for (int i = 0; i < 16; i += 4) {
+            const float4 w = *reinterpret_cast<const float4*>(src + i);
+            acc[i] += w.x;
+            acc[i + 1] += w.y;
+            acc[i + 2] += w.z;
+            acc[i + 3] += w.w;
           }
         }
-        // Tokens [32, NT): residuals loaded per group of 16.
-        for (int col0 = kRowsPrefetchTokens; col0 < p.NT; col0 += 16) {
-          float v[16], rr[16];
+        const int m0 = c16 * 16;
+        if (pre) {
 #pragma unroll
           for (int i = 0; i < 16; ++i)
-            rr[i] = (live && col0 + i < p.M) ? __bfloat162float(p.R[(size_t)(col0 + i) * p.ldr + n]) : 0.f;
-          rows_ld_chains(taddr + (uint32_t)col0, p.NT, p.chains, v);
-          if (live) {
+            if (m0 + i < p.M) p.Y[(size_t)(m0 + i) * p.ldy + n] = __float2bfloat16_rn(acc[i] + rpre[i]);
+        } else {
+          float rr16[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              if (col0 + i < p.M) p.Y[(size_t)(col0 + i) * p.ldy + n] = __float2bfloat16_rn(v[i] + rr[i]);
-          }
+          for (int i = 0; i < 16; ++i)
+            rr16[i] = (m0 + i < p.M) ? __bfloat162float(p.R[(size_t)(m0 + i) * p.ldr + n]) : 0.f;
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            if (m0 + i < p.M) p.Y[(size_t)(m0 + i) * p.ldy + n] = __float2bfloat16_rn(acc[i] + rr16[i]);
         }
       }
     }
@@ -332,8 +359,21 @@ inline int rows_plan(const sgr_config& c, int sms, int M, int N, int K, RowsPara
   p->k_stages = (K + kstage_elems - 1) / kstage_elems;
   p->kbps = c.k_blocks_per_stage;
   p->stages = c.stages;
-  p->chains = nt <= 128 ? 4 : 2;  // chains * NT <= 512 TMEM columns
-  p->tmem_cols = detail::pow2_at_least(p->chains * nt);
+  // Diagonal packing: as many consecutive K blocks per MMA as fit in the
+  // 128-row window and the 256-column N limit, dividing the stage's blocks,
+  // with room to stage the epilogue's partial sums in the drained ring.
+  p->groups = 1;
+  for (int gcount = 4; gcount >= 2; gcount /= 2)
+    if (gcount * rb <= kTcTileRows && gcount * nt <= 256 && c.k_blocks_per_stage % gcount == 0) {
+      p->groups = gcount;
+      break;
+    }
+  while (p->groups > 1 &&
+         rows_stage_floats(p->groups, rb, nt) * 4 > (size_t)c.stages * rows_stage_bytes(c.k_blocks_per_stage, rb, nt))
+    p->groups /= 2;
+  if (rows_stage_floats(p->groups, rb, nt) * 4 > (size_t)c.stages * rows_stage_bytes(c.k_blocks_per_stage, rb, nt))
+    return SGR_ERR_UNSUPPORTED;
+  p->tmem_cols = detail::pow2_at_least(p->groups * nt);
   *grid = (N + rb - 1) / rb;
   *smem = sm;
   return SGR_OK;
