@@ -23,7 +23,8 @@
 //  * Rows are reduced in batches of 32/MT rows so that each lane holds 32
 //    partial sums; one transposing butterfly (31 shuffles) leaves lane l
 //    with the warp's total for output l, the 7 warps' totals meet in shared
-//    memory, and warp 0 adds R, rounds once and stores.
+//    memory, and warp 0 adds R (loaded early, while W streams), rounds once
+//    and stores.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -35,6 +36,7 @@ namespace sgr {
 constexpr int kSimtConsumerWarps = 7;
 constexpr int kSimtConsumers = kSimtConsumerWarps * 32;  // 224 threads
 constexpr int kSimtThreads = kSimtConsumers + 32;        // + one producer warp
+constexpr int kSimtRPrefetch = 4;  // reduction batches whose residuals are loaded early
 
 struct SimtParams {
   const __nv_bfloat16* A;  // [M, K], row stride lda (elements)
@@ -82,7 +84,7 @@ __device__ __forceinline__ float transpose_reduce32(float (&x)[32], int lane) {
 // MT: rows of A handled (M <= MT, rows >= M masked); VPT: 16-byte K vectors
 // per consumer thread (K <= 224 * 8 * VPT).
 template <int MT, int VPT>
-__global__ void __launch_bounds__(kSimtThreads, (MT <= 4 ? 2 : 1))
+__global__ void __launch_bounds__(kSimtThreads, (MT <= 2 ? 3 : (MT <= 4 ? 2 : 1)))
     simt_skinny_kernel(const SimtParams p) {
   constexpr int B = 32 / MT;                    // rows per reduction batch
   constexpr bool kPackedA = MT * VPT * 8 > 64;  // keep A as bf16x2 when large
@@ -174,14 +176,27 @@ __global__ void __launch_bounds__(kSimtThreads, (MT <= 4 ? 2 : 1))
     }
   }
 
+  // Residuals of the first batches, loaded now so the epilogue does not wait
+  // on memory (warp 0 stores; lane l handles output l of each batch).
+  constexpr int kB = 32 / MT;
+  float rpre[kSimtRPrefetch];
+#pragma unroll
+  for (int b = 0; b < kSimtRPrefetch; ++b) {
+    const int j = lane / MT, m = lane % MT, row = b * kB + j;
+    rpre[b] = (warp == 0 && row < nrows && m < p.M)
+                  ? __bfloat162float(p.R[(size_t)m * p.ldr + n0 + row])
+                  : 0.f;
+  }
+
   bool ok = true;
   int buf = 0;
+  int bi = 0;  // reduction batch index
   int slot = 0, rr = 0;   // ring slot of the current stage, row within the stage
   uint32_t phase = 0;     // parity of the current stage's fill of that slot
   const uint32_t ring_base = smem_u32(ring);
   const uint32_t row_bytes = (uint32_t)p.K * 2u;
   uint32_t row_addr = ring_base;
-  for (int base = 0; base < nrows; base += B) {
+  for (int base = 0; base < nrows; base += B, ++bi) {
     float acc[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) acc[i] = 0.f;
@@ -249,7 +264,11 @@ __global__ void __launch_bounds__(kSimtThreads, (MT <= 4 ? 2 : 1))
       const int j = lane / MT, m = lane % MT;
       if (base + j < nrows && m < p.M) {
         const int n = n0 + base + j;
-        const float r = __bfloat162float(p.R[(size_t)m * p.ldr + n]);
+        float r = 0.f;
+#pragma unroll
+        for (int k = 0; k < kSimtRPrefetch; ++k)
+          if (k == bi) r = rpre[k];
+        if (bi >= kSimtRPrefetch) r = __bfloat162float(p.R[(size_t)m * p.ldr + n]);
         p.Y[(size_t)m * p.ldy + n] = __float2bfloat16_rn(total + r);
       }
     }

@@ -29,11 +29,11 @@ def candidate_configs(path: int, M: int, K: int, grid: str) -> list[dict]:
     if path == sgr.SGR_PATH_SIMT:
         if M > 16:
             return []
-        for cps in (1, 2):
+        for cps in (1, 2, 3):
             for rps in (1, 2, 4):
                 for st in (2, 3, 4, 6, 8, 12, 16):
                     smem = 2048 + st * rps * K * 2
-                    if smem * cps > 228 * 1024 or smem > 232448:
+                    if smem * cps > 227 * 1024 or smem > 232448 or (cps == 3 and M > 2):
                         continue
                     if grid == "small" and st not in (4, 8, 12):
                         continue
