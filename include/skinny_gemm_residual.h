@@ -70,7 +70,7 @@
 extern "C" {
 #endif
 
-#define SGR_ABI_VERSION 1
+#define SGR_ABI_VERSION 2
 
 typedef enum {
   SGR_OK = 0,
@@ -124,7 +124,8 @@ typedef struct {
   int rows_per_stage;     /* SIMT: W rows per ring stage */
   int k_blocks_per_stage; /* TC, TC_ROWS: 64-wide K blocks per ring stage */
   int token_tile;         /* TC, TC_ROWS: activation rows per MMA (multiple of 16, <= 256) */
-  int reserved[2];        /* must be zero */
+  int prefetch_stages;    /* TC_ROWS: weight stages requested before the dependency wait */
+  int reserved[1];        /* must be zero */
 } sgr_config;
 
 /*

@@ -229,6 +229,7 @@ int resolve_config(int dev_sms, int M, int N, int K, const sgr_config* in, sgr_c
       out->stages = e->stages;
       if (path == SGR_PATH_SIMT) out->rows_per_stage = e->rows_per_stage;
       else out->k_blocks_per_stage = e->k_blocks_per_stage;
+      if (path == SGR_PATH_TC_ROWS) out->prefetch_stages = e->prefetch_stages;
     }
   }
   if (in) {
@@ -239,6 +240,7 @@ int resolve_config(int dev_sms, int M, int N, int K, const sgr_config* in, sgr_c
     if (in->stages) out->stages = in->stages;
     if (in->k_blocks_per_stage) out->k_blocks_per_stage = in->k_blocks_per_stage;
     if (in->token_tile) out->token_tile = in->token_tile;
+    if (in->prefetch_stages) out->prefetch_stages = in->prefetch_stages;
   }
   if (out->ctas_per_sm < 1 || out->ctas_per_sm > 8 || out->stages < 1 || out->stages > 64)
     return SGR_ERR_UNSUPPORTED;

@@ -62,6 +62,7 @@ struct RowsParams {
   int kbps;      // 64-wide K blocks per stage
   int stages;    // ring depth
   int groups;    // K blocks packed into one MMA along its diagonal (1, 2 or 4)
+  int prefetch;  // W stages requested before griddepcontrol.wait (1..stages)
   int tmem_cols;
 };
 
@@ -144,7 +145,10 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_a = policy_evict_last();
-      const int pre = KS < S ? KS : S;
+      // W for the first `prefetch` stages before the dependency wait.  A
+      // slot left free lets weights keep streaming while A (needed by the
+      // first MMA) is fetched after the wait.
+      const int pre = KS < p.prefetch ? KS : p.prefetch;
       for (int s = 0; s < pre; ++s) {
         const uint32_t fb = smem_u32(&full[s]);
         mbar_arrive_expect_tx(fb, stage_bytes);
@@ -162,7 +166,7 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
       int issued = pre;
       for (int s = pre; s < KS; ++s) {
         const int slot = s % S;
-        if (!mbar_wait_or_abort(smem_u32(&empty[slot]), ((s / S) - 1) & 1, abort_flag)) {
+        if (s >= S && !mbar_wait_or_abort(smem_u32(&empty[slot]), ((s / S) - 1) & 1, abort_flag)) {
           if (!*abort_flag) report_error(p.err, kErrWaitEmpty);
           *abort_flag = 1;
           break;
@@ -359,6 +363,8 @@ inline int rows_plan(const sgr_config& c, int sms, int M, int N, int K, RowsPara
   p->k_stages = (K + kstage_elems - 1) / kstage_elems;
   p->kbps = c.k_blocks_per_stage;
   p->stages = c.stages;
+  p->prefetch = c.prefetch_stages > 0 ? c.prefetch_stages : (c.stages > 2 ? c.stages - 1 : c.stages);
+  if (p->prefetch > c.stages) return SGR_ERR_UNSUPPORTED;
   // Diagonal packing: as many consecutive K blocks per MMA as fit in the
   // 128-row window and the 256-column N limit, dividing the stage's blocks,
   // with room to stage the epilogue's partial sums in the drained ring.

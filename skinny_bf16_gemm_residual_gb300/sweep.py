@@ -51,7 +51,9 @@ def candidate_configs(path: int, M: int, K: int, grid: str) -> list[dict]:
                     continue
                 if grid == "small" and st not in (3, 4, 6):
                     continue
-                out.append(dict(path=path, ctas_per_sm=1, k_blocks_per_stage=kb, stages=st))
+                for pf in sorted({st, max(1, st - 1), max(1, st - 2)}):
+                    out.append(dict(path=path, ctas_per_sm=1, k_blocks_per_stage=kb, stages=st,
+                                    prefetch_stages=pf))
     else:
         tiles = (M + 255) // 256
         nt = ((M + tiles - 1) // tiles + 15) // 16 * 16  # the library's token tile
