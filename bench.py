@@ -64,12 +64,25 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_digest() -> str:
+# Source files each kernel is compiled from: a committed DRAM-traffic figure
+# stays valid while these files are unchanged.
+KERNEL_SOURCES = {
+    "simt_skinny_kernel": ("sgr_simt.cuh", "sgr_ptx.cuh"),
+    "rows_skinny_kernel": ("sgr_rows.cuh", "sgr_tc.cuh", "sgr_ptx.cuh"),
+    "tc_skinny_kernel": ("sgr_tc.cuh", "sgr_ptx.cuh"),
+    "tile_gemm_kernel": ("sgr_gemm.cuh", "sgr_tc.cuh", "sgr_ptx.cuh"),
+}
+
+
+def kernel_source_digest(kernel: str) -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "skinny_bf16_gemm_residual_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + b"\0" + f.read())
+    for name in sorted(KERNEL_SOURCES.get(kernel, ())):
+        try:
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+        except OSError:
+            h.update(name.encode() + b"\0missing")
     return h.hexdigest()[:16]
 
 
@@ -86,7 +99,7 @@ def committed_traffic(kernel: str):
         if ":" in line and line.strip().startswith("- "):
             k, v = line.strip()[2:].split(":", 1)
             vals[k.strip()] = v.strip().strip("`")
-    if vals.get("source_digest") != kernel_source_digest():
+    if vals.get("source_digest") != kernel_source_digest(kernel):
         return None
     try:
         return float(vals["dram_bytes_per_launch"])
