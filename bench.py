@@ -40,7 +40,7 @@ METRIC = "µs/call and achieved HBM GB/s, BF16 skinny GEMM+residual, M=1..16, N7
 N_DIM, K_DIM = 7168, 3584
 M_LIST = (1, 2, 4, 8, 16)
 COPIES = 4
-PATH_NAMES = {1: "simt", 2: "tc", 3: "rows"}
+PATH_NAMES = {1: "simt", 2: "tc", 3: "rows", 4: "tile"}
 KERNEL_NAMES = {"simt": "simt_skinny_kernel", "tc": "tc_skinny_kernel", "rows": "rows_skinny_kernel"}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 

@@ -70,7 +70,7 @@
 extern "C" {
 #endif
 
-#define SGR_ABI_VERSION 2
+#define SGR_ABI_VERSION 3
 
 typedef enum {
   SGR_OK = 0,
@@ -91,6 +91,7 @@ typedef enum {
 #define SGR_PATH_SIMT 1 /* CUDA-core streaming kernel, M <= 16 */
 #define SGR_PATH_TC 2      /* tcgen05 kernel, persistent stream-K with split-K fixup */
 #define SGR_PATH_TC_ROWS 3 /* tcgen05 kernel, one contiguous W row slab per CTA (M <= 256) */
+#define SGR_PATH_TILE 4    /* tcgen05 kernel, 128-token x tile_n output tiles (large M) */
 
 /*
  * Y = bf16(A . W^T + R) with contiguous operands (lda = K, ldr = ldy = N).
@@ -124,8 +125,9 @@ typedef struct {
   int rows_per_stage;     /* SIMT: W rows per ring stage */
   int k_blocks_per_stage; /* TC, TC_ROWS: 64-wide K blocks per ring stage */
   int token_tile;         /* TC, TC_ROWS: activation rows per MMA (multiple of 16, <= 256) */
-  int prefetch_stages;    /* TC_ROWS: weight stages requested before the dependency wait */
-  int reserved[1];        /* must be zero */
+  int prefetch_stages;    /* TC_ROWS, TILE: weight stages requested before the dependency wait */
+  int tile_n;             /* TILE: W rows per output tile (MMA N): 64, 128, 192 or 256 */
+  int reserved[2];        /* must be zero */
 } sgr_config;
 
 /*
@@ -147,7 +149,7 @@ int sgr_validate(const void* A, int64_t lda, const void* W, const void* R,
 
 /*
  * Kernel path the library chooses for this shape with SGR_PATH_AUTO
- * (SGR_PATH_SIMT, SGR_PATH_TC or SGR_PATH_TC_ROWS), or a negative sgr_status
+ * (SGR_PATH_SIMT, SGR_PATH_TC, SGR_PATH_TC_ROWS or SGR_PATH_TILE), or a negative sgr_status
  * if none can run it.  Host-only.
  */
 int sgr_select_path(int M, int N, int K);

@@ -23,6 +23,7 @@ from .binding import (  # noqa: F401
     SGR_PATH_SIMT,
     SGR_PATH_TC,
     SGR_PATH_TC_ROWS,
+    SGR_PATH_TILE,
     SgrError,
     load,
     make_config,

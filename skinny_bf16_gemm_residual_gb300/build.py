@@ -34,6 +34,7 @@ def _nvcc() -> str:
 
 def sources() -> list[str]:
     return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cuh"))
+                  + glob.glob(os.path.join(CSRC, "*.h"))
                   + glob.glob(os.path.join(INCLUDE, "*.h")))
 
 

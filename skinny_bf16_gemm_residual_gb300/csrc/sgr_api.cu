@@ -13,6 +13,7 @@
 #include "sgr_simt.cuh"
 #include "sgr_tc.cuh"
 #include "sgr_rows.cuh"
+#include "sgr_gemm.cuh"
 #include "sgr_table.h"
 
 namespace {
@@ -152,6 +153,7 @@ int init_device(int dev) {
           ok = SGR_ERR_DEVICE;
     if (ok == SGR_OK && sgr::tc_init_device(sms, &st.ws) != cudaSuccess) ok = SGR_ERR_DEVICE;
     if (ok == SGR_OK && sgr::rows_init_device() != cudaSuccess) ok = SGR_ERR_DEVICE;
+    if (ok == SGR_OK && sgr::tile_init_device() != cudaSuccess) ok = SGR_ERR_DEVICE;
     if (ok != SGR_OK) cudaGetLastError();
     st.sms = sms;
     st.err = static_cast<unsigned*>(errp);
@@ -173,15 +175,17 @@ const sgr::TableEntry* table_lookup(int M, int N, int K) {
 
 // Library choice for a shape: the measured per-M table where it covers the
 // shape; otherwise the SIMT kernel for M <= 2, the row-slab tensor-core
-// kernel up to 256 tokens, and the stream-K tensor-core kernel beyond.
+// kernel up to 64 tokens, and the tile GEMM beyond.
 int select_path(int M, int N, int K, int sms) {
   if (const sgr::TableEntry* e = table_lookup(M, N, K)) {
     if (e->path == SGR_PATH_SIMT && M <= 16 && simt_vpt(K) > 0) return SGR_PATH_SIMT;
     if (e->path == SGR_PATH_TC_ROWS && sgr::rows_supported(sms, M, N, K)) return SGR_PATH_TC_ROWS;
     if (e->path == SGR_PATH_TC && sgr::tc_supported(M, N, K)) return SGR_PATH_TC;
+    if (e->path == SGR_PATH_TILE && sgr::tile_supported(M, N, K)) return SGR_PATH_TILE;
   }
   if (M <= 2 && simt_vpt(K) > 0) return SGR_PATH_SIMT;
-  if (sgr::rows_supported(sms, M, N, K)) return SGR_PATH_TC_ROWS;
+  if (M <= 64 && sgr::rows_supported(sms, M, N, K)) return SGR_PATH_TC_ROWS;
+  if (sgr::tile_supported(M, N, K)) return SGR_PATH_TILE;
   if (sgr::tc_supported(M, N, K)) return SGR_PATH_TC;
   if (M <= 16 && simt_vpt(K) > 0) return SGR_PATH_SIMT;
   return -SGR_ERR_UNSUPPORTED;
@@ -219,6 +223,9 @@ int resolve_config(int dev_sms, int M, int N, int K, const sgr_config* in, sgr_c
   } else if (path == SGR_PATH_TC_ROWS) {
     if (!sgr::rows_supported(dev_sms, M, N, K)) return SGR_ERR_UNSUPPORTED;
     sgr::rows_default_config(dev_sms, M, N, K, out);
+  } else if (path == SGR_PATH_TILE) {
+    if (!sgr::tile_supported(M, N, K)) return SGR_ERR_UNSUPPORTED;
+    sgr::tile_default_config(dev_sms > 0 ? dev_sms : 1, M, N, K, out);
   } else {
     return SGR_ERR_UNSUPPORTED;
   }
@@ -228,8 +235,9 @@ int resolve_config(int dev_sms, int M, int N, int K, const sgr_config* in, sgr_c
       out->ctas_per_sm = e->ctas_per_sm;
       out->stages = e->stages;
       if (path == SGR_PATH_SIMT) out->rows_per_stage = e->rows_per_stage;
-      else out->k_blocks_per_stage = e->k_blocks_per_stage;
-      if (path == SGR_PATH_TC_ROWS) out->prefetch_stages = e->prefetch_stages;
+      else if (path != SGR_PATH_TILE) out->k_blocks_per_stage = e->k_blocks_per_stage;
+      if (path == SGR_PATH_TC_ROWS || path == SGR_PATH_TILE) out->prefetch_stages = e->prefetch_stages;
+      if (path == SGR_PATH_TILE && e->tile_n) out->tile_n = e->tile_n;
     }
   }
   if (in) {
@@ -241,6 +249,9 @@ int resolve_config(int dev_sms, int M, int N, int K, const sgr_config* in, sgr_c
     if (in->k_blocks_per_stage) out->k_blocks_per_stage = in->k_blocks_per_stage;
     if (in->token_tile) out->token_tile = in->token_tile;
     if (in->prefetch_stages) out->prefetch_stages = in->prefetch_stages;
+    if (in->tile_n) out->tile_n = in->tile_n;
+    // A tile width chosen without a ring depth gets the deepest ring that fits it.
+    if (path == SGR_PATH_TILE && in->tile_n && !in->stages) out->stages = sgr::tile_default_stages(out->tile_n);
   }
   if (out->ctas_per_sm < 1 || out->ctas_per_sm > 8 || out->stages < 1 || out->stages > 64)
     return SGR_ERR_UNSUPPORTED;
@@ -256,6 +267,13 @@ int resolve_config(int dev_sms, int M, int N, int K, const sgr_config* in, sgr_c
     int grid = 0;
     size_t smem = 0;
     int rc = sgr::rows_plan(*out, dev_sms > 0 ? dev_sms : 1, M, N, K, &rp, &grid, &smem);
+    if (rc != SGR_OK) return rc;
+  }
+  if (path == SGR_PATH_TILE) {
+    sgr::TileParams gp;
+    int grid = 0;
+    size_t smem = 0;
+    int rc = sgr::tile_plan(*out, dev_sms > 0 ? dev_sms : 1, M, N, K, &gp, &grid, &smem);
     if (rc != SGR_OK) return rc;
   }
   if (path == SGR_PATH_SIMT) {
@@ -331,6 +349,9 @@ int run(const void* A, long long lda, const void* W, const void* R, long long ld
     return launch_simt(c, st.sms, st.err, A, lda, W, R, ldr, Y, ldy, M, N, K, flags, stream);
   if (c.path == SGR_PATH_TC_ROWS)
     return sgr::rows_launch(c, st.sms, st.err, A, lda, W, R, ldr, Y, ldy, M, N, K,
+                            (flags & SGR_FLAG_NO_PDL) == 0, stream);
+  if (c.path == SGR_PATH_TILE)
+    return sgr::tile_launch(c, st.sms, st.err, A, lda, W, R, ldr, Y, ldy, M, N, K,
                             (flags & SGR_FLAG_NO_PDL) == 0, stream);
   return sgr::tc_launch(c, st.sms, st.err, &st.ws, A, lda, W, R, ldr, Y, ldy, M, N, K,
                         (flags & SGR_FLAG_NO_PDL) == 0, stream);
@@ -526,6 +547,13 @@ int sgr_kernel_resources(int device, int path, int M, int N, int K, int* regs, i
     if (sgr::rows_plan(c, sms, M, N, K, &rp, &grid, &smem) != SGR_OK) return SGR_ERR_UNSUPPORTED;
     *smem_bytes = (int)smem;
     *threads = sgr::kRowsThreads;
+  } else if (c.path == SGR_PATH_TILE) {
+    if (cudaFuncGetAttributes(&fa, sgr::tile_gemm_kernel) != cudaSuccess) {
+      cudaGetLastError();
+      return SGR_ERR_DEVICE;
+    }
+    *smem_bytes = (int)sgr::tile_smem_bytes(c.stages, c.tile_n);
+    *threads = sgr::kTileThreads;
   } else {
     int s = 0, t = 0;
     const void* fn = sgr::tc_kernel_for(M, N, K, &c, &s, &t);

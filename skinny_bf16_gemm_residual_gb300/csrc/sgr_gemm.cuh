@@ -1,0 +1,492 @@
+// sgr_gemm.cuh -- tensor-core tile GEMM for compute-bound token counts.
+//
+// Same operation as the other kernels: Y[m,n] = bf16_rn( sum_k A[m,k] W[n,k]
+// + R[m,n] ) with FP32 accumulation and one rounding (vLLM
+// "benchmark_k3_cutedsl_residual.py", module docstring and its correctness()
+// reference).  Above a few hundred tokens the arithmetic intensity (about M
+// FLOP per byte of W) passes the ridge point of tensor peak over HBM
+// bandwidth (the roofline reasoning in the bitsandbytes "QLORA-2" comparison
+// page, agents/kbit_gemm_context.md), so this kernel is organised around the
+// tensor core instead of the weight stream.
+//
+// Operand roles (not swapped): a tile of 128 activation rows (tokens) is the
+// MMA's M side and lives in TMEM lanes 0..127; a tile of NT rows of W (NT =
+// 64, 128, 192 or 256) is the MMA's N side (TMEM columns).  Output tiles are
+// 128 x NT and never split along K: no workspace, no fixup.  NT is chosen per
+// shape so that the tile count fills the SMs in whole waves (N = 7168 with
+// NT = 192 gives 38 column tiles: 152 tiles at M = 512, 304 at M = 1024 on
+// 152 SMs).
+//
+// Persistent grid of min(tiles, SMs) CTAs; CTA c takes tiles c, c + G, ...,
+// each tile index t split as (t mod m_tiles, t div m_tiles), so the CTAs
+// running at the same time share W column tiles and the whole of A in L2.
+//
+// Warp roles (192 threads): warp 0 lane 0 issues TMA loads of one 64-wide K
+// block of A (128 x 64) and of W (NT x 64) per ring stage; warp 1 owns 2 x NT
+// TMEM columns (two accumulators) and its lane 0 issues tcgen05.mma (4 per K
+// block) and commits stage releases and accumulator hand-offs to mbarriers;
+// warps 2-5 are the epilogue, one per 32-lane TMEM quarter: each warp loads
+// its 32 x NT residual block with TMA into its own shared-memory staging
+// (128-byte swizzle, 32 x 64 boxes), adds the accumulator, rounds once to
+// BF16 in place and stores the block with TMA.  The two accumulators let the
+// epilogue of one tile run under the MMAs of the next.  W (input-only by the
+// launch contract) is requested for the first ring stages before
+// griddepcontrol.wait; A, R and Y are touched only after it.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "sgr_ptx.cuh"
+#include "sgr_tc.cuh"
+#include "skinny_gemm_residual.h"
+
+namespace sgr {
+
+constexpr int kTileThreads = 192;
+constexpr int kTileM = 128;       // tokens per tile (MMA M, TMEM lanes)
+constexpr int kTileBoxCols = 64;  // residual/output TMA box width (128 bytes)
+constexpr int kTileEpiRows = 32;  // rows per epilogue warp (its TMEM lane quarter)
+constexpr int kTileMaxN = 256;    // largest MMA N for M = 128
+constexpr uint32_t kTileBoxBytes = kTileEpiRows * kTileBoxCols * 2;  // 4 KB
+
+struct TileParams {
+  unsigned* err;
+  int M, N, K;
+  int NT;        // W rows per tile = MMA N (64, 128, 192 or 256)
+  int m_tiles;   // ceil(M / 128)
+  int n_tiles;   // ceil(N / NT)
+  int k_blocks;  // ceil(K / 64)
+  int stages;    // ring depth (one K block of A and W per stage)
+  int prefetch;  // W stages requested before griddepcontrol.wait (0..stages)
+  int tmem_cols;
+};
+
+__host__ __device__ inline uint32_t tile_stage_bytes(int nt) {
+  return (uint32_t)kTileM * 128u + (uint32_t)nt * 128u;
+}
+
+// Epilogue staging: 4 warps x (NT / 64) boxes of 32 rows x 128 bytes.
+__host__ __device__ inline uint32_t tile_epi_bytes(int nt) {
+  return 4u * (uint32_t)(nt / kTileBoxCols) * kTileBoxBytes;
+}
+
+__host__ __device__ inline size_t tile_smem_bytes(int stages, int nt) {
+  return 1024 /* alignment slack */ + 1024 /* barriers */ + (size_t)stages * tile_stage_bytes(nt) +
+         tile_epi_bytes(nt);
+}
+
+// ------------------------------------------------------ TMA stores (bulk groups)
+// 2-D tensor copy shared -> global of one box at (x = inner, y = outer);
+// elements outside the tensor are not written.
+__device__ __forceinline__ void tma_store_2d(const void* tmap, int32_t x, int32_t y, uint32_t src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(tmap),
+               "r"(x), "r"(y), "r"(src)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// The shared-memory sources of every committed bulk group have been read.
+__device__ __forceinline__ void bulk_wait_group_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Every committed bulk group has completed (global writes performed).
+__device__ __forceinline__ void bulk_wait_group0() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+
+// Two 16-column TMEM loads (32x32b.x16) followed by one wait; the wait names
+// every destination register so that no use can be scheduled before it.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
+        "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+        "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr + 16u)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                 "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+                 "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]),
+                 "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]),
+                 "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+}
+
+// acc (FP32 bits) + two BF16 residuals packed in `res`, rounded once to BF16x2.
+__device__ __forceinline__ uint32_t add_round_bf16x2(uint32_t acc_lo, uint32_t acc_hi, uint32_t res) {
+  const __nv_bfloat162 y =
+      __floats2bfloat162_rn(__uint_as_float(acc_lo) + bf16lo(res), __uint_as_float(acc_hi) + bf16hi(res));
+  return *reinterpret_cast<const uint32_t*>(&y);
+}
+
+__global__ void __launch_bounds__(kTileThreads, 1)
+    tile_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
+                     const __grid_constant__ CUtensorMap tmR, const __grid_constant__ CUtensorMap tmY,
+                     const TileParams p) {
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  unsigned char* sb = smem_raw + (base - raw);
+  const int S = p.stages;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sb);  // [S]  TMA -> MMA
+  uint64_t* empty = full + S;                         // [S]  MMA -> TMA
+  uint64_t* acc_full = empty + S;                     // [2]  MMA -> epilogue
+  uint64_t* acc_empty = acc_full + 2;                 // [2]  epilogue (4 warps) -> MMA
+  uint64_t* rfull = acc_empty + 2;                    // [4]  residual block landed (per epilogue warp)
+  uint64_t* drain = rfull + 4;                        // [1]  MMA completion at exit
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t a_bytes = (uint32_t)kTileM * 128u;
+  const uint32_t stage_bytes = tile_stage_bytes(p.NT);
+  const uint32_t ring = base + 1024;  // [S] x {A box 128 x 64, W box NT x 64}
+  const uint32_t epi = ring + (uint32_t)S * stage_bytes;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = gridDim.x;
+  const int tiles = p.m_tiles * p.n_tiles;
+  const int my_tiles = (tiles - (int)blockIdx.x + G - 1) / G;  // >= 1: grid <= tiles
+  const int KB = p.k_blocks;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&acc_full[b]), 1);
+      mbar_init(smem_u32(&acc_empty[b]), 4);
+    }
+    for (int q = 0; q < 4; ++q) mbar_init(smem_u32(&rfull[q]), 1);
+    mbar_init(smem_u32(drain), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncwarp();
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), (uint32_t)p.tmem_cols);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmW);
+    prefetch_tmap(&tmR);
+    prefetch_tmap(&tmY);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_launch_dependents();  // the dependent grid still waits for our completion before reading
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_normal();  // re-read by the CTAs of the other token tiles
+      const uint64_t pol_a = policy_evict_last();    // re-read for every W column tile
+      const int total = my_tiles * KB;               // stages this CTA loads
+      // Stage `it` holds K block it % KB of local tile it / KB.
+      auto coords = [&](int it, int* kx, int* m0, int* n0) {
+        const int t = (int)blockIdx.x + (it / KB) * G;
+        *kx = (it % KB) * kTcKBlock;
+        *m0 = (t % p.m_tiles) * kTileM;
+        *n0 = (t / p.m_tiles) * p.NT;
+      };
+      const int pre = total < p.prefetch ? total : p.prefetch;
+      for (int it = 0; it < pre; ++it) {
+        int kx, m0, n0;
+        coords(it, &kx, &m0, &n0);
+        const uint32_t fb = smem_u32(&full[it]);
+        mbar_arrive_expect_tx(fb, stage_bytes);
+        tma_load_2d(ring + (uint32_t)it * stage_bytes + a_bytes, &tmW, kx, n0, fb, pol_w);
+      }
+      pdl_wait();
+      for (int it = 0; it < pre; ++it) {
+        int kx, m0, n0;
+        coords(it, &kx, &m0, &n0);
+        tma_load_2d(ring + (uint32_t)it * stage_bytes, &tmA, kx, m0, smem_u32(&full[it]), pol_a);
+      }
+      int issued = pre;
+      for (int it = pre; it < total; ++it) {
+        const int slot = it % S;
+        if (it >= S && !mbar_wait_or_abort(smem_u32(&empty[slot]), ((it / S) - 1) & 1, abort_flag)) {
+          if (!*abort_flag) report_error(p.err, kErrWaitEmpty);
+          *abort_flag = 1;
+          break;
+        }
+        int kx, m0, n0;
+        coords(it, &kx, &m0, &n0);
+        const uint32_t fb = smem_u32(&full[slot]);
+        const uint32_t st = ring + (uint32_t)slot * stage_bytes;
+        mbar_arrive_expect_tx(fb, stage_bytes);
+        tma_load_2d(st, &tmA, kx, m0, fb, pol_a);
+        tma_load_2d(st + a_bytes, &tmW, kx, n0, fb, pol_w);
+        issued = it + 1;
+      }
+      // Drain: every issued copy has landed before the CTA may exit.
+      for (int t = issued > S ? issued - S : 0; t < issued; ++t)
+        if (!mbar_wait(smem_u32(&full[t % S]), (t / S) & 1)) {
+          report_error(p.err, kErrDrain);
+          break;
+        }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(kTileM, p.NT);
+      const uint64_t adesc0 = smem_desc_sw128(ring);
+      const uint64_t wdesc0 = smem_desc_sw128(ring + a_bytes);
+      bool ok = true;
+      int it = 0;
+      for (int i = 0; i < my_tiles && ok; ++i) {
+        const int buf = i & 1;
+        if (i >= 2 && !mbar_wait_or_abort(smem_u32(&acc_empty[buf]), ((i >> 1) - 1) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(buf * p.NT);
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const int slot = it % S;
+          if (!mbar_wait_or_abort(smem_u32(&full[slot]), (it / S) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t off = (uint64_t)(slot * stage_bytes) >> 4;
+#pragma unroll
+          for (int kk = 0; kk < kTcKBlock / 16; ++kk)
+            mma_bf16(d, adesc0 + off + (uint64_t)(kk * 2), wdesc0 + off + (uint64_t)(kk * 2), idesc,
+                     (kb | kk) != 0 ? 1u : 0u);
+          mma_commit(smem_u32(&empty[slot]));
+        }
+        if (ok) mma_commit(smem_u32(&acc_full[buf]));
+      }
+      if (!ok) {
+        if (!*abort_flag) report_error(p.err, kErrWaitMma);
+        *abort_flag = 1;
+      }
+      mma_commit(smem_u32(drain));
+      if (!mbar_wait(smem_u32(drain), 0)) report_error(p.err, kErrDrain);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    pdl_wait();  // R may come from the preceding kernel; Y may be read by it
+    const int q = warp & 3;  // TMEM lane quarter = tile rows [32 q, 32 q + 32)
+    const int nbox = p.NT / kTileBoxCols;
+    const uint32_t stg = epi + (uint32_t)q * (uint32_t)nbox * kTileBoxBytes;
+    const uint32_t rbar = smem_u32(&rfull[q]);
+    const uint64_t pol_r = policy_evict_first();
+    const uint32_t sw = (uint32_t)(lane & 7);  // 128-byte swizzle phase of this row
+    auto issue_r = [&](int i) {                // residual block of local tile i -> staging
+      const int t = (int)blockIdx.x + i * G;
+      const int m0 = (t % p.m_tiles) * kTileM + q * kTileEpiRows;
+      const int n0 = (t / p.m_tiles) * p.NT;
+      mbar_arrive_expect_tx(rbar, (uint32_t)nbox * kTileBoxBytes);
+      for (int b = 0; b < nbox; ++b)
+        tma_load_2d(stg + (uint32_t)b * kTileBoxBytes, &tmR, n0 + b * kTileBoxCols, m0, rbar, pol_r);
+    };
+    if (lane == 0) issue_r(0);
+    int pending = 0;  // local tile whose residual load is in flight, or -1
+    for (int i = 0; i < my_tiles; ++i) {
+      const int buf = i & 1;
+      bool ok = mbar_wait_or_abort(smem_u32(&acc_full[buf]), (i >> 1) & 1, abort_flag) &&
+                mbar_wait_or_abort(rbar, i & 1, abort_flag);
+      if (!ok) {
+        if (!*abort_flag) report_error(p.err, kErrWaitMma);
+        *abort_flag = 1;
+      }
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      pending = -1;
+      tc_fence_after();
+      const int t = (int)blockIdx.x + i * G;
+      const int m0 = (t % p.m_tiles) * kTileM + q * kTileEpiRows;
+      const int n0 = (t / p.m_tiles) * p.NT;
+      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * p.NT);
+      for (int c = 0; c < p.NT / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(taddr + (uint32_t)(c * 32), v);
+        // Columns [32 c, 32 c + 32) of this row: half (c & 1) of box c / 2,
+        // 16-byte chunks 4 (c & 1) .. 4 (c & 1) + 3 before swizzling.
+        const uint32_t row = stg + (uint32_t)(c >> 1) * kTileBoxBytes + (uint32_t)lane * 128u;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t addr = row + ((((uint32_t)((c & 1) * 4 + j)) ^ sw) << 4);
+          const uint4 r = lds128(addr);
+          const int e = j * 8;
+          sts128(addr, add_round_bf16x2(v[e + 0], v[e + 1], r.x), add_round_bf16x2(v[e + 2], v[e + 3], r.y),
+                 add_round_bf16x2(v[e + 4], v[e + 5], r.z), add_round_bf16x2(v[e + 6], v[e + 7], r.w));
+        }
+      }
+      // Accumulator buffer free for the MMAs of tile i + 2.
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&acc_empty[buf]));
+      // Make the staged outputs visible to the TMA engine, then store them.
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        for (int b = 0; b < nbox; ++b)
+          tma_store_2d(&tmY, n0 + b * kTileBoxCols, m0, stg + (uint32_t)b * kTileBoxBytes);
+        bulk_commit_group();
+        bulk_wait_group_read0();  // staging may be overwritten again
+        if (i + 1 < my_tiles) issue_r(i + 1);
+      }
+      if (i + 1 < my_tiles) pending = i + 1;
+      __syncwarp();
+    }
+    if (lane == 0) {
+      // A residual load that was issued but not consumed (only after an
+      // abort) lands before the CTA exits; every store completes.
+      if (pending >= 0 && !mbar_wait(rbar, pending & 1)) report_error(p.err, kErrDrain);
+      bulk_wait_group0();
+    }
+  }
+
+  __syncwarp();  // lane-0 roles rejoin their warp before the CTA-wide barrier
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, (uint32_t)p.tmem_cols);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+inline bool tile_supported(int M, int N, int K) {
+  return M >= 1 && N >= 8 && K >= 8 && N % 8 == 0 && K % 8 == 0;
+}
+
+// Tile width: the NT in {192, 256, 128, 64} with the least work per SM
+// (waves of tiles x NT); the first listed wins ties.
+inline int tile_default_nt(int sms, int M, int N) {
+  const long long mt = (M + kTileM - 1) / kTileM;
+  const int cand[4] = {192, 256, 128, 64};
+  int best = cand[0];
+  long long best_cost = -1;
+  for (int nt : cand) {
+    const long long tiles = mt * ((N + nt - 1) / nt);
+    const long long cost = ((tiles + sms - 1) / sms) * nt;
+    if (best_cost < 0 || cost < best_cost) {
+      best = nt;
+      best_cost = cost;
+    }
+  }
+  return best;
+}
+
+// Deepest ring (up to 8 stages) that fits beside the epilogue staging.
+inline int tile_default_stages(int nt) {
+  const long long room = 232448 - 2048 - (long long)tile_epi_bytes(nt);
+  long long s = room / tile_stage_bytes(nt);
+  return (int)(s > 8 ? 8 : (s < 2 ? 2 : s));
+}
+
+inline void tile_default_config(int sms, int M, int N, int K, sgr_config* c) {
+  (void)K;
+  c->path = SGR_PATH_TILE;
+  c->ctas_per_sm = 1;
+  c->tile_n = tile_default_nt(sms, M, N);
+  c->stages = tile_default_stages(c->tile_n);
+  c->prefetch_stages = 0;  // all stages
+  c->token_tile = kTileM;
+  c->k_blocks_per_stage = 1;
+  c->rows_per_stage = 0;
+}
+
+inline cudaError_t tile_init_device() {
+  return set_kernel_smem_attrs(reinterpret_cast<const void*>(tile_gemm_kernel));
+}
+
+// Checks a resolved configuration for this shape; fills the kernel params.
+inline int tile_plan(const sgr_config& c, int sms, int M, int N, int K, TileParams* p, int* grid,
+                     size_t* smem) {
+  if (!tile_supported(M, N, K)) return SGR_ERR_UNSUPPORTED;
+  const int nt = c.tile_n;
+  if (nt < kTileBoxCols || nt > kTileMaxN || nt % kTileBoxCols != 0) return SGR_ERR_UNSUPPORTED;
+  if (c.ctas_per_sm != 1) return SGR_ERR_UNSUPPORTED;
+  if (c.token_tile != 0 && c.token_tile != kTileM) return SGR_ERR_UNSUPPORTED;
+  if (c.k_blocks_per_stage != 0 && c.k_blocks_per_stage != 1) return SGR_ERR_UNSUPPORTED;
+  if (c.stages < 2 || c.stages > 32) return SGR_ERR_UNSUPPORTED;
+  if (c.prefetch_stages < 0 || c.prefetch_stages > c.stages) return SGR_ERR_UNSUPPORTED;  // 0: all
+  const size_t sm = tile_smem_bytes(c.stages, nt);
+  if (sm > 232448) return SGR_ERR_UNSUPPORTED;
+  const long long m_tiles = (M + kTileM - 1) / kTileM;
+  const long long n_tiles = (N + nt - 1) / nt;
+  if (m_tiles * n_tiles > (1ll << 30)) return SGR_ERR_UNSUPPORTED;
+  const long long tiles = m_tiles * n_tiles;
+  p->M = M;
+  p->N = N;
+  p->K = K;
+  p->NT = nt;
+  p->m_tiles = (int)m_tiles;
+  p->n_tiles = (int)n_tiles;
+  p->k_blocks = (K + kTcKBlock - 1) / kTcKBlock;
+  p->stages = c.stages;
+  p->prefetch = c.prefetch_stages > 0 ? c.prefetch_stages : c.stages;
+  p->tmem_cols = detail::pow2_at_least(2 * nt);
+  *grid = (int)(tiles < sms ? tiles : sms);
+  *smem = sm;
+  return SGR_OK;
+}
+
+inline int tile_launch(const sgr_config& c, int sms, unsigned* err, const void* A, long long lda,
+                       const void* W, const void* R, long long ldr, void* Y, long long ldy, int M,
+                       int N, int K, bool pdl, cudaStream_t stream) {
+  TileParams p;
+  int grid = 0;
+  size_t smem = 0;
+  int rc = tile_plan(c, sms, M, N, K, &p, &grid, &smem);
+  if (rc != SGR_OK) return rc;
+  CUtensorMap tmA, tmW, tmR, tmY;
+  if (!detail::make_tmap(&tmA, A, M, K, lda, kTileM, kTcKBlock)) return SGR_ERR_LAUNCH;
+  if (!detail::make_tmap(&tmW, W, N, K, K, p.NT, kTcKBlock)) return SGR_ERR_LAUNCH;
+  if (!detail::make_tmap(&tmR, R, M, N, ldr, kTileEpiRows, kTileBoxCols)) return SGR_ERR_LAUNCH;
+  if (!detail::make_tmap(&tmY, Y, M, N, ldy, kTileEpiRows, kTileBoxCols)) return SGR_ERR_LAUNCH;
+  p.err = err;
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3((unsigned)grid, 1, 1);
+  lc.blockDim = dim3(kTileThreads, 1, 1);
+  lc.dynamicSmemBytes = smem;
+  lc.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = pdl ? 1 : 0;
+  if (cudaLaunchKernelEx(&lc, tile_gemm_kernel, tmA, tmW, tmR, tmY, p) != cudaSuccess) {
+    cudaGetLastError();
+    return SGR_ERR_LAUNCH;
+  }
+  return SGR_OK;
+}
+
+}  // namespace sgr

@@ -54,6 +54,19 @@ def candidate_configs(path: int, M: int, K: int, grid: str) -> list[dict]:
                 for pf in sorted({st, max(1, st - 1), max(1, st - 2)}):
                     out.append(dict(path=path, ctas_per_sm=1, k_blocks_per_stage=kb, stages=st,
                                     prefetch_stages=pf))
+    elif path == sgr.SGR_PATH_TILE:
+        if M < 32:
+            return []
+        for nt in (64, 128, 192, 256):
+            stage = 128 * 128 + nt * 128
+            epi = 4 * (nt // 64) * 4096
+            for st in range(2, 9):
+                if 2048 + st * stage + epi > 232448:
+                    continue
+                if grid == "small" and st not in (3, 4, 6):
+                    continue
+                for pf in sorted({st, max(1, st - 1)}):
+                    out.append(dict(path=path, ctas_per_sm=1, tile_n=nt, stages=st, prefetch_stages=pf))
     else:
         tiles = (M + 255) // 256
         nt = ((M + tiles - 1) // tiles + 15) // 16 * 16  # the library's token tile
@@ -117,7 +130,7 @@ def main(argv=None):
     ap.add_argument("--m", type=int, nargs="+", default=[1, 2, 4, 8, 16])
     ap.add_argument("--n", type=int, default=inputs.N_LATENT_MOE)
     ap.add_argument("--k", type=int, default=inputs.K_LATENT_MOE)
-    ap.add_argument("--paths", default="simt,tc,rows")
+    ap.add_argument("--paths", default="simt,tc,rows,tile")
     ap.add_argument("--grid", choices=("small", "full"), default="full")
     ap.add_argument("--copies", type=int, default=4)
     ap.add_argument("--repeats", type=int, default=7)
@@ -135,7 +148,8 @@ def main(argv=None):
     meta = {"device": props.name, "sms": props.multi_processor_count,
             "l2_bytes": props.L2_cache_size, "torch": torch.__version__}
     out = open(args.output, "w") if args.output else None
-    paths = {"simt": sgr.SGR_PATH_SIMT, "tc": sgr.SGR_PATH_TC, "rows": sgr.SGR_PATH_TC_ROWS}
+    paths = {"simt": sgr.SGR_PATH_SIMT, "tc": sgr.SGR_PATH_TC, "rows": sgr.SGR_PATH_TC_ROWS,
+             "tile": sgr.SGR_PATH_TILE}
     for M in args.m:
         A = inputs.make_rows(M, K, seed=10_000 + M).to(dev)
         Rs = [inputs.make_rows(M, N, seed=20_000 + 100 * M + s).to(dev) for s in range(args.copies)]
