@@ -41,12 +41,23 @@ N_DIM, K_DIM = 7168, 3584
 M_LIST = (1, 2, 4, 8, 16)
 COPIES = 4
 PATH_NAMES = {1: "simt", 2: "tc", 3: "rows", 4: "tile"}
-KERNEL_NAMES = {"simt": "simt_skinny_kernel", "tc": "tc_skinny_kernel", "rows": "rows_skinny_kernel"}
+KERNEL_NAMES = {"simt": "simt_skinny_kernel", "tc": "tc_skinny_kernel", "rows": "rows_skinny_kernel",
+                "tile": "tile_gemm_kernel"}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
 def alg_bytes(M: int, N: int = N_DIM, K: int = K_DIM) -> int:
     return 2 * (N * K + M * K + 2 * M * N)
+
+
+def alg_flops(M: int, N: int = N_DIM, K: int = K_DIM) -> int:
+    return 2 * M * N * K
+
+
+def tensor_bound(M: int, peaks: dict) -> bool:
+    """True when the call's FLOPs at the BF16 tensor peak take longer than its
+    bytes at the HBM peak (the roofline's ridge point lies below M)."""
+    return alg_flops(M) / (peaks["bf16_tflops"] * 1e12) > alg_bytes(M) / (peaks["hbm_gbs"] * 1e9)
 
 
 def alg_flops(M: int, N: int = N_DIM, K: int = K_DIM) -> int:
@@ -390,9 +401,12 @@ def run_ours(args):
         samples = [t / COPIES for t in time_graph(g, stream, args.replays, args.repeats)]
         s = summarize(samples)
         gbs = alg_bytes(M) / (s["median_us"] * 1e-6) / 1e9
+        tflops = alg_flops(M) / (s["median_us"] * 1e-6) / 1e12
         per_m_out[str(M)] = {
             "us_per_call": s["median_us"], "p10_us": s["p10_us"], "p90_us": s["p90_us"],
             "cv_pct": s["cv_pct"], "gbs": gbs, "frac_of_hbm_peak": gbs / peaks["hbm_gbs"],
+            "tflops": tflops, "frac_of_tensor_peak": tflops / peaks["bf16_tflops"],
+            "bound": "tensor" if tensor_bound(M, peaks) else "hbm",
             "path": PATH_NAMES.get(sgr.sgr_select_path(M, N_DIM, K_DIM), "?"),
         }
         del g
@@ -445,14 +459,23 @@ def run_ours(args):
     dominant_path = max(share, key=share.get)
     dominant = KERNEL_NAMES.get(dominant_path, dominant_path)
     traffic = committed_traffic(dominant)
+    flops_per_step = sum(alg_flops(M) for M in m_list) * COPIES
+    if all(tensor_bound(M, peaks) for M in m_list):
+        t_ach = flops_per_step / launches_per_step / avg_launch_s / 1e12
+        roofline_bound = {"bound": "tensor", "achieved": t_ach, "peak": peaks["bf16_tflops"],
+                          "unit": "TFLOP/s", "frac": t_ach / peaks["bf16_tflops"]}
+    else:
+        roofline_bound = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                          "frac": achieved / peaks["hbm_gbs"]}
     roofline = {
-        "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-        "frac": achieved / peaks["hbm_gbs"], "traffic": traffic, "peak_source": peak_src,
+        **roofline_bound, "traffic": traffic, "peak_source": peak_src,
         "kernel": dominant,
         "kernels_in_step": {KERNEL_NAMES.get(k, k): round(v / sum(share.values()), 3) for k, v in share.items()},
         "bytes_per_launch": bytes_per_step / launches_per_step,
-        "note": "algorithmic bytes 2*(N*K + M*K + 2*M*N) per call averaged over the step's calls / "
-                "average launch duration over the timed region (CUDA events on the launch stream)",
+        "flops_per_launch": flops_per_step / launches_per_step,
+        "note": "algorithmic bytes 2*(N*K + M*K + 2*M*N) (or FLOPs 2*M*N*K when every M of the step "
+                "is past the ridge point) per call averaged over the step's calls / average launch "
+                "duration over the timed region (CUDA events on the launch stream)",
     }
     cpu = None
     if ws == 1 and not args.no_cpu_baseline:

@@ -548,7 +548,7 @@ int sgr_kernel_resources(int device, int path, int M, int N, int K, int* regs, i
     *smem_bytes = (int)smem;
     *threads = sgr::kRowsThreads;
   } else if (c.path == SGR_PATH_TILE) {
-    if (cudaFuncGetAttributes(&fa, sgr::tile_gemm_kernel) != cudaSuccess) {
+    if (cudaFuncGetAttributes(&fa, sgr::tile_kernel_for(c.tile_n)) != cudaSuccess) {
       cudaGetLastError();
       return SGR_ERR_DEVICE;
     }

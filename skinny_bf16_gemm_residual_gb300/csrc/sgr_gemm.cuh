@@ -25,13 +25,21 @@
 // block of A (128 x 64) and of W (NT x 64) per ring stage; warp 1 owns 2 x NT
 // TMEM columns (two accumulators) and its lane 0 issues tcgen05.mma (4 per K
 // block) and commits stage releases and accumulator hand-offs to mbarriers;
-// warps 2-5 are the epilogue, one per 32-lane TMEM quarter: each warp loads
-// its 32 x NT residual block with TMA into its own shared-memory staging
-// (128-byte swizzle, 32 x 64 boxes), adds the accumulator, rounds once to
-// BF16 in place and stores the block with TMA.  The two accumulators let the
-// epilogue of one tile run under the MMAs of the next.  W (input-only by the
-// launch contract) is requested for the first ring stages before
-// griddepcontrol.wait; A, R and Y are touched only after it.
+// warps 2-5 are the epilogue, one per 32-lane TMEM quarter, one output row
+// per thread: the thread loads its row's NT residuals into registers when
+// the tile starts (they arrive while the MMAs run), then adds the
+// accumulator, rounds once to BF16 and stores 16-byte vectors.  Keeping the
+// epilogue out of shared memory leaves all of it to the ring, whose depth is
+// what hides the operand latency (about 1 us from L2 under full load).  The
+// two accumulators let the epilogue of one tile run under the MMAs of the
+// next.  W (input-only by the launch contract) is requested for the first
+// ring stages before griddepcontrol.wait; A, R and Y are touched only after
+// it.
+//
+// The single producer and MMA threads keep their ring position, K offset
+// and tile coordinates by increments: an integer division on their
+// per-stage path costs more issue time than the tensor core needs for a K
+// block.
 #pragma once
 
 #include <cuda.h>
@@ -46,12 +54,14 @@ namespace sgr {
 
 constexpr int kTileThreads = 192;
 constexpr int kTileM = 128;       // tokens per tile (MMA M, TMEM lanes)
-constexpr int kTileBoxCols = 64;  // residual/output TMA box width (128 bytes)
 constexpr int kTileEpiRows = 32;  // rows per epilogue warp (its TMEM lane quarter)
 constexpr int kTileMaxN = 256;    // largest MMA N for M = 128
-constexpr uint32_t kTileBoxBytes = kTileEpiRows * kTileBoxCols * 2;  // 4 KB
+constexpr int kTileMaxStages = 16;
 
 struct TileParams {
+  const __nv_bfloat16* R;
+  __nv_bfloat16* Y;
+  long long ldr, ldy;
   unsigned* err;
   int M, N, K;
   int NT;        // W rows per tile = MMA N (64, 128, 192 or 256)
@@ -67,48 +77,14 @@ __host__ __device__ inline uint32_t tile_stage_bytes(int nt) {
   return (uint32_t)kTileM * 128u + (uint32_t)nt * 128u;
 }
 
-// Epilogue staging: 4 warps x (NT / 64) boxes of 32 rows x 128 bytes.
-__host__ __device__ inline uint32_t tile_epi_bytes(int nt) {
-  return 4u * (uint32_t)(nt / kTileBoxCols) * kTileBoxBytes;
-}
-
 __host__ __device__ inline size_t tile_smem_bytes(int stages, int nt) {
-  return 1024 /* alignment slack */ + 1024 /* barriers */ + (size_t)stages * tile_stage_bytes(nt) +
-         tile_epi_bytes(nt);
-}
-
-// ------------------------------------------------------ TMA stores (bulk groups)
-// 2-D tensor copy shared -> global of one box at (x = inner, y = outer);
-// elements outside the tensor are not written.
-__device__ __forceinline__ void tma_store_2d(const void* tmap, int32_t x, int32_t y, uint32_t src) {
-  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(tmap),
-               "r"(x), "r"(y), "r"(src)
-               : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit_group() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-
-// The shared-memory sources of every committed bulk group have been read.
-__device__ __forceinline__ void bulk_wait_group_read0() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-
-// Every committed bulk group has completed (global writes performed).
-__device__ __forceinline__ void bulk_wait_group0() {
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+  return 1024 /* alignment slack */ + 1024 /* barriers */ + (size_t)stages * tile_stage_bytes(nt);
 }
 
 __device__ __forceinline__ uint64_t policy_evict_normal() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
   return p;
-}
-
-__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
-               : "memory");
 }
 
 // Two 16-column TMEM loads (32x32b.x16) followed by one wait; the wait names
@@ -147,9 +123,21 @@ __device__ __forceinline__ uint32_t add_round_bf16x2(uint32_t acc_lo, uint32_t a
   return *reinterpret_cast<const uint32_t*>(&y);
 }
 
+// The residual row segment R[m, n0 .. n0 + NT) of one thread into registers
+// (zeros outside the matrix; N is a multiple of 8, so a 16-byte chunk is
+// either wholly inside or wholly outside).
+template <int NT>
+__device__ __forceinline__ void load_residual_row(const TileParams& p, int m, int n0, uint4 (&rv)[NT / 8]) {
+  const bool row_ok = m < p.M;
+  const __nv_bfloat16* src = p.R + (size_t)(row_ok ? m : 0) * p.ldr + n0;
+#pragma unroll
+  for (int j = 0; j < NT / 8; ++j)
+    rv[j] = (row_ok && n0 + 8 * j < p.N) ? *reinterpret_cast<const uint4*>(src + 8 * j) : make_uint4(0u, 0u, 0u, 0u);
+}
+
+template <int NT>
 __global__ void __launch_bounds__(kTileThreads, 1)
     tile_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
-                     const __grid_constant__ CUtensorMap tmR, const __grid_constant__ CUtensorMap tmY,
                      const TileParams p) {
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -160,14 +148,12 @@ __global__ void __launch_bounds__(kTileThreads, 1)
   uint64_t* empty = full + S;                         // [S]  MMA -> TMA
   uint64_t* acc_full = empty + S;                     // [2]  MMA -> epilogue
   uint64_t* acc_empty = acc_full + 2;                 // [2]  epilogue (4 warps) -> MMA
-  uint64_t* rfull = acc_empty + 2;                    // [4]  residual block landed (per epilogue warp)
-  uint64_t* drain = rfull + 4;                        // [1]  MMA completion at exit
+  uint64_t* drain = acc_empty + 2;                    // [1]  MMA completion at exit
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const uint32_t a_bytes = (uint32_t)kTileM * 128u;
-  const uint32_t stage_bytes = tile_stage_bytes(p.NT);
+  const uint32_t stage_bytes = tile_stage_bytes(NT);
   const uint32_t ring = base + 1024;  // [S] x {A box 128 x 64, W box NT x 64}
-  const uint32_t epi = ring + (uint32_t)S * stage_bytes;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x;
@@ -184,7 +170,6 @@ __global__ void __launch_bounds__(kTileThreads, 1)
       mbar_init(smem_u32(&acc_full[b]), 1);
       mbar_init(smem_u32(&acc_empty[b]), 4);
     }
-    for (int q = 0; q < 4; ++q) mbar_init(smem_u32(&rfull[q]), 1);
     mbar_init(smem_u32(drain), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -197,8 +182,6 @@ __global__ void __launch_bounds__(kTileThreads, 1)
   if (threadIdx.x == 0) {
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmW);
-    prefetch_tmap(&tmR);
-    prefetch_tmap(&tmY);
   }
   tc_fence_before();
   __syncthreads();
@@ -212,43 +195,66 @@ __global__ void __launch_bounds__(kTileThreads, 1)
       const uint64_t pol_w = policy_evict_normal();  // re-read by the CTAs of the other token tiles
       const uint64_t pol_a = policy_evict_last();    // re-read for every W column tile
       const int total = my_tiles * KB;               // stages this CTA loads
-      // Stage `it` holds K block it % KB of local tile it / KB.
-      auto coords = [&](int it, int* kx, int* m0, int* n0) {
-        const int t = (int)blockIdx.x + (it / KB) * G;
-        *kx = (it % KB) * kTcKBlock;
-        *m0 = (t % p.m_tiles) * kTileM;
-        *n0 = (t / p.m_tiles) * p.NT;
+      // Cursor over (local tile, K block) advanced by increments only: the
+      // producer's per-stage path holds no integer division, which on this
+      // single issuing thread costs more than the MMAs it feeds.
+      struct Cursor {
+        int kx, t, m0, n0, kb;
       };
-      const int pre = total < p.prefetch ? total : p.prefetch;
-      for (int it = 0; it < pre; ++it) {
-        int kx, m0, n0;
-        coords(it, &kx, &m0, &n0);
+      auto start = [&](Cursor& c) {
+        c.kx = 0;
+        c.kb = 0;
+        c.t = (int)blockIdx.x;
+        c.m0 = (c.t % p.m_tiles) * kTileM;
+        c.n0 = (c.t / p.m_tiles) * NT;
+      };
+      auto advance = [&](Cursor& c) {
+        c.kx += kTcKBlock;
+        if (++c.kb == KB) {
+          c.kb = 0;
+          c.kx = 0;
+          c.t += G;
+          c.m0 = (c.t % p.m_tiles) * kTileM;
+          c.n0 = (c.t / p.m_tiles) * NT;
+        }
+      };
+      const int pre = total < p.prefetch ? total : p.prefetch;  // <= S: slots 0 .. pre-1
+      Cursor c;
+      start(c);
+      for (int it = 0; it < pre; ++it, advance(c)) {
         const uint32_t fb = smem_u32(&full[it]);
         mbar_arrive_expect_tx(fb, stage_bytes);
-        tma_load_2d(ring + (uint32_t)it * stage_bytes + a_bytes, &tmW, kx, n0, fb, pol_w);
+        tma_load_2d(ring + (uint32_t)it * stage_bytes + a_bytes, &tmW, c.kx, c.n0, fb, pol_w);
       }
       pdl_wait();
-      for (int it = 0; it < pre; ++it) {
-        int kx, m0, n0;
-        coords(it, &kx, &m0, &n0);
-        tma_load_2d(ring + (uint32_t)it * stage_bytes, &tmA, kx, m0, smem_u32(&full[it]), pol_a);
+      {
+        Cursor ca;
+        start(ca);
+        for (int it = 0; it < pre; ++it, advance(ca))
+          tma_load_2d(ring + (uint32_t)it * stage_bytes, &tmA, ca.kx, ca.m0, smem_u32(&full[it]), pol_a);
       }
+      int slot = pre == S ? 0 : pre;
+      uint32_t par = pre == S ? 1u : 0u;  // ring round parity of `slot`
+      uint32_t soff = (uint32_t)slot * stage_bytes;
       int issued = pre;
-      for (int it = pre; it < total; ++it) {
-        const int slot = it % S;
-        if (it >= S && !mbar_wait_or_abort(smem_u32(&empty[slot]), ((it / S) - 1) & 1, abort_flag)) {
+      for (int it = pre; it < total; ++it, advance(c)) {
+        if (it >= S && !mbar_wait_or_abort(smem_u32(&empty[slot]), par ^ 1u, abort_flag)) {
           if (!*abort_flag) report_error(p.err, kErrWaitEmpty);
           *abort_flag = 1;
           break;
         }
-        int kx, m0, n0;
-        coords(it, &kx, &m0, &n0);
         const uint32_t fb = smem_u32(&full[slot]);
-        const uint32_t st = ring + (uint32_t)slot * stage_bytes;
+        const uint32_t st = ring + soff;
         mbar_arrive_expect_tx(fb, stage_bytes);
-        tma_load_2d(st, &tmA, kx, m0, fb, pol_a);
-        tma_load_2d(st + a_bytes, &tmW, kx, n0, fb, pol_w);
+        tma_load_2d(st, &tmA, c.kx, c.m0, fb, pol_a);
+        tma_load_2d(st + a_bytes, &tmW, c.kx, c.n0, fb, pol_w);
         issued = it + 1;
+        soff += stage_bytes;
+        if (++slot == S) {
+          slot = 0;
+          soff = 0;
+          par ^= 1u;
+        }
       }
       // Drain: every issued copy has landed before the CTA may exit.
       for (int t = issued > S ? issued - S : 0; t < issued; ++t)
@@ -260,11 +266,14 @@ __global__ void __launch_bounds__(kTileThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(kTileM, p.NT);
+      const uint32_t idesc = idesc_bf16_f32(kTileM, NT);
       const uint64_t adesc0 = smem_desc_sw128(ring);
       const uint64_t wdesc0 = smem_desc_sw128(ring + a_bytes);
       bool ok = true;
-      int it = 0;
+      int slot = 0;
+      uint32_t par = 0;   // ring round parity of `slot`
+      uint64_t doff = 0;  // slot * stage_bytes >> 4 (descriptor start-address units)
+      const uint64_t dstep = stage_bytes >> 4;
       for (int i = 0; i < my_tiles && ok; ++i) {
         const int buf = i & 1;
         if (i >= 2 && !mbar_wait_or_abort(smem_u32(&acc_empty[buf]), ((i >> 1) - 1) & 1, abort_flag)) {
@@ -272,20 +281,24 @@ __global__ void __launch_bounds__(kTileThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t d = tmem + (uint32_t)(buf * p.NT);
-        for (int kb = 0; kb < KB; ++kb, ++it) {
-          const int slot = it % S;
-          if (!mbar_wait_or_abort(smem_u32(&full[slot]), (it / S) & 1, abort_flag)) {
+        const uint32_t d = tmem + (uint32_t)(buf * NT);
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait_or_abort(smem_u32(&full[slot]), par, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t off = (uint64_t)(slot * stage_bytes) >> 4;
 #pragma unroll
           for (int kk = 0; kk < kTcKBlock / 16; ++kk)
-            mma_bf16(d, adesc0 + off + (uint64_t)(kk * 2), wdesc0 + off + (uint64_t)(kk * 2), idesc,
+            mma_bf16(d, adesc0 + doff + (uint64_t)(kk * 2), wdesc0 + doff + (uint64_t)(kk * 2), idesc,
                      (kb | kk) != 0 ? 1u : 0u);
           mma_commit(smem_u32(&empty[slot]));
+          doff += dstep;
+          if (++slot == S) {
+            slot = 0;
+            doff = 0;
+            par ^= 1u;
+          }
         }
         if (ok) mma_commit(smem_u32(&acc_full[buf]));
       }
@@ -300,74 +313,46 @@ __global__ void __launch_bounds__(kTileThreads, 1)
     // ------------------------------------------------------------ epilogue
     pdl_wait();  // R may come from the preceding kernel; Y may be read by it
     const int q = warp & 3;  // TMEM lane quarter = tile rows [32 q, 32 q + 32)
-    const int nbox = p.NT / kTileBoxCols;
-    const uint32_t stg = epi + (uint32_t)q * (uint32_t)nbox * kTileBoxBytes;
-    const uint32_t rbar = smem_u32(&rfull[q]);
-    const uint64_t pol_r = policy_evict_first();
-    const uint32_t sw = (uint32_t)(lane & 7);  // 128-byte swizzle phase of this row
-    auto issue_r = [&](int i) {                // residual block of local tile i -> staging
-      const int t = (int)blockIdx.x + i * G;
-      const int m0 = (t % p.m_tiles) * kTileM + q * kTileEpiRows;
-      const int n0 = (t / p.m_tiles) * p.NT;
-      mbar_arrive_expect_tx(rbar, (uint32_t)nbox * kTileBoxBytes);
-      for (int b = 0; b < nbox; ++b)
-        tma_load_2d(stg + (uint32_t)b * kTileBoxBytes, &tmR, n0 + b * kTileBoxCols, m0, rbar, pol_r);
-    };
-    if (lane == 0) issue_r(0);
-    int pending = 0;  // local tile whose residual load is in flight, or -1
+    int t = (int)blockIdx.x;
+    int m = (t % p.m_tiles) * kTileM + q * kTileEpiRows + lane;  // this thread's output row
+    int n0 = (t / p.m_tiles) * NT;
+    uint4 rv[NT / 8];
+    load_residual_row<NT>(p, m, n0, rv);
     for (int i = 0; i < my_tiles; ++i) {
       const int buf = i & 1;
-      bool ok = mbar_wait_or_abort(smem_u32(&acc_full[buf]), (i >> 1) & 1, abort_flag) &&
-                mbar_wait_or_abort(rbar, i & 1, abort_flag);
+      bool ok = mbar_wait_or_abort(smem_u32(&acc_full[buf]), (i >> 1) & 1, abort_flag);
       if (!ok) {
         if (!*abort_flag) report_error(p.err, kErrWaitMma);
         *abort_flag = 1;
       }
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
-      pending = -1;
       tc_fence_after();
-      const int t = (int)blockIdx.x + i * G;
-      const int m0 = (t % p.m_tiles) * kTileM + q * kTileEpiRows;
-      const int n0 = (t / p.m_tiles) * p.NT;
-      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * p.NT);
-      for (int c = 0; c < p.NT / 32; ++c) {
+      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * NT);
+      __nv_bfloat16* dst = p.Y + (size_t)(m < p.M ? m : 0) * p.ldy + n0;
+#pragma unroll
+      for (int c = 0; c < NT / 32; ++c) {
         uint32_t v[32];
-        tmem_ld32(taddr + (uint32_t)(c * 32), v);
-        // Columns [32 c, 32 c + 32) of this row: half (c & 1) of box c / 2,
-        // 16-byte chunks 4 (c & 1) .. 4 (c & 1) + 3 before swizzling.
-        const uint32_t row = stg + (uint32_t)(c >> 1) * kTileBoxBytes + (uint32_t)lane * 128u;
+        tmem_ld32(taddr + (uint32_t)(c * 32), v);  // warp-collective: every lane loads
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const uint32_t addr = row + ((((uint32_t)((c & 1) * 4 + j)) ^ sw) << 4);
-          const uint4 r = lds128(addr);
+          const uint4 r = rv[c * 4 + j];
           const int e = j * 8;
-          sts128(addr, add_round_bf16x2(v[e + 0], v[e + 1], r.x), add_round_bf16x2(v[e + 2], v[e + 3], r.y),
-                 add_round_bf16x2(v[e + 4], v[e + 5], r.z), add_round_bf16x2(v[e + 6], v[e + 7], r.w));
+          const uint4 y = make_uint4(add_round_bf16x2(v[e + 0], v[e + 1], r.x), add_round_bf16x2(v[e + 2], v[e + 3], r.y),
+                                     add_round_bf16x2(v[e + 4], v[e + 5], r.z), add_round_bf16x2(v[e + 6], v[e + 7], r.w));
+          if (m < p.M && n0 + c * 32 + e < p.N) *reinterpret_cast<uint4*>(dst + c * 32 + e) = y;
         }
       }
       // Accumulator buffer free for the MMAs of tile i + 2.
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&acc_empty[buf]));
-      // Make the staged outputs visible to the TMA engine, then store them.
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        for (int b = 0; b < nbox; ++b)
-          tma_store_2d(&tmY, n0 + b * kTileBoxCols, m0, stg + (uint32_t)b * kTileBoxBytes);
-        bulk_commit_group();
-        bulk_wait_group_read0();  // staging may be overwritten again
-        if (i + 1 < my_tiles) issue_r(i + 1);
+      if (i + 1 < my_tiles) {  // next tile's residuals arrive during its main loop
+        t += G;
+        m = (t % p.m_tiles) * kTileM + q * kTileEpiRows + lane;
+        n0 = (t / p.m_tiles) * NT;
+        load_residual_row<NT>(p, m, n0, rv);
       }
-      if (i + 1 < my_tiles) pending = i + 1;
-      __syncwarp();
-    }
-    if (lane == 0) {
-      // A residual load that was issued but not consumed (only after an
-      // abort) lands before the CTA exits; every store completes.
-      if (pending >= 0 && !mbar_wait(rbar, pending & 1)) report_error(p.err, kErrDrain);
-      bulk_wait_group0();
     }
   }
 
@@ -403,11 +388,10 @@ inline int tile_default_nt(int sms, int M, int N) {
   return best;
 }
 
-// Deepest ring (up to 8 stages) that fits beside the epilogue staging.
+// Deepest ring that fits in the shared memory of one CTA.
 inline int tile_default_stages(int nt) {
-  const long long room = 232448 - 2048 - (long long)tile_epi_bytes(nt);
-  long long s = room / tile_stage_bytes(nt);
-  return (int)(s > 8 ? 8 : (s < 2 ? 2 : s));
+  long long st = (232448 - 2048) / tile_stage_bytes(nt);
+  return (int)(st > kTileMaxStages ? kTileMaxStages : (st < 2 ? 2 : st));
 }
 
 inline void tile_default_config(int sms, int M, int N, int K, sgr_config* c) {
@@ -422,8 +406,28 @@ inline void tile_default_config(int sms, int M, int N, int K, sgr_config* c) {
   c->rows_per_stage = 0;
 }
 
+template <int NT>
+inline cudaError_t tile_init_one() {
+  return set_kernel_smem_attrs(reinterpret_cast<const void*>(tile_gemm_kernel<NT>));
+}
+
 inline cudaError_t tile_init_device() {
-  return set_kernel_smem_attrs(reinterpret_cast<const void*>(tile_gemm_kernel));
+  cudaError_t e = tile_init_one<64>();
+  if (e == cudaSuccess) e = tile_init_one<128>();
+  if (e == cudaSuccess) e = tile_init_one<192>();
+  if (e == cudaSuccess) e = tile_init_one<256>();
+  return e;
+}
+
+// The kernel instantiation for a tile width (nullptr if there is none).
+inline const void* tile_kernel_for(int nt) {
+  switch (nt) {
+    case 64: return reinterpret_cast<const void*>(tile_gemm_kernel<64>);
+    case 128: return reinterpret_cast<const void*>(tile_gemm_kernel<128>);
+    case 192: return reinterpret_cast<const void*>(tile_gemm_kernel<192>);
+    case 256: return reinterpret_cast<const void*>(tile_gemm_kernel<256>);
+    default: return nullptr;
+  }
 }
 
 // Checks a resolved configuration for this shape; fills the kernel params.
@@ -431,11 +435,11 @@ inline int tile_plan(const sgr_config& c, int sms, int M, int N, int K, TilePara
                      size_t* smem) {
   if (!tile_supported(M, N, K)) return SGR_ERR_UNSUPPORTED;
   const int nt = c.tile_n;
-  if (nt < kTileBoxCols || nt > kTileMaxN || nt % kTileBoxCols != 0) return SGR_ERR_UNSUPPORTED;
+  if (!tile_kernel_for(nt)) return SGR_ERR_UNSUPPORTED;
   if (c.ctas_per_sm != 1) return SGR_ERR_UNSUPPORTED;
   if (c.token_tile != 0 && c.token_tile != kTileM) return SGR_ERR_UNSUPPORTED;
   if (c.k_blocks_per_stage != 0 && c.k_blocks_per_stage != 1) return SGR_ERR_UNSUPPORTED;
-  if (c.stages < 2 || c.stages > 32) return SGR_ERR_UNSUPPORTED;
+  if (c.stages < 2 || c.stages > kTileMaxStages) return SGR_ERR_UNSUPPORTED;
   if (c.prefetch_stages < 0 || c.prefetch_stages > c.stages) return SGR_ERR_UNSUPPORTED;  // 0: all
   const size_t sm = tile_smem_bytes(c.stages, nt);
   if (sm > 232448) return SGR_ERR_UNSUPPORTED;
@@ -466,11 +470,13 @@ inline int tile_launch(const sgr_config& c, int sms, unsigned* err, const void* 
   size_t smem = 0;
   int rc = tile_plan(c, sms, M, N, K, &p, &grid, &smem);
   if (rc != SGR_OK) return rc;
-  CUtensorMap tmA, tmW, tmR, tmY;
+  CUtensorMap tmA, tmW;
   if (!detail::make_tmap(&tmA, A, M, K, lda, kTileM, kTcKBlock)) return SGR_ERR_LAUNCH;
   if (!detail::make_tmap(&tmW, W, N, K, K, p.NT, kTcKBlock)) return SGR_ERR_LAUNCH;
-  if (!detail::make_tmap(&tmR, R, M, N, ldr, kTileEpiRows, kTileBoxCols)) return SGR_ERR_LAUNCH;
-  if (!detail::make_tmap(&tmY, Y, M, N, ldy, kTileEpiRows, kTileBoxCols)) return SGR_ERR_LAUNCH;
+  p.R = static_cast<const __nv_bfloat16*>(R);
+  p.Y = static_cast<__nv_bfloat16*>(Y);
+  p.ldr = ldr;
+  p.ldy = ldy;
   p.err = err;
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3((unsigned)grid, 1, 1);
@@ -482,7 +488,14 @@ inline int tile_launch(const sgr_config& c, int sms, unsigned* err, const void* 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
   lc.numAttrs = pdl ? 1 : 0;
-  if (cudaLaunchKernelEx(&lc, tile_gemm_kernel, tmA, tmW, tmR, tmY, p) != cudaSuccess) {
+  cudaError_t e = cudaErrorInvalidValue;
+  switch (p.NT) {
+    case 64: e = cudaLaunchKernelEx(&lc, tile_gemm_kernel<64>, tmA, tmW, p); break;
+    case 128: e = cudaLaunchKernelEx(&lc, tile_gemm_kernel<128>, tmA, tmW, p); break;
+    case 192: e = cudaLaunchKernelEx(&lc, tile_gemm_kernel<192>, tmA, tmW, p); break;
+    case 256: e = cudaLaunchKernelEx(&lc, tile_gemm_kernel<256>, tmA, tmW, p); break;
+  }
+  if (e != cudaSuccess) {
     cudaGetLastError();
     return SGR_ERR_LAUNCH;
   }

@@ -163,23 +163,36 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
           tma_load_2d(as + (uint32_t)j * ablk, &tmA, (s * p.kbps + j) * kTcKBlock, 0,
                       smem_u32(&full[s]), pol_a);
       }
+      // Ring position kept by increments: no integer division on the
+      // per-stage path of this single issuing thread.
       int issued = pre;
+      int slot = pre == S ? 0 : pre;
+      uint32_t par = pre == S ? 1u : 0u;  // ring round parity of `slot`
+      uint32_t ws = w_ring + (uint32_t)slot * w_stage, as = a_ring + (uint32_t)slot * a_stage;
+      int kx = pre * p.kbps * kTcKBlock;
+      const int kstep = p.kbps * kTcKBlock;
       for (int s = pre; s < KS; ++s) {
-        const int slot = s % S;
-        if (s >= S && !mbar_wait_or_abort(smem_u32(&empty[slot]), ((s / S) - 1) & 1, abort_flag)) {
+        if (s >= S && !mbar_wait_or_abort(smem_u32(&empty[slot]), par ^ 1u, abort_flag)) {
           if (!*abort_flag) report_error(p.err, kErrWaitEmpty);
           *abort_flag = 1;
           break;
         }
         const uint32_t fb = smem_u32(&full[slot]);
         mbar_arrive_expect_tx(fb, stage_bytes);
-        const uint32_t ws = w_ring + (uint32_t)slot * w_stage;
-        const uint32_t as = a_ring + (uint32_t)slot * a_stage;
         for (int j = 0; j < p.kbps; ++j)
-          tma_load_2d(ws + (uint32_t)j * wblk, &tmW, (s * p.kbps + j) * kTcKBlock, n0, fb, pol_w);
+          tma_load_2d(ws + (uint32_t)j * wblk, &tmW, kx + j * kTcKBlock, n0, fb, pol_w);
         for (int j = 0; j < p.kbps; ++j)
-          tma_load_2d(as + (uint32_t)j * ablk, &tmA, (s * p.kbps + j) * kTcKBlock, 0, fb, pol_a);
+          tma_load_2d(as + (uint32_t)j * ablk, &tmA, kx + j * kTcKBlock, 0, fb, pol_a);
         issued = s + 1;
+        kx += kstep;
+        ws += w_stage;
+        as += a_stage;
+        if (++slot == S) {
+          slot = 0;
+          par ^= 1u;
+          ws = w_ring;
+          as = a_ring;
+        }
       }
       for (int t = issued > S ? issued - S : 0; t < issued; ++t)
         if (!mbar_wait(smem_u32(&full[t % S]), (t / S) & 1)) {
@@ -196,15 +209,15 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
       const uint64_t wdesc0 = smem_desc_sw128(w_ring);
       const uint64_t adesc0 = smem_desc_sw128(a_ring);
       bool ok = true;
+      int slot = 0;
+      uint32_t par = 0;  // ring round parity of `slot`
+      uint64_t wd = wdesc0, ad = adesc0;
       for (int s = 0; s < KS; ++s) {
-        const int slot = s % S;
-        if (!mbar_wait_or_abort(smem_u32(&full[slot]), (s / S) & 1, abort_flag)) {
+        if (!mbar_wait_or_abort(smem_u32(&full[slot]), par, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint64_t wd = wdesc0 + ((uint64_t)(slot * w_stage) >> 4);
-        const uint64_t ad = adesc0 + ((uint64_t)(slot * a_stage) >> 4);
         for (int j = 0; j < p.kbps; j += p.groups) {
 #pragma unroll
           for (int kk = 0; kk < kTcKBlock / 16; ++kk) {
@@ -214,6 +227,14 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
           }
         }
         mma_commit(smem_u32(&empty[slot]));
+        wd += w_stage >> 4;
+        ad += a_stage >> 4;
+        if (++slot == S) {
+          slot = 0;
+          par ^= 1u;
+          wd = wdesc0;
+          ad = adesc0;
+        }
       }
       if (ok) {
         mma_commit(smem_u32(acc_full));

@@ -125,20 +125,34 @@ __global__ void __launch_bounds__(kSimtThreads, (MT <= 2 ? 3 : (MT <= 4 ? 2 : 1)
       const uint64_t pol = policy_evict_first();
       const uint32_t row_bytes = (uint32_t)p.K * 2u;
       const char* wbase = reinterpret_cast<const char*>(p.W) + (size_t)n0 * row_bytes;
+      // Ring position kept by increments: no integer division on the
+      // per-stage path of this single issuing thread.
       int issued = 0;
+      int slot = 0;
+      uint32_t par = 0;  // ring round parity of `slot`
+      const uint32_t ring0 = smem_u32(ring);
+      const uint32_t stage_bytes = (uint32_t)RS * row_bytes;
+      uint32_t dst = ring0;
+      const char* src = wbase;
+      int left = nrows;
       for (int s = 0; s < nstages; ++s) {
-        const int slot = s % S;
-        if (s >= S && !mbar_wait(smem_u32(&empty[slot]), ((s / S) - 1) & 1)) {
+        if (s >= S && !mbar_wait(smem_u32(&empty[slot]), par ^ 1u)) {
           report_error(p.err, kErrWaitEmpty);
           break;
         }
-        const int rows = min(RS, nrows - s * RS);
-        const uint32_t bytes = (uint32_t)rows * row_bytes;
+        const uint32_t bytes = left < RS ? (uint32_t)left * row_bytes : stage_bytes;
         const uint32_t fb = smem_u32(&full[slot]);
         mbar_arrive_expect_tx(fb, bytes);
-        bulk_g2s(smem_u32(ring + (size_t)slot * RS * p.K), wbase + (size_t)s * RS * row_bytes,
-                 bytes, fb, pol);
+        bulk_g2s(dst, src, bytes, fb, pol);
         issued = s + 1;
+        left -= RS;
+        src += stage_bytes;
+        dst += stage_bytes;
+        if (++slot == S) {
+          slot = 0;
+          par ^= 1u;
+          dst = ring0;
+        }
       }
       // Before this CTA can exit, every copy it issued must have landed.
       for (int t = max(0, issued - S); t < issued; ++t) {

@@ -59,11 +59,9 @@ def candidate_configs(path: int, M: int, K: int, grid: str) -> list[dict]:
             return []
         for nt in (64, 128, 192, 256):
             stage = 128 * 128 + nt * 128
-            epi = 4 * (nt // 64) * 4096
-            for st in range(2, 9):
-                if 2048 + st * stage + epi > 232448:
-                    continue
-                if grid == "small" and st not in (3, 4, 6):
+            deepest = (232448 - 2048) // stage
+            for st in range(2, min(deepest, 16) + 1):
+                if grid == "small" and st < deepest - 2:
                     continue
                 for pf in sorted({st, max(1, st - 1)}):
                     out.append(dict(path=path, ctas_per_sm=1, tile_n=nt, stages=st, prefetch_stages=pf))

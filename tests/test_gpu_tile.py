@@ -1,5 +1,5 @@
-"""GPU parity of the tile GEMM path (128-token x tile_n output tiles, tcgen05
-with TMA-staged residual and output) against the CPU oracle."""
+"""GPU parity of the tile GEMM path (128-token x tile_n output tiles on
+tcgen05, residual and output handled row per thread) against the CPU oracle."""
 from __future__ import annotations
 
 import numpy as np
@@ -38,8 +38,8 @@ def run_tile(p, **cfg):
 
 
 # Ragged in every dimension: M below, at and across the 128-token tile; N not
-# a multiple of the tile width or of the 64-column output box; K not a
-# multiple of the 64-wide K block, and K = 8 (a single partial block).
+# a multiple of the tile width or of 64 columns; K not a multiple of the
+# 64-wide K block, and K = 8 (a single partial block).
 SMALL = [(1, 520, 264), (5, 304, 8), (100, 1024, 520), (128, 256, 64), (129, 392, 1000),
          (250, 264, 1000), (300, 392, 264), (383, 1000, 136), (512, 2056, 1800), (640, 776, 3584)]
 
@@ -71,8 +71,9 @@ def test_tile_full_size_compute_bound_sampled(M):
 
 
 def test_tile_full_size_every_tile_corner():
-    """M = 1024: the four corner elements of every 128 x 192 output tile (the
-    library's choice of tile width at this size) and of every 64-column box."""
+    """M = 1024: the corner elements of every 128 x 192 output tile (the
+    library's choice of tile width at this size), of every epilogue warp's
+    32-row block and of every 64-column group."""
     M = 1024
     p = inputs.make_problem(M, N_FULL, K_FULL, seed=9)
     got = run_tile(p, tile_n=192)
@@ -86,7 +87,10 @@ def test_tile_full_size_every_tile_corner():
 
 TILE_CONFIGS = [
     dict(tile_n=64, stages=2),
-    dict(tile_n=64, stages=8),
+    dict(tile_n=64, stages=9),
+    dict(tile_n=128, stages=7, prefetch_stages=3),
+    dict(tile_n=192, stages=5),
+    dict(tile_n=256, stages=4),
     dict(tile_n=128, stages=3, prefetch_stages=1),
     dict(tile_n=128, stages=6),
     dict(tile_n=192, stages=2),
@@ -108,7 +112,7 @@ def test_tile_rejects_bad_config():
     p = inputs.make_problem(300, 256, 256, seed=1)
     A, W, R = (t.cuda() for t in (p.A, p.W, p.R))
     for cfg in (dict(tile_n=96), dict(tile_n=320), dict(tile_n=32), dict(ctas_per_sm=2),
-                dict(tile_n=256, stages=4), dict(tile_n=64, stages=3, prefetch_stages=4),
+                dict(tile_n=256, stages=5), dict(tile_n=64, stages=3, prefetch_stages=4), dict(stages=17),
                 dict(token_tile=64), dict(k_blocks_per_stage=2)):
         with pytest.raises(sgr.SgrError) as e:
             sgr.skinny_gemm_residual_ex(A, W, R, config=sgr.make_config(path=TILE, **cfg))
