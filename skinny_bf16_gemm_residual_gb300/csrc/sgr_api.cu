@@ -174,8 +174,8 @@ const sgr::TableEntry* table_lookup(int M, int N, int K) {
 }
 
 // Library choice for a shape: the measured per-M table where it covers the
-// shape; otherwise the SIMT kernel for M <= 2, the row-slab tensor-core
-// kernel up to 64 tokens, and the tile GEMM beyond.
+// shape; otherwise the row-slab tensor-core kernel up to 64 tokens (the SIMT
+// kernel where the row slab does not fit), and the tile GEMM beyond.
 int select_path(int M, int N, int K, int sms) {
   if (const sgr::TableEntry* e = table_lookup(M, N, K)) {
     if (e->path == SGR_PATH_SIMT && M <= 16 && simt_vpt(K) > 0) return SGR_PATH_SIMT;
@@ -183,8 +183,8 @@ int select_path(int M, int N, int K, int sms) {
     if (e->path == SGR_PATH_TC && sgr::tc_supported(M, N, K)) return SGR_PATH_TC;
     if (e->path == SGR_PATH_TILE && sgr::tile_supported(M, N, K)) return SGR_PATH_TILE;
   }
-  if (M <= 2 && simt_vpt(K) > 0) return SGR_PATH_SIMT;
   if (M <= 64 && sgr::rows_supported(sms, M, N, K)) return SGR_PATH_TC_ROWS;
+  if (M <= 2 && simt_vpt(K) > 0) return SGR_PATH_SIMT;
   if (sgr::tile_supported(M, N, K)) return SGR_PATH_TILE;
   if (sgr::tc_supported(M, N, K)) return SGR_PATH_TC;
   if (M <= 16 && simt_vpt(K) > 0) return SGR_PATH_SIMT;

@@ -33,6 +33,13 @@
 // before griddepcontrol.wait, A after it); warp 1 owns TMEM and lane 0 issues
 // the MMAs; warps 2-5 are the epilogue: they load their residual values while
 // the MMAs run, then tcgen05.ld the accumulator, add, round once and store.
+//
+// For up to 16 tokens the epilogue is one TMEM load, one shared-memory
+// hand-over of group 1's partial sums and the stores, with the residuals and
+// addresses prepared while the MMAs run: it sits on the critical path after
+// the last weight byte lands, so it is kept short (counting each stage's
+// packed groups on separate barriers, to start the last stage's MMAs early,
+// measured slower).
 #pragma once
 
 #include <cuda.h>
@@ -249,74 +256,146 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
     // ------------------------------------------------------------ epilogue
     pdl_wait();  // R may come from the preceding kernel; Y may be read by it
     const int q = warp & 3;       // TMEM lane quarter this warp may access
-    const int etid = threadIdx.x - 64;
-    const int L = q * 32 + lane;  // TMEM lane = row of the MMA window
-    const int g = L / p.RB, r = L % p.RB;
-    const int G = p.groups;
-    const int chunks = p.NT / 16;  // 16-column groups per token tile
-    const int ldp = p.NT + 4;      // staging row stride (floats)
-    float* part = reinterpret_cast<float*>(sb + 1024);  // reuses the drained ring
-    // Residuals for the combine step (one row per thread when NT == 16).
-    float rpre[kRowsPrefetchTokens];
-    const bool pre = (p.NT == kRowsPrefetchTokens) && etid < p.RB && n0 + etid < p.N;
+    if (p.NT == kRowsPrefetchTokens && p.groups <= 2 && p.groups * p.RB <= kTcTileRows) {
+      // Decode epilogue (at most 16 tokens, at most two packed groups): the
+      // thread on TMEM lane r < RB owns output column n0 + r and holds group
+      // 0's partial sums; the thread on lane RB + r holds group 1's and hands
+      // them over through shared memory.  Everything but the TMEM load, one
+      // exchange and the stores is done before the accumulator is ready.
+      const int L = q * 32 + lane;
+      const int G = p.groups;
+      const bool owner = L < p.RB && n0 + L < p.N;
+      const bool helper = G == 2 && L >= p.RB && L < 2 * p.RB;
+      const int r = owner ? L : L - p.RB;
+      const uint32_t xch = w_ring + (uint32_t)(helper || owner ? r : 0) * 80u;  // drained ring: 16 floats + pad per row
+      float res[kRowsPrefetchTokens];
 #pragma unroll
-    for (int i = 0; i < kRowsPrefetchTokens; ++i)
-      rpre[i] = (pre && i < p.M) ? __bfloat162float(p.R[(size_t)i * p.ldr + n0 + etid]) : 0.f;
-    bool ok = mbar_wait_or_abort(smem_u32(acc_full), 0, abort_flag);
-    if (!ok) {
-      if (!*abort_flag) report_error(p.err, kErrWaitMma);
-      *abort_flag = 1;
-    }
-    ok = __all_sync(0xffffffffu, ok);
-    tc_fence_after();
-    // Step 1: each lane copies its diagonal block row (group g, row r) to shared memory.
-    if (ok) {
-      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16);
-      for (int c = 0; c < G * chunks; ++c) {
-        float v[16];
-        tmem_ld16(taddr + (uint32_t)(c * 16), v);  // warp-collective: every lane loads
-        if (g < G && c / chunks == g) {
-          float* dst = part + ((size_t)g * p.RB + r) * ldp + (c % chunks) * 16;
-#pragma unroll
-          for (int i = 0; i < 16; i += 4)
-            *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-        }
+      for (int m = 0; m < kRowsPrefetchTokens; ++m)
+        res[m] = (owner && m < p.M) ? __bfloat162float(p.R[(size_t)m * p.ldr + n0 + L]) : 0.f;
+      bool ok = mbar_wait_or_abort(smem_u32(acc_full), 0, abort_flag);
+      if (!ok) {
+        if (!*abort_flag) report_error(p.err, kErrWaitMma);
+        *abort_flag = 1;
       }
-    }
-    named_bar_sync(1, 128);
-    // Step 2: sum the groups (g order), add the residual, round once, store.
-    if (ok) {
-      for (int item = etid; item < p.RB * chunks; item += 128) {
-        const int rr = item % p.RB, c16 = item / p.RB;
-        const int n = n0 + rr;
-        if (n >= p.N) continue;
-        float acc[16];
+      ok = __all_sync(0xffffffffu, ok);
+      tc_fence_after();
+      float v[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) acc[i] = 0.f;
-        for (int gg = 0; gg < G; ++gg) {
-          const float* src = part + ((size_t)gg * p.RB + rr) * ldp + c16 * 16;
+      for (int i = 0; i < 16; ++i) v[i] = 0.f;
+      if (ok && q * 32 < G * p.RB) {  // warp-uniform: this warp holds rows of the MMA window in use
+        const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16);
+        if (G == 1 || (q + 1) * 32 <= p.RB) {
+          tmem_ld16(taddr, v);  // group-0 columns only
+        } else if (q * 32 >= p.RB) {
+          tmem_ld16(taddr + 16u, v);  // group-1 columns only
+        } else {
+          float v1[16];
+          tmem_ld16(taddr, v);
+          tmem_ld16(taddr + 16u, v1);
+          if (L >= p.RB) {
 #pragma unroll
-          for (int i = 0; i < 16; i += 4) {
-            const float4 w = *reinterpret_cast<const float4*>(src + i);
-            acc[i] += w.x;
-            acc[i + 1] += w.y;
-            acc[i + 2] += w.z;
-            acc[i + 3] += w.w;
+            for (int i = 0; i < 16; ++i) v[i] = v1[i];
           }
         }
-        const int m0 = c16 * 16;
-        if (pre) {
+      }
+      if (ok && helper) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            if (m0 + i < p.M) p.Y[(size_t)(m0 + i) * p.ldy + n] = __float2bfloat16_rn(acc[i] + rpre[i]);
-        } else {
-          float rr16[16];
+        for (int i = 0; i < 16; i += 4)
+          asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(xch + (uint32_t)i * 4u), "f"(v[i]),
+                       "f"(v[i + 1]), "f"(v[i + 2]), "f"(v[i + 3])
+                       : "memory");
+      }
+      named_bar_sync(1, 128);
+      if (ok && owner) {
+        if (G == 2) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            rr16[i] = (m0 + i < p.M) ? __bfloat162float(p.R[(size_t)(m0 + i) * p.ldr + n]) : 0.f;
+          for (int i = 0; i < 16; i += 4) {
+            float a0, a1, a2, a3;
+            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(a0), "=f"(a1), "=f"(a2), "=f"(a3)
+                         : "r"(xch + (uint32_t)i * 4u)
+                         : "memory");
+            v[i] += a0;
+            v[i + 1] += a1;
+            v[i + 2] += a2;
+            v[i + 3] += a3;
+          }
+        }
+        __nv_bfloat16* yp = p.Y + n0 + L;
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            if (m0 + i < p.M) p.Y[(size_t)(m0 + i) * p.ldy + n] = __float2bfloat16_rn(acc[i] + rr16[i]);
+        for (int m = 0; m < kRowsPrefetchTokens; ++m)
+          if (m < p.M) yp[(size_t)m * p.ldy] = __float2bfloat16_rn(v[m] + res[m]);
+      }
+    } else {
+      const int etid = threadIdx.x - 64;
+      const int L = q * 32 + lane;  // TMEM lane = row of the MMA window
+      const int g = L / p.RB, r = L % p.RB;
+      const int G = p.groups;
+      const int chunks = p.NT / 16;  // 16-column groups per token tile
+      const int ldp = p.NT + 4;      // staging row stride (floats)
+      float* part = reinterpret_cast<float*>(sb + 1024);  // reuses the drained ring
+      // Residuals for the combine step (one row per thread when NT == 16).
+      float rpre[kRowsPrefetchTokens];
+      const bool pre = (p.NT == kRowsPrefetchTokens) && etid < p.RB && n0 + etid < p.N;
+#pragma unroll
+      for (int i = 0; i < kRowsPrefetchTokens; ++i)
+        rpre[i] = (pre && i < p.M) ? __bfloat162float(p.R[(size_t)i * p.ldr + n0 + etid]) : 0.f;
+      bool ok = mbar_wait_or_abort(smem_u32(acc_full), 0, abort_flag);
+      if (!ok) {
+        if (!*abort_flag) report_error(p.err, kErrWaitMma);
+        *abort_flag = 1;
+      }
+      ok = __all_sync(0xffffffffu, ok);
+      tc_fence_after();
+      // Step 1: each lane copies its diagonal block row (group g, row r) to shared memory.
+      if (ok) {
+        const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16);
+        for (int c = 0; c < G * chunks; ++c) {
+          float v[16];
+          tmem_ld16(taddr + (uint32_t)(c * 16), v);  // warp-collective: every lane loads
+          if (g < G && c / chunks == g) {
+            float* dst = part + ((size_t)g * p.RB + r) * ldp + (c % chunks) * 16;
+#pragma unroll
+            for (int i = 0; i < 16; i += 4)
+              *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+          }
+        }
+      }
+      named_bar_sync(1, 128);
+      // Step 2: sum the groups (g order), add the residual, round once, store.
+      if (ok) {
+        for (int item = etid; item < p.RB * chunks; item += 128) {
+          const int rr = item % p.RB, c16 = item / p.RB;
+          const int n = n0 + rr;
+          if (n >= p.N) continue;
+          float acc[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+          for (int gg = 0; gg < G; ++gg) {
+            const float* src = part + ((size_t)gg * p.RB + rr) * ldp + c16 * 16;
+#pragma unroll
+            for (int i = 0; i < 16; i += 4) {
+              const float4 w = *reinterpret_cast<const float4*>(src + i);
+              acc[i] += w.x;
+              acc[i + 1] += w.y;
+              acc[i + 2] += w.z;
+              acc[i + 3] += w.w;
+            }
+          }
+          const int m0 = c16 * 16;
+          if (pre) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              if (m0 + i < p.M) p.Y[(size_t)(m0 + i) * p.ldy + n] = __float2bfloat16_rn(acc[i] + rpre[i]);
+          } else {
+            float rr16[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              rr16[i] = (m0 + i < p.M) ? __bfloat162float(p.R[(size_t)(m0 + i) * p.ldr + n]) : 0.f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              if (m0 + i < p.M) p.Y[(size_t)(m0 + i) * p.ldy + n] = __float2bfloat16_rn(acc[i] + rr16[i]);
+          }
         }
       }
     }
