@@ -509,30 +509,47 @@ def run_ours(args):
 
 
 def run_e2e(sgr, per_m, Ws, m_list, device, stream, steps: int):
-    """Each step: for every (M, copy) call, copy A and R from pinned host
-    memory, run the public call, copy Y back; W stays resident (weights)."""
+    """Each step: one host->device copy of the step's inputs (A for every M,
+    R for every call) from a pinned host buffer, the public call for every
+    (M, copy), one device->host copy of every Y into pinned host memory, and a
+    stream synchronise; W stays resident (weights)."""
     import torch
 
-    host = {}
-    h2d = d2h = 0
+    # one contiguous pinned staging buffer per direction, with views per operand
+    in_sizes, out_sizes = [], []
+    for M in m_list:
+        in_sizes.append(M * K_DIM)
+        in_sizes += [M * N_DIM] * COPIES
+        out_sizes += [M * N_DIM] * COPIES
+    h_in = torch.empty(sum(in_sizes), dtype=torch.bfloat16).pin_memory()
+    d_in = torch.empty(sum(in_sizes), dtype=torch.bfloat16, device=device)
+    h_out = torch.empty(sum(out_sizes), dtype=torch.bfloat16).pin_memory()
+    d_out = torch.empty(sum(out_sizes), dtype=torch.bfloat16, device=device)
+    calls = []
+    pos_in = pos_out = 0
     for M in m_list:
         d = per_m[M]
-        host[M] = {"A": d["A_cpu"].pin_memory(), "R": [r.pin_memory() for r in d["R_cpu"]],
-                   "Y": [torch.empty((M, N_DIM), dtype=torch.bfloat16).pin_memory() for _ in range(COPIES)],
-                   "Ad": torch.empty_like(d["A"]), "Rd": [torch.empty_like(r) for r in d["R"]],
-                   "Yd": [torch.empty_like(y) for y in d["Y"]]}
-        h2d += COPIES * (M * K_DIM + M * N_DIM) * 2
-        d2h += COPIES * M * N_DIM * 2
+        a_off = pos_in
+        h_in[pos_in:pos_in + M * K_DIM].copy_(d["A_cpu"].reshape(-1))
+        pos_in += M * K_DIM
+        for c in range(COPIES):
+            h_in[pos_in:pos_in + M * N_DIM].copy_(d["R_cpu"][c].reshape(-1))
+            calls.append((d_in.data_ptr() + 2 * a_off, Ws[c].data_ptr(), d_in.data_ptr() + 2 * pos_in,
+                          d_out.data_ptr() + 2 * pos_out, M))
+            pos_in += M * N_DIM
+            pos_out += M * N_DIM
+    h2d = h_in.numel() * 2
+    d2h = h_out.numel() * 2
+    s = stream.cuda_stream
 
     def one_step():
         with torch.cuda.stream(stream):
-            for M in m_list:
-                h = host[M]
-                for c in range(COPIES):
-                    h["Ad"].copy_(h["A"], non_blocking=True)
-                    h["Rd"][c].copy_(h["R"][c], non_blocking=True)
-                    sgr.skinny_gemm_residual(h["Ad"], Ws[c], h["Rd"][c], h["Yd"][c], stream=stream)
-                    h["Y"][c].copy_(h["Yd"][c], non_blocking=True)
+            d_in.copy_(h_in, non_blocking=True)
+            for A, W, R, Y, M in calls:
+                rc = sgr.skinny_gemm_residual_ptr(A, W, R, Y, M, N_DIM, K_DIM, s)
+                if rc != sgr.SGR_OK:
+                    raise sgr.SgrError(rc, "skinny_gemm_residual")
+            h_out.copy_(d_out, non_blocking=True)
         stream.synchronize()
 
     for _ in range(3):
