@@ -70,7 +70,7 @@
 extern "C" {
 #endif
 
-#define SGR_ABI_VERSION 4
+#define SGR_ABI_VERSION 3
 
 typedef enum {
   SGR_OK = 0,
@@ -127,8 +127,7 @@ typedef struct {
   int token_tile;         /* TC, TC_ROWS: activation rows per MMA (multiple of 16, <= 256) */
   int prefetch_stages;    /* TC_ROWS, TILE: weight stages requested before the dependency wait */
   int tile_n;             /* TILE: W rows per output tile (MMA N): 64, 128, 192 or 256 */
-  int tail_k_blocks;      /* TC_ROWS: the last stage's K blocks go in stages of this many (0: no split) */
-  int reserved[1];        /* must be zero */
+  int reserved[2];        /* must be zero */
 } sgr_config;
 
 /*

@@ -238,7 +238,6 @@ int resolve_config(int dev_sms, int M, int N, int K, const sgr_config* in, sgr_c
       else if (path != SGR_PATH_TILE) out->k_blocks_per_stage = e->k_blocks_per_stage;
       if (path == SGR_PATH_TC_ROWS || path == SGR_PATH_TILE) out->prefetch_stages = e->prefetch_stages;
       if (path == SGR_PATH_TILE && e->tile_n) out->tile_n = e->tile_n;
-      if (path == SGR_PATH_TC_ROWS) out->tail_k_blocks = e->tail_k_blocks;
     }
   }
   if (in) {
@@ -251,7 +250,6 @@ int resolve_config(int dev_sms, int M, int N, int K, const sgr_config* in, sgr_c
     if (in->token_tile) out->token_tile = in->token_tile;
     if (in->prefetch_stages) out->prefetch_stages = in->prefetch_stages;
     if (in->tile_n) out->tile_n = in->tile_n;
-    if (in->tail_k_blocks) out->tail_k_blocks = in->tail_k_blocks;
     // A tile width chosen without a ring depth gets the deepest ring that fits it.
     if (path == SGR_PATH_TILE && in->tile_n && !in->stages) out->stages = sgr::tile_default_stages(out->tile_n);
   }

@@ -65,10 +65,8 @@ struct RowsParams {
   int M, N, K;
   int RB;        // W rows per CTA (multiple of 8, <= 128)
   int NT;        // token tile = MMA N (multiple of 16, >= M)
-  int k_stages;     // ring stages in all: full_stages + tail stages
-  int full_stages;  // stages of kbps K blocks; the rest carry tail_kb K blocks each
-  int kbps;      // 64-wide K blocks per full stage
-  int tail_kb;   // K blocks per tail stage (the last full stage's blocks split up), == kbps if none
+  int k_stages;  // ceil(K / (64 * kbps))
+  int kbps;      // 64-wide K blocks per stage
   int stages;    // ring depth
   int groups;    // K blocks packed into one MMA along its diagonal (1, 2 or 4)
   int prefetch;  // W stages requested before griddepcontrol.wait (1..stages)
@@ -116,6 +114,7 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
   const uint32_t ablk = (uint32_t)p.NT * 128u;   // bytes of one A box
   const uint32_t w_stage = (uint32_t)p.kbps * wblk;
   const uint32_t a_stage = (uint32_t)p.kbps * ablk;
+  const uint32_t stage_bytes = w_stage + a_stage;  // bytes one stage brings in
   const uint32_t w_ring = base + 1024;                         // [stages][kbps] W boxes
   const uint32_t a_ring = w_ring + (uint32_t)S * w_stage;      // [stages][kbps] A boxes
 
@@ -156,26 +155,20 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
       // W for the first `prefetch` stages before the dependency wait.  A
       // slot left free lets weights keep streaming while A (needed by the
       // first MMA) is fetched after the wait.
-      // Stage s carries nkb(s) K blocks: kbps, or tail_kb for the stages
-      // that split the last full stage (so that its MMAs start earlier).
       const int pre = KS < p.prefetch ? KS : p.prefetch;
-      for (int s = 0, kx = 0; s < pre; ++s) {
-        const int nkb = s < p.full_stages ? p.kbps : p.tail_kb;
+      for (int s = 0; s < pre; ++s) {
         const uint32_t fb = smem_u32(&full[s]);
-        mbar_arrive_expect_tx(fb, (uint32_t)nkb * (wblk + ablk));
+        mbar_arrive_expect_tx(fb, stage_bytes);
         const uint32_t ws = w_ring + (uint32_t)s * w_stage;
-        for (int j = 0; j < nkb; ++j)
-          tma_load_2d(ws + (uint32_t)j * wblk, &tmW, kx + j * kTcKBlock, n0, fb, pol_w);
-        kx += nkb * kTcKBlock;
+        for (int j = 0; j < p.kbps; ++j)
+          tma_load_2d(ws + (uint32_t)j * wblk, &tmW, (s * p.kbps + j) * kTcKBlock, n0, fb, pol_w);
       }
       pdl_wait();
-      int kx = 0;
       for (int s = 0; s < pre; ++s) {
-        const int nkb = s < p.full_stages ? p.kbps : p.tail_kb;
         const uint32_t as = a_ring + (uint32_t)s * a_stage;
-        for (int j = 0; j < nkb; ++j)
-          tma_load_2d(as + (uint32_t)j * ablk, &tmA, kx + j * kTcKBlock, 0, smem_u32(&full[s]), pol_a);
-        kx += nkb * kTcKBlock;
+        for (int j = 0; j < p.kbps; ++j)
+          tma_load_2d(as + (uint32_t)j * ablk, &tmA, (s * p.kbps + j) * kTcKBlock, 0,
+                      smem_u32(&full[s]), pol_a);
       }
       // Ring position kept by increments: no integer division on the
       // per-stage path of this single issuing thread.
@@ -183,21 +176,22 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
       int slot = pre == S ? 0 : pre;
       uint32_t par = pre == S ? 1u : 0u;  // ring round parity of `slot`
       uint32_t ws = w_ring + (uint32_t)slot * w_stage, as = a_ring + (uint32_t)slot * a_stage;
+      int kx = pre * p.kbps * kTcKBlock;
+      const int kstep = p.kbps * kTcKBlock;
       for (int s = pre; s < KS; ++s) {
         if (s >= S && !mbar_wait_or_abort(smem_u32(&empty[slot]), par ^ 1u, abort_flag)) {
           if (!*abort_flag) report_error(p.err, kErrWaitEmpty);
           *abort_flag = 1;
           break;
         }
-        const int nkb = s < p.full_stages ? p.kbps : p.tail_kb;
         const uint32_t fb = smem_u32(&full[slot]);
-        mbar_arrive_expect_tx(fb, (uint32_t)nkb * (wblk + ablk));
-        for (int j = 0; j < nkb; ++j)
+        mbar_arrive_expect_tx(fb, stage_bytes);
+        for (int j = 0; j < p.kbps; ++j)
           tma_load_2d(ws + (uint32_t)j * wblk, &tmW, kx + j * kTcKBlock, n0, fb, pol_w);
-        for (int j = 0; j < nkb; ++j)
+        for (int j = 0; j < p.kbps; ++j)
           tma_load_2d(as + (uint32_t)j * ablk, &tmA, kx + j * kTcKBlock, 0, fb, pol_a);
         issued = s + 1;
-        kx += nkb * kTcKBlock;
+        kx += kstep;
         ws += w_stage;
         as += a_stage;
         if (++slot == S) {
@@ -231,8 +225,7 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
           break;
         }
         tc_fence_after();
-        const int nkb = s < p.full_stages ? p.kbps : p.tail_kb;
-        for (int j = 0; j < nkb; j += p.groups) {
+        for (int j = 0; j < p.kbps; j += p.groups) {
 #pragma unroll
           for (int kk = 0; kk < kTcKBlock / 16; ++kk) {
             const bool first = (s == 0) && (j == 0) && (kk == 0);
@@ -486,22 +479,6 @@ inline int rows_plan(const sgr_config& c, int sms, int M, int N, int K, RowsPara
     p->groups /= 2;
   if (rows_stage_floats(p->groups, rb, nt) * 4 > (size_t)c.stages * rows_stage_bytes(c.k_blocks_per_stage, rb, nt))
     return SGR_ERR_UNSUPPORTED;
-  // Tail split: the K blocks of the last full stage go in stages of tail_kb
-  // blocks (a multiple of the packing), so fewer MMAs remain once the last
-  // weight byte has landed.
-  const int kb_total = (K + kTcKBlock - 1) / kTcKBlock;
-  const int tkb = c.tail_k_blocks;
-  if (tkb < 0 || tkb > c.k_blocks_per_stage) return SGR_ERR_UNSUPPORTED;
-  if (tkb == 0 || tkb == c.k_blocks_per_stage) {
-    p->tail_kb = c.k_blocks_per_stage;
-    p->full_stages = p->k_stages;
-  } else {
-    if (tkb % p->groups != 0) return SGR_ERR_UNSUPPORTED;
-    p->tail_kb = tkb;
-    p->full_stages = (kb_total - 1) / c.k_blocks_per_stage;
-    const int rem = kb_total - p->full_stages * c.k_blocks_per_stage;
-    p->k_stages = p->full_stages + (rem + tkb - 1) / tkb;
-  }
   p->tmem_cols = detail::pow2_at_least(p->groups * nt);
   *grid = (N + rb - 1) / rb;
   *smem = sm;

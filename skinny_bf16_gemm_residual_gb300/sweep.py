@@ -52,9 +52,8 @@ def candidate_configs(path: int, M: int, K: int, grid: str) -> list[dict]:
                 if grid == "small" and st not in (3, 4, 6):
                     continue
                 for pf in sorted({st, max(1, st - 1), max(1, st - 2)}):
-                    for tail in sorted({0, 2, 4} & set(range(0, kb))):
-                        out.append(dict(path=path, ctas_per_sm=1, k_blocks_per_stage=kb, stages=st,
-                                        prefetch_stages=pf, tail_k_blocks=tail))
+                    out.append(dict(path=path, ctas_per_sm=1, k_blocks_per_stage=kb, stages=st,
+                                    prefetch_stages=pf))
     elif path == sgr.SGR_PATH_TILE:
         if M < 32:
             return []

@@ -85,25 +85,7 @@ ROWS_CONFIGS = [
     dict(k_blocks_per_stage=8, stages=3, prefetch_stages=1),
     dict(k_blocks_per_stage=8, stages=3, prefetch_stages=3),
     dict(k_blocks_per_stage=4, stages=4, prefetch_stages=2),
-    dict(k_blocks_per_stage=8, stages=3, prefetch_stages=1, tail_k_blocks=2),
-    dict(k_blocks_per_stage=8, stages=3, prefetch_stages=3, tail_k_blocks=4),
-    dict(k_blocks_per_stage=4, stages=5, prefetch_stages=2, tail_k_blocks=2),
-    dict(k_blocks_per_stage=3, stages=4, tail_k_blocks=1),
 ]
-
-
-@pytest.mark.parametrize("K", [64, 520, 1000, 1800, 3584])
-@pytest.mark.parametrize("tail", [1, 2, 4, 6])
-def test_rows_tail_split_ragged_k(K, tail):
-    """The last stage's K blocks split into stages of `tail` blocks, for K
-    that is not a multiple of the stage or of the 64-wide K block."""
-    kb = 6 if tail == 6 else 8
-    if tail % 2:  # an odd tail needs unpacked MMAs (one K block per MMA)
-        kb = 3
-    p = inputs.make_problem(16, 1512, K, seed=K + tail)
-    compare(run_tc(p, ROWS, k_blocks_per_stage=kb, stages=3, tail_k_blocks=tail),
-            oracle_full(p.A, p.W, p.R), f"rows tail={tail} K={K}")
-
 
 
 @pytest.mark.parametrize("cfg", ROWS_CONFIGS, ids=lambda c: "-".join(f"{k}{v}" for k, v in c.items()))
@@ -117,8 +99,7 @@ def test_rows_rejects_bad_config():
     p = inputs.make_problem(20, 256, 256, seed=1)
     A, W, R = (t.cuda() for t in (p.A, p.W, p.R))
     for cfg in (dict(token_tile=16), dict(ctas_per_sm=2), dict(k_blocks_per_stage=8, stages=12),
-                dict(stages=2, prefetch_stages=3), dict(k_blocks_per_stage=4, stages=3, tail_k_blocks=5),
-                dict(k_blocks_per_stage=4, stages=3, tail_k_blocks=3)):
+                dict(stages=2, prefetch_stages=3)):
         with pytest.raises(sgr.SgrError) as e:
             sgr.skinny_gemm_residual_ex(A, W, R, config=sgr.make_config(path=ROWS, **cfg))
         assert e.value.status == sgr.SGR_ERR_UNSUPPORTED
