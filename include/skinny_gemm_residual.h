@@ -70,7 +70,7 @@
 extern "C" {
 #endif
 
-#define SGR_ABI_VERSION 3
+#define SGR_ABI_VERSION 4
 
 typedef enum {
   SGR_OK = 0,
@@ -127,7 +127,8 @@ typedef struct {
   int token_tile;         /* TC, TC_ROWS: activation rows per MMA (multiple of 16, <= 256) */
   int prefetch_stages;    /* TC_ROWS, TILE: weight stages requested before the dependency wait */
   int tile_n;             /* TILE: W rows per output tile (MMA N): 64, 128, 192 or 256 */
-  int reserved[2];        /* must be zero */
+  int k_split;            /* TILE: 1, or 2 = K split over a 2-CTA cluster (one tile per cluster; tile_n <= 192) */
+  int reserved[1];        /* must be zero */
 } sgr_config;
 
 /*

@@ -238,6 +238,7 @@ int resolve_config(int dev_sms, int M, int N, int K, const sgr_config* in, sgr_c
       else if (path != SGR_PATH_TILE) out->k_blocks_per_stage = e->k_blocks_per_stage;
       if (path == SGR_PATH_TC_ROWS || path == SGR_PATH_TILE) out->prefetch_stages = e->prefetch_stages;
       if (path == SGR_PATH_TILE && e->tile_n) out->tile_n = e->tile_n;
+      if (path == SGR_PATH_TILE) out->k_split = e->k_split > 0 ? e->k_split : 1;
     }
   }
   if (in) {
@@ -250,6 +251,8 @@ int resolve_config(int dev_sms, int M, int N, int K, const sgr_config* in, sgr_c
     if (in->token_tile) out->token_tile = in->token_tile;
     if (in->prefetch_stages) out->prefetch_stages = in->prefetch_stages;
     if (in->tile_n) out->tile_n = in->tile_n;
+    if (in->k_split) out->k_split = in->k_split;
+    else if (path == SGR_PATH_TILE && in->tile_n) out->k_split = 1;  // a chosen width runs unsplit unless asked
     // A tile width chosen without a ring depth gets the deepest ring that fits it.
     if (path == SGR_PATH_TILE && in->tile_n && !in->stages) out->stages = sgr::tile_default_stages(out->tile_n);
   }
@@ -548,7 +551,7 @@ int sgr_kernel_resources(int device, int path, int M, int N, int K, int* regs, i
     *smem_bytes = (int)smem;
     *threads = sgr::kRowsThreads;
   } else if (c.path == SGR_PATH_TILE) {
-    if (cudaFuncGetAttributes(&fa, sgr::tile_kernel_for(c.tile_n)) != cudaSuccess) {
+    if (cudaFuncGetAttributes(&fa, sgr::tile_kernel_for(c.tile_n, c.k_split > 0 ? c.k_split : 1)) != cudaSuccess) {
       cudaGetLastError();
       return SGR_ERR_DEVICE;
     }

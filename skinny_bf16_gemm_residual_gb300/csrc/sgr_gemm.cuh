@@ -70,6 +70,7 @@ struct TileParams {
   int k_blocks;  // ceil(K / 64)
   int stages;    // ring depth (one K block of A and W per stage)
   int prefetch;  // W stages requested before griddepcontrol.wait (0..stages)
+  int kb_split;  // K split over a 2-CTA cluster: rank 0 takes K blocks [0, kb_split), rank 1 the rest
   int tmem_cols;
 };
 
@@ -123,6 +124,62 @@ __device__ __forceinline__ uint32_t add_round_bf16x2(uint32_t acc_lo, uint32_t a
   return *reinterpret_cast<const uint32_t*>(&y);
 }
 
+// ------------------------------------------------------------ cluster helpers
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Address of the same shared-memory location in cluster CTA `rank`.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+
+// Arrive on an mbarrier of another CTA of the cluster, releasing this
+// thread's prior writes at cluster scope.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// Phase test that acquires at cluster scope (sees the writes released by
+// remote arrivals).
+__device__ __forceinline__ bool mbar_test_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_test_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (mbar_test_wait_cluster(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > SGR_WAIT_LIMIT_NS) return false;
+  }
+}
+
+// All threads of every CTA of the cluster.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // The residual row segment R[m, n0 .. n0 + NT) of one thread into registers
 // (zeros outside the matrix; N is a multiple of 8, so a 16-byte chunk is
 // either wholly inside or wholly outside).
@@ -135,10 +192,19 @@ __device__ __forceinline__ void load_residual_row(const TileParams& p, int m, in
     rv[j] = (row_ok && n0 + 8 * j < p.N) ? *reinterpret_cast<const uint4*>(src + 8 * j) : make_uint4(0u, 0u, 0u, 0u);
 }
 
-template <int NT>
+// KSPLIT = 1: persistent CTAs, each tile's whole K in one CTA.
+// KSPLIT = 2: one tile per 2-CTA cluster, rank 0 accumulating K blocks
+// [0, kb_split) and rank 1 the rest; at the end each rank sends the half of
+// its accumulator that the other rank owns through distributed shared memory
+// (into the other rank's drained ring), adds the half it received to its own
+// and stores that half of the tile.  (a + b is the same in either order, so
+// the result does not depend on which rank finishes first.)  This doubles
+// the CTAs working on a problem with few tiles (M <= 256 at N = 7168).
+template <int NT, int KSPLIT>
 __global__ void __launch_bounds__(kTileThreads, 1)
     tile_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                      const TileParams p) {
+  static_assert(KSPLIT == 1 || (KSPLIT == 2 && (NT / 2) % 32 == 0), "split tiles hand over 32-column chunks");
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -149,17 +215,22 @@ __global__ void __launch_bounds__(kTileThreads, 1)
   uint64_t* acc_full = empty + S;                     // [2]  MMA -> epilogue
   uint64_t* acc_empty = acc_full + 2;                 // [2]  epilogue (4 warps) -> MMA
   uint64_t* drain = acc_empty + 2;                    // [1]  MMA completion at exit
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* peer_drained = drain + 1;                 // [1]  split: the other rank's ring is free
+  uint64_t* received = peer_drained + 1;              // [1]  split: the other rank's half has arrived
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(received + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const uint32_t a_bytes = (uint32_t)kTileM * 128u;
   const uint32_t stage_bytes = tile_stage_bytes(NT);
   const uint32_t ring = base + 1024;  // [S] x {A box 128 x 64, W box NT x 64}
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int G = gridDim.x;
+  const uint32_t rank = KSPLIT == 2 ? cluster_ctarank() : 0u;
+  const int G = (int)gridDim.x / KSPLIT;      // tile-processing units (CTAs or clusters)
+  const int unit = (int)blockIdx.x / KSPLIT;  // this CTA's unit
   const int tiles = p.m_tiles * p.n_tiles;
-  const int my_tiles = (tiles - (int)blockIdx.x + G - 1) / G;  // >= 1: grid <= tiles
-  const int KB = p.k_blocks;
+  const int my_tiles = (tiles - unit + G - 1) / G;  // >= 1: units <= tiles; 1 when split
+  const int kb0 = (KSPLIT == 2 && rank == 1) ? p.kb_split : 0;
+  const int KB = (KSPLIT == 2 && rank == 0) ? p.kb_split : p.k_blocks - kb0;  // K blocks of this CTA
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -171,6 +242,8 @@ __global__ void __launch_bounds__(kTileThreads, 1)
       mbar_init(smem_u32(&acc_empty[b]), 4);
     }
     mbar_init(smem_u32(drain), 1);
+    mbar_init(smem_u32(peer_drained), 1);
+    mbar_init(smem_u32(received), 4 * 32);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -186,6 +259,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if constexpr (KSPLIT == 2) cluster_sync_all();  // the other rank's barriers exist before any remote arrive
   const uint32_t tmem = *tmem_slot;
   pdl_launch_dependents();  // the dependent grid still waits for our completion before reading
 
@@ -202,9 +276,9 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         int kx, t, m0, n0, kb;
       };
       auto start = [&](Cursor& c) {
-        c.kx = 0;
+        c.kx = kb0 * kTcKBlock;
         c.kb = 0;
-        c.t = (int)blockIdx.x;
+        c.t = unit;
         c.m0 = (c.t % p.m_tiles) * kTileM;
         c.n0 = (c.t / p.m_tiles) * NT;
       };
@@ -212,7 +286,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         c.kx += kTcKBlock;
         if (++c.kb == KB) {
           c.kb = 0;
-          c.kx = 0;
+          c.kx = kb0 * kTcKBlock;
           c.t += G;
           c.m0 = (c.t % p.m_tiles) * kTileM;
           c.n0 = (c.t / p.m_tiles) * NT;
@@ -309,11 +383,11 @@ __global__ void __launch_bounds__(kTileThreads, 1)
       mma_commit(smem_u32(drain));
       if (!mbar_wait(smem_u32(drain), 0)) report_error(p.err, kErrDrain);
     }
-  } else {
+  } else if constexpr (KSPLIT == 1) {
     // ------------------------------------------------------------ epilogue
     pdl_wait();  // R may come from the preceding kernel; Y may be read by it
     const int q = warp & 3;  // TMEM lane quarter = tile rows [32 q, 32 q + 32)
-    int t = (int)blockIdx.x;
+    int t = unit;
     int m = (t % p.m_tiles) * kTileM + q * kTileEpiRows + lane;  // this thread's output row
     int n0 = (t / p.m_tiles) * NT;
     uint4 rv[NT / 8];
@@ -354,6 +428,80 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         load_residual_row<NT>(p, m, n0, rv);
       }
     }
+  } else {
+    // ------------------------------------------------------- split epilogue
+    pdl_wait();  // R may come from the preceding kernel; Y may be read by it
+    constexpr int H = NT / 2;          // columns each rank finishes
+    constexpr int LD = H + 4;          // row stride (floats) of the hand-over buffer
+    const int q = warp & 3;            // TMEM lane quarter = tile rows [32 q, 32 q + 32)
+    const int row = q * 32 + lane;     // row within the tile
+    const uint32_t other = rank ^ 1u;
+    const int m = (unit % p.m_tiles) * kTileM + row;
+    const int own0 = (int)rank * H;    // first column (within the tile) this rank finishes
+    const int n0 = (unit / p.m_tiles) * NT + own0;
+    uint4 rv[H / 8];
+    load_residual_row<H>(p, m, n0, rv);
+    bool ok = mbar_wait_or_abort(smem_u32(&acc_full[0]), 0, abort_flag);
+    if (!ok) {
+      if (!*abort_flag) report_error(p.err, kErrWaitMma);
+      *abort_flag = 1;
+    }
+    ok = __all_sync(0xffffffffu, ok);
+    // This rank's ring is drained (all its MMAs are done): tell the other rank.
+    named_bar_sync(1, 128);
+    if (threadIdx.x == 64) mbar_arrive_remote(map_to_rank(smem_u32(peer_drained), other));
+    // Wait until the other rank's ring is drained, then write into it the half
+    // of this accumulator that the other rank finishes.
+    bool peer_ok = mbar_wait_cluster(smem_u32(peer_drained), 0, abort_flag);
+    peer_ok = __all_sync(0xffffffffu, peer_ok);
+    tc_fence_after();
+    const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16);
+    if (ok && peer_ok) {
+      const uint32_t dst = map_to_rank(ring + (uint32_t)row * (uint32_t)LD * 4u, other);
+      const int peer0 = (int)other * H;
+#pragma unroll
+      for (int c = 0; c < H / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(taddr + (uint32_t)(peer0 + c * 32), v);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          st_cluster_v4(dst + (uint32_t)(c * 32 + 4 * j) * 4u, v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+      }
+    } else if (!peer_ok) {
+      if (!*abort_flag) report_error(p.err, kErrWaitFixup);
+      *abort_flag = 1;
+    }
+    mbar_arrive_remote(map_to_rank(smem_u32(received), other));  // every thread: its writes are released
+    // The other rank's half of this rank's columns has arrived: add, round, store.
+    bool got = mbar_wait_cluster(smem_u32(received), 0, abort_flag);
+    got = __all_sync(0xffffffffu, got);
+    if (!got) {
+      if (!*abort_flag) report_error(p.err, kErrWaitFixup);
+      *abort_flag = 1;
+    }
+    if (ok && peer_ok && got) {
+      const uint32_t src = ring + (uint32_t)row * (uint32_t)LD * 4u;
+      __nv_bfloat16* yrow = p.Y + (size_t)(m < p.M ? m : 0) * p.ldy + n0;
+#pragma unroll
+      for (int c = 0; c < H / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(taddr + (uint32_t)(own0 + c * 32), v);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint4 o0 = lds128(src + (uint32_t)(c * 32 + 8 * j) * 4u);
+          const uint4 o1 = lds128(src + (uint32_t)(c * 32 + 8 * j + 4) * 4u);
+          const uint32_t s[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
+          uint32_t w[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            w[e] = __float_as_uint(__uint_as_float(v[8 * j + e]) + __uint_as_float(s[e]));
+          const uint4 r = rv[c * 4 + j];
+          const uint4 y = make_uint4(add_round_bf16x2(w[0], w[1], r.x), add_round_bf16x2(w[2], w[3], r.y),
+                                     add_round_bf16x2(w[4], w[5], r.z), add_round_bf16x2(w[6], w[7], r.w));
+          if (m < p.M && n0 + c * 32 + 8 * j < p.N) *reinterpret_cast<uint4*>(yrow + c * 32 + 8 * j) = y;
+        }
+      }
+    }
   }
 
   __syncwarp();  // lane-0 roles rejoin their warp before the CTA-wide barrier
@@ -363,6 +511,9 @@ __global__ void __launch_bounds__(kTileThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, (uint32_t)p.tmem_cols);
   }
+  // No rank leaves while the other may still write into its shared memory or
+  // arrive on its barriers.
+  if constexpr (KSPLIT == 2) cluster_sync_all();
 }
 
 // ------------------------------------------------------------------ host side
@@ -370,10 +521,22 @@ inline bool tile_supported(int M, int N, int K) {
   return M >= 1 && N >= 8 && K >= 8 && N % 8 == 0 && K % 8 == 0;
 }
 
-// Tile width: the NT in {192, 256, 128, 64} with the least work per SM
-// (waves of tiles x NT); the first listed wins ties.
-inline int tile_default_nt(int sms, int M, int N) {
+// Tile width and K split.  With the K split over 2-CTA clusters (one tile per
+// cluster, so it needs 2 x tiles <= SMs) the smallest width in {128, 192}
+// that fits is taken while the problem has at most two 128-token tiles;
+// otherwise the NT in {192, 256, 128, 64} with the least work per SM (waves
+// of tiles x NT), the first listed winning ties.
+inline void tile_default_shape(int sms, int M, int N, int K, int* nt_out, int* split_out) {
   const long long mt = (M + kTileM - 1) / kTileM;
+  if (mt <= 2 && (K + kTcKBlock - 1) / kTcKBlock >= 2) {
+    for (int nt : {128, 192}) {
+      if (2 * mt * ((N + nt - 1) / nt) <= sms) {
+        *nt_out = nt;
+        *split_out = 2;
+        return;
+      }
+    }
+  }
   const int cand[4] = {192, 256, 128, 64};
   int best = cand[0];
   long long best_cost = -1;
@@ -385,7 +548,8 @@ inline int tile_default_nt(int sms, int M, int N) {
       best_cost = cost;
     }
   }
-  return best;
+  *nt_out = best;
+  *split_out = 1;
 }
 
 // Deepest ring that fits in the shared memory of one CTA.
@@ -395,10 +559,9 @@ inline int tile_default_stages(int nt) {
 }
 
 inline void tile_default_config(int sms, int M, int N, int K, sgr_config* c) {
-  (void)K;
   c->path = SGR_PATH_TILE;
   c->ctas_per_sm = 1;
-  c->tile_n = tile_default_nt(sms, M, N);
+  tile_default_shape(sms, M, N, K, &c->tile_n, &c->k_split);
   c->stages = tile_default_stages(c->tile_n);
   c->prefetch_stages = 0;  // all stages
   c->token_tile = kTileM;
@@ -406,28 +569,37 @@ inline void tile_default_config(int sms, int M, int N, int K, sgr_config* c) {
   c->rows_per_stage = 0;
 }
 
-template <int NT>
-inline cudaError_t tile_init_one() {
-  return set_kernel_smem_attrs(reinterpret_cast<const void*>(tile_gemm_kernel<NT>));
+// The kernel instantiation for a tile width and K split (nullptr if none).
+inline const void* tile_kernel_for(int nt, int split) {
+  if (split == 1) {
+    switch (nt) {
+      case 64: return reinterpret_cast<const void*>(tile_gemm_kernel<64, 1>);
+      case 128: return reinterpret_cast<const void*>(tile_gemm_kernel<128, 1>);
+      case 192: return reinterpret_cast<const void*>(tile_gemm_kernel<192, 1>);
+      case 256: return reinterpret_cast<const void*>(tile_gemm_kernel<256, 1>);
+      default: return nullptr;
+    }
+  }
+  if (split == 2) {
+    switch (nt) {
+      case 64: return reinterpret_cast<const void*>(tile_gemm_kernel<64, 2>);
+      case 128: return reinterpret_cast<const void*>(tile_gemm_kernel<128, 2>);
+      case 192: return reinterpret_cast<const void*>(tile_gemm_kernel<192, 2>);
+      default: return nullptr;
+    }
+  }
+  return nullptr;
 }
 
 inline cudaError_t tile_init_device() {
-  cudaError_t e = tile_init_one<64>();
-  if (e == cudaSuccess) e = tile_init_one<128>();
-  if (e == cudaSuccess) e = tile_init_one<192>();
-  if (e == cudaSuccess) e = tile_init_one<256>();
-  return e;
-}
-
-// The kernel instantiation for a tile width (nullptr if there is none).
-inline const void* tile_kernel_for(int nt) {
-  switch (nt) {
-    case 64: return reinterpret_cast<const void*>(tile_gemm_kernel<64>);
-    case 128: return reinterpret_cast<const void*>(tile_gemm_kernel<128>);
-    case 192: return reinterpret_cast<const void*>(tile_gemm_kernel<192>);
-    case 256: return reinterpret_cast<const void*>(tile_gemm_kernel<256>);
-    default: return nullptr;
-  }
+  for (int split : {1, 2})
+    for (int nt : {64, 128, 192, 256}) {
+      const void* fn = tile_kernel_for(nt, split);
+      if (!fn) continue;
+      cudaError_t e = set_kernel_smem_attrs(fn);
+      if (e != cudaSuccess) return e;
+    }
+  return cudaSuccess;
 }
 
 // Checks a resolved configuration for this shape; fills the kernel params.
@@ -435,7 +607,8 @@ inline int tile_plan(const sgr_config& c, int sms, int M, int N, int K, TilePara
                      size_t* smem) {
   if (!tile_supported(M, N, K)) return SGR_ERR_UNSUPPORTED;
   const int nt = c.tile_n;
-  if (!tile_kernel_for(nt)) return SGR_ERR_UNSUPPORTED;
+  const int split = c.k_split == 0 ? 1 : c.k_split;
+  if (!tile_kernel_for(nt, split)) return SGR_ERR_UNSUPPORTED;
   if (c.ctas_per_sm != 1) return SGR_ERR_UNSUPPORTED;
   if (c.token_tile != 0 && c.token_tile != kTileM) return SGR_ERR_UNSUPPORTED;
   if (c.k_blocks_per_stage != 0 && c.k_blocks_per_stage != 1) return SGR_ERR_UNSUPPORTED;
@@ -447,17 +620,25 @@ inline int tile_plan(const sgr_config& c, int sms, int M, int N, int K, TilePara
   const long long n_tiles = (N + nt - 1) / nt;
   if (m_tiles * n_tiles > (1ll << 30)) return SGR_ERR_UNSUPPORTED;
   const long long tiles = m_tiles * n_tiles;
+  const int k_blocks = (K + kTcKBlock - 1) / kTcKBlock;
+  if (split == 2) {
+    // One tile per cluster, both ranks with at least one K block, and the
+    // hand-over buffer (128 rows x (NT/2 + 4) floats) inside the ring.
+    if (2 * tiles > sms || k_blocks < 2) return SGR_ERR_UNSUPPORTED;
+    if ((size_t)kTileM * (nt / 2 + 4) * 4 > (size_t)c.stages * tile_stage_bytes(nt)) return SGR_ERR_UNSUPPORTED;
+  }
   p->M = M;
   p->N = N;
   p->K = K;
   p->NT = nt;
   p->m_tiles = (int)m_tiles;
   p->n_tiles = (int)n_tiles;
-  p->k_blocks = (K + kTcKBlock - 1) / kTcKBlock;
+  p->k_blocks = k_blocks;
+  p->kb_split = (k_blocks + 1) / 2;
   p->stages = c.stages;
   p->prefetch = c.prefetch_stages > 0 ? c.prefetch_stages : c.stages;
   p->tmem_cols = detail::pow2_at_least(2 * nt);
-  *grid = (int)(tiles < sms ? tiles : sms);
+  *grid = split == 2 ? (int)(2 * tiles) : (int)(tiles < sms ? tiles : sms);
   *smem = sm;
   return SGR_OK;
 }
@@ -470,6 +651,7 @@ inline int tile_launch(const sgr_config& c, int sms, unsigned* err, const void* 
   size_t smem = 0;
   int rc = tile_plan(c, sms, M, N, K, &p, &grid, &smem);
   if (rc != SGR_OK) return rc;
+  const int split = c.k_split == 0 ? 1 : c.k_split;
   CUtensorMap tmA, tmW;
   if (!detail::make_tmap(&tmA, A, M, K, lda, kTileM, kTcKBlock)) return SGR_ERR_LAUNCH;
   if (!detail::make_tmap(&tmW, W, N, K, K, p.NT, kTcKBlock)) return SGR_ERR_LAUNCH;
@@ -483,17 +665,36 @@ inline int tile_launch(const sgr_config& c, int sms, unsigned* err, const void* 
   lc.blockDim = dim3(kTileThreads, 1, 1);
   lc.dynamicSmemBytes = smem;
   lc.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  unsigned n_attr = 0;
+  if (pdl) {
+    attr[n_attr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n_attr].val.programmaticStreamSerializationAllowed = 1;
+    ++n_attr;
+  }
+  if (split == 2) {
+    attr[n_attr].id = cudaLaunchAttributeClusterDimension;
+    attr[n_attr].val.clusterDim.x = 2;
+    attr[n_attr].val.clusterDim.y = 1;
+    attr[n_attr].val.clusterDim.z = 1;
+    ++n_attr;
+  }
   lc.attrs = attr;
-  lc.numAttrs = pdl ? 1 : 0;
+  lc.numAttrs = n_attr;
   cudaError_t e = cudaErrorInvalidValue;
-  switch (p.NT) {
-    case 64: e = cudaLaunchKernelEx(&lc, tile_gemm_kernel<64>, tmA, tmW, p); break;
-    case 128: e = cudaLaunchKernelEx(&lc, tile_gemm_kernel<128>, tmA, tmW, p); break;
-    case 192: e = cudaLaunchKernelEx(&lc, tile_gemm_kernel<192>, tmA, tmW, p); break;
-    case 256: e = cudaLaunchKernelEx(&lc, tile_gemm_kernel<256>, tmA, tmW, p); break;
+  if (split == 1) {
+    switch (p.NT) {
+      case 64: e = cudaLaunchKernelEx(&lc, tile_gemm_kernel<64, 1>, tmA, tmW, p); break;
+      case 128: e = cudaLaunchKernelEx(&lc, tile_gemm_kernel<128, 1>, tmA, tmW, p); break;
+      case 192: e = cudaLaunchKernelEx(&lc, tile_gemm_kernel<192, 1>, tmA, tmW, p); break;
+      case 256: e = cudaLaunchKernelEx(&lc, tile_gemm_kernel<256, 1>, tmA, tmW, p); break;
+    }
+  } else {
+    switch (p.NT) {
+      case 64: e = cudaLaunchKernelEx(&lc, tile_gemm_kernel<64, 2>, tmA, tmW, p); break;
+      case 128: e = cudaLaunchKernelEx(&lc, tile_gemm_kernel<128, 2>, tmA, tmW, p); break;
+      case 192: e = cudaLaunchKernelEx(&lc, tile_gemm_kernel<192, 2>, tmA, tmW, p); break;
+    }
   }
   if (e != cudaSuccess) {
     cudaGetLastError();

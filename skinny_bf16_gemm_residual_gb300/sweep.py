@@ -64,7 +64,9 @@ def candidate_configs(path: int, M: int, K: int, grid: str) -> list[dict]:
                 if grid == "small" and st < deepest - 2:
                     continue
                 for pf in sorted({st, max(1, st - 1)}):
-                    out.append(dict(path=path, ctas_per_sm=1, tile_n=nt, stages=st, prefetch_stages=pf))
+                    for split in ((1, 2) if nt <= 192 else (1,)):
+                        out.append(dict(path=path, ctas_per_sm=1, tile_n=nt, stages=st, prefetch_stages=pf,
+                                        k_split=split))
     else:
         tiles = (M + 255) // 256
         nt = ((M + tiles - 1) // tiles + 15) // 16 * 16  # the library's token tile

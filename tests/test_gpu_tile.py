@@ -85,6 +85,76 @@ def test_tile_full_size_every_tile_corner():
     compare(got[ms, ns], ref, "tile corners")
 
 
+SPLIT_CONFIGS = [
+    dict(tile_n=64, k_split=2, stages=9),
+    dict(tile_n=128, k_split=2, stages=7),
+    dict(tile_n=128, k_split=2, stages=3, prefetch_stages=1),
+    dict(tile_n=192, k_split=2, stages=5),
+    dict(tile_n=192, k_split=2, stages=2),
+]
+
+
+@pytest.mark.parametrize("cfg", SPLIT_CONFIGS, ids=lambda c: "-".join(f"{k}{v}" for k, v in c.items()))
+@pytest.mark.parametrize("M,N,K", [(1, 1024, 1032), (100, 2056, 72), (128, 1000, 136), (200, 1512, 3584),
+                                   (256, 2056, 1000)])
+def test_tile_split_k_cluster(cfg, M, N, K):
+    """K split over a 2-CTA cluster, partial sums handed over through
+    distributed shared memory; K of 2 or 3 K blocks (one rank gets a single
+    block) and ragged M and N."""
+    p = inputs.make_problem(M, N, K, seed=3 * M + K)
+    compare(run_tile(p, **cfg), oracle_full(p.A, p.W, p.R), f"tile split M={M} N={N} K={K} {cfg}")
+
+
+@pytest.mark.parametrize("M", [32, 128, 256])
+def test_tile_split_full_size(M):
+    p = inputs.make_problem(M, N_FULL, K_FULL, seed=M + 5)
+    got = run_tile(p, tile_n=128 if M <= 128 else 192, k_split=2)
+    if M <= 128:
+        compare(got, oracle_full(p.A, p.W, p.R), f"tile split M={M}")
+    else:
+        rng = np.random.default_rng(M)
+        ms = np.concatenate([rng.integers(0, M, 6000), np.zeros(N_FULL, int), np.full(N_FULL, M - 1)])
+        ns = np.concatenate([rng.integers(0, N_FULL, 6000), np.arange(N_FULL), np.arange(N_FULL)])
+        compare(got[ms, ns], oracle.load().sample(p.A, p.W, p.R, ms, ns), f"tile split M={M} sampled")
+
+
+def test_tile_split_strided_in_place_and_deterministic():
+    M, N, K = 150, 1024, 1032
+    p = inputs.make_problem(M, N, K, seed=57)
+    cfg = dict(tile_n=128, k_split=2)
+    Abig = torch.zeros((M, K + 136), dtype=torch.bfloat16, device="cuda")
+    A = Abig[:, 64:64 + K]
+    A.copy_(p.A)
+    big = torch.full((M, N + 512), 3.0, dtype=torch.bfloat16, device="cuda")
+    RY = big[:, 256:256 + N]
+    RY.copy_(p.R)
+    sgr.skinny_gemm_residual_ex(A, p.W.cuda(), RY, RY, config=sgr.make_config(path=TILE, **cfg))
+    torch.cuda.synchronize()
+    compare(bits(RY), oracle_full(p.A, p.W, p.R), "tile split strided in-place")
+    assert torch.all(big[:, :256] == 3.0) and torch.all(big[:, 256 + N:] == 3.0)
+    y1, y2 = run_tile(p, **cfg), run_tile(p, **cfg)
+    assert np.array_equal(y1, y2) and np.array_equal(y1, bits(RY))
+
+
+def test_tile_split_rejects():
+    p = inputs.make_problem(300, 256, 256, seed=2)
+    A, W, R = (t.cuda() for t in (p.A, p.W, p.R))
+    for cfg in (dict(tile_n=256, k_split=2), dict(tile_n=128, k_split=3), dict(tile_n=64, k_split=-1)):
+        with pytest.raises(sgr.SgrError) as e:
+            sgr.skinny_gemm_residual_ex(A, W, R, config=sgr.make_config(path=TILE, **cfg))
+        assert e.value.status == sgr.SGR_ERR_UNSUPPORTED, cfg
+    q = inputs.make_problem(4, 256, 8, seed=3)  # a single K block cannot be split
+    with pytest.raises(sgr.SgrError) as e:
+        sgr.skinny_gemm_residual_ex(q.A.cuda(), q.W.cuda(), q.R.cuda(),
+                                    config=sgr.make_config(path=TILE, tile_n=64, k_split=2))
+    assert e.value.status == sgr.SGR_ERR_UNSUPPORTED
+    big = inputs.make_problem(1024, N_FULL, 64, seed=4)  # 304 tiles: more than one per cluster
+    with pytest.raises(sgr.SgrError) as e:
+        sgr.skinny_gemm_residual_ex(big.A.cuda(), big.W.cuda(), big.R.cuda(),
+                                    config=sgr.make_config(path=TILE, tile_n=192, k_split=2))
+    assert e.value.status == sgr.SGR_ERR_UNSUPPORTED
+
+
 TILE_CONFIGS = [
     dict(tile_n=64, stages=2),
     dict(tile_n=64, stages=9),
