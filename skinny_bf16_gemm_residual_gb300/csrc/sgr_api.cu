@@ -235,7 +235,7 @@ int resolve_config(int dev_sms, int M, int N, int K, const sgr_config* in, sgr_c
       out->ctas_per_sm = e->ctas_per_sm;
       out->stages = e->stages;
       if (path == SGR_PATH_SIMT) out->rows_per_stage = e->rows_per_stage;
-      else if (path != SGR_PATH_TILE) out->k_blocks_per_stage = e->k_blocks_per_stage;
+      else if (path != SGR_PATH_TILE || e->k_blocks_per_stage > 0) out->k_blocks_per_stage = e->k_blocks_per_stage;
       if (path == SGR_PATH_TC_ROWS || path == SGR_PATH_TILE) out->prefetch_stages = e->prefetch_stages;
       if (path == SGR_PATH_TILE && e->tile_n) out->tile_n = e->tile_n;
       if (path == SGR_PATH_TILE) out->k_split = e->k_split > 0 ? e->k_split : 1;
@@ -254,7 +254,8 @@ int resolve_config(int dev_sms, int M, int N, int K, const sgr_config* in, sgr_c
     if (in->k_split) out->k_split = in->k_split;
     else if (path == SGR_PATH_TILE && in->tile_n) out->k_split = 1;  // a chosen width runs unsplit unless asked
     // A tile width chosen without a ring depth gets the deepest ring that fits it.
-    if (path == SGR_PATH_TILE && in->tile_n && !in->stages) out->stages = sgr::tile_default_stages(out->tile_n);
+    if (path == SGR_PATH_TILE && (in->tile_n || in->k_blocks_per_stage) && !in->stages)
+      out->stages = sgr::tile_default_stages(out->tile_n, out->k_blocks_per_stage > 0 ? out->k_blocks_per_stage : 1);
   }
   if (out->ctas_per_sm < 1 || out->ctas_per_sm > 8 || out->stages < 1 || out->stages > 64)
     return SGR_ERR_UNSUPPORTED;
@@ -555,7 +556,7 @@ int sgr_kernel_resources(int device, int path, int M, int N, int K, int* regs, i
       cudaGetLastError();
       return SGR_ERR_DEVICE;
     }
-    *smem_bytes = (int)sgr::tile_smem_bytes(c.stages, c.tile_n);
+    *smem_bytes = (int)sgr::tile_smem_bytes(c.stages, c.tile_n, c.k_blocks_per_stage > 0 ? c.k_blocks_per_stage : 1);
     *threads = sgr::kTileThreads;
   } else {
     int s = 0, t = 0;

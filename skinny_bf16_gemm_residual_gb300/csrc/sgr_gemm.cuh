@@ -68,18 +68,20 @@ struct TileParams {
   int m_tiles;   // ceil(M / 128)
   int n_tiles;   // ceil(N / NT)
   int k_blocks;  // ceil(K / 64)
-  int stages;    // ring depth (one K block of A and W per stage)
+  int stages;    // ring depth
+  int kbps;      // K blocks per ring stage (1, 2 or 4): more contiguous bytes per W row and fetch
   int prefetch;  // W stages requested before griddepcontrol.wait (0..stages)
   int kb_split;  // K split over a 2-CTA cluster: rank 0 takes K blocks [0, kb_split), rank 1 the rest
   int tmem_cols;
 };
 
-__host__ __device__ inline uint32_t tile_stage_bytes(int nt) {
-  return (uint32_t)kTileM * 128u + (uint32_t)nt * 128u;
+// One ring stage: kbps K blocks of A (128 x 64 boxes) then of W (NT x 64).
+__host__ __device__ inline uint32_t tile_stage_bytes(int nt, int kbps) {
+  return (uint32_t)kbps * ((uint32_t)kTileM * 128u + (uint32_t)nt * 128u);
 }
 
-__host__ __device__ inline size_t tile_smem_bytes(int stages, int nt) {
-  return 1024 /* alignment slack */ + 1024 /* barriers */ + (size_t)stages * tile_stage_bytes(nt);
+__host__ __device__ inline size_t tile_smem_bytes(int stages, int nt, int kbps) {
+  return 1024 /* alignment slack */ + 1024 /* barriers */ + (size_t)stages * tile_stage_bytes(nt, kbps);
 }
 
 __device__ __forceinline__ uint64_t policy_evict_normal() {
@@ -219,9 +221,12 @@ __global__ void __launch_bounds__(kTileThreads, 1)
   uint64_t* received = peer_drained + 1;              // [1]  split: the other rank's half has arrived
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(received + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  const uint32_t a_bytes = (uint32_t)kTileM * 128u;
-  const uint32_t stage_bytes = tile_stage_bytes(NT);
-  const uint32_t ring = base + 1024;  // [S] x {A box 128 x 64, W box NT x 64}
+  const int KP = p.kbps;
+  const uint32_t a_box = (uint32_t)kTileM * 128u;     // one A box: 128 rows x 64 K
+  const uint32_t w_box = (uint32_t)NT * 128u;         // one W box: NT rows x 64 K
+  const uint32_t a_part = (uint32_t)KP * a_box;       // A boxes at the start of a stage, W boxes after
+  const uint32_t stage_bytes = tile_stage_bytes(NT, KP);
+  const uint32_t ring = base + 1024;  // [S] x {KP A boxes, KP W boxes}
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = KSPLIT == 2 ? cluster_ctarank() : 0u;
@@ -231,6 +236,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
   const int my_tiles = (tiles - unit + G - 1) / G;  // >= 1: units <= tiles; 1 when split
   const int kb0 = (KSPLIT == 2 && rank == 1) ? p.kb_split : 0;
   const int KB = (KSPLIT == 2 && rank == 0) ? p.kb_split : p.k_blocks - kb0;  // K blocks of this CTA
+  const int KS = (KB + KP - 1) / KP;  // ring stages per tile
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -268,7 +274,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_normal();  // re-read by the CTAs of the other token tiles
       const uint64_t pol_a = policy_evict_last();    // re-read for every W column tile
-      const int total = my_tiles * KB;               // stages this CTA loads
+      const int total = my_tiles * KS;               // stages this CTA loads
       // Cursor over (local tile, K block) advanced by increments only: the
       // producer's per-stage path holds no integer division, which on this
       // single issuing thread costs more than the MMAs it feeds.
@@ -283,8 +289,8 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         c.n0 = (c.t / p.m_tiles) * NT;
       };
       auto advance = [&](Cursor& c) {
-        c.kx += kTcKBlock;
-        if (++c.kb == KB) {
+        c.kx += KP * kTcKBlock;
+        if (++c.kb == KS) {
           c.kb = 0;
           c.kx = kb0 * kTcKBlock;
           c.t += G;
@@ -298,14 +304,18 @@ __global__ void __launch_bounds__(kTileThreads, 1)
       for (int it = 0; it < pre; ++it, advance(c)) {
         const uint32_t fb = smem_u32(&full[it]);
         mbar_arrive_expect_tx(fb, stage_bytes);
-        tma_load_2d(ring + (uint32_t)it * stage_bytes + a_bytes, &tmW, c.kx, c.n0, fb, pol_w);
+        for (int j = 0; j < KP; ++j)
+          tma_load_2d(ring + (uint32_t)it * stage_bytes + a_part + (uint32_t)j * w_box, &tmW,
+                      c.kx + j * kTcKBlock, c.n0, fb, pol_w);
       }
       pdl_wait();
       {
         Cursor ca;
         start(ca);
         for (int it = 0; it < pre; ++it, advance(ca))
-          tma_load_2d(ring + (uint32_t)it * stage_bytes, &tmA, ca.kx, ca.m0, smem_u32(&full[it]), pol_a);
+          for (int j = 0; j < KP; ++j)
+            tma_load_2d(ring + (uint32_t)it * stage_bytes + (uint32_t)j * a_box, &tmA, ca.kx + j * kTcKBlock,
+                        ca.m0, smem_u32(&full[it]), pol_a);
       }
       int slot = pre == S ? 0 : pre;
       uint32_t par = pre == S ? 1u : 0u;  // ring round parity of `slot`
@@ -320,8 +330,10 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         const uint32_t fb = smem_u32(&full[slot]);
         const uint32_t st = ring + soff;
         mbar_arrive_expect_tx(fb, stage_bytes);
-        tma_load_2d(st, &tmA, c.kx, c.m0, fb, pol_a);
-        tma_load_2d(st + a_bytes, &tmW, c.kx, c.n0, fb, pol_w);
+        for (int j = 0; j < KP; ++j) {
+          tma_load_2d(st + (uint32_t)j * a_box, &tmA, c.kx + j * kTcKBlock, c.m0, fb, pol_a);
+          tma_load_2d(st + a_part + (uint32_t)j * w_box, &tmW, c.kx + j * kTcKBlock, c.n0, fb, pol_w);
+        }
         issued = it + 1;
         soff += stage_bytes;
         if (++slot == S) {
@@ -342,7 +354,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16_f32(kTileM, NT);
       const uint64_t adesc0 = smem_desc_sw128(ring);
-      const uint64_t wdesc0 = smem_desc_sw128(ring + a_bytes);
+      const uint64_t wdesc0 = smem_desc_sw128(ring + a_part);
       bool ok = true;
       int slot = 0;
       uint32_t par = 0;   // ring round parity of `slot`
@@ -356,16 +368,19 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         }
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(buf * NT);
-        for (int kb = 0; kb < KB; ++kb) {
+        for (int ks = 0; ks < KS; ++ks) {
           if (!mbar_wait_or_abort(smem_u32(&full[slot]), par, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
+          for (int j = 0; j < KP; ++j) {
+            const uint64_t ao = doff + (uint64_t)((j * a_box) >> 4), wo = doff + (uint64_t)((j * w_box) >> 4);
 #pragma unroll
-          for (int kk = 0; kk < kTcKBlock / 16; ++kk)
-            mma_bf16(d, adesc0 + doff + (uint64_t)(kk * 2), wdesc0 + doff + (uint64_t)(kk * 2), idesc,
-                     (kb | kk) != 0 ? 1u : 0u);
+            for (int kk = 0; kk < kTcKBlock / 16; ++kk)
+              mma_bf16(d, adesc0 + ao + (uint64_t)(kk * 2), wdesc0 + wo + (uint64_t)(kk * 2), idesc,
+                       (ks | j | kk) != 0 ? 1u : 0u);
+          }
           mma_commit(smem_u32(&empty[slot]));
           doff += dstep;
           if (++slot == S) {
@@ -553,8 +568,8 @@ inline void tile_default_shape(int sms, int M, int N, int K, int* nt_out, int* s
 }
 
 // Deepest ring that fits in the shared memory of one CTA.
-inline int tile_default_stages(int nt) {
-  long long st = (232448 - 2048) / tile_stage_bytes(nt);
+inline int tile_default_stages(int nt, int kbps = 1) {
+  long long st = (232448 - 2048) / tile_stage_bytes(nt, kbps);
   return (int)(st > kTileMaxStages ? kTileMaxStages : (st < 2 ? 2 : st));
 }
 
@@ -611,21 +626,25 @@ inline int tile_plan(const sgr_config& c, int sms, int M, int N, int K, TilePara
   if (!tile_kernel_for(nt, split)) return SGR_ERR_UNSUPPORTED;
   if (c.ctas_per_sm != 1) return SGR_ERR_UNSUPPORTED;
   if (c.token_tile != 0 && c.token_tile != kTileM) return SGR_ERR_UNSUPPORTED;
-  if (c.k_blocks_per_stage != 0 && c.k_blocks_per_stage != 1) return SGR_ERR_UNSUPPORTED;
+  const int kbps = c.k_blocks_per_stage == 0 ? 1 : c.k_blocks_per_stage;
+  if (kbps != 1 && kbps != 2 && kbps != 4) return SGR_ERR_UNSUPPORTED;
   if (c.stages < 2 || c.stages > kTileMaxStages) return SGR_ERR_UNSUPPORTED;
   if (c.prefetch_stages < 0 || c.prefetch_stages > c.stages) return SGR_ERR_UNSUPPORTED;  // 0: all
-  const size_t sm = tile_smem_bytes(c.stages, nt);
+  const size_t sm = tile_smem_bytes(c.stages, nt, kbps);
   if (sm > 232448) return SGR_ERR_UNSUPPORTED;
   const long long m_tiles = (M + kTileM - 1) / kTileM;
   const long long n_tiles = (N + nt - 1) / nt;
   if (m_tiles * n_tiles > (1ll << 30)) return SGR_ERR_UNSUPPORTED;
   const long long tiles = m_tiles * n_tiles;
   const int k_blocks = (K + kTcKBlock - 1) / kTcKBlock;
+  // Split: rank 0 takes the first half of the K blocks rounded up to whole
+  // stages (so that its last stage reads nothing of rank 1's range).
+  const int kb_split = ((k_blocks + 1) / 2 + kbps - 1) / kbps * kbps;
   if (split == 2) {
     // One tile per cluster, both ranks with at least one K block, and the
     // hand-over buffer (128 rows x (NT/2 + 4) floats) inside the ring.
-    if (2 * tiles > sms || k_blocks < 2) return SGR_ERR_UNSUPPORTED;
-    if ((size_t)kTileM * (nt / 2 + 4) * 4 > (size_t)c.stages * tile_stage_bytes(nt)) return SGR_ERR_UNSUPPORTED;
+    if (2 * tiles > sms || k_blocks - kb_split < 1) return SGR_ERR_UNSUPPORTED;
+    if ((size_t)kTileM * (nt / 2 + 4) * 4 > (size_t)c.stages * tile_stage_bytes(nt, kbps)) return SGR_ERR_UNSUPPORTED;
   }
   p->M = M;
   p->N = N;
@@ -634,7 +653,8 @@ inline int tile_plan(const sgr_config& c, int sms, int M, int N, int K, TilePara
   p->m_tiles = (int)m_tiles;
   p->n_tiles = (int)n_tiles;
   p->k_blocks = k_blocks;
-  p->kb_split = (k_blocks + 1) / 2;
+  p->kb_split = kb_split;
+  p->kbps = kbps;
   p->stages = c.stages;
   p->prefetch = c.prefetch_stages > 0 ? c.prefetch_stages : c.stages;
   p->tmem_cols = detail::pow2_at_least(2 * nt);

@@ -58,15 +58,16 @@ def candidate_configs(path: int, M: int, K: int, grid: str) -> list[dict]:
         if M < 32:
             return []
         for nt in (64, 128, 192, 256):
-            stage = 128 * 128 + nt * 128
-            deepest = (232448 - 2048) // stage
-            for st in range(2, min(deepest, 16) + 1):
-                if grid == "small" and st < deepest - 2:
-                    continue
-                for pf in sorted({st, max(1, st - 1)}):
-                    for split in ((1, 2) if nt <= 192 else (1,)):
-                        out.append(dict(path=path, ctas_per_sm=1, tile_n=nt, stages=st, prefetch_stages=pf,
-                                        k_split=split))
+            for kb in (1, 2, 4):
+                stage = kb * (128 * 128 + nt * 128)
+                deepest = (232448 - 2048) // stage
+                for st in range(2, min(deepest, 16) + 1):
+                    if grid == "small" and st < deepest - 2:
+                        continue
+                    for pf in sorted({st, max(1, st - 1)}):
+                        for split in ((1, 2) if nt <= 192 else (1,)):
+                            out.append(dict(path=path, ctas_per_sm=1, tile_n=nt, k_blocks_per_stage=kb, stages=st,
+                                            prefetch_stages=pf, k_split=split))
     else:
         tiles = (M + 255) // 256
         nt = ((M + tiles - 1) // tiles + 15) // 16 * 16  # the library's token tile
@@ -136,6 +137,8 @@ def main(argv=None):
     ap.add_argument("--repeats", type=int, default=7)
     ap.add_argument("--replays", type=int, default=50)
     ap.add_argument("--no-cublas", action="store_true")
+    ap.add_argument("--config", action="append", default=[],
+                    help="time only this configuration (JSON object of sgr_config fields; repeatable)")
     ap.add_argument("--output", default=None)
     args = ap.parse_args(argv)
     torch.cuda.set_device(0)
@@ -160,7 +163,9 @@ def main(argv=None):
             launch = lambda c: torch.addmm(Rs[c], A, Ws[c].t(), out=Ys[c])
             rows.append(("cublas_addmm", {}, graph_samples(launch, args.copies, stream, args.repeats, args.replays)))
         for name in args.paths.split(","):
-            for cfg in candidate_configs(paths[name], M, K, args.grid):
+            cands = ([dict(json.loads(c), path=paths[name]) for c in args.config] if args.config
+                     else candidate_configs(paths[name], M, K, args.grid))
+            for cfg in cands:
                 c = sgr.make_config(**cfg)
                 launch = lambda i, c=c: sgr.skinny_gemm_residual_ex(A, Ws[i], Rs[i], Ys[i], stream=stream, config=c)
                 try:

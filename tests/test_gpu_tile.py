@@ -87,6 +87,8 @@ def test_tile_full_size_every_tile_corner():
 
 SPLIT_CONFIGS = [
     dict(tile_n=64, k_split=2, stages=9),
+    dict(tile_n=128, k_split=2, k_blocks_per_stage=2, stages=3),
+    dict(tile_n=64, k_split=2, k_blocks_per_stage=4, stages=2),
     dict(tile_n=128, k_split=2, stages=7),
     dict(tile_n=128, k_split=2, stages=3, prefetch_stages=1),
     dict(tile_n=192, k_split=2, stages=5),
@@ -102,6 +104,12 @@ def test_tile_split_k_cluster(cfg, M, N, K):
     distributed shared memory; K of 2 or 3 K blocks (one rank gets a single
     block) and ragged M and N."""
     p = inputs.make_problem(M, N, K, seed=3 * M + K)
+    kb, kp = (K + 63) // 64, cfg.get("k_blocks_per_stage", 1)
+    if kb - ((kb + 1) // 2 + kp - 1) // kp * kp < 1:  # rank 1 would get no K block: refused
+        with pytest.raises(sgr.SgrError) as e:
+            run_tile(p, **cfg)
+        assert e.value.status == sgr.SGR_ERR_UNSUPPORTED
+        return
     compare(run_tile(p, **cfg), oracle_full(p.A, p.W, p.R), f"tile split M={M} N={N} K={K} {cfg}")
 
 
@@ -167,6 +175,9 @@ TILE_CONFIGS = [
     dict(tile_n=192, stages=4, prefetch_stages=2),
     dict(tile_n=256, stages=3),
     dict(tile_n=256, stages=2, prefetch_stages=1),
+    dict(tile_n=128, k_blocks_per_stage=2, stages=3),
+    dict(tile_n=192, k_blocks_per_stage=2, stages=2, prefetch_stages=1),
+    dict(tile_n=64, k_blocks_per_stage=4, stages=2),
 ]
 
 
@@ -183,7 +194,7 @@ def test_tile_rejects_bad_config():
     A, W, R = (t.cuda() for t in (p.A, p.W, p.R))
     for cfg in (dict(tile_n=96), dict(tile_n=320), dict(tile_n=32), dict(ctas_per_sm=2),
                 dict(tile_n=256, stages=5), dict(tile_n=64, stages=3, prefetch_stages=4), dict(stages=17),
-                dict(token_tile=64), dict(k_blocks_per_stage=2)):
+                dict(token_tile=64), dict(k_blocks_per_stage=3), dict(tile_n=256, k_blocks_per_stage=4, stages=2)):
         with pytest.raises(sgr.SgrError) as e:
             sgr.skinny_gemm_residual_ex(A, W, R, config=sgr.make_config(path=TILE, **cfg))
         assert e.value.status == sgr.SGR_ERR_UNSUPPORTED, cfg
