@@ -445,6 +445,8 @@ def run_ours(args):
                    "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                    "steps": e2e["steps"]}
 
+    chain = None if (args.skip_chain or rank != 0) else run_chain(sgr, device, stream)
+
     if rank != 0:
         return 0
 
@@ -496,6 +498,7 @@ def run_ours(args):
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e_out,
+        "chain": chain,
         "gpu_launches": args.steps * launches_per_step,
         "clocks": clk,
         "peaks": {"hbm_gbs": peaks["hbm_gbs"], "source": peak_src},
@@ -506,6 +509,39 @@ def run_ours(args):
 
         dist.destroy_process_group()
     return 0
+
+
+def run_chain(sgr, device, stream, layers: int = 8, M: int = 4, replays: int = 50, repeats: int = 9):
+    """The chain of dependent projections: layer i reads A_i = Y_{i-1}[:, :K]
+    (row stride N) and its own W_i (8 distinct weights, 411 MB, so none is in
+    L2) and R_i; one CUDA graph of all layers, timed with programmatic
+    dependent launch on and off.  Returns us per layer for both."""
+    import torch
+
+    from skinny_bf16_gemm_residual_gb300 import inputs
+
+    Ws = [inputs.make_weights(N_DIM, K_DIM, seed=1000 + i).to(device) for i in range(layers)]
+    Rs = [inputs.make_rows(M, N_DIM, seed=2000 + i).to(device) for i in range(layers)]
+    A0 = inputs.make_rows(M, K_DIM, seed=3000).to(device)
+    Ys = [torch.empty((M, N_DIM), dtype=torch.bfloat16, device=device) for _ in range(layers)]
+    out = {}
+    for name, flags in (("pdl", 0), ("no_pdl", sgr.SGR_FLAG_NO_PDL)):
+        def layer(i, flags=flags):
+            A = A0 if i == 0 else Ys[i - 1][:, :K_DIM]
+            return lambda: sgr.skinny_gemm_residual_ex(A, Ws[i], Rs[i], Ys[i], flags=flags, stream=stream)
+
+        g = capture([layer(i) for i in range(layers)], stream)
+        with torch.cuda.stream(stream):
+            for _ in range(5):
+                g.replay()
+        stream.synchronize()
+        samples = [t / layers for t in time_graph(g, stream, replays, repeats)]
+        out[name] = summarize(samples)["median_us"]
+        del g
+    gbs = alg_bytes(M) / (out["pdl"] * 1e-6) / 1e9
+    return {"layers": layers, "m": M, "us_per_layer": out["pdl"], "us_per_layer_no_pdl": out["no_pdl"],
+            "pdl_saving_us": out["no_pdl"] - out["pdl"], "gbs": gbs,
+            "note": "graph of 8 dependent calls, A_i = Y_{i-1}[:, :K] (lda = N), distinct W_i"}
 
 
 def run_e2e(sgr, per_m, Ws, m_list, device, stream, steps: int):
@@ -576,6 +612,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--skip-per-m", action="store_true", help="skip the per-M repeat/replay timing")
     ap.add_argument("--skip-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--skip-chain", action="store_true", help="skip the 8-layer dependent chain leg")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
