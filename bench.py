@@ -46,11 +46,24 @@ KERNEL_NAMES = {"simt": "simt_skinny_kernel", "tc": "tc_skinny_kernel", "rows": 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
-def alg_bytes(M: int, N: int = N_DIM, K: int = K_DIM) -> int:
+def set_shape(n: int, k: int) -> None:
+    """Another projection shape (e.g. the down-projection, --n 3584 --k 7168):
+    every leg runs on it and the metric names it."""
+    global N_DIM, K_DIM, METRIC
+    if (n, k) != (N_DIM, K_DIM):
+        METRIC = METRIC.replace(f"N{N_DIM} K{K_DIM}", f"N{n} K{k}")
+        N_DIM, K_DIM = n, k
+
+
+def alg_bytes(M: int, N: int | None = None, K: int | None = None) -> int:
+    N = N_DIM if N is None else N
+    K = K_DIM if K is None else K
     return 2 * (N * K + M * K + 2 * M * N)
 
 
-def alg_flops(M: int, N: int = N_DIM, K: int = K_DIM) -> int:
+def alg_flops(M: int, N: int | None = None, K: int | None = None) -> int:
+    N = N_DIM if N is None else N
+    K = K_DIM if K is None else K
     return 2 * M * N * K
 
 
@@ -60,7 +73,9 @@ def tensor_bound(M: int, peaks: dict) -> bool:
     return alg_flops(M) / (peaks["bf16_tflops"] * 1e12) > alg_bytes(M) / (peaks["hbm_gbs"] * 1e9)
 
 
-def alg_flops(M: int, N: int = N_DIM, K: int = K_DIM) -> int:
+def alg_flops(M: int, N: int | None = None, K: int | None = None) -> int:
+    N = N_DIM if N is None else N
+    K = K_DIM if K is None else K
     return 2 * M * N * K
 
 
@@ -613,9 +628,12 @@ def main(argv=None):
     ap.add_argument("--skip-per-m", action="store_true", help="skip the per-M repeat/replay timing")
     ap.add_argument("--skip-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--skip-chain", action="store_true", help="skip the 8-layer dependent chain leg")
+    ap.add_argument("--n", type=int, default=7168, help="output features (the headline shape is 7168)")
+    ap.add_argument("--k", type=int, default=3584, help="input features (the headline shape is 3584)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    set_shape(args.n, args.k)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -256,22 +256,26 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
     // ------------------------------------------------------------ epilogue
     pdl_wait();  // R may come from the preceding kernel; Y may be read by it
     const int q = warp & 3;       // TMEM lane quarter this warp may access
-    if (p.NT == kRowsPrefetchTokens && p.groups <= 2 && p.groups * p.RB <= kTcTileRows) {
-      // Decode epilogue (at most 16 tokens, at most two packed groups): the
-      // thread on TMEM lane r < RB owns output column n0 + r and holds group
-      // 0's partial sums; the thread on lane RB + r holds group 1's and hands
-      // them over through shared memory.  Everything but the TMEM load, one
-      // exchange and the stores is done before the accumulator is ready.
+    if (p.NT == kRowsPrefetchTokens && p.groups * p.RB <= kTcTileRows) {
+      // Decode epilogue (at most 16 tokens): the thread on TMEM lane r < RB
+      // owns output column n0 + r and holds packed group 0's partial sums;
+      // the thread on lane g*RB + r (g = 1 .. G-1) holds group g's and hands
+      // them over through shared memory; the owner adds them in g order.
+      // Everything but the TMEM load, one exchange and the stores is done
+      // before the accumulator is ready.
       const int L = q * 32 + lane;
       const int G = p.groups;
-      const bool owner = L < p.RB && n0 + L < p.N;
-      const bool helper = G == 2 && L >= p.RB && L < 2 * p.RB;
-      const int r = owner ? L : L - p.RB;
-      const uint32_t xch = w_ring + (uint32_t)(helper || owner ? r : 0) * 80u;  // drained ring: 16 floats + pad per row
+      const int g = L / p.RB;  // packed group of this lane (>= G: unused lane)
+      const int r = L - g * p.RB;
+      const bool owner = g == 0 && n0 + r < p.N;
+      const bool helper = g >= 1 && g < G;
+      // drained ring: [G-1][RB] rows of 16 floats + 4 pad
+      const uint32_t xch0 = w_ring + (uint32_t)r * 80u;
+      const uint32_t xstep = (uint32_t)p.RB * 80u;
       float res[kRowsPrefetchTokens];
 #pragma unroll
       for (int m = 0; m < kRowsPrefetchTokens; ++m)
-        res[m] = (owner && m < p.M) ? __bfloat162float(p.R[(size_t)m * p.ldr + n0 + L]) : 0.f;
+        res[m] = (owner && m < p.M) ? __bfloat162float(p.R[(size_t)m * p.ldr + n0 + r]) : 0.f;
       bool ok = mbar_wait_or_abort(smem_u32(acc_full), 0, abort_flag);
       if (!ok) {
         if (!*abort_flag) report_error(p.err, kErrWaitMma);
@@ -283,37 +287,38 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
 #pragma unroll
       for (int i = 0; i < 16; ++i) v[i] = 0.f;
       if (ok && q * 32 < G * p.RB) {  // warp-uniform: this warp holds rows of the MMA window in use
+        // The warp's lanes hold groups glo .. ghi: load their columns
+        // (16 per group) and keep this lane's.
         const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16);
-        if (G == 1 || (q + 1) * 32 <= p.RB) {
-          tmem_ld16(taddr, v);  // group-0 columns only
-        } else if (q * 32 >= p.RB) {
-          tmem_ld16(taddr + 16u, v);  // group-1 columns only
-        } else {
-          float v1[16];
-          tmem_ld16(taddr, v);
-          tmem_ld16(taddr + 16u, v1);
-          if (L >= p.RB) {
+        const int glo = (q * 32) / p.RB;
+        const int ghi = min(G - 1, (q * 32 + 31) / p.RB);
+        for (int gg = glo; gg <= ghi; ++gg) {
+          float w[16];
+          tmem_ld16(taddr + (uint32_t)(gg * 16), w);  // warp-collective
+          if (gg == g) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = v1[i];
+            for (int i = 0; i < 16; ++i) v[i] = w[i];
           }
         }
       }
       if (ok && helper) {
+        const uint32_t dst = xch0 + (uint32_t)(g - 1) * xstep;
 #pragma unroll
         for (int i = 0; i < 16; i += 4)
-          asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(xch + (uint32_t)i * 4u), "f"(v[i]),
+          asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(dst + (uint32_t)i * 4u), "f"(v[i]),
                        "f"(v[i + 1]), "f"(v[i + 2]), "f"(v[i + 3])
                        : "memory");
       }
       named_bar_sync(1, 128);
       if (ok && owner) {
-        if (G == 2) {
+        for (int gg = 1; gg < G; ++gg) {
+          const uint32_t src = xch0 + (uint32_t)(gg - 1) * xstep;
 #pragma unroll
           for (int i = 0; i < 16; i += 4) {
             float a0, a1, a2, a3;
             asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
                          : "=f"(a0), "=f"(a1), "=f"(a2), "=f"(a3)
-                         : "r"(xch + (uint32_t)i * 4u)
+                         : "r"(src + (uint32_t)i * 4u)
                          : "memory");
             v[i] += a0;
             v[i + 1] += a1;
@@ -321,7 +326,7 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
             v[i + 3] += a3;
           }
         }
-        __nv_bfloat16* yp = p.Y + n0 + L;
+        __nv_bfloat16* yp = p.Y + n0 + r;
 #pragma unroll
         for (int m = 0; m < kRowsPrefetchTokens; ++m)
           if (m < p.M) yp[(size_t)m * p.ldy] = __float2bfloat16_rn(v[m] + res[m]);

@@ -61,6 +61,40 @@ def test_parity_full_size_every_element(M, seed):
     assert m["cosine"] > 0.999
 
 
+# The down-projection of the same block (K = 7168 -> N = 3584): the row slab
+# holds 24 weight rows per CTA there, so four K blocks share one MMA.
+N_DOWN, K_DOWN = 3584, 7168
+
+
+@pytest.mark.parametrize("M", [1, 2, 4, 8, 16, 32, 64, 128])
+def test_parity_down_projection_every_element(M):
+    p = inputs.make_problem(M, N_DOWN, K_DOWN, seed=500 + M)
+    m = compare(run_gpu(p), oracle_full(p.A, p.W, p.R), f"down M={M}")
+    assert m["cosine"] > 0.999
+
+
+@pytest.mark.parametrize("M", [256, 512, 1024])
+def test_parity_down_projection_sampled(M):
+    import oracle
+
+    p = inputs.make_problem(M, N_DOWN, K_DOWN, seed=500 + M)
+    got = run_gpu(p)
+    rng = np.random.default_rng(M)
+    ms = np.concatenate([rng.integers(0, M, 5000), np.zeros(N_DOWN, int), np.full(N_DOWN, M - 1)])
+    ns = np.concatenate([rng.integers(0, N_DOWN, 5000), np.arange(N_DOWN), np.arange(N_DOWN)])
+    compare(got[ms, ns], oracle.load().sample(p.A, p.W, p.R, ms, ns), f"down M={M} sampled")
+
+
+@pytest.mark.parametrize("kb,stages", [(4, 4), (8, 3), (8, 2), (2, 6)])
+@pytest.mark.parametrize("M", [1, 7, 16])
+def test_parity_down_projection_rows_packing(kb, stages, M):
+    """Row slab with 24 rows: 4 (kb = 4, 8) or 2 (kb = 2) K blocks per MMA,
+    combined by the decode epilogue."""
+    p = inputs.make_problem(M, N_DOWN, K_DOWN, seed=600 + M + kb)
+    cfg = sgr.make_config(path=sgr.SGR_PATH_TC_ROWS, k_blocks_per_stage=kb, stages=stages)
+    compare(run_gpu(p, config=cfg), oracle_full(p.A, p.W, p.R), f"down rows M={M} kb={kb}")
+
+
 @pytest.mark.parametrize("M", [3, 5, 6, 7, 9, 12, 15])
 def test_parity_full_size_odd_m(M):
     p = inputs.make_problem(M, N_FULL, K_FULL, seed=100 + M)
