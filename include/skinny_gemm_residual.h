@@ -222,6 +222,43 @@ int skinny_gemm_residual_noalloc(const void* A, int64_t lda, const void* W,
                                  const void* R, int64_t ldr, void* Y, int64_t ldy,
                                  int M, int N, int K, unsigned flags, void* stream);
 
+/*
+ * One problem of a grouped call (an expert of a mixture-of-experts layer):
+ * its activations A [M, K] (row stride lda), weights W [N, K] (contiguous),
+ * residual R and output Y [M, N] (row strides ldr, ldy), all device pointers
+ * owned by the caller with the same rules as skinny_gemm_residual_ex.
+ * M = 0 (no token routed to this expert) is allowed and skipped: its W is not
+ * read.
+ */
+typedef struct {
+  const void* A;
+  int64_t lda;
+  const void* W;
+  const void* R;
+  int64_t ldr;
+  void* Y;
+  int64_t ldy;
+  int M;
+  int reserved; /* must be zero */
+} sgr_group;
+
+/*
+ * Y_g = bf16(A_g . W_g^T + R_g) for every group g, all with the same N and K,
+ * in one kernel launch (per 32 groups with M > 0): the grouped expert GEMM of
+ * the bitsandbytes "QLORA-2" comparison page (QLORA_GUIDE.md, "Grouped Expert
+ * GEMM": all active experts batched into one launch so that the SMs stay
+ * busy), here for BF16 weights on the row-slab kernel.  Each group's M must
+ * be at most 256 (decode-sized expert batches); the launch configuration is
+ * the library's choice for the largest M (or `cfg`, path SGR_PATH_AUTO or
+ * SGR_PATH_TC_ROWS).  Errors as for skinny_gemm_residual_ex, checked for
+ * every group before anything is enqueued; in addition SGR_ERR_ALIAS when a
+ * group's Y overlaps another group's A, W, R or Y, and SGR_ERR_UNSUPPORTED for
+ * num_groups < 0 or a group with M > 256.  `groups` is a host array read
+ * during the call only.  Returns an sgr_status.
+ */
+int skinny_gemm_residual_grouped(const sgr_group* groups, int num_groups, int N, int K,
+                                 const sgr_config* cfg, unsigned flags, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

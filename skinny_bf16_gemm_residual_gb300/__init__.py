@@ -42,6 +42,9 @@ from .binding import (  # noqa: F401
     skinny_gemm_residual_ex,
     skinny_gemm_residual_ex_ptr,
     skinny_gemm_residual_noalloc,
+    skinny_gemm_residual_grouped,
+    skinny_gemm_residual_grouped_ptr,
+    sgr_group,
     skinny_gemm_residual_noalloc_ptr,
     skinny_gemm_residual_ptr,
 )

@@ -34,6 +34,12 @@ SGR_PATH_TC_ROWS = 3
 SGR_PATH_TILE = 4
 
 
+class sgr_group(ctypes.Structure):
+    _fields_ = [("A", ctypes.c_void_p), ("lda", ctypes.c_int64), ("W", ctypes.c_void_p),
+                ("R", ctypes.c_void_p), ("ldr", ctypes.c_int64), ("Y", ctypes.c_void_p),
+                ("ldy", ctypes.c_int64), ("M", ctypes.c_int), ("reserved", ctypes.c_int)]
+
+
 class SgrError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
@@ -71,6 +77,7 @@ EXPORTS = (
     "sgr_status_string",
     "sgr_abi_version",
     "skinny_gemm_residual_noalloc",
+    "skinny_gemm_residual_grouped",
 )
 
 
@@ -106,6 +113,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.sgr_status_string.restype = ctypes.c_char_p
         lib.sgr_abi_version.argtypes = []
         lib.skinny_gemm_residual_noalloc.argtypes = [vp, i64, vp, vp, i64, vp, i64, I, I, I, U, vp]
+        lib.skinny_gemm_residual_grouped.argtypes = [ctypes.POINTER(sgr_group), I, I, I,
+                                                     ctypes.POINTER(sgr_config), U, vp]
         for name in EXPORTS:
             if name != "sgr_status_string":
                 getattr(lib, name).restype = ctypes.c_int
@@ -304,6 +313,48 @@ def skinny_gemm_residual_noalloc(A, W, R, Y, flags: int = 0, stream=None):
     if rc != SGR_OK:
         raise SgrError(rc, "skinny_gemm_residual_noalloc")
     return Y
+
+
+def skinny_gemm_residual_grouped_ptr(groups, N: int, K: int, config: sgr_config | None = None,
+                                     flags: int = 0, stream: int = 0) -> int:
+    """Grouped entry point on an array of sgr_group (raw device addresses);
+    returns the status."""
+    arr = (sgr_group * max(1, len(groups)))(*groups)
+    cfg = ctypes.byref(config) if config is not None else None
+    return load().skinny_gemm_residual_grouped(arr, len(groups), N, K, cfg, flags, stream)
+
+
+def skinny_gemm_residual_grouped(problems, flags: int = 0, stream=None, config: sgr_config | None = None):
+    """Y_g = bf16(A_g . W_g^T + R_g) for every (A, W, R, Y) in `problems`
+    (the experts of a mixture-of-experts layer: same N and K, own weights and
+    token counts; an A with zero rows skips that expert), in one launch.
+    Y may be None (allocated).  Returns the list of Y."""
+    import torch
+
+    groups, outs = [], []
+    N = K = None
+    for A, W, R, Y in problems:
+        for t, n in ((A, "A"), (W, "W"), (R, "R")):
+            _check_tensor(t, n)
+        M, k = A.shape
+        n_out = W.shape[0]
+        if N is None:
+            N, K = n_out, k
+        if (n_out, W.shape[1], k) != (N, K, K) or tuple(R.shape) != (M, N):
+            raise ValueError("every group needs W [N, K], A [M, K], R [M, N] with one N and K")
+        if not W.is_contiguous():
+            raise ValueError("W must be contiguous [N, K]")
+        if Y is None:
+            Y = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+        _check_tensor(Y, "Y")
+        if tuple(Y.shape) != (M, N):
+            raise ValueError("Y must be [M, N]")
+        groups.append(sgr_group(A.data_ptr(), _ld(A), W.data_ptr(), R.data_ptr(), _ld(R), Y.data_ptr(), _ld(Y), M, 0))
+        outs.append(Y)
+    rc = skinny_gemm_residual_grouped_ptr(groups, N or 0, K or 0, config, flags, _stream_handle(stream))
+    if rc != SGR_OK:
+        raise SgrError(rc, "skinny_gemm_residual_grouped")
+    return outs
 
 
 def make_config(path: int = SGR_PATH_AUTO, ctas_per_sm: int = 0, stages: int = 0,

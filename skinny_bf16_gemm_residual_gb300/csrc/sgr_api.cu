@@ -452,6 +452,77 @@ int run_noalloc(const void* A, long long lda, const void* W, const void* R, long
                         (flags & SGR_FLAG_NO_PDL) == 0, stream);
 }
 
+// ------------------------------------------------------------ grouped launch
+int run_grouped(const sgr_group* groups, int num_groups, int N, int K, const sgr_config* cfg, unsigned flags,
+                void* stream_ptr) {
+  if (num_groups < 0) return SGR_ERR_UNSUPPORTED;
+  if (num_groups > 0 && !groups) return SGR_ERR_NULL;
+  if (cfg && cfg->path != SGR_PATH_AUTO && cfg->path != SGR_PATH_TC_ROWS) return SGR_ERR_UNSUPPORTED;
+  int m_max = 0, active = 0;
+  for (int i = 0; i < num_groups; ++i) {
+    const sgr_group& g = groups[i];
+    if (g.reserved != 0) return SGR_ERR_UNSUPPORTED;
+    int rc = validate(g.A, g.lda, g.W, g.R, g.ldr, g.Y, g.ldy, g.M, N, K);
+    if (rc != SGR_OK) return rc;
+    if (g.M > sgr::kRowsMaxTokens) return SGR_ERR_UNSUPPORTED;
+    if (g.M > 0) {
+      ++active;
+      m_max = g.M > m_max ? g.M : m_max;
+    }
+  }
+  // No group's output may overlap another group's operands.
+  for (int i = 0; i < num_groups; ++i) {
+    const sgr_group& g = groups[i];
+    if (g.M == 0 || N == 0) continue;
+    const Extent ey = extent(g.Y, g.M, g.ldy, N);
+    for (int j = 0; j < num_groups; ++j) {
+      const sgr_group& h = groups[j];
+      if (j == i || h.M == 0) continue;
+      if (overlap(ey, extent(h.Y, h.M, h.ldy, N)) || overlap(ey, extent(h.R, h.M, h.ldr, N))) return SGR_ERR_ALIAS;
+      if (K > 0 && (overlap(ey, extent(h.A, h.M, h.lda, K)) || overlap(ey, extent(h.W, N, K, K)))) return SGR_ERR_ALIAS;
+    }
+  }
+  if (active == 0 || N == 0) return SGR_OK;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  if (K == 0) {  // empty sums: Y = R per group
+    for (int i = 0; i < num_groups; ++i) {
+      const sgr_group& g = groups[i];
+      if (g.M == 0 || g.Y == g.R) continue;
+      if (cudaMemcpy2DAsync(g.Y, (size_t)g.ldy * 2, g.R, (size_t)g.ldr * 2, (size_t)N * 2, (size_t)g.M,
+                            cudaMemcpyDeviceToDevice, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return SGR_ERR_LAUNCH;
+      }
+    }
+    return SGR_OK;
+  }
+  int dev, rc;
+  if ((rc = current_device(&dev)) != SGR_OK) return rc;
+  if ((rc = init_device(dev)) != SGR_OK) return rc;
+  DeviceState& st = g_dev[dev];
+  if (!sgr::rows_supported(st.sms, m_max, N, K)) return SGR_ERR_UNSUPPORTED;
+  sgr_config in = {};
+  if (cfg) in = *cfg;
+  in.path = SGR_PATH_TC_ROWS;
+  sgr_config c;
+  if ((rc = resolve_config(st.sms, m_max, N, K, &in, &c)) != SGR_OK) return rc;
+  // Active groups in launches of up to 32.
+  sgr::RowsGroupArgs batch[sgr::kRowsMaxGroups];
+  int n = 0;
+  for (int i = 0; i <= num_groups; ++i) {
+    if (i < num_groups && groups[i].M > 0) {
+      const sgr_group& g = groups[i];
+      batch[n++] = sgr::RowsGroupArgs{g.A, g.lda, g.W, g.R, g.ldr, g.Y, g.ldy, g.M};
+    }
+    if (n == sgr::kRowsMaxGroups || (i == num_groups && n > 0)) {
+      rc = sgr::rows_grouped_launch(c, st.sms, st.err, batch, n, N, K, (flags & SGR_FLAG_NO_PDL) == 0, stream);
+      if (rc != SGR_OK) return rc;
+      n = 0;
+    }
+  }
+  return SGR_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -588,6 +659,11 @@ const char* sgr_status_string(int status) {
 }
 
 int sgr_abi_version(void) { return SGR_ABI_VERSION; }
+
+int skinny_gemm_residual_grouped(const sgr_group* groups, int num_groups, int N, int K,
+                                 const sgr_config* cfg, unsigned flags, void* stream) {
+  return run_grouped(groups, num_groups, N, K, cfg, flags, stream);
+}
 
 int skinny_gemm_residual_noalloc(const void* A, int64_t lda, const void* W, const void* R,
                                  int64_t ldr, void* Y, int64_t ldy, int M, int N, int K,

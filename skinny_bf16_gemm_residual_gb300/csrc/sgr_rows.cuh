@@ -42,6 +42,8 @@
 // measured slower).
 #pragma once
 
+#include <cstring>
+
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -96,9 +98,19 @@ __host__ __device__ inline size_t rows_stage_floats(int groups, int rb, int nt) 
   return (size_t)groups * rb * (nt + 4);
 }
 
-__global__ void __launch_bounds__(kRowsThreads, 1)
-    rows_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA,
-                       const RowsParams p) {
+// One problem's operands: the tensor maps of W and A (in kernel parameter
+// space) and the residual / output.
+struct RowsIO {
+  const CUtensorMap* tmW;
+  const CUtensorMap* tmA;
+  const __nv_bfloat16* R;
+  __nv_bfloat16* Y;
+  long long ldr, ldy;
+  int M;
+};
+
+// One CTA: the RB-row slab of W starting at row n0 of the problem `io`.
+__device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, int n0) {
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -119,8 +131,9 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
   const uint32_t a_ring = w_ring + (uint32_t)S * w_stage;      // [stages][kbps] A boxes
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * p.RB;
   const int KS = p.k_stages;
+  const CUtensorMap* tmW = io.tmW;
+  const CUtensorMap* tmA = io.tmA;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -138,8 +151,8 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
     tmem_relinquish();
   }
   if (threadIdx.x == 0) {
-    prefetch_tmap(&tmW);
-    prefetch_tmap(&tmA);
+    prefetch_tmap(tmW);
+    prefetch_tmap(tmA);
   }
   tc_fence_before();
   __syncthreads();
@@ -161,13 +174,13 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
         mbar_arrive_expect_tx(fb, stage_bytes);
         const uint32_t ws = w_ring + (uint32_t)s * w_stage;
         for (int j = 0; j < p.kbps; ++j)
-          tma_load_2d(ws + (uint32_t)j * wblk, &tmW, (s * p.kbps + j) * kTcKBlock, n0, fb, pol_w);
+          tma_load_2d(ws + (uint32_t)j * wblk, tmW, (s * p.kbps + j) * kTcKBlock, n0, fb, pol_w);
       }
       pdl_wait();
       for (int s = 0; s < pre; ++s) {
         const uint32_t as = a_ring + (uint32_t)s * a_stage;
         for (int j = 0; j < p.kbps; ++j)
-          tma_load_2d(as + (uint32_t)j * ablk, &tmA, (s * p.kbps + j) * kTcKBlock, 0,
+          tma_load_2d(as + (uint32_t)j * ablk, tmA, (s * p.kbps + j) * kTcKBlock, 0,
                       smem_u32(&full[s]), pol_a);
       }
       // Ring position kept by increments: no integer division on the
@@ -187,9 +200,9 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
         const uint32_t fb = smem_u32(&full[slot]);
         mbar_arrive_expect_tx(fb, stage_bytes);
         for (int j = 0; j < p.kbps; ++j)
-          tma_load_2d(ws + (uint32_t)j * wblk, &tmW, kx + j * kTcKBlock, n0, fb, pol_w);
+          tma_load_2d(ws + (uint32_t)j * wblk, tmW, kx + j * kTcKBlock, n0, fb, pol_w);
         for (int j = 0; j < p.kbps; ++j)
-          tma_load_2d(as + (uint32_t)j * ablk, &tmA, kx + j * kTcKBlock, 0, fb, pol_a);
+          tma_load_2d(as + (uint32_t)j * ablk, tmA, kx + j * kTcKBlock, 0, fb, pol_a);
         issued = s + 1;
         kx += kstep;
         ws += w_stage;
@@ -275,7 +288,7 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
       float res[kRowsPrefetchTokens];
 #pragma unroll
       for (int m = 0; m < kRowsPrefetchTokens; ++m)
-        res[m] = (owner && m < p.M) ? __bfloat162float(p.R[(size_t)m * p.ldr + n0 + r]) : 0.f;
+        res[m] = (owner && m < io.M) ? __bfloat162float(io.R[(size_t)m * io.ldr + n0 + r]) : 0.f;
       bool ok = mbar_wait_or_abort(smem_u32(acc_full), 0, abort_flag);
       if (!ok) {
         if (!*abort_flag) report_error(p.err, kErrWaitMma);
@@ -326,10 +339,10 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
             v[i + 3] += a3;
           }
         }
-        __nv_bfloat16* yp = p.Y + n0 + r;
+        __nv_bfloat16* yp = io.Y + n0 + r;
 #pragma unroll
         for (int m = 0; m < kRowsPrefetchTokens; ++m)
-          if (m < p.M) yp[(size_t)m * p.ldy] = __float2bfloat16_rn(v[m] + res[m]);
+          if (m < io.M) yp[(size_t)m * io.ldy] = __float2bfloat16_rn(v[m] + res[m]);
       }
     } else {
       const int etid = threadIdx.x - 64;
@@ -344,7 +357,7 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
       const bool pre = (p.NT == kRowsPrefetchTokens) && etid < p.RB && n0 + etid < p.N;
 #pragma unroll
       for (int i = 0; i < kRowsPrefetchTokens; ++i)
-        rpre[i] = (pre && i < p.M) ? __bfloat162float(p.R[(size_t)i * p.ldr + n0 + etid]) : 0.f;
+        rpre[i] = (pre && i < io.M) ? __bfloat162float(io.R[(size_t)i * io.ldr + n0 + etid]) : 0.f;
       bool ok = mbar_wait_or_abort(smem_u32(acc_full), 0, abort_flag);
       if (!ok) {
         if (!*abort_flag) report_error(p.err, kErrWaitMma);
@@ -391,15 +404,15 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
           if (pre) {
 #pragma unroll
             for (int i = 0; i < 16; ++i)
-              if (m0 + i < p.M) p.Y[(size_t)(m0 + i) * p.ldy + n] = __float2bfloat16_rn(acc[i] + rpre[i]);
+              if (m0 + i < io.M) io.Y[(size_t)(m0 + i) * io.ldy + n] = __float2bfloat16_rn(acc[i] + rpre[i]);
           } else {
             float rr16[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i)
-              rr16[i] = (m0 + i < p.M) ? __bfloat162float(p.R[(size_t)(m0 + i) * p.ldr + n]) : 0.f;
+              rr16[i] = (m0 + i < io.M) ? __bfloat162float(io.R[(size_t)(m0 + i) * io.ldr + n]) : 0.f;
 #pragma unroll
             for (int i = 0; i < 16; ++i)
-              if (m0 + i < p.M) p.Y[(size_t)(m0 + i) * p.ldy + n] = __float2bfloat16_rn(acc[i] + rr16[i]);
+              if (m0 + i < io.M) io.Y[(size_t)(m0 + i) * io.ldy + n] = __float2bfloat16_rn(acc[i] + rr16[i]);
           }
         }
       }
@@ -413,6 +426,42 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, (uint32_t)p.tmem_cols);
   }
+}
+
+__global__ void __launch_bounds__(kRowsThreads, 1)
+    rows_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA,
+                       const RowsParams p) {
+  const RowsIO io{&tmW, &tmA, p.R, p.Y, p.ldr, p.ldy, p.M};
+  rows_run(p, io, (int)blockIdx.x * p.RB);
+}
+
+// Grouped launch: several independent problems with the same N and K and
+// their own W, A, R, Y and token count (the experts of a mixture-of-experts
+// layer).  CTA b works on slab b / count of problem b % count, so the CTAs
+// that run at the same time stream different problems' weights.
+constexpr int kRowsMaxGroups = 32;
+
+struct RowsGroup {  // the tensor maps keep their own (64-byte or larger) alignment
+  CUtensorMap tmW;
+  CUtensorMap tmA;
+  const __nv_bfloat16* R;
+  __nv_bfloat16* Y;
+  long long ldr, ldy;
+  int M;
+};
+
+struct RowsGroupList {
+  RowsGroup g[kRowsMaxGroups];
+  int count;
+};
+
+__global__ void __launch_bounds__(kRowsThreads, 1)
+    rows_grouped_kernel(const __grid_constant__ RowsGroupList list, const RowsParams p) {
+  const int e = (int)blockIdx.x % list.count;
+  const int slab = (int)blockIdx.x / list.count;
+  const RowsGroup& g = list.g[e];
+  const RowsIO io{&g.tmW, &g.tmA, g.R, g.Y, g.ldr, g.ldy, g.M};
+  rows_run(p, io, slab * p.RB);
 }
 
 // ------------------------------------------------------------------ host side
@@ -491,7 +540,9 @@ inline int rows_plan(const sgr_config& c, int sms, int M, int N, int K, RowsPara
 }
 
 inline cudaError_t rows_init_device() {
-  return set_kernel_smem_attrs(reinterpret_cast<const void*>(rows_skinny_kernel));
+  cudaError_t e = set_kernel_smem_attrs(reinterpret_cast<const void*>(rows_skinny_kernel));
+  if (e == cudaSuccess) e = set_kernel_smem_attrs(reinterpret_cast<const void*>(rows_grouped_kernel));
+  return e;
 }
 
 inline int rows_launch(const sgr_config& c, int sms, unsigned* err, const void* A, long long lda,
@@ -521,6 +572,61 @@ inline int rows_launch(const sgr_config& c, int sms, unsigned* err, const void* 
   lc.attrs = attr;
   lc.numAttrs = pdl ? 1 : 0;
   if (cudaLaunchKernelEx(&lc, rows_skinny_kernel, tmW, tmA, p) != cudaSuccess) {
+    cudaGetLastError();
+    return SGR_ERR_LAUNCH;
+  }
+  return SGR_OK;
+}
+
+// Grouped launch of up to kRowsMaxGroups problems (all with M >= 1, M <= the
+// plan's token tile) sharing N and K; the configuration is planned for the
+// largest M.  One kernel launch; CTA count = slabs x problems.
+struct RowsGroupArgs {
+  const void* A;
+  long long lda;
+  const void* W;
+  const void* R;
+  long long ldr;
+  void* Y;
+  long long ldy;
+  int M;
+};
+
+inline int rows_grouped_launch(const sgr_config& c, int sms, unsigned* err, const RowsGroupArgs* gs, int count,
+                               int N, int K, bool pdl, cudaStream_t stream) {
+  if (count < 1 || count > kRowsMaxGroups) return SGR_ERR_UNSUPPORTED;
+  int m_max = 0;
+  for (int i = 0; i < count; ++i) m_max = gs[i].M > m_max ? gs[i].M : m_max;
+  RowsParams p;
+  int grid = 0;
+  size_t smem = 0;
+  int rc = rows_plan(c, sms, m_max, N, K, &p, &grid, &smem);
+  if (rc != SGR_OK) return rc;
+  p.err = err;
+  RowsGroupList list;
+  std::memset(&list, 0, sizeof list);
+  list.count = count;
+  for (int i = 0; i < count; ++i) {
+    RowsGroup& g = list.g[i];
+    if (!detail::make_tmap(&g.tmW, gs[i].W, N, K, K, p.RB, kTcKBlock)) return SGR_ERR_LAUNCH;
+    if (!detail::make_tmap(&g.tmA, gs[i].A, gs[i].M, K, gs[i].lda, p.NT, kTcKBlock)) return SGR_ERR_LAUNCH;
+    g.R = static_cast<const __nv_bfloat16*>(gs[i].R);
+    g.Y = static_cast<__nv_bfloat16*>(gs[i].Y);
+    g.ldr = gs[i].ldr;
+    g.ldy = gs[i].ldy;
+    g.M = gs[i].M;
+  }
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3((unsigned)(grid * count), 1, 1);
+  lc.blockDim = dim3(kRowsThreads, 1, 1);
+  lc.dynamicSmemBytes = smem;
+  lc.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = pdl ? 1 : 0;
+  if (cudaLaunchKernelEx(&lc, rows_grouped_kernel, list, p) != cudaSuccess) {
     cudaGetLastError();
     return SGR_ERR_LAUNCH;
   }

@@ -122,3 +122,37 @@ def test_table_header_is_sorted_and_covers_the_latent_moe_shape():
     for ms in shapes.values():
         assert ms == sorted(ms)
     assert (7168, 3584) in shapes and shapes[(7168, 3584)][0] == 1
+
+
+# ------------------------------------------------------------ grouped call (host-side checks only)
+def grp(i, M=4, **kw):
+    """Group i with fake addresses spaced 16 GiB apart (never dereferenced)."""
+    off = i << 34
+    f = dict(A=A_ + off, lda=3584, W=W_ + off, R=R_ + off, ldr=7168, Y=Y_ + off, ldy=7168, M=M)
+    f.update(kw)
+    return binding.sgr_group(f["A"], f["lda"], f["W"], f["R"], f["ldr"], f["Y"], f["ldy"], f["M"], 0)
+
+
+def g_call(groups, N=7168, K=3584, n=None):
+    return binding.skinny_gemm_residual_grouped_ptr(groups if n is None else groups[:n], N, K)
+
+
+def test_grouped_rejects_before_launch():
+    assert g_call([grp(0), grp(1, M=257)]) == sgr.SGR_ERR_UNSUPPORTED     # an expert batch above 256 tokens
+    assert g_call([grp(0), grp(1, lda=3588)]) == sgr.SGR_ERR_ALIGN         # one bad group rejects the call
+    assert g_call([grp(0), grp(1, R=0)]) == sgr.SGR_ERR_NULL
+    # group 1 writes into group 0's residual / weights / output
+    assert g_call([grp(0), grp(1, Y=R_)]) == sgr.SGR_ERR_ALIAS
+    assert g_call([grp(0), grp(1, Y=W_)]) == sgr.SGR_ERR_ALIAS
+    assert g_call([grp(0), grp(1, Y=Y_)]) == sgr.SGR_ERR_ALIAS
+    bad = grp(0)
+    bad.reserved = 1
+    assert g_call([bad]) == sgr.SGR_ERR_UNSUPPORTED
+    lib = sgr.load()
+    assert lib.skinny_gemm_residual_grouped(None, 2, 7168, 3584, None, 0, None) == sgr.SGR_ERR_NULL
+    assert lib.skinny_gemm_residual_grouped(None, -1, 7168, 3584, None, 0, None) == sgr.SGR_ERR_UNSUPPORTED
+
+
+def test_grouped_nothing_to_do_needs_no_device():
+    assert g_call([]) == sgr.SGR_OK
+    assert g_call([grp(0, M=0), grp(1, M=0)]) == sgr.SGR_OK   # no expert received a token
