@@ -461,6 +461,7 @@ def run_ours(args):
                    "steps": e2e["steps"]}
 
     chain = None if (args.skip_chain or rank != 0) else run_chain(sgr, device, stream)
+    grouped = None if (args.skip_grouped or rank != 0) else run_grouped(sgr, device, stream)
 
     if rank != 0:
         return 0
@@ -514,6 +515,7 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "e2e": e2e_out,
         "chain": chain,
+        "grouped": grouped,
         "gpu_launches": args.steps * launches_per_step,
         "clocks": clk,
         "peaks": {"hbm_gbs": peaks["hbm_gbs"], "source": peak_src},
@@ -557,6 +559,45 @@ def run_chain(sgr, device, stream, layers: int = 8, M: int = 4, replays: int = 5
     return {"layers": layers, "m": M, "us_per_layer": out["pdl"], "us_per_layer_no_pdl": out["no_pdl"],
             "pdl_saving_us": out["no_pdl"] - out["pdl"], "gbs": gbs,
             "note": "graph of 8 dependent calls, A_i = Y_{i-1}[:, :K] (lda = N), distinct W_i"}
+
+
+def run_grouped(sgr, device, stream, experts: int = 8, tokens: int = 16, top_k: int = 2,
+                replays: int = 50, repeats: int = 9):
+    """Mixture-of-experts step: `tokens` tokens routed top-k over `experts`
+    experts (seeded synthetic routing), each expert its own W_e; one grouped
+    launch versus one call per expert, both in a CUDA graph with PDL."""
+    import numpy as np
+    import torch
+
+    from skinny_bf16_gemm_residual_gb300 import inputs
+
+    rng = np.random.default_rng(2024)
+    choice = np.stack([rng.choice(experts, size=top_k, replace=False) for _ in range(tokens)])
+    counts = np.bincount(choice.ravel(), minlength=experts).tolist()
+    Ws = [inputs.make_weights(N_DIM, K_DIM, seed=4000 + e).to(device) for e in range(experts)]
+    As = [inputs.make_rows(m, K_DIM, seed=5000 + e).to(device) for e, m in enumerate(counts)]
+    Rs = [inputs.make_rows(m, N_DIM, seed=6000 + e).to(device) for e, m in enumerate(counts)]
+    Ys = [torch.empty((m, N_DIM), dtype=torch.bfloat16, device=device) for m in counts]
+    problems = list(zip(As, Ws, Rs, Ys))
+    active = [(A, W, R, Y) for A, W, R, Y in problems if A.shape[0] > 0]
+    nbytes = sum(alg_bytes(A.shape[0]) for A, _, _, _ in active)
+    out = {}
+    for name, calls in (
+            ("grouped", [lambda: sgr.skinny_gemm_residual_grouped(problems, stream=stream)]),
+            ("per_expert", [lambda A=A, W=W, R=R, Y=Y: sgr.skinny_gemm_residual(A, W, R, Y, stream=stream)
+                            for A, W, R, Y in active])):
+        g = capture(calls, stream)
+        with torch.cuda.stream(stream):
+            for _ in range(5):
+                g.replay()
+        stream.synchronize()
+        out[name] = summarize(time_graph(g, stream, replays, repeats))["median_us"]
+        del g
+    return {"experts": experts, "tokens": tokens, "top_k": top_k, "tokens_per_expert": counts,
+            "us_grouped": out["grouped"], "us_per_expert_calls": out["per_expert"],
+            "gbs_grouped": nbytes / (out["grouped"] * 1e-6) / 1e9,
+            "gbs_per_expert_calls": nbytes / (out["per_expert"] * 1e-6) / 1e9,
+            "note": "one step = all experts with tokens; bytes = sum over those experts of 2*(N*K + M*K + 2*M*N)"}
 
 
 def run_e2e(sgr, per_m, Ws, m_list, device, stream, steps: int):
@@ -628,6 +669,7 @@ def main(argv=None):
     ap.add_argument("--skip-per-m", action="store_true", help="skip the per-M repeat/replay timing")
     ap.add_argument("--skip-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--skip-chain", action="store_true", help="skip the 8-layer dependent chain leg")
+    ap.add_argument("--skip-grouped", action="store_true", help="skip the mixture-of-experts grouped leg")
     ap.add_argument("--n", type=int, default=7168, help="output features (the headline shape is 7168)")
     ap.add_argument("--k", type=int, default=3584, help="input features (the headline shape is 3584)")
     args = ap.parse_args(argv)
