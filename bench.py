@@ -232,6 +232,12 @@ def dist_max(value: float, ws: int, device=None) -> float:
     return float(t.item())
 
 
+def job_gbs(bytes_per_step: float, ws: int, steps: int, slowest_ms: float) -> float:
+    """Whole-job throughput: the bytes every rank processed (each rank runs the
+    same step on its own GPU: replicas) over the slowest rank's time."""
+    return bytes_per_step * ws * steps / (slowest_ms * 1e-3) / 1e9
+
+
 def dist_barrier(ws: int):
     if ws > 1:
         import torch.distributed as dist
@@ -449,7 +455,7 @@ def run_ours(args):
     elapsed_ms = ev0.elapsed_time(ev1)
     elapsed_ms = dist_max(elapsed_ms, ws, device)
     ms_per_step = elapsed_ms / args.steps
-    value = bytes_per_step * ws * args.steps / (elapsed_ms * 1e-3) / 1e9
+    value = job_gbs(bytes_per_step, ws, args.steps, elapsed_ms)
 
     # end to end through the public call with host buffers (pinned), W resident
     e2e_out = None
