@@ -339,6 +339,57 @@ __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, 
         for (int m = 0; m < kRowsPrefetchTokens; ++m)
           if (m < io.M) yp[(size_t)m * io.ldy] = __float2bfloat16_rn(v[m] + res[m]);
       }
+    } else if (p.NT == kRowsPrefetchTokens && p.groups == 4 && p.RB == 32) {
+      // 32-row slabs, four packed groups: warp quarter q holds group q whole.
+      // Warps 1-3 hand their partial sums to warp 0's lanes (one output
+      // column each) through shared memory; warp 0 adds them in group order.
+      const bool owner = q == 0 && n0 + lane < p.N;
+      const uint32_t xch = w_ring + (uint32_t)lane * 80u;  // drained ring: [3][32] rows of 16 floats + pad
+      float res[kRowsPrefetchTokens];
+#pragma unroll
+      for (int m = 0; m < kRowsPrefetchTokens; ++m)
+        res[m] = (owner && m < io.M) ? __bfloat162float(io.R[(size_t)m * io.ldr + n0 + lane]) : 0.f;
+      bool ok = mbar_wait_or_abort(smem_u32(acc_full), 0, abort_flag);
+      if (!ok) {
+        if (!*abort_flag) report_error(p.err, kErrWaitMma);
+        *abort_flag = 1;
+      }
+      ok = __all_sync(0xffffffffu, ok);
+      tc_fence_after();
+      float v[16];
+      if (ok) {
+        tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(q * 16), v);
+        if (q > 0) {
+          const uint32_t dst = xch + (uint32_t)(q - 1) * 32u * 80u;
+#pragma unroll
+          for (int i = 0; i < 16; i += 4)
+            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(dst + (uint32_t)i * 4u), "f"(v[i]),
+                         "f"(v[i + 1]), "f"(v[i + 2]), "f"(v[i + 3])
+                         : "memory");
+        }
+      }
+      named_bar_sync(1, 128);
+      if (ok && owner) {
+#pragma unroll
+        for (int gg = 0; gg < 3; ++gg) {
+#pragma unroll
+          for (int i = 0; i < 16; i += 4) {
+            float a0, a1, a2, a3;
+            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(a0), "=f"(a1), "=f"(a2), "=f"(a3)
+                         : "r"(xch + (uint32_t)gg * 32u * 80u + (uint32_t)i * 4u)
+                         : "memory");
+            v[i] += a0;
+            v[i + 1] += a1;
+            v[i + 2] += a2;
+            v[i + 3] += a3;
+          }
+        }
+        __nv_bfloat16* yp = io.Y + n0 + lane;
+#pragma unroll
+        for (int m = 0; m < kRowsPrefetchTokens; ++m)
+          if (m < io.M) yp[(size_t)m * io.ldy] = __float2bfloat16_rn(v[m] + res[m]);
+      }
     } else if (p.NT == kRowsPrefetchTokens && p.groups * p.RB <= kTcTileRows) {
       // The same for three or four packed groups (short slabs, e.g. 24 rows
       // when N = 3584): lane g*RB + r (g = 1 .. G-1) hands group g's partial
@@ -574,7 +625,11 @@ inline int rows_plan(const sgr_config& c, int sms, int M, int N, int K, RowsPara
   if (c.k_blocks_per_stage < 1 || c.k_blocks_per_stage > 8) return SGR_ERR_UNSUPPORTED;
   if (c.ctas_per_sm != 1) return SGR_ERR_UNSUPPORTED;
   if (c.stages < 2 || c.stages > 32) return SGR_ERR_UNSUPPORTED;
-  const int rb = rows_per_cta(sms, N);
+  // W rows per CTA: N / SMs rounded up to 8 unless the configuration names a
+  // slab height (rows_per_stage; e.g. 32 rows: 224 CTAs for N = 7168, two per
+  // SM, four K blocks per MMA).
+  const int rb = c.rows_per_stage > 0 ? c.rows_per_stage : rows_per_cta(sms, N);
+  if (rb % 8 != 0 || rb > kTcTileRows) return SGR_ERR_UNSUPPORTED;
   const size_t sm = rows_smem_bytes(c.stages, c.k_blocks_per_stage, rb, nt);
   if (sm > 232448) return SGR_ERR_UNSUPPORTED;
   const int kstage_elems = kTcKBlock * c.k_blocks_per_stage;

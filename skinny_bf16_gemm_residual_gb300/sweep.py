@@ -42,18 +42,19 @@ def candidate_configs(path: int, M: int, K: int, grid: str) -> list[dict]:
         if M > 256:
             return []
         nt = (M + 15) // 16 * 16
-        rb = 48
-        for kb in (1, 2, 4, 8):
-            for st in (2, 3, 4, 5, 6, 8, 10, 12):
-                slack = max(0, 16384 - rb * 128 - st * kb * nt * 128)
-                smem = 2048 + st * kb * (rb * 128 + nt * 128) + slack
-                if smem > 232448:
-                    continue
-                if grid == "small" and st not in (3, 4, 6):
-                    continue
-                for pf in sorted({st, max(1, st - 1), max(1, st - 2)}):
-                    out.append(dict(path=path, ctas_per_sm=1, k_blocks_per_stage=kb, stages=st,
-                                    prefetch_stages=pf))
+        # slab height: N / SMs (48 at N = 7168), or 32 rows (two CTAs per SM)
+        for rb, cfg_rb in ((48, 0), (32, 32)):
+            for kb in (1, 2, 4, 8):
+                for st in (2, 3, 4, 5, 6, 8, 10, 12):
+                    slack = max(0, 16384 - rb * 128 - st * kb * nt * 128)
+                    smem = 2048 + st * kb * (rb * 128 + nt * 128) + slack
+                    if smem > 232448 or (cfg_rb and (M > 16 or smem > 113 * 1024)):
+                        continue
+                    if grid == "small" and st not in (2, 3, 4, 6):
+                        continue
+                    for pf in sorted({st, max(1, st - 1), max(1, st - 2)}):
+                        out.append(dict(path=path, ctas_per_sm=1, k_blocks_per_stage=kb, stages=st,
+                                        prefetch_stages=pf, rows_per_stage=cfg_rb))
     elif path == sgr.SGR_PATH_TILE:
         if M < 32:
             return []

@@ -85,6 +85,11 @@ ROWS_CONFIGS = [
     dict(k_blocks_per_stage=8, stages=3, prefetch_stages=1),
     dict(k_blocks_per_stage=8, stages=3, prefetch_stages=3),
     dict(k_blocks_per_stage=4, stages=4, prefetch_stages=2),
+    dict(rows_per_stage=32, k_blocks_per_stage=8, stages=2),
+    dict(rows_per_stage=32, k_blocks_per_stage=4, stages=4, prefetch_stages=2),
+    dict(rows_per_stage=24, k_blocks_per_stage=4, stages=3),
+    dict(rows_per_stage=64, k_blocks_per_stage=4, stages=3),
+    dict(rows_per_stage=8, k_blocks_per_stage=8, stages=3),
 ]
 
 
@@ -99,7 +104,7 @@ def test_rows_rejects_bad_config():
     p = inputs.make_problem(20, 256, 256, seed=1)
     A, W, R = (t.cuda() for t in (p.A, p.W, p.R))
     for cfg in (dict(token_tile=16), dict(ctas_per_sm=2), dict(k_blocks_per_stage=8, stages=12),
-                dict(stages=2, prefetch_stages=3)):
+                dict(stages=2, prefetch_stages=3), dict(rows_per_stage=20), dict(rows_per_stage=136)):
         with pytest.raises(sgr.SgrError) as e:
             sgr.skinny_gemm_residual_ex(A, W, R, config=sgr.make_config(path=ROWS, **cfg))
         assert e.value.status == sgr.SGR_ERR_UNSUPPORTED
