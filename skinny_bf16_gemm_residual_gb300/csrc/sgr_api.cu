@@ -239,6 +239,7 @@ int resolve_config(int dev_sms, int M, int N, int K, const sgr_config* in, sgr_c
       if (path == SGR_PATH_TC_ROWS || path == SGR_PATH_TILE) out->prefetch_stages = e->prefetch_stages;
       if (path == SGR_PATH_TILE && e->tile_n) out->tile_n = e->tile_n;
       if (path == SGR_PATH_TILE) out->k_split = e->k_split > 0 ? e->k_split : 1;
+      if (path == SGR_PATH_TILE) out->pair_w = e->pair_w;
     }
   }
   if (in) {
@@ -251,8 +252,11 @@ int resolve_config(int dev_sms, int M, int N, int K, const sgr_config* in, sgr_c
     if (in->token_tile) out->token_tile = in->token_tile;
     if (in->prefetch_stages) out->prefetch_stages = in->prefetch_stages;
     if (in->tile_n) out->tile_n = in->tile_n;
+    // A chosen tile width runs unsplit and unpaired unless those are asked for too.
     if (in->k_split) out->k_split = in->k_split;
-    else if (path == SGR_PATH_TILE && in->tile_n) out->k_split = 1;  // a chosen width runs unsplit unless asked
+    else if (path == SGR_PATH_TILE && in->tile_n) out->k_split = 1;
+    if (in->pair_w) out->pair_w = in->pair_w;
+    else if (path == SGR_PATH_TILE && (in->tile_n || in->k_split)) out->pair_w = 0;
     // A tile width chosen without a ring depth gets the deepest ring that fits it.
     if (path == SGR_PATH_TILE && (in->tile_n || in->k_blocks_per_stage) && !in->stages)
       out->stages = sgr::tile_default_stages(out->tile_n, out->k_blocks_per_stage > 0 ? out->k_blocks_per_stage : 1);
@@ -623,12 +627,12 @@ int sgr_kernel_resources(int device, int path, int M, int N, int K, int* regs, i
     *smem_bytes = (int)smem;
     *threads = sgr::kRowsThreads;
   } else if (c.path == SGR_PATH_TILE) {
-    if (cudaFuncGetAttributes(&fa, sgr::tile_kernel_for(c.tile_n, c.k_split > 0 ? c.k_split : 1)) != cudaSuccess) {
+    if (cudaFuncGetAttributes(&fa, sgr::tile_kernel_for(c.tile_n, sgr::tile_mode(c))) != cudaSuccess) {
       cudaGetLastError();
       return SGR_ERR_DEVICE;
     }
     *smem_bytes = (int)sgr::tile_smem_bytes(c.stages, c.tile_n, c.k_blocks_per_stage > 0 ? c.k_blocks_per_stage : 1);
-    *threads = sgr::kTileThreads;
+    *threads = sgr::tile_threads(sgr::tile_mode(c));
   } else {
     int s = 0, t = 0;
     const void* fn = sgr::tc_kernel_for(M, N, K, &c, &s, &t);

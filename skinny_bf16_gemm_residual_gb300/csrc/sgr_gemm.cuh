@@ -177,6 +177,26 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
   }
 }
 
+// 2-D tensor copy global -> the same shared-memory offset in every CTA of
+// `mask` (cluster multicast), completion counted on the mbarrier at the same
+// offset in each of them.
+__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const void* tmap, int32_t x, int32_t y,
+                                                      uint32_t bar, uint16_t mask, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(dst),
+      "l"(tmap), "r"(x), "r"(y), "r"(bar), "h"(mask), "l"(policy)
+      : "memory");
+}
+
+// Arrive on the mbarrier at `bar`'s offset in every CTA of `mask` once all
+// prior tcgen05 operations of this thread have completed.
+__device__ __forceinline__ void mma_commit_multicast(uint32_t bar, uint16_t mask) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+               "h"(mask)
+               : "memory");
+}
+
 // All threads of every CTA of the cluster.
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -194,19 +214,38 @@ __device__ __forceinline__ void load_residual_row(const TileParams& p, int m, in
     rv[j] = (row_ok && n0 + 8 * j < p.N) ? *reinterpret_cast<const uint4*>(src + 8 * j) : make_uint4(0u, 0u, 0u, 0u);
 }
 
-// KSPLIT = 1: persistent CTAs, each tile's whole K in one CTA.
-// KSPLIT = 2: one tile per 2-CTA cluster, rank 0 accumulating K blocks
+// Modes (template parameter MODE):
+// kTilePlain: persistent CTAs, each tile's whole K in one CTA.
+// kTilePairW: persistent 2-CTA clusters on the two token tiles 2i, 2i+1 of
+// the same W column tile; each rank loads half of every W box and multicasts
+// it to both, so each W byte leaves L2 once per pair (the operand feed from
+// L2, not the tensor core, bounds large tiles); the MMA's stage release is
+// multicast too, so a slot is reloaded only when both ranks are done with it.
+// kTileSplitK: one tile per 2-CTA cluster, rank 0 accumulating K blocks
 // [0, kb_split) and rank 1 the rest; at the end each rank sends the half of
 // its accumulator that the other rank owns through distributed shared memory
 // (into the other rank's drained ring), adds the half it received to its own
 // and stores that half of the tile.  (a + b is the same in either order, so
 // the result does not depend on which rank finishes first.)  This doubles
 // the CTAs working on a problem with few tiles (M <= 256 at N = 7168).
-template <int NT, int KSPLIT>
-__global__ void __launch_bounds__(kTileThreads, 1)
+enum : int { kTilePlain = 1, kTileSplitK = 2, kTilePairW = 3 };
+
+// Threads per CTA: producer warp, MMA warp, four epilogue warps.  (A second
+// MMA-issuing warp taking every other ring slot into its own accumulator was
+// measured 1-4% slower here: with the whole ring in flight the K-block rate
+// is set by the operand latency, not by the issuing thread's loop.)
+__host__ __device__ constexpr int tile_threads(int mode) { return (void)mode, kTileThreads; }
+
+template <int NT, int MODE>
+__global__ void __launch_bounds__(tile_threads(MODE), 1)
     tile_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                      const TileParams p) {
-  static_assert(KSPLIT == 1 || (KSPLIT == 2 && (NT / 2) % 32 == 0), "split tiles hand over 32-column chunks");
+  constexpr int KSPLIT = MODE == kTileSplitK ? 2 : 1;
+  constexpr bool PAIR = MODE == kTilePairW;
+  constexpr int CL = MODE == kTilePlain ? 1 : 2;  // CTAs per cluster
+
+  static_assert(MODE != kTileSplitK || (NT / 2) % 32 == 0, "split tiles hand over 32-column chunks");
+  static_assert(!PAIR || (NT / 2) % 8 == 0, "each rank's half W box is whole 8-row swizzle atoms");
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -229,10 +268,13 @@ __global__ void __launch_bounds__(kTileThreads, 1)
   const uint32_t ring = base + 1024;  // [S] x {KP A boxes, KP W boxes}
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t rank = KSPLIT == 2 ? cluster_ctarank() : 0u;
-  const int G = (int)gridDim.x / KSPLIT;      // tile-processing units (CTAs or clusters)
-  const int unit = (int)blockIdx.x / KSPLIT;  // this CTA's unit
-  const int tiles = p.m_tiles * p.n_tiles;
+  const uint32_t rank = CL == 2 ? cluster_ctarank() : 0u;
+  const int G = (int)gridDim.x / CL;      // tile-processing units (CTAs or clusters)
+  const int unit = (int)blockIdx.x / CL;  // this CTA's unit
+  // Tiles of a unit: plain / split: (token tile, W column tile); pair: (pair
+  // of token tiles, W column tile), this rank taking token tile 2 i + rank.
+  const int mt_u = PAIR ? p.m_tiles / 2 : p.m_tiles;
+  const int tiles = mt_u * p.n_tiles;
   const int my_tiles = (tiles - unit + G - 1) / G;  // >= 1: units <= tiles; 1 when split
   const int kb0 = (KSPLIT == 2 && rank == 1) ? p.kb_split : 0;
   const int KB = (KSPLIT == 2 && rank == 0) ? p.kb_split : p.k_blocks - kb0;  // K blocks of this CTA
@@ -241,7 +283,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
-      mbar_init(smem_u32(&empty[s]), 1);
+      mbar_init(smem_u32(&empty[s]), PAIR ? 2 : 1);  // pair: both ranks' MMAs release a slot
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&acc_full[b]), 1);
@@ -265,7 +307,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if constexpr (KSPLIT == 2) cluster_sync_all();  // the other rank's barriers exist before any remote arrive
+  if constexpr (CL == 2) cluster_sync_all();  // the other rank's barriers exist before any remote access
   const uint32_t tmem = *tmem_slot;
   pdl_launch_dependents();  // the dependent grid still waits for our completion before reading
 
@@ -285,8 +327,8 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         c.kx = kb0 * kTcKBlock;
         c.kb = 0;
         c.t = unit;
-        c.m0 = (c.t % p.m_tiles) * kTileM;
-        c.n0 = (c.t / p.m_tiles) * NT;
+        c.m0 = ((c.t % mt_u) * (PAIR ? 2 : 1) + (int)rank * (PAIR ? 1 : 0)) * kTileM;
+        c.n0 = (c.t / mt_u) * NT;
       };
       auto advance = [&](Cursor& c) {
         c.kx += KP * kTcKBlock;
@@ -294,9 +336,19 @@ __global__ void __launch_bounds__(kTileThreads, 1)
           c.kb = 0;
           c.kx = kb0 * kTcKBlock;
           c.t += G;
-          c.m0 = (c.t % p.m_tiles) * kTileM;
-          c.n0 = (c.t / p.m_tiles) * NT;
+          c.m0 = ((c.t % mt_u) * (PAIR ? 2 : 1) + (int)rank * (PAIR ? 1 : 0)) * kTileM;
+          c.n0 = (c.t / mt_u) * NT;
         }
+      };
+      // W box j of a stage; a pair rank loads its half of the rows into both
+      // ranks' shared memory.
+      auto load_w = [&](uint32_t stage, int j, int kx, int n0, uint32_t fb) {
+        const uint32_t dst = stage + a_part + (uint32_t)j * w_box;
+        if constexpr (PAIR)
+          tma_load_2d_multicast(dst + rank * (uint32_t)(NT / 2) * 128u, &tmW, kx + j * kTcKBlock,
+                                n0 + (int)rank * (NT / 2), fb, (uint16_t)0x3, pol_w);
+        else
+          tma_load_2d(dst, &tmW, kx + j * kTcKBlock, n0, fb, pol_w);
       };
       const int pre = total < p.prefetch ? total : p.prefetch;  // <= S: slots 0 .. pre-1
       Cursor c;
@@ -304,9 +356,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
       for (int it = 0; it < pre; ++it, advance(c)) {
         const uint32_t fb = smem_u32(&full[it]);
         mbar_arrive_expect_tx(fb, stage_bytes);
-        for (int j = 0; j < KP; ++j)
-          tma_load_2d(ring + (uint32_t)it * stage_bytes + a_part + (uint32_t)j * w_box, &tmW,
-                      c.kx + j * kTcKBlock, c.n0, fb, pol_w);
+        for (int j = 0; j < KP; ++j) load_w(ring + (uint32_t)it * stage_bytes, j, c.kx, c.n0, fb);
       }
       pdl_wait();
       {
@@ -332,7 +382,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         mbar_arrive_expect_tx(fb, stage_bytes);
         for (int j = 0; j < KP; ++j) {
           tma_load_2d(st + (uint32_t)j * a_box, &tmA, c.kx + j * kTcKBlock, c.m0, fb, pol_a);
-          tma_load_2d(st + a_part + (uint32_t)j * w_box, &tmW, c.kx + j * kTcKBlock, c.n0, fb, pol_w);
+          load_w(st, j, c.kx, c.n0, fb);
         }
         issued = it + 1;
         soff += stage_bytes;
@@ -381,7 +431,10 @@ __global__ void __launch_bounds__(kTileThreads, 1)
               mma_bf16(d, adesc0 + ao + (uint64_t)(kk * 2), wdesc0 + wo + (uint64_t)(kk * 2), idesc,
                        (ks | j | kk) != 0 ? 1u : 0u);
           }
-          mma_commit(smem_u32(&empty[slot]));
+          if constexpr (PAIR)
+            mma_commit_multicast(smem_u32(&empty[slot]), (uint16_t)0x3);
+          else
+            mma_commit(smem_u32(&empty[slot]));
           doff += dstep;
           if (++slot == S) {
             slot = 0;
@@ -398,13 +451,14 @@ __global__ void __launch_bounds__(kTileThreads, 1)
       mma_commit(smem_u32(drain));
       if (!mbar_wait(smem_u32(drain), 0)) report_error(p.err, kErrDrain);
     }
-  } else if constexpr (KSPLIT == 1) {
+  } else if constexpr (KSPLIT == 1) {  // plain and pair
     // ------------------------------------------------------------ epilogue
     pdl_wait();  // R may come from the preceding kernel; Y may be read by it
     const int q = warp & 3;  // TMEM lane quarter = tile rows [32 q, 32 q + 32)
+    const int mstep = PAIR ? 2 : 1, moff = PAIR ? (int)rank : 0;
     int t = unit;
-    int m = (t % p.m_tiles) * kTileM + q * kTileEpiRows + lane;  // this thread's output row
-    int n0 = (t / p.m_tiles) * NT;
+    int m = ((t % mt_u) * mstep + moff) * kTileM + q * kTileEpiRows + lane;  // this thread's output row
+    int n0 = (t / mt_u) * NT;
     uint4 rv[NT / 8];
     load_residual_row<NT>(p, m, n0, rv);
     for (int i = 0; i < my_tiles; ++i) {
@@ -438,8 +492,8 @@ __global__ void __launch_bounds__(kTileThreads, 1)
       if (lane == 0) mbar_arrive(smem_u32(&acc_empty[buf]));
       if (i + 1 < my_tiles) {  // next tile's residuals arrive during its main loop
         t += G;
-        m = (t % p.m_tiles) * kTileM + q * kTileEpiRows + lane;
-        n0 = (t / p.m_tiles) * NT;
+        m = ((t % mt_u) * mstep + moff) * kTileM + q * kTileEpiRows + lane;
+        n0 = (t / mt_u) * NT;
         load_residual_row<NT>(p, m, n0, rv);
       }
     }
@@ -528,7 +582,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
   }
   // No rank leaves while the other may still write into its shared memory or
   // arrive on its barriers.
-  if constexpr (KSPLIT == 2) cluster_sync_all();
+  if constexpr (CL == 2) cluster_sync_all();
 }
 
 // ------------------------------------------------------------------ host side
@@ -584,32 +638,39 @@ inline void tile_default_config(int sms, int M, int N, int K, sgr_config* c) {
   c->rows_per_stage = 0;
 }
 
-// The kernel instantiation for a tile width and K split (nullptr if none).
-inline const void* tile_kernel_for(int nt, int split) {
-  if (split == 1) {
-    switch (nt) {
-      case 64: return reinterpret_cast<const void*>(tile_gemm_kernel<64, 1>);
-      case 128: return reinterpret_cast<const void*>(tile_gemm_kernel<128, 1>);
-      case 192: return reinterpret_cast<const void*>(tile_gemm_kernel<192, 1>);
-      case 256: return reinterpret_cast<const void*>(tile_gemm_kernel<256, 1>);
-      default: return nullptr;
-    }
+// The kernel instantiation for a tile width and mode (nullptr if none).
+template <int MODE>
+inline const void* tile_kernel_mode(int nt) {
+  switch (nt) {
+    case 64: return reinterpret_cast<const void*>(tile_gemm_kernel<64, MODE>);
+    case 128: return reinterpret_cast<const void*>(tile_gemm_kernel<128, MODE>);
+    case 192: return reinterpret_cast<const void*>(tile_gemm_kernel<192, MODE>);
+    case 256: return MODE == kTileSplitK ? nullptr : reinterpret_cast<const void*>(tile_gemm_kernel<256, MODE>);
+    default: return nullptr;
   }
-  if (split == 2) {
-    switch (nt) {
-      case 64: return reinterpret_cast<const void*>(tile_gemm_kernel<64, 2>);
-      case 128: return reinterpret_cast<const void*>(tile_gemm_kernel<128, 2>);
-      case 192: return reinterpret_cast<const void*>(tile_gemm_kernel<192, 2>);
-      default: return nullptr;
-    }
-  }
+}
+
+inline const void* tile_kernel_for(int nt, int mode) {
+  if (mode == kTilePlain) return tile_kernel_mode<kTilePlain>(nt);
+  if (mode == kTileSplitK) return tile_kernel_mode<kTileSplitK>(nt);
+  if (mode == kTilePairW) return tile_kernel_mode<kTilePairW>(nt);
   return nullptr;
 }
 
+// Mode of a configuration: k_split 2 -> split K; pair_w 1 -> W shared by a
+// pair of token tiles; both 0/1 -> plain (both set: none).
+inline int tile_mode(const sgr_config& c) {
+  const int split = c.k_split == 0 ? 1 : c.k_split;
+  if (split == 2 && c.pair_w == 0) return kTileSplitK;
+  if (split == 1 && c.pair_w == 1) return kTilePairW;
+  if (split == 1 && c.pair_w == 0) return kTilePlain;
+  return 0;
+}
+
 inline cudaError_t tile_init_device() {
-  for (int split : {1, 2})
+  for (int mode : {kTilePlain, kTileSplitK, kTilePairW})
     for (int nt : {64, 128, 192, 256}) {
-      const void* fn = tile_kernel_for(nt, split);
+      const void* fn = tile_kernel_for(nt, mode);
       if (!fn) continue;
       cudaError_t e = set_kernel_smem_attrs(fn);
       if (e != cudaSuccess) return e;
@@ -622,8 +683,8 @@ inline int tile_plan(const sgr_config& c, int sms, int M, int N, int K, TilePara
                      size_t* smem) {
   if (!tile_supported(M, N, K)) return SGR_ERR_UNSUPPORTED;
   const int nt = c.tile_n;
-  const int split = c.k_split == 0 ? 1 : c.k_split;
-  if (!tile_kernel_for(nt, split)) return SGR_ERR_UNSUPPORTED;
+  const int mode = tile_mode(c);
+  if (!tile_kernel_for(nt, mode)) return SGR_ERR_UNSUPPORTED;
   if (c.ctas_per_sm != 1) return SGR_ERR_UNSUPPORTED;
   if (c.token_tile != 0 && c.token_tile != kTileM) return SGR_ERR_UNSUPPORTED;
   const int kbps = c.k_blocks_per_stage == 0 ? 1 : c.k_blocks_per_stage;
@@ -640,7 +701,8 @@ inline int tile_plan(const sgr_config& c, int sms, int M, int N, int K, TilePara
   // Split: rank 0 takes the first half of the K blocks rounded up to whole
   // stages (so that its last stage reads nothing of rank 1's range).
   const int kb_split = ((k_blocks + 1) / 2 + kbps - 1) / kbps * kbps;
-  if (split == 2) {
+  if (mode == kTilePairW && m_tiles % 2 != 0) return SGR_ERR_UNSUPPORTED;  // token tiles go in pairs
+  if (mode == kTileSplitK) {
     // One tile per cluster, both ranks with at least one K block, and the
     // hand-over buffer (128 rows x (NT/2 + 4) floats) inside the ring.
     if (2 * tiles > sms || k_blocks - kb_split < 1) return SGR_ERR_UNSUPPORTED;
@@ -658,7 +720,14 @@ inline int tile_plan(const sgr_config& c, int sms, int M, int N, int K, TilePara
   p->stages = c.stages;
   p->prefetch = c.prefetch_stages > 0 ? c.prefetch_stages : c.stages;
   p->tmem_cols = detail::pow2_at_least(2 * nt);
-  *grid = split == 2 ? (int)(2 * tiles) : (int)(tiles < sms ? tiles : sms);
+  if (mode == kTileSplitK) {
+    *grid = (int)(2 * tiles);
+  } else if (mode == kTilePairW) {
+    const long long units = tiles / 2, max_units = sms / 2;
+    *grid = (int)(2 * (units < max_units ? units : max_units));
+  } else {
+    *grid = (int)(tiles < sms ? tiles : sms);
+  }
   *smem = sm;
   return SGR_OK;
 }
@@ -671,10 +740,11 @@ inline int tile_launch(const sgr_config& c, int sms, unsigned* err, const void* 
   size_t smem = 0;
   int rc = tile_plan(c, sms, M, N, K, &p, &grid, &smem);
   if (rc != SGR_OK) return rc;
-  const int split = c.k_split == 0 ? 1 : c.k_split;
+  const int mode = tile_mode(c);
   CUtensorMap tmA, tmW;
   if (!detail::make_tmap(&tmA, A, M, K, lda, kTileM, kTcKBlock)) return SGR_ERR_LAUNCH;
-  if (!detail::make_tmap(&tmW, W, N, K, K, p.NT, kTcKBlock)) return SGR_ERR_LAUNCH;
+  // a pair rank loads half of each W box
+  if (!detail::make_tmap(&tmW, W, N, K, K, mode == kTilePairW ? p.NT / 2 : p.NT, kTcKBlock)) return SGR_ERR_LAUNCH;
   p.R = static_cast<const __nv_bfloat16*>(R);
   p.Y = static_cast<__nv_bfloat16*>(Y);
   p.ldr = ldr;
@@ -682,7 +752,7 @@ inline int tile_launch(const sgr_config& c, int sms, unsigned* err, const void* 
   p.err = err;
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3((unsigned)grid, 1, 1);
-  lc.blockDim = dim3(kTileThreads, 1, 1);
+  lc.blockDim = dim3((unsigned)tile_threads(mode), 1, 1);
   lc.dynamicSmemBytes = smem;
   lc.stream = stream;
   cudaLaunchAttribute attr[2];
@@ -692,7 +762,7 @@ inline int tile_launch(const sgr_config& c, int sms, unsigned* err, const void* 
     attr[n_attr].val.programmaticStreamSerializationAllowed = 1;
     ++n_attr;
   }
-  if (split == 2) {
+  if (mode != kTilePlain) {
     attr[n_attr].id = cudaLaunchAttributeClusterDimension;
     attr[n_attr].val.clusterDim.x = 2;
     attr[n_attr].val.clusterDim.y = 1;
@@ -702,19 +772,18 @@ inline int tile_launch(const sgr_config& c, int sms, unsigned* err, const void* 
   lc.attrs = attr;
   lc.numAttrs = n_attr;
   cudaError_t e = cudaErrorInvalidValue;
-  if (split == 1) {
-    switch (p.NT) {
-      case 64: e = cudaLaunchKernelEx(&lc, tile_gemm_kernel<64, 1>, tmA, tmW, p); break;
-      case 128: e = cudaLaunchKernelEx(&lc, tile_gemm_kernel<128, 1>, tmA, tmW, p); break;
-      case 192: e = cudaLaunchKernelEx(&lc, tile_gemm_kernel<192, 1>, tmA, tmW, p); break;
-      case 256: e = cudaLaunchKernelEx(&lc, tile_gemm_kernel<256, 1>, tmA, tmW, p); break;
-    }
-  } else {
-    switch (p.NT) {
-      case 64: e = cudaLaunchKernelEx(&lc, tile_gemm_kernel<64, 2>, tmA, tmW, p); break;
-      case 128: e = cudaLaunchKernelEx(&lc, tile_gemm_kernel<128, 2>, tmA, tmW, p); break;
-      case 192: e = cudaLaunchKernelEx(&lc, tile_gemm_kernel<192, 2>, tmA, tmW, p); break;
-    }
+  switch (mode * 1000 + p.NT) {
+    case kTilePlain * 1000 + 64: e = cudaLaunchKernelEx(&lc, tile_gemm_kernel<64, kTilePlain>, tmA, tmW, p); break;
+    case kTilePlain * 1000 + 128: e = cudaLaunchKernelEx(&lc, tile_gemm_kernel<128, kTilePlain>, tmA, tmW, p); break;
+    case kTilePlain * 1000 + 192: e = cudaLaunchKernelEx(&lc, tile_gemm_kernel<192, kTilePlain>, tmA, tmW, p); break;
+    case kTilePlain * 1000 + 256: e = cudaLaunchKernelEx(&lc, tile_gemm_kernel<256, kTilePlain>, tmA, tmW, p); break;
+    case kTileSplitK * 1000 + 64: e = cudaLaunchKernelEx(&lc, tile_gemm_kernel<64, kTileSplitK>, tmA, tmW, p); break;
+    case kTileSplitK * 1000 + 128: e = cudaLaunchKernelEx(&lc, tile_gemm_kernel<128, kTileSplitK>, tmA, tmW, p); break;
+    case kTileSplitK * 1000 + 192: e = cudaLaunchKernelEx(&lc, tile_gemm_kernel<192, kTileSplitK>, tmA, tmW, p); break;
+    case kTilePairW * 1000 + 64: e = cudaLaunchKernelEx(&lc, tile_gemm_kernel<64, kTilePairW>, tmA, tmW, p); break;
+    case kTilePairW * 1000 + 128: e = cudaLaunchKernelEx(&lc, tile_gemm_kernel<128, kTilePairW>, tmA, tmW, p); break;
+    case kTilePairW * 1000 + 192: e = cudaLaunchKernelEx(&lc, tile_gemm_kernel<192, kTilePairW>, tmA, tmW, p); break;
+    case kTilePairW * 1000 + 256: e = cudaLaunchKernelEx(&lc, tile_gemm_kernel<256, kTilePairW>, tmA, tmW, p); break;
   }
   if (e != cudaSuccess) {
     cudaGetLastError();
