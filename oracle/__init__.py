@@ -1,4 +1,5 @@
-"""CPU oracle for Y = bf16(A . W^T + R)  --  TEST INFRASTRUCTURE ONLY.
+"""CPU oracle for Y = bf16(A . W^T + R) and its low-bit weight variant
+Y = bf16(scale . A . e4m3(Wq)^T + R)  --  TEST INFRASTRUCTURE ONLY.
 
 Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline /
 reference leg may import this package.  The product path (the CUDA library and
@@ -7,8 +8,8 @@ its Python binding) never calls it and shares no code with it.
 The arithmetic lives in ``skinny_ref.c`` (plain C, FP64 accumulation, one
 round-to-nearest-even to BF16; see the header of that file for the passages it
 follows).  This module compiles it with gcc and wraps it with ctypes.  BF16
-arrays travel as numpy uint16 bit patterns; torch tensors are accepted and
-converted with ``to_bits``.
+arrays travel as numpy uint16 bit patterns, FP8 E4M3 weights as uint8 codes;
+torch tensors are accepted and converted with ``to_bits`` / ``to_codes``.
 """
 from __future__ import annotations
 
@@ -56,6 +57,27 @@ def to_bits(x) -> np.ndarray:
     return x.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
+def _to_numpy(x) -> np.ndarray:
+    if isinstance(x, np.ndarray):
+        return x
+    return x.detach().cpu().contiguous().numpy()
+
+
+def to_codes(x) -> np.ndarray:
+    """FP8 E4M3 codes: uint8 array, or a torch uint8 / float8_e4m3fn tensor -> numpy uint8."""
+    if isinstance(x, np.ndarray):
+        if x.dtype != np.uint8:
+            raise TypeError("expected uint8 E4M3 codes")
+        return x
+    import torch
+
+    if x.dtype == torch.float8_e4m3fn:
+        x = x.view(torch.uint8)
+    if x.dtype != torch.uint8:
+        raise TypeError(f"expected torch.uint8 or float8_e4m3fn, got {x.dtype}")
+    return x.detach().cpu().contiguous().numpy()
+
+
 def from_bits(bits: np.ndarray):
     """numpy uint16 bits -> torch.bfloat16 CPU tensor."""
     import torch
@@ -95,6 +117,14 @@ class Oracle:
         lib.sgr_ref_gemm_residual_f64.argtypes = [u16p, L, u16p, L, u16p, L, dp, L, L, L, L, I]
         lib.sgr_ref_sample.restype = I
         lib.sgr_ref_sample.argtypes = [u16p, L, u16p, L, u16p, L, L, L, L, lp, lp, L, u16p]
+        u8p = ctypes.POINTER(ctypes.c_uint8)
+        fp = ctypes.POINTER(ctypes.c_float)
+        lib.sgr_ref_gemm_residual_w8.restype = I
+        lib.sgr_ref_gemm_residual_w8.argtypes = [u16p, L, u8p, L, fp, u16p, L, u16p, L, L, L, L, I]
+        lib.sgr_ref_sample_w8.restype = I
+        lib.sgr_ref_sample_w8.argtypes = [u16p, L, u8p, L, fp, u16p, L, L, L, L, lp, lp, L, u16p]
+        lib.sgr_ref_e4m3_to_double.restype = ctypes.c_double
+        lib.sgr_ref_e4m3_to_double.argtypes = [ctypes.c_uint8]
         lib.sgr_ref_mutant.restype = I
         lib.sgr_ref_mutant.argtypes = []
         self.lib = lib
@@ -157,6 +187,55 @@ class Oracle:
             raise RuntimeError(f"oracle failed with status {rc}")
         return out
 
+    def _operands_w8(self, A, Wq, scale, R):
+        A, lda = _rows(to_bits(A))
+        Wq, ldw = _rows(to_codes(Wq))
+        R, ldr = _rows(to_bits(R))
+        scale = np.ascontiguousarray(_to_numpy(scale), dtype=np.float32)
+        M, K = A.shape
+        N = Wq.shape[0]
+        if Wq.shape[1] != K or R.shape != (M, N) or scale.shape != (N,):
+            raise ValueError(f"shape mismatch: A{A.shape} Wq{Wq.shape} scale{scale.shape} R{R.shape}")
+        return A, lda, Wq, ldw, scale, R, ldr, M, N, K
+
+    def gemm_residual_w8(self, A, Wq, scale, R, threads: int | None = None) -> np.ndarray:
+        """Y = bf16_rne(scale[n] * A . e4m3(Wq)^T + R) as uint16 [M,N] (every element).
+
+        Wq: [N,K] E4M3 codes (uint8 array or torch uint8 / float8_e4m3fn
+        tensor); scale: [N] float32."""
+        A, lda, Wq, ldw, scale, R, ldr, M, N, K = self._operands_w8(A, Wq, scale, R)
+        Y = np.empty((M, N), dtype=np.uint16)
+        threads = threads or os.cpu_count() or 1
+        rc = self.lib.sgr_ref_gemm_residual_w8(
+            self._p(A, ctypes.c_uint16), lda, self._p(Wq, ctypes.c_uint8), ldw,
+            self._p(scale, ctypes.c_float), self._p(R, ctypes.c_uint16), ldr,
+            self._p(Y, ctypes.c_uint16), N, M, N, K, int(threads))
+        if rc != 0:
+            raise RuntimeError(f"oracle failed with status {rc}")
+        return Y
+
+    def sample_w8(self, A, Wq, scale, R, ms, ns) -> np.ndarray:
+        """Y[ms[i], ns[i]] of the low-bit variant, as uint16."""
+        A, lda, Wq, ldw, scale, R, ldr, M, N, K = self._operands_w8(A, Wq, scale, R)
+        ms = np.ascontiguousarray(ms, dtype=np.int64)
+        ns = np.ascontiguousarray(ns, dtype=np.int64)
+        if ms.shape != ns.shape or ms.ndim != 1:
+            raise ValueError("ms and ns must be 1-D and of equal length")
+        out = np.empty(ms.shape, dtype=np.uint16)
+        rc = self.lib.sgr_ref_sample_w8(
+            self._p(A, ctypes.c_uint16), lda, self._p(Wq, ctypes.c_uint8), ldw,
+            self._p(scale, ctypes.c_float), self._p(R, ctypes.c_uint16), ldr, M, N, K,
+            self._p(ms, ctypes.c_long), self._p(ns, ctypes.c_long), len(ms),
+            self._p(out, ctypes.c_uint16))
+        if rc != 0:
+            raise RuntimeError(f"oracle failed with status {rc}")
+        return out
+
+    def e4m3_to_double(self, codes) -> np.ndarray:
+        codes = np.ascontiguousarray(codes, dtype=np.uint8)
+        return np.array([self.lib.sgr_ref_e4m3_to_double(int(b)) for b in codes.ravel()]
+                        ).reshape(codes.shape)
+
     def round_bf16(self, t) -> np.ndarray:
         t = np.ascontiguousarray(t, dtype=np.float64)
         out = np.empty(t.shape, dtype=np.uint16)
@@ -181,3 +260,7 @@ def load(mutant: int = 0, out_dir: str | None = None) -> Oracle:
 
 def gemm_residual(A, W, R, threads: int | None = None) -> np.ndarray:
     return load().gemm_residual(A, W, R, threads)
+
+
+def gemm_residual_w8(A, Wq, scale, R, threads: int | None = None) -> np.ndarray:
+    return load().gemm_residual_w8(A, Wq, scale, R, threads)

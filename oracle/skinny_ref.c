@@ -32,6 +32,22 @@
  * Build: gcc -O2 -std=c11 -ffp-contract=off -fPIC -shared -pthread ... -lm
  * (no -ffast-math: the k order of the sum is part of the definition above).
  *
+ * Low-bit weight variant (sgr_ref_gemm_residual_w8): the weight arrives as
+ * one FP8 code per element plus one FP32 scale per output column n, as in the
+ * FP8 / k-bit weight work of the bitsandbytes "QLORA-2" page (its scalar
+ * GEMV, "Three-Kernel Strategy": quantized weights, BF16 activations, the
+ * block scale applied to the dot product).  The pages do not fix the FP8
+ * encoding; the reading taken is OCP E4M3 without infinities (bias 7, three
+ * fraction bits, subnormals, S.1111.111 = NaN), the format of
+ * torch.float8_e4m3fn and of the tensor cores' e4m3 type:
+ *
+ *     Y[m,n] = bf16_rne( scale[n] * sum_k A[m,k] * e4m3(Wq[n,k])  +  R[m,n] )
+ *
+ * Each decoded code is exact in double; each product of a BF16 value and an
+ * E4M3 value is exact (8 + 4 significant bits); the scale multiplies the FP64
+ * sum once (one FP64 rounding), then R is added and the double is rounded to
+ * BF16 as above.
+ *
  * SGR_REF_MUTANT (compile-time, default 0) plants one known mistake so that
  * the test suite can show its pins catch it; a normal build never sets it.
  */
@@ -54,6 +70,33 @@ static double bf16_to_double(uint16_t h)
     float f;
     memcpy(&f, &bits, sizeof f);
     return (double)f;
+}
+
+/*
+ * Exact E4M3 -> double.  Fields: sign s (bit 7), exponent e (bits 6-3, bias
+ * 7), fraction f (bits 2-0).  e > 0: (1 + f/8) * 2^(e-7) = (8 + f) * 2^(e-10);
+ * e = 0: subnormal f/8 * 2^-6 = f * 2^-9; e = 15 with f = 7 is NaN (the format
+ * has no infinities, so e = 15, f < 7 are ordinary numbers up to 448).
+ */
+static double e4m3_to_double(uint8_t b)
+{
+    int s = b >> 7, e = (b >> 3) & 15, f = b & 7;
+#if SGR_REF_MUTANT == 12
+    if (e == 15 && f == 7)
+        return s ? -480.0 : 480.0;            /* planted: no NaN code */
+#else
+    if (e == 15 && f == 7)
+        return NAN;
+#endif
+    double mag;
+#if SGR_REF_MUTANT == 9
+    mag = ldexp(8 + f, e - 10);               /* planted: subnormals read as normals */
+#elif SGR_REF_MUTANT == 10
+    mag = e == 0 ? ldexp(f, -10) : ldexp(8 + f, e - 11); /* planted: bias 8 */
+#else
+    mag = e == 0 ? ldexp(f, -9) : ldexp(8 + f, e - 10);
+#endif
+    return s ? -mag : mag;
 }
 
 /*
@@ -134,14 +177,42 @@ static double dot_plus_residual(const uint16_t *a, const uint16_t *w, uint16_t r
 #endif
 }
 
+/* The same for the low-bit weight variant:
+ * t = scale * sum_k a[k]*e4m3(wq[k]) + r. */
+static double dot_w8_plus_residual(const uint16_t *a, const uint8_t *wq, float scale,
+                                   uint16_t r, long K)
+{
+    double s = 0.0;
+    for (long k = 0; k < K; ++k)
+        s += bf16_to_double(a[k]) * e4m3_to_double(wq[k]);
+#if SGR_REF_MUTANT == 11
+    return (double)scale * (s + bf16_to_double(r)); /* planted: residual scaled too */
+#else
+    return (double)scale * s + bf16_to_double(r);
+#endif
+}
+
 typedef struct {
     const uint16_t *A, *W, *R;
+    const uint8_t *Wq;    /* low-bit weights (W unused), or NULL */
+    const float *scale;   /* per-column scales of Wq */
     uint16_t *Y;      /* rounded output, or NULL */
     double *T;        /* unrounded output, or NULL */
     long lda, ldw, ldr, ldy, ldt;
-    long M, K;
+    long M, K, N;
     long n0, n1;      /* this worker's output columns [n0, n1) */
 } ref_job;
+
+/* Scale of output column n. */
+static float column_scale(const float *scale, long n, long N)
+{
+#if SGR_REF_MUTANT == 13
+    return scale[(n + 1) % N];                /* planted: neighbouring column's scale */
+#else
+    (void)N;
+    return scale[n];
+#endif
+}
 
 static void *ref_worker(void *p)
 {
@@ -153,8 +224,12 @@ static void *ref_worker(void *p)
 #else
             long rrow = m;
 #endif
-            double t = dot_plus_residual(j->A + m * j->lda, j->W + n * j->ldw,
-                                         j->R[rrow * j->ldr + n], j->K);
+            double t = j->Wq
+                ? dot_w8_plus_residual(j->A + m * j->lda, j->Wq + n * j->ldw,
+                                       column_scale(j->scale, n, j->N),
+                                       j->R[rrow * j->ldr + n], j->K)
+                : dot_plus_residual(j->A + m * j->lda, j->W + n * j->ldw,
+                                    j->R[rrow * j->ldr + n], j->K);
             long out = m * j->ldy + n;
             if (j->Y)
                 j->Y[out] = sgr_ref_round_bf16(t);
@@ -167,11 +242,11 @@ static void *ref_worker(void *p)
 
 /* Returns 0 on success, -1 on bad arguments, -2 if threads could not start,
  * -3 if the FP rounding mode is not round-to-nearest. */
-static int run_ref(const uint16_t *A, long lda, const uint16_t *W, long ldw,
-                   const uint16_t *R, long ldr, uint16_t *Y, long ldy,
-                   double *T, long ldt, long M, long N, long K, int threads)
+static int run_ref(const uint16_t *A, long lda, const uint16_t *W, const uint8_t *Wq,
+                   const float *scale, long ldw, const uint16_t *R, long ldr, uint16_t *Y,
+                   long ldy, double *T, long ldt, long M, long N, long K, int threads)
 {
-    if (!A || !W || !R || (!Y && !T) || M < 0 || N < 0 || K < 0)
+    if (!A || (!W && !(Wq && scale)) || !R || (!Y && !T) || M < 0 || N < 0 || K < 0)
         return -1;
     if (lda < K || ldw < K || ldr < N || (Y && ldy < N) || (T && ldt < N))
         return -1;
@@ -188,7 +263,7 @@ static int run_ref(const uint16_t *A, long lda, const uint16_t *W, long ldw,
     ref_job jobs[256];
     pthread_t tids[256];
     for (int i = 0; i < threads; ++i) {
-        ref_job j = {A, W, R, Y, T, lda, ldw, ldr, ldy, ldt, M, K,
+        ref_job j = {A, W, R, Wq, scale, Y, T, lda, ldw, ldr, ldy, ldt, M, K, N,
                      N * i / threads, N * (i + 1) / threads};
         jobs[i] = j;
     }
@@ -212,7 +287,7 @@ int sgr_ref_gemm_residual(const uint16_t *A, long lda, const uint16_t *W, long l
                           const uint16_t *R, long ldr, uint16_t *Y, long ldy,
                           long M, long N, long K, int threads)
 {
-    return run_ref(A, lda, W, ldw, R, ldr, Y, ldy, NULL, 0, M, N, K, threads);
+    return run_ref(A, lda, W, NULL, NULL, ldw, R, ldr, Y, ldy, NULL, 0, M, N, K, threads);
 }
 
 /* T = A . W^T + R in FP64, unrounded (for error analysis). */
@@ -220,7 +295,7 @@ int sgr_ref_gemm_residual_f64(const uint16_t *A, long lda, const uint16_t *W, lo
                               const uint16_t *R, long ldr, double *T, long ldt,
                               long M, long N, long K, int threads)
 {
-    return run_ref(A, lda, W, ldw, R, ldr, NULL, 0, T, ldt, M, N, K, threads);
+    return run_ref(A, lda, W, NULL, NULL, ldw, R, ldr, NULL, 0, T, ldt, M, N, K, threads);
 }
 
 /* Selected elements only: out[i] = Y[ms[i], ns[i]].  For full-size checks
@@ -241,5 +316,38 @@ int sgr_ref_sample(const uint16_t *A, long lda, const uint16_t *W, long ldw,
     }
     return 0;
 }
+
+/* Low-bit weights: Y = bf16_rne(scale[n] * A . e4m3(Wq)^T + R), every
+ * element.  Wq is [N,K] bytes with row stride ldw, scale has N entries. */
+int sgr_ref_gemm_residual_w8(const uint16_t *A, long lda, const uint8_t *Wq, long ldw,
+                             const float *scale, const uint16_t *R, long ldr, uint16_t *Y,
+                             long ldy, long M, long N, long K, int threads)
+{
+    if (!Wq || !scale)
+        return -1;
+    return run_ref(A, lda, NULL, Wq, scale, ldw, R, ldr, Y, ldy, NULL, 0, M, N, K, threads);
+}
+
+/* Selected elements of the low-bit variant: out[i] = Y[ms[i], ns[i]]. */
+int sgr_ref_sample_w8(const uint16_t *A, long lda, const uint8_t *Wq, long ldw,
+                      const float *scale, const uint16_t *R, long ldr, long M, long N, long K,
+                      const long *ms, const long *ns, long count, uint16_t *out)
+{
+    if (!A || !Wq || !scale || !R || !ms || !ns || !out || count < 0 || lda < K || ldw < K ||
+        ldr < N)
+        return -1;
+    if (fegetround() != FE_TONEAREST)
+        return -3;
+    for (long i = 0; i < count; ++i) {
+        long m = ms[i], n = ns[i];
+        if (m < 0 || m >= M || n < 0 || n >= N)
+            return -1;
+        out[i] = sgr_ref_round_bf16(dot_w8_plus_residual(
+            A + m * lda, Wq + n * ldw, column_scale(scale, n, N), R[m * ldr + n], K));
+    }
+    return 0;
+}
+
+double sgr_ref_e4m3_to_double(uint8_t b) { return e4m3_to_double(b); }
 
 int sgr_ref_mutant(void) { return SGR_REF_MUTANT; }

@@ -94,3 +94,71 @@ def integer_bf16(shape, lo: int, hi: int, seed: int) -> torch.Tensor:
     g = torch.Generator(device="cpu")
     g.manual_seed(seed)
     return torch.randint(lo, hi + 1, shape, generator=g).to(torch.bfloat16)
+
+
+@dataclass
+class ProblemW8:
+    """A low-bit weight problem: A [M,K] BF16, Wq [N,K] FP8 E4M3 codes (torch.uint8),
+    scale [N] float32 (one per output column), R [M,N] BF16 (all CPU)."""
+
+    A: torch.Tensor
+    Wq: torch.Tensor
+    scale: torch.Tensor
+    R: torch.Tensor
+    seed: int
+
+    @property
+    def M(self) -> int:
+        return self.A.shape[0]
+
+    @property
+    def N(self) -> int:
+        return self.Wq.shape[0]
+
+    @property
+    def K(self) -> int:
+        return self.A.shape[1]
+
+
+E4M3_MAX = 448.0
+
+
+def make_problem_w8(M: int, N: int = N_LATENT_MOE, K: int = K_LATENT_MOE, seed: int = 0) -> ProblemW8:
+    """A, R ~ N(0,1) BF16 and per-column FP8 weights of a W ~ N(0,1)/sqrt(K).
+
+    Draw order A, W, R from ``torch.Generator().manual_seed(seed)`` (the same
+    draws as ``make_problem``).  Each row n of the float32 W gets the scale
+    max|W[n,:]| / 448 (1 for an all-zero row) and the codes are torch's
+    float32 -> float8_e4m3fn cast of W[n,:] / scale[n] (nearest, saturating):
+    the per-channel absmax weight quantisation that produces such operands."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    A = torch.randn((M, K), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    W = torch.randn((N, K), generator=g, dtype=torch.float32) * (1.0 / math.sqrt(K) if K > 0 else 1.0)
+    R = torch.randn((M, N), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    amax = W.abs().amax(dim=1) if K > 0 else torch.zeros(N)
+    scale = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax)).to(torch.float32)
+    Wq = (W / scale[:, None]).to(torch.float8_e4m3fn).view(torch.uint8)
+    return ProblemW8(A, Wq.contiguous(), scale.contiguous(), R, seed)
+
+
+def random_e4m3_codes(shape, seed: int, nan: bool = False) -> torch.Tensor:
+    """Uniformly random FP8 E4M3 codes (torch.uint8, CPU): every sign, exponent
+    (subnormals and zero included) and fraction; the two NaN codes 0x7F / 0xFF
+    only when ``nan``."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    c = torch.randint(0, 256, shape, generator=g, dtype=torch.int64)
+    if not nan:
+        c = torch.where((c & 0x7F) == 0x7F, c - 1, c)
+    return c.to(torch.uint8)
+
+
+def random_scales(n: int, seed: int, lo_exp: int = -12, hi_exp: int = 2) -> torch.Tensor:
+    """Positive float32 scales with random exponents in [lo_exp, hi_exp] and a
+    random 23-bit fraction (CPU)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    expo = torch.randint(lo_exp, hi_exp + 1, (n,), generator=g).to(torch.float64)
+    frac = torch.randint(0, 1 << 23, (n,), generator=g).to(torch.float64)
+    return ((1.0 + frac / float(1 << 23)) * torch.pow(2.0, expo)).to(torch.float32)

@@ -266,6 +266,142 @@ def check_strided_rows(orc):
     _eq(orc.gemm_residual(a_view, W, r_view), want, "strided operands")
 
 
+# ------------------------------------------------------ low-bit weight pins
+def e4m3_value(code: int) -> Fraction | None:
+    """Exact value of an FP8 E4M3 code from its fields (None for NaN)."""
+    s, e, f = code >> 7, (code >> 3) & 15, code & 7
+    if e == 15 and f == 7:
+        return None
+    mag = Fraction(f, 8) * Fraction(2) ** -6 if e == 0 else (1 + Fraction(f, 8)) * Fraction(2) ** (e - 7)
+    return -mag if s else mag
+
+
+def load_e4m3_fixture():
+    rows = []
+    with open(os.path.join(GOLDEN, "e4m3_codes.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            c, v = line.split()
+            rows.append((int(c, 16), float("nan") if v == "nan" else float.fromhex(v)))
+    return rows
+
+
+def exact_reference_w8(A: np.ndarray, Wq: np.ndarray, scale: np.ndarray, R: np.ndarray) -> np.ndarray:
+    """Brute force: Y[m,n] = rne(scale[n] * sum_k A[m,k] e4m3(Wq[n,k]) + R[m,n]) in exact rationals."""
+    M, K = A.shape
+    N = Wq.shape[0]
+    out = np.empty((M, N), dtype=np.uint16)
+    for m in range(M):
+        for n in range(N):
+            s = sum((bf16_value(int(A[m, k])) * e4m3_value(int(Wq[n, k])) for k in range(K)), Fraction(0))
+            out[m, n] = rne_bf16_exact(Fraction(float(scale[n])) * s + bf16_value(int(R[m, n])))
+    return out
+
+
+def _same_float(got: np.ndarray, want: np.ndarray) -> bool:
+    """Equal values, NaN matching NaN, and the sign of zero compared too."""
+    both_nan = np.isnan(got) & np.isnan(want)
+    same = (got == want) & (np.signbit(got) == np.signbit(want))
+    return bool(np.all(both_nan | same))
+
+
+def check_e4m3_fixture(orc):
+    rows = load_e4m3_fixture()
+    got = orc.e4m3_to_double(np.array([c for c, _ in rows], dtype=np.uint8))
+    want = np.array([v for _, v in rows])
+    if not _same_float(got, want):
+        bad = [(hex(c), g, w) for (c, w), g in zip(rows, got) if not _same_float(np.array([g]), np.array([w]))]
+        raise AssertionError(f"E4M3 fixture mismatches (code, got, want): {bad[:4]}")
+
+
+def check_e4m3_all_codes_vs_library(orc):
+    """All 256 codes against torch's float8_e4m3fn -> float64 conversion and
+    against the field formula above (signed zero included)."""
+    codes = np.arange(256, dtype=np.uint8)
+    got = orc.e4m3_to_double(codes)
+    lib = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    if not _same_float(got, lib):
+        raise AssertionError("E4M3 decode differs from torch.float8_e4m3fn")
+    field = []
+    for c in codes:
+        v = e4m3_value(int(c))
+        field.append(np.nan if v is None else np.copysign(float(abs(v)), -1.0 if c >= 128 else 1.0))
+    if not _same_float(got, np.array(field)):
+        raise AssertionError("E4M3 decode differs from the field formula")
+
+
+def check_w8_brute_force_exact(orc):
+    """Tiny shapes with every kind of code (zero, subnormal, normal, both
+    signs) and random non-power-of-two scales: oracle == exact rationals."""
+    for (M, N, K, seed) in ((3, 5, 8, 1), (1, 1, 1, 2), (2, 7, 19, 3), (4, 3, 32, 4)):
+        A = bits(inputs.random_bf16_bits((M, K), seed + 300, lo_exp=-6, hi_exp=4))
+        Wq = inputs.random_e4m3_codes((N, K), seed + 400).numpy()
+        sc = inputs.random_scales(N, seed + 500).numpy()
+        R = bits(inputs.random_bf16_bits((M, N), seed + 600, lo_exp=-6, hi_exp=6))
+        _eq(orc.gemm_residual_w8(A, Wq, sc, R, threads=2), exact_reference_w8(A, Wq, sc, R),
+            f"w8 brute force {M}x{N}x{K}")
+
+
+def check_w8_subnormal_codes_exact(orc):
+    """Only zero, subnormal and smallest-binade codes (exponent field 0 or 1),
+    where the subnormal decoding decides the result."""
+    M, N, K = 2, 6, 24
+    A = bits(inputs.random_bf16_bits((M, K), 351, lo_exp=-2, hi_exp=2))
+    Wq = (inputs.random_e4m3_codes((N, K), 352) & 0x8F).numpy()
+    sc = inputs.random_scales(N, 353, lo_exp=4, hi_exp=8).numpy()
+    R = bits(inputs.random_bf16_bits((M, N), 354, lo_exp=-4, hi_exp=0))
+    _eq(orc.gemm_residual_w8(A, Wq, sc, R), exact_reference_w8(A, Wq, sc, R), "w8 subnormal codes")
+
+
+def check_w8_unit_scale_is_bf16_gemm(orc):
+    """scale = 1: every E4M3 value is a BF16 value (4 significant bits, exponent
+    in range), so the low-bit variant equals the BF16 operation on the
+    library-decoded weights."""
+    M, N, K = 4, 33, 200
+    A = bits(inputs.random_bf16_bits((M, K), 71, lo_exp=-4, hi_exp=4))
+    R = bits(inputs.random_bf16_bits((M, N), 72, lo_exp=-2, hi_exp=6))
+    Wq = inputs.random_e4m3_codes((N, K), 73)
+    Wb = bits(Wq.view(torch.float8_e4m3fn).to(torch.bfloat16))
+    ones = np.ones(N, dtype=np.float32)
+    _eq(orc.gemm_residual_w8(A, Wq.numpy(), ones, R), orc.gemm_residual(A, Wb, R), "w8 unit scale")
+
+
+def check_w8_power_of_two_scales(orc):
+    """scale[n] = 2^j[n]: equals the BF16 operation on weights e4m3 * 2^j,
+    which are still exact BF16 values."""
+    M, N, K = 3, 16, 96
+    A = bits(inputs.random_bf16_bits((M, K), 81, lo_exp=-4, hi_exp=4))
+    R = bits(inputs.random_bf16_bits((M, N), 82))
+    Wq = inputs.random_e4m3_codes((N, K), 83)
+    j = np.arange(N) % 9 - 6
+    sc = np.ldexp(np.ones(N), j).astype(np.float32)
+    Wf = Wq.view(torch.float8_e4m3fn).to(torch.float64) * torch.from_numpy(np.ldexp(np.ones(N), j))[:, None]
+    Wb = bits(Wf.to(torch.float32).to(torch.bfloat16))
+    assert np.array_equal(_f64(Wb), Wf.numpy()), "scaled weights not exact in BF16"
+    _eq(orc.gemm_residual_w8(A, Wq.numpy(), sc, R), orc.gemm_residual(A, Wb, R), "w8 power-of-two scales")
+
+
+def check_w8_strided_rows(orc):
+    M, N, K = 2, 4, 16
+    A = bits(inputs.random_bf16_bits((M, 2 * K), 91))
+    Wq = inputs.random_e4m3_codes((N, 3 * K), 92).numpy()
+    sc = inputs.random_scales(N, 93).numpy()
+    R = bits(inputs.random_bf16_bits((M, 2 * N), 94))
+    a_v, w_v, r_v = A[:, K:], Wq[:, K:2 * K], R[:, N:]
+    want = exact_reference_w8(np.ascontiguousarray(a_v), np.ascontiguousarray(w_v), sc, np.ascontiguousarray(r_v))
+    _eq(orc.gemm_residual_w8(a_v, w_v, sc, r_v), want, "w8 strided operands")
+
+
+def check_w8_sample_matches_full(orc):
+    p = inputs.make_problem_w8(3, N=40, K=64, seed=95)
+    full = orc.gemm_residual_w8(p.A, p.Wq, p.scale, p.R)
+    ms = np.array([0, 2, 1, 2, 0])
+    ns = np.array([0, 39, 17, 3, 21])
+    _eq(orc.sample_w8(p.A, p.Wq, p.scale, p.R, ms, ns), full[ms, ns], "w8 sample")
+
+
 ALL_CHECKS = [
     check_rounding_fixture,
     check_rounding_vs_exact_bisection,
@@ -277,4 +413,12 @@ ALL_CHECKS = [
     check_integer_exact,
     check_transpose_symmetry,
     check_strided_rows,
+    check_e4m3_fixture,
+    check_e4m3_all_codes_vs_library,
+    check_w8_brute_force_exact,
+    check_w8_subnormal_codes_exact,
+    check_w8_unit_scale_is_bf16_gemm,
+    check_w8_power_of_two_scales,
+    check_w8_strided_rows,
+    check_w8_sample_matches_full,
 ]
