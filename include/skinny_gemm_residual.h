@@ -70,7 +70,7 @@
 extern "C" {
 #endif
 
-#define SGR_ABI_VERSION 5
+#define SGR_ABI_VERSION 6
 
 typedef enum {
   SGR_OK = 0,
@@ -92,6 +92,7 @@ typedef enum {
 #define SGR_PATH_TC 2      /* tcgen05 kernel, persistent stream-K with split-K fixup */
 #define SGR_PATH_TC_ROWS 3 /* tcgen05 kernel, one contiguous W row slab per CTA (M <= 256) */
 #define SGR_PATH_TILE 4    /* tcgen05 kernel, 128-token x tile_n output tiles (large M) */
+#define SGR_PATH_W8 5      /* tcgen05 row-slab kernel for FP8 weights (skinny_gemm_residual_w8 only, M <= 256) */
 
 /*
  * Y = bf16(A . W^T + R) with contiguous operands (lda = K, ldr = ldy = N).
@@ -158,7 +159,7 @@ int sgr_select_path(int M, int N, int K);
 
 /*
  * The configuration the library uses for this shape on the given path
- * (SGR_PATH_AUTO resolves first).  Writes *cfg.  Host-only apart from a
+ * (SGR_PATH_AUTO resolves first; SGR_PATH_W8 gives the FP8-weight kernel's).  Writes *cfg.  Host-only apart from a
  * device-attribute query for the SM count of `device`.  Returns an sgr_status.
  */
 int sgr_default_config(int device, int M, int N, int K, int path, sgr_config* cfg);
@@ -259,6 +260,49 @@ typedef struct {
  */
 int skinny_gemm_residual_grouped(const sgr_group* groups, int num_groups, int N, int K,
                                  const sgr_config* cfg, unsigned flags, void* stream);
+
+/*
+ * Low-bit weight variant: FP8 E4M3 weights with one FP32 scale per output
+ * column, BF16 activations, residual and output:
+ *
+ *     Y[m,n] = bf16( scale[n] * sum_k A[m,k] * e4m3(Wq[n,k]) + R[m,n] )
+ *
+ * with FP32 accumulation and one round-to-nearest-even, the quantized-weight
+ * decode kernel direction of the bitsandbytes "QLORA-2" page ("Three-Kernel
+ * Strategy": weights stored in few bits, 16-bit activations, the scale
+ * applied to the dot product; here per output column).  E4M3 is the OCP 8-bit
+ * format (sign, 4 exponent bits with bias 7, 3 fraction bits, subnormals, no
+ * infinities; the value of torch.float8_e4m3fn).  The weight bytes read per
+ * call are half those of the BF16 entry points.
+ *
+ *     A      [M, K]  BF16, row stride lda >= K (elements, multiple of 8)
+ *     Wq     [N, K]  E4M3 codes (one byte each), row stride ldw >= K bytes,
+ *                    a multiple of 16; the codes 0x7F and 0xFF (NaN) must not
+ *                    occur (their result is unspecified; quantisers that
+ *                    saturate never write them)
+ *     scale  [N]     FP32, 4-byte aligned
+ *     R, Y   [M, N]  BF16, row strides ldr, ldy >= N (multiples of 8)
+ *
+ * M <= 256 (decode-sized batches), N and K multiples of 8.  Device pointers,
+ * ownership, asynchrony, PDL (Wq and scale are read before the dependency
+ * wait, like W), graph capture and errors as for skinny_gemm_residual_ex; in
+ * addition SGR_ERR_ALIGN for ldw not a multiple of 16 or a misaligned scale,
+ * and SGR_ERR_ALIAS when Y overlaps Wq or scale.  `cfg` may be NULL (library
+ * choice); its path must be SGR_PATH_AUTO or SGR_PATH_W8, and it may set
+ * stages (depth of the weight-code ring, 2..16), prefetch_stages (depth of
+ * the activation ring, 2..8), k_blocks_per_stage (64-wide K blocks per
+ * stage: even, 2..8), token_tile and rows_per_stage (W rows per CTA, a
+ * multiple of 8 up to 128).  Returns an sgr_status.
+ */
+int skinny_gemm_residual_w8(const void* A, int64_t lda, const void* Wq, int64_t ldw,
+                            const float* scale, const void* R, int64_t ldr, void* Y,
+                            int64_t ldy, int M, int N, int K, const sgr_config* cfg,
+                            unsigned flags, void* stream);
+
+/* Host-only argument check of skinny_gemm_residual_w8 (its exact rules). */
+int sgr_validate_w8(const void* A, int64_t lda, const void* Wq, int64_t ldw,
+                    const float* scale, const void* R, int64_t ldr, const void* Y,
+                    int64_t ldy, int M, int N, int K);
 
 #ifdef __cplusplus
 }

@@ -2,6 +2,10 @@
 
     Y[M,N] = bf16( A[M,K] . W[N,K]^T  (FP32 accumulate)  +  R[M,N] )
 
+and its low-bit weight variant (FP8 E4M3 codes Wq with a per-column scale):
+
+    Y[M,N] = bf16( scale[N] * A[M,K] . e4m3(Wq[N,K])^T  +  R[M,N] )
+
 The work runs in hand-written CUDA kernels behind the C ABI declared in
 include/skinny_gemm_residual.h; this package is a ctypes binding with the
 same function names (see ``binding``), the build step (``build``) and the
@@ -24,6 +28,7 @@ from .binding import (  # noqa: F401
     SGR_PATH_TC,
     SGR_PATH_TC_ROWS,
     SGR_PATH_TILE,
+    SGR_PATH_W8,
     SgrError,
     load,
     make_config,
@@ -47,4 +52,7 @@ from .binding import (  # noqa: F401
     sgr_group,
     skinny_gemm_residual_noalloc_ptr,
     skinny_gemm_residual_ptr,
+    skinny_gemm_residual_w8,
+    skinny_gemm_residual_w8_ptr,
+    sgr_validate_w8_ptr,
 )

@@ -14,7 +14,7 @@ import threading
 
 from . import build as _build
 
-ABI_VERSION = 5  # must equal SGR_ABI_VERSION of the loaded library
+ABI_VERSION = 6  # must equal SGR_ABI_VERSION of the loaded library
 
 SGR_OK = 0
 SGR_ERR_NULL = 1
@@ -32,6 +32,7 @@ SGR_PATH_SIMT = 1
 SGR_PATH_TC = 2
 SGR_PATH_TC_ROWS = 3
 SGR_PATH_TILE = 4
+SGR_PATH_W8 = 5
 
 
 class sgr_group(ctypes.Structure):
@@ -80,6 +81,8 @@ EXPORTS = (
     "sgr_abi_version",
     "skinny_gemm_residual_noalloc",
     "skinny_gemm_residual_grouped",
+    "skinny_gemm_residual_w8",
+    "sgr_validate_w8",
 )
 
 
@@ -117,6 +120,10 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.skinny_gemm_residual_noalloc.argtypes = [vp, i64, vp, vp, i64, vp, i64, I, I, I, U, vp]
         lib.skinny_gemm_residual_grouped.argtypes = [ctypes.POINTER(sgr_group), I, I, I,
                                                      ctypes.POINTER(sgr_config), U, vp]
+        fp = ctypes.POINTER(ctypes.c_float)
+        lib.skinny_gemm_residual_w8.argtypes = [vp, i64, vp, i64, fp, vp, i64, vp, i64, I, I, I,
+                                                ctypes.POINTER(sgr_config), U, vp]
+        lib.sgr_validate_w8.argtypes = [vp, i64, vp, i64, fp, vp, i64, vp, i64, I, I, I]
         for name in EXPORTS:
             if name != "sgr_status_string":
                 getattr(lib, name).restype = ctypes.c_int
@@ -290,6 +297,58 @@ def skinny_gemm_residual_config(A, W, R, Y=None, config: sgr_config | None = Non
     """Explicit launch configuration (sweeps, tests)."""
     return skinny_gemm_residual_ex(A, W, R, Y, flags=flags, stream=stream,
                                    config=config if config is not None else sgr_config())
+
+
+def _fptr(addr: int):
+    return ctypes.cast(ctypes.c_void_p(addr), ctypes.POINTER(ctypes.c_float)) if addr else None
+
+
+def sgr_validate_w8_ptr(A: int, lda: int, Wq: int, ldw: int, scale: int, R: int, ldr: int, Y: int, ldy: int,
+                        M: int, N: int, K: int) -> int:
+    """Host-only argument check of the FP8-weight entry point (no GPU needed)."""
+    return load().sgr_validate_w8(A, lda, Wq, ldw, _fptr(scale), R, ldr, Y, ldy, M, N, K)
+
+
+def skinny_gemm_residual_w8_ptr(A: int, lda: int, Wq: int, ldw: int, scale: int, R: int, ldr: int, Y: int,
+                                ldy: int, M: int, N: int, K: int, cfg: sgr_config | None, flags: int,
+                                stream: int) -> int:
+    """FP8-weight entry point on raw device addresses; returns the status."""
+    return load().skinny_gemm_residual_w8(A, lda, Wq, ldw, _fptr(scale), R, ldr, Y, ldy, M, N, K,
+                                          ctypes.byref(cfg) if cfg is not None else None, flags, stream)
+
+
+def skinny_gemm_residual_w8(A, Wq, scale, R, Y=None, flags: int = 0, stream=None,
+                            config: sgr_config | None = None):
+    """Y = bf16(scale[n] * A . e4m3(Wq)^T + R).
+
+    A [M,K], R and Y [M,N]: CUDA bf16 with unit inner stride (row strides
+    allowed).  Wq [N,K]: CUDA torch.uint8 or torch.float8_e4m3fn codes with
+    unit inner stride and a row stride that is a multiple of 16 bytes.
+    scale [N]: contiguous CUDA float32.  Returns Y."""
+    import torch
+
+    for t, n in ((A, "A"), (R, "R")):
+        _check_tensor(t, n)
+    if Wq.dtype not in (torch.uint8, torch.float8_e4m3fn):
+        raise TypeError(f"Wq must be torch.uint8 or torch.float8_e4m3fn, got {Wq.dtype}")
+    if not Wq.is_cuda or Wq.dim() != 2 or (Wq.shape[0] > 1 and Wq.shape[1] > 0 and Wq.stride(1) != 1):
+        raise ValueError("Wq must be a 2-D CUDA tensor with unit inner stride")
+    if scale.dtype != torch.float32 or not scale.is_cuda or scale.dim() != 1 or not scale.is_contiguous():
+        raise ValueError("scale must be a contiguous 1-D CUDA float32 tensor")
+    if Y is None:
+        Y = torch.empty(R.shape, dtype=R.dtype, device=R.device)
+    _check_tensor(Y, "Y")
+    M, K = A.shape
+    N = Wq.shape[0]
+    if Wq.shape[1] != K or tuple(R.shape) != (M, N) or tuple(Y.shape) != (M, N) or scale.shape[0] != N:
+        raise ValueError(f"shape mismatch A{tuple(A.shape)} Wq{tuple(Wq.shape)} scale{tuple(scale.shape)} "
+                         f"R{tuple(R.shape)} Y{tuple(Y.shape)}")
+    rc = skinny_gemm_residual_w8_ptr(A.data_ptr(), _ld(A), Wq.data_ptr(), _ld(Wq), scale.data_ptr(),
+                                     R.data_ptr(), _ld(R), Y.data_ptr(), _ld(Y), M, N, K, config, flags,
+                                     _stream_handle(stream))
+    if rc != SGR_OK:
+        raise SgrError(rc, "skinny_gemm_residual_w8")
+    return Y
 
 
 def skinny_gemm_residual_noalloc_ptr(A: int, lda: int, W: int, R: int, ldr: int, Y: int, ldy: int,

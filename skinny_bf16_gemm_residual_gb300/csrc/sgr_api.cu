@@ -14,6 +14,7 @@
 #include "sgr_tc.cuh"
 #include "sgr_rows.cuh"
 #include "sgr_gemm.cuh"
+#include "sgr_w8.cuh"
 #include "sgr_table.h"
 
 namespace {
@@ -154,6 +155,7 @@ int init_device(int dev) {
     if (ok == SGR_OK && sgr::tc_init_device(sms, &st.ws) != cudaSuccess) ok = SGR_ERR_DEVICE;
     if (ok == SGR_OK && sgr::rows_init_device() != cudaSuccess) ok = SGR_ERR_DEVICE;
     if (ok == SGR_OK && sgr::tile_init_device() != cudaSuccess) ok = SGR_ERR_DEVICE;
+    if (ok == SGR_OK && sgr::w8_init_device() != cudaSuccess) ok = SGR_ERR_DEVICE;
     if (ok != SGR_OK) cudaGetLastError();
     st.sms = sms;
     st.err = static_cast<unsigned*>(errp);
@@ -456,6 +458,87 @@ int run_noalloc(const void* A, long long lda, const void* W, const void* R, long
                         (flags & SGR_FLAG_NO_PDL) == 0, stream);
 }
 
+// ------------------------------------------------------------ FP8 weights
+// Argument rules of skinny_gemm_residual_w8: those of the BF16 entry points
+// for A, R and Y; Wq is [N, K] bytes with row stride ldw (>= K, a multiple of
+// 16, 16-byte aligned base); scale holds N floats (4-byte aligned).
+int validate_w8(const void* A, long long lda, const void* Wq, long long ldw, const float* scale, const void* R,
+                long long ldr, const void* Y, long long ldy, int M, int N, int K) {
+  if (M < 0 || N < 0 || K < 0) return SGR_ERR_SHAPE;
+  if (M == 0 || N == 0) return SGR_OK;
+  if (M > kMaxM || N > kMaxN || K > kMaxK) return SGR_ERR_UNSUPPORTED;
+  if (N % 8 != 0 || K % 8 != 0) return SGR_ERR_SHAPE;
+  if (!R || !Y) return SGR_ERR_NULL;
+  if (K > 0 && (!A || !Wq || !scale)) return SGR_ERR_NULL;
+  if (ldr < N || ldy < N) return SGR_ERR_SHAPE;
+  if (K > 0 && (lda < K || ldw < K)) return SGR_ERR_SHAPE;
+  if (ldr % 8 != 0 || ldy % 8 != 0 || (K > 0 && (lda % 8 != 0 || ldw % 16 != 0))) return SGR_ERR_ALIGN;
+  if (!aligned16(R) || !aligned16(Y)) return SGR_ERR_ALIGN;
+  if (K > 0 && (!aligned16(A) || !aligned16(Wq) || (reinterpret_cast<uintptr_t>(scale) & 3u) != 0))
+    return SGR_ERR_ALIGN;
+  const Extent ey = extent(Y, M, ldy, N);
+  if (K > 0) {
+    if (overlap(ey, extent(A, M, lda, K))) return SGR_ERR_ALIAS;
+    const uintptr_t wb = reinterpret_cast<uintptr_t>(Wq);
+    if (overlap(ey, Extent{wb, wb + static_cast<uintptr_t>((long long)(N - 1) * ldw + K)})) return SGR_ERR_ALIAS;
+    const uintptr_t sb = reinterpret_cast<uintptr_t>(scale);
+    if (overlap(ey, Extent{sb, sb + static_cast<uintptr_t>(N) * 4u})) return SGR_ERR_ALIAS;
+  }
+  const bool in_place = (Y == R) && (ldy == ldr);
+  if (!in_place && overlap(ey, extent(R, M, ldr, N))) return SGR_ERR_ALIAS;
+  return SGR_OK;
+}
+
+// Configuration of the FP8-weight kernel: the library default for this
+// shape, then any non-zero field of `in` (path must be AUTO or W8).
+int resolve_config_w8(int sms, int M, int N, int K, const sgr_config* in, sgr_config* out) {
+  if (!sgr::w8_supported(sms, M, N, K)) return SGR_ERR_UNSUPPORTED;
+  sgr::w8_default_config(sms, M, N, K, out);
+  if (in) {
+    if (in->path != SGR_PATH_AUTO && in->path != SGR_PATH_W8) return SGR_ERR_UNSUPPORTED;
+    for (int r : in->reserved)
+      if (r != 0) return SGR_ERR_UNSUPPORTED;
+    if (in->tile_n || in->k_split || in->pair_w) return SGR_ERR_UNSUPPORTED;
+    if (in->ctas_per_sm) out->ctas_per_sm = in->ctas_per_sm;
+    if (in->rows_per_stage) out->rows_per_stage = in->rows_per_stage;
+    if (in->stages) out->stages = in->stages;
+    if (in->k_blocks_per_stage) out->k_blocks_per_stage = in->k_blocks_per_stage;
+    if (in->token_tile) out->token_tile = in->token_tile;
+    if (in->prefetch_stages) out->prefetch_stages = in->prefetch_stages;
+  }
+  out->path = SGR_PATH_W8;
+  sgr::W8Params p;
+  int grid = 0;
+  size_t smem = 0;
+  return sgr::w8_plan(*out, sms, M, N, K, &p, &grid, &smem);
+}
+
+int run_w8(const void* A, long long lda, const void* Wq, long long ldw, const float* scale, const void* R,
+           long long ldr, void* Y, long long ldy, int M, int N, int K, const sgr_config* cfg, unsigned flags,
+           void* stream_ptr) {
+  int rc = validate_w8(A, lda, Wq, ldw, scale, R, ldr, Y, ldy, M, N, K);
+  if (rc != SGR_OK) return rc;
+  if (M == 0 || N == 0) return SGR_OK;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  if (K == 0) {  // empty sum: Y = R
+    if (Y == R) return SGR_OK;
+    if (cudaMemcpy2DAsync(Y, (size_t)ldy * 2, R, (size_t)ldr * 2, (size_t)N * 2, (size_t)M,
+                          cudaMemcpyDeviceToDevice, stream) != cudaSuccess) {
+      cudaGetLastError();
+      return SGR_ERR_LAUNCH;
+    }
+    return SGR_OK;
+  }
+  int dev;
+  if ((rc = current_device(&dev)) != SGR_OK) return rc;
+  if ((rc = init_device(dev)) != SGR_OK) return rc;
+  DeviceState& st = g_dev[dev];
+  sgr_config c;
+  if ((rc = resolve_config_w8(st.sms, M, N, K, cfg, &c)) != SGR_OK) return rc;
+  return sgr::w8_launch(c, st.sms, st.err, A, lda, Wq, ldw, scale, R, ldr, Y, ldy, M, N, K,
+                        (flags & SGR_FLAG_NO_PDL) == 0, stream);
+}
+
 // ------------------------------------------------------------ grouped launch
 int run_grouped(const sgr_group* groups, int num_groups, int N, int K, const sgr_config* cfg, unsigned flags,
                 void* stream_ptr) {
@@ -574,6 +657,7 @@ int sgr_default_config(int device, int M, int N, int K, int path, sgr_config* cf
   }
   sgr_config in = {};
   in.path = path;
+  if (path == SGR_PATH_W8) return resolve_config_w8(sms, M, N, K, &in, cfg);
   return resolve_config(sms, M, N, K, &in, cfg);
 }
 
@@ -626,6 +710,19 @@ int sgr_kernel_resources(int device, int path, int M, int N, int K, int* regs, i
     if (sgr::rows_plan(c, sms, M, N, K, &rp, &grid, &smem) != SGR_OK) return SGR_ERR_UNSUPPORTED;
     *smem_bytes = (int)smem;
     *threads = sgr::kRowsThreads;
+  } else if (c.path == SGR_PATH_W8) {
+    if (cudaFuncGetAttributes(&fa, sgr::w8_rows_kernel) != cudaSuccess) {
+      cudaGetLastError();
+      return SGR_ERR_DEVICE;
+    }
+    sgr::W8Params wp;
+    int grid = 0;
+    size_t smem = 0;
+    int sms = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+    if (sgr::w8_plan(c, sms, M, N, K, &wp, &grid, &smem) != SGR_OK) return SGR_ERR_UNSUPPORTED;
+    *smem_bytes = (int)smem;
+    *threads = sgr::kW8Threads;
   } else if (c.path == SGR_PATH_TILE) {
     if (cudaFuncGetAttributes(&fa, sgr::tile_kernel_for(c.tile_n, sgr::tile_mode(c))) != cudaSuccess) {
       cudaGetLastError();
@@ -673,6 +770,17 @@ int skinny_gemm_residual_noalloc(const void* A, int64_t lda, const void* W, cons
                                  int64_t ldr, void* Y, int64_t ldy, int M, int N, int K,
                                  unsigned flags, void* stream) {
   return run_noalloc(A, lda, W, R, ldr, Y, ldy, M, N, K, flags, stream);
+}
+
+int skinny_gemm_residual_w8(const void* A, int64_t lda, const void* Wq, int64_t ldw, const float* scale,
+                            const void* R, int64_t ldr, void* Y, int64_t ldy, int M, int N, int K,
+                            const sgr_config* cfg, unsigned flags, void* stream) {
+  return run_w8(A, lda, Wq, ldw, scale, R, ldr, Y, ldy, M, N, K, cfg, flags, stream);
+}
+
+int sgr_validate_w8(const void* A, int64_t lda, const void* Wq, int64_t ldw, const float* scale, const void* R,
+                    int64_t ldr, const void* Y, int64_t ldy, int M, int N, int K) {
+  return validate_w8(A, lda, Wq, ldw, scale, R, ldr, Y, ldy, M, N, K);
 }
 
 }  // extern "C"

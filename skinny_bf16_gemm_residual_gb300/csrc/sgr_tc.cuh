@@ -105,6 +105,27 @@ __device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity
   }
 }
 
+// The same for waits that may last microseconds (a consumer ahead of its
+// producer, an epilogue waiting for the whole main loop, a CTA launched early
+// by programmatic dependent launch): after a short spin the thread sleeps
+// between polls (32 ns doubling to 256 ns), so that it does not take issue
+// slots from the warps that do the work on the same SM sub-partition.
+__device__ __forceinline__ bool mbar_wait_sleepy_or_abort(uint32_t bar, uint32_t parity,
+                                                          volatile int* abort_flag) {
+#pragma unroll 1
+  for (int i = 0; i < 8; ++i)
+    if (mbar_test_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  unsigned ns = 32;
+  while (true) {
+    __nanosleep(ns);
+    if (mbar_test_wait(bar, parity)) return true;
+    if (ns < 256) ns <<= 1;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > SGR_WAIT_LIMIT_NS) return false;
+  }
+}
+
 // 16 accumulator columns summed over the chains, chain 0 first (fixed order).
 __device__ __forceinline__ void tc_ld_chains(uint32_t taddr, int nt, int chains, float (&v)[16]) {
   tmem_ld16(taddr, v);

@@ -156,3 +156,48 @@ def test_grouped_rejects_before_launch():
 def test_grouped_nothing_to_do_needs_no_device():
     assert g_call([]) == sgr.SGR_OK
     assert g_call([grp(0, M=0), grp(1, M=0)]) == sgr.SGR_OK   # no expert received a token
+
+
+# ------------------------------------------------------------ FP8-weight entry point (host-side checks only)
+S_ = BASE + (4 << 32)
+
+
+def v8(A=A_, lda=3584, Wq=W_, ldw=3584, scale=S_, R=R_, ldr=7168, Y=Y_, ldy=7168, M=4, N=7168, K=3584):
+    return sgr.sgr_validate_w8_ptr(A, lda, Wq, ldw, scale, R, ldr, Y, ldy, M, N, K)
+
+
+def test_validate_w8_accepts_good_arguments():
+    assert v8() == sgr.SGR_OK
+    assert v8(M=256, ldw=3600) == sgr.SGR_OK            # padded code rows (multiple of 16 bytes)
+    assert v8(Y=R_) == sgr.SGR_OK                       # in-place residual
+    assert v8(M=0, A=0, Wq=0, scale=0, R=0, Y=0) == sgr.SGR_OK
+    assert v8(K=0, A=0, Wq=0, scale=0) == sgr.SGR_OK    # empty sum: Y = R
+    assert v8(scale=S_ + 4) == sgr.SGR_OK               # scales need only float alignment
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(M=-1), sgr.SGR_ERR_SHAPE),
+    (dict(K=3580, lda=3584, ldw=3584), sgr.SGR_ERR_SHAPE),
+    (dict(Wq=0), sgr.SGR_ERR_NULL),
+    (dict(scale=0), sgr.SGR_ERR_NULL),
+    (dict(ldw=3576), sgr.SGR_ERR_SHAPE),
+    (dict(ldw=3592), sgr.SGR_ERR_ALIGN),                # row stride not a multiple of 16 bytes
+    (dict(Wq=W_ + 8), sgr.SGR_ERR_ALIGN),
+    (dict(scale=S_ + 2), sgr.SGR_ERR_ALIGN),
+    (dict(Y=W_ + 4096), sgr.SGR_ERR_ALIAS),              # Y inside the codes
+    (dict(Y=S_ - 4096), sgr.SGR_ERR_ALIAS),              # Y runs into the scales
+    (dict(Y=A_), sgr.SGR_ERR_ALIAS),
+    (dict(Y=R_ + 16), sgr.SGR_ERR_ALIAS),
+])
+def test_validate_w8_rejects(kw, status):
+    assert v8(**kw) == status
+
+
+def test_w8_config_rejections_need_no_device():
+    """A path other than AUTO / W8, or tile-only fields, are refused before any launch."""
+    lib = sgr.load()
+    cfg = sgr.make_config(path=sgr.SGR_PATH_TILE)
+    rc = binding.skinny_gemm_residual_w8_ptr(A_, 3584, W_, 3584, S_, R_, 7168, Y_, 7168, 0, 7168, 3584,
+                                             cfg, 0, 0)
+    assert rc == sgr.SGR_OK  # M = 0: nothing to do, nothing checked further
+    assert lib.sgr_validate_w8(None, 3584, None, 3584, None, None, 7168, None, 7168, 4, 7168, 3584) == sgr.SGR_ERR_NULL
