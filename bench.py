@@ -97,6 +97,7 @@ KERNEL_SOURCES = {
     "rows_skinny_kernel": ("sgr_rows.cuh", "sgr_tc.cuh", "sgr_ptx.cuh"),
     "tc_skinny_kernel": ("sgr_tc.cuh", "sgr_ptx.cuh"),
     "tile_gemm_kernel": ("sgr_gemm.cuh", "sgr_tc.cuh", "sgr_ptx.cuh"),
+    "w8_rows_kernel": ("sgr_w8.cuh", "sgr_tc.cuh", "sgr_ptx.cuh"),
 }
 
 
@@ -468,6 +469,7 @@ def run_ours(args):
 
     chain = None if (args.skip_chain or rank != 0) else run_chain(sgr, device, stream)
     grouped = None if (args.skip_grouped or rank != 0) else run_grouped(sgr, device, stream)
+    w8 = None if (args.skip_w8 or rank != 0) else run_w8(sgr, device, stream, peaks)
 
     if rank != 0:
         return 0
@@ -522,6 +524,7 @@ def run_ours(args):
         "e2e": e2e_out,
         "chain": chain,
         "grouped": grouped,
+        "w8": w8,
         "gpu_launches": args.steps * launches_per_step,
         "clocks": clk,
         "peaks": {"hbm_gbs": peaks["hbm_gbs"], "source": peak_src},
@@ -606,6 +609,40 @@ def run_grouped(sgr, device, stream, experts: int = 8, tokens: int = 16, top_k: 
             "note": "one step = all experts with tokens; bytes = sum over those experts of 2*(N*K + M*K + 2*M*N)"}
 
 
+def run_w8(sgr, device, stream, peaks: dict, m_list=(1, 4, 16), copies: int = 8, replays: int = 50,
+           repeats: int = 9):
+    """Low-bit weight leg: the same projection with FP8 E4M3 weights and a
+    per-column scale (skinny_gemm_residual_w8).  Per M, one CUDA graph of
+    `copies` calls over distinct weight copies (8 x 25.7 MB, more than L2),
+    PDL on.  Bytes per call = N*K (codes) + 4N (scales) + 2MK + 4MN."""
+    import torch
+
+    from skinny_bf16_gemm_residual_gb300 import inputs
+
+    qs = [inputs.make_problem_w8(1, N_DIM, K_DIM, seed=7000 + c) for c in range(copies)]
+    Wq = [q.Wq.to(device) for q in qs]
+    Sc = [q.scale.to(device) for q in qs]
+    rows = []
+    for M in m_list:
+        A = inputs.make_rows(M, K_DIM, seed=8000 + M).to(device)
+        R = inputs.make_rows(M, N_DIM, seed=9000 + M).to(device)
+        Y = torch.empty((M, N_DIM), dtype=torch.bfloat16, device=device)
+        calls = [lambda c=c: sgr.skinny_gemm_residual_w8(A, Wq[c], Sc[c], R, Y, stream=stream) for c in range(copies)]
+        g = capture(calls, stream)
+        with torch.cuda.stream(stream):
+            for _ in range(5):
+                g.replay()
+        stream.synchronize()
+        us = summarize([t / copies for t in time_graph(g, stream, replays, repeats)])["median_us"]
+        del g
+        nbytes = N_DIM * K_DIM + 4 * N_DIM + 2 * M * K_DIM + 4 * M * N_DIM
+        gbs = nbytes / (us * 1e-6) / 1e9
+        rows.append({"m": M, "us": us, "bytes": nbytes, "gbs": gbs,
+                     "frac_of_hbm_peak": gbs / peaks["hbm_gbs"] if peaks.get("hbm_gbs") else None})
+    return {"kernel": "w8_rows_kernel", "per_m": rows,
+            "note": "FP8 E4M3 weights + FP32 per-column scale, BF16 A/R/Y; graph of 8 calls over distinct weight copies"}
+
+
 def run_e2e(sgr, per_m, Ws, m_list, device, stream, steps: int):
     """Each step: one host->device copy of the step's inputs (A for every M,
     R for every call) from a pinned host buffer, the public call for every
@@ -676,6 +713,7 @@ def main(argv=None):
     ap.add_argument("--skip-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--skip-chain", action="store_true", help="skip the 8-layer dependent chain leg")
     ap.add_argument("--skip-grouped", action="store_true", help="skip the mixture-of-experts grouped leg")
+    ap.add_argument("--skip-w8", action="store_true", help="skip the FP8-weight leg")
     ap.add_argument("--n", type=int, default=7168, help="output features (the headline shape is 7168)")
     ap.add_argument("--k", type=int, default=3584, help="input features (the headline shape is 3584)")
     args = ap.parse_args(argv)
