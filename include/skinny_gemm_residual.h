@@ -92,7 +92,8 @@ typedef enum {
 #define SGR_PATH_TC 2      /* tcgen05 kernel, persistent stream-K with split-K fixup */
 #define SGR_PATH_TC_ROWS 3 /* tcgen05 kernel, one contiguous W row slab per CTA (M <= 256) */
 #define SGR_PATH_TILE 4    /* tcgen05 kernel, 128-token x tile_n output tiles (large M) */
-#define SGR_PATH_W8 5      /* tcgen05 row-slab kernel for FP8 weights (skinny_gemm_residual_w8 only, M <= 256) */
+#define SGR_PATH_W8 5      /* tcgen05 row-slab kernel for FP8 weights (skinny_gemm_residual_w8 only, M <= 256);
+                              skinny_gemm_residual_w8 also takes SGR_PATH_SIMT (CUDA-core kernel, M <= 8) */
 
 /*
  * Y = bf16(A . W^T + R) with contiguous operands (lda = K, ldr = ldy = N).
@@ -288,11 +289,15 @@ int skinny_gemm_residual_grouped(const sgr_group* groups, int num_groups, int N,
  * wait, like W), graph capture and errors as for skinny_gemm_residual_ex; in
  * addition SGR_ERR_ALIGN for ldw not a multiple of 16 or a misaligned scale,
  * and SGR_ERR_ALIAS when Y overlaps Wq or scale.  `cfg` may be NULL (library
- * choice); its path must be SGR_PATH_AUTO or SGR_PATH_W8, and it may set
- * stages (depth of the weight-code ring, 2..16), prefetch_stages (depth of
- * the activation ring, 2..8), k_blocks_per_stage (64-wide K blocks per
- * stage: even, 2..8), token_tile and rows_per_stage (W rows per CTA, a
- * multiple of 8 up to 128).  Returns an sgr_status.
+ * choice).  Two kernels: SGR_PATH_W8, the tensor-core row-slab kernel (any
+ * M <= 256; cfg may set stages = depth of the weight-code ring 2..16,
+ * prefetch_stages = depth of the activation ring 2..8, k_blocks_per_stage =
+ * 64-wide K blocks per stage, even, 2..8, token_tile, and rows_per_stage = W
+ * rows per CTA, a multiple of 8 up to 128), and SGR_PATH_SIMT, the CUDA-core
+ * kernel (M <= 8, contiguous code rows ldw == K, K a multiple of 16; cfg may
+ * set ctas_per_sm, rows_per_stage = code rows per ring stage, stages).
+ * SGR_PATH_AUTO takes the CUDA-core kernel for M <= 2 where it can run, else
+ * the tensor-core kernel.  Returns an sgr_status.
  */
 int skinny_gemm_residual_w8(const void* A, int64_t lda, const void* Wq, int64_t ldw,
                             const float* scale, const void* R, int64_t ldr, void* Y,

@@ -60,6 +60,37 @@ SimtFn simt_fn(int mt, int vpt) {
   }
 }
 
+// FP8-weight instantiations (M <= 8).
+template <int MT>
+SimtFn simt_w8_fn_vpt(int vpt) {
+  switch (vpt) {
+    case 1: return sgr::simt_skinny_kernel<MT, 1, true>;
+    case 2: return sgr::simt_skinny_kernel<MT, 2, true>;
+    case 4: return sgr::simt_skinny_kernel<MT, 4, true>;
+    default: return nullptr;
+  }
+}
+
+SimtFn simt_w8_fn(int mt, int vpt) {
+  switch (mt) {
+    case 1: return simt_w8_fn_vpt<1>(vpt);
+    case 2: return simt_w8_fn_vpt<2>(vpt);
+    case 4: return simt_w8_fn_vpt<4>(vpt);
+    case 8: return simt_w8_fn_vpt<8>(vpt);
+    default: return nullptr;
+  }
+}
+
+// 16-code vectors per row slice: K a multiple of 16, K <= 224 * 16 * 4.
+int simt_w8_vpt(int K) {
+  if (K % 16 != 0) return 0;
+  const int kv = K / 16;
+  if (kv <= sgr::kSimtConsumers) return 1;
+  if (kv <= 2 * sgr::kSimtConsumers) return 2;
+  if (kv <= 4 * sgr::kSimtConsumers) return 4;
+  return 0;
+}
+
 int simt_mt(int M) {
   if (M <= 1) return 1;
   if (M <= 2) return 2;
@@ -149,9 +180,13 @@ int init_device(int dev) {
     const int mts[5] = {1, 2, 4, 8, 16};
     const int vpts[3] = {1, 2, 4};
     for (int mt : mts)
-      for (int v : vpts)
+      for (int v : vpts) {
         if (ok == SGR_OK && sgr::set_kernel_smem_attrs(reinterpret_cast<const void*>(simt_fn(mt, v))) != cudaSuccess)
           ok = SGR_ERR_DEVICE;
+        if (ok == SGR_OK && mt <= 8 &&
+            sgr::set_kernel_smem_attrs(reinterpret_cast<const void*>(simt_w8_fn(mt, v))) != cudaSuccess)
+          ok = SGR_ERR_DEVICE;
+      }
     if (ok == SGR_OK && sgr::tc_init_device(sms, &st.ws) != cudaSuccess) ok = SGR_ERR_DEVICE;
     if (ok == SGR_OK && sgr::rows_init_device() != cudaSuccess) ok = SGR_ERR_DEVICE;
     if (ok == SGR_OK && sgr::tile_init_device() != cudaSuccess) ok = SGR_ERR_DEVICE;
@@ -333,6 +368,46 @@ int launch_simt(const sgr_config& c, int sms, unsigned* err, const void* A, long
   return SGR_OK;
 }
 
+int launch_simt_w8(const sgr_config& c, int sms, unsigned* err, const void* A, long long lda, const void* Wq,
+                   const float* scale, const void* R, long long ldr, void* Y, long long ldy, int M, int N, int K,
+                   unsigned flags, cudaStream_t stream) {
+  SimtFn fn = simt_w8_fn(simt_mt(M), simt_w8_vpt(K));
+  if (!fn) return SGR_ERR_UNSUPPORTED;
+  sgr::SimtParams p;
+  std::memset(&p, 0, sizeof p);
+  p.A = static_cast<const __nv_bfloat16*>(A);
+  p.Wq = static_cast<const uint8_t*>(Wq);
+  p.scale = scale;
+  p.R = static_cast<const __nv_bfloat16*>(R);
+  p.Y = static_cast<__nv_bfloat16*>(Y);
+  p.lda = lda;
+  p.ldr = ldr;
+  p.ldy = ldy;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.rows_per_stage = c.rows_per_stage;
+  p.stages = c.stages;
+  p.err = err;
+  long long grid = (long long)sms * c.ctas_per_sm;
+  if (grid > N) grid = N;
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3((unsigned)grid, 1, 1);
+  lc.blockDim = dim3(sgr::kSimtThreads, 1, 1);
+  lc.dynamicSmemBytes = sgr::simt_smem_bytes(c.stages, c.rows_per_stage, K, 1);
+  lc.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = (flags & SGR_FLAG_NO_PDL) ? 0 : 1;
+  if (cudaLaunchKernelEx(&lc, fn, p) != cudaSuccess) {
+    cudaGetLastError();
+    return SGR_ERR_LAUNCH;
+  }
+  return SGR_OK;
+}
+
 int run(const void* A, long long lda, const void* W, const void* R, long long ldr, void* Y,
         long long ldy, int M, int N, int K, const sgr_config* cfg, unsigned flags,
         void* stream_ptr) {
@@ -489,13 +564,56 @@ int validate_w8(const void* A, long long lda, const void* Wq, long long ldw, con
   return SGR_OK;
 }
 
-// Configuration of the FP8-weight kernel: the library default for this
-// shape, then any non-zero field of `in` (path must be AUTO or W8).
-int resolve_config_w8(int sms, int M, int N, int K, const sgr_config* in, sgr_config* out) {
+// The CUDA-core FP8 kernel runs M <= 8 with contiguous code rows (one bulk
+// copy per ring stage) and K a multiple of 16.
+bool simt_w8_supported(int M, int K, long long ldw) {
+  return M >= 1 && M <= 8 && ldw == K && simt_w8_vpt(K) > 0;
+}
+
+// The library chooses the CUDA-core kernel up to this many tokens (measured:
+// 10.6 / 11.5 us at M = 1 / 2 against 13.1 for the tensor-core kernel; at
+// M = 4 the two are equal, beyond it the CUDA-core kernel is slower).
+constexpr int kW8SimtMaxM = 2;
+
+// CUDA-core FP8 configuration: ring stages of two code rows, 4 stages,
+// CTAs per SM by token count (the register footprint grows with M).
+void default_simt_w8_config(int M, sgr_config* c) {
+  std::memset(c, 0, sizeof *c);
+  c->path = SGR_PATH_SIMT;
+  c->ctas_per_sm = M <= 2 ? 3 : (M <= 4 ? 2 : 1);
+  c->rows_per_stage = 2;
+  c->stages = 4;
+}
+
+// Configuration of the FP8-weight kernels: the library default for this
+// shape, then any non-zero field of `in` (path AUTO, W8 or SIMT).
+int resolve_config_w8(int sms, int M, int N, int K, long long ldw, const sgr_config* in, sgr_config* out) {
+  int path = in ? in->path : SGR_PATH_AUTO;
+  if (path == SGR_PATH_AUTO)
+    path = (M <= kW8SimtMaxM && simt_w8_supported(M, K, ldw)) ? SGR_PATH_SIMT : SGR_PATH_W8;
+  if (path == SGR_PATH_SIMT) {
+    if (!simt_w8_supported(M, K, ldw)) return SGR_ERR_UNSUPPORTED;
+    default_simt_w8_config(M, out);
+    if (in) {
+      for (int r : in->reserved)
+        if (r != 0) return SGR_ERR_UNSUPPORTED;
+      if (in->tile_n || in->k_split || in->pair_w || in->k_blocks_per_stage || in->token_tile ||
+          in->prefetch_stages)
+        return SGR_ERR_UNSUPPORTED;
+      if (in->ctas_per_sm) out->ctas_per_sm = in->ctas_per_sm;
+      if (in->rows_per_stage) out->rows_per_stage = in->rows_per_stage;
+      if (in->stages) out->stages = in->stages;
+    }
+    if (out->ctas_per_sm < 1 || out->ctas_per_sm > 8 || out->stages < 2 || out->stages > 16) return SGR_ERR_UNSUPPORTED;
+    if (out->rows_per_stage < 1 || out->rows_per_stage > 64) return SGR_ERR_UNSUPPORTED;
+    if (sgr::simt_smem_bytes(out->stages, out->rows_per_stage, K, 1) > (size_t)kMaxDynSmem)
+      return SGR_ERR_UNSUPPORTED;
+    return SGR_OK;
+  }
+  if (path != SGR_PATH_W8) return SGR_ERR_UNSUPPORTED;
   if (!sgr::w8_supported(sms, M, N, K)) return SGR_ERR_UNSUPPORTED;
   sgr::w8_default_config(sms, M, N, K, out);
   if (in) {
-    if (in->path != SGR_PATH_AUTO && in->path != SGR_PATH_W8) return SGR_ERR_UNSUPPORTED;
     for (int r : in->reserved)
       if (r != 0) return SGR_ERR_UNSUPPORTED;
     if (in->tile_n || in->k_split || in->pair_w) return SGR_ERR_UNSUPPORTED;
@@ -534,7 +652,9 @@ int run_w8(const void* A, long long lda, const void* Wq, long long ldw, const fl
   if ((rc = init_device(dev)) != SGR_OK) return rc;
   DeviceState& st = g_dev[dev];
   sgr_config c;
-  if ((rc = resolve_config_w8(st.sms, M, N, K, cfg, &c)) != SGR_OK) return rc;
+  if ((rc = resolve_config_w8(st.sms, M, N, K, ldw, cfg, &c)) != SGR_OK) return rc;
+  if (c.path == SGR_PATH_SIMT)
+    return launch_simt_w8(c, st.sms, st.err, A, lda, Wq, scale, R, ldr, Y, ldy, M, N, K, flags, stream);
   return sgr::w8_launch(c, st.sms, st.err, A, lda, Wq, ldw, scale, R, ldr, Y, ldy, M, N, K,
                         (flags & SGR_FLAG_NO_PDL) == 0, stream);
 }
@@ -657,7 +777,7 @@ int sgr_default_config(int device, int M, int N, int K, int path, sgr_config* cf
   }
   sgr_config in = {};
   in.path = path;
-  if (path == SGR_PATH_W8) return resolve_config_w8(sms, M, N, K, &in, cfg);
+  if (path == SGR_PATH_W8) return resolve_config_w8(sms, M, N, K, K, &in, cfg);
   return resolve_config(sms, M, N, K, &in, cfg);
 }
 

@@ -25,10 +25,18 @@
 //    with the warp's total for output l, the 7 warps' totals meet in shared
 //    memory, and warp 0 adds R (loaded early, while W streams), rounds once
 //    and stores.
+//
+// The W8 instantiation is the low-bit weight variant (FP8 E4M3 codes Wq with
+// one FP32 scale per output column, the quantized-weight decode direction of
+// the bitsandbytes "QLORA-2" page): the ring carries rows of K codes (half
+// the bytes), each 16-byte vector holds 16 codes, which are widened exactly
+// in registers (sgr_e4m3.cuh) before the FP32 FMAs, and the epilogue computes
+// fmaf(sum, scale[n] * 2^8, R) with one rounding.
 #pragma once
 
 #include <cuda_bf16.h>
 
+#include "sgr_e4m3.cuh"
 #include "sgr_ptx.cuh"
 
 namespace sgr {
@@ -40,7 +48,9 @@ constexpr int kSimtRPrefetch = 4;  // reduction batches whose residuals are load
 
 struct SimtParams {
   const __nv_bfloat16* A;  // [M, K], row stride lda (elements)
-  const __nv_bfloat16* W;  // [N, K], contiguous rows
+  const __nv_bfloat16* W;  // [N, K], contiguous rows (BF16 weights)
+  const uint8_t* Wq;       // [N, K], contiguous rows of E4M3 codes (W8 only)
+  const float* scale;      // [N] per-column scales (W8 only)
   const __nv_bfloat16* R;  // [M, N], row stride ldr
   __nv_bfloat16* Y;        // [M, N], row stride ldy
   long long lda, ldr, ldy;
@@ -55,8 +65,8 @@ __host__ __device__ constexpr size_t simt_ring_offset(int stages) {
   return ((size_t)stages * 16 + 2 * kSimtConsumerWarps * 32 * 4 + 127) / 128 * 128;
 }
 
-__host__ __device__ constexpr size_t simt_smem_bytes(int stages, int rows_per_stage, int K) {
-  return simt_ring_offset(stages) + (size_t)stages * rows_per_stage * K * 2;
+__host__ __device__ constexpr size_t simt_smem_bytes(int stages, int rows_per_stage, int K, int elem_bytes = 2) {
+  return simt_ring_offset(stages) + (size_t)stages * rows_per_stage * K * elem_bytes;
 }
 
 // Butterfly over 32 lanes that also transposes: on entry each lane holds 32
@@ -82,12 +92,13 @@ __device__ __forceinline__ float transpose_reduce32(float (&x)[32], int lane) {
 }
 
 // MT: rows of A handled (M <= MT, rows >= M masked); VPT: 16-byte K vectors
-// per consumer thread (K <= 224 * 8 * VPT).
-template <int MT, int VPT>
+// per consumer thread (K <= 224 * EPV * VPT); W8: E4M3 codes + scales.
+template <int MT, int VPT, bool W8 = false>
 __global__ void __launch_bounds__(kSimtThreads, (MT <= 2 ? 3 : (MT <= 4 ? 2 : 1)))
     simt_skinny_kernel(const SimtParams p) {
-  constexpr int B = 32 / MT;                    // rows per reduction batch
-  constexpr bool kPackedA = MT * VPT * 8 > 64;  // keep A as bf16x2 when large
+  constexpr int B = 32 / MT;                      // rows per reduction batch
+  constexpr int EPV = W8 ? 16 : 8;                // weight elements per 16-byte vector
+  constexpr bool kPackedA = MT * VPT * EPV > 64;  // keep A as bf16x2 when large
   extern __shared__ __align__(128) unsigned char smem[];
 
   const int S = p.stages;
@@ -104,7 +115,7 @@ __global__ void __launch_bounds__(kSimtThreads, (MT <= 2 ? 3 : (MT <= 4 ? 2 : 1)
   const int n1 = (int)((long long)p.N * (c + 1) / G);
   const int nrows = n1 - n0;
   const int nstages = (nrows + RS - 1) / RS;
-  const int KV = p.K >> 3;
+  const int KV = W8 ? (p.K >> 4) : (p.K >> 3);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -123,8 +134,9 @@ __global__ void __launch_bounds__(kSimtThreads, (MT <= 2 ? 3 : (MT <= 4 ? 2 : 1)
     // ---------------- producer: stream this CTA's W slab through the ring
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
-      const uint32_t row_bytes = (uint32_t)p.K * 2u;
-      const char* wbase = reinterpret_cast<const char*>(p.W) + (size_t)n0 * row_bytes;
+      const uint32_t row_bytes = (uint32_t)p.K * (W8 ? 1u : 2u);
+      const char* wbase = (W8 ? reinterpret_cast<const char*>(p.Wq) : reinterpret_cast<const char*>(p.W)) +
+                          (size_t)n0 * row_bytes;
       // Ring position kept by increments: no integer division on the
       // per-stage path of this single issuing thread.
       int issued = 0;
@@ -168,24 +180,27 @@ __global__ void __launch_bounds__(kSimtThreads, (MT <= 2 ? 3 : (MT <= 4 ? 2 : 1)
   // ---------------- consumers
   pdl_wait();  // A and R may be produced by the preceding kernel; Y may be read by it
 
-  // This thread's K slice of A, loaded once.
-  float af[kPackedA ? 1 : MT][kPackedA ? 1 : VPT][8];
-  uint32_t ap[kPackedA ? MT : 1][kPackedA ? VPT : 1][4];
+  // This thread's K slice of A (EPV elements per vector), loaded once.
+  float af[kPackedA ? 1 : MT][kPackedA ? 1 : VPT][EPV];
+  uint32_t ap[kPackedA ? MT : 1][kPackedA ? VPT : 1][EPV / 2];
 #pragma unroll
   for (int m = 0; m < MT; ++m) {
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
       const int vid = threadIdx.x + v * kSimtConsumers;
-      uint4 q = make_uint4(0u, 0u, 0u, 0u);
-      if (m < p.M && vid < KV)
-        q = *reinterpret_cast<const uint4*>(p.A + (size_t)m * p.lda + (size_t)vid * 8);
-      if constexpr (kPackedA) {
-        ap[m][v][0] = q.x; ap[m][v][1] = q.y; ap[m][v][2] = q.z; ap[m][v][3] = q.w;
-      } else {
-        af[m][v][0] = bf16lo(q.x); af[m][v][1] = bf16hi(q.x);
-        af[m][v][2] = bf16lo(q.y); af[m][v][3] = bf16hi(q.y);
-        af[m][v][4] = bf16lo(q.z); af[m][v][5] = bf16hi(q.z);
-        af[m][v][6] = bf16lo(q.w); af[m][v][7] = bf16hi(q.w);
+#pragma unroll
+      for (int h = 0; h < EPV / 8; ++h) {
+        uint4 q = make_uint4(0u, 0u, 0u, 0u);
+        if (m < p.M && vid < KV)
+          q = *reinterpret_cast<const uint4*>(p.A + (size_t)m * p.lda + (size_t)vid * EPV + h * 8);
+        if constexpr (kPackedA) {
+          ap[m][v][4 * h + 0] = q.x; ap[m][v][4 * h + 1] = q.y; ap[m][v][4 * h + 2] = q.z; ap[m][v][4 * h + 3] = q.w;
+        } else {
+          af[m][v][8 * h + 0] = bf16lo(q.x); af[m][v][8 * h + 1] = bf16hi(q.x);
+          af[m][v][8 * h + 2] = bf16lo(q.y); af[m][v][8 * h + 3] = bf16hi(q.y);
+          af[m][v][8 * h + 4] = bf16lo(q.z); af[m][v][8 * h + 5] = bf16hi(q.z);
+          af[m][v][8 * h + 6] = bf16lo(q.w); af[m][v][8 * h + 7] = bf16hi(q.w);
+        }
       }
     }
   }
@@ -194,12 +209,14 @@ __global__ void __launch_bounds__(kSimtThreads, (MT <= 2 ? 3 : (MT <= 4 ? 2 : 1)
   // on memory (warp 0 stores; lane l handles output l of each batch).
   constexpr int kB = 32 / MT;
   float rpre[kSimtRPrefetch];
+  float spre[W8 ? kSimtRPrefetch : 1];  // scales * 2^8 of the same outputs (W8)
 #pragma unroll
   for (int b = 0; b < kSimtRPrefetch; ++b) {
     const int j = lane / MT, m = lane % MT, row = b * kB + j;
     rpre[b] = (warp == 0 && row < nrows && m < p.M)
                   ? __bfloat162float(p.R[(size_t)m * p.ldr + n0 + row])
                   : 0.f;
+    if constexpr (W8) spre[b] = (warp == 0 && row < nrows) ? p.scale[n0 + row] * kE4m3Unscale : 0.f;
   }
 
   bool ok = true;
@@ -208,7 +225,7 @@ __global__ void __launch_bounds__(kSimtThreads, (MT <= 2 ? 3 : (MT <= 4 ? 2 : 1)
   int slot = 0, rr = 0;   // ring slot of the current stage, row within the stage
   uint32_t phase = 0;     // parity of the current stage's fill of that slot
   const uint32_t ring_base = smem_u32(ring);
-  const uint32_t row_bytes = (uint32_t)p.K * 2u;
+  const uint32_t row_bytes = (uint32_t)p.K * (W8 ? 1u : 2u);
   uint32_t row_addr = ring_base;
   for (int base = 0; base < nrows; base += B, ++bi) {
     float acc[32];
@@ -228,21 +245,35 @@ __global__ void __launch_bounds__(kSimtThreads, (MT <= 2 ? 3 : (MT <= 4 ? 2 : 1)
             const int vid = threadIdx.x + v * kSimtConsumers;
             if (vid < KV) {
               const uint4 q = lds128(row_addr + (uint32_t)vid * 16u);
-              float w[8];
-              w[0] = bf16lo(q.x); w[1] = bf16hi(q.x); w[2] = bf16lo(q.y); w[3] = bf16hi(q.y);
-              w[4] = bf16lo(q.z); w[5] = bf16hi(q.z); w[6] = bf16lo(q.w); w[7] = bf16hi(q.w);
+              uint32_t wp[EPV / 2];  // weights as BF16 pairs
+              if constexpr (W8) {
+                const uint32_t x[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  wp[2 * i] = e4m3x2_to_bf16x2_scaled<0x9180u>(x[i]);
+                  wp[2 * i + 1] = e4m3x2_to_bf16x2_scaled<0xB3A2u>(x[i]);
+                }
+              } else {
+                wp[0] = q.x; wp[1] = q.y; wp[2] = q.z; wp[3] = q.w;
+              }
+              float w[EPV];
+#pragma unroll
+              for (int i = 0; i < EPV / 2; ++i) {
+                w[2 * i] = bf16lo(wp[i]);
+                w[2 * i + 1] = bf16hi(wp[i]);
+              }
 #pragma unroll
               for (int m = 0; m < MT; ++m) {
                 float t = acc[j * MT + m];
                 if constexpr (kPackedA) {
 #pragma unroll
-                  for (int e = 0; e < 4; ++e) {
+                  for (int e = 0; e < EPV / 2; ++e) {
                     t = fmaf(bf16lo(ap[m][v][e]), w[2 * e], t);
                     t = fmaf(bf16hi(ap[m][v][e]), w[2 * e + 1], t);
                   }
                 } else {
 #pragma unroll
-                  for (int e = 0; e < 8; ++e) t = fmaf(af[m][v][e], w[e], t);
+                  for (int e = 0; e < EPV; ++e) t = fmaf(af[m][v][e], w[e], t);
                 }
                 acc[j * MT + m] = t;
               }
@@ -283,7 +314,16 @@ __global__ void __launch_bounds__(kSimtThreads, (MT <= 2 ? 3 : (MT <= 4 ? 2 : 1)
         for (int k = 0; k < kSimtRPrefetch; ++k)
           if (k == bi) r = rpre[k];
         if (bi >= kSimtRPrefetch) r = __bfloat162float(p.R[(size_t)m * p.ldr + n]);
-        p.Y[(size_t)m * p.ldy + n] = __float2bfloat16_rn(total + r);
+        if constexpr (W8) {
+          float sc = 0.f;
+#pragma unroll
+          for (int k = 0; k < kSimtRPrefetch; ++k)
+            if (k == bi) sc = spre[k];
+          if (bi >= kSimtRPrefetch) sc = p.scale[n] * kE4m3Unscale;
+          p.Y[(size_t)m * p.ldy + n] = __float2bfloat16_rn(fmaf(total, sc, r));
+        } else {
+          p.Y[(size_t)m * p.ldy + n] = __float2bfloat16_rn(total + r);
+        }
       }
     }
     buf ^= 1;

@@ -22,17 +22,11 @@
 // widened weights never go back through shared memory: per weight byte there
 // is one TMA write and one shared-memory read.
 //
-// Widening, exact for every code: placing the code's seven magnitude bits
-// eeee.fff at bits 10-4 of a BF16 pattern (sign at bit 15) gives a BF16 whose
-// exponent field is the code's unbiased one, the code's value times 2^-120
-// (zero and subnormal codes land on BF16 zero and subnormals); one BF16x2
-// multiply by 2^112 then gives the code's value times 2^-8, exactly (a
-// power-of-two product, normal or zero).  Per two codes: a byte permute that
-// also replicates the sign, a shift, a mask and the multiply.  The 2^8 comes
-// back in the epilogue, where the FP32 sum is multiplied by scale * 2^8 (a
-// power-of-two product, exact).  The NaN codes (0x7F, 0xFF) are outside the
-// supported domain: a saturating quantiser never writes them, and the kernel
-// reads them as +-480.
+// Widening (sgr_e4m3.cuh): exact for every code, one byte permute, a shift,
+// a mask and a BF16x2 multiply per two codes, giving code * 2^-8; the
+// epilogue multiplies the FP32 sum by scale * 2^8 (exact).  The NaN codes
+// (0x7F, 0xFF) are outside the supported domain: a saturating quantiser never
+// writes them, and the kernel reads them as +-480.
 //
 // Warp roles (352 threads): warp 0 lane 0 streams the weight codes with TMA
 // into their own ring, released by the converters (the codes do not depend on
@@ -49,6 +43,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "sgr_e4m3.cuh"
 #include "sgr_ptx.cuh"
 #include "sgr_tc.cuh"
 #include "skinny_gemm_residual.h"
@@ -94,30 +89,13 @@ __host__ __device__ inline size_t w8_smem_bytes(int stages, int a_stages, int kb
          (size_t)a_stages * w8_astage_bytes(kbps, nt) + w8_rtile_bytes(rb, nt);
 }
 
-// Two E4M3 codes (bytes SEL of x) -> two BF16 patterns holding code * 2^-8,
-// exact for every code but NaN.  The permute puts each code in the low byte
-// of its 16-bit half with its sign replicated in the high byte; the shift and
-// mask leave s | eeee.fff << 4, the BF16 pattern whose exponent field is the
-// code's unbiased one: code * 2^-120 (BF16 subnormals for e = 0, where the
-// code itself is subnormal or zero).  The BF16x2 multiply by 2^112 is exact
-// (a power of two, the result normal or zero; BF16 arithmetic keeps
-// subnormal inputs).
-template <uint32_t SEL>
-__device__ __forceinline__ uint32_t w8_widen2(uint32_t x) {
-  uint32_t t, d;
-  asm("prmt.b32 %0, %1, 0, %2;" : "=r"(t) : "r"(x), "n"(SEL));
-  t = (t << 4) & 0x87F087F0u;
-  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(t), "r"(0x77807780u));  // 0x7780 = 2^112
-  return d;
-}
-
 // 32 codes (8 words, code i in byte i%4 of word i/4) -> 16 words of BF16
 // pairs (column c holds codes 2c, 2c+1, the lower in the low half).
 __device__ __forceinline__ void w8_widen32(const uint32_t (&x)[8], uint32_t (&o)[16]) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    o[2 * i] = w8_widen2<0x9180u>(x[i]);
-    o[2 * i + 1] = w8_widen2<0xB3A2u>(x[i]);
+    o[2 * i] = e4m3x2_to_bf16x2_scaled<0x9180u>(x[i]);
+    o[2 * i + 1] = e4m3x2_to_bf16x2_scaled<0xB3A2u>(x[i]);
   }
 }
 
@@ -311,7 +289,7 @@ __global__ void __launch_bounds__(kW8Threads, 2)
     const bool epi = half == 0;
     // Scale of the output column this lane may own (a weight: readable before the dependency wait).
     const bool owner = epi && L < p.RB && n0 + L < p.N;
-    const float sc = owner ? p.scale[n0 + L] * 256.0f : 0.f;
+    const float sc = owner ? p.scale[n0 + L] * kE4m3Unscale : 0.f;
     if (q * 32 < G * p.RB) {  // warp-uniform: the quarter holds rows of the window
       int g = L / p.RB, r = L - g * p.RB;
       if (g >= G) {  // lanes past the window duplicate a real row (their TMEM rows are never read)
@@ -488,7 +466,7 @@ __global__ void __launch_bounds__(kW8Threads, 2)
             const int rr = item % p.RB, c16 = item / p.RB;
             const int n = n0 + rr;
             if (n >= p.N) continue;
-            const float scn = p.scale[n] * 256.0f;
+            const float scn = p.scale[n] * kE4m3Unscale;
             float acc[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) acc[i] = 0.f;

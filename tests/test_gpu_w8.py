@@ -253,7 +253,7 @@ def test_w8_empty_and_k0():
 def test_w8_rejects_bad_config():
     p = inputs.make_problem_w8(20, 256, 256, seed=1)
     A, Wq, sc, R = p.A.cuda(), p.Wq.cuda(), p.scale.cuda(), p.R.cuda()
-    for cfg in (dict(path=sgr.SGR_PATH_TC_ROWS), dict(path=sgr.SGR_PATH_W8, token_tile=16),
+    for cfg in (dict(path=sgr.SGR_PATH_TC_ROWS), dict(path=sgr.SGR_PATH_TILE), dict(path=sgr.SGR_PATH_W8, token_tile=16),
                 dict(path=sgr.SGR_PATH_W8, k_blocks_per_stage=3), dict(path=sgr.SGR_PATH_W8, stages=17),
                 dict(path=sgr.SGR_PATH_W8, rows_per_stage=20), dict(path=sgr.SGR_PATH_W8, tile_n=128),
                 dict(path=sgr.SGR_PATH_W8, prefetch_stages=9), dict(path=sgr.SGR_PATH_W8, stages=8, prefetch_stages=1)):
@@ -263,4 +263,79 @@ def test_w8_rejects_bad_config():
     with pytest.raises(sgr.SgrError) as e:  # more than 256 tokens
         q = inputs.make_problem_w8(257, 256, 256, seed=2)
         sgr.skinny_gemm_residual_w8(q.A.cuda(), q.Wq.cuda(), q.scale.cuda(), q.R.cuda())
+    assert e.value.status == sgr.SGR_ERR_UNSUPPORTED
+
+
+# ------------------------------------------------------------------ CUDA-core FP8 kernel (M <= 8)
+SIMT = sgr.SGR_PATH_SIMT
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 8])
+def test_w8_simt_full_size(M):
+    p = inputs.make_problem_w8(M, N_FULL, K_FULL, seed=300 + M)
+    compare(run(p, path=SIMT), ref(p), f"w8 simt M={M}")
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 520, 272), (3, 304, 16), (4, 2056, 3584), (8, 152, 1792), (2, 8, 7168),
+                                   (1, 1000, 14336), (7, 1512, 1808)])
+def test_w8_simt_small_shapes(M, N, K):
+    p = codes_problem(M, N, K, seed=M + N + K + 1)
+    compare(run(p, path=SIMT), ref(p), f"w8 simt random codes {M}x{N}x{K}")
+
+
+def test_w8_simt_subnormal_codes():
+    p = codes_problem(4, 1024, 1024, seed=6, mask=0x8F)
+    p.scale.mul_(2.0 ** 12)
+    compare(run(p, path=SIMT), ref(p), "w8 simt subnormal codes")
+
+
+SIMT_CONFIGS = [dict(ctas_per_sm=1, rows_per_stage=4, stages=4), dict(ctas_per_sm=2, rows_per_stage=1, stages=8),
+                dict(ctas_per_sm=3, rows_per_stage=2, stages=2), dict(ctas_per_sm=1, rows_per_stage=16, stages=3)]
+
+
+@pytest.mark.parametrize("cfg", SIMT_CONFIGS, ids=lambda c: "-".join(f"{k}{v}" for k, v in c.items()))
+@pytest.mark.parametrize("M", [1, 4])
+def test_w8_simt_configs(cfg, M):
+    p = inputs.make_problem_w8(M, N_FULL, K_FULL, seed=400 + M)
+    compare(run(p, path=SIMT, **cfg), ref(p), f"w8 simt M={M} {cfg}")
+
+
+def test_w8_simt_strided_in_place():
+    M, N, K = 3, 2048, 1024
+    p = inputs.make_problem_w8(M, N, K, seed=57)
+    Abig = torch.zeros((M, K + 64), dtype=torch.bfloat16, device="cuda")
+    A = Abig[:, 32:32 + K]
+    A.copy_(p.A)
+    RY = torch.zeros((M, N + 16), dtype=torch.bfloat16, device="cuda")
+    view = RY[:, 8:8 + N]
+    view.copy_(p.R)
+    sgr.skinny_gemm_residual_w8(A, p.Wq.cuda(), p.scale.cuda(), view, view,
+                                config=sgr.make_config(path=SIMT))
+    torch.cuda.synchronize()
+    compare(bits(view), ref(p), "w8 simt strided in place")
+
+
+def test_w8_auto_small_m_matches_tensor_core_path():
+    """AUTO picks the CUDA-core kernel for M <= 2; both kernels agree with the oracle."""
+    p = inputs.make_problem_w8(2, N_FULL, K_FULL, seed=58)
+    want = ref(p)
+    compare(run(p), want, "w8 auto M=2")
+    compare(run(p, path=sgr.SGR_PATH_W8), want, "w8 tensor-core M=2")
+
+
+def test_w8_simt_rejects():
+    p = inputs.make_problem_w8(9, 256, 256, seed=3)
+    with pytest.raises(sgr.SgrError) as e:  # more than 8 tokens
+        sgr.skinny_gemm_residual_w8(p.A.cuda(), p.Wq.cuda(), p.scale.cuda(), p.R.cuda(),
+                                    config=sgr.make_config(path=SIMT))
+    assert e.value.status == sgr.SGR_ERR_UNSUPPORTED
+    q = inputs.make_problem_w8(2, 256, 264, seed=4)  # K not a multiple of 16 (padded code rows)
+    with pytest.raises(sgr.SgrError) as e:
+        sgr.skinny_gemm_residual_w8(q.A.cuda(), codes_on_device(q.Wq), q.scale.cuda(), q.R.cuda(),
+                                    config=sgr.make_config(path=SIMT))
+    assert e.value.status == sgr.SGR_ERR_UNSUPPORTED
+    r = inputs.make_problem_w8(2, 256, 256, seed=5)
+    with pytest.raises(sgr.SgrError) as e:  # a tile-only field
+        sgr.skinny_gemm_residual_w8(r.A.cuda(), r.Wq.cuda(), r.scale.cuda(), r.R.cuda(),
+                                    config=sgr.make_config(path=SIMT, token_tile=16))
     assert e.value.status == sgr.SGR_ERR_UNSUPPORTED
