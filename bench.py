@@ -609,7 +609,7 @@ def run_grouped(sgr, device, stream, experts: int = 8, tokens: int = 16, top_k: 
             "note": "one step = all experts with tokens; bytes = sum over those experts of 2*(N*K + M*K + 2*M*N)"}
 
 
-def run_w8(sgr, device, stream, peaks: dict, m_list=(1, 4, 16), copies: int = 8, replays: int = 50,
+def run_w8(sgr, device, stream, peaks: dict, m_list=(1, 2, 4, 16), copies: int = 8, replays: int = 50,
            repeats: int = 9):
     """Low-bit weight leg: the same projection with FP8 E4M3 weights and a
     per-column scale (skinny_gemm_residual_w8).  Per M, one CUDA graph of
@@ -637,10 +637,12 @@ def run_w8(sgr, device, stream, peaks: dict, m_list=(1, 4, 16), copies: int = 8,
         del g
         nbytes = N_DIM * K_DIM + 4 * N_DIM + 2 * M * K_DIM + 4 * M * N_DIM
         gbs = nbytes / (us * 1e-6) / 1e9
-        rows.append({"m": M, "us": us, "bytes": nbytes, "gbs": gbs,
+        rows.append({"m": M, "kernel": "simt_skinny_kernel<W8>" if M <= 2 else "w8_rows_kernel",
+                     "us": us, "bytes": nbytes, "gbs": gbs,
                      "frac_of_hbm_peak": gbs / peaks["hbm_gbs"] if peaks.get("hbm_gbs") else None})
-    return {"kernel": "w8_rows_kernel", "per_m": rows,
-            "note": "FP8 E4M3 weights + FP32 per-column scale, BF16 A/R/Y; graph of 8 calls over distinct weight copies"}
+    return {"per_m": rows,
+            "note": "FP8 E4M3 weights + FP32 per-column scale, BF16 A/R/Y; graph of 8 calls over distinct weight "
+                    "copies; the library's own kernel choice (CUDA-core kernel for M <= 2, tensor-core row slab above)"}
 
 
 def run_e2e(sgr, per_m, Ws, m_list, device, stream, steps: int):
