@@ -309,6 +309,18 @@ int sgr_validate_w8(const void* A, int64_t lda, const void* Wq, int64_t ldw,
                     const float* scale, const void* R, int64_t ldr, const void* Y,
                     int64_t ldy, int M, int N, int K);
 
+/*
+ * Self-test of the failure path of the kernels' bounded waits: on the
+ * current device, one thread waits on an mbarrier that nothing arrives on,
+ * gives up after limit_us microseconds (1..100000) of the GPU's global timer
+ * and records the timeout in the device error word, as a kernel's wait does
+ * after its one-second limit.  The call clears the word, runs the wait,
+ * synchronises, writes the recorded code to *code (1 = a consumer gave up
+ * waiting for its data) and clears the word again.  Nothing faults or hangs
+ * and the context stays usable.  Returns an sgr_status.
+ */
+int sgr_selftest_wait_timeout(unsigned limit_us, unsigned* code);
+
 #ifdef __cplusplus
 }
 #endif

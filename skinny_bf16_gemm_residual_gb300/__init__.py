@@ -55,4 +55,5 @@ from .binding import (  # noqa: F401
     skinny_gemm_residual_w8,
     skinny_gemm_residual_w8_ptr,
     sgr_validate_w8_ptr,
+    sgr_selftest_wait_timeout,
 )

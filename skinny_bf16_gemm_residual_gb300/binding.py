@@ -83,6 +83,7 @@ EXPORTS = (
     "skinny_gemm_residual_grouped",
     "skinny_gemm_residual_w8",
     "sgr_validate_w8",
+    "sgr_selftest_wait_timeout",
 )
 
 
@@ -124,6 +125,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.skinny_gemm_residual_w8.argtypes = [vp, i64, vp, i64, fp, vp, i64, vp, i64, I, I, I,
                                                 ctypes.POINTER(sgr_config), U, vp]
         lib.sgr_validate_w8.argtypes = [vp, i64, vp, i64, fp, vp, i64, vp, i64, I, I, I]
+        lib.sgr_selftest_wait_timeout.argtypes = [U, ctypes.POINTER(ctypes.c_uint)]
         for name in EXPORTS:
             if name != "sgr_status_string":
                 getattr(lib, name).restype = ctypes.c_int
@@ -297,6 +299,16 @@ def skinny_gemm_residual_config(A, W, R, Y=None, config: sgr_config | None = Non
     """Explicit launch configuration (sweeps, tests)."""
     return skinny_gemm_residual_ex(A, W, R, Y, flags=flags, stream=stream,
                                    config=config if config is not None else sgr_config())
+
+
+def sgr_selftest_wait_timeout(limit_us: int = 1000) -> int:
+    """Run the bounded-wait failure self-test on the current device; returns
+    the error code the timed-out wait recorded (1 expected)."""
+    code = ctypes.c_uint(0)
+    rc = load().sgr_selftest_wait_timeout(int(limit_us), ctypes.byref(code))
+    if rc != SGR_OK:
+        raise SgrError(rc, "sgr_selftest_wait_timeout")
+    return code.value
 
 
 def _fptr(addr: int):

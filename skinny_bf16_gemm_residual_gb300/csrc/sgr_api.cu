@@ -659,6 +659,48 @@ int run_w8(const void* A, long long lda, const void* Wq, long long ldw, const fl
                         (flags & SGR_FLAG_NO_PDL) == 0, stream);
 }
 
+// ------------------------------------------------------------ wait self-test
+// One thread waits on an mbarrier that nothing arrives on, with a limit of
+// `limit_ns` nanoseconds of %globaltimer instead of the kernels' one second,
+// and reports the timeout through the device error word exactly as the
+// kernels' waits do.  Exercises the failure path without faulting or hanging
+// the GPU.
+__global__ void sgr_selftest_wait_kernel(unsigned long long limit_ns, unsigned* err) {
+  __shared__ uint64_t bar;
+  const uint32_t b = sgr::smem_u32(&bar);
+  sgr::mbar_init(b, 1);
+  sgr::fence_mbar_init();
+  const uint64_t t0 = sgr::globaltimer_ns();
+  bool done = false;
+  while (!done && sgr::globaltimer_ns() - t0 <= limit_ns)
+    for (int i = 0; i < 64 && !done; ++i) done = sgr::mbar_test_wait(b, 0);
+  if (!done) sgr::report_error(err, sgr::kErrWaitFull);
+}
+
+int run_selftest_wait(unsigned limit_us, unsigned* code) {
+  if (!code) return SGR_ERR_NULL;
+  if (limit_us == 0 || limit_us > 100000) return SGR_ERR_UNSUPPORTED;
+  int dev, rc;
+  if ((rc = current_device(&dev)) != SGR_OK) return rc;
+  if ((rc = init_device(dev)) != SGR_OK) return rc;
+  DeviceState& st = g_dev[dev];
+  unsigned zero = 0;
+  if (cudaMemcpy(st.err, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) {
+    cudaGetLastError();
+    return SGR_ERR_DEVICE;
+  }
+  sgr_selftest_wait_kernel<<<1, 1>>>((unsigned long long)limit_us * 1000ull, st.err);
+  if (cudaGetLastError() != cudaSuccess) return SGR_ERR_LAUNCH;
+  unsigned v = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess || cudaMemcpy(&v, st.err, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemcpy(st.err, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) {
+    cudaGetLastError();
+    return SGR_ERR_DEVICE;
+  }
+  *code = v;
+  return SGR_OK;
+}
+
 // ------------------------------------------------------------ grouped launch
 int run_grouped(const sgr_group* groups, int num_groups, int N, int K, const sgr_config* cfg, unsigned flags,
                 void* stream_ptr) {
@@ -902,5 +944,7 @@ int sgr_validate_w8(const void* A, int64_t lda, const void* Wq, int64_t ldw, con
                     int64_t ldr, const void* Y, int64_t ldy, int M, int N, int K) {
   return validate_w8(A, lda, Wq, ldw, scale, R, ldr, Y, ldy, M, N, K);
 }
+
+int sgr_selftest_wait_timeout(unsigned limit_us, unsigned* code) { return run_selftest_wait(limit_us, code); }
 
 }  // extern "C"
