@@ -296,7 +296,7 @@ int skinny_gemm_residual_grouped(const sgr_group* groups, int num_groups, int N,
  * rows per CTA, a multiple of 8 up to 128), and SGR_PATH_SIMT, the CUDA-core
  * kernel (M <= 8, contiguous code rows ldw == K, K a multiple of 16; cfg may
  * set ctas_per_sm, rows_per_stage = code rows per ring stage, stages).
- * SGR_PATH_AUTO takes the CUDA-core kernel for M <= 2 where it can run, else
+ * SGR_PATH_AUTO takes the CUDA-core kernel for M = 1 where it can run, else
  * the tensor-core kernel.  Returns an sgr_status.
  */
 int skinny_gemm_residual_w8(const void* A, int64_t lda, const void* Wq, int64_t ldw,

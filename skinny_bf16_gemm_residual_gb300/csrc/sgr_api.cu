@@ -570,10 +570,10 @@ bool simt_w8_supported(int M, int K, long long ldw) {
   return M >= 1 && M <= 8 && ldw == K && simt_w8_vpt(K) > 0;
 }
 
-// The library chooses the CUDA-core kernel up to this many tokens (measured:
-// 10.6 / 11.5 us at M = 1 / 2 against 13.1 for the tensor-core kernel; at
-// M = 4 the two are equal, beyond it the CUDA-core kernel is slower).
-constexpr int kW8SimtMaxM = 2;
+// The library chooses the CUDA-core kernel up to this many tokens (measured
+// at N = 7168, K = 3584: 10.7 us at M = 1 for both kernels, 11.5 against
+// 10.8 us at M = 2, the tensor-core kernel ahead from there on).
+constexpr int kW8SimtMaxM = 1;
 
 // CUDA-core FP8 configuration: ring stages of two code rows, 4 stages,
 // CTAs per SM by token count (the register footprint grows with M).

@@ -151,6 +151,10 @@ __global__ void __launch_bounds__(kW8Threads, 2)
     fence_mbar_init();
   }
   __syncwarp();
+  // Tensor memory first: a CTA launched early by programmatic dependent launch
+  // waits here (in the allocation) until the previous kernel's CTA on this SM
+  // releases its columns.  Letting it stream its first weight stages before
+  // the allocation measured slower (15.9 against 10.8 us per call).
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), (uint32_t)p.tmem_cols);
     tmem_relinquish();
@@ -548,33 +552,33 @@ inline bool w8_supported(int sms, int M, int N, int K) {
          w8_rows_per_cta(sms, N) <= kTcTileRows;
 }
 
-// Default: four K blocks per stage, a 3-stage activation ring and the
-// deepest weight-code ring (up to 8 stages) that keeps the CTA at or under
-// ~110 KB of shared memory, so that the next call's CTA can be resident on
-// the same SM.
+// Default: two-deep rings of the largest stages (8, else 4, else 2 K blocks)
+// that keep the CTA at or under ~110 KB of shared memory, so that the next
+// call's CTA is already resident on the SM (waiting in its tensor-memory
+// allocation) when this one finishes.  Measured at N = 7168, K = 3584, M = 1-16:
+// few large stages beat deep rings of small ones (10.8 us against 13.3 us
+// for four K blocks per stage with a six-deep ring): every stage costs a
+// hand-off between the converter warps and the MMA thread.
 inline void w8_default_config(int sms, int M, int N, int K, sgr_config* c) {
   (void)K;
   std::memset(c, 0, sizeof *c);
   c->path = SGR_PATH_W8;
   c->ctas_per_sm = 1;
   c->token_tile = (M + 15) / 16 * 16;
-  c->prefetch_stages = 3;
-  const int rb = w8_rows_per_cta(sms, N);
-  const size_t budget = 110u * 1024u;
-  for (int kb = 4; kb >= 2; kb /= 2)
-    for (int st = 8; st >= 2; --st)
-      if (w8_smem_bytes(st, 3, kb, rb, c->token_tile) <= budget) {
-        c->k_blocks_per_stage = kb;
-        c->stages = st;
-        return;
-      }
-  c->k_blocks_per_stage = 2;
   c->stages = 2;
   c->prefetch_stages = 2;
+  const int rb = w8_rows_per_cta(sms, N);
+  const size_t budget = 110u * 1024u;
+  c->k_blocks_per_stage = 2;
+  for (int kb = 8; kb >= 2; kb /= 2)
+    if (w8_smem_bytes(2, 2, kb, rb, c->token_tile) <= budget) {
+      c->k_blocks_per_stage = kb;
+      return;
+    }
 }
 
 // stages = depth of the weight-code ring, prefetch_stages = depth of the
-// activation ring (0: 3).
+// activation ring (0: 2).
 inline int w8_plan(const sgr_config& c, int sms, int M, int N, int K, W8Params* p, int* grid, size_t* smem) {
   if (!w8_supported(sms, M, N, K)) return SGR_ERR_UNSUPPORTED;
   if (c.path != SGR_PATH_AUTO && c.path != SGR_PATH_W8) return SGR_ERR_UNSUPPORTED;
@@ -584,7 +588,7 @@ inline int w8_plan(const sgr_config& c, int sms, int M, int N, int K, W8Params* 
   if (kb < 2 || kb > 8 || kb % 2 != 0) return SGR_ERR_UNSUPPORTED;
   if (c.ctas_per_sm != 1) return SGR_ERR_UNSUPPORTED;
   if (c.stages < 2 || c.stages > kW8MaxStages) return SGR_ERR_UNSUPPORTED;
-  const int sa = c.prefetch_stages > 0 ? c.prefetch_stages : 3;
+  const int sa = c.prefetch_stages > 0 ? c.prefetch_stages : 2;
   if (sa < 2 || sa > kW8MaxAStages) return SGR_ERR_UNSUPPORTED;
   const int rb = c.rows_per_stage > 0 ? c.rows_per_stage : w8_rows_per_cta(sms, N);
   if (rb % 8 != 0 || rb > kTcTileRows) return SGR_ERR_UNSUPPORTED;

@@ -316,11 +316,11 @@ def test_w8_simt_strided_in_place():
 
 
 def test_w8_auto_small_m_matches_tensor_core_path():
-    """AUTO picks the CUDA-core kernel for M <= 2; both kernels agree with the oracle."""
-    p = inputs.make_problem_w8(2, N_FULL, K_FULL, seed=58)
+    """AUTO picks the CUDA-core kernel for M = 1; both kernels agree with the oracle."""
+    p = inputs.make_problem_w8(1, N_FULL, K_FULL, seed=58)
     want = ref(p)
-    compare(run(p), want, "w8 auto M=2")
-    compare(run(p, path=sgr.SGR_PATH_W8), want, "w8 tensor-core M=2")
+    compare(run(p), want, "w8 auto M=1")
+    compare(run(p, path=sgr.SGR_PATH_W8), want, "w8 tensor-core M=1")
 
 
 def test_w8_simt_rejects():
