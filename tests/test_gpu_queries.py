@@ -1,0 +1,54 @@
+"""The host queries that need a device: default configurations per path and
+the resources of the kernel each path launches (registers, spills, shared
+memory, threads), like the register/spill query of the benchmark page."""
+import pytest
+import torch
+
+import skinny_bf16_gemm_residual_gb300 as sgr
+
+pytestmark = pytest.mark.gpu
+
+N, K = 7168, 3584
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _device():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    torch.cuda.set_device(0)
+    sgr.sgr_init(0)
+
+
+@pytest.mark.parametrize("M", [1, 4, 16, 64, 256, 1024])
+def test_default_config_auto_matches_selected_path(M):
+    c = sgr.sgr_default_config(M, N, K)
+    assert c.path == sgr.sgr_select_path(M, N, K)
+    assert c.stages >= 1 and c.ctas_per_sm >= 1
+
+
+@pytest.mark.parametrize("path,M,threads", [
+    (sgr.SGR_PATH_TC_ROWS, 4, 192), (sgr.SGR_PATH_TILE, 1024, 192), (sgr.SGR_PATH_SIMT, 4, 256),
+    (sgr.SGR_PATH_TC, 8, None), (sgr.SGR_PATH_W8, 4, 352)])
+def test_kernel_resources(path, M, threads):
+    r = sgr.sgr_kernel_resources(M, N, K, path=path)
+    assert 0 < r["registers_per_thread"] <= 255
+    assert r["spill_bytes"] == 0, r
+    assert r["smem_bytes"] <= 232448
+    if threads is not None:
+        assert r["threads"] == threads
+    assert r["registers_per_thread"] * r["threads"] <= 65536
+
+
+def test_fp8_default_config():
+    c = sgr.sgr_default_config(4, N, K, path=sgr.SGR_PATH_W8)
+    assert (c.path, c.k_blocks_per_stage, c.stages, c.prefetch_stages, c.token_tile) == (sgr.SGR_PATH_W8, 8, 2, 2, 16)
+    r = sgr.sgr_kernel_resources(4, N, K, path=sgr.SGR_PATH_W8)
+    assert 2 * (r["smem_bytes"] + 1024) <= 233472, "two CTAs per SM must fit"
+    assert 2 * r["registers_per_thread"] * r["threads"] <= 65536
+
+
+def test_queries_reject_bad_shapes():
+    with pytest.raises(sgr.SgrError):
+        sgr.sgr_default_config(4, 7170, K)
+    with pytest.raises(sgr.SgrError):
+        sgr.sgr_kernel_resources(0, N, K)
