@@ -272,7 +272,8 @@ int resolve_config(int dev_sms, int M, int N, int K, const sgr_config* in, sgr_c
       out->ctas_per_sm = e->ctas_per_sm;
       out->stages = e->stages;
       if (path == SGR_PATH_SIMT || path == SGR_PATH_TC_ROWS) out->rows_per_stage = e->rows_per_stage;
-      else if (path != SGR_PATH_TILE || e->k_blocks_per_stage > 0) out->k_blocks_per_stage = e->k_blocks_per_stage;
+      if (path != SGR_PATH_SIMT && (path != SGR_PATH_TILE || e->k_blocks_per_stage > 0))
+        out->k_blocks_per_stage = e->k_blocks_per_stage;
       if (path == SGR_PATH_TC_ROWS || path == SGR_PATH_TILE) out->prefetch_stages = e->prefetch_stages;
       if (path == SGR_PATH_TILE && e->tile_n) out->tile_n = e->tile_n;
       if (path == SGR_PATH_TILE) out->k_split = e->k_split > 0 ? e->k_split : 1;

@@ -109,6 +109,97 @@ struct RowsIO {
   int M;
 };
 
+// Epilogue for 17..64 tokens (token tile T = 32, 48 or 64) with at most two
+// packed groups: the ownership of the 16-token decode epilogue (lane r < RB
+// owns output column n0 + r, lane RB + r holds group 1's partial sums and
+// hands them over through the drained ring), with T accumulator columns per
+// group loaded in 16-column pieces and the residuals of all T token rows
+// loaded into registers before the accumulator is ready.  Called by the four
+// epilogue warps (q: TMEM lane quarter of the warp).
+template <int T>
+__device__ __forceinline__ void rows_epilogue_wide(const RowsParams& p, const RowsIO& io, int n0, uint32_t tmem,
+                                                   uint32_t w_ring, uint64_t* acc_full, volatile int* abort_flag,
+                                                   int q, int lane) {
+  constexpr int C = T / 16;
+  const int L = q * 32 + lane;
+  const int G = p.groups;
+  const bool owner = L < p.RB && n0 + L < p.N;
+  const bool helper = G == 2 && L >= p.RB && L < 2 * p.RB;
+  const int r = owner ? L : L - p.RB;
+  const uint32_t xch = w_ring + (uint32_t)(helper || owner ? r : 0) * (uint32_t)((T + 4) * 4);  // T floats + pad per row
+  // Residuals kept as BF16 pairs (half the registers of FP32 values).
+  const unsigned short* rp = reinterpret_cast<const unsigned short*>(io.R) + n0 + L;
+  uint32_t res2[T / 2];
+#pragma unroll
+  for (int m = 0; m < T; m += 2) {
+    const uint32_t lo = (owner && m < io.M) ? rp[(size_t)m * io.ldr] : 0u;
+    const uint32_t hi = (owner && m + 1 < io.M) ? rp[(size_t)(m + 1) * io.ldr] : 0u;
+    res2[m / 2] = lo | (hi << 16);
+  }
+  bool ok = mbar_wait_or_abort(smem_u32(acc_full), 0, abort_flag);
+  if (!ok) {
+    if (!*abort_flag) report_error(p.err, kErrWaitMma);
+    *abort_flag = 1;
+  }
+  ok = __all_sync(0xffffffffu, ok);
+  tc_fence_after();
+  float v[T];
+#pragma unroll
+  for (int i = 0; i < T; ++i) v[i] = 0.f;
+  if (ok && q * 32 < G * p.RB) {  // warp-uniform: this warp holds rows of the MMA window in use
+    const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16);
+    // Columns [0, T) hold group 0's diagonal block, [T, 2T) group 1's.
+    const bool straddle = G == 2 && q * 32 < p.RB && (q + 1) * 32 > p.RB;
+    const uint32_t col0 = (G == 2 && q * 32 >= p.RB) ? (uint32_t)T : 0u;
+#pragma unroll
+    for (int c = 0; c < C; ++c) {
+      float a[16];
+      tmem_ld16(taddr + col0 + (uint32_t)(16 * c), a);  // warp-collective
+      if (straddle) {
+        float b[16];
+        tmem_ld16(taddr + (uint32_t)(T + 16 * c), b);
+        if (L >= p.RB) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) a[i] = b[i];
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[16 * c + i] = a[i];
+    }
+  }
+  if (ok && helper) {
+#pragma unroll
+    for (int i = 0; i < T; i += 4)
+      asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(xch + (uint32_t)i * 4u), "f"(v[i]), "f"(v[i + 1]),
+                   "f"(v[i + 2]), "f"(v[i + 3])
+                   : "memory");
+  }
+  named_bar_sync(1, 128);
+  if (ok && owner) {
+    if (G == 2) {
+#pragma unroll
+      for (int i = 0; i < T; i += 4) {
+        float a0, a1, a2, a3;
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(a0), "=f"(a1), "=f"(a2), "=f"(a3)
+                     : "r"(xch + (uint32_t)i * 4u)
+                     : "memory");
+        v[i] += a0;
+        v[i + 1] += a1;
+        v[i + 2] += a2;
+        v[i + 3] += a3;
+      }
+    }
+    __nv_bfloat16* yp = io.Y + n0 + L;
+#pragma unroll
+    for (int m = 0; m < T; ++m)
+      if (m < io.M) {
+        const float rm = (m & 1) ? bf16hi(res2[m / 2]) : bf16lo(res2[m / 2]);
+        yp[(size_t)m * io.ldy] = __float2bfloat16_rn(v[m] + rm);
+      }
+  }
+}
+
 // One CTA: the RB-row slab of W starting at row n0 of the problem `io`.
 __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, int n0) {
   extern __shared__ unsigned char smem_raw[];
@@ -339,6 +430,10 @@ __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, 
         for (int m = 0; m < kRowsPrefetchTokens; ++m)
           if (m < io.M) yp[(size_t)m * io.ldy] = __float2bfloat16_rn(v[m] + res[m]);
       }
+    } else if (p.NT == 32 && p.groups <= 2 && p.groups * p.RB <= kTcTileRows) {
+      rows_epilogue_wide<32>(p, io, n0, tmem, w_ring, acc_full, abort_flag, q, lane);
+    } else if (p.NT == 48 && p.groups <= 2 && p.groups * p.RB <= kTcTileRows) {
+      rows_epilogue_wide<48>(p, io, n0, tmem, w_ring, acc_full, abort_flag, q, lane);
     } else if (p.NT == kRowsPrefetchTokens && p.groups == 4 && p.RB == 32) {
       // 32-row slabs, four packed groups: warp quarter q holds group q whole.
       // Warps 1-3 hand their partial sums to warp 0's lanes (one output

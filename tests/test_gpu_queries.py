@@ -54,3 +54,38 @@ def test_queries_reject_bad_shapes():
         sgr.sgr_default_config(4, 7170, K)
     with pytest.raises(sgr.SgrError):
         sgr.sgr_kernel_resources(0, N, K)
+
+
+def table_entries(n: int, k: int):
+    import os
+    import re
+    path = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                        "skinny_bf16_gemm_residual_gb300", "csrc", "sgr_table.h")
+    rows = []
+    for m in re.finditer(r"\{(\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+),",
+                         open(path).read()):
+        v = [int(x) for x in m.groups()]
+        if v[0] == n and v[1] == k:
+            rows.append(dict(m=v[2], path=v[3], ctas_per_sm=v[4], stages=v[5], rows_per_stage=v[6],
+                             k_blocks_per_stage=v[7], prefetch_stages=v[8], tile_n=v[9], k_split=v[10], pair_w=v[11]))
+    return rows
+
+
+@pytest.mark.parametrize("n,k", [(7168, 3584), (3584, 7168)])
+def test_automatic_config_is_the_measured_table_entry(n, k):
+    """Every field the table holds for a shape reaches the launch configuration
+    the library uses for it (at the table's own M)."""
+    entries = table_entries(n, k)
+    assert entries
+    for e in entries:
+        c = sgr.sgr_default_config(e["m"], n, k)
+        assert c.path == e["path"], e
+        assert (c.ctas_per_sm, c.stages) == (e["ctas_per_sm"], e["stages"]), (e, c.as_dict())
+        if e["path"] != sgr.SGR_PATH_SIMT and (e["path"] != sgr.SGR_PATH_TILE or e["k_blocks_per_stage"] > 0):
+            assert c.k_blocks_per_stage == e["k_blocks_per_stage"], (e, c.as_dict())
+        if e["path"] in (sgr.SGR_PATH_TC_ROWS, sgr.SGR_PATH_SIMT):
+            assert c.rows_per_stage == e["rows_per_stage"], (e, c.as_dict())
+        if e["path"] in (sgr.SGR_PATH_TC_ROWS, sgr.SGR_PATH_TILE):
+            assert c.prefetch_stages == e["prefetch_stages"], (e, c.as_dict())
+        if e["path"] == sgr.SGR_PATH_TILE:
+            assert (c.tile_n, c.k_split, c.pair_w) == (e["tile_n"], max(e["k_split"], 1), e["pair_w"]), (e, c.as_dict())
