@@ -434,6 +434,8 @@ __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, 
       rows_epilogue_wide<32>(p, io, n0, tmem, w_ring, acc_full, abort_flag, q, lane);
     } else if (p.NT == 48 && p.groups <= 2 && p.groups * p.RB <= kTcTileRows) {
       rows_epilogue_wide<48>(p, io, n0, tmem, w_ring, acc_full, abort_flag, q, lane);
+    } else if (p.NT == 64 && p.groups <= 2 && p.groups * p.RB <= kTcTileRows) {
+      rows_epilogue_wide<64>(p, io, n0, tmem, w_ring, acc_full, abort_flag, q, lane);
     } else if (p.NT == kRowsPrefetchTokens && p.groups == 4 && p.RB == 32) {
       // 32-row slabs, four packed groups: warp quarter q holds group q whole.
       // Warps 1-3 hand their partial sums to warp 0's lanes (one output
