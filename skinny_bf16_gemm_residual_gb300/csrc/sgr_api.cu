@@ -861,16 +861,18 @@ int sgr_kernel_resources(int device, int path, int M, int N, int K, int* regs, i
     *smem_bytes = (int)sgr::simt_smem_bytes(c.stages, c.rows_per_stage, K);
     *threads = sgr::kSimtThreads;
   } else if (c.path == SGR_PATH_TC_ROWS) {
-    if (cudaFuncGetAttributes(&fa, sgr::rows_skinny_kernel) != cudaSuccess) {
-      cudaGetLastError();
-      return SGR_ERR_DEVICE;
-    }
     sgr::RowsParams rp;
     int grid = 0;
     size_t smem = 0;
     int sms = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
     if (sgr::rows_plan(c, sms, M, N, K, &rp, &grid, &smem) != SGR_OK) return SGR_ERR_UNSUPPORTED;
+    const void* fn = (rp.NT == 64 && rp.groups <= 2) ? reinterpret_cast<const void*>(sgr::rows_skinny64_kernel)
+                                                     : reinterpret_cast<const void*>(sgr::rows_skinny_kernel);
+    if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) {
+      cudaGetLastError();
+      return SGR_ERR_DEVICE;
+    }
     *smem_bytes = (int)smem;
     *threads = sgr::kRowsThreads;
   } else if (c.path == SGR_PATH_W8) {

@@ -201,6 +201,10 @@ __device__ __forceinline__ void rows_epilogue_wide(const RowsParams& p, const Ro
 }
 
 // One CTA: the RB-row slab of W starting at row n0 of the problem `io`.
+// kWide64: include the 64-token register epilogue (more registers per
+// thread: only the kernel instance launched for 64-token tiles has it, so
+// that the others keep two CTAs per SM where their shared memory allows).
+template <bool kWide64>
 __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, int n0) {
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -434,7 +438,7 @@ __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, 
       rows_epilogue_wide<32>(p, io, n0, tmem, w_ring, acc_full, abort_flag, q, lane);
     } else if (p.NT == 48 && p.groups <= 2 && p.groups * p.RB <= kTcTileRows) {
       rows_epilogue_wide<48>(p, io, n0, tmem, w_ring, acc_full, abort_flag, q, lane);
-    } else if (p.NT == 64 && p.groups <= 2 && p.groups * p.RB <= kTcTileRows) {
+    } else if (kWide64 && p.NT == 64 && p.groups <= 2 && p.groups * p.RB <= kTcTileRows) {
       rows_epilogue_wide<64>(p, io, n0, tmem, w_ring, acc_full, abort_flag, q, lane);
     } else if (p.NT == kRowsPrefetchTokens && p.groups == 4 && p.RB == 32) {
       // 32-row slabs, four packed groups: warp quarter q holds group q whole.
@@ -649,7 +653,15 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
     rows_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA,
                        const RowsParams p) {
   const RowsIO io{&tmW, &tmA, p.R, p.Y, p.ldr, p.ldy, p.M};
-  rows_run(p, io, (int)blockIdx.x * p.RB);
+  rows_run<false>(p, io, (int)blockIdx.x * p.RB);
+}
+
+// The same for 64-token tiles (33 <= M <= 64), with the 64-token epilogue.
+__global__ void __launch_bounds__(kRowsThreads, 1)
+    rows_skinny64_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA,
+                         const RowsParams p) {
+  const RowsIO io{&tmW, &tmA, p.R, p.Y, p.ldr, p.ldy, p.M};
+  rows_run<true>(p, io, (int)blockIdx.x * p.RB);
 }
 
 // Grouped launch: several independent problems with the same N and K and
@@ -678,7 +690,7 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
   const int slab = (int)blockIdx.x / list.count;
   const RowsGroup& g = list.g[e];
   const RowsIO io{&g.tmW, &g.tmA, g.R, g.Y, g.ldr, g.ldy, g.M};
-  rows_run(p, io, slab * p.RB);
+  rows_run<false>(p, io, slab * p.RB);
 }
 
 // ------------------------------------------------------------------ host side
@@ -762,6 +774,7 @@ inline int rows_plan(const sgr_config& c, int sms, int M, int N, int K, RowsPara
 
 inline cudaError_t rows_init_device() {
   cudaError_t e = set_kernel_smem_attrs(reinterpret_cast<const void*>(rows_skinny_kernel));
+  if (e == cudaSuccess) e = set_kernel_smem_attrs(reinterpret_cast<const void*>(rows_skinny64_kernel));
   if (e == cudaSuccess) e = set_kernel_smem_attrs(reinterpret_cast<const void*>(rows_grouped_kernel));
   return e;
 }
@@ -792,7 +805,8 @@ inline int rows_launch(const sgr_config& c, int sms, unsigned* err, const void* 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
   lc.numAttrs = pdl ? 1 : 0;
-  if (cudaLaunchKernelEx(&lc, rows_skinny_kernel, tmW, tmA, p) != cudaSuccess) {
+  const bool wide64 = p.NT == 64 && p.groups <= 2;
+  if (cudaLaunchKernelEx(&lc, wide64 ? rows_skinny64_kernel : rows_skinny_kernel, tmW, tmA, p) != cudaSuccess) {
     cudaGetLastError();
     return SGR_ERR_LAUNCH;
   }
