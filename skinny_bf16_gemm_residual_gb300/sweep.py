@@ -6,9 +6,14 @@ timed by batched CUDA-graph replay over rotating weight/residual copies that
 together exceed L2, and one JSON row per (M, path, config) is written.  A
 `torch.addmm` (cuBLAS) row under the same protocol is included as context.
 The per-M table compiled into the library is generated from these rows by
-``gen_table.py``.
+``gen_table.py``.  The paths ``w8`` (tensor-core FP8-weight kernel) and
+``w8simt`` (CUDA-core FP8-weight kernel) time ``skinny_gemm_residual_w8`` over
+rotating copies of per-column-quantised E4M3 weights; their rows (backend
+``w8`` / ``w8_simt``) are for choosing that entry point's defaults and are
+not part of the BF16 table.
 
     python -m skinny_bf16_gemm_residual_gb300.sweep --m 1 2 4 8 16 --output sweep.jsonl
+    python -m skinny_bf16_gemm_residual_gb300.sweep --paths w8,w8simt --copies 8 --output sweep_w8.jsonl
 """
 from __future__ import annotations
 
@@ -22,6 +27,33 @@ import torch
 
 from . import binding as sgr
 from . import inputs
+
+
+def candidate_configs_w8(simt: bool, M: int, K: int, grid: str) -> list[dict]:
+    """Launch configurations of the FP8-weight kernels (shared memory checked
+    by the library, which refuses what does not fit)."""
+    out = []
+    if simt:
+        if M > 8 or K % 16:
+            return []
+        for cps in (1, 2, 3):
+            for rps in (1, 2, 4):
+                for st in (2, 4, 6, 8):
+                    if grid == "small" and st not in (4, 6):
+                        continue
+                    out.append(dict(path=sgr.SGR_PATH_SIMT, ctas_per_sm=cps, rows_per_stage=rps, stages=st))
+        return out
+    if M > 256:
+        return []
+    for rb in (0, 64):
+        for kb in (2, 4, 8):
+            for st in (2, 3, 4, 6):
+                for sa in (2, 3):
+                    if grid == "small" and (st > 3 or sa > 2):
+                        continue
+                    out.append(dict(path=sgr.SGR_PATH_W8, k_blocks_per_stage=kb, stages=st, prefetch_stages=sa,
+                                    rows_per_stage=rb))
+    return out
 
 
 def candidate_configs(path: int, M: int, K: int, grid: str) -> list[dict]:
@@ -157,7 +189,12 @@ def main(argv=None):
             "l2_bytes": props.L2_cache_size, "torch": torch.__version__}
     out = open(args.output, "w") if args.output else None
     paths = {"simt": sgr.SGR_PATH_SIMT, "tc": sgr.SGR_PATH_TC, "rows": sgr.SGR_PATH_TC_ROWS,
-             "tile": sgr.SGR_PATH_TILE}
+             "tile": sgr.SGR_PATH_TILE, "w8": sgr.SGR_PATH_W8, "w8simt": sgr.SGR_PATH_SIMT}
+    fp8 = [name for name in args.paths.split(",") if name in ("w8", "w8simt")]
+    if fp8:  # per-column-quantised E4M3 copies of the same weights
+        q = [inputs.make_problem_w8(1, N, K, seed=s) for s in range(args.copies)]
+        Wqs = [x.Wq.to(dev) for x in q]
+        Scs = [x.scale.to(dev) for x in q]
     for M in args.m:
         A = inputs.make_rows(M, K, seed=10_000 + M).to(dev)
         Rs = [inputs.make_rows(M, N, seed=20_000 + 100 * M + s).to(dev) for s in range(args.copies)]
@@ -168,15 +205,26 @@ def main(argv=None):
             launch = lambda c: torch.addmm(Rs[c], A, Ws[c].t(), out=Ys[c])
             rows.append(("cublas_addmm", {}, graph_samples(launch, args.copies, stream, args.repeats, args.replays)))
         for name in args.paths.split(","):
-            cands = ([dict(json.loads(c), path=paths[name]) for c in args.config] if args.config
-                     else candidate_configs(paths[name], M, K, args.grid))
+            w8 = name in ("w8", "w8simt")
+            if args.config:
+                cands = [dict(json.loads(c), path=paths[name]) for c in args.config]
+            elif w8:
+                cands = candidate_configs_w8(name == "w8simt", M, K, args.grid)
+            else:
+                cands = candidate_configs(paths[name], M, K, args.grid)
+            backend = {"w8": "w8", "w8simt": "w8_simt"}.get(name, name)
             for cfg in cands:
                 c = sgr.make_config(**cfg)
-                launch = lambda i, c=c: sgr.skinny_gemm_residual_ex(A, Ws[i], Rs[i], Ys[i], stream=stream, config=c)
+                if w8:
+                    launch = lambda i, c=c: sgr.skinny_gemm_residual_w8(A, Wqs[i], Scs[i], Rs[i], Ys[i], stream=stream,
+                                                                       config=c)
+                else:
+                    launch = lambda i, c=c: sgr.skinny_gemm_residual_ex(A, Ws[i], Rs[i], Ys[i], stream=stream,
+                                                                        config=c)
                 try:
-                    rows.append((name, cfg, graph_samples(launch, args.copies, stream, args.repeats, args.replays)))
+                    rows.append((backend, cfg, graph_samples(launch, args.copies, stream, args.repeats, args.replays)))
                 except sgr.SgrError as e:
-                    rows.append((name, cfg, str(e)))
+                    rows.append((backend, cfg, str(e)))
         for backend, cfg, samples in rows:
             row = {"m": M, "n": N, "k": K, "backend": backend, "config": cfg, "num_buffers": args.copies, **meta}
             if isinstance(samples, str):
@@ -184,7 +232,8 @@ def main(argv=None):
             else:
                 s = summarize(samples)
                 row.update(s)
-                row["gbs"] = nbytes / (s["median_us"] * 1e-6) / 1e9
+                fp8_bytes = N * K + 4 * N + 2 * M * K + 4 * M * N
+                row["gbs"] = (fp8_bytes if backend.startswith("w8") else nbytes) / (s["median_us"] * 1e-6) / 1e9
             line = json.dumps(row, sort_keys=True)
             if out:
                 out.write(line + "\n")
