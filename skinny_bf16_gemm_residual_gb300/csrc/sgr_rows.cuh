@@ -39,7 +39,11 @@
 // addresses prepared while the MMAs run: it sits on the critical path after
 // the last weight byte lands, so it is kept short (counting each stage's
 // packed groups on separate barriers, to start the last stage's MMAs early,
-// measured slower).
+// measured slower).  Token tiles of 32, 48 and 64 use the same register form
+// with the accumulator loaded in 16-column pieces (rows_epilogue_wide; the
+// 64-token form in its own kernel instance, rows_skinny64_kernel, because of
+// its register count); only larger tiles stage partial sums through shared
+// memory.
 #pragma once
 
 #include <cstring>
