@@ -307,6 +307,46 @@ def _same_float(got: np.ndarray, want: np.ndarray) -> bool:
     return bool(np.all(both_nan | same))
 
 
+def load_crafted_w8_fixture():
+    cases, cur = [], None
+    with open(os.path.join(GOLDEN, "crafted_w8.txt")) as f:
+        for raw in f:
+            line = raw.strip()
+            if not line or line.startswith("#"):
+                continue
+            if line.startswith("case "):
+                cur = {"name": line[5:].split(":", 1)[0]}
+                cases.append(cur)
+            elif ":" not in line:
+                cur["M"], cur["N"], cur["K"] = (int(v) for v in line.split())
+            else:
+                key, vals = line.split(":", 1)
+                vals = vals.split()
+                if key == "Y":
+                    cur["Y"] = np.array([int(v, 16) for v in vals], dtype=np.uint16)
+                elif key == "Wq":
+                    cur["Wq"] = np.array([int(v, 16) for v in vals], dtype=np.uint8)
+                elif key == "scale":
+                    cur["scale"] = np.array([float.fromhex(v) for v in vals], dtype=np.float32)
+                else:
+                    f32 = np.array([float.fromhex(v) for v in vals], dtype=np.float32)
+                    cur[key] = bits(torch.from_numpy(f32).to(torch.bfloat16))
+    for c in cases:
+        c["A"] = c["A"].reshape(c["M"], c["K"])
+        c["Wq"] = c["Wq"].reshape(c["N"], c["K"])
+        c["R"] = c["R"].reshape(c["M"], c["N"])
+        c["Y"] = c["Y"].reshape(c["M"], c["N"])
+    return cases
+
+
+def check_w8_crafted_fixture(orc):
+    for c in load_crafted_w8_fixture():
+        _eq(orc.gemm_residual_w8(c["A"], c["Wq"], c["scale"], c["R"], threads=1), c["Y"],
+            f"crafted w8 case {c['name']}")
+        _eq(exact_reference_w8(c["A"], c["Wq"], c["scale"], c["R"]), c["Y"],
+            f"crafted w8 case {c['name']} (exact rationals)")
+
+
 def check_e4m3_fixture(orc):
     rows = load_e4m3_fixture()
     got = orc.e4m3_to_double(np.array([c for c, _ in rows], dtype=np.uint8))
@@ -415,6 +455,7 @@ ALL_CHECKS = [
     check_strided_rows,
     check_e4m3_fixture,
     check_e4m3_all_codes_vs_library,
+    check_w8_crafted_fixture,
     check_w8_brute_force_exact,
     check_w8_subnormal_codes_exact,
     check_w8_unit_scale_is_bf16_gemm,
