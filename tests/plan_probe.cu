@@ -1,0 +1,92 @@
+// Host-only driver for tests/test_plans.py: runs the launch planners of the
+// row-slab, FP8 row-slab and tile kernels over a grid of shapes and launch
+// configurations and prints one JSON object per accepted plan.  No CUDA call
+// is made; the kernels' headers are included for their host planners only.
+#include <cstdio>
+
+#include "sgr_rows.cuh"
+#include "sgr_w8.cuh"
+#include "sgr_gemm.cuh"
+
+int main() {
+  const int sms = 152;
+  const int Ms[] = {1, 3, 16, 17, 32, 40, 48, 64, 100, 128, 200, 256};
+  const int NKs[][2] = {{7168, 3584}, {3584, 7168}, {520, 264}, {8, 3584}, {1024, 1024}, {152, 1792}};
+  for (auto& nk : NKs) {
+    const int N = nk[0], K = nk[1];
+    for (int M : Ms) {
+      const int nt = (M + 15) / 16 * 16;
+      // row-slab kernel
+      for (int rb : {0, 8, 24, 32, 48, 64, 128})
+        for (int kb : {1, 2, 4, 8})
+          for (int st : {2, 3, 4, 6, 8}) {
+            sgr_config c = {};
+            c.path = SGR_PATH_TC_ROWS;
+            c.ctas_per_sm = 1;
+            c.rows_per_stage = rb;
+            c.k_blocks_per_stage = kb;
+            c.stages = st;
+            c.token_tile = nt;
+            sgr::RowsParams p;
+            int grid = 0;
+            size_t smem = 0;
+            if (sgr::rows_plan(c, sms, M, N, K, &p, &grid, &smem) != SGR_OK) continue;
+            const size_t w_ring = (size_t)st * kb * p.RB * 128, a_ring = (size_t)st * kb * p.NT * 128;
+            std::printf("{\"kind\": \"rows\", \"M\": %d, \"N\": %d, \"K\": %d, \"RB\": %d, \"NT\": %d, \"G\": %d, "
+                        "\"kbps\": %d, \"stages\": %d, \"prefetch\": %d, \"k_stages\": %d, \"tmem_cols\": %d, "
+                        "\"grid\": %d, \"smem\": %zu, \"w_ring\": %zu, \"a_ring\": %zu}\n",
+                        M, N, K, p.RB, p.NT, p.groups, p.kbps, p.stages, p.prefetch, p.k_stages, p.tmem_cols, grid,
+                        smem, w_ring, a_ring);
+          }
+      // FP8 row-slab kernel
+      for (int rb : {0, 8, 24, 32, 64, 128})
+        for (int kb : {2, 4, 6, 8})
+          for (int st : {2, 3, 4, 6, 12})
+            for (int sa : {2, 3, 8}) {
+              sgr_config c = {};
+              c.path = SGR_PATH_W8;
+              c.ctas_per_sm = 1;
+              c.rows_per_stage = rb;
+              c.k_blocks_per_stage = kb;
+              c.stages = st;
+              c.prefetch_stages = sa;
+              c.token_tile = nt;
+              sgr::W8Params p;
+              int grid = 0;
+              size_t smem = 0;
+              if (sgr::w8_plan(c, sms, M, N, K, &p, &grid, &smem) != SGR_OK) continue;
+              std::printf("{\"kind\": \"w8\", \"M\": %d, \"N\": %d, \"K\": %d, \"RB\": %d, \"NT\": %d, \"G\": %d, "
+                          "\"kbps\": %d, \"stages\": %d, \"a_stages\": %d, \"k_stages\": %d, \"slots\": %d, "
+                          "\"acc_cols\": %d, \"tmem_cols\": %d, \"conv_warps\": %d, \"grid\": %d, \"smem\": %zu, "
+                          "\"rtile\": %u, \"w_ring\": %zu, \"a_ring\": %zu}\n",
+                          M, N, K, p.RB, p.NT, p.groups, p.kbps, p.stages, p.a_stages, p.k_stages, p.slots,
+                          p.acc_cols, p.tmem_cols, p.conv_warps, grid, smem, sgr::w8_rtile_bytes(p.RB, p.NT),
+                          (size_t)p.stages * sgr::w8_wstage_bytes(p.kbps, p.RB),
+                          (size_t)p.a_stages * sgr::w8_astage_bytes(p.kbps, p.NT));
+            }
+      // tile kernel
+      for (int tn : {64, 128, 192, 256})
+        for (int kb : {1, 2, 4})
+          for (int st : {2, 4, 7})
+            for (int split : {1, 2}) {
+              sgr_config c = {};
+              c.path = SGR_PATH_TILE;
+              c.ctas_per_sm = 1;
+              c.tile_n = tn;
+              c.k_blocks_per_stage = kb;
+              c.stages = st;
+              c.k_split = split;
+              sgr::TileParams p;
+              int grid = 0;
+              size_t smem = 0;
+              if (sgr::tile_plan(c, sms, M, N, K, &p, &grid, &smem) != SGR_OK) continue;
+              std::printf("{\"kind\": \"tile\", \"M\": %d, \"N\": %d, \"K\": %d, \"NT\": %d, \"kbps\": %d, "
+                          "\"stages\": %d, \"split\": %d, \"m_tiles\": %d, \"n_tiles\": %d, \"k_blocks\": %d, "
+                          "\"kb_split\": %d, \"tmem_cols\": %d, \"grid\": %d, \"smem\": %zu}\n",
+                          M, N, K, p.NT, p.kbps, p.stages, split, p.m_tiles, p.n_tiles, p.k_blocks, p.kb_split,
+                          p.tmem_cols, grid, smem);
+            }
+    }
+  }
+  return 0;
+}

@@ -1,0 +1,97 @@
+"""Launch-plan invariants checked on the CPU: the host planners of the
+row-slab, FP8 row-slab and tile kernels (compiled with nvcc into a small host
+program, tests/plan_probe.cu) are run over a grid of shapes and
+configurations, and every accepted plan must fit the budgets the kernels rely
+on: shared memory per CTA, tensor-memory columns, the barrier region, the MMA
+window (128 rows, N <= 256), whole coverage of N and K, and room for the
+epilogue's hand-over buffers in the drained rings."""
+import json
+import os
+import shutil
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+CSRC = os.path.join(ROOT, "skinny_bf16_gemm_residual_gb300", "csrc")
+SMEM_LIMIT = 232448
+
+
+@pytest.fixture(scope="module")
+def plans(tmp_path_factory):
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    if not os.path.exists(nvcc):
+        pytest.skip("nvcc not available")
+    exe = str(tmp_path_factory.mktemp("plans") / "plan_probe")
+    subprocess.run([nvcc, "-std=c++17", "-gencode", "arch=compute_103a,code=sm_103a", f"-I{CSRC}",
+                    f"-I{os.path.join(ROOT, 'include')}", os.path.join(ROOT, "tests", "plan_probe.cu"),
+                    "-o", exe, "-lcuda"], check=True, capture_output=True)
+    out = subprocess.run([exe], check=True, capture_output=True, text=True).stdout
+    rows = [json.loads(line) for line in out.splitlines() if line.strip()]
+    assert rows
+    return rows
+
+
+def test_row_slab_plans(plans):
+    rows = [p for p in plans if p["kind"] == "rows"]
+    assert len(rows) > 100
+    for p in rows:
+        assert p["smem"] <= SMEM_LIMIT, p
+        assert p["RB"] % 8 == 0 and p["RB"] <= 128, p
+        assert p["G"] * p["RB"] <= 128 and p["G"] * p["NT"] <= 256, p            # one MMA window
+        assert p["kbps"] % p["G"] == 0, p
+        assert p["NT"] >= p["M"] and p["NT"] % 16 == 0, p
+        assert p["tmem_cols"] >= p["G"] * p["NT"] and p["tmem_cols"] <= 512, p
+        assert p["grid"] * p["RB"] >= p["N"] > (p["grid"] - 1) * p["RB"], p      # every row, no empty CTA
+        assert p["k_stages"] * p["kbps"] * 64 >= p["K"], p
+        assert 1 <= p["prefetch"] <= p["stages"], p
+        drained = p["w_ring"] + p["a_ring"]
+        # hand-over buffers of the epilogues live in the drained rings
+        if p["NT"] == 16 and p["G"] <= 2:
+            assert p["RB"] * 80 <= drained, p
+        elif p["NT"] in (32, 48, 64) and p["G"] <= 2:
+            assert p["RB"] * (p["NT"] + 4) * 4 <= drained, p
+        else:
+            assert p["G"] * p["RB"] * (p["NT"] + 4) * 4 <= drained, p
+
+
+def test_fp8_row_slab_plans(plans):
+    rows = [p for p in plans if p["kind"] == "w8"]
+    assert len(rows) > 100
+    for p in rows:
+        assert p["smem"] <= SMEM_LIMIT, p
+        assert p["G"] * p["RB"] <= 128 and p["G"] * p["NT"] <= 256, p
+        assert p["kbps"] % 2 == 0 and p["kbps"] % p["G"] == 0, p
+        wins = p["kbps"] // p["G"]
+        assert p["tmem_cols"] in (256, 512), p
+        assert p["acc_cols"] >= p["G"] * p["NT"], p
+        assert p["slots"] >= 2 and p["acc_cols"] + p["slots"] * wins * 32 <= p["tmem_cols"], p
+        barriers = (2 * p["stages"] + 2 * p["a_stages"] + 2 * p["slots"] + 3) * 8 + 8
+        assert barriers <= 1024, p
+        quarters = (p["G"] * p["RB"] + 31) // 32
+        assert p["conv_warps"] == 2 * quarters and p["conv_warps"] <= 8, p
+        assert p["grid"] * p["RB"] >= p["N"] > (p["grid"] - 1) * p["RB"], p
+        assert p["k_stages"] * p["kbps"] * 64 >= p["K"], p
+        assert p["rtile"] >= p["RB"] * p["NT"] * 2, p
+        drained = p["w_ring"] + p["a_ring"]
+        if p["NT"] == 16 and p["G"] <= 2:
+            assert p["RB"] * 80 <= drained, p
+        else:
+            assert p["G"] * p["RB"] * (p["NT"] + 4) * 4 <= drained, p
+
+
+def test_tile_plans(plans):
+    rows = [p for p in plans if p["kind"] == "tile"]
+    assert len(rows) > 50
+    for p in rows:
+        assert p["smem"] <= SMEM_LIMIT, p
+        assert p["NT"] in (64, 128, 192, 256), p
+        assert p["tmem_cols"] >= 2 * p["NT"] and p["tmem_cols"] <= 512, p       # two accumulators
+        assert p["m_tiles"] * 128 >= p["M"] and p["n_tiles"] * p["NT"] >= p["N"], p
+        assert p["k_blocks"] * 64 >= p["K"], p
+        if p["split"] == 2:
+            assert 1 <= p["kb_split"] < p["k_blocks"], p                         # both ranks get K blocks
+            assert p["kb_split"] % p["kbps"] == 0, p
+            assert p["grid"] == 2 * p["m_tiles"] * p["n_tiles"] <= 152, p
+        else:
+            assert p["grid"] == min(p["m_tiles"] * p["n_tiles"], 152), p
