@@ -52,8 +52,9 @@
  *                       exactly R (Y == R with ldy == ldr, an in-place residual
  *                       update, is allowed: each element of R is read before
  *                       the same thread writes it)
- *   SGR_ERR_UNSUPPORTED a size beyond the library's limits, or a forced
- *                       path/config that cannot run this shape
+ *   SGR_ERR_UNSUPPORTED a size beyond the library's limits (M <= 2^20,
+ *                       N <= 2^24, K <= 2^20, row strides <= 2^36 elements),
+ *                       or a forced path/config that cannot run this shape
  *   SGR_ERR_LAUNCH      the CUDA launch itself failed (cudaGetLastError)
  *   SGR_ERR_DEVICE      no usable device, or device set-up failed
  * Empty problems (M == 0 or N == 0) return SGR_OK and enqueue nothing.

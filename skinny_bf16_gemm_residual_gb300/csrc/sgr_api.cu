@@ -24,6 +24,9 @@ constexpr int kMaxDynSmem = 232448;  // 227 KB, the per-CTA opt-in limit on sm_1
 constexpr long long kMaxN = 1 << 24;
 constexpr long long kMaxK = 1 << 20;
 constexpr long long kMaxM = 1 << 20;
+// Row strides in elements: keeps the overlap arithmetic far from 64-bit
+// overflow and every byte stride below the tensor maps' 2^40 limit.
+constexpr long long kMaxLd = 1LL << 36;
 
 __device__ unsigned g_sgr_error_word;
 
@@ -133,6 +136,7 @@ int validate(const void* A, long long lda, const void* W, const void* R, long lo
   if (K > 0 && (!A || !W)) return SGR_ERR_NULL;
   if (ldr < N || ldy < N) return SGR_ERR_SHAPE;
   if (K > 0 && lda < K) return SGR_ERR_SHAPE;
+  if (ldr > kMaxLd || ldy > kMaxLd || (K > 0 && lda > kMaxLd)) return SGR_ERR_UNSUPPORTED;
   if (ldr % 8 != 0 || ldy % 8 != 0 || (K > 0 && lda % 8 != 0)) return SGR_ERR_ALIGN;
   if (!aligned16(R) || !aligned16(Y)) return SGR_ERR_ALIGN;
   if (K > 0 && (!aligned16(A) || !aligned16(W))) return SGR_ERR_ALIGN;
@@ -548,6 +552,7 @@ int validate_w8(const void* A, long long lda, const void* Wq, long long ldw, con
   if (K > 0 && (!A || !Wq || !scale)) return SGR_ERR_NULL;
   if (ldr < N || ldy < N) return SGR_ERR_SHAPE;
   if (K > 0 && (lda < K || ldw < K)) return SGR_ERR_SHAPE;
+  if (ldr > kMaxLd || ldy > kMaxLd || (K > 0 && (lda > kMaxLd || ldw > kMaxLd))) return SGR_ERR_UNSUPPORTED;
   if (ldr % 8 != 0 || ldy % 8 != 0 || (K > 0 && (lda % 8 != 0 || ldw % 16 != 0))) return SGR_ERR_ALIGN;
   if (!aligned16(R) || !aligned16(Y)) return SGR_ERR_ALIGN;
   if (K > 0 && (!aligned16(A) || !aligned16(Wq) || (reinterpret_cast<uintptr_t>(scale) & 3u) != 0))
@@ -805,7 +810,7 @@ int sgr_select_path(int M, int N, int K) {
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
     cudaGetLastError();
-    sms = 148;  // no device visible: plan for a GB300-class part
+    sms = 152;  // no device visible: plan for a GB300 (152 SMs)
   }
   return select_path(M, N, K, sms);
 }
@@ -831,8 +836,10 @@ int sgr_device_error(int device, unsigned* code, int clear) {
   int rc = init_device(device);
   if (rc != SGR_OK) return rc;
   int prev = -1;
-  if (cudaGetDevice(&prev) != cudaSuccess) return SGR_ERR_DEVICE;
-  if (prev != device && cudaSetDevice(device) != cudaSuccess) return SGR_ERR_DEVICE;
+  if (cudaGetDevice(&prev) != cudaSuccess || (prev != device && cudaSetDevice(device) != cudaSuccess)) {
+    cudaGetLastError();
+    return SGR_ERR_DEVICE;
+  }
   unsigned v = 0;
   cudaError_t e = cudaMemcpy(&v, g_dev[device].err, sizeof v, cudaMemcpyDeviceToHost);
   if (e == cudaSuccess && clear) e = cudaMemset(g_dev[device].err, 0, sizeof v);

@@ -84,9 +84,18 @@ def test_validate_accepts_good_arguments():
     (dict(Y=R_ + 16), sgr.SGR_ERR_ALIAS),
     (dict(Y=R_, ldy=7176), sgr.SGR_ERR_ALIAS),
     (dict(M=(1 << 20) + 1), sgr.SGR_ERR_UNSUPPORTED),
+    (dict(lda=(1 << 36) + 8), sgr.SGR_ERR_UNSUPPORTED),  # strides beyond 2^36 elements
+    (dict(ldr=(1 << 36) + 8), sgr.SGR_ERR_UNSUPPORTED),
+    (dict(ldy=1 << 62), sgr.SGR_ERR_UNSUPPORTED),        # would overflow the overlap arithmetic
 ])
 def test_validate_rejects(kw, status):
     assert v(**kw) == status
+
+
+def test_validate_largest_stride():
+    big = dict(A=1 << 44, R=2 << 44, Y=3 << 44, ldr=1 << 36, ldy=1 << 36, M=2)  # regions 16 TiB apart
+    assert v(W=4 << 44, lda=1 << 36, **big) == sgr.SGR_OK
+    assert v8(Wq=4 << 44, scale=5 << 44, lda=1 << 36, ldw=1 << 36, **big) == sgr.SGR_OK
 
 
 def test_validate_in_place_and_empty():
@@ -188,6 +197,8 @@ def test_validate_w8_accepts_good_arguments():
     (dict(Y=S_ - 4096), sgr.SGR_ERR_ALIAS),              # Y runs into the scales
     (dict(Y=A_), sgr.SGR_ERR_ALIAS),
     (dict(Y=R_ + 16), sgr.SGR_ERR_ALIAS),
+    (dict(ldw=(1 << 36) + 16), sgr.SGR_ERR_UNSUPPORTED),
+    (dict(ldr=1 << 62), sgr.SGR_ERR_UNSUPPORTED),
 ])
 def test_validate_w8_rejects(kw, status):
     assert v8(**kw) == status
