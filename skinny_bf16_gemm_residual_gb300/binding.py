@@ -200,13 +200,27 @@ def sgr_kernel_resources(M: int, N: int, K: int, path: int = SGR_PATH_AUTO,
 
 
 # ---------------------------------------------------------------- launches
-def _stream_handle(stream) -> int:
+def _common_device(tensors):
+    """The one device every tensor lives on.  The library launches on the
+    calling thread's current CUDA device, so the tensor-level calls make that
+    device current for the call; tensors on different devices are refused
+    (their addresses would reach a kernel on a device that does not own them)."""
+    dev = tensors[0].device
+    for t in tensors[1:]:
+        if t.device != dev:
+            raise ValueError(f"all tensors must be on one CUDA device, got {dev} and {t.device}")
+    return dev
+
+
+def _stream_handle(stream, device=None) -> int:
     import torch
 
     if stream is None:
-        return torch.cuda.current_stream().cuda_stream
+        return torch.cuda.current_stream(device).cuda_stream
     if isinstance(stream, int):
         return stream
+    if device is not None and stream.device != device:
+        raise ValueError(f"stream is on {stream.device}, tensors on {device}")
     return stream.cuda_stream
 
 
@@ -219,7 +233,7 @@ def _check_tensor(t, name: str):
         raise ValueError(f"{name} must be a CUDA tensor")
     if t.dim() != 2:
         raise ValueError(f"{name} must be 2-D")
-    if t.shape[0] > 1 and t.shape[1] > 0 and t.stride(1) != 1:
+    if t.shape[1] > 1 and t.stride(1) != 1:
         raise ValueError(f"{name} must have unit inner stride")
 
 
@@ -259,8 +273,10 @@ def skinny_gemm_residual(A, W, R, Y=None, stream=None):
         raise ValueError(f"shape mismatch A{tuple(A.shape)} W{tuple(W.shape)} R{tuple(R.shape)} Y{tuple(Y.shape)}")
     if not (A.is_contiguous() and W.is_contiguous() and R.is_contiguous() and Y.is_contiguous()):
         raise ValueError("skinny_gemm_residual takes contiguous tensors; use skinny_gemm_residual_ex")
-    rc = load().skinny_gemm_residual(A.data_ptr(), W.data_ptr(), R.data_ptr(), Y.data_ptr(),
-                                     M, N, K, _stream_handle(stream))
+    dev = _common_device((A, W, R, Y))
+    with torch.cuda.device(dev):
+        rc = load().skinny_gemm_residual(A.data_ptr(), W.data_ptr(), R.data_ptr(), Y.data_ptr(),
+                                         M, N, K, _stream_handle(stream, dev))
     if rc != SGR_OK:
         raise SgrError(rc, "skinny_gemm_residual")
     return Y
@@ -281,15 +297,17 @@ def skinny_gemm_residual_ex(A, W, R, Y=None, flags: int = 0, stream=None, config
         raise ValueError(f"shape mismatch A{tuple(A.shape)} W{tuple(W.shape)} R{tuple(R.shape)} Y{tuple(Y.shape)}")
     if not W.is_contiguous():
         raise ValueError("W must be contiguous [N, K]")
-    if config is None:
-        rc = load().skinny_gemm_residual_ex(A.data_ptr(), _ld(A), W.data_ptr(), R.data_ptr(), _ld(R),
-                                            Y.data_ptr(), _ld(Y), M, N, K, flags, _stream_handle(stream))
-        what = "skinny_gemm_residual_ex"
-    else:
-        rc = skinny_gemm_residual_config_ptr(A.data_ptr(), _ld(A), W.data_ptr(), R.data_ptr(), _ld(R),
-                                             Y.data_ptr(), _ld(Y), M, N, K, config, flags,
-                                             _stream_handle(stream))
-        what = "skinny_gemm_residual_config"
+    dev = _common_device((A, W, R, Y))
+    with torch.cuda.device(dev):
+        if config is None:
+            rc = load().skinny_gemm_residual_ex(A.data_ptr(), _ld(A), W.data_ptr(), R.data_ptr(), _ld(R),
+                                                Y.data_ptr(), _ld(Y), M, N, K, flags, _stream_handle(stream, dev))
+            what = "skinny_gemm_residual_ex"
+        else:
+            rc = skinny_gemm_residual_config_ptr(A.data_ptr(), _ld(A), W.data_ptr(), R.data_ptr(), _ld(R),
+                                                 Y.data_ptr(), _ld(Y), M, N, K, config, flags,
+                                                 _stream_handle(stream, dev))
+            what = "skinny_gemm_residual_config"
     if rc != SGR_OK:
         raise SgrError(rc, what)
     return Y
@@ -343,7 +361,7 @@ def skinny_gemm_residual_w8(A, Wq, scale, R, Y=None, flags: int = 0, stream=None
         _check_tensor(t, n)
     if Wq.dtype not in (torch.uint8, torch.float8_e4m3fn):
         raise TypeError(f"Wq must be torch.uint8 or torch.float8_e4m3fn, got {Wq.dtype}")
-    if not Wq.is_cuda or Wq.dim() != 2 or (Wq.shape[0] > 1 and Wq.shape[1] > 0 and Wq.stride(1) != 1):
+    if not Wq.is_cuda or Wq.dim() != 2 or (Wq.shape[1] > 1 and Wq.stride(1) != 1):
         raise ValueError("Wq must be a 2-D CUDA tensor with unit inner stride")
     if scale.dtype != torch.float32 or not scale.is_cuda or scale.dim() != 1 or not scale.is_contiguous():
         raise ValueError("scale must be a contiguous 1-D CUDA float32 tensor")
@@ -355,9 +373,11 @@ def skinny_gemm_residual_w8(A, Wq, scale, R, Y=None, flags: int = 0, stream=None
     if Wq.shape[1] != K or tuple(R.shape) != (M, N) or tuple(Y.shape) != (M, N) or scale.shape[0] != N:
         raise ValueError(f"shape mismatch A{tuple(A.shape)} Wq{tuple(Wq.shape)} scale{tuple(scale.shape)} "
                          f"R{tuple(R.shape)} Y{tuple(Y.shape)}")
-    rc = skinny_gemm_residual_w8_ptr(A.data_ptr(), _ld(A), Wq.data_ptr(), _ld(Wq), scale.data_ptr(),
-                                     R.data_ptr(), _ld(R), Y.data_ptr(), _ld(Y), M, N, K, config, flags,
-                                     _stream_handle(stream))
+    dev = _common_device((A, Wq, scale, R, Y))
+    with torch.cuda.device(dev):
+        rc = skinny_gemm_residual_w8_ptr(A.data_ptr(), _ld(A), Wq.data_ptr(), _ld(Wq), scale.data_ptr(),
+                                         R.data_ptr(), _ld(R), Y.data_ptr(), _ld(Y), M, N, K, config, flags,
+                                         _stream_handle(stream, dev))
     if rc != SGR_OK:
         raise SgrError(rc, "skinny_gemm_residual_w8")
     return Y
@@ -373,6 +393,8 @@ def skinny_gemm_residual_noalloc(A, W, R, Y, flags: int = 0, stream=None):
     """Y = bf16(A . W^T + R) without any device allocation (fixed scratch
     inside the library; see include/skinny_gemm_residual.h).  Y is required:
     this call allocates nothing, not even its output."""
+    import torch
+
     for t, n in ((A, "A"), (W, "W"), (R, "R"), (Y, "Y")):
         _check_tensor(t, n)
     M, K = A.shape
@@ -381,8 +403,10 @@ def skinny_gemm_residual_noalloc(A, W, R, Y, flags: int = 0, stream=None):
         raise ValueError(f"shape mismatch A{tuple(A.shape)} W{tuple(W.shape)} R{tuple(R.shape)} Y{tuple(Y.shape)}")
     if not W.is_contiguous():
         raise ValueError("W must be contiguous [N, K]")
-    rc = skinny_gemm_residual_noalloc_ptr(A.data_ptr(), _ld(A), W.data_ptr(), R.data_ptr(), _ld(R),
-                                          Y.data_ptr(), _ld(Y), M, N, K, flags, _stream_handle(stream))
+    dev = _common_device((A, W, R, Y))
+    with torch.cuda.device(dev):
+        rc = skinny_gemm_residual_noalloc_ptr(A.data_ptr(), _ld(A), W.data_ptr(), R.data_ptr(), _ld(R),
+                                              Y.data_ptr(), _ld(Y), M, N, K, flags, _stream_handle(stream, dev))
     if rc != SGR_OK:
         raise SgrError(rc, "skinny_gemm_residual_noalloc")
     return Y
@@ -404,7 +428,7 @@ def skinny_gemm_residual_grouped(problems, flags: int = 0, stream=None, config: 
     Y may be None (allocated).  Returns the list of Y."""
     import torch
 
-    groups, outs = [], []
+    groups, outs, tensors = [], [], []
     N = K = None
     for A, W, R, Y in problems:
         for t, n in ((A, "A"), (W, "W"), (R, "R")):
@@ -424,7 +448,12 @@ def skinny_gemm_residual_grouped(problems, flags: int = 0, stream=None, config: 
             raise ValueError("Y must be [M, N]")
         groups.append(sgr_group(A.data_ptr(), _ld(A), W.data_ptr(), R.data_ptr(), _ld(R), Y.data_ptr(), _ld(Y), M, 0))
         outs.append(Y)
-    rc = skinny_gemm_residual_grouped_ptr(groups, N or 0, K or 0, config, flags, _stream_handle(stream))
+        tensors += [A, W, R, Y]
+    if not groups:
+        return outs
+    dev = _common_device(tensors)
+    with torch.cuda.device(dev):
+        rc = skinny_gemm_residual_grouped_ptr(groups, N, K, config, flags, _stream_handle(stream, dev))
     if rc != SGR_OK:
         raise SgrError(rc, "skinny_gemm_residual_grouped")
     return outs
