@@ -3,7 +3,7 @@
 Workload (the decode-sized latent-MoE projection of the vLLM
 "benchmark_k3_cutedsl_residual.py" page): Y = bf16(A . W^T + R) with
 N = 7168, K = 3584, for each M in {1, 2, 4, 8, 16}, with 4 rotating copies of
-W (~205 MB together, more than the 126 MB L2) so every call streams W from
+W (~205 MB together, more than the 136 MB L2 the device reports) so every call streams W from
 HBM.  One step = one call per (M, copy) pair = 20 calls, captured once in a
 CUDA graph and replayed (the page's graph-replay method).  Synthetic inputs:
 A, R ~ N(0,1), W ~ N(0,1)/sqrt(K), BF16, seeded.
