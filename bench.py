@@ -73,12 +73,6 @@ def tensor_bound(M: int, peaks: dict) -> bool:
     return alg_flops(M) / (peaks["bf16_tflops"] * 1e12) > alg_bytes(M) / (peaks["hbm_gbs"] * 1e9)
 
 
-def alg_flops(M: int, N: int | None = None, K: int | None = None) -> int:
-    N = N_DIM if N is None else N
-    K = K_DIM if K is None else K
-    return 2 * M * N * K
-
-
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:

@@ -1,7 +1,6 @@
 """Failure detection without a GPU fault: a bounded wait that runs out records
 its code in the device error word, the host reads it, and the context stays
 usable for the next call."""
-import numpy as np
 import pytest
 import torch
 
