@@ -133,6 +133,25 @@ def test_table_header_is_sorted_and_covers_the_latent_moe_shape():
     assert (7168, 3584) in shapes and shapes[(7168, 3584)][0] == 1
 
 
+def test_table_header_is_generated_from_the_committed_tuning_rows():
+    """sgr_table.h holds exactly what gen_table.py writes from the committed
+    sweep rows (the comment block above the code aside)."""
+    import glob
+    import json
+
+    from skinny_bf16_gemm_residual_gb300 import gen_table
+
+    pkg = os.path.join(ROOT, "skinny_bf16_gemm_residual_gb300")
+    rows = []
+    for path in sorted(glob.glob(os.path.join(pkg, "tuning", "*.jsonl"))):
+        with open(path) as f:
+            rows += [json.loads(line) for line in f if line.strip()]
+    want = gen_table.render(gen_table.best_rows(rows), "tuning")
+    have = open(os.path.join(pkg, "csrc", "sgr_table.h")).read()
+    code = lambda text: text[text.index("#pragma once"):]  # noqa: E731
+    assert code(have) == code(want)
+
+
 # ------------------------------------------------------------ grouped call (host-side checks only)
 def grp(i, M=4, **kw):
     """Group i with fake addresses spaced 16 GiB apart (never dereferenced)."""
