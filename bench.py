@@ -73,6 +73,11 @@ def tensor_bound(M: int, peaks: dict) -> bool:
     return alg_flops(M) / (peaks["bf16_tflops"] * 1e12) > alg_bytes(M) / (peaks["hbm_gbs"] * 1e9)
 
 
+def workload_name(m_list) -> str:
+    """The `config.workload` both arms report for the same M sweep."""
+    return f"M sweep {list(m_list)} x {COPIES} rotating W/R copies, N={N_DIM}, K={K_DIM}"
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -364,8 +369,8 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": total / len(times) * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"M sweep {list(m_list)}, N={N_DIM}, K={K_DIM}, 4 rotating W/R copies "
-                               f"(bounded CPU sample: {rows} output columns per call)"},
+        "config": {"workload": workload_name(m_list), "sample_columns": rows,
+                   "parallelism": "host cores, rank 0 only"},
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -509,7 +514,7 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {
-            "workload": f"M sweep {list(m_list)} x {COPIES} rotating W/R copies, N={N_DIM}, K={K_DIM}",
+            "workload": workload_name(m_list),
             "calls_per_step": launches_per_step, "l2": "inputs larger than L2 (4 W copies = "
             f"{w_total / 1e6:.0f} MB vs L2 {l2 / 1e6:.0f} MB); no flush",
             "launch": "one CUDA graph per step, PDL on", "parallelism": "replicas" if ws > 1 else "single GPU",

@@ -1,0 +1,58 @@
+"""Host-side parts of the benchmark that need no GPU: the reference arm's JSON
+line (the CPU oracle timed on a bounded sample, same metric and workload as
+the GPU arm) and the rule that a committed DRAM-traffic figure counts only
+while the kernel's sources are the ones it was captured on."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def test_reference_arm_json_line():
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "3",
+                        "--warmup", "3", "--ref-budget", "2"], env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference"
+    assert d["metric"] == bench.METRIC and d["unit"] == "GB/s" and d["higher_is_better"] is True
+    assert d["config"]["workload"] == bench.workload_name(bench.M_LIST)  # the GPU arm's workload
+    assert (d["steps"], d["warmup"], d["n_gpus"]) == (3, 3, 1)
+    assert d["value"] > 0 and d["ms_per_step"] > 0
+    cpu = d["cpu_baseline"]
+    assert cpu["kind"] == "oracle" and cpu["value"] == d["value"] and cpu["cores"] >= 1 and cpu["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_committed_traffic_follows_the_source_digest(tmp_path, monkeypatch):
+    kernel = "rows_skinny_kernel"
+    csrc = tmp_path / "skinny_bf16_gemm_residual_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    for name in bench.KERNEL_SOURCES[kernel]:
+        (csrc / name).write_text("first version of " + name)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    digest = bench.kernel_source_digest(kernel)
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / f"{kernel}_traffic.md").write_text(
+        f"# traffic\n\n- source_digest: `{digest}`\n- dram_bytes_per_launch: `51803648`\n")
+    assert bench.committed_traffic(kernel) == pytest.approx(51803648.0)
+    (csrc / bench.KERNEL_SOURCES[kernel][0]).write_text("changed")
+    assert bench.committed_traffic(kernel) is None  # kernel changed since the capture
+    assert bench.committed_traffic("no_such_kernel") is None
+
+
+def test_algorithmic_bytes_and_ridge():
+    assert bench.alg_bytes(1) == 2 * (7168 * 3584 + 3584 + 2 * 7168)
+    assert bench.alg_flops(16) == 2 * 16 * 7168 * 3584
+    peaks = {"hbm_gbs": 6772.9, "bf16_tflops": 1900.0}
+    assert not bench.tensor_bound(16, peaks) and not bench.tensor_bound(128, peaks)
+    assert bench.tensor_bound(1024, peaks)
