@@ -26,6 +26,7 @@ import hashlib
 import json
 import math
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -300,12 +301,36 @@ def time_graph(g, stream, replays: int, repeats: int):
 
 
 # ------------------------------------------------------------------ CPU arms
-def cpu_oracle_rate(Ws_cpu, per_m_cpu, m_list, budget_s: float, n_rows: int | None = None):
-    """Time the oracle (all host cores) on the workload, bounded by budget_s.
+def cpu_model() -> str:
+    """The host CPU's name as /proc/cpuinfo gives it (x86 "model name"; on Arm
+    the implementer and part codes when no name is listed)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            lines = f.read().splitlines()
+    except OSError:
+        lines = []
+    fields = {}
+    for line in lines:
+        if ":" in line:
+            k, v = line.split(":", 1)
+            fields.setdefault(k.strip(), v.strip())
+    for key in ("model name", "Model", "Hardware"):
+        if fields.get(key):
+            return fields[key]
+    if "CPU part" in fields:
+        return f"{platform.machine()} implementer {fields.get('CPU implementer', '?')} part {fields['CPU part']}"
+    return platform.machine() or "unknown"
+
+
+def cpu_oracle_rate(Ws_cpu, per_m_cpu, m_list, budget_s: float, n_rows: int | None = None,
+                    threads: int | None = None):
+    """Time the oracle on the workload, bounded by budget_s, on `threads` host
+    threads (default: all cores).  The threads split the output rows, so the
+    bits do not depend on the count.
     Returns (GB/s of algorithmic bytes, threads, sample description, seconds)."""
     import oracle
 
-    threads = os.cpu_count() or 1
+    threads = threads or os.cpu_count() or 1
     lib = oracle.load()
     n_rows = n_rows or N_DIM
     done_bytes, t0, calls = 0, time.perf_counter(), 0
@@ -371,7 +396,8 @@ def run_reference(args):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": workload_name(m_list), "sample_columns": rows,
                    "parallelism": "host cores, rank 0 only"},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample,
+                         "cpu_model": cpu_model()},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -507,8 +533,10 @@ def run_ours(args):
     cpu = None
     if ws == 1 and not args.no_cpu_baseline:
         rate, threads, desc, secs = cpu_oracle_rate(Ws_cpu, per_m, m_list, args.cpu_budget)
+        rate1, _, desc1, secs1 = cpu_oracle_rate(Ws_cpu, per_m, m_list, args.cpu_single_budget, threads=1)
         cpu = {"value": rate, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": desc,
-               "seconds": secs}
+               "seconds": secs, "cpu_model": cpu_model(),
+               "single_thread": {"value": rate1, "unit": "GB/s", "sample": desc1, "seconds": secs1}}
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -739,6 +767,8 @@ def main(argv=None):
     ap.add_argument("--replays", type=int, default=200)
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--cpu-single-budget", type=float, default=4.0,
+                    help="seconds of single-threaded oracle time (cpu_baseline.single_thread)")
     ap.add_argument("--ref-budget", type=float, default=90.0, help="seconds for the reference arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--skip-per-m", action="store_true", help="skip the per-M repeat/replay timing")

@@ -30,6 +30,7 @@ def test_reference_arm_json_line():
     assert d["value"] > 0 and d["ms_per_step"] > 0
     cpu = d["cpu_baseline"]
     assert cpu["kind"] == "oracle" and cpu["value"] == d["value"] and cpu["cores"] >= 1 and cpu["sample"]
+    assert cpu["cpu_model"]
     assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
 
 
@@ -56,3 +57,24 @@ def test_algorithmic_bytes_and_ridge():
     peaks = {"hbm_gbs": 6772.9, "bf16_tflops": 1900.0}
     assert not bench.tensor_bound(16, peaks) and not bench.tensor_bound(128, peaks)
     assert bench.tensor_bound(1024, peaks)
+
+
+def test_cpu_oracle_rate_single_and_all_threads():
+    """The CPU baseline's two legs on a small slice of the workload: all host
+    threads and one thread, each within its time budget."""
+    from skinny_bf16_gemm_residual_gb300 import inputs
+
+    Ws = [inputs.make_weights(64, 256, seed=s) for s in range(2)]
+    per_m = {M: {"A_cpu": inputs.make_rows(M, 256, seed=M),
+                 "R_cpu": [inputs.make_rows(M, 64, seed=100 + M + s) for s in range(2)]} for M in (1, 4)}
+    old = (bench.N_DIM, bench.K_DIM)
+    try:
+        bench.N_DIM, bench.K_DIM = 64, 256
+        rate, threads, desc, secs = bench.cpu_oracle_rate(Ws, per_m, (1, 4), 0.2)
+        rate1, threads1, _, secs1 = bench.cpu_oracle_rate(Ws, per_m, (1, 4), 0.2, threads=1)
+    finally:
+        bench.N_DIM, bench.K_DIM = old
+    assert threads == (os.cpu_count() or 1) and threads1 == 1
+    assert rate > 0 and rate1 > 0 and 0.2 <= secs < 5 and 0.2 <= secs1 < 5
+    assert "threads" in desc
+    assert bench.cpu_model()
