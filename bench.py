@@ -301,16 +301,21 @@ def time_graph(g, stream, replays: int, repeats: int):
 
 
 # ------------------------------------------------------------------ CPU arms
-def cpu_model() -> str:
-    """The host CPU's name as /proc/cpuinfo gives it (x86 "model name"; on Arm
-    the implementer and part codes when no name is listed)."""
-    try:
-        with open("/proc/cpuinfo") as f:
-            lines = f.read().splitlines()
-    except OSError:
-        lines = []
+ARM_CORES = {("0x41", "0xd4f"): "Arm Neoverse V2", ("0x41", "0xd40"): "Arm Neoverse V1",
+             ("0x41", "0xd49"): "Arm Neoverse N2", ("0x41", "0xd0c"): "Arm Neoverse N1"}
+
+
+def cpu_model(cpuinfo: str | None = None) -> str:
+    """The host CPU's name as /proc/cpuinfo gives it (x86 "model name"; on Arm,
+    which lists no name, the core named from its implementer and part codes)."""
+    if cpuinfo is None:
+        try:
+            with open("/proc/cpuinfo") as f:
+                cpuinfo = f.read()
+        except OSError:
+            cpuinfo = ""
     fields = {}
-    for line in lines:
+    for line in cpuinfo.splitlines():
         if ":" in line:
             k, v = line.split(":", 1)
             fields.setdefault(k.strip(), v.strip())
@@ -318,7 +323,9 @@ def cpu_model() -> str:
         if fields.get(key):
             return fields[key]
     if "CPU part" in fields:
-        return f"{platform.machine()} implementer {fields.get('CPU implementer', '?')} part {fields['CPU part']}"
+        impl, part = fields.get("CPU implementer", "?"), fields["CPU part"]
+        name = ARM_CORES.get((impl, part))
+        return f"{name} (implementer {impl}, part {part})" if name else f"{platform.machine()} implementer {impl} part {part}"
     return platform.machine() or "unknown"
 
 

@@ -78,3 +78,13 @@ def test_cpu_oracle_rate_single_and_all_threads():
     assert rate > 0 and rate1 > 0 and 0.2 <= secs < 5 and 0.2 <= secs1 < 5
     assert "threads" in desc
     assert bench.cpu_model()
+
+
+def test_cpu_model_names():
+    x86 = "processor\t: 0\nvendor_id\t: GenuineIntel\nmodel name\t: Intel(R) Xeon(R) Processor\n"
+    assert bench.cpu_model(x86) == "Intel(R) Xeon(R) Processor"
+    grace = "processor\t: 0\nBogoMIPS\t: 2000.00\nCPU implementer\t: 0x41\nCPU architecture: 8\nCPU part\t: 0xd4f\n"
+    assert bench.cpu_model(grace).startswith("Arm Neoverse V2")
+    other = "CPU implementer\t: 0x51\nCPU part\t: 0x001\n"
+    assert "part 0x001" in bench.cpu_model(other)
+    assert bench.cpu_model("")
