@@ -14,6 +14,10 @@ not part of the BF16 table.
 
     python -m skinny_bf16_gemm_residual_gb300.sweep --m 1 2 4 8 16 --output sweep.jsonl
     python -m skinny_bf16_gemm_residual_gb300.sweep --paths w8,w8simt --copies 8 --output sweep_w8.jsonl
+
+Rows are written as soon as they are timed.  With ``--resume`` the output file
+is appended to and every (M, N, K, backend, configuration) already in it is
+skipped, so an interrupted sweep continues where it stopped.
 """
 from __future__ import annotations
 
@@ -120,6 +124,48 @@ def candidate_configs(path: int, M: int, K: int, grid: str) -> list[dict]:
     return out
 
 
+def row_key(m: int, n: int, k: int, backend: str, cfg: dict) -> tuple:
+    """Identity of a sweep row: shape, backend and launch configuration."""
+    return (int(m), int(n), int(k), backend, json.dumps(cfg, sort_keys=True))
+
+
+def load_done(path: str) -> set:
+    """Keys of the rows already in a sweep output file (a missing file has
+    none; a line cut short by an interrupted run is ignored)."""
+    done = set()
+    try:
+        with open(path) as f:
+            for line in f:
+                try:
+                    r = json.loads(line)
+                    done.add(row_key(r["m"], r["n"], r["k"], r["backend"], r["config"]))
+                except (ValueError, KeyError, TypeError):
+                    continue
+    except OSError:
+        pass
+    return done
+
+
+def open_output(path: str, resume: bool):
+    """The output file, appended to when resuming (after a newline if an
+    interrupted run left the last line unfinished), else truncated."""
+    if not resume:
+        return open(path, "w")
+    tail = b""
+    try:
+        with open(path, "rb") as f:
+            f.seek(0, 2)
+            if f.tell() > 0:
+                f.seek(-1, 2)
+                tail = f.read(1)
+    except OSError:
+        pass
+    out = open(path, "a")
+    if tail and tail != b"\n":
+        out.write("\n")
+    return out
+
+
 def summarize(samples):
     ordered = sorted(samples)
 
@@ -177,7 +223,10 @@ def main(argv=None):
     ap.add_argument("--config", action="append", default=[],
                     help="time only this configuration (JSON object of sgr_config fields; repeatable)")
     ap.add_argument("--output", default=None)
+    ap.add_argument("--resume", action="store_true", help="append to --output, skipping rows already in it")
     args = ap.parse_args(argv)
+    if args.resume and not args.output:
+        ap.error("--resume needs --output")
     torch.cuda.set_device(0)
     sgr.sgr_init(0)
     dev = torch.device("cuda", 0)
@@ -187,7 +236,8 @@ def main(argv=None):
     props = torch.cuda.get_device_properties(dev)
     meta = {"device": props.name, "sms": props.multi_processor_count,
             "l2_bytes": props.L2_cache_size, "torch": torch.__version__}
-    out = open(args.output, "w") if args.output else None
+    done = load_done(args.output) if args.resume else set()
+    out = open_output(args.output, args.resume) if args.output else None
     paths = {"simt": sgr.SGR_PATH_SIMT, "tc": sgr.SGR_PATH_TC, "rows": sgr.SGR_PATH_TC_ROWS,
              "tile": sgr.SGR_PATH_TILE, "w8": sgr.SGR_PATH_W8, "w8simt": sgr.SGR_PATH_SIMT}
     fp8 = [name for name in args.paths.split(",") if name in ("w8", "w8simt")]
@@ -201,9 +251,24 @@ def main(argv=None):
         Ys = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for _ in range(args.copies)]
         nbytes = 2 * (N * K + M * K + 2 * M * N)
         rows = []
-        if not args.no_cublas:
+
+        def record(backend, cfg, samples):
+            row = {"m": M, "n": N, "k": K, "backend": backend, "config": cfg, "num_buffers": args.copies, **meta}
+            if isinstance(samples, str):
+                row.update({"valid": False, "error": samples})
+            else:
+                s = summarize(samples)
+                row.update(s)
+                fp8_bytes = N * K + 4 * N + 2 * M * K + 4 * M * N
+                row["gbs"] = (fp8_bytes if backend.startswith("w8") else nbytes) / (s["median_us"] * 1e-6) / 1e9
+            if out:
+                out.write(json.dumps(row, sort_keys=True) + "\n")
+                out.flush()
+            rows.append((backend, cfg, samples))
+
+        if not args.no_cublas and row_key(M, N, K, "cublas_addmm", {}) not in done:
             launch = lambda c: torch.addmm(Rs[c], A, Ws[c].t(), out=Ys[c])
-            rows.append(("cublas_addmm", {}, graph_samples(launch, args.copies, stream, args.repeats, args.replays)))
+            record("cublas_addmm", {}, graph_samples(launch, args.copies, stream, args.repeats, args.replays))
         for name in args.paths.split(","):
             w8 = name in ("w8", "w8simt")
             if args.config:
@@ -214,6 +279,8 @@ def main(argv=None):
                 cands = candidate_configs(paths[name], M, K, args.grid)
             backend = {"w8": "w8", "w8simt": "w8_simt"}.get(name, name)
             for cfg in cands:
+                if row_key(M, N, K, backend, cfg) in done:
+                    continue
                 c = sgr.make_config(**cfg)
                 if w8:
                     launch = lambda i, c=c: sgr.skinny_gemm_residual_w8(A, Wqs[i], Scs[i], Rs[i], Ys[i], stream=stream,
@@ -222,22 +289,10 @@ def main(argv=None):
                     launch = lambda i, c=c: sgr.skinny_gemm_residual_ex(A, Ws[i], Rs[i], Ys[i], stream=stream,
                                                                         config=c)
                 try:
-                    rows.append((backend, cfg, graph_samples(launch, args.copies, stream, args.repeats, args.replays)))
+                    samples = graph_samples(launch, args.copies, stream, args.repeats, args.replays)
                 except sgr.SgrError as e:
-                    rows.append((backend, cfg, str(e)))
-        for backend, cfg, samples in rows:
-            row = {"m": M, "n": N, "k": K, "backend": backend, "config": cfg, "num_buffers": args.copies, **meta}
-            if isinstance(samples, str):
-                row.update({"valid": False, "error": samples})
-            else:
-                s = summarize(samples)
-                row.update(s)
-                fp8_bytes = N * K + 4 * N + 2 * M * K + 4 * M * N
-                row["gbs"] = (fp8_bytes if backend.startswith("w8") else nbytes) / (s["median_us"] * 1e-6) / 1e9
-            line = json.dumps(row, sort_keys=True)
-            if out:
-                out.write(line + "\n")
-                out.flush()
+                    samples = str(e)
+                record(backend, cfg, samples)
         best = {}
         for backend, cfg, samples in rows:
             if isinstance(samples, str):
