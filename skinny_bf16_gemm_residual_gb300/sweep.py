@@ -24,6 +24,7 @@ from __future__ import annotations
 import argparse
 import json
 import math
+import os
 import statistics
 import sys
 
@@ -122,6 +123,44 @@ def candidate_configs(path: int, M: int, K: int, grid: str) -> list[dict]:
                         continue
                     out.append(dict(path=path, ctas_per_sm=cps, k_blocks_per_stage=kb, stages=st))
     return out
+
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+
+
+def load_peaks(path: str | None = None) -> tuple[dict, str]:
+    """HBM copy bandwidth (GB/s) and BF16 tensor throughput (TFLOP/s) measured
+    on this GPU model (MEASURED_PEAKS.json at the repository root), else the
+    fallback figures; returns (peaks, "measured" | "fallback")."""
+    path = path or os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"])}, "measured"
+    except (OSError, KeyError, ValueError, TypeError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def build_row(M: int, N: int, K: int, backend: str, cfg: dict, copies: int, meta: dict, samples,
+              peaks: dict, peak_source: str) -> dict:
+    """One sweep row: timing statistics, achieved GB/s of algorithmic bytes
+    (BF16: W, A, R, Y once; FP8 weights: codes, scales, A, R, Y once), TFLOP/s
+    (2*M*N*K) and both as fractions of the peaks; or the error of a refused
+    configuration (`samples` a string)."""
+    row = {"m": M, "n": N, "k": K, "backend": backend, "config": cfg, "num_buffers": copies, **meta}
+    if isinstance(samples, str):
+        row.update({"valid": False, "error": samples})
+        return row
+    st = summarize(samples)
+    row.update(st)
+    nbytes = (N * K + 4 * N + 2 * M * K + 4 * M * N) if backend.startswith("w8") else 2 * (N * K + M * K + 2 * M * N)
+    sec = st["median_us"] * 1e-6
+    row["gbs"] = nbytes / sec / 1e9
+    row["tflops"] = 2.0 * M * N * K / sec / 1e12
+    row["frac_of_hbm_peak"] = row["gbs"] / peaks["hbm_gbs"]
+    row["frac_of_tensor_peak"] = row["tflops"] / peaks["bf16_tflops"]
+    row["peak_source"] = peak_source
+    return row
 
 
 def row_key(m: int, n: int, k: int, backend: str, cfg: dict) -> tuple:
@@ -236,6 +275,7 @@ def main(argv=None):
     props = torch.cuda.get_device_properties(dev)
     meta = {"device": props.name, "sms": props.multi_processor_count,
             "l2_bytes": props.L2_cache_size, "torch": torch.__version__}
+    peaks, peak_source = load_peaks()
     done = load_done(args.output) if args.resume else set()
     out = open_output(args.output, args.resume) if args.output else None
     paths = {"simt": sgr.SGR_PATH_SIMT, "tc": sgr.SGR_PATH_TC, "rows": sgr.SGR_PATH_TC_ROWS,
@@ -249,18 +289,10 @@ def main(argv=None):
         A = inputs.make_rows(M, K, seed=10_000 + M).to(dev)
         Rs = [inputs.make_rows(M, N, seed=20_000 + 100 * M + s).to(dev) for s in range(args.copies)]
         Ys = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for _ in range(args.copies)]
-        nbytes = 2 * (N * K + M * K + 2 * M * N)
         rows = []
 
         def record(backend, cfg, samples):
-            row = {"m": M, "n": N, "k": K, "backend": backend, "config": cfg, "num_buffers": args.copies, **meta}
-            if isinstance(samples, str):
-                row.update({"valid": False, "error": samples})
-            else:
-                s = summarize(samples)
-                row.update(s)
-                fp8_bytes = N * K + 4 * N + 2 * M * K + 4 * M * N
-                row["gbs"] = (fp8_bytes if backend.startswith("w8") else nbytes) / (s["median_us"] * 1e-6) / 1e9
+            row = build_row(M, N, K, backend, cfg, args.copies, meta, samples, peaks, peak_source)
             if out:
                 out.write(json.dumps(row, sort_keys=True) + "\n")
                 out.flush()

@@ -48,3 +48,26 @@ def test_fresh_output_and_missing_file(tmp_path):
     with sweep.open_output(str(path), resume=False) as out:  # a fresh sweep truncates
         out.write("")
     assert path.read_text() == ""
+
+
+def test_row_metrics():
+    peaks = {"hbm_gbs": 6772.9, "bf16_tflops": 1900.0}
+    samples = [10.0, 11.0, 12.0]
+    r = sweep.build_row(4, 7168, 3584, "rows", {"path": 3}, 4, {"device": "x"}, samples, peaks, "measured")
+    nbytes = 2 * (7168 * 3584 + 4 * 3584 + 2 * 4 * 7168)
+    assert r["median_us"] == 11.0 and r["device"] == "x" and r["num_buffers"] == 4
+    assert abs(r["gbs"] - nbytes / 11e-6 / 1e9) < 1e-9
+    assert abs(r["tflops"] - 2 * 4 * 7168 * 3584 / 11e-6 / 1e12) < 1e-9
+    assert abs(r["frac_of_hbm_peak"] - r["gbs"] / 6772.9) < 1e-12
+    assert abs(r["frac_of_tensor_peak"] - r["tflops"] / 1900.0) < 1e-12
+    w = sweep.build_row(4, 7168, 3584, "w8", {"path": 5}, 8, {}, samples, peaks, "measured")
+    assert abs(w["gbs"] - (7168 * 3584 + 4 * 7168 + 2 * 4 * 3584 + 4 * 4 * 7168) / 11e-6 / 1e9) < 1e-9
+    e = sweep.build_row(4, 7168, 3584, "tile", {"path": 4}, 4, {}, "status 5", peaks, "measured")
+    assert e["valid"] is False and e["error"] == "status 5" and "gbs" not in e
+
+
+def test_peaks_file(tmp_path):
+    p = tmp_path / "peaks.json"
+    p.write_text(json.dumps({"hbm_gbs": 6772.9, "bf16_tflops": 1900}))
+    assert sweep.load_peaks(str(p)) == ({"hbm_gbs": 6772.9, "bf16_tflops": 1900.0}, "measured")
+    assert sweep.load_peaks(str(tmp_path / "absent.json"))[1] == "fallback"
