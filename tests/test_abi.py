@@ -37,6 +37,53 @@ def test_library_exports_every_declared_symbol():
         ctypes.cast(getattr(lib, name), ctypes.c_void_p)
 
 
+def _header_text():
+    text = "".join(open(h).read() for h in glob.glob(os.path.join(ROOT, "include", "*.h")))
+    return re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+
+
+def test_header_constants_match_binding():
+    """Every SGR_ constant of the header (ABI version, status codes, flags,
+    paths) has the same value in the Python binding."""
+    text = _header_text()
+    consts = {m.group(1): int(m.group(2), 0) for m in re.finditer(r"#define\s+(SGR_\w+)\s+(0x[0-9a-fA-F]+|\d+)u?", text)}
+    consts.update({m.group(1): int(m.group(2)) for m in re.finditer(r"\b(SGR_\w+)\s*=\s*(\d+)", text)})
+    assert len(consts) >= 15, consts
+    for name, value in consts.items():
+        key = "ABI_VERSION" if name == "SGR_ABI_VERSION" else name
+        assert getattr(binding, key) == value, (name, value, getattr(binding, key, None))
+
+
+def _struct_fields(text, name):
+    body = re.search(r"typedef struct\s*\{([^{}]*)\}\s*" + name + r"\s*;", text).group(1)
+    return [m.group(1) for m in re.finditer(r"(\w+)\s*(?:\[\s*\d+\s*\])?\s*;", body)]
+
+
+def test_header_structs_match_binding():
+    """The ctypes structures list the C structures' fields in the same order
+    with the same sizes (a stale layout would pass garbage to the library)."""
+    text = _header_text()
+    assert _struct_fields(text, "sgr_config") == [f[0] for f in binding.sgr_config._fields_]
+    assert _struct_fields(text, "sgr_group") == [f[0] for f in binding.sgr_group._fields_]
+    assert ctypes.sizeof(binding.sgr_config) == 11 * 4
+    assert ctypes.sizeof(binding.sgr_group) == 7 * 8 + 2 * 4
+
+
+def test_binding_argument_counts_match_header():
+    """Each function's ctypes argument list is as long as its C parameter list."""
+    text = _header_text()
+    lib = sgr.load()
+    seen = 0
+    for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(\w+)\s*\(([^()]*)\)\s*;", text, flags=re.M):
+        name, params = m.group(1), m.group(2).strip()
+        if name not in binding.EXPORTS:
+            continue
+        n = 0 if params in ("", "void") else params.count(",") + 1
+        assert len(getattr(lib, name).argtypes) == n, (name, n, getattr(lib, name).argtypes)
+        seen += 1
+    assert seen == len(binding.EXPORTS)
+
+
 def test_abi_version_and_status_strings():
     assert sgr.sgr_abi_version() == sgr.ABI_VERSION
     for s in range(0, 8):
