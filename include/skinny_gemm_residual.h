@@ -27,6 +27,11 @@
  * no reference to them after the call returns.  A per-device workspace used by
  * the tensor-core split-K path is owned by the library, allocated once per
  * device by sgr_init() (or lazily on first use) and released at process exit.
+ * Calls forced onto that path (SGR_PATH_TC) share it: such calls whose
+ * kernels may overlap on the GPU (different streams, graphs replayed
+ * concurrently) must be serialised by the caller.  The library's own choice
+ * (SGR_PATH_AUTO) never takes that path, and every other path keeps no state
+ * between calls.
  *
  * Asynchrony.  Calls enqueue work on `stream` (a cudaStream_t; NULL is the
  * legacy default stream) and return without synchronising.  Kernels launch

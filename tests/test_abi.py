@@ -164,6 +164,16 @@ def test_select_path():
     assert sgr.sgr_select_path(4, 7170, 3584) < 0
 
 
+def test_automatic_choice_never_takes_the_shared_workspace_path():
+    """The stream-K kernel shares the library's per-device workspace, so only
+    an explicit configuration may select it (the header says so)."""
+    for N in (8, 152, 1024, 3584, 7168, 7176, 1 << 17):
+        for K in (8, 64, 520, 3584, 7168, 65536):
+            for M in (1, 2, 3, 16, 17, 64, 65, 128, 256, 257, 1024, 5000):
+                path = sgr.sgr_select_path(M, N, K)
+                assert path > 0 and path != sgr.SGR_PATH_TC, (M, N, K, path)
+
+
 def test_table_header_is_sorted_and_covers_the_latent_moe_shape():
     """The generated per-M table lists entries by increasing M per (N, K)."""
     import re
