@@ -10,8 +10,12 @@
 
 int main() {
   const int sms = 152;
-  const int Ms[] = {1, 3, 16, 17, 32, 40, 48, 64, 100, 128, 200, 256};
-  const int NKs[][2] = {{7168, 3584}, {3584, 7168}, {520, 264}, {8, 3584}, {1024, 1024}, {152, 1792}};
+  const int Ms[] = {1, 3, 16, 17, 32, 40, 48, 64, 100, 128, 200, 256, 1024};
+  // The latent-MoE shapes, ragged and tiny ones, and the large ends: N = 2^17
+  // (past the row slab's 128 rows per CTA), K = 65536 and K = 2^20 (the
+  // library's largest K).
+  const int NKs[][2] = {{7168, 3584}, {3584, 7168}, {520, 264}, {8, 3584}, {1024, 1024}, {152, 1792},
+                        {131072, 64}, {152, 65536}, {16, 1048576}};
   for (auto& nk : NKs) {
     const int N = nk[0], K = nk[1];
     for (int M : Ms) {

@@ -95,3 +95,14 @@ def test_tile_plans(plans):
             assert p["grid"] == 2 * p["m_tiles"] * p["n_tiles"] <= 152, p
         else:
             assert p["grid"] == min(p["m_tiles"] * p["n_tiles"], 152), p
+
+
+def test_large_ends_are_planned_or_refused(plans):
+    """The largest K is planned by every kernel; N = 2^17 is refused by the
+    row slabs (more than 128 rows per CTA on 152 SMs) and planned by the tile
+    kernel, which also takes M = 1024 (the row slabs hold at most 256 tokens)."""
+    kinds = lambda **kw: {p["kind"] for p in plans if all(p[k] == v for k, v in kw.items())}  # noqa: E731
+    assert kinds(K=1048576) == {"rows", "w8", "tile"}
+    assert kinds(N=131072) == {"tile"}
+    assert kinds(M=1024) == {"tile"}
+    assert {"rows", "w8", "tile"} <= kinds(K=65536, M=256)
