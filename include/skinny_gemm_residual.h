@@ -76,7 +76,7 @@
 extern "C" {
 #endif
 
-#define SGR_ABI_VERSION 6
+#define SGR_ABI_VERSION 7
 
 typedef enum {
   SGR_OK = 0,
@@ -136,8 +136,7 @@ typedef struct {
   int prefetch_stages;    /* TC_ROWS, TILE: weight stages requested before the dependency wait */
   int tile_n;             /* TILE: W rows per output tile (MMA N): 64, 128, 192 or 256 */
   int k_split;            /* TILE: 1, or 2 = K split over a 2-CTA cluster (one tile per cluster; tile_n <= 192) */
-  int pair_w;             /* TILE: 1 = 2-CTA clusters on token tiles 2i, 2i+1 share each W tile (multicast) */
-  int reserved[1];        /* must be zero */
+  int reserved[2];        /* must be zero */
 } sgr_config;
 
 /*

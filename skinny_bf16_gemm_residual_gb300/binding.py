@@ -14,7 +14,7 @@ import threading
 
 from . import build as _build
 
-ABI_VERSION = 6  # must equal SGR_ABI_VERSION of the loaded library
+ABI_VERSION = 7  # must equal SGR_ABI_VERSION of the loaded library
 
 SGR_OK = 0
 SGR_ERR_NULL = 1
@@ -52,15 +52,14 @@ class sgr_config(ctypes.Structure):
                 ("stages", ctypes.c_int), ("rows_per_stage", ctypes.c_int),
                 ("k_blocks_per_stage", ctypes.c_int), ("token_tile", ctypes.c_int),
                 ("prefetch_stages", ctypes.c_int), ("tile_n", ctypes.c_int),
-                ("k_split", ctypes.c_int), ("pair_w", ctypes.c_int),
-                ("reserved", ctypes.c_int * 1)]
+                ("k_split", ctypes.c_int),
+                ("reserved", ctypes.c_int * 2)]
 
     def as_dict(self) -> dict:
         return {"path": self.path, "ctas_per_sm": self.ctas_per_sm, "stages": self.stages,
                 "rows_per_stage": self.rows_per_stage,
                 "k_blocks_per_stage": self.k_blocks_per_stage, "token_tile": self.token_tile,
-                "prefetch_stages": self.prefetch_stages, "tile_n": self.tile_n, "k_split": self.k_split,
-                "pair_w": self.pair_w}
+                "prefetch_stages": self.prefetch_stages, "tile_n": self.tile_n, "k_split": self.k_split}
 
 
 _lock = threading.Lock()
@@ -461,9 +460,9 @@ def skinny_gemm_residual_grouped(problems, flags: int = 0, stream=None, config: 
 
 def make_config(path: int = SGR_PATH_AUTO, ctas_per_sm: int = 0, stages: int = 0,
                 rows_per_stage: int = 0, k_blocks_per_stage: int = 0, token_tile: int = 0,
-                prefetch_stages: int = 0, tile_n: int = 0, k_split: int = 0, pair_w: int = 0) -> sgr_config:
+                prefetch_stages: int = 0, tile_n: int = 0, k_split: int = 0) -> sgr_config:
     c = sgr_config()
     c.path, c.ctas_per_sm, c.stages = path, ctas_per_sm, stages
     c.rows_per_stage, c.k_blocks_per_stage, c.token_tile = rows_per_stage, k_blocks_per_stage, token_tile
-    c.prefetch_stages, c.tile_n, c.k_split, c.pair_w = prefetch_stages, tile_n, k_split, pair_w
+    c.prefetch_stages, c.tile_n, c.k_split = prefetch_stages, tile_n, k_split
     return c

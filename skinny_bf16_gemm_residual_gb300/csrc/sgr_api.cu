@@ -281,7 +281,6 @@ int resolve_config(int dev_sms, int M, int N, int K, const sgr_config* in, sgr_c
       if (path == SGR_PATH_TC_ROWS || path == SGR_PATH_TILE) out->prefetch_stages = e->prefetch_stages;
       if (path == SGR_PATH_TILE && e->tile_n) out->tile_n = e->tile_n;
       if (path == SGR_PATH_TILE) out->k_split = e->k_split > 0 ? e->k_split : 1;
-      if (path == SGR_PATH_TILE) out->pair_w = e->pair_w;
     }
   }
   if (in) {
@@ -294,11 +293,9 @@ int resolve_config(int dev_sms, int M, int N, int K, const sgr_config* in, sgr_c
     if (in->token_tile) out->token_tile = in->token_tile;
     if (in->prefetch_stages) out->prefetch_stages = in->prefetch_stages;
     if (in->tile_n) out->tile_n = in->tile_n;
-    // A chosen tile width runs unsplit and unpaired unless those are asked for too.
+    // A chosen tile width runs unsplit unless the split is asked for too.
     if (in->k_split) out->k_split = in->k_split;
     else if (path == SGR_PATH_TILE && in->tile_n) out->k_split = 1;
-    if (in->pair_w) out->pair_w = in->pair_w;
-    else if (path == SGR_PATH_TILE && (in->tile_n || in->k_split)) out->pair_w = 0;
     // A tile width chosen without a ring depth gets the deepest ring that fits it.
     if (path == SGR_PATH_TILE && (in->tile_n || in->k_blocks_per_stage) && !in->stages)
       out->stages = sgr::tile_default_stages(out->tile_n, out->k_blocks_per_stage > 0 ? out->k_blocks_per_stage : 1);
@@ -603,7 +600,7 @@ int resolve_config_w8(int sms, int M, int N, int K, long long ldw, const sgr_con
     if (in) {
       for (int r : in->reserved)
         if (r != 0) return SGR_ERR_UNSUPPORTED;
-      if (in->tile_n || in->k_split || in->pair_w || in->k_blocks_per_stage || in->token_tile ||
+      if (in->tile_n || in->k_split || in->k_blocks_per_stage || in->token_tile ||
           in->prefetch_stages)
         return SGR_ERR_UNSUPPORTED;
       if (in->ctas_per_sm) out->ctas_per_sm = in->ctas_per_sm;
@@ -622,7 +619,7 @@ int resolve_config_w8(int sms, int M, int N, int K, long long ldw, const sgr_con
   if (in) {
     for (int r : in->reserved)
       if (r != 0) return SGR_ERR_UNSUPPORTED;
-    if (in->tile_n || in->k_split || in->pair_w) return SGR_ERR_UNSUPPORTED;
+    if (in->tile_n || in->k_split) return SGR_ERR_UNSUPPORTED;
     if (in->ctas_per_sm) out->ctas_per_sm = in->ctas_per_sm;
     if (in->rows_per_stage) out->rows_per_stage = in->rows_per_stage;
     if (in->stages) out->stages = in->stages;

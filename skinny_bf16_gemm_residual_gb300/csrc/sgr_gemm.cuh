@@ -177,26 +177,6 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
   }
 }
 
-// 2-D tensor copy global -> the same shared-memory offset in every CTA of
-// `mask` (cluster multicast), completion counted on the mbarrier at the same
-// offset in each of them.
-__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const void* tmap, int32_t x, int32_t y,
-                                                      uint32_t bar, uint16_t mask, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(dst),
-      "l"(tmap), "r"(x), "r"(y), "r"(bar), "h"(mask), "l"(policy)
-      : "memory");
-}
-
-// Arrive on the mbarrier at `bar`'s offset in every CTA of `mask` once all
-// prior tcgen05 operations of this thread have completed.
-__device__ __forceinline__ void mma_commit_multicast(uint32_t bar, uint16_t mask) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
-               "h"(mask)
-               : "memory");
-}
-
 // All threads of every CTA of the cluster.
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -216,11 +196,6 @@ __device__ __forceinline__ void load_residual_row(const TileParams& p, int m, in
 
 // Modes (template parameter MODE):
 // kTilePlain: persistent CTAs, each tile's whole K in one CTA.
-// kTilePairW: persistent 2-CTA clusters on the two token tiles 2i, 2i+1 of
-// the same W column tile; each rank loads half of every W box and multicasts
-// it to both, so each W byte leaves L2 once per pair (the operand feed from
-// L2, not the tensor core, bounds large tiles); the MMA's stage release is
-// multicast too, so a slot is reloaded only when both ranks are done with it.
 // kTileSplitK: one tile per 2-CTA cluster, rank 0 accumulating K blocks
 // [0, kb_split) and rank 1 the rest; at the end each rank sends the half of
 // its accumulator that the other rank owns through distributed shared memory
@@ -228,7 +203,9 @@ __device__ __forceinline__ void load_residual_row(const TileParams& p, int m, in
 // and stores that half of the tile.  (a + b is the same in either order, so
 // the result does not depend on which rank finishes first.)  This doubles
 // the CTAs working on a problem with few tiles (M <= 256 at N = 7168).
-enum : int { kTilePlain = 1, kTileSplitK = 2, kTilePairW = 3 };
+// Every CTA loads its own operands with plain TMA copies into its own
+// shared memory.
+enum : int { kTilePlain = 1, kTileSplitK = 2 };
 
 // Threads per CTA: producer warp, MMA warp, four epilogue warps.  (A second
 // MMA-issuing warp taking every other ring slot into its own accumulator was
@@ -241,11 +218,9 @@ __global__ void __launch_bounds__(tile_threads(MODE), 1)
     tile_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                      const TileParams p) {
   constexpr int KSPLIT = MODE == kTileSplitK ? 2 : 1;
-  constexpr bool PAIR = MODE == kTilePairW;
   constexpr int CL = MODE == kTilePlain ? 1 : 2;  // CTAs per cluster
 
   static_assert(MODE != kTileSplitK || (NT / 2) % 32 == 0, "split tiles hand over 32-column chunks");
-  static_assert(!PAIR || (NT / 2) % 8 == 0, "each rank's half W box is whole 8-row swizzle atoms");
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -271,9 +246,8 @@ __global__ void __launch_bounds__(tile_threads(MODE), 1)
   const uint32_t rank = CL == 2 ? cluster_ctarank() : 0u;
   const int G = (int)gridDim.x / CL;      // tile-processing units (CTAs or clusters)
   const int unit = (int)blockIdx.x / CL;  // this CTA's unit
-  // Tiles of a unit: plain / split: (token tile, W column tile); pair: (pair
-  // of token tiles, W column tile), this rank taking token tile 2 i + rank.
-  const int mt_u = PAIR ? p.m_tiles / 2 : p.m_tiles;
+  // Tiles of a unit: (token tile, W column tile).
+  const int mt_u = p.m_tiles;
   const int tiles = mt_u * p.n_tiles;
   const int my_tiles = (tiles - unit + G - 1) / G;  // >= 1: units <= tiles; 1 when split
   const int kb0 = (KSPLIT == 2 && rank == 1) ? p.kb_split : 0;
@@ -283,7 +257,7 @@ __global__ void __launch_bounds__(tile_threads(MODE), 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
-      mbar_init(smem_u32(&empty[s]), PAIR ? 2 : 1);  // pair: both ranks' MMAs release a slot
+      mbar_init(smem_u32(&empty[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&acc_full[b]), 1);
@@ -327,7 +301,7 @@ __global__ void __launch_bounds__(tile_threads(MODE), 1)
         c.kx = kb0 * kTcKBlock;
         c.kb = 0;
         c.t = unit;
-        c.m0 = ((c.t % mt_u) * (PAIR ? 2 : 1) + (int)rank * (PAIR ? 1 : 0)) * kTileM;
+        c.m0 = (c.t % mt_u) * kTileM;
         c.n0 = (c.t / mt_u) * NT;
       };
       auto advance = [&](Cursor& c) {
@@ -336,19 +310,13 @@ __global__ void __launch_bounds__(tile_threads(MODE), 1)
           c.kb = 0;
           c.kx = kb0 * kTcKBlock;
           c.t += G;
-          c.m0 = ((c.t % mt_u) * (PAIR ? 2 : 1) + (int)rank * (PAIR ? 1 : 0)) * kTileM;
+          c.m0 = (c.t % mt_u) * kTileM;
           c.n0 = (c.t / mt_u) * NT;
         }
       };
-      // W box j of a stage; a pair rank loads its half of the rows into both
-      // ranks' shared memory.
+      // W box j of a stage.
       auto load_w = [&](uint32_t stage, int j, int kx, int n0, uint32_t fb) {
-        const uint32_t dst = stage + a_part + (uint32_t)j * w_box;
-        if constexpr (PAIR)
-          tma_load_2d_multicast(dst + rank * (uint32_t)(NT / 2) * 128u, &tmW, kx + j * kTcKBlock,
-                                n0 + (int)rank * (NT / 2), fb, (uint16_t)0x3, pol_w);
-        else
-          tma_load_2d(dst, &tmW, kx + j * kTcKBlock, n0, fb, pol_w);
+        tma_load_2d(stage + a_part + (uint32_t)j * w_box, &tmW, kx + j * kTcKBlock, n0, fb, pol_w);
       };
       const int pre = total < p.prefetch ? total : p.prefetch;  // <= S: slots 0 .. pre-1
       Cursor c;
@@ -431,10 +399,7 @@ __global__ void __launch_bounds__(tile_threads(MODE), 1)
               mma_bf16(d, adesc0 + ao + (uint64_t)(kk * 2), wdesc0 + wo + (uint64_t)(kk * 2), idesc,
                        (ks | j | kk) != 0 ? 1u : 0u);
           }
-          if constexpr (PAIR)
-            mma_commit_multicast(smem_u32(&empty[slot]), (uint16_t)0x3);
-          else
-            mma_commit(smem_u32(&empty[slot]));
+          mma_commit(smem_u32(&empty[slot]));
           doff += dstep;
           if (++slot == S) {
             slot = 0;
@@ -451,13 +416,12 @@ __global__ void __launch_bounds__(tile_threads(MODE), 1)
       mma_commit(smem_u32(drain));
       if (!mbar_wait(smem_u32(drain), 0)) report_error(p.err, kErrDrain);
     }
-  } else if constexpr (KSPLIT == 1) {  // plain and pair
+  } else if constexpr (KSPLIT == 1) {
     // ------------------------------------------------------------ epilogue
     pdl_wait();  // R may come from the preceding kernel; Y may be read by it
     const int q = warp & 3;  // TMEM lane quarter = tile rows [32 q, 32 q + 32)
-    const int mstep = PAIR ? 2 : 1, moff = PAIR ? (int)rank : 0;
     int t = unit;
-    int m = ((t % mt_u) * mstep + moff) * kTileM + q * kTileEpiRows + lane;  // this thread's output row
+    int m = (t % mt_u) * kTileM + q * kTileEpiRows + lane;  // this thread's output row
     int n0 = (t / mt_u) * NT;
     uint4 rv[NT / 8];
     load_residual_row<NT>(p, m, n0, rv);
@@ -492,7 +456,7 @@ __global__ void __launch_bounds__(tile_threads(MODE), 1)
       if (lane == 0) mbar_arrive(smem_u32(&acc_empty[buf]));
       if (i + 1 < my_tiles) {  // next tile's residuals arrive during its main loop
         t += G;
-        m = ((t % mt_u) * mstep + moff) * kTileM + q * kTileEpiRows + lane;
+        m = (t % mt_u) * kTileM + q * kTileEpiRows + lane;
         n0 = (t / mt_u) * NT;
         load_residual_row<NT>(p, m, n0, rv);
       }
@@ -653,22 +617,19 @@ inline const void* tile_kernel_mode(int nt) {
 inline const void* tile_kernel_for(int nt, int mode) {
   if (mode == kTilePlain) return tile_kernel_mode<kTilePlain>(nt);
   if (mode == kTileSplitK) return tile_kernel_mode<kTileSplitK>(nt);
-  if (mode == kTilePairW) return tile_kernel_mode<kTilePairW>(nt);
   return nullptr;
 }
 
-// Mode of a configuration: k_split 2 -> split K; pair_w 1 -> W shared by a
-// pair of token tiles; both 0/1 -> plain (both set: none).
+// Mode of a configuration: k_split 2 -> split K; 0 or 1 -> plain.
 inline int tile_mode(const sgr_config& c) {
   const int split = c.k_split == 0 ? 1 : c.k_split;
-  if (split == 2 && c.pair_w == 0) return kTileSplitK;
-  if (split == 1 && c.pair_w == 1) return kTilePairW;
-  if (split == 1 && c.pair_w == 0) return kTilePlain;
+  if (split == 2) return kTileSplitK;
+  if (split == 1) return kTilePlain;
   return 0;
 }
 
 inline cudaError_t tile_init_device() {
-  for (int mode : {kTilePlain, kTileSplitK, kTilePairW})
+  for (int mode : {kTilePlain, kTileSplitK})
     for (int nt : {64, 128, 192, 256}) {
       const void* fn = tile_kernel_for(nt, mode);
       if (!fn) continue;
@@ -701,7 +662,6 @@ inline int tile_plan(const sgr_config& c, int sms, int M, int N, int K, TilePara
   // Split: rank 0 takes the first half of the K blocks rounded up to whole
   // stages (so that its last stage reads nothing of rank 1's range).
   const int kb_split = ((k_blocks + 1) / 2 + kbps - 1) / kbps * kbps;
-  if (mode == kTilePairW && m_tiles % 2 != 0) return SGR_ERR_UNSUPPORTED;  // token tiles go in pairs
   if (mode == kTileSplitK) {
     // One tile per cluster, both ranks with at least one K block, and the
     // hand-over buffer (128 rows x (NT/2 + 4) floats) inside the ring.
@@ -722,9 +682,6 @@ inline int tile_plan(const sgr_config& c, int sms, int M, int N, int K, TilePara
   p->tmem_cols = detail::pow2_at_least(2 * nt);
   if (mode == kTileSplitK) {
     *grid = (int)(2 * tiles);
-  } else if (mode == kTilePairW) {
-    const long long units = tiles / 2, max_units = sms / 2;
-    *grid = (int)(2 * (units < max_units ? units : max_units));
   } else {
     *grid = (int)(tiles < sms ? tiles : sms);
   }
@@ -743,8 +700,7 @@ inline int tile_launch(const sgr_config& c, int sms, unsigned* err, const void* 
   const int mode = tile_mode(c);
   CUtensorMap tmA, tmW;
   if (!detail::make_tmap(&tmA, A, M, K, lda, kTileM, kTcKBlock)) return SGR_ERR_LAUNCH;
-  // a pair rank loads half of each W box
-  if (!detail::make_tmap(&tmW, W, N, K, K, mode == kTilePairW ? p.NT / 2 : p.NT, kTcKBlock)) return SGR_ERR_LAUNCH;
+  if (!detail::make_tmap(&tmW, W, N, K, K, p.NT, kTcKBlock)) return SGR_ERR_LAUNCH;
   p.R = static_cast<const __nv_bfloat16*>(R);
   p.Y = static_cast<__nv_bfloat16*>(Y);
   p.ldr = ldr;
@@ -780,10 +736,6 @@ inline int tile_launch(const sgr_config& c, int sms, unsigned* err, const void* 
     case kTileSplitK * 1000 + 64: e = cudaLaunchKernelEx(&lc, tile_gemm_kernel<64, kTileSplitK>, tmA, tmW, p); break;
     case kTileSplitK * 1000 + 128: e = cudaLaunchKernelEx(&lc, tile_gemm_kernel<128, kTileSplitK>, tmA, tmW, p); break;
     case kTileSplitK * 1000 + 192: e = cudaLaunchKernelEx(&lc, tile_gemm_kernel<192, kTileSplitK>, tmA, tmW, p); break;
-    case kTilePairW * 1000 + 64: e = cudaLaunchKernelEx(&lc, tile_gemm_kernel<64, kTilePairW>, tmA, tmW, p); break;
-    case kTilePairW * 1000 + 128: e = cudaLaunchKernelEx(&lc, tile_gemm_kernel<128, kTilePairW>, tmA, tmW, p); break;
-    case kTilePairW * 1000 + 192: e = cudaLaunchKernelEx(&lc, tile_gemm_kernel<192, kTilePairW>, tmA, tmW, p); break;
-    case kTilePairW * 1000 + 256: e = cudaLaunchKernelEx(&lc, tile_gemm_kernel<256, kTilePairW>, tmA, tmW, p); break;
   }
   if (e != cudaSuccess) {
     cudaGetLastError();

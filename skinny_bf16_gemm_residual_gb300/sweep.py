@@ -103,13 +103,11 @@ def candidate_configs(path: int, M: int, K: int, grid: str) -> list[dict]:
                     if grid == "small" and st < deepest - 2:
                         continue
                     for pf in sorted({st, max(1, st - 1)}):
-                        for split, pair in ((1, 0), (2, 0), (1, 1)):
+                        for split in (1, 2):
                             if split == 2 and nt > 192:
                                 continue
-                            if pair and ((M + 127) // 128) % 2:
-                                continue
                             out.append(dict(path=path, ctas_per_sm=1, tile_n=nt, k_blocks_per_stage=kb, stages=st,
-                                            prefetch_stages=pf, k_split=split, pair_w=pair))
+                                            prefetch_stages=pf, k_split=split))
     else:
         tiles = (M + 255) // 256
         nt = ((M + tiles - 1) // tiles + 15) // 16 * 16  # the library's token tile

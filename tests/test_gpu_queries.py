@@ -62,12 +62,12 @@ def table_entries(n: int, k: int):
     path = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
                         "skinny_bf16_gemm_residual_gb300", "csrc", "sgr_table.h")
     rows = []
-    for m in re.finditer(r"\{(\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+),",
+    for m in re.finditer(r"\{(\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+), (\d+),",
                          open(path).read()):
         v = [int(x) for x in m.groups()]
         if v[0] == n and v[1] == k:
             rows.append(dict(m=v[2], path=v[3], ctas_per_sm=v[4], stages=v[5], rows_per_stage=v[6],
-                             k_blocks_per_stage=v[7], prefetch_stages=v[8], tile_n=v[9], k_split=v[10], pair_w=v[11]))
+                             k_blocks_per_stage=v[7], prefetch_stages=v[8], tile_n=v[9], k_split=v[10]))
     return rows
 
 
@@ -88,4 +88,4 @@ def test_automatic_config_is_the_measured_table_entry(n, k):
         if e["path"] in (sgr.SGR_PATH_TC_ROWS, sgr.SGR_PATH_TILE):
             assert c.prefetch_stages == e["prefetch_stages"], (e, c.as_dict())
         if e["path"] == sgr.SGR_PATH_TILE:
-            assert (c.tile_n, c.k_split, c.pair_w) == (e["tile_n"], max(e["k_split"], 1), e["pair_w"]), (e, c.as_dict())
+            assert (c.tile_n, c.k_split) == (e["tile_n"], max(e["k_split"], 1)), (e, c.as_dict())

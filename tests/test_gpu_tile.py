@@ -163,48 +163,6 @@ def test_tile_split_rejects():
     assert e.value.status == sgr.SGR_ERR_UNSUPPORTED
 
 
-PAIR_CONFIGS = [
-    dict(tile_n=192, pair_w=1, stages=5),
-    dict(tile_n=256, pair_w=1, stages=4),
-    dict(tile_n=128, pair_w=1, k_blocks_per_stage=2, stages=3),
-    dict(tile_n=64, pair_w=1, stages=2, prefetch_stages=1),
-]
-
-
-@pytest.mark.parametrize("cfg", PAIR_CONFIGS, ids=lambda c: "-".join(f"{k}{v}" for k, v in c.items()))
-@pytest.mark.parametrize("M,N,K", [(256, 2056, 1032), (129, 1000, 136), (512, 776, 3584), (1000, 1512, 520)])
-def test_tile_pair_multicast(cfg, M, N, K):
-    """Token-tile pairs sharing each W tile through cluster multicast; M whose
-    128-token tiles come in an odd number is refused."""
-    p = inputs.make_problem(M, N, K, seed=7 * M + N)
-    if ((M + 127) // 128) % 2:
-        with pytest.raises(sgr.SgrError) as e:
-            run_tile(p, **cfg)
-        assert e.value.status == sgr.SGR_ERR_UNSUPPORTED
-        return
-    compare(run_tile(p, **cfg), oracle_full(p.A, p.W, p.R), f"tile pair M={M} N={N} K={K} {cfg}")
-
-
-@pytest.mark.parametrize("M", [512, 1024])
-def test_tile_pair_full_size_sampled(M):
-    p = inputs.make_problem(M, N_FULL, K_FULL, seed=M + 9)
-    got = run_tile(p, tile_n=192, pair_w=1)
-    rng = np.random.default_rng(M + 1)
-    ms = np.concatenate([rng.integers(0, M, 6000), np.zeros(N_FULL, int), np.full(N_FULL, M - 1),
-                         np.full(N_FULL, 128), np.full(N_FULL, 255)])
-    ns = np.concatenate([rng.integers(0, N_FULL, 6000)] + [np.arange(N_FULL)] * 4)
-    compare(got[ms, ns], oracle.load().sample(p.A, p.W, p.R, ms, ns), f"tile pair M={M} sampled")
-    y2 = run_tile(p, tile_n=192, pair_w=1)
-    assert np.array_equal(got, y2)
-
-
-def test_tile_pair_rejects_split_together():
-    p = inputs.make_problem(256, 1024, 256, seed=3)
-    with pytest.raises(sgr.SgrError) as e:
-        run_tile(p, tile_n=128, pair_w=1, k_split=2)
-    assert e.value.status == sgr.SGR_ERR_UNSUPPORTED
-
-
 TILE_CONFIGS = [
     dict(tile_n=64, stages=2),
     dict(tile_n=64, stages=9),
