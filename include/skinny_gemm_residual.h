@@ -62,7 +62,11 @@
  *                       or a forced path/config that cannot run this shape
  *   SGR_ERR_LAUNCH      the CUDA launch itself failed (cudaGetLastError)
  *   SGR_ERR_DEVICE      no usable device, or device set-up failed
- * Empty problems (M == 0 or N == 0) return SGR_OK and enqueue nothing.
+ * Empty problems (M == 0 or N == 0) return SGR_OK and enqueue nothing.  This
+ * is deliberate, and a departure from the plain "M >= 1" contract: an empty
+ * batch (a mixture-of-experts expert to which no token was routed, the last
+ * empty slice of a split batch) is a valid request with nothing to compute,
+ * so it is a no-op rather than an error.  Negative sizes are errors.
  * K == 0 makes the product an empty sum, so Y = R (a device copy).
  * Device-side waits are bounded (about one second); a wait that runs out
  * records a code readable with sgr_device_error() instead of hanging.
@@ -180,7 +184,9 @@ int sgr_init(int device);
 /*
  * Read (and with clear != 0, reset) the device error word of `device`, which
  * a kernel sets when one of its bounded waits runs out (0 = no error).
- * Synchronises with the device.  Returns an sgr_status.
+ * Synchronises with the device.  Allocates no device memory and does not run
+ * sgr_init(), so callers of skinny_gemm_residual_noalloc can use it too.
+ * Returns an sgr_status.
  */
 int sgr_device_error(int device, unsigned* code, int clear);
 
@@ -201,8 +207,8 @@ int sgr_abi_version(void);
 
 /*
  * Allocation-free variant (no counterpart on the pages; added for callers
- * that must not allocate device memory).  Same operation, arguments, errors
- * and PDL contract as skinny_gemm_residual_ex, computed by the stream-K
+ * that must not allocate device memory).  Same operation, arguments and
+ * errors as skinny_gemm_residual_ex, computed by the stream-K
  * tensor-core kernel, with its split-K scratch taken from a fixed array
  * inside this library instead of the workspace that sgr_init() allocates.
  * Who needs it: code that runs while a stream is being captured in a mode
@@ -222,9 +228,14 @@ int sgr_abi_version(void);
  * The first call on a device resolves the array's device address (with that
  * device current) and sets kernel attributes; make that first call before
  * any stream capture.  Every call on a device shares the one array: it clears
- * the counters it uses before its kernel runs, and calls whose work may
- * overlap on the GPU (different streams, or graphs replayed concurrently)
- * race on the array and must be serialised by the caller.
+ * the counters it uses with a cudaMemsetAsync on `stream` before its kernel
+ * runs, and calls whose work may overlap on the GPU (different streams, or
+ * graphs replayed concurrently) race on the array and must be serialised by
+ * the caller.  Because of that memset, the kernel of this call does not
+ * start early under programmatic dependent launch: it runs after the
+ * preceding work on `stream` has finished (W may therefore be written by
+ * that work, unlike with skinny_gemm_residual_ex).  sgr_device_error() reads
+ * the error word without allocating.
  */
 int skinny_gemm_residual_noalloc(const void* A, int64_t lda, const void* W,
                                  const void* R, int64_t ldr, void* Y, int64_t ldy,
@@ -325,6 +336,23 @@ int sgr_validate_w8(const void* A, int64_t lda, const void* Wq, int64_t ldw,
  * and the context stays usable.  Returns an sgr_status.
  */
 int sgr_selftest_wait_timeout(unsigned limit_us, unsigned* code);
+
+/*
+ * Self-test of the stream-K kernel's abort path (SGR_PATH_TC): one launch on
+ * the current device and the legacy default stream with contiguous operands
+ * (as skinny_gemm_residual), in which CTA `cta` of the persistent grid acts
+ * as if its first wait for an accumulator had run out.  That CTA records
+ * code 3 in the device error word, stops its copy and MMA threads at their
+ * next wait, and still arrives on the split-K tile counters of its segments
+ * without contributing partial sums, so that every counter is back at zero
+ * when the kernel ends.  Y is unspecified afterwards.  The call clears the
+ * error word, launches, synchronises the device, writes the recorded code to
+ * *code and clears the word again.  Nothing faults or hangs.  Errors as for
+ * skinny_gemm_residual; SGR_ERR_UNSUPPORTED when `cta` is negative or not
+ * below the grid size.  Returns an sgr_status.
+ */
+int sgr_selftest_streamk_abort(const void* A, const void* W, const void* R, void* Y, int M, int N, int K,
+                               int cta, unsigned* code);
 
 #ifdef __cplusplus
 }

@@ -56,4 +56,5 @@ from .binding import (  # noqa: F401
     skinny_gemm_residual_w8_ptr,
     sgr_validate_w8_ptr,
     sgr_selftest_wait_timeout,
+    sgr_selftest_streamk_abort,
 )

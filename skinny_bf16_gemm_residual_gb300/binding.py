@@ -83,6 +83,7 @@ EXPORTS = (
     "skinny_gemm_residual_w8",
     "sgr_validate_w8",
     "sgr_selftest_wait_timeout",
+    "sgr_selftest_streamk_abort",
 )
 
 
@@ -125,6 +126,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                                                 ctypes.POINTER(sgr_config), U, vp]
         lib.sgr_validate_w8.argtypes = [vp, i64, vp, i64, fp, vp, i64, vp, i64, I, I, I]
         lib.sgr_selftest_wait_timeout.argtypes = [U, ctypes.POINTER(ctypes.c_uint)]
+        lib.sgr_selftest_streamk_abort.argtypes = [vp, vp, vp, vp, I, I, I, I, ctypes.POINTER(ctypes.c_uint)]
         for name in EXPORTS:
             if name != "sgr_status_string":
                 getattr(lib, name).restype = ctypes.c_int
@@ -325,6 +327,26 @@ def sgr_selftest_wait_timeout(limit_us: int = 1000) -> int:
     rc = load().sgr_selftest_wait_timeout(int(limit_us), ctypes.byref(code))
     if rc != SGR_OK:
         raise SgrError(rc, "sgr_selftest_wait_timeout")
+    return code.value
+
+
+def sgr_selftest_streamk_abort(A, W, R, Y, cta: int) -> int:
+    """One stream-K launch on the current device's default stream in which CTA
+    `cta` acts as if its first accumulator wait ran out; returns the code the
+    kernel recorded (3 expected).  Contiguous CUDA tensors; Y is overwritten
+    with unspecified values."""
+    import torch
+
+    for t in (A, W, R, Y):
+        if not (t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous()):
+            raise ValueError("sgr_selftest_streamk_abort takes contiguous CUDA bfloat16 tensors")
+    M, K = A.shape
+    N = W.shape[0]
+    code = ctypes.c_uint(0)
+    rc = load().sgr_selftest_streamk_abort(A.data_ptr(), W.data_ptr(), R.data_ptr(), Y.data_ptr(), M, N, K,
+                                           int(cta), ctypes.byref(code))
+    if rc != SGR_OK:
+        raise SgrError(rc, "sgr_selftest_streamk_abort")
     return code.value
 
 

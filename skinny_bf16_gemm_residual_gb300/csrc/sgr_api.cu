@@ -30,6 +30,38 @@ constexpr long long kMaxLd = 1LL << 36;
 
 __device__ unsigned g_sgr_error_word;
 
+// Device address of g_sgr_error_word per device, resolved once with that
+// device current.  Allocates nothing, so the allocation-free entry point and
+// the error query can use it without the workspace set-up of init_device.
+struct ErrorWord {
+  std::once_flag once;
+  int status = SGR_ERR_DEVICE;
+  unsigned* ptr = nullptr;
+};
+ErrorWord g_err_word[kMaxDevices];
+
+int error_word(int dev, unsigned** out) {
+  if (dev < 0 || dev >= kMaxDevices) return SGR_ERR_DEVICE;
+  ErrorWord& w = g_err_word[dev];
+  std::call_once(w.once, [&] {
+    int prev = -1;
+    if (cudaGetDevice(&prev) != cudaSuccess || (prev != dev && cudaSetDevice(dev) != cudaSuccess)) {
+      cudaGetLastError();
+      return;
+    }
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_sgr_error_word) == cudaSuccess) {
+      w.ptr = static_cast<unsigned*>(p);
+      w.status = SGR_OK;
+    } else {
+      cudaGetLastError();
+    }
+    if (prev != dev) cudaSetDevice(prev);
+  });
+  *out = w.ptr;
+  return w.status;
+}
+
 struct DeviceState {
   std::once_flag once;
   int status = SGR_ERR_DEVICE;
@@ -178,8 +210,8 @@ int init_device(int dev) {
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
       ok = SGR_ERR_DEVICE;
-    void* errp = nullptr;
-    if (ok == SGR_OK && cudaGetSymbolAddress(&errp, g_sgr_error_word) != cudaSuccess) ok = SGR_ERR_DEVICE;
+    unsigned* errp = nullptr;
+    if (ok == SGR_OK && error_word(dev, &errp) != SGR_OK) ok = SGR_ERR_DEVICE;
     if (ok == SGR_OK && cudaMemset(errp, 0, sizeof(unsigned)) != cudaSuccess) ok = SGR_ERR_DEVICE;
     const int mts[5] = {1, 2, 4, 8, 16};
     const int vpts[3] = {1, 2, 4};
@@ -197,7 +229,7 @@ int init_device(int dev) {
     if (ok == SGR_OK && sgr::w8_init_device() != cudaSuccess) ok = SGR_ERR_DEVICE;
     if (ok != SGR_OK) cudaGetLastError();
     st.sms = sms;
-    st.err = static_cast<unsigned*>(errp);
+    st.err = errp;
     st.status = ok;
     if (prev != dev) cudaSetDevice(prev);
   });
@@ -473,19 +505,19 @@ int noalloc_setup(int dev) {
     int ok = SGR_OK;
     int sms = 0;
     void* scratch = nullptr;
-    void* errp = nullptr;
+    unsigned* errp = nullptr;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
       ok = SGR_ERR_DEVICE;
     if (ok == SGR_OK && cudaGetSymbolAddress(&scratch, g_sgr_noalloc_scratch) != cudaSuccess)
       ok = SGR_ERR_DEVICE;
-    if (ok == SGR_OK && cudaGetSymbolAddress(&errp, g_sgr_error_word) != cudaSuccess) ok = SGR_ERR_DEVICE;
+    if (ok == SGR_OK && error_word(dev, &errp) != SGR_OK) ok = SGR_ERR_DEVICE;
     if (ok == SGR_OK &&
         sgr::set_kernel_smem_attrs(reinterpret_cast<const void*>(sgr::tc_skinny_kernel)) != cudaSuccess)
       ok = SGR_ERR_DEVICE;
     if (ok != SGR_OK) cudaGetLastError();
     st.sms = sms;
     st.scratch = static_cast<unsigned char*>(scratch);
-    st.err = static_cast<unsigned*>(errp);
+    st.err = errp;
     st.status = ok;
   });
   return st.status;
@@ -704,6 +736,46 @@ int run_selftest_wait(unsigned limit_us, unsigned* code) {
   return SGR_OK;
 }
 
+// ------------------------------------------------------------ stream-K abort self-test
+// One stream-K launch (the library's workspace, contiguous operands) in which
+// CTA `cta` acts as if its first accumulator wait had run out: it records
+// kErrWaitMma, raises its abort flag (its producer and MMA threads stop at
+// their next wait and drain) and arrives on the split-K counters of its
+// remaining segments without contributing a partial.  Exercises the abort
+// path of the kernel without faulting or hanging anything.
+int run_selftest_streamk_abort(const void* A, const void* W, const void* R, void* Y, int M, int N, int K, int cta,
+                               unsigned* code) {
+  if (!code) return SGR_ERR_NULL;
+  if (M < 1 || N < 1 || K < 1) return SGR_ERR_SHAPE;
+  int rc = validate(A, K, W, R, N, Y, N, M, N, K);
+  if (rc != SGR_OK) return rc;
+  if (cta < 0) return SGR_ERR_UNSUPPORTED;
+  int dev;
+  if ((rc = current_device(&dev)) != SGR_OK) return rc;
+  if ((rc = init_device(dev)) != SGR_OK) return rc;
+  DeviceState& st = g_dev[dev];
+  sgr_config in = {};
+  in.path = SGR_PATH_TC;
+  sgr_config c;
+  if ((rc = resolve_config(st.sms, M, N, K, &in, &c)) != SGR_OK) return rc;
+  unsigned zero = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess ||
+      cudaMemcpy(st.err, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) {
+    cudaGetLastError();
+    return SGR_ERR_DEVICE;
+  }
+  rc = sgr::tc_launch(c, st.sms, st.err, &st.ws, A, K, W, R, N, Y, N, M, N, K, false, nullptr, cta);
+  if (rc != SGR_OK) return rc;
+  unsigned v = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess || cudaMemcpy(&v, st.err, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemcpy(st.err, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) {
+    cudaGetLastError();
+    return SGR_ERR_DEVICE;
+  }
+  *code = v;
+  return SGR_OK;
+}
+
 // ------------------------------------------------------------ grouped launch
 int run_grouped(const sgr_group* groups, int num_groups, int N, int K, const sgr_config* cfg, unsigned flags,
                 void* stream_ptr) {
@@ -830,7 +902,8 @@ int sgr_init(int device) { return init_device(device); }
 
 int sgr_device_error(int device, unsigned* code, int clear) {
   if (!code) return SGR_ERR_NULL;
-  int rc = init_device(device);
+  unsigned* word = nullptr;
+  int rc = error_word(device, &word);  // no workspace set-up: allocates nothing
   if (rc != SGR_OK) return rc;
   int prev = -1;
   if (cudaGetDevice(&prev) != cudaSuccess || (prev != device && cudaSetDevice(device) != cudaSuccess)) {
@@ -838,8 +911,8 @@ int sgr_device_error(int device, unsigned* code, int clear) {
     return SGR_ERR_DEVICE;
   }
   unsigned v = 0;
-  cudaError_t e = cudaMemcpy(&v, g_dev[device].err, sizeof v, cudaMemcpyDeviceToHost);
-  if (e == cudaSuccess && clear) e = cudaMemset(g_dev[device].err, 0, sizeof v);
+  cudaError_t e = cudaMemcpy(&v, word, sizeof v, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && clear) e = cudaMemset(word, 0, sizeof v);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (prev != device) cudaSetDevice(prev);
   if (e != cudaSuccess) {
@@ -953,5 +1026,10 @@ int sgr_validate_w8(const void* A, int64_t lda, const void* Wq, int64_t ldw, con
 }
 
 int sgr_selftest_wait_timeout(unsigned limit_us, unsigned* code) { return run_selftest_wait(limit_us, code); }
+
+int sgr_selftest_streamk_abort(const void* A, const void* W, const void* R, void* Y, int M, int N, int K, int cta,
+                               unsigned* code) {
+  return run_selftest_streamk_abort(A, W, R, Y, M, N, K, cta, code);
+}
 
 }  // extern "C"

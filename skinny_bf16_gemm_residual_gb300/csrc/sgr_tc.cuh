@@ -19,6 +19,8 @@
 // others write FP32 partial tiles to a workspace and the last CTA to arrive
 // at the tile's counter sums every partial in K order (so results do not
 // depend on arrival order), adds R, rounds and stores, and resets the counter.
+// Every contributor arrives on the counter even after one of its waits ran
+// out, so the counters are zero again at the end of every call.
 // This replaces the vLLM page's one-CTA-per-outputs_per_block-rows grid,
 // which leaves most of 152 SMs idle or in a ragged last wave.
 //
@@ -72,6 +74,7 @@ struct TcParams {
   int stages;    // ring depth
   int chains;    // independent TMEM accumulators per buffer (1, 2 or 4)
   int tmem_cols;
+  int abort_cta;  // self-test only: this CTA's epilogue acts as if its first wait ran out (-1: none)
 };
 
 __host__ __device__ inline uint32_t tc_stage_bytes(int kbps, int nt) {
@@ -328,7 +331,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int n = n_tile * kTcTileRows + row;
       const int m_base = m_tile * p.NT;
       const int m_count = min(p.NT, p.M - m_base);
-      if (ok && !mbar_wait_or_abort(smem_u32(&acc_full[buf]), nuse[buf] & 1, abort_flag)) {
+      if (ok && (c == p.abort_cta || !mbar_wait_or_abort(smem_u32(&acc_full[buf]), nuse[buf] & 1, abort_flag))) {
         if (!*abort_flag) report_error(p.err, kErrWaitMma);
         *abort_flag = 1;
         ok = false;
@@ -380,14 +383,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int c_first = tc_cta_of(U, G, t_begin);
         const int c_last = tc_cta_of(U, G, t_end - 1);
         if (etid == 0) {
-          int last = 0;
-          if (ok) {
-            const unsigned prev = atomicAdd(&p.counters[t], 1u);
-            last = (prev == (unsigned)(c_last - c_first));
-            if (last) p.counters[t] = 0u;  // every contributor has arrived: reset for the next call
-            __threadfence();
-          }
-          *bcast = last;
+          // Every contributor arrives, also one whose wait ran out (the error
+          // word records that), so that the counter always returns to zero
+          // and the next call that uses it starts clean.  A contributor
+          // without its own partial (ok false) never runs the fixup.
+          const unsigned prev = atomicAdd(&p.counters[t], 1u);
+          const bool last = (prev == (unsigned)(c_last - c_first));
+          if (last) p.counters[t] = 0u;  // every contributor has arrived: reset for the next call
+          __threadfence();
+          *bcast = (last && ok) ? 1 : 0;
         }
         named_bar_sync(1, 128);
         if (*bcast && n < p.N) {
@@ -545,6 +549,7 @@ inline int tc_plan(const sgr_config& c, int sms, int M, int N, int K, TcParams* 
   p->units = units;
   p->chains = nt <= 64 ? 4 : (nt <= 128 ? 2 : 1);  // 2 buffers * chains * NT <= 512 TMEM columns
   p->tmem_cols = detail::pow2_at_least(2 * p->chains * nt);
+  p->abort_cta = -1;
   *grid = (int)g;
   *smem = sm;
   return SGR_OK;
@@ -552,12 +557,14 @@ inline int tc_plan(const sgr_config& c, int sms, int M, int N, int K, TcParams* 
 
 inline int tc_launch(const sgr_config& c, int sms, unsigned* err, TcWorkspace* ws, const void* A,
                      long long lda, const void* W, const void* R, long long ldr, void* Y, long long ldy,
-                     int M, int N, int K, bool pdl, cudaStream_t stream) {
+                     int M, int N, int K, bool pdl, cudaStream_t stream, int abort_cta = -1) {
   TcParams p;
   int grid = 0;
   size_t smem = 0;
   int rc = tc_plan(c, sms, M, N, K, &p, &grid, &smem);
   if (rc != SGR_OK) return rc;
+  if (abort_cta >= grid) return SGR_ERR_UNSUPPORTED;
+  p.abort_cta = abort_cta;
   if (!ws->partials || (size_t)grid * 2 * p.NT * kTcTileRows > ws->partial_floats) return SGR_ERR_UNSUPPORTED;
   CUtensorMap tmW, tmA;
   if (!detail::make_tmap(&tmW, W, N, K, K, kTcTileRows, kTcKBlock)) return SGR_ERR_LAUNCH;

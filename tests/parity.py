@@ -51,3 +51,21 @@ def compare(got_bits: np.ndarray, ref_bits: np.ndarray, what: str = "") -> dict:
 
 def oracle_full(A, W, R) -> np.ndarray:
     return oracle.load().gemm_residual(A, W, R)
+
+
+_ORACLE_CACHE: dict = {}
+
+
+def oracle_problem(M: int, N: int, K: int, seed: int, **kw):
+    """(problem, oracle result) for a seeded problem, memoised for the few
+    full-size problems that several tests check against every element (the
+    oracle takes about a second per thousand tokens at N = 7168, K = 3584)."""
+    from skinny_bf16_gemm_residual_gb300 import inputs
+
+    key = (M, N, K, seed, tuple(sorted(kw.items())))
+    if key not in _ORACLE_CACHE:
+        if len(_ORACLE_CACHE) >= 4:
+            _ORACLE_CACHE.pop(next(iter(_ORACLE_CACHE)))
+        p = inputs.make_problem(M, N, K, seed=seed, **kw)
+        _ORACLE_CACHE[key] = (p, oracle_full(p.A, p.W, p.R))
+    return _ORACLE_CACHE[key]

@@ -191,6 +191,38 @@ def check_brute_force_exact(orc):
             f"brute force {M}x{N}x{K}")
 
 
+def check_unrounded_sum_vs_exact(orc):
+    """The oracle's unrounded FP64 value of A . W^T + R against exact rationals.
+    FP64 summation of K + 1 terms in order is within (K + 1) * 2^-53 of the
+    sum of magnitudes (each product of two BF16 values is exact in FP64), far
+    inside half a BF16 ulp, so a value that was already rounded to BF16, or
+    one that drops or mis-signs a term, falls outside the bound.  With integer
+    operands every step is exact and the values must be equal."""
+    for (M, N, K, seed) in ((4, 8, 16, 61), (3, 5, 33, 62), (2, 7, 64, 63)):
+        A = bits(inputs.random_bf16_bits((M, K), seed))
+        W = bits(inputs.random_bf16_bits((N, K), seed + 100))
+        R = bits(inputs.random_bf16_bits((M, N), seed + 200))
+        t = orc.gemm_residual_f64(A, W, R, threads=2)
+        a = [[bf16_value(int(v)) for v in row] for row in A]
+        w = [[bf16_value(int(v)) for v in row] for row in W]
+        far = 0
+        for m in range(M):
+            for n in range(N):
+                terms = [a[m][k] * w[n][k] for k in range(K)] + [bf16_value(int(R[m, n]))]
+                exact = sum(terms, Fraction(0))
+                bound = Fraction(K + 1, 2 ** 53) * sum((abs(x) for x in terms), Fraction(0))
+                assert abs(Fraction(float(t[m, n])) - exact) <= bound, \
+                    f"unrounded sum {M}x{N}x{K} at ({m},{n}): {t[m, n]!r} vs {float(exact)!r}"
+                far += abs(exact - bf16_value(rne_bf16_exact(exact))) > bound
+        assert far > 0, "no element of the case separates rounded from unrounded values"
+    Ai = inputs.integer_bf16((5, 24), -3, 3, 64)
+    Wi = inputs.integer_bf16((6, 24), -3, 3, 65)
+    Ri = inputs.integer_bf16((5, 6), -8, 8, 66)
+    want = (Ai.to(torch.int64) @ Wi.to(torch.int64).T + Ri.to(torch.int64)).numpy().astype(np.float64)
+    t = orc.gemm_residual_f64(bits(Ai), bits(Wi), bits(Ri))
+    assert np.array_equal(t, want), "unrounded sum of integer operands is not exact"
+
+
 def check_identity_weight(orc):
     """N = K and W = I: Y = bf16(A + R), a single library rounding."""
     K = 24
@@ -447,6 +479,7 @@ ALL_CHECKS = [
     check_rounding_vs_exact_bisection,
     check_crafted_fixture,
     check_brute_force_exact,
+    check_unrounded_sum_vs_exact,
     check_identity_weight,
     check_one_hot_activation,
     check_zero_operands,

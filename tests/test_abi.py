@@ -147,7 +147,13 @@ def test_validate_largest_stride():
 
 def test_validate_in_place_and_empty():
     assert v(Y=R_) == sgr.SGR_OK                       # Y == R exactly: in-place residual
+    # M = 0 is a deliberate no-op (an expert with no tokens), not an error;
+    # negative sizes are errors.
     assert v(M=0, A=0, W=0, R=0, Y=0) == sgr.SGR_OK    # empty problem
+    assert v(M=-1) == sgr.SGR_ERR_SHAPE
+    lib = sgr.load()
+    assert lib.skinny_gemm_residual(None, None, None, None, 0, 7168, 3584, None) == sgr.SGR_OK
+    assert lib.skinny_gemm_residual(None, None, None, None, -1, 7168, 3584, None) == sgr.SGR_ERR_SHAPE
     assert v(N=0, A=0, W=0, R=0, Y=0) == sgr.SGR_OK
     assert v(K=0, A=0, W=0) == sgr.SGR_OK              # empty sum: Y = R
 

@@ -8,7 +8,7 @@ import torch
 
 import skinny_bf16_gemm_residual_gb300 as sgr
 from skinny_bf16_gemm_residual_gb300 import inputs
-from parity import bits, compare, oracle_full
+from parity import bits, compare, oracle_full, oracle_problem
 
 pytestmark = pytest.mark.gpu
 
@@ -74,15 +74,28 @@ def test_parity_down_projection_every_element(M):
 
 
 @pytest.mark.parametrize("M", [256, 512, 1024])
-def test_parity_down_projection_sampled(M):
-    import oracle
-
+def test_parity_down_projection_every_element_large_m(M):
     p = inputs.make_problem(M, N_DOWN, K_DOWN, seed=500 + M)
-    got = run_gpu(p)
-    rng = np.random.default_rng(M)
-    ms = np.concatenate([rng.integers(0, M, 5000), np.zeros(N_DOWN, int), np.full(N_DOWN, M - 1)])
-    ns = np.concatenate([rng.integers(0, N_DOWN, 5000), np.arange(N_DOWN), np.arange(N_DOWN)])
-    compare(got[ms, ns], oracle.load().sample(p.A, p.W, p.R, ms, ns), f"down M={M} sampled")
+    m = compare(run_gpu(p), oracle_full(p.A, p.W, p.R), f"down M={M}")
+    assert m["cosine"] > 0.999
+
+
+@pytest.mark.parametrize("M", [256, 512, 1024])
+def test_parity_compute_bound_sweep_every_element(M):
+    """The compute-bound sweep at the latent-MoE shape through the library's
+    own choice of kernel: every output element."""
+    p, ref = oracle_problem(M, N_FULL, K_FULL, seed=M)
+    m = compare(run_gpu(p), ref, f"M={M}")
+    assert m["cosine"] > 0.999
+
+
+@pytest.mark.parametrize("M", [32, 64, 128])
+def test_parity_transition_sweep_every_element(M):
+    """The transition sweep at the latent-MoE shape through the library's own
+    choice of kernel: every output element."""
+    p, ref = oracle_problem(M, N_FULL, K_FULL, seed=M + 1)
+    m = compare(run_gpu(p), ref, f"M={M}")
+    assert m["cosine"] > 0.999
 
 
 @pytest.mark.parametrize("kb,stages", [(4, 4), (8, 3), (8, 2), (2, 6)])

@@ -7,7 +7,7 @@ import torch
 
 import skinny_bf16_gemm_residual_gb300 as sgr
 from skinny_bf16_gemm_residual_gb300 import inputs
-from parity import bits, compare, oracle_full
+from parity import bits, compare, oracle_full, oracle_problem
 
 import oracle
 
@@ -111,16 +111,10 @@ def test_rows_rejects_bad_config():
 
 
 @pytest.mark.parametrize("M", [256, 512, 1024])
-def test_tc_full_size_compute_bound_sampled(M):
-    """Every output row of a strided subset of columns is checked (the oracle
-    computes sampled elements one by one), plus full rows 0 and M-1."""
-    p = inputs.make_problem(M, N_FULL, K_FULL, seed=M)
-    got = run_tc(p)
-    rng = np.random.default_rng(M)
-    ms = np.concatenate([rng.integers(0, M, 4000), np.zeros(N_FULL, int), np.full(N_FULL, M - 1)])
-    ns = np.concatenate([rng.integers(0, N_FULL, 4000), np.arange(N_FULL), np.arange(N_FULL)])
-    ref = oracle.load().sample(p.A, p.W, p.R, ms, ns)
-    compare(got[ms, ns], ref, f"tc M={M} sampled")
+def test_tc_full_size_compute_bound_every_element(M):
+    """The stream-K kernel on the compute-bound sweep: every output element."""
+    p, ref = oracle_problem(M, N_FULL, K_FULL, seed=M)
+    compare(run_tc(p), ref, f"tc M={M}")
 
 
 TC_CONFIGS = [
