@@ -10,9 +10,16 @@ A, R ~ N(0,1), W ~ N(0,1)/sqrt(K), BF16, seeded.
 
 Prints ONE JSON line (rank 0).  `value` is achieved HBM GB/s over the whole
 step: algorithmic bytes 2*(N*K + M*K + 2*M*N) per call, summed over the
-step's calls, divided by the device time per step (CUDA events).
+step's calls, divided by the device time per step (CUDA events).  The timed
+region of K steps is repeated until the repeats span about two seconds (so
+that the clock sampler sees the load); `value` and `ms_per_step` come from
+the median repeat, `headline` holds the spread.
 Per-M microseconds per call (median of repeats, the page's summary) are in
-`per_m`.
+`per_m`, with the cuBLAS `torch.addmm` comparator timed the same way beside
+each M.  `transition` times every kernel path at M = 32, 64, 128 and
+`compute_bound` the library's choice at M = 256, 512, 1024 against the BF16
+tensor peak, both with the same comparator (the page's `addmm` backend and
+`graph_samples` method).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -42,6 +49,9 @@ N_DIM, K_DIM = 7168, 3584
 M_LIST = (1, 2, 4, 8, 16)
 COPIES = 4
 PATH_NAMES = {1: "simt", 2: "tc", 3: "rows", 4: "tile"}
+PATH_IDS = {v: k for k, v in PATH_NAMES.items()}
+TRANSITION_M = (32, 64, 128)
+COMPUTE_M = (256, 512, 1024)
 KERNEL_NAMES = {"simt": "simt_skinny_kernel", "tc": "tc_skinny_kernel", "rows": "rows_skinny_kernel",
                 "tile": "tile_gemm_kernel"}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -300,6 +310,85 @@ def time_graph(g, stream, replays: int, repeats: int):
     return out
 
 
+def time_calls(calls, stream, replays: int, repeats: int, warm: int = 20) -> dict:
+    """One CUDA graph of `calls` (eager warm-up first), `warm` untimed replays,
+    then `repeats` x `replays` between CUDA events; summary per call."""
+    import torch
+
+    g = capture(calls, stream)
+    with torch.cuda.stream(stream):
+        for _ in range(warm):
+            g.replay()
+    stream.synchronize()
+    s = summarize([t / len(calls) for t in time_graph(g, stream, replays, repeats)])
+    del g
+    return s
+
+
+def call_metrics(M: int, s: dict, peaks: dict) -> dict:
+    """Per-call figures of one timing summary: GB/s and TFLOP/s of the
+    algorithmic bytes and FLOPs, their fractions of the measured peaks (the
+    burst tensor peak for a kernel timed on its own, the sustained one beside
+    it), and the fraction of the roofline time max(bytes / HBM peak,
+    FLOPs / tensor peak)."""
+    us = s["median_us"]
+    gbs = alg_bytes(M) / (us * 1e-6) / 1e9
+    tflops = alg_flops(M) / (us * 1e-6) / 1e12
+    roof_us = max(alg_bytes(M) / (peaks["hbm_gbs"] * 1e9), alg_flops(M) / (peaks["bf16_tflops"] * 1e12)) * 1e6
+    return {"us_per_call": us, "p10_us": s["p10_us"], "p90_us": s["p90_us"], "cv_pct": s["cv_pct"],
+            "gbs": gbs, "frac_of_hbm_peak": gbs / peaks["hbm_gbs"],
+            "tflops": tflops, "frac_of_tensor_peak": tflops / peaks["bf16_tflops"],
+            "frac_of_tensor_peak_sustained": tflops / peaks["bf16_tflops_sustained"],
+            "roofline_us": roof_us, "frac_of_roofline": roof_us / us,
+            "bound": "tensor" if tensor_bound(M, peaks) else "hbm"}
+
+
+def addmm_calls(A, Ws, Rs, Ys, stream):
+    """The cuBLAS comparator of the vLLM benchmark page (its `addmm` backend):
+    Y = R + A . W^T by torch.addmm into the output buffer, one call per copy."""
+    import torch
+
+    def one(c):
+        def f():
+            with torch.cuda.stream(stream):
+                torch.addmm(Rs[c], A, Ws[c].t(), out=Ys[c])
+        return f
+    return [one(c) for c in range(len(Ws))]
+
+
+def run_sweep(sgr, Ws, device, stream, peaks: dict, m_list, paths, replays: int, repeats: int) -> dict:
+    """Every kernel path in `paths` (plus the library's automatic choice and
+    cuBLAS addmm) at each M, each as one CUDA graph of one call per rotating W
+    copy, PDL on.  A path that cannot run the shape is recorded as such."""
+    import torch
+
+    from skinny_bf16_gemm_residual_gb300 import inputs
+
+    out = {}
+    for M in m_list:
+        A = inputs.make_rows(M, K_DIM, seed=10_000 + M).to(device)
+        Rs = [inputs.make_rows(M, N_DIM, seed=20_000 + 100 * M + c).to(device) for c in range(COPIES)]
+        Ys = [torch.empty((M, N_DIM), dtype=torch.bfloat16, device=device) for _ in range(COPIES)]
+        auto = PATH_NAMES.get(sgr.sgr_select_path(M, N_DIM, K_DIM), "?")
+        entry = {"library_choice": auto, "paths": {}}
+        for name in list(paths) + ["auto"]:
+            cfg = None if name == "auto" else sgr.make_config(path=PATH_IDS[name])
+            calls = [lambda c=c, cfg=cfg: sgr.skinny_gemm_residual_ex(A, Ws[c], Rs[c], Ys[c], config=cfg,
+                                                                      stream=stream) for c in range(COPIES)]
+            try:
+                calls[0]()
+                stream.synchronize()
+            except sgr.SgrError as e:
+                entry["paths"][name] = {"unsupported": str(e)}
+                continue
+            entry["paths"][name] = call_metrics(M, time_calls(calls, stream, replays, repeats), peaks)
+        entry["paths"]["cublas_addmm"] = call_metrics(
+            M, time_calls(addmm_calls(A, Ws, Rs, Ys, stream), stream, replays, repeats), peaks)
+        out[str(M)] = entry
+        del A, Rs, Ys
+    return out
+
+
 # ------------------------------------------------------------------ CPU arms
 ARM_CORES = {("0x41", "0xd4f"): "Arm Neoverse V2", ("0x41", "0xd40"): "Arm Neoverse V1",
              ("0x41", "0xd49"): "Arm Neoverse N2", ("0x41", "0xd0c"): "Arm Neoverse N1"}
@@ -443,52 +532,70 @@ def run_ours(args):
     bytes_per_step = sum(alg_bytes(M) for M in m_list for _ in range(COPIES))
     g_step = capture(step_calls, stream)
 
-    # per-M microseconds per call: one graph of the 4 copies, repeats x replays
+    # per-M microseconds per call: one graph of the 4 copies, repeats x replays;
+    # the cuBLAS addmm comparator the same way; the first M measured again
+    # after the others (a measurement-order check)
     per_m_out = {}
     peaks, peak_src = load_peaks()
     for M in (() if args.skip_per_m else m_list):
-        g = capture([call(M, c) for c in range(COPIES)], stream)
-        with torch.cuda.stream(stream):
-            for _ in range(20):
-                g.replay()
-        stream.synchronize()
-        samples = [t / COPIES for t in time_graph(g, stream, args.replays, args.repeats)]
-        s = summarize(samples)
-        gbs = alg_bytes(M) / (s["median_us"] * 1e-6) / 1e9
-        tflops = alg_flops(M) / (s["median_us"] * 1e-6) / 1e12
-        per_m_out[str(M)] = {
-            "us_per_call": s["median_us"], "p10_us": s["p10_us"], "p90_us": s["p90_us"],
-            "cv_pct": s["cv_pct"], "gbs": gbs, "frac_of_hbm_peak": gbs / peaks["hbm_gbs"],
-            "tflops": tflops, "frac_of_tensor_peak": tflops / peaks["bf16_tflops"],
-            "bound": "tensor" if tensor_bound(M, peaks) else "hbm",
-            "path": PATH_NAMES.get(sgr.sgr_select_path(M, N_DIM, K_DIM), "?"),
-        }
-        del g
+        s = time_calls([call(M, c) for c in range(COPIES)], stream, args.replays, args.repeats)
+        per_m_out[str(M)] = {**call_metrics(M, s, peaks),
+                             "path": PATH_NAMES.get(sgr.sgr_select_path(M, N_DIM, K_DIM), "?")}
+        if not args.skip_cublas:
+            d = per_m[M]
+            sc = time_calls(addmm_calls(d["A"], Ws, d["R"], d["Y"], stream), stream, args.replays, args.repeats)
+            per_m_out[str(M)]["cublas_addmm"] = call_metrics(M, sc, peaks)
+    if per_m_out and len(m_list) > 1:
+        M = m_list[0]
+        s = time_calls([call(M, c) for c in range(COPIES)], stream, args.replays, args.repeats)
+        per_m_out[str(M)]["measured_again_last"] = call_metrics(M, s, peaks)
 
-    # headline: K timed steps of the whole M sweep
+    # headline: K timed steps of the whole M sweep, the K-step region repeated
+    # (each repeat bracketed by a barrier and a device synchronise, timed with
+    # CUDA events on the launch stream) until the repeats span about
+    # args.headline_seconds, so that the clock sampler sees the load
     clocks = ClockSampler(device.index)
     clocks.start()
     with torch.cuda.stream(stream):  # replay() launches on the current stream
         for _ in range(args.warmup):
             g_step.replay()
     stream.synchronize()
-    dist_barrier(ws)
-    torch.cuda.synchronize()
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        ev0.record(stream)
-        for _ in range(args.steps):
-            g_step.replay()
-        ev1.record(stream)
-    ev1.synchronize()
-    torch.cuda.synchronize()
-    dist_barrier(ws)
+
+    def timed_region():
+        dist_barrier(ws)
+        torch.cuda.synchronize()
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for _ in range(args.steps):
+                g_step.replay()
+            ev1.record(stream)
+        ev1.synchronize()
+        torch.cuda.synchronize()
+        dist_barrier(ws)
+        return ev0.elapsed_time(ev1)
+
+    first_ms = timed_region()
+    repeats = max(args.min_headline_repeats, math.ceil(args.headline_seconds * 1e3 / max(first_ms, 1e-3)))
+    repeats = int(dist_max(float(repeats), ws, device))  # every rank runs the same count
+    region_ms = [first_ms] + [timed_region() for _ in range(repeats - 1)]
     clk = clocks.stop()
-    elapsed_ms = ev0.elapsed_time(ev1)
-    elapsed_ms = dist_max(elapsed_ms, ws, device)
+    if ws > 1:
+        t = torch.tensor(region_ms, dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        region_ms = t.tolist()  # per repeat, the slowest rank
+    rs = summarize(region_ms)  # milliseconds here, despite the key names
+    elapsed_ms = rs["median_us"]
     ms_per_step = elapsed_ms / args.steps
     value = job_gbs(bytes_per_step, ws, args.steps, elapsed_ms)
+    headline = {"repeats": repeats, "steps_per_repeat": args.steps,
+                "ms_per_repeat": {"median": rs["median_us"], "p10": rs["p10_us"], "p90": rs["p90_us"],
+                                  "cv_pct": rs["cv_pct"]},
+                "gbs_p10_time": job_gbs(bytes_per_step, ws, args.steps, rs["p10_us"]),
+                "gbs_p90_time": job_gbs(bytes_per_step, ws, args.steps, rs["p90_us"]),
+                "seconds_timed": sum(region_ms) / 1e3,
+                "note": "value and ms_per_step from the median repeat of the K-step region"}
 
     # end to end through the public call with host buffers (pinned), W resident
     e2e_out = None
@@ -501,6 +608,10 @@ def run_ours(args):
                    "note": "host wall clock; every step copies its inputs in and its outputs out (pinned); "
                            "steps pipelined over two buffer sets and separate copy streams"}
 
+    transition = None if (args.skip_sweeps or rank != 0) else run_sweep(
+        sgr, Ws, device, stream, peaks, TRANSITION_M, ("rows", "tc", "tile"), args.sweep_replays, args.repeats)
+    compute_bound = None if (args.skip_sweeps or rank != 0) else run_sweep(
+        sgr, Ws, device, stream, peaks, COMPUTE_M, (), args.sweep_replays, args.repeats)
     chain = None if (args.skip_chain or rank != 0) else run_chain(sgr, device, stream)
     grouped = None if (args.skip_grouped or rank != 0) else run_grouped(sgr, device, stream)
     w8 = None if (args.skip_w8 or rank != 0) else run_w8(sgr, device, stream, peaks)
@@ -508,7 +619,7 @@ def run_ours(args):
     if rank != 0:
         return 0
 
-    avg_launch_s = elapsed_ms * 1e-3 / (args.steps * launches_per_step)
+    avg_launch_s = elapsed_ms * 1e-3 / (args.steps * launches_per_step)  # median repeat
     achieved = bytes_per_step / launches_per_step / avg_launch_s / 1e9
     # dominant kernel: the path with the largest share of the step's time
     share = {}
@@ -554,16 +665,20 @@ def run_ours(args):
             f"{w_total / 1e6:.0f} MB vs L2 {l2 / 1e6:.0f} MB); no flush",
             "launch": "one CUDA graph per step, PDL on", "parallelism": "replicas" if ws > 1 else "single GPU",
         },
+        "headline": headline,
         "per_m": per_m_out,
+        "transition": transition,
+        "compute_bound": compute_bound,
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e_out,
         "chain": chain,
         "grouped": grouped,
         "w8": w8,
-        "gpu_launches": args.steps * launches_per_step,
+        "gpu_launches": repeats * args.steps * launches_per_step,
         "clocks": clk,
-        "peaks": {"hbm_gbs": peaks["hbm_gbs"], "source": peak_src},
+        "peaks": {"hbm_gbs": peaks["hbm_gbs"], "bf16_tflops": peaks["bf16_tflops"],
+                  "bf16_tflops_sustained": peaks["bf16_tflops_sustained"], "source": peak_src},
     }
     print(json.dumps(line), flush=True)
     if ws > 1:
@@ -783,6 +898,13 @@ def main(argv=None):
     ap.add_argument("--skip-chain", action="store_true", help="skip the 8-layer dependent chain leg")
     ap.add_argument("--skip-grouped", action="store_true", help="skip the mixture-of-experts grouped leg")
     ap.add_argument("--skip-w8", action="store_true", help="skip the FP8-weight leg")
+    ap.add_argument("--skip-sweeps", action="store_true",
+                    help="skip the transition (M = 32-128) and compute-bound (M = 256-1024) legs")
+    ap.add_argument("--skip-cublas", action="store_true", help="skip the cuBLAS addmm rows of the per-M leg")
+    ap.add_argument("--sweep-replays", type=int, default=100, help="replays per repeat in the M = 32-1024 legs")
+    ap.add_argument("--headline-seconds", type=float, default=2.0,
+                    help="repeat the K-step timed region until the repeats span about this long")
+    ap.add_argument("--min-headline-repeats", type=int, default=5)
     ap.add_argument("--n", type=int, default=7168, help="output features (the headline shape is 7168)")
     ap.add_argument("--k", type=int, default=3584, help="input features (the headline shape is 3584)")
     args = ap.parse_args(argv)
