@@ -48,12 +48,12 @@ METRIC = "µs/call and achieved HBM GB/s, BF16 skinny GEMM+residual, M=1..16, N7
 N_DIM, K_DIM = 7168, 3584
 M_LIST = (1, 2, 4, 8, 16)
 COPIES = 4
-PATH_NAMES = {1: "simt", 2: "tc", 3: "rows", 4: "tile"}
+PATH_NAMES = {1: "simt", 2: "tc", 3: "rows", 4: "tile", 6: "pair"}
 PATH_IDS = {v: k for k, v in PATH_NAMES.items()}
 TRANSITION_M = (32, 64, 128)
 COMPUTE_M = (256, 512, 1024)
 KERNEL_NAMES = {"simt": "simt_skinny_kernel", "tc": "tc_skinny_kernel", "rows": "rows_skinny_kernel",
-                "tile": "tile_gemm_kernel"}
+                "tile": "tile_gemm_kernel", "pair": "pair_gemm_kernel"}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -107,6 +107,7 @@ KERNEL_SOURCES = {
     "rows_skinny_kernel": ("sgr_rows.cuh", "sgr_tc.cuh", "sgr_ptx.cuh"),
     "tc_skinny_kernel": ("sgr_tc.cuh", "sgr_ptx.cuh"),
     "tile_gemm_kernel": ("sgr_gemm.cuh", "sgr_tc.cuh", "sgr_ptx.cuh"),
+    "pair_gemm_kernel": ("sgr_pair.cuh", "sgr_gemm.cuh", "sgr_tc.cuh", "sgr_ptx.cuh"),
     "w8_rows_kernel": ("sgr_w8.cuh", "sgr_tc.cuh", "sgr_ptx.cuh"),
 }
 
@@ -609,9 +610,9 @@ def run_ours(args):
                            "steps pipelined over two buffer sets and separate copy streams"}
 
     transition = None if (args.skip_sweeps or rank != 0) else run_sweep(
-        sgr, Ws, device, stream, peaks, TRANSITION_M, ("rows", "tc", "tile"), args.sweep_replays, args.repeats)
+        sgr, Ws, device, stream, peaks, TRANSITION_M, ("rows", "tc", "tile", "pair"), args.sweep_replays, args.repeats)
     compute_bound = None if (args.skip_sweeps or rank != 0) else run_sweep(
-        sgr, Ws, device, stream, peaks, COMPUTE_M, (), args.sweep_replays, args.repeats)
+        sgr, Ws, device, stream, peaks, COMPUTE_M, ("tile", "pair"), args.sweep_replays, args.repeats)
     chain = None if (args.skip_chain or rank != 0) else run_chain(sgr, device, stream)
     grouped = None if (args.skip_grouped or rank != 0) else run_grouped(sgr, device, stream)
     w8 = None if (args.skip_w8 or rank != 0) else run_w8(sgr, device, stream, peaks)

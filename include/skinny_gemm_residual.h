@@ -80,7 +80,7 @@
 extern "C" {
 #endif
 
-#define SGR_ABI_VERSION 7
+#define SGR_ABI_VERSION 8
 
 typedef enum {
   SGR_OK = 0,
@@ -104,6 +104,7 @@ typedef enum {
 #define SGR_PATH_TILE 4    /* tcgen05 kernel, 128-token x tile_n output tiles (large M) */
 #define SGR_PATH_W8 5      /* tcgen05 row-slab kernel for FP8 weights (skinny_gemm_residual_w8 only, M <= 256);
                               skinny_gemm_residual_w8 also takes SGR_PATH_SIMT (CUDA-core kernel, M <= 8) */
+#define SGR_PATH_PAIR 6    /* tcgen05 tile kernel on 2-CTA clusters (cta_group::2), 256-token x tile_n tiles (large M) */
 
 /*
  * Y = bf16(A . W^T + R) with contiguous operands (lda = K, ldr = ldy = N).
@@ -135,10 +136,11 @@ typedef struct {
   int ctas_per_sm;        /* persistent grid = SM count x ctas_per_sm */
   int stages;             /* shared-memory ring depth */
   int rows_per_stage;     /* SIMT: W rows per ring stage */
-  int k_blocks_per_stage; /* TC, TC_ROWS: 64-wide K blocks per ring stage */
+  int k_blocks_per_stage; /* TC, TC_ROWS, TILE, PAIR: 64-wide K blocks per ring stage */
   int token_tile;         /* TC, TC_ROWS: activation rows per MMA (multiple of 16, <= 256) */
-  int prefetch_stages;    /* TC_ROWS, TILE: weight stages requested before the dependency wait */
-  int tile_n;             /* TILE: W rows per output tile (MMA N): 64, 128, 192 or 256 */
+  int prefetch_stages;    /* TC_ROWS, TILE, PAIR: weight stages requested before the dependency wait */
+  int tile_n;             /* TILE: W rows per output tile (MMA N): 64, 128, 192 or 256;
+                             PAIR: W rows per 256-token tile: 64, 96, 128, 192 or 256 */
   int k_split;            /* TILE: 1, or 2 = K split over a 2-CTA cluster (one tile per cluster; tile_n <= 192) */
   int reserved[2];        /* must be zero */
 } sgr_config;
@@ -162,7 +164,7 @@ int sgr_validate(const void* A, int64_t lda, const void* W, const void* R,
 
 /*
  * Kernel path the library chooses for this shape with SGR_PATH_AUTO
- * (SGR_PATH_SIMT, SGR_PATH_TC, SGR_PATH_TC_ROWS or SGR_PATH_TILE), or a negative sgr_status
+ * (SGR_PATH_SIMT, SGR_PATH_TC, SGR_PATH_TC_ROWS, SGR_PATH_TILE or SGR_PATH_PAIR), or a negative sgr_status
  * if none can run it.  Host-only.
  */
 int sgr_select_path(int M, int N, int K);

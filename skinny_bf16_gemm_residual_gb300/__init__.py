@@ -29,6 +29,7 @@ from .binding import (  # noqa: F401
     SGR_PATH_TC_ROWS,
     SGR_PATH_TILE,
     SGR_PATH_W8,
+    SGR_PATH_PAIR,
     SgrError,
     load,
     make_config,

@@ -14,7 +14,7 @@ import threading
 
 from . import build as _build
 
-ABI_VERSION = 7  # must equal SGR_ABI_VERSION of the loaded library
+ABI_VERSION = 8  # must equal SGR_ABI_VERSION of the loaded library
 
 SGR_OK = 0
 SGR_ERR_NULL = 1
@@ -33,6 +33,7 @@ SGR_PATH_TC = 2
 SGR_PATH_TC_ROWS = 3
 SGR_PATH_TILE = 4
 SGR_PATH_W8 = 5
+SGR_PATH_PAIR = 6
 
 
 class sgr_group(ctypes.Structure):

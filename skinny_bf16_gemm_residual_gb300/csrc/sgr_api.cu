@@ -14,6 +14,7 @@
 #include "sgr_tc.cuh"
 #include "sgr_rows.cuh"
 #include "sgr_gemm.cuh"
+#include "sgr_pair.cuh"
 #include "sgr_w8.cuh"
 #include "sgr_table.h"
 
@@ -226,6 +227,7 @@ int init_device(int dev) {
     if (ok == SGR_OK && sgr::tc_init_device(sms, &st.ws) != cudaSuccess) ok = SGR_ERR_DEVICE;
     if (ok == SGR_OK && sgr::rows_init_device() != cudaSuccess) ok = SGR_ERR_DEVICE;
     if (ok == SGR_OK && sgr::tile_init_device() != cudaSuccess) ok = SGR_ERR_DEVICE;
+    if (ok == SGR_OK && sgr::pair_init_device(dev) != cudaSuccess) ok = SGR_ERR_DEVICE;
     if (ok == SGR_OK && sgr::w8_init_device() != cudaSuccess) ok = SGR_ERR_DEVICE;
     if (ok != SGR_OK) cudaGetLastError();
     st.sms = sms;
@@ -255,6 +257,7 @@ int select_path(int M, int N, int K, int sms) {
     if (e->path == SGR_PATH_TC_ROWS && sgr::rows_supported(sms, M, N, K)) return SGR_PATH_TC_ROWS;
     if (e->path == SGR_PATH_TC && sgr::tc_supported(M, N, K)) return SGR_PATH_TC;
     if (e->path == SGR_PATH_TILE && sgr::tile_supported(M, N, K)) return SGR_PATH_TILE;
+    if (e->path == SGR_PATH_PAIR && sgr::pair_supported(M, N, K) && sms >= 2) return SGR_PATH_PAIR;
   }
   if (M <= 64 && sgr::rows_supported(sms, M, N, K)) return SGR_PATH_TC_ROWS;
   if (M <= 2 && simt_vpt(K) > 0) return SGR_PATH_SIMT;
@@ -279,6 +282,17 @@ void default_simt_config(int sms, int M, int K, sgr_config* c) {
   c->token_tile = 0;
 }
 
+// 2-CTA clusters available to the pair kernel on the current device (SMs / 2
+// when no device is current or none was queried).
+int pair_pairs(int dev_sms) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    dev = -1;
+  }
+  return sgr::pair_grid_pairs(dev_sms > 0 ? dev_sms : 2, dev);
+}
+
 int resolve_config(int dev_sms, int M, int N, int K, const sgr_config* in, sgr_config* out) {
   std::memset(out, 0, sizeof *out);
   int path = in ? in->path : SGR_PATH_AUTO;
@@ -299,6 +313,9 @@ int resolve_config(int dev_sms, int M, int N, int K, const sgr_config* in, sgr_c
   } else if (path == SGR_PATH_TILE) {
     if (!sgr::tile_supported(M, N, K)) return SGR_ERR_UNSUPPORTED;
     sgr::tile_default_config(dev_sms > 0 ? dev_sms : 1, M, N, K, out);
+  } else if (path == SGR_PATH_PAIR) {
+    if (!sgr::pair_supported(M, N, K)) return SGR_ERR_UNSUPPORTED;
+    sgr::pair_default_config(pair_pairs(dev_sms), M, N, K, out);
   } else {
     return SGR_ERR_UNSUPPORTED;
   }
@@ -308,10 +325,11 @@ int resolve_config(int dev_sms, int M, int N, int K, const sgr_config* in, sgr_c
       out->ctas_per_sm = e->ctas_per_sm;
       out->stages = e->stages;
       if (path == SGR_PATH_SIMT || path == SGR_PATH_TC_ROWS) out->rows_per_stage = e->rows_per_stage;
-      if (path != SGR_PATH_SIMT && (path != SGR_PATH_TILE || e->k_blocks_per_stage > 0))
+      const bool tiled = path == SGR_PATH_TILE || path == SGR_PATH_PAIR;
+      if (path != SGR_PATH_SIMT && (!tiled || e->k_blocks_per_stage > 0))
         out->k_blocks_per_stage = e->k_blocks_per_stage;
-      if (path == SGR_PATH_TC_ROWS || path == SGR_PATH_TILE) out->prefetch_stages = e->prefetch_stages;
-      if (path == SGR_PATH_TILE && e->tile_n) out->tile_n = e->tile_n;
+      if (path == SGR_PATH_TC_ROWS || tiled) out->prefetch_stages = e->prefetch_stages;
+      if (tiled && e->tile_n) out->tile_n = e->tile_n;
       if (path == SGR_PATH_TILE) out->k_split = e->k_split > 0 ? e->k_split : 1;
     }
   }
@@ -331,6 +349,8 @@ int resolve_config(int dev_sms, int M, int N, int K, const sgr_config* in, sgr_c
     // A tile width chosen without a ring depth gets the deepest ring that fits it.
     if (path == SGR_PATH_TILE && (in->tile_n || in->k_blocks_per_stage) && !in->stages)
       out->stages = sgr::tile_default_stages(out->tile_n, out->k_blocks_per_stage > 0 ? out->k_blocks_per_stage : 1);
+    if (path == SGR_PATH_PAIR && (in->tile_n || in->k_blocks_per_stage) && !in->stages)
+      out->stages = sgr::pair_default_stages(out->tile_n, out->k_blocks_per_stage > 0 ? out->k_blocks_per_stage : 1);
   }
   if (out->ctas_per_sm < 1 || out->ctas_per_sm > 8 || out->stages < 1 || out->stages > 64)
     return SGR_ERR_UNSUPPORTED;
@@ -353,6 +373,13 @@ int resolve_config(int dev_sms, int M, int N, int K, const sgr_config* in, sgr_c
     int grid = 0;
     size_t smem = 0;
     int rc = sgr::tile_plan(*out, dev_sms > 0 ? dev_sms : 1, M, N, K, &gp, &grid, &smem);
+    if (rc != SGR_OK) return rc;
+  }
+  if (path == SGR_PATH_PAIR) {
+    sgr::PairParams pp;
+    int grid = 0;
+    size_t smem = 0;
+    int rc = sgr::pair_plan(*out, pair_pairs(dev_sms), M, N, K, &pp, &grid, &smem);
     if (rc != SGR_OK) return rc;
   }
   if (path == SGR_PATH_SIMT) {
@@ -471,6 +498,9 @@ int run(const void* A, long long lda, const void* W, const void* R, long long ld
                             (flags & SGR_FLAG_NO_PDL) == 0, stream);
   if (c.path == SGR_PATH_TILE)
     return sgr::tile_launch(c, st.sms, st.err, A, lda, W, R, ldr, Y, ldy, M, N, K,
+                            (flags & SGR_FLAG_NO_PDL) == 0, stream);
+  if (c.path == SGR_PATH_PAIR)
+    return sgr::pair_launch(c, sgr::pair_grid_pairs(st.sms, dev), st.err, A, lda, W, R, ldr, Y, ldy, M, N, K,
                             (flags & SGR_FLAG_NO_PDL) == 0, stream);
   return sgr::tc_launch(c, st.sms, st.err, &st.ws, A, lda, W, R, ldr, Y, ldy, M, N, K,
                         (flags & SGR_FLAG_NO_PDL) == 0, stream);
@@ -965,6 +995,13 @@ int sgr_kernel_resources(int device, int path, int M, int N, int K, int* regs, i
     if (sgr::w8_plan(c, sms, M, N, K, &wp, &grid, &smem) != SGR_OK) return SGR_ERR_UNSUPPORTED;
     *smem_bytes = (int)smem;
     *threads = sgr::kW8Threads;
+  } else if (c.path == SGR_PATH_PAIR) {
+    if (cudaFuncGetAttributes(&fa, sgr::pair_kernel_for(c.tile_n)) != cudaSuccess) {
+      cudaGetLastError();
+      return SGR_ERR_DEVICE;
+    }
+    *smem_bytes = (int)sgr::pair_smem_bytes(c.stages, c.tile_n, c.k_blocks_per_stage > 0 ? c.k_blocks_per_stage : 1);
+    *threads = sgr::kPairThreads;
   } else if (c.path == SGR_PATH_TILE) {
     if (cudaFuncGetAttributes(&fa, sgr::tile_kernel_for(c.tile_n, sgr::tile_mode(c))) != cudaSuccess) {
       cudaGetLastError();

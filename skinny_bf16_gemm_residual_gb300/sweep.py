@@ -108,6 +108,19 @@ def candidate_configs(path: int, M: int, K: int, grid: str) -> list[dict]:
                                 continue
                             out.append(dict(path=path, ctas_per_sm=1, tile_n=nt, k_blocks_per_stage=kb, stages=st,
                                             prefetch_stages=pf, k_split=split))
+    elif path == sgr.SGR_PATH_PAIR:
+        if M < 32:
+            return []
+        for nt in (64, 96, 128, 192, 256):
+            for kb in (1, 2, 4):
+                stage = kb * (128 * 128 + (nt // 2) * 128)
+                deepest = (232448 - 2048) // stage
+                for st in range(2, min(deepest, 16) + 1):
+                    if grid == "small" and st < deepest - 2:
+                        continue
+                    for pf in sorted({st, max(1, st - 1)}):
+                        out.append(dict(path=path, ctas_per_sm=1, tile_n=nt, k_blocks_per_stage=kb, stages=st,
+                                        prefetch_stages=pf))
     else:
         tiles = (M + 255) // 256
         nt = ((M + tiles - 1) // tiles + 15) // 16 * 16  # the library's token tile
@@ -277,7 +290,7 @@ def main(argv=None):
     done = load_done(args.output) if args.resume else set()
     out = open_output(args.output, args.resume) if args.output else None
     paths = {"simt": sgr.SGR_PATH_SIMT, "tc": sgr.SGR_PATH_TC, "rows": sgr.SGR_PATH_TC_ROWS,
-             "tile": sgr.SGR_PATH_TILE, "w8": sgr.SGR_PATH_W8, "w8simt": sgr.SGR_PATH_SIMT}
+             "tile": sgr.SGR_PATH_TILE, "pair": sgr.SGR_PATH_PAIR, "w8": sgr.SGR_PATH_W8, "w8simt": sgr.SGR_PATH_SIMT}
     fp8 = [name for name in args.paths.split(",") if name in ("w8", "w8simt")]
     if fp8:  # per-column-quantised E4M3 copies of the same weights
         q = [inputs.make_problem_w8(1, N, K, seed=s) for s in range(args.copies)]

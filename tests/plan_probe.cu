@@ -7,6 +7,7 @@
 #include "sgr_rows.cuh"
 #include "sgr_w8.cuh"
 #include "sgr_gemm.cuh"
+#include "sgr_pair.cuh"
 
 int main() {
   const int sms = 152;
@@ -90,6 +91,26 @@ int main() {
                           M, N, K, p.NT, p.kbps, p.stages, split, p.m_tiles, p.n_tiles, p.k_blocks, p.kb_split,
                           p.tmem_cols, grid, smem);
             }
+      // 2-CTA tile kernel (76 pairs: a 152-SM device whose SMs all pair up)
+      for (int tn : {64, 96, 128, 192, 256})
+        for (int kb : {1, 2, 4})
+          for (int st : {2, 4, 7, 10, 16}) {
+            sgr_config c = {};
+            c.path = SGR_PATH_PAIR;
+            c.ctas_per_sm = 1;
+            c.tile_n = tn;
+            c.k_blocks_per_stage = kb;
+            c.stages = st;
+            sgr::PairParams p;
+            int grid = 0;
+            size_t smem = 0;
+            if (sgr::pair_plan(c, sms / 2, M, N, K, &p, &grid, &smem) != SGR_OK) continue;
+            std::printf("{\"kind\": \"pair\", \"M\": %d, \"N\": %d, \"K\": %d, \"NT\": %d, \"kbps\": %d, "
+                        "\"stages\": %d, \"m_tiles\": %d, \"n_tiles\": %d, \"k_blocks\": %d, \"tmem_cols\": %d, "
+                        "\"grid\": %d, \"smem\": %zu, \"stage_bytes\": %u}\n",
+                        M, N, K, p.NT, p.kbps, p.stages, p.m_tiles, p.n_tiles, p.k_blocks, p.tmem_cols, grid, smem,
+                        sgr::pair_stage_bytes(p.NT, p.kbps));
+          }
     }
   }
   return 0;

@@ -45,6 +45,9 @@ def test_row_slab_plans(plans):
         assert p["grid"] * p["RB"] >= p["N"] > (p["grid"] - 1) * p["RB"], p      # every row, no empty CTA
         assert p["k_stages"] * p["kbps"] * 64 >= p["K"], p
         assert 1 <= p["prefetch"] <= p["stages"], p
+        # landing and slot-free barriers per stage, accumulator and drain
+        # barriers, the TMEM address and the abort flag
+        assert (2 * p["stages"] + 2) * 8 + 8 <= 1024, p
         drained = p["w_ring"] + p["a_ring"]
         # hand-over buffers of the epilogues live in the drained rings
         if p["NT"] == 16 and p["G"] <= 2:
@@ -97,12 +100,29 @@ def test_tile_plans(plans):
             assert p["grid"] == min(p["m_tiles"] * p["n_tiles"], 152), p
 
 
+def test_pair_plans(plans):
+    rows = [p for p in plans if p["kind"] == "pair"]
+    assert len(rows) > 50
+    for p in rows:
+        assert p["smem"] <= SMEM_LIMIT, p
+        assert p["NT"] in (64, 96, 128, 192, 256), p
+        assert p["tmem_cols"] >= 2 * p["NT"] and p["tmem_cols"] <= 512, p       # two accumulators
+        assert p["m_tiles"] * 256 >= p["M"] and p["n_tiles"] * p["NT"] >= p["N"], p
+        assert p["k_blocks"] * 64 >= p["K"], p
+        assert p["grid"] % 2 == 0 and p["grid"] == 2 * min(p["m_tiles"] * p["n_tiles"], 76), p
+        # every box of a stage starts on a 1024-byte swizzle-atom boundary
+        assert (128 * 128) % 1024 == 0 and (p["NT"] // 2 * 128) % 1024 == 0 and p["stage_bytes"] % 1024 == 0, p
+        assert (2 * p["stages"] + 5) * 8 + 8 <= 1024, p                         # barrier region
+        # the even CTA arms each stage with both CTAs' bytes: within the tx-count range
+        assert 2 * p["stage_bytes"] < 2 ** 20, p
+
+
 def test_large_ends_are_planned_or_refused(plans):
     """The largest K is planned by every kernel; N = 2^17 is refused by the
     row slabs (more than 128 rows per CTA on 152 SMs) and planned by the tile
-    kernel, which also takes M = 1024 (the row slabs hold at most 256 tokens)."""
+    kernels, which also take M = 1024 (the row slabs hold at most 256 tokens)."""
     kinds = lambda **kw: {p["kind"] for p in plans if all(p[k] == v for k, v in kw.items())}  # noqa: E731
-    assert kinds(K=1048576) == {"rows", "w8", "tile"}
-    assert kinds(N=131072) == {"tile"}
-    assert kinds(M=1024) == {"tile"}
+    assert kinds(K=1048576) == {"rows", "w8", "tile", "pair"}
+    assert kinds(N=131072) == {"tile", "pair"}
+    assert kinds(M=1024) == {"tile", "pair"}
     assert {"rows", "w8", "tile"} <= kinds(K=65536, M=256)
