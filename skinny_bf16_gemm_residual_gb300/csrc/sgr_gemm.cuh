@@ -427,7 +427,9 @@ __global__ void __launch_bounds__(tile_threads(MODE), 1)
     load_residual_row<NT>(p, m, n0, rv);
     for (int i = 0; i < my_tiles; ++i) {
       const int buf = i & 1;
-      bool ok = mbar_wait_or_abort(smem_u32(&acc_full[buf]), (i >> 1) & 1, abort_flag);
+      // Sleeping poll: warps 4 and 5 share sub-partitions with the copy and
+      // MMA threads, whose issue slots a tight spin would take.
+      bool ok = mbar_wait_sleepy_or_abort(smem_u32(&acc_full[buf]), (i >> 1) & 1, abort_flag);
       if (!ok) {
         if (!*abort_flag) report_error(p.err, kErrWaitMma);
         *abort_flag = 1;
@@ -474,7 +476,7 @@ __global__ void __launch_bounds__(tile_threads(MODE), 1)
     const int n0 = (unit / p.m_tiles) * NT + own0;
     uint4 rv[H / 8];
     load_residual_row<H>(p, m, n0, rv);
-    bool ok = mbar_wait_or_abort(smem_u32(&acc_full[0]), 0, abort_flag);
+    bool ok = mbar_wait_sleepy_or_abort(smem_u32(&acc_full[0]), 0, abort_flag);
     if (!ok) {
       if (!*abort_flag) report_error(p.err, kErrWaitMma);
       *abort_flag = 1;

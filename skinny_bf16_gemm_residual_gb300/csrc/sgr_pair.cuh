@@ -356,7 +356,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     pair_residual_row<NT>(p, m, n0, rv);
     for (int i = 0; i < my_tiles; ++i) {
       const int buf = i & 1;
-      bool ok = mbar_wait_or_abort(smem_u32(&acc_full[buf]), (i >> 1) & 1, abort_flag);
+      // Sleeping poll: warps 4 and 5 share sub-partitions with the copy and
+      // MMA threads, whose issue slots a tight spin would take.
+      bool ok = mbar_wait_sleepy_or_abort(smem_u32(&acc_full[buf]), (i >> 1) & 1, abort_flag);
       if (!ok) {
         if (!*abort_flag) report_error(p.err, kErrWaitMma);
         *abort_flag = 1;
