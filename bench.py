@@ -109,6 +109,7 @@ KERNEL_SOURCES = {
     "tile_gemm_kernel": ("sgr_gemm.cuh", "sgr_tc.cuh", "sgr_ptx.cuh"),
     "pair_gemm_kernel": ("sgr_pair.cuh", "sgr_gemm.cuh", "sgr_tc.cuh", "sgr_ptx.cuh"),
     "w8_rows_kernel": ("sgr_w8.cuh", "sgr_tc.cuh", "sgr_ptx.cuh"),
+    "w8s_kernel": ("sgr_w8s.cuh", "sgr_w8.cuh", "sgr_tc.cuh", "sgr_ptx.cuh"),
 }
 
 
@@ -789,12 +790,13 @@ def run_w8(sgr, device, stream, peaks: dict, m_list=(1, 2, 4, 16), copies: int =
         del g
         nbytes = N_DIM * K_DIM + 4 * N_DIM + 2 * M * K_DIM + 4 * M * N_DIM
         gbs = nbytes / (us * 1e-6) / 1e9
-        rows.append({"m": M, "kernel": "simt_skinny_kernel<W8>" if M <= 1 else "w8_rows_kernel",
+        rows.append({"m": M, "kernel": "w8s_kernel" if M <= 4 else "w8_rows_kernel",
                      "us": us, "bytes": nbytes, "gbs": gbs,
                      "frac_of_hbm_peak": gbs / peaks["hbm_gbs"] if peaks.get("hbm_gbs") else None})
     return {"per_m": rows,
             "note": "FP8 E4M3 weights + FP32 per-column scale, BF16 A/R/Y; graph of 8 calls over distinct weight "
-                    "copies; the library's own kernel choice (CUDA-core kernel for M = 1, tensor-core row slab above)"}
+                    "copies; the library's own kernel choice (FP8 tensor-core kernel with split activations for "
+                    "M <= 4, the widening row-slab kernel above)"}
 
 
 def run_e2e(sgr, per_m, Ws, m_list, device, stream, steps: int):

@@ -105,6 +105,8 @@ typedef enum {
 #define SGR_PATH_W8 5      /* tcgen05 row-slab kernel for FP8 weights (skinny_gemm_residual_w8 only, M <= 256);
                               skinny_gemm_residual_w8 also takes SGR_PATH_SIMT (CUDA-core kernel, M <= 8) */
 #define SGR_PATH_PAIR 6    /* tcgen05 tile kernel on 2-CTA clusters (cta_group::2), 256-token x tile_n tiles (large M) */
+#define SGR_PATH_W8S 7     /* FP8 weights on the FP8 tensor-core path (kind::f8f6f4), activations split exactly into
+                              two E4M3 parts (skinny_gemm_residual_w8 only, M <= 16) */
 
 /*
  * Y = bf16(A . W^T + R) with contiguous operands (lda = K, ldr = ldy = N).
@@ -313,9 +315,22 @@ int skinny_gemm_residual_grouped(const sgr_group* groups, int num_groups, int N,
  * 64-wide K blocks per stage, even, 2..8, token_tile, and rows_per_stage = W
  * rows per CTA, a multiple of 8 up to 128), and SGR_PATH_SIMT, the CUDA-core
  * kernel (M <= 8, contiguous code rows ldw == K, K a multiple of 16; cfg may
- * set ctas_per_sm, rows_per_stage = code rows per ring stage, stages).
- * SGR_PATH_AUTO takes the CUDA-core kernel for M = 1 where it can run, else
- * the tensor-core kernel.  Returns an sgr_status.
+ * set ctas_per_sm, rows_per_stage = code rows per ring stage, stages), and
+ * SGR_PATH_W8S, the FP8 tensor-core kernel (M <= 16 and the split activation
+ * operand of all of K in shared memory: K <= 3584 for 9-16 tokens, 7168 for
+ * up to 8; cfg may set stages 2..8, k_blocks_per_stage = 128-code K blocks
+ * per stage 1..8, token_tile 8 or 16, rows_per_stage).  SGR_PATH_W8S feeds
+ * the codes to the tensor core unchanged and brings the activations into
+ * E4M3 instead: each token row is scaled by a power of two that puts its
+ * largest magnitude in [128, 256), and each scaled value b is held as
+ * hi + lo/16 with hi = e4m3(b), lo = e4m3(16 (b - hi)).  That is exact for
+ * every activation within 2^13 of its row's largest magnitude; smaller ones
+ * are represented with an absolute error below 2^-21 times that magnitude
+ * (so a row whose values span more than 2^13 can differ from the exact
+ * result by up to sum_k |scale[n] e4m3(Wq[n,k])| * 2^-21 * max_k |A[m,k]|).
+ * SGR_PATH_AUTO takes SGR_PATH_W8S for M <= 4 where it can run, else the
+ * CUDA-core kernel for M = 1 where it can run, else the tensor-core row-slab
+ * kernel.  Returns an sgr_status.
  */
 int skinny_gemm_residual_w8(const void* A, int64_t lda, const void* Wq, int64_t ldw,
                             const float* scale, const void* R, int64_t ldr, void* Y,

@@ -30,6 +30,7 @@ from .binding import (  # noqa: F401
     SGR_PATH_TILE,
     SGR_PATH_W8,
     SGR_PATH_PAIR,
+    SGR_PATH_W8S,
     SgrError,
     load,
     make_config,

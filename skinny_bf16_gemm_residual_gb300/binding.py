@@ -34,6 +34,7 @@ SGR_PATH_TC_ROWS = 3
 SGR_PATH_TILE = 4
 SGR_PATH_W8 = 5
 SGR_PATH_PAIR = 6
+SGR_PATH_W8S = 7
 
 
 class sgr_group(ctypes.Structure):

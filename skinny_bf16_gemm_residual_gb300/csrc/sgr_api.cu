@@ -16,6 +16,7 @@
 #include "sgr_gemm.cuh"
 #include "sgr_pair.cuh"
 #include "sgr_w8.cuh"
+#include "sgr_w8s.cuh"
 #include "sgr_table.h"
 
 namespace {
@@ -229,6 +230,7 @@ int init_device(int dev) {
     if (ok == SGR_OK && sgr::tile_init_device() != cudaSuccess) ok = SGR_ERR_DEVICE;
     if (ok == SGR_OK && sgr::pair_init_device(dev) != cudaSuccess) ok = SGR_ERR_DEVICE;
     if (ok == SGR_OK && sgr::w8_init_device() != cudaSuccess) ok = SGR_ERR_DEVICE;
+    if (ok == SGR_OK && sgr::w8s_init_device() != cudaSuccess) ok = SGR_ERR_DEVICE;
     if (ok != SGR_OK) cudaGetLastError();
     st.sms = sms;
     st.err = errp;
@@ -640,6 +642,13 @@ bool simt_w8_supported(int M, int K, long long ldw) {
 // 10.8 us at M = 2, the tensor-core kernel ahead from there on).
 constexpr int kW8SimtMaxM = 1;
 
+// The FP8 tensor-core path with split activations up to this many tokens
+// (measured at N = 7168, K = 3584, graph of 8 calls: 9.2 / 9.4 / 9.8 us at
+// M = 1 / 2 / 4 against 10.8 us for the widening kernel; even at M = 8; the
+// widening kernel ahead at M = 16, where converting all of A in every CTA
+// costs more than it saves).
+constexpr int kW8sAutoMaxM = 4;
+
 // CUDA-core FP8 configuration: ring stages of two code rows, 4 stages,
 // CTAs per SM by token count (the register footprint grows with M).
 void default_simt_w8_config(int M, sgr_config* c) {
@@ -654,8 +663,12 @@ void default_simt_w8_config(int M, sgr_config* c) {
 // shape, then any non-zero field of `in` (path AUTO, W8 or SIMT).
 int resolve_config_w8(int sms, int M, int N, int K, long long ldw, const sgr_config* in, sgr_config* out) {
   int path = in ? in->path : SGR_PATH_AUTO;
-  if (path == SGR_PATH_AUTO)
-    path = (M <= kW8SimtMaxM && simt_w8_supported(M, K, ldw)) ? SGR_PATH_SIMT : SGR_PATH_W8;
+  if (path == SGR_PATH_AUTO) {
+    if (M <= kW8sAutoMaxM && sgr::w8s_supported(sms, M, N, K, ldw))
+      path = SGR_PATH_W8S;
+    else
+      path = (M <= kW8SimtMaxM && simt_w8_supported(M, K, ldw)) ? SGR_PATH_SIMT : SGR_PATH_W8;
+  }
   if (path == SGR_PATH_SIMT) {
     if (!simt_w8_supported(M, K, ldw)) return SGR_ERR_UNSUPPORTED;
     default_simt_w8_config(M, out);
@@ -674,6 +687,25 @@ int resolve_config_w8(int sms, int M, int N, int K, long long ldw, const sgr_con
     if (sgr::simt_smem_bytes(out->stages, out->rows_per_stage, K, 1) > (size_t)kMaxDynSmem)
       return SGR_ERR_UNSUPPORTED;
     return SGR_OK;
+  }
+  if (path == SGR_PATH_W8S) {
+    if (!sgr::w8s_supported(sms, M, N, K, ldw)) return SGR_ERR_UNSUPPORTED;
+    sgr::w8s_default_config(sms, M, N, K, out);
+    if (in) {
+      for (int r : in->reserved)
+        if (r != 0) return SGR_ERR_UNSUPPORTED;
+      if (in->tile_n || in->k_split || in->prefetch_stages) return SGR_ERR_UNSUPPORTED;
+      if (in->ctas_per_sm) out->ctas_per_sm = in->ctas_per_sm;
+      if (in->rows_per_stage) out->rows_per_stage = in->rows_per_stage;
+      if (in->stages) out->stages = in->stages;
+      if (in->k_blocks_per_stage) out->k_blocks_per_stage = in->k_blocks_per_stage;
+      if (in->token_tile) out->token_tile = in->token_tile;
+    }
+    out->path = SGR_PATH_W8S;
+    sgr::W8sParams p;
+    int grid = 0;
+    size_t smem = 0;
+    return sgr::w8s_plan(*out, sms, M, N, K, ldw, &p, &grid, &smem);
   }
   if (path != SGR_PATH_W8) return SGR_ERR_UNSUPPORTED;
   if (!sgr::w8_supported(sms, M, N, K)) return SGR_ERR_UNSUPPORTED;
@@ -720,6 +752,9 @@ int run_w8(const void* A, long long lda, const void* Wq, long long ldw, const fl
   if ((rc = resolve_config_w8(st.sms, M, N, K, ldw, cfg, &c)) != SGR_OK) return rc;
   if (c.path == SGR_PATH_SIMT)
     return launch_simt_w8(c, st.sms, st.err, A, lda, Wq, scale, R, ldr, Y, ldy, M, N, K, flags, stream);
+  if (c.path == SGR_PATH_W8S)
+    return sgr::w8s_launch(c, st.sms, st.err, A, lda, Wq, ldw, scale, R, ldr, Y, ldy, M, N, K,
+                           (flags & SGR_FLAG_NO_PDL) == 0, stream);
   return sgr::w8_launch(c, st.sms, st.err, A, lda, Wq, ldw, scale, R, ldr, Y, ldy, M, N, K,
                         (flags & SGR_FLAG_NO_PDL) == 0, stream);
 }
@@ -924,7 +959,7 @@ int sgr_default_config(int device, int M, int N, int K, int path, sgr_config* cf
   }
   sgr_config in = {};
   in.path = path;
-  if (path == SGR_PATH_W8) return resolve_config_w8(sms, M, N, K, K, &in, cfg);
+  if (path == SGR_PATH_W8 || path == SGR_PATH_W8S) return resolve_config_w8(sms, M, N, K, K, &in, cfg);
   return resolve_config(sms, M, N, K, &in, cfg);
 }
 
@@ -995,6 +1030,19 @@ int sgr_kernel_resources(int device, int path, int M, int N, int K, int* regs, i
     if (sgr::w8_plan(c, sms, M, N, K, &wp, &grid, &smem) != SGR_OK) return SGR_ERR_UNSUPPORTED;
     *smem_bytes = (int)smem;
     *threads = sgr::kW8Threads;
+  } else if (c.path == SGR_PATH_W8S) {
+    if (cudaFuncGetAttributes(&fa, sgr::w8s_kernel) != cudaSuccess) {
+      cudaGetLastError();
+      return SGR_ERR_DEVICE;
+    }
+    sgr::W8sParams wp;
+    int grid = 0;
+    size_t smem = 0;
+    int sms = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+    if (sgr::w8s_plan(c, sms, M, N, K, K, &wp, &grid, &smem) != SGR_OK) return SGR_ERR_UNSUPPORTED;
+    *smem_bytes = (int)smem;
+    *threads = sgr::kW8sThreads;
   } else if (c.path == SGR_PATH_PAIR) {
     if (cudaFuncGetAttributes(&fa, sgr::pair_kernel_for(c.tile_n)) != cudaSuccess) {
       cudaGetLastError();

@@ -442,8 +442,11 @@ inline void pair_default_config(int pairs, int M, int N, int K, sgr_config* c) {
   c->path = SGR_PATH_PAIR;
   c->ctas_per_sm = 1;
   c->tile_n = pair_default_nt(pairs, M, N);
-  c->k_blocks_per_stage = 1;
-  c->stages = pair_default_stages(c->tile_n, 1);
+  // Two K blocks per stage: half the stage-release commits of one-block
+  // stages, whose cost in the issuing thread measured larger than the loss
+  // of ring depth.
+  c->k_blocks_per_stage = 2;
+  c->stages = pair_default_stages(c->tile_n, 2);
   c->prefetch_stages = 0;  // all stages
   c->token_tile = kPairM;
   c->rows_per_stage = 0;

@@ -159,12 +159,12 @@ def test_validate_in_place_and_empty():
 
 
 def test_select_path():
-    paths = (sgr.SGR_PATH_SIMT, sgr.SGR_PATH_TC, sgr.SGR_PATH_TC_ROWS, sgr.SGR_PATH_TILE)
+    paths = (sgr.SGR_PATH_SIMT, sgr.SGR_PATH_TC, sgr.SGR_PATH_TC_ROWS, sgr.SGR_PATH_TILE, sgr.SGR_PATH_PAIR)
     for M in (1, 2, 3, 4, 8, 16, 32, 100, 256, 257, 1024, 5000):
         assert sgr.sgr_select_path(M, 7168, 3584) in paths
     for M in (1, 7, 300):  # shapes outside the measured table use the fallback rules
         assert sgr.sgr_select_path(M, 1024, 512) in paths
-    assert sgr.sgr_select_path(257, 7168, 3584) in (sgr.SGR_PATH_TC, sgr.SGR_PATH_TILE)  # row slab holds <= 256 tokens
+    assert sgr.sgr_select_path(257, 7168, 3584) in (sgr.SGR_PATH_TC, sgr.SGR_PATH_TILE, sgr.SGR_PATH_PAIR)  # row slab holds <= 256 tokens
     assert sgr.sgr_select_path(5000, 1024, 512) == sgr.SGR_PATH_TILE  # large M off the table: tile GEMM
     assert sgr.sgr_select_path(0, 7168, 3584) < 0
     assert sgr.sgr_select_path(4, 7170, 3584) < 0
@@ -190,7 +190,7 @@ def test_table_header_is_sorted_and_covers_the_latent_moe_shape():
     shapes = {}
     for n, k, m, path in rows:
         shapes.setdefault((n, k), []).append(m)
-        assert path in (1, 2, 3, 4)
+        assert path in (1, 2, 3, 4, 6)
     for ms in shapes.values():
         assert ms == sorted(ms)
     assert (7168, 3584) in shapes and shapes[(7168, 3584)][0] == 1

@@ -72,11 +72,11 @@ def test_pair_full_size_other_m(M):
 
 PAIR_CONFIGS = [
     dict(tile_n=64, stages=2),
-    dict(tile_n=96, stages=10),
+    dict(tile_n=96, k_blocks_per_stage=1, stages=10),
     dict(tile_n=128, stages=4, prefetch_stages=2),
-    dict(tile_n=192, stages=8),
+    dict(tile_n=192, k_blocks_per_stage=1, stages=8),
     dict(tile_n=192, stages=3, prefetch_stages=1),
-    dict(tile_n=256, stages=7),
+    dict(tile_n=256, k_blocks_per_stage=1, stages=7),
     dict(tile_n=256, stages=2),
     dict(tile_n=128, k_blocks_per_stage=2, stages=4),
     dict(tile_n=192, k_blocks_per_stage=2, stages=3),

@@ -85,7 +85,9 @@ def test_automatic_config_is_the_measured_table_entry(n, k):
             assert c.k_blocks_per_stage == e["k_blocks_per_stage"], (e, c.as_dict())
         if e["path"] in (sgr.SGR_PATH_TC_ROWS, sgr.SGR_PATH_SIMT):
             assert c.rows_per_stage == e["rows_per_stage"], (e, c.as_dict())
-        if e["path"] in (sgr.SGR_PATH_TC_ROWS, sgr.SGR_PATH_TILE):
+        if e["path"] in (sgr.SGR_PATH_TC_ROWS, sgr.SGR_PATH_TILE, sgr.SGR_PATH_PAIR):
             assert c.prefetch_stages == e["prefetch_stages"], (e, c.as_dict())
         if e["path"] == sgr.SGR_PATH_TILE:
             assert (c.tile_n, c.k_split) == (e["tile_n"], max(e["k_split"], 1)), (e, c.as_dict())
+        if e["path"] == sgr.SGR_PATH_PAIR:
+            assert c.tile_n == e["tile_n"], (e, c.as_dict())

@@ -316,11 +316,15 @@ def test_w8_simt_strided_in_place():
 
 
 def test_w8_auto_small_m_matches_tensor_core_path():
-    """AUTO picks the CUDA-core kernel for M = 1; both kernels agree with the oracle."""
+    """AUTO picks the FP8 tensor-core kernel with split activations for M = 1;
+    it, the widening tensor-core kernel and the CUDA-core kernel all agree
+    with the oracle."""
     p = inputs.make_problem_w8(1, N_FULL, K_FULL, seed=58)
     want = ref(p)
     compare(run(p), want, "w8 auto M=1")
+    compare(run(p, path=sgr.SGR_PATH_W8S), want, "w8 split FP8 M=1")
     compare(run(p, path=sgr.SGR_PATH_W8), want, "w8 tensor-core M=1")
+    compare(run(p, path=sgr.SGR_PATH_SIMT), want, "w8 CUDA-core M=1")
 
 
 def test_w8_simt_rejects():
