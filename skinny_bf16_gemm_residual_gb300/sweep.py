@@ -6,7 +6,8 @@ timed by batched CUDA-graph replay over rotating weight/residual copies that
 together exceed L2, and one JSON row per (M, path, config) is written.  A
 `torch.addmm` (cuBLAS) row under the same protocol is included as context.
 The per-M table compiled into the library is generated from these rows by
-``gen_table.py``.  The paths ``w8`` (tensor-core FP8-weight kernel) and
+``gen_table.py``.  The paths ``w8`` (widening tensor-core FP8-weight kernel), ``w8s`` (FP8
+tensor-core kernel with split activations) and
 ``w8simt`` (CUDA-core FP8-weight kernel) time ``skinny_gemm_residual_w8`` over
 rotating copies of per-column-quantised E4M3 weights; their rows (backend
 ``w8`` / ``w8_simt``) are for choosing that entry point's defaults and are
@@ -32,6 +33,20 @@ import torch
 
 from . import binding as sgr
 from . import inputs
+
+
+def candidate_configs_w8s(M: int, grid: str) -> list[dict]:
+    """Launch configurations of the FP8 tensor-core kernel with split
+    activations (M <= 16; shared memory checked by the library)."""
+    if M > 16:
+        return []
+    out = []
+    for kb in (2, 4, 8):
+        for st in (2, 3, 4, 6):
+            if grid == "small" and st > 4:
+                continue
+            out.append(dict(path=sgr.SGR_PATH_W8S, k_blocks_per_stage=kb, stages=st))
+    return out
 
 
 def candidate_configs_w8(simt: bool, M: int, K: int, grid: str) -> list[dict]:
@@ -290,8 +305,9 @@ def main(argv=None):
     done = load_done(args.output) if args.resume else set()
     out = open_output(args.output, args.resume) if args.output else None
     paths = {"simt": sgr.SGR_PATH_SIMT, "tc": sgr.SGR_PATH_TC, "rows": sgr.SGR_PATH_TC_ROWS,
-             "tile": sgr.SGR_PATH_TILE, "pair": sgr.SGR_PATH_PAIR, "w8": sgr.SGR_PATH_W8, "w8simt": sgr.SGR_PATH_SIMT}
-    fp8 = [name for name in args.paths.split(",") if name in ("w8", "w8simt")]
+             "tile": sgr.SGR_PATH_TILE, "pair": sgr.SGR_PATH_PAIR, "w8": sgr.SGR_PATH_W8, "w8simt": sgr.SGR_PATH_SIMT,
+             "w8s": sgr.SGR_PATH_W8S}
+    fp8 = [name for name in args.paths.split(",") if name in ("w8", "w8simt", "w8s")]
     if fp8:  # per-column-quantised E4M3 copies of the same weights
         q = [inputs.make_problem_w8(1, N, K, seed=s) for s in range(args.copies)]
         Wqs = [x.Wq.to(dev) for x in q]
@@ -313,14 +329,16 @@ def main(argv=None):
             launch = lambda c: torch.addmm(Rs[c], A, Ws[c].t(), out=Ys[c])
             record("cublas_addmm", {}, graph_samples(launch, args.copies, stream, args.repeats, args.replays))
         for name in args.paths.split(","):
-            w8 = name in ("w8", "w8simt")
+            w8 = name in ("w8", "w8simt", "w8s")
             if args.config:
                 cands = [dict(json.loads(c), path=paths[name]) for c in args.config]
+            elif name == "w8s":
+                cands = candidate_configs_w8s(M, args.grid)
             elif w8:
                 cands = candidate_configs_w8(name == "w8simt", M, K, args.grid)
             else:
                 cands = candidate_configs(paths[name], M, K, args.grid)
-            backend = {"w8": "w8", "w8simt": "w8_simt"}.get(name, name)
+            backend = {"w8": "w8", "w8simt": "w8_simt", "w8s": "w8s"}.get(name, name)
             for cfg in cands:
                 if row_key(M, N, K, backend, cfg) in done:
                     continue
