@@ -143,7 +143,8 @@ typedef struct {
   int prefetch_stages;    /* TC_ROWS, TILE, PAIR: weight stages requested before the dependency wait */
   int tile_n;             /* TILE: W rows per output tile (MMA N): 64, 128, 192 or 256;
                              PAIR: W rows per 256-token tile: 64, 96, 128, 192 or 256 */
-  int k_split;            /* TILE: 1, or 2 = K split over a 2-CTA cluster (one tile per cluster; tile_n <= 192) */
+  int k_split;            /* TILE: 1, or S = 2, 3, 4 = K split over an S-CTA cluster (one tile per cluster, all
+                             clusters resident at once); tile_n 64/128/192 for S = 2, 192 for 3, 128/192/256 for 4 */
   int reserved[2];        /* must be zero */
 } sgr_config;
 

@@ -227,7 +227,7 @@ int init_device(int dev) {
       }
     if (ok == SGR_OK && sgr::tc_init_device(sms, &st.ws) != cudaSuccess) ok = SGR_ERR_DEVICE;
     if (ok == SGR_OK && sgr::rows_init_device() != cudaSuccess) ok = SGR_ERR_DEVICE;
-    if (ok == SGR_OK && sgr::tile_init_device() != cudaSuccess) ok = SGR_ERR_DEVICE;
+    if (ok == SGR_OK && sgr::tile_init_device(dev) != cudaSuccess) ok = SGR_ERR_DEVICE;
     if (ok == SGR_OK && sgr::pair_init_device(dev) != cudaSuccess) ok = SGR_ERR_DEVICE;
     if (ok == SGR_OK && sgr::w8_init_device() != cudaSuccess) ok = SGR_ERR_DEVICE;
     if (ok == SGR_OK && sgr::w8s_init_device() != cudaSuccess) ok = SGR_ERR_DEVICE;
@@ -284,15 +284,20 @@ void default_simt_config(int sms, int M, int K, sgr_config* c) {
   c->token_tile = 0;
 }
 
-// 2-CTA clusters available to the pair kernel on the current device (SMs / 2
-// when no device is current or none was queried).
-int pair_pairs(int dev_sms) {
+// The current device, or -1 when none is current.
+int current_device_or_none() {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) {
     cudaGetLastError();
     dev = -1;
   }
-  return sgr::pair_grid_pairs(dev_sms > 0 ? dev_sms : 2, dev);
+  return dev;
+}
+
+// 2-CTA clusters available to the pair kernel on the current device (SMs / 2
+// when no device is current or none was queried).
+int pair_pairs(int dev_sms) {
+  return sgr::pair_grid_pairs(dev_sms > 0 ? dev_sms : 2, current_device_or_none());
 }
 
 int resolve_config(int dev_sms, int M, int N, int K, const sgr_config* in, sgr_config* out) {
@@ -374,7 +379,7 @@ int resolve_config(int dev_sms, int M, int N, int K, const sgr_config* in, sgr_c
     sgr::TileParams gp;
     int grid = 0;
     size_t smem = 0;
-    int rc = sgr::tile_plan(*out, dev_sms > 0 ? dev_sms : 1, M, N, K, &gp, &grid, &smem);
+    int rc = sgr::tile_plan(*out, dev_sms > 0 ? dev_sms : 1, M, N, K, &gp, &grid, &smem, current_device_or_none());
     if (rc != SGR_OK) return rc;
   }
   if (path == SGR_PATH_PAIR) {
@@ -499,7 +504,7 @@ int run(const void* A, long long lda, const void* W, const void* R, long long ld
     return sgr::rows_launch(c, st.sms, st.err, A, lda, W, R, ldr, Y, ldy, M, N, K,
                             (flags & SGR_FLAG_NO_PDL) == 0, stream);
   if (c.path == SGR_PATH_TILE)
-    return sgr::tile_launch(c, st.sms, st.err, A, lda, W, R, ldr, Y, ldy, M, N, K,
+    return sgr::tile_launch(c, st.sms, dev, st.err, A, lda, W, R, ldr, Y, ldy, M, N, K,
                             (flags & SGR_FLAG_NO_PDL) == 0, stream);
   if (c.path == SGR_PATH_PAIR)
     return sgr::pair_launch(c, sgr::pair_grid_pairs(st.sms, dev), st.err, A, lda, W, R, ldr, Y, ldy, M, N, K,

@@ -12,10 +12,12 @@
 // Operand roles (not swapped): a tile of 128 activation rows (tokens) is the
 // MMA's M side and lives in TMEM lanes 0..127; a tile of NT rows of W (NT =
 // 64, 128, 192 or 256) is the MMA's N side (TMEM columns).  Output tiles are
-// 128 x NT and never split along K: no workspace, no fixup.  NT is chosen per
-// shape so that the tile count fills the SMs in whole waves (N = 7168 with
-// NT = 192 gives 38 column tiles: 152 tiles at M = 512, 304 at M = 1024 on
-// 152 SMs).
+// 128 x NT.  NT is chosen per shape so that the tile count fills the SMs in
+// whole waves (N = 7168 with NT = 192 gives 38 column tiles: 152 tiles at
+// M = 512, 304 at M = 1024 on 152 SMs).  A problem with too few tiles for the
+// SMs splits each tile's K over the S = 2, 3 or 4 CTAs of a cluster, which
+// sum their partial accumulators through distributed shared memory (no
+// workspace; see the modes below).
 //
 // Persistent grid of min(tiles, SMs) CTAs; CTA c takes tiles c, c + G, ...,
 // each tile index t split as (t mod m_tiles, t div m_tiles), so the CTAs
@@ -71,7 +73,7 @@ struct TileParams {
   int stages;    // ring depth
   int kbps;      // K blocks per ring stage (1, 2 or 4): more contiguous bytes per W row and fetch
   int prefetch;  // W stages requested before griddepcontrol.wait (0..stages)
-  int kb_split;  // K split over a 2-CTA cluster: rank 0 takes K blocks [0, kb_split), rank 1 the rest
+  int kb_split;  // K split over an S-CTA cluster: rank r takes K blocks [r kb_split, (r + 1) kb_split), the last rank the rest
   int tmem_cols;
 };
 
@@ -117,6 +119,35 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
                  "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
                :
                : "memory");
+}
+
+// 16 TMEM columns with the wait naming every destination register.
+__device__ __forceinline__ void tmem_ld16w(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                 "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+                 "+r"(r[14]), "+r"(r[15])
+               :
+               : "memory");
+}
+
+// CH (16 or 32) consecutive TMEM columns of this thread's lane.
+template <int CH>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[CH]) {
+  static_assert(CH == 16 || CH == 32, "16 or 32 columns");
+  if constexpr (CH == 32) {
+    tmem_ld32(taddr, r);
+  } else {
+    tmem_ld16w(taddr, r);
+  }
 }
 
 // acc (FP32 bits) + two BF16 residuals packed in `res`, rounded once to BF16x2.
@@ -194,18 +225,24 @@ __device__ __forceinline__ void load_residual_row(const TileParams& p, int m, in
     rv[j] = (row_ok && n0 + 8 * j < p.N) ? *reinterpret_cast<const uint4*>(src + 8 * j) : make_uint4(0u, 0u, 0u, 0u);
 }
 
-// Modes (template parameter MODE):
-// kTilePlain: persistent CTAs, each tile's whole K in one CTA.
-// kTileSplitK: one tile per 2-CTA cluster, rank 0 accumulating K blocks
-// [0, kb_split) and rank 1 the rest; at the end each rank sends the half of
-// its accumulator that the other rank owns through distributed shared memory
-// (into the other rank's drained ring), adds the half it received to its own
-// and stores that half of the tile.  (a + b is the same in either order, so
-// the result does not depend on which rank finishes first.)  This doubles
-// the CTAs working on a problem with few tiles (M <= 256 at N = 7168).
+// Modes (template parameter MODE = S, the CTAs per tile):
+// kTilePlain (S = 1): persistent CTAs, each tile's whole K in one CTA.
+// kTileSplitK, kTileSplit3, kTileSplit4 (S = 2, 3, 4): one tile per S-CTA
+// cluster, rank r accumulating the r-th run of kb_split K blocks (the last
+// rank the rest).  Rank r owns the tile's columns [r NT/S, (r+1) NT/S).  At
+// the end every rank sends each other rank the columns that rank owns
+// through distributed shared memory (into the receiver's drained ring, one
+// slot per sender), then sums its own columns over the S partial
+// accumulators in rank order (rank 0 first, whichever rank finished first,
+// so the result is deterministic), adds the residual, rounds once and
+// stores.  A slot holds the sender's columns in groups of four, each group
+// as 128 rows of 16 bytes, so the 32 lanes of a warp (32 consecutive rows)
+// write one contiguous 512-byte run per store: scattered 16-byte remote
+// stores (one row per lane) measured 4-5x slower.  This multiplies the CTAs working on a problem with few tiles
+// (M <= 256 at N = 7168) and divides each CTA's operand bytes and MMAs by S.
 // Every CTA loads its own operands with plain TMA copies into its own
 // shared memory.
-enum : int { kTilePlain = 1, kTileSplitK = 2 };
+enum : int { kTilePlain = 1, kTileSplitK = 2, kTileSplit3 = 3, kTileSplit4 = 4 };
 
 // Threads per CTA: producer warp, MMA warp, four epilogue warps.  (A second
 // MMA-issuing warp taking every other ring slot into its own accumulator was
@@ -217,10 +254,11 @@ template <int NT, int MODE>
 __global__ void __launch_bounds__(tile_threads(MODE), 1)
     tile_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                      const TileParams p) {
-  constexpr int KSPLIT = MODE == kTileSplitK ? 2 : 1;
-  constexpr int CL = MODE == kTilePlain ? 1 : 2;  // CTAs per cluster
+  constexpr int KSPLIT = MODE;  // CTAs per tile
+  constexpr int CL = MODE;      // CTAs per cluster
 
-  static_assert(MODE != kTileSplitK || (NT / 2) % 32 == 0, "split tiles hand over 32-column chunks");
+  static_assert(MODE >= 1 && MODE <= 4 && NT % MODE == 0 && (NT / MODE) % 16 == 0,
+                "split tiles hand over whole 16-column pieces");
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -231,8 +269,8 @@ __global__ void __launch_bounds__(tile_threads(MODE), 1)
   uint64_t* acc_full = empty + S;                     // [2]  MMA -> epilogue
   uint64_t* acc_empty = acc_full + 2;                 // [2]  epilogue (4 warps) -> MMA
   uint64_t* drain = acc_empty + 2;                    // [1]  MMA completion at exit
-  uint64_t* peer_drained = drain + 1;                 // [1]  split: the other rank's ring is free
-  uint64_t* received = peer_drained + 1;              // [1]  split: the other rank's half has arrived
+  uint64_t* peer_drained = drain + 1;                 // [1]  split: every other rank's ring is free
+  uint64_t* received = peer_drained + 1;              // [1]  split: every other rank's columns have arrived
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(received + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const int KP = p.kbps;
@@ -243,15 +281,15 @@ __global__ void __launch_bounds__(tile_threads(MODE), 1)
   const uint32_t ring = base + 1024;  // [S] x {KP A boxes, KP W boxes}
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t rank = CL == 2 ? cluster_ctarank() : 0u;
+  const uint32_t rank = CL > 1 ? cluster_ctarank() : 0u;
   const int G = (int)gridDim.x / CL;      // tile-processing units (CTAs or clusters)
   const int unit = (int)blockIdx.x / CL;  // this CTA's unit
   // Tiles of a unit: (token tile, W column tile).
   const int mt_u = p.m_tiles;
   const int tiles = mt_u * p.n_tiles;
   const int my_tiles = (tiles - unit + G - 1) / G;  // >= 1: units <= tiles; 1 when split
-  const int kb0 = (KSPLIT == 2 && rank == 1) ? p.kb_split : 0;
-  const int KB = (KSPLIT == 2 && rank == 0) ? p.kb_split : p.k_blocks - kb0;  // K blocks of this CTA
+  const int kb0 = KSPLIT > 1 ? (int)rank * p.kb_split : 0;
+  const int KB = (KSPLIT > 1 && (int)rank < KSPLIT - 1) ? p.kb_split : p.k_blocks - kb0;  // K blocks of this CTA
   const int KS = (KB + KP - 1) / KP;  // ring stages per tile
 
   if (threadIdx.x == 0) {
@@ -264,8 +302,8 @@ __global__ void __launch_bounds__(tile_threads(MODE), 1)
       mbar_init(smem_u32(&acc_empty[b]), 4);
     }
     mbar_init(smem_u32(drain), 1);
-    mbar_init(smem_u32(peer_drained), 1);
-    mbar_init(smem_u32(received), 4 * 32);
+    mbar_init(smem_u32(peer_drained), KSPLIT > 1 ? KSPLIT - 1 : 1);
+    mbar_init(smem_u32(received), KSPLIT > 1 ? (KSPLIT - 1) * 4 * 32 : 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -281,7 +319,7 @@ __global__ void __launch_bounds__(tile_threads(MODE), 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if constexpr (CL == 2) cluster_sync_all();  // the other rank's barriers exist before any remote access
+  if constexpr (CL > 1) cluster_sync_all();  // the other ranks' barriers exist before any remote access
   const uint32_t tmem = *tmem_slot;
   pdl_launch_dependents();  // the dependent grid still waits for our completion before reading
 
@@ -466,11 +504,12 @@ __global__ void __launch_bounds__(tile_threads(MODE), 1)
   } else {
     // ------------------------------------------------------- split epilogue
     pdl_wait();  // R may come from the preceding kernel; Y may be read by it
-    constexpr int H = NT / 2;          // columns each rank finishes
-    constexpr int LD = H + 4;          // row stride (floats) of the hand-over buffer
+    constexpr int H = NT / KSPLIT;                 // columns each rank finishes
+    constexpr int CH = H % 32 == 0 ? 32 : 16;      // columns per TMEM load
+    constexpr uint32_t SLOT = (uint32_t)kTileM * (uint32_t)H * 4u;  // bytes of one sender's slot
+    // Column group g (columns 4g .. 4g+3) of row r sits at (g * 128 + r) * 16.
     const int q = warp & 3;            // TMEM lane quarter = tile rows [32 q, 32 q + 32)
     const int row = q * 32 + lane;     // row within the tile
-    const uint32_t other = rank ^ 1u;
     const int m = (unit % p.m_tiles) * kTileM + row;
     const int own0 = (int)rank * H;    // first column (within the tile) this rank finishes
     const int n0 = (unit / p.m_tiles) * NT + own0;
@@ -482,32 +521,42 @@ __global__ void __launch_bounds__(tile_threads(MODE), 1)
       *abort_flag = 1;
     }
     ok = __all_sync(0xffffffffu, ok);
-    // This rank's ring is drained (all its MMAs are done): tell the other rank.
+    // This rank's ring is drained (all its MMAs are done): tell the others.
     named_bar_sync(1, 128);
-    if (threadIdx.x == 64) mbar_arrive_remote(map_to_rank(smem_u32(peer_drained), other));
-    // Wait until the other rank's ring is drained, then write into it the half
-    // of this accumulator that the other rank finishes.
+    if (threadIdx.x == 64)
+      for (int o = 0; o < KSPLIT; ++o)
+        if (o != (int)rank) mbar_arrive_remote(map_to_rank(smem_u32(peer_drained), (uint32_t)o));
+    // Wait until every other rank's ring is drained, then write into rank o's
+    // ring (slot of this sender) the columns of this accumulator that o finishes.
     bool peer_ok = mbar_wait_cluster(smem_u32(peer_drained), 0, abort_flag);
     peer_ok = __all_sync(0xffffffffu, peer_ok);
     tc_fence_after();
     const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16);
     if (ok && peer_ok) {
-      const uint32_t dst = map_to_rank(ring + (uint32_t)row * (uint32_t)LD * 4u, other);
-      const int peer0 = (int)other * H;
 #pragma unroll
-      for (int c = 0; c < H / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(taddr + (uint32_t)(peer0 + c * 32), v);
+      for (int o = 0; o < KSPLIT; ++o) {
+        if (o == (int)rank) continue;
+        const uint32_t sidx = (int)rank < o ? rank : rank - 1u;  // this sender's slot at rank o
+        const uint32_t dst = map_to_rank(ring + sidx * SLOT + (uint32_t)row * 16u, (uint32_t)o);
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          st_cluster_v4(dst + (uint32_t)(c * 32 + 4 * j) * 4u, v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        for (int c = 0; c < H / CH; ++c) {
+          uint32_t v[CH];
+          tmem_ld_cols<CH>(taddr + (uint32_t)(o * H + c * CH), v);
+#pragma unroll
+          for (int j = 0; j < CH / 4; ++j)
+            st_cluster_v4(dst + (uint32_t)((c * CH) / 4 + j) * (uint32_t)kTileM * 16u, v[4 * j], v[4 * j + 1],
+                          v[4 * j + 2], v[4 * j + 3]);
+        }
       }
     } else if (!peer_ok) {
       if (!*abort_flag) report_error(p.err, kErrWaitFixup);
       *abort_flag = 1;
     }
-    mbar_arrive_remote(map_to_rank(smem_u32(received), other));  // every thread: its writes are released
-    // The other rank's half of this rank's columns has arrived: add, round, store.
+    // Every thread: its writes are released to each receiver.
+    for (int o = 0; o < KSPLIT; ++o)
+      if (o != (int)rank) mbar_arrive_remote(map_to_rank(smem_u32(received), (uint32_t)o));
+    // Every other rank's partial of this rank's columns has arrived: sum in
+    // rank order, add the residual, round, store.
     bool got = mbar_wait_cluster(smem_u32(received), 0, abort_flag);
     got = __all_sync(0xffffffffu, got);
     if (!got) {
@@ -515,25 +564,40 @@ __global__ void __launch_bounds__(tile_threads(MODE), 1)
       *abort_flag = 1;
     }
     if (ok && peer_ok && got) {
-      const uint32_t src = ring + (uint32_t)row * (uint32_t)LD * 4u;
+      const uint32_t src = ring + (uint32_t)row * 16u;
       __nv_bfloat16* yrow = p.Y + (size_t)(m < p.M ? m : 0) * p.ldy + n0;
 #pragma unroll
-      for (int c = 0; c < H / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(taddr + (uint32_t)(own0 + c * 32), v);
+      for (int c = 0; c < H / CH; ++c) {
+        uint32_t v[CH];
+        tmem_ld_cols<CH>(taddr + (uint32_t)(own0 + c * CH), v);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint4 o0 = lds128(src + (uint32_t)(c * 32 + 8 * j) * 4u);
-          const uint4 o1 = lds128(src + (uint32_t)(c * 32 + 8 * j + 4) * 4u);
-          const uint32_t s[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
-          uint32_t w[8];
+        for (int j = 0; j < CH / 8; ++j) {
+          const int col = c * CH + 8 * j;
+          float w[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            w[e] = __float_as_uint(__uint_as_float(v[8 * j + e]) + __uint_as_float(s[e]));
-          const uint4 r = rv[c * 4 + j];
-          const uint4 y = make_uint4(add_round_bf16x2(w[0], w[1], r.x), add_round_bf16x2(w[2], w[3], r.y),
-                                     add_round_bf16x2(w[4], w[5], r.z), add_round_bf16x2(w[6], w[7], r.w));
-          if (m < p.M && n0 + c * 32 + 8 * j < p.N) *reinterpret_cast<uint4*>(yrow + c * 32 + 8 * j) = y;
+          for (int r = 0; r < KSPLIT; ++r) {
+            float part[8];
+            if (r == (int)rank) {
+#pragma unroll
+              for (int e = 0; e < 8; ++e) part[e] = __uint_as_float(v[8 * j + e]);
+            } else {
+              const uint32_t sa = src + (uint32_t)(r < (int)rank ? r : r - 1) * SLOT + (uint32_t)(col / 4) * kTileM * 16u;
+              const uint4 o0 = lds128(sa), o1 = lds128(sa + (uint32_t)kTileM * 16u);
+              part[0] = __uint_as_float(o0.x), part[1] = __uint_as_float(o0.y);
+              part[2] = __uint_as_float(o0.z), part[3] = __uint_as_float(o0.w);
+              part[4] = __uint_as_float(o1.x), part[5] = __uint_as_float(o1.y);
+              part[6] = __uint_as_float(o1.z), part[7] = __uint_as_float(o1.w);
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) w[e] = r == 0 ? part[e] : w[e] + part[e];
+          }
+          const uint4 rr = rv[col / 8];
+          const uint4 y = make_uint4(
+              add_round_bf16x2(__float_as_uint(w[0]), __float_as_uint(w[1]), rr.x),
+              add_round_bf16x2(__float_as_uint(w[2]), __float_as_uint(w[3]), rr.y),
+              add_round_bf16x2(__float_as_uint(w[4]), __float_as_uint(w[5]), rr.z),
+              add_round_bf16x2(__float_as_uint(w[6]), __float_as_uint(w[7]), rr.w));
+          if (m < p.M && n0 + col < p.N) *reinterpret_cast<uint4*>(yrow + col) = y;
         }
       }
     }
@@ -546,9 +610,9 @@ __global__ void __launch_bounds__(tile_threads(MODE), 1)
     tc_fence_after();
     tmem_dealloc(tmem, (uint32_t)p.tmem_cols);
   }
-  // No rank leaves while the other may still write into its shared memory or
+  // No rank leaves while another may still write into its shared memory or
   // arrive on its barriers.
-  if constexpr (CL == 2) cluster_sync_all();
+  if constexpr (CL > 1) cluster_sync_all();
 }
 
 // ------------------------------------------------------------------ host side
@@ -604,46 +668,104 @@ inline void tile_default_config(int sms, int M, int N, int K, sgr_config* c) {
   c->rows_per_stage = 0;
 }
 
+// Tile widths each mode is built for: every width without a split; with an
+// S-way split, widths whose share per rank (NT / S) is a whole number of
+// 16-column pieces, limited to the ones that fill the SMs at N = 7168
+// (S = 2: 64, 128, 192; S = 3: 192; S = 4: 128, 192, 256).
+__host__ __device__ constexpr bool tile_has(int nt, int mode) {
+  return mode == kTilePlain ? (nt == 64 || nt == 128 || nt == 192 || nt == 256)
+         : mode == kTileSplitK ? (nt == 64 || nt == 128 || nt == 192)
+         : mode == kTileSplit3 ? nt == 192
+         : mode == kTileSplit4 ? (nt == 128 || nt == 192 || nt == 256)
+                               : false;
+}
+
 // The kernel instantiation for a tile width and mode (nullptr if none).
 template <int MODE>
 inline const void* tile_kernel_mode(int nt) {
   switch (nt) {
-    case 64: return reinterpret_cast<const void*>(tile_gemm_kernel<64, MODE>);
-    case 128: return reinterpret_cast<const void*>(tile_gemm_kernel<128, MODE>);
-    case 192: return reinterpret_cast<const void*>(tile_gemm_kernel<192, MODE>);
-    case 256: return MODE == kTileSplitK ? nullptr : reinterpret_cast<const void*>(tile_gemm_kernel<256, MODE>);
+    case 64:
+      if constexpr (tile_has(64, MODE)) return reinterpret_cast<const void*>(tile_gemm_kernel<64, MODE>);
+      break;
+    case 128:
+      if constexpr (tile_has(128, MODE)) return reinterpret_cast<const void*>(tile_gemm_kernel<128, MODE>);
+      break;
+    case 192:
+      if constexpr (tile_has(192, MODE)) return reinterpret_cast<const void*>(tile_gemm_kernel<192, MODE>);
+      break;
+    case 256:
+      if constexpr (tile_has(256, MODE)) return reinterpret_cast<const void*>(tile_gemm_kernel<256, MODE>);
+      break;
+    default:
+      break;
+  }
+  return nullptr;
+}
+
+inline const void* tile_kernel_for(int nt, int mode) {
+  switch (mode) {
+    case kTilePlain: return tile_kernel_mode<kTilePlain>(nt);
+    case kTileSplitK: return tile_kernel_mode<kTileSplitK>(nt);
+    case kTileSplit3: return tile_kernel_mode<kTileSplit3>(nt);
+    case kTileSplit4: return tile_kernel_mode<kTileSplit4>(nt);
     default: return nullptr;
   }
 }
 
-inline const void* tile_kernel_for(int nt, int mode) {
-  if (mode == kTilePlain) return tile_kernel_mode<kTilePlain>(nt);
-  if (mode == kTileSplitK) return tile_kernel_mode<kTileSplitK>(nt);
-  return nullptr;
-}
-
-// Mode of a configuration: k_split 2 -> split K; 0 or 1 -> plain.
+// Mode of a configuration: k_split 0 or 1 -> plain; 2, 3, 4 -> that split;
+// anything else -> 0 (unsupported).
 inline int tile_mode(const sgr_config& c) {
   const int split = c.k_split == 0 ? 1 : c.k_split;
-  if (split == 2) return kTileSplitK;
-  if (split == 1) return kTilePlain;
-  return 0;
+  return split >= 1 && split <= 4 ? split : 0;
 }
 
-inline cudaError_t tile_init_device() {
-  for (int mode : {kTilePlain, kTileSplitK})
+// Clusters of S = 2, 3, 4 CTAs (one CTA per SM) the device holds at once,
+// per device, from cudaOccupancyMaxActiveClusters: a split launch has one
+// tile per cluster and must fit in one wave.
+inline int* tile_split_cluster_table() {
+  static int table[64][5] = {{0}};
+  return &table[0][0];
+}
+
+inline cudaError_t tile_init_device(int dev) {
+  for (int mode = kTilePlain; mode <= kTileSplit4; ++mode)
     for (int nt : {64, 128, 192, 256}) {
       const void* fn = tile_kernel_for(nt, mode);
       if (!fn) continue;
       cudaError_t e = set_kernel_smem_attrs(fn);
       if (e != cudaSuccess) return e;
     }
+  for (int S = 2; S <= 4; ++S) {
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3((unsigned)S, 1, 1);
+    lc.blockDim = dim3((unsigned)kTileThreads, 1, 1);
+    lc.dynamicSmemBytes = 232448 - 1024;  // above half an SM's shared memory: one CTA per SM
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)S;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    int n = 0;
+    cudaError_t e = cudaOccupancyMaxActiveClusters(&n, tile_kernel_for(192, S), &lc);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) tile_split_cluster_table()[dev * 5 + S] = n;
+  }
   return cudaSuccess;
+}
+
+// Tiles an S-way split launch may have: the queried cluster count of the
+// device, else SMs / S (host-only planning without a device).
+inline int tile_split_capacity(int sms, int dev, int S) {
+  const int q = (dev >= 0 && dev < 64 && S >= 2 && S <= 4) ? tile_split_cluster_table()[dev * 5 + S] : 0;
+  const int even = S > 0 ? sms / S : 0;
+  return q > 0 && q < even ? q : even;
 }
 
 // Checks a resolved configuration for this shape; fills the kernel params.
 inline int tile_plan(const sgr_config& c, int sms, int M, int N, int K, TileParams* p, int* grid,
-                     size_t* smem) {
+                     size_t* smem, int dev = -1) {
   if (!tile_supported(M, N, K)) return SGR_ERR_UNSUPPORTED;
   const int nt = c.tile_n;
   const int mode = tile_mode(c);
@@ -661,14 +783,18 @@ inline int tile_plan(const sgr_config& c, int sms, int M, int N, int K, TilePara
   if (m_tiles * n_tiles > (1ll << 30)) return SGR_ERR_UNSUPPORTED;
   const long long tiles = m_tiles * n_tiles;
   const int k_blocks = (K + kTcKBlock - 1) / kTcKBlock;
-  // Split: rank 0 takes the first half of the K blocks rounded up to whole
-  // stages (so that its last stage reads nothing of rank 1's range).
-  const int kb_split = ((k_blocks + 1) / 2 + kbps - 1) / kbps * kbps;
-  if (mode == kTileSplitK) {
-    // One tile per cluster, both ranks with at least one K block, and the
-    // hand-over buffer (128 rows x (NT/2 + 4) floats) inside the ring.
-    if (2 * tiles > sms || k_blocks - kb_split < 1) return SGR_ERR_UNSUPPORTED;
-    if ((size_t)kTileM * (nt / 2 + 4) * 4 > (size_t)c.stages * tile_stage_bytes(nt, kbps)) return SGR_ERR_UNSUPPORTED;
+  // Split over S ranks: each rank but the last takes ceil(k_blocks / S) K
+  // blocks rounded up to whole stages (so that no stage reads into the next
+  // rank's range), the last rank the rest.
+  const int S = mode;
+  const int kb_split = S > 1 ? ((k_blocks + S - 1) / S + kbps - 1) / kbps * kbps : k_blocks;
+  if (S > 1) {
+    // One tile per cluster, all clusters resident at once, every rank with
+    // at least one K block, and the hand-over buffer (S - 1 slots of 128 rows
+    // x NT/S floats) inside the ring.
+    if (tiles > tile_split_capacity(sms, dev, S) || k_blocks - (S - 1) * kb_split < 1) return SGR_ERR_UNSUPPORTED;
+    if ((size_t)(S - 1) * kTileM * (nt / S) * 4 > (size_t)c.stages * tile_stage_bytes(nt, kbps))
+      return SGR_ERR_UNSUPPORTED;
   }
   p->M = M;
   p->N = N;
@@ -682,8 +808,8 @@ inline int tile_plan(const sgr_config& c, int sms, int M, int N, int K, TilePara
   p->stages = c.stages;
   p->prefetch = c.prefetch_stages > 0 ? c.prefetch_stages : c.stages;
   p->tmem_cols = detail::pow2_at_least(2 * nt);
-  if (mode == kTileSplitK) {
-    *grid = (int)(2 * tiles);
+  if (S > 1) {
+    *grid = (int)(S * tiles);
   } else {
     *grid = (int)(tiles < sms ? tiles : sms);
   }
@@ -691,13 +817,35 @@ inline int tile_plan(const sgr_config& c, int sms, int M, int N, int K, TilePara
   return SGR_OK;
 }
 
-inline int tile_launch(const sgr_config& c, int sms, unsigned* err, const void* A, long long lda,
+template <int MODE>
+inline cudaError_t tile_launch_mode(const cudaLaunchConfig_t* lc, int nt, const CUtensorMap& tmA, const CUtensorMap& tmW,
+                                    const TileParams& p) {
+  switch (nt) {
+    case 64:
+      if constexpr (tile_has(64, MODE)) return cudaLaunchKernelEx(lc, tile_gemm_kernel<64, MODE>, tmA, tmW, p);
+      break;
+    case 128:
+      if constexpr (tile_has(128, MODE)) return cudaLaunchKernelEx(lc, tile_gemm_kernel<128, MODE>, tmA, tmW, p);
+      break;
+    case 192:
+      if constexpr (tile_has(192, MODE)) return cudaLaunchKernelEx(lc, tile_gemm_kernel<192, MODE>, tmA, tmW, p);
+      break;
+    case 256:
+      if constexpr (tile_has(256, MODE)) return cudaLaunchKernelEx(lc, tile_gemm_kernel<256, MODE>, tmA, tmW, p);
+      break;
+    default:
+      break;
+  }
+  return cudaErrorInvalidValue;
+}
+
+inline int tile_launch(const sgr_config& c, int sms, int dev, unsigned* err, const void* A, long long lda,
                        const void* W, const void* R, long long ldr, void* Y, long long ldy, int M,
                        int N, int K, bool pdl, cudaStream_t stream) {
   TileParams p;
   int grid = 0;
   size_t smem = 0;
-  int rc = tile_plan(c, sms, M, N, K, &p, &grid, &smem);
+  int rc = tile_plan(c, sms, M, N, K, &p, &grid, &smem, dev);
   if (rc != SGR_OK) return rc;
   const int mode = tile_mode(c);
   CUtensorMap tmA, tmW;
@@ -722,7 +870,7 @@ inline int tile_launch(const sgr_config& c, int sms, unsigned* err, const void* 
   }
   if (mode != kTilePlain) {
     attr[n_attr].id = cudaLaunchAttributeClusterDimension;
-    attr[n_attr].val.clusterDim.x = 2;
+    attr[n_attr].val.clusterDim.x = (unsigned)mode;
     attr[n_attr].val.clusterDim.y = 1;
     attr[n_attr].val.clusterDim.z = 1;
     ++n_attr;
@@ -730,14 +878,12 @@ inline int tile_launch(const sgr_config& c, int sms, unsigned* err, const void* 
   lc.attrs = attr;
   lc.numAttrs = n_attr;
   cudaError_t e = cudaErrorInvalidValue;
-  switch (mode * 1000 + p.NT) {
-    case kTilePlain * 1000 + 64: e = cudaLaunchKernelEx(&lc, tile_gemm_kernel<64, kTilePlain>, tmA, tmW, p); break;
-    case kTilePlain * 1000 + 128: e = cudaLaunchKernelEx(&lc, tile_gemm_kernel<128, kTilePlain>, tmA, tmW, p); break;
-    case kTilePlain * 1000 + 192: e = cudaLaunchKernelEx(&lc, tile_gemm_kernel<192, kTilePlain>, tmA, tmW, p); break;
-    case kTilePlain * 1000 + 256: e = cudaLaunchKernelEx(&lc, tile_gemm_kernel<256, kTilePlain>, tmA, tmW, p); break;
-    case kTileSplitK * 1000 + 64: e = cudaLaunchKernelEx(&lc, tile_gemm_kernel<64, kTileSplitK>, tmA, tmW, p); break;
-    case kTileSplitK * 1000 + 128: e = cudaLaunchKernelEx(&lc, tile_gemm_kernel<128, kTileSplitK>, tmA, tmW, p); break;
-    case kTileSplitK * 1000 + 192: e = cudaLaunchKernelEx(&lc, tile_gemm_kernel<192, kTileSplitK>, tmA, tmW, p); break;
+  switch (mode) {
+    case kTilePlain: e = tile_launch_mode<kTilePlain>(&lc, p.NT, tmA, tmW, p); break;
+    case kTileSplitK: e = tile_launch_mode<kTileSplitK>(&lc, p.NT, tmA, tmW, p); break;
+    case kTileSplit3: e = tile_launch_mode<kTileSplit3>(&lc, p.NT, tmA, tmW, p); break;
+    case kTileSplit4: e = tile_launch_mode<kTileSplit4>(&lc, p.NT, tmA, tmW, p); break;
+    default: break;
   }
   if (e != cudaSuccess) {
     cudaGetLastError();

@@ -118,8 +118,8 @@ def candidate_configs(path: int, M: int, K: int, grid: str) -> list[dict]:
                     if grid == "small" and st < deepest - 2:
                         continue
                     for pf in sorted({st, max(1, st - 1)}):
-                        for split in (1, 2):
-                            if split == 2 and nt > 192:
+                        for split in (1, 2, 3, 4):
+                            if (split == 2 and nt > 192) or (split == 3 and nt != 192) or (split == 4 and nt == 64):
                                 continue
                             out.append(dict(path=path, ctas_per_sm=1, tile_n=nt, k_blocks_per_stage=kb, stages=st,
                                             prefetch_stages=pf, k_split=split))

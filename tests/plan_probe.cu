@@ -73,7 +73,7 @@ int main() {
       for (int tn : {64, 128, 192, 256})
         for (int kb : {1, 2, 4})
           for (int st : {2, 4, 7})
-            for (int split : {1, 2}) {
+            for (int split : {1, 2, 3, 4}) {
               sgr_config c = {};
               c.path = SGR_PATH_TILE;
               c.ctas_per_sm = 1;

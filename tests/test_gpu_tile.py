@@ -89,19 +89,35 @@ SPLIT_CONFIGS = [
     dict(tile_n=128, k_split=2, stages=3, prefetch_stages=1),
     dict(tile_n=192, k_split=2, stages=5),
     dict(tile_n=192, k_split=2, stages=2),
+    dict(tile_n=192, k_split=3, stages=5),
+    dict(tile_n=192, k_split=3, k_blocks_per_stage=2, stages=2, prefetch_stages=1),
+    dict(tile_n=128, k_split=4, stages=7),
+    dict(tile_n=128, k_split=4, k_blocks_per_stage=2, stages=3),
+    dict(tile_n=192, k_split=4, stages=5),
+    dict(tile_n=256, k_split=4, stages=4),
+    dict(tile_n=256, k_split=4, k_blocks_per_stage=2, stages=2),
 ]
+
+
+def split_refused(K, cfg):
+    """The planner's rule: every rank but the last takes ceil(k_blocks / S)
+    K blocks rounded up to whole stages, and the last rank needs at least one."""
+    S, kp = cfg.get("k_split", 1), cfg.get("k_blocks_per_stage", 1)
+    kb = (K + 63) // 64
+    chunk = ((kb + S - 1) // S + kp - 1) // kp * kp
+    return kb - (S - 1) * chunk < 1
 
 
 @pytest.mark.parametrize("cfg", SPLIT_CONFIGS, ids=lambda c: "-".join(f"{k}{v}" for k, v in c.items()))
 @pytest.mark.parametrize("M,N,K", [(1, 1024, 1032), (100, 2056, 72), (128, 1000, 136), (200, 1512, 3584),
                                    (256, 2056, 1000)])
 def test_tile_split_k_cluster(cfg, M, N, K):
-    """K split over a 2-CTA cluster, partial sums handed over through
-    distributed shared memory; K of 2 or 3 K blocks (one rank gets a single
-    block) and ragged M and N."""
+    """K split over a 2-, 3- or 4-CTA cluster, partial sums handed over
+    through distributed shared memory and summed in rank order; K of 2 or 3
+    K blocks (a rank with a single block, or none: refused) and ragged M and
+    N."""
     p = inputs.make_problem(M, N, K, seed=3 * M + K)
-    kb, kp = (K + 63) // 64, cfg.get("k_blocks_per_stage", 1)
-    if kb - ((kb + 1) // 2 + kp - 1) // kp * kp < 1:  # rank 1 would get no K block: refused
+    if split_refused(K, cfg):  # the last rank would get no K block
         with pytest.raises(sgr.SgrError) as e:
             run_tile(p, **cfg)
         assert e.value.status == sgr.SGR_ERR_UNSUPPORTED
@@ -116,10 +132,26 @@ def test_tile_split_full_size(M):
     compare(got, oracle_full(p.A, p.W, p.R), f"tile split M={M}")
 
 
-def test_tile_split_strided_in_place_and_deterministic():
+@pytest.mark.parametrize("tile_n,k_split", [(192, 3), (256, 4), (128, 4)])
+@pytest.mark.parametrize("M", [32, 64, 100, 128])
+def test_tile_wide_split_full_size_every_element(M, tile_n, k_split):
+    """3- and 4-way K splits at the latent-MoE shape (38 x 3 or 28 x 4 CTAs),
+    every element against the oracle.  A split whose clusters do not all fit
+    on the device at once (56 four-CTA clusters at tile_n = 128) is refused."""
+    p, ref = oracle_problem(M, N_FULL, K_FULL, seed=M + 6)
+    try:
+        got = run_tile(p, tile_n=tile_n, k_split=k_split)
+    except sgr.SgrError as e:
+        assert e.status == sgr.SGR_ERR_UNSUPPORTED and (N_FULL + tile_n - 1) // tile_n > 36
+        return
+    compare(got, ref, f"tile split {k_split} M={M} nt={tile_n}")
+
+
+@pytest.mark.parametrize("cfg", [dict(tile_n=128, k_split=2), dict(tile_n=192, k_split=3), dict(tile_n=256, k_split=4)],
+                         ids=lambda c: f"nt{c['tile_n']}-s{c['k_split']}")
+def test_tile_split_strided_in_place_and_deterministic(cfg):
     M, N, K = 150, 1024, 1032
     p = inputs.make_problem(M, N, K, seed=57)
-    cfg = dict(tile_n=128, k_split=2)
     Abig = torch.zeros((M, K + 136), dtype=torch.bfloat16, device="cuda")
     A = Abig[:, 64:64 + K]
     A.copy_(p.A)
@@ -137,7 +169,9 @@ def test_tile_split_strided_in_place_and_deterministic():
 def test_tile_split_rejects():
     p = inputs.make_problem(300, 256, 256, seed=2)
     A, W, R = (t.cuda() for t in (p.A, p.W, p.R))
-    for cfg in (dict(tile_n=256, k_split=2), dict(tile_n=128, k_split=3), dict(tile_n=64, k_split=-1)):
+    for cfg in (dict(tile_n=256, k_split=2), dict(tile_n=128, k_split=3), dict(tile_n=64, k_split=-1),
+                dict(tile_n=64, k_split=3), dict(tile_n=64, k_split=4), dict(tile_n=256, k_split=3),
+                dict(tile_n=192, k_split=5)):
         with pytest.raises(sgr.SgrError) as e:
             sgr.skinny_gemm_residual_ex(A, W, R, config=sgr.make_config(path=TILE, **cfg))
         assert e.value.status == sgr.SGR_ERR_UNSUPPORTED, cfg

@@ -86,16 +86,21 @@ def test_fp8_row_slab_plans(plans):
 def test_tile_plans(plans):
     rows = [p for p in plans if p["kind"] == "tile"]
     assert len(rows) > 50
+    assert {p["split"] for p in rows} == {1, 2, 3, 4}, "every split width is planned somewhere on the grid"
     for p in rows:
         assert p["smem"] <= SMEM_LIMIT, p
         assert p["NT"] in (64, 128, 192, 256), p
         assert p["tmem_cols"] >= 2 * p["NT"] and p["tmem_cols"] <= 512, p       # two accumulators
         assert p["m_tiles"] * 128 >= p["M"] and p["n_tiles"] * p["NT"] >= p["N"], p
         assert p["k_blocks"] * 64 >= p["K"], p
-        if p["split"] == 2:
-            assert 1 <= p["kb_split"] < p["k_blocks"], p                         # both ranks get K blocks
+        S = p["split"]
+        if S > 1:
+            assert 1 <= p["kb_split"] and (S - 1) * p["kb_split"] < p["k_blocks"], p  # every rank gets K blocks
             assert p["kb_split"] % p["kbps"] == 0, p
-            assert p["grid"] == 2 * p["m_tiles"] * p["n_tiles"] <= 152, p
+            assert p["grid"] == S * p["m_tiles"] * p["n_tiles"] <= 152, p         # one tile per cluster, one wave
+            assert (p["NT"] // S) % 16 == 0 and p["NT"] % S == 0, p               # whole 16-column pieces per rank
+            ring = p["stages"] * p["kbps"] * (128 * 128 + p["NT"] * 128)
+            assert (S - 1) * 128 * (p["NT"] // S) * 4 <= ring, p                 # hand-over slots inside the ring
         else:
             assert p["grid"] == min(p["m_tiles"] * p["n_tiles"], 152), p
 
