@@ -317,8 +317,33 @@ __global__ void __launch_bounds__(kW8sThreads, 1)
         asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
       }
     }
+    // When a thread's share of its token row is at most kW8sStageVec vectors
+    // (M <= 4 at K = 3584), the max pass keeps them in registers (cur[i] =
+    // vector part + i tpt) and the stage loop converts them from there;
+    // otherwise the stage loop reads each stage's vectors again, one stage
+    // ahead.  (Reading them again puts one memory round trip per stage on the
+    // converters' path, which then paces the MMAs and the weight ring.)
+    const int nreg = (nvec + tpt - 1) / tpt;
+    const bool in_regs = nreg <= kW8sStageVec;  // the same in every thread: depends on M and K only
+    uint4 cur[kW8sStageVec], nxt[kW8sStageVec];
     uint32_t mag = 0;  // largest |A[t,k]| of this thread as a BF16 magnitude pattern
-    if (row_ok) {
+    if (in_regs) {
+#pragma unroll
+      for (int i = 0; i < kW8sStageVec; ++i) {
+        const int v = part + i * tpt;
+        cur[i] = (row_ok && v < nvec) ? *reinterpret_cast<const uint4*>(arow + (size_t)v * 8) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int i = 0; i < kW8sStageVec; ++i) {
+        const uint32_t w4[4] = {cur[i].x, cur[i].y, cur[i].z, cur[i].w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const uint32_t lo = w4[h] & 0x7FFFu, hi = (w4[h] >> 16) & 0x7FFFu;
+          mag = lo > mag ? lo : mag;
+          mag = hi > mag ? hi : mag;
+        }
+      }
+    } else if (row_ok) {
 #pragma unroll 4
       for (int v = part; v < nvec; v += tpt) {
         const uint4 a = *reinterpret_cast<const uint4*>(arow + (size_t)v * 8);
@@ -356,11 +381,41 @@ __global__ void __launch_bounds__(kW8sThreads, 1)
     }
     named_bar_sync(2, kW8sConvThreads);
     // Stage by stage (kbps blocks of 128 codes = kbps * 16 vectors), in K
-    // order; the stage's activations are read again (from L2), those of the
-    // next stage requested while this one is converted.
+    // order: from the registers of the max pass, or read again (from L2) with
+    // the next stage's vectors requested while this one is converted.
     const int vps = p.kbps * (kW8sKBlock / 8);  // vectors per stage
     const int voff = ((part % tpt) + tpt) % tpt;
-    uint4 cur[kW8sStageVec], nxt[kW8sStageVec];
+    // Split one 16-byte vector (8 activations of token t at K = 8 v) into its
+    // hi and lo E4M3 parts and store both into the operand's block.
+    auto convert_store = [&](const uint4& a, int v) {
+      const uint32_t w4[4] = {a.x, a.y, a.z, a.w};
+      uint32_t hiw[2], low[2];
+#pragma unroll
+      for (int h = 0; h < 4; h += 2) {
+        uint32_t b16[2], hi16[2], r16[2];
+        uint16_t hi8[2], lo8[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(b16[u]) : "f"(bf16hi(w4[h + u]) * sc), "f"(bf16lo(w4[h + u]) * sc));
+          asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(hi8[u]) : "r"(b16[u]));
+          hi16[u] = e4m3x2_to_f16x2(hi8[u]);
+          asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r16[u]) : "r"(b16[u]), "r"(hi16[u]));      // exact
+          asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r16[u]) : "r"(r16[u]), "r"(0x4C004C00u));  // x 16, exact
+          asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(lo8[u]) : "r"(r16[u]));
+        }
+        hiw[h >> 1] = (uint32_t)hi8[0] | ((uint32_t)hi8[1] << 16);
+        low[h >> 1] = (uint32_t)lo8[0] | ((uint32_t)lo8[1] << 16);
+      }
+      const int j = v >> 4;               // K block
+      const int cc = (v & 15) >> 1;       // 16-byte chunk of the 128-byte row
+      const uint32_t half = (uint32_t)(v & 1) * 8u;
+      const int rh = t, rl = p.NT + t;    // hi row, lo row of the block
+      const uint32_t blk = b_buf + (uint32_t)j * bblk;
+      const uint32_t ah = blk + (uint32_t)rh * 128u + (uint32_t)((cc ^ (rh & 7)) * 16) + half;
+      const uint32_t al = blk + (uint32_t)rl * 128u + (uint32_t)((cc ^ (rl & 7)) * 16) + half;
+      asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(ah), "r"(hiw[0]), "r"(hiw[1]) : "memory");
+      asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(al), "r"(low[0]), "r"(low[1]) : "memory");
+    };
     auto load_stage = [&](int st, uint4 (&buf)[kW8sStageVec]) {
       const int v0 = st * vps;
       const int v1 = v0 + vps < nvec ? v0 + vps : nvec;
@@ -372,51 +427,42 @@ __global__ void __launch_bounds__(kW8sThreads, 1)
                                               : make_uint4(0u, 0u, 0u, 0u);
       }
     };
-    load_stage(0, cur);
-    for (int st = 0; st < KS; ++st) {
-      load_stage(st + 1, nxt);
-      const int v0 = st * vps;
-      const int v1 = v0 + vps < nvec ? v0 + vps : nvec;
-      const int vfirst = v0 + ((voff - v0) % tpt + tpt) % tpt;
-      if (row_ok) {
+    if (in_regs) {
+      for (int st = 0; st < KS; ++st) {
+        const int v0 = st * vps;
+        const int v1 = v0 + vps < nvec ? v0 + vps : nvec;
+        if (row_ok) {
 #pragma unroll
-        for (int i = 0; i < kW8sStageVec; ++i) {
-          const int v = vfirst + i * tpt;
-          if (v >= v1) break;
-          const uint32_t w4[4] = {cur[i].x, cur[i].y, cur[i].z, cur[i].w};
-          uint32_t hiw[2], low[2];
-#pragma unroll
-          for (int h = 0; h < 4; h += 2) {
-            uint32_t b16[2], hi16[2], r16[2];
-            uint16_t hi8[2], lo8[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(b16[u]) : "f"(bf16hi(w4[h + u]) * sc), "f"(bf16lo(w4[h + u]) * sc));
-              asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(hi8[u]) : "r"(b16[u]));
-              hi16[u] = e4m3x2_to_f16x2(hi8[u]);
-              asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r16[u]) : "r"(b16[u]), "r"(hi16[u]));      // exact
-              asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r16[u]) : "r"(r16[u]), "r"(0x4C004C00u));  // x 16, exact
-              asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(lo8[u]) : "r"(r16[u]));
-            }
-            hiw[h >> 1] = (uint32_t)hi8[0] | ((uint32_t)hi8[1] << 16);
-            low[h >> 1] = (uint32_t)lo8[0] | ((uint32_t)lo8[1] << 16);
+          for (int i = 0; i < kW8sStageVec; ++i) {
+            const int v = part + i * tpt;
+            if (v >= v0 && v < v1) convert_store(cur[i], v);
           }
-          const int j = v >> 4;               // K block
-          const int cc = (v & 15) >> 1;       // 16-byte chunk of the 128-byte row
-          const uint32_t half = (uint32_t)(v & 1) * 8u;
-          const int rh = t, rl = p.NT + t;    // hi row, lo row of the block
-          const uint32_t blk = b_buf + (uint32_t)j * bblk;
-          const uint32_t ah = blk + (uint32_t)rh * 128u + (uint32_t)((cc ^ (rh & 7)) * 16) + half;
-          const uint32_t al = blk + (uint32_t)rl * 128u + (uint32_t)((cc ^ (rl & 7)) * 16) + half;
-          asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(ah), "r"(hiw[0]), "r"(hiw[1]) : "memory");
-          asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(al), "r"(low[0]), "r"(low[1]) : "memory");
         }
+        fence_proxy_async_smem();  // the generic-proxy writes become visible to the tensor core
+        named_bar_sync(2, kW8sConvThreads);
+        if (ct == 0) mbar_arrive(smem_u32(&bready[st]));
       }
+    } else {
+      load_stage(0, cur);
+      for (int st = 0; st < KS; ++st) {
+        load_stage(st + 1, nxt);
+        const int v0 = st * vps;
+        const int v1 = v0 + vps < nvec ? v0 + vps : nvec;
+        const int vfirst = v0 + ((voff - v0) % tpt + tpt) % tpt;
+        if (row_ok) {
 #pragma unroll
-      for (int i = 0; i < kW8sStageVec; ++i) cur[i] = nxt[i];
-      fence_proxy_async_smem();  // the generic-proxy writes become visible to the tensor core
-      named_bar_sync(2, kW8sConvThreads);
-      if (ct == 0) mbar_arrive(smem_u32(&bready[st]));
+          for (int i = 0; i < kW8sStageVec; ++i) {
+            const int v = vfirst + i * tpt;
+            if (v >= v1) break;
+            convert_store(cur[i], v);
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < kW8sStageVec; ++i) cur[i] = nxt[i];
+        fence_proxy_async_smem();  // the generic-proxy writes become visible to the tensor core
+        named_bar_sync(2, kW8sConvThreads);
+        if (ct == 0) mbar_arrive(smem_u32(&bready[st]));
+      }
     }
 
     if (warp < 6) {
