@@ -62,9 +62,6 @@ constexpr int kRowsThreads = 192;
 constexpr int kRowsMaxTokens = 256;
 constexpr int kRowsPrefetchTokens = 16;  // residual values held in registers before the MMAs end
 constexpr uint32_t kRowsSlack = kTcTileRows * 128u;  // MMA window over-read past the ring
-#ifndef SGR_ROWS_TAIL
-#define SGR_ROWS_TAIL 1  // sub-stages the last stage's K range is split into (1: none)
-#endif
 
 struct RowsParams {
   const __nv_bfloat16* R;
@@ -74,10 +71,8 @@ struct RowsParams {
   int M, N, K;
   int RB;        // W rows per CTA (multiple of 8, <= 128)
   int NT;        // token tile = MMA N (multiple of 16, >= M)
-  int k_stages;  // ring stages: full stages of kbps K blocks, then the tail's sub-stages
+  int k_stages;  // ceil(K / (64 * kbps))
   int kbps;      // 64-wide K blocks per stage
-  int full_stages;  // stages of kbps K blocks before the tail
-  int tail_kb;      // K blocks per tail stage (kbps, or a divisor of it that the packing groups divide)
   int stages;    // ring depth
   int groups;    // K blocks packed into one MMA along its diagonal (1, 2 or 4)
   int prefetch;  // W stages requested before griddepcontrol.wait (1..stages)
@@ -236,11 +231,6 @@ __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, 
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int KS = p.k_stages;
-  // Stages 0 .. KF-1 hold kbps K blocks each; the last stage's range is split
-  // into stages of tail_kb blocks, so that the MMAs left to run after the
-  // final weight bytes land are those of a few blocks, not of a whole stage.
-  const int TB = p.tail_kb;
-  const int KF = p.full_stages;
   const CUtensorMap* tmW = io.tmW;
   const CUtensorMap* tmA = io.tmA;
 
@@ -278,23 +268,19 @@ __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, 
       // slot left free lets weights keep streaming while A (needed by the
       // first MMA) is fetched after the wait.
       const int pre = KS < p.prefetch ? KS : p.prefetch;
-      // First K block and block count of stage s.
-      auto first_block = [&](int s) { return s < KF ? s * p.kbps : KF * p.kbps + (s - KF) * TB; };
-      auto stage_blocks = [&](int s) { return s < KF ? p.kbps : TB; };
       for (int s = 0; s < pre; ++s) {
         const uint32_t fb = smem_u32(&full[s]);
-        const int nb = stage_blocks(s), b0 = first_block(s);
-        mbar_arrive_expect_tx(fb, (uint32_t)nb * (wblk + ablk));
+        mbar_arrive_expect_tx(fb, stage_bytes);
         const uint32_t ws = w_ring + (uint32_t)s * w_stage;
-        for (int j = 0; j < nb; ++j)
-          tma_load_2d(ws + (uint32_t)j * wblk, tmW, (b0 + j) * kTcKBlock, n0, fb, pol_w);
+        for (int j = 0; j < p.kbps; ++j)
+          tma_load_2d(ws + (uint32_t)j * wblk, tmW, (s * p.kbps + j) * kTcKBlock, n0, fb, pol_w);
       }
       pdl_wait();
       for (int s = 0; s < pre; ++s) {
         const uint32_t as = a_ring + (uint32_t)s * a_stage;
-        const int nb = stage_blocks(s), b0 = first_block(s);
-        for (int j = 0; j < nb; ++j)
-          tma_load_2d(as + (uint32_t)j * ablk, tmA, (b0 + j) * kTcKBlock, 0, smem_u32(&full[s]), pol_a);
+        for (int j = 0; j < p.kbps; ++j)
+          tma_load_2d(as + (uint32_t)j * ablk, tmA, (s * p.kbps + j) * kTcKBlock, 0,
+                      smem_u32(&full[s]), pol_a);
       }
       // Ring position kept by increments: no integer division on the
       // per-stage path of this single issuing thread.
@@ -302,24 +288,22 @@ __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, 
       int slot = pre == S ? 0 : pre;
       uint32_t par = pre == S ? 1u : 0u;  // ring round parity of `slot`
       uint32_t ws = w_ring + (uint32_t)slot * w_stage, as = a_ring + (uint32_t)slot * a_stage;
-      int kx = first_block(pre) * kTcKBlock;
-      const uint32_t tail_bytes = (uint32_t)TB * (wblk + ablk);
+      int kx = pre * p.kbps * kTcKBlock;
+      const int kstep = p.kbps * kTcKBlock;
       for (int s = pre; s < KS; ++s) {
         if (s >= S && !mbar_wait_or_abort(smem_u32(&empty[slot]), par ^ 1u, abort_flag)) {
           if (!*abort_flag) report_error(p.err, kErrWaitEmpty);
           *abort_flag = 1;
           break;
         }
-        const bool full_stage = s < KF;
-        const int nb = full_stage ? p.kbps : TB;
         const uint32_t fb = smem_u32(&full[slot]);
-        mbar_arrive_expect_tx(fb, full_stage ? stage_bytes : tail_bytes);
-        for (int j = 0; j < nb; ++j)
+        mbar_arrive_expect_tx(fb, stage_bytes);
+        for (int j = 0; j < p.kbps; ++j)
           tma_load_2d(ws + (uint32_t)j * wblk, tmW, kx + j * kTcKBlock, n0, fb, pol_w);
-        for (int j = 0; j < nb; ++j)
+        for (int j = 0; j < p.kbps; ++j)
           tma_load_2d(as + (uint32_t)j * ablk, tmA, kx + j * kTcKBlock, 0, fb, pol_a);
         issued = s + 1;
-        kx += nb * kTcKBlock;
+        kx += kstep;
         ws += w_stage;
         as += a_stage;
         if (++slot == S) {
@@ -353,8 +337,7 @@ __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, 
           break;
         }
         tc_fence_after();
-        const int nb = s < KF ? p.kbps : TB;
-        for (int j = 0; j < nb; j += p.groups) {
+        for (int j = 0; j < p.kbps; j += p.groups) {
 #pragma unroll
           for (int kk = 0; kk < kTcKBlock / 16; ++kk) {
             const bool first = (s == 0) && (j == 0) && (kk == 0);
@@ -768,6 +751,7 @@ inline int rows_plan(const sgr_config& c, int sms, int M, int N, int K, RowsPara
   p->K = K;
   p->RB = rb;
   p->NT = nt;
+  p->k_stages = (K + kstage_elems - 1) / kstage_elems;
   p->kbps = c.k_blocks_per_stage;
   p->stages = c.stages;
   p->prefetch = c.prefetch_stages > 0 ? c.prefetch_stages : (c.stages > 2 ? c.stages - 1 : c.stages);
@@ -786,17 +770,6 @@ inline int rows_plan(const sgr_config& c, int sms, int M, int N, int K, RowsPara
     p->groups /= 2;
   if (rows_stage_floats(p->groups, rb, nt) * 4 > (size_t)c.stages * rows_stage_bytes(c.k_blocks_per_stage, rb, nt))
     return SGR_ERR_UNSUPPORTED;
-  // The last full stage's range in stages of tail_kb blocks (SGR_ROWS_TAIL
-  // sub-stages where they divide it in whole packing groups), only those
-  // that hold K blocks.
-  const int kb = (K + kTcKBlock - 1) / kTcKBlock;
-  const int full = (K + kstage_elems - 1) / kstage_elems;  // stages of kbps blocks covering K
-  int tkb = p->kbps;
-  if (SGR_ROWS_TAIL > 1 && p->kbps % SGR_ROWS_TAIL == 0 && (p->kbps / SGR_ROWS_TAIL) % p->groups == 0)
-    tkb = p->kbps / SGR_ROWS_TAIL;
-  p->full_stages = full - 1;
-  p->tail_kb = tkb;
-  p->k_stages = p->full_stages + (kb - p->full_stages * p->kbps + tkb - 1) / tkb;
   p->tmem_cols = detail::pow2_at_least(p->groups * nt);
   *grid = (N + rb - 1) / rb;
   *smem = sm;

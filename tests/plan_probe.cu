@@ -38,10 +38,10 @@ int main() {
             if (sgr::rows_plan(c, sms, M, N, K, &p, &grid, &smem) != SGR_OK) continue;
             const size_t w_ring = (size_t)st * kb * p.RB * 128, a_ring = (size_t)st * kb * p.NT * 128;
             std::printf("{\"kind\": \"rows\", \"M\": %d, \"N\": %d, \"K\": %d, \"RB\": %d, \"NT\": %d, \"G\": %d, "
-                        "\"kbps\": %d, \"stages\": %d, \"prefetch\": %d, \"k_stages\": %d, \"full_stages\": %d, "
-                        "\"tail_kb\": %d, \"tmem_cols\": %d, \"grid\": %d, \"smem\": %zu, \"w_ring\": %zu, \"a_ring\": %zu}\n",
-                        M, N, K, p.RB, p.NT, p.groups, p.kbps, p.stages, p.prefetch, p.k_stages, p.full_stages,
-                        p.tail_kb, p.tmem_cols, grid, smem, w_ring, a_ring);
+                        "\"kbps\": %d, \"stages\": %d, \"prefetch\": %d, \"k_stages\": %d, \"tmem_cols\": %d, "
+                        "\"grid\": %d, \"smem\": %zu, \"w_ring\": %zu, \"a_ring\": %zu}\n",
+                        M, N, K, p.RB, p.NT, p.groups, p.kbps, p.stages, p.prefetch, p.k_stages, p.tmem_cols, grid,
+                        smem, w_ring, a_ring);
           }
       // FP8 row-slab kernel
       for (int rb : {0, 8, 24, 32, 64, 128})
