@@ -1,5 +1,6 @@
-"""CPU oracle for Y = bf16(A . W^T + R) and its low-bit weight variant
-Y = bf16(scale . A . e4m3(Wq)^T + R)  --  TEST INFRASTRUCTURE ONLY.
+"""CPU oracle for Y = bf16(A . W^T + R) and its low-bit weight variants
+Y = bf16(scale . A . e4m3(Wq)^T + R) (FP8) and
+Y = bf16(gs . A . (e2m1(Wq4) . e4m3(bs))^T + R) (NVFP4)  --  TEST INFRASTRUCTURE ONLY.
 
 Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline /
 reference leg may import this package.  The product path (the CUDA library and
@@ -8,8 +9,10 @@ its Python binding) never calls it and shares no code with it.
 The arithmetic lives in ``skinny_ref.c`` (plain C, FP64 accumulation, one
 round-to-nearest-even to BF16; see the header of that file for the passages it
 follows).  This module compiles it with gcc and wraps it with ctypes.  BF16
-arrays travel as numpy uint16 bit patterns, FP8 E4M3 weights as uint8 codes;
-torch tensors are accepted and converted with ``to_bits`` / ``to_codes``.
+arrays travel as numpy uint16 bit patterns, FP8 E4M3 weights as uint8 codes,
+NVFP4 weights as uint8 bytes holding two E2M1 codes (element 2i in the low
+nibble) plus uint8 E4M3 block scales (one per 16 elements of a row); torch
+tensors are accepted and converted with ``to_bits`` / ``to_codes``.
 """
 from __future__ import annotations
 
@@ -125,6 +128,14 @@ class Oracle:
         lib.sgr_ref_sample_w8.argtypes = [u16p, L, u8p, L, fp, u16p, L, L, L, L, lp, lp, L, u16p]
         lib.sgr_ref_e4m3_to_double.restype = ctypes.c_double
         lib.sgr_ref_e4m3_to_double.argtypes = [ctypes.c_uint8]
+        lib.sgr_ref_gemm_residual_w4.restype = I
+        lib.sgr_ref_gemm_residual_w4.argtypes = [u16p, L, u8p, L, u8p, L, ctypes.c_float, u16p, L, u16p, L,
+                                                 L, L, L, I]
+        lib.sgr_ref_sample_w4.restype = I
+        lib.sgr_ref_sample_w4.argtypes = [u16p, L, u8p, L, u8p, L, ctypes.c_float, u16p, L, L, L, L, lp, lp, L,
+                                          u16p]
+        lib.sgr_ref_e2m1_to_double.restype = ctypes.c_double
+        lib.sgr_ref_e2m1_to_double.argtypes = [ctypes.c_uint8]
         lib.sgr_ref_mutant.restype = I
         lib.sgr_ref_mutant.argtypes = []
         self.lib = lib
@@ -231,6 +242,55 @@ class Oracle:
             raise RuntimeError(f"oracle failed with status {rc}")
         return out
 
+    def _operands_w4(self, A, Wq4, bs, R):
+        A, lda = _rows(to_bits(A))
+        Wq4, ldw = _rows(to_codes(Wq4))
+        bs, ldbs = _rows(to_codes(bs))
+        R, ldr = _rows(to_bits(R))
+        M, K = A.shape
+        N = Wq4.shape[0]
+        if K % 2 or Wq4.shape[1] != K // 2 or bs.shape != (N, (K + 15) // 16) or R.shape != (M, N):
+            raise ValueError(f"shape mismatch: A{A.shape} Wq4{Wq4.shape} bs{bs.shape} R{R.shape}")
+        return A, lda, Wq4, ldw, bs, ldbs, R, ldr, M, N, K
+
+    def gemm_residual_w4(self, A, Wq4, bs, gs: float, R, threads: int | None = None) -> np.ndarray:
+        """Y = bf16_rne(gs * A . (e2m1(Wq4) * e4m3(bs))^T + R) as uint16 [M,N] (every element).
+
+        Wq4: [N, K/2] bytes of two E2M1 codes (element 2i in the low nibble);
+        bs: [N, ceil(K/16)] E4M3 block scales; gs: the tensor's float32 scale."""
+        A, lda, Wq4, ldw, bs, ldbs, R, ldr, M, N, K = self._operands_w4(A, Wq4, bs, R)
+        Y = np.empty((M, N), dtype=np.uint16)
+        threads = threads or os.cpu_count() or 1
+        rc = self.lib.sgr_ref_gemm_residual_w4(
+            self._p(A, ctypes.c_uint16), lda, self._p(Wq4, ctypes.c_uint8), ldw, self._p(bs, ctypes.c_uint8),
+            ldbs, float(np.float32(gs)), self._p(R, ctypes.c_uint16), ldr, self._p(Y, ctypes.c_uint16), N, M, N,
+            K, int(threads))
+        if rc != 0:
+            raise RuntimeError(f"oracle failed with status {rc}")
+        return Y
+
+    def sample_w4(self, A, Wq4, bs, gs: float, R, ms, ns) -> np.ndarray:
+        """Y[ms[i], ns[i]] of the NVFP4 variant, as uint16."""
+        A, lda, Wq4, ldw, bs, ldbs, R, ldr, M, N, K = self._operands_w4(A, Wq4, bs, R)
+        ms = np.ascontiguousarray(ms, dtype=np.int64)
+        ns = np.ascontiguousarray(ns, dtype=np.int64)
+        if ms.shape != ns.shape or ms.ndim != 1:
+            raise ValueError("ms and ns must be 1-D and of equal length")
+        out = np.empty(ms.shape, dtype=np.uint16)
+        rc = self.lib.sgr_ref_sample_w4(
+            self._p(A, ctypes.c_uint16), lda, self._p(Wq4, ctypes.c_uint8), ldw, self._p(bs, ctypes.c_uint8),
+            ldbs, float(np.float32(gs)), self._p(R, ctypes.c_uint16), ldr, M, N, K, self._p(ms, ctypes.c_long),
+            self._p(ns, ctypes.c_long), len(ms), self._p(out, ctypes.c_uint16))
+        if rc != 0:
+            raise RuntimeError(f"oracle failed with status {rc}")
+        return out
+
+    def e2m1_to_double(self, codes) -> np.ndarray:
+        """Values of 4-bit E2M1 codes (the low nibble of each uint8)."""
+        codes = np.ascontiguousarray(codes, dtype=np.uint8)
+        return np.array([self.lib.sgr_ref_e2m1_to_double(int(b)) for b in codes.ravel()]
+                        ).reshape(codes.shape)
+
     def e4m3_to_double(self, codes) -> np.ndarray:
         codes = np.ascontiguousarray(codes, dtype=np.uint8)
         return np.array([self.lib.sgr_ref_e4m3_to_double(int(b)) for b in codes.ravel()]
@@ -264,3 +324,7 @@ def gemm_residual(A, W, R, threads: int | None = None) -> np.ndarray:
 
 def gemm_residual_w8(A, Wq, scale, R, threads: int | None = None) -> np.ndarray:
     return load().gemm_residual_w8(A, Wq, scale, R, threads)
+
+
+def gemm_residual_w4(A, Wq4, bs, gs: float, R, threads: int | None = None) -> np.ndarray:
+    return load().gemm_residual_w4(A, Wq4, bs, gs, R, threads)

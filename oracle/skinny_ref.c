@@ -48,6 +48,21 @@
  * sum once (one FP64 rounding), then R is added and the double is rounded to
  * BF16 as above.
  *
+ * NVFP4 weight variant (sgr_ref_gemm_residual_w4): the pages name NVFP4
+ * weights (the bitsandbytes "QLORA-2" page's NVFP4 sm100 GEMM targets) without
+ * defining the format; the reading taken is the published NVFP4 layout: each
+ * weight is a 4-bit E2M1 code (sign, 2 exponent bits with bias 1, 1 fraction
+ * bit: magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6), two codes per byte with element
+ * 2i in the low nibble and 2i+1 in the high nibble; every 16 consecutive
+ * elements of a row share one E4M3 block scale; one FP32 scale covers the
+ * whole tensor:
+ *
+ *     Y[m,n] = bf16_rne( gs * sum_k A[m,k] * e2m1(Wq[n,k]) * e4m3(bs[n,k/16])  +  R[m,n] )
+ *
+ * Each product of a BF16 value, an E2M1 value and an E4M3 value is exact in
+ * double (8 + 2 + 4 significant bits); the sum runs in FP64 with k ascending;
+ * gs multiplies it once; R is added and the double is rounded to BF16 once.
+ *
  * SGR_REF_MUTANT (compile-time, default 0) plants one known mistake so that
  * the test suite can show its pins catch it; a normal build never sets it.
  */
@@ -97,6 +112,35 @@ static double e4m3_to_double(uint8_t b)
     mag = e == 0 ? ldexp(f, -9) : ldexp(8 + f, e - 10);
 #endif
     return s ? -mag : mag;
+}
+
+/*
+ * Exact E2M1 -> double for the 4-bit code in the low bits of c.  Fields: sign
+ * s (bit 3), exponent e (bits 2-1, bias 1), fraction f (bit 0).  e > 0:
+ * (1 + f/2) * 2^(e-1) = (2 + f) * 2^(e-2); e = 0: subnormal f/2.  The format
+ * has neither infinities nor NaN.
+ */
+static double e2m1_to_double(uint8_t c)
+{
+    int s = (c >> 3) & 1, e = (c >> 1) & 3, f = c & 1;
+    double mag;
+#if SGR_REF_MUTANT == 16
+    mag = ldexp(2 + f, e - 2);                /* planted: subnormals read as normals */
+#else
+    mag = e == 0 ? 0.5 * f : ldexp(2 + f, e - 2);
+#endif
+    return s ? -mag : mag;
+}
+
+/* Code of element k of a packed NVFP4 row (two codes per byte). */
+static uint8_t e2m1_code(const uint8_t *row, long k)
+{
+    uint8_t b = row[k >> 1];
+#if SGR_REF_MUTANT == 14
+    return (k & 1) ? (b & 15) : (b >> 4);    /* planted: nibble order swapped */
+#else
+    return (k & 1) ? (b >> 4) : (b & 15);
+#endif
 }
 
 /*
@@ -192,10 +236,35 @@ static double dot_w8_plus_residual(const uint16_t *a, const uint8_t *wq, float s
 #endif
 }
 
+/* The same for the NVFP4 variant:
+ * t = gs * sum_k a[k]*e2m1(code k)*e4m3(bs[k/16]) + r. */
+static double dot_w4_plus_residual(const uint16_t *a, const uint8_t *wq4, const uint8_t *bs, float gs,
+                                   uint16_t r, long K)
+{
+    double s = 0.0;
+    for (long k = 0; k < K; ++k) {
+#if SGR_REF_MUTANT == 15
+        double scale = e4m3_to_double(bs[k / 32]); /* planted: blocks of 32 */
+#else
+        double scale = e4m3_to_double(bs[k / 16]);
+#endif
+        s += bf16_to_double(a[k]) * e2m1_to_double(e2m1_code(wq4, k)) * scale;
+    }
+#if SGR_REF_MUTANT == 17
+    return (double)gs * (s + bf16_to_double(r)); /* planted: residual scaled too */
+#else
+    return (double)gs * s + bf16_to_double(r);
+#endif
+}
+
 typedef struct {
     const uint16_t *A, *W, *R;
     const uint8_t *Wq;    /* low-bit weights (W unused), or NULL */
     const float *scale;   /* per-column scales of Wq */
+    const uint8_t *Wq4;   /* NVFP4 codes (W, Wq unused), or NULL */
+    const uint8_t *bs;    /* E4M3 block scales of Wq4, row stride ldbs bytes */
+    long ldbs;
+    float gs;             /* tensor scale of Wq4 */
     uint16_t *Y;      /* rounded output, or NULL */
     double *T;        /* unrounded output, or NULL */
     long lda, ldw, ldr, ldy, ldt;
@@ -224,7 +293,10 @@ static void *ref_worker(void *p)
 #else
             long rrow = m;
 #endif
-            double t = j->Wq
+            double t = j->Wq4
+                ? dot_w4_plus_residual(j->A + m * j->lda, j->Wq4 + n * j->ldw, j->bs + n * j->ldbs, j->gs,
+                                       j->R[rrow * j->ldr + n], j->K)
+                : j->Wq
                 ? dot_w8_plus_residual(j->A + m * j->lda, j->Wq + n * j->ldw,
                                        column_scale(j->scale, n, j->N),
                                        j->R[rrow * j->ldr + n], j->K)
@@ -242,13 +314,16 @@ static void *ref_worker(void *p)
 
 /* Returns 0 on success, -1 on bad arguments, -2 if threads could not start,
  * -3 if the FP rounding mode is not round-to-nearest. */
-static int run_ref(const uint16_t *A, long lda, const uint16_t *W, const uint8_t *Wq,
-                   const float *scale, long ldw, const uint16_t *R, long ldr, uint16_t *Y,
-                   long ldy, double *T, long ldt, long M, long N, long K, int threads)
+static int run_ref4(const uint16_t *A, long lda, const uint16_t *W, const uint8_t *Wq,
+                    const float *scale, const uint8_t *Wq4, const uint8_t *bs, long ldbs, float gs,
+                    long ldw, const uint16_t *R, long ldr, uint16_t *Y, long ldy, double *T, long ldt,
+                    long M, long N, long K, int threads)
 {
-    if (!A || (!W && !(Wq && scale)) || !R || (!Y && !T) || M < 0 || N < 0 || K < 0)
+    if (!A || (!W && !(Wq && scale) && !(Wq4 && bs)) || !R || (!Y && !T) || M < 0 || N < 0 || K < 0)
         return -1;
-    if (lda < K || ldw < K || ldr < N || (Y && ldy < N) || (T && ldt < N))
+    if (Wq4 ? (K % 2 != 0 || ldw < K / 2 || ldbs < (K + 15) / 16) : ldw < K)
+        return -1;
+    if (lda < K || ldr < N || (Y && ldy < N) || (T && ldt < N))
         return -1;
     if (fegetround() != FE_TONEAREST)
         return -3;
@@ -263,7 +338,7 @@ static int run_ref(const uint16_t *A, long lda, const uint16_t *W, const uint8_t
     ref_job jobs[256];
     pthread_t tids[256];
     for (int i = 0; i < threads; ++i) {
-        ref_job j = {A, W, R, Wq, scale, Y, T, lda, ldw, ldr, ldy, ldt, M, K, N,
+        ref_job j = {A, W, R, Wq, scale, Wq4, bs, ldbs, gs, Y, T, lda, ldw, ldr, ldy, ldt, M, K, N,
                      N * i / threads, N * (i + 1) / threads};
         jobs[i] = j;
     }
@@ -280,6 +355,13 @@ static int run_ref(const uint16_t *A, long lda, const uint16_t *W, const uint8_t
     for (int i = 1; i <= started; ++i)
         pthread_join(tids[i], NULL);
     return rc;
+}
+
+static int run_ref(const uint16_t *A, long lda, const uint16_t *W, const uint8_t *Wq,
+                   const float *scale, long ldw, const uint16_t *R, long ldr, uint16_t *Y,
+                   long ldy, double *T, long ldt, long M, long N, long K, int threads)
+{
+    return run_ref4(A, lda, W, Wq, scale, NULL, NULL, 0, 0.0f, ldw, R, ldr, Y, ldy, T, ldt, M, N, K, threads);
 }
 
 /* Y = bf16_rne(A . W^T + R), every element. */
@@ -349,5 +431,39 @@ int sgr_ref_sample_w8(const uint16_t *A, long lda, const uint8_t *Wq, long ldw,
 }
 
 double sgr_ref_e4m3_to_double(uint8_t b) { return e4m3_to_double(b); }
+
+/* NVFP4 weights: Y = bf16_rne(gs * A . (e2m1(Wq4) * e4m3(bs))^T + R), every
+ * element.  Wq4 is [N, K/2] bytes (two codes each) with row stride ldw bytes;
+ * bs is [N, ceil(K/16)] E4M3 block scales with row stride ldbs bytes; K even. */
+int sgr_ref_gemm_residual_w4(const uint16_t *A, long lda, const uint8_t *Wq4, long ldw, const uint8_t *bs,
+                             long ldbs, float gs, const uint16_t *R, long ldr, uint16_t *Y, long ldy,
+                             long M, long N, long K, int threads)
+{
+    if (!Wq4 || !bs)
+        return -1;
+    return run_ref4(A, lda, NULL, NULL, NULL, Wq4, bs, ldbs, gs, ldw, R, ldr, Y, ldy, NULL, 0, M, N, K, threads);
+}
+
+/* Selected elements of the NVFP4 variant: out[i] = Y[ms[i], ns[i]]. */
+int sgr_ref_sample_w4(const uint16_t *A, long lda, const uint8_t *Wq4, long ldw, const uint8_t *bs, long ldbs,
+                      float gs, const uint16_t *R, long ldr, long M, long N, long K, const long *ms,
+                      const long *ns, long count, uint16_t *out)
+{
+    if (!A || !Wq4 || !bs || !R || !ms || !ns || !out || count < 0 || K % 2 != 0 || lda < K ||
+        ldw < K / 2 || ldbs < (K + 15) / 16 || ldr < N)
+        return -1;
+    if (fegetround() != FE_TONEAREST)
+        return -3;
+    for (long i = 0; i < count; ++i) {
+        long m = ms[i], n = ns[i];
+        if (m < 0 || m >= M || n < 0 || n >= N)
+            return -1;
+        out[i] = sgr_ref_round_bf16(
+            dot_w4_plus_residual(A + m * lda, Wq4 + n * ldw, bs + n * ldbs, gs, R[m * ldr + n], K));
+    }
+    return 0;
+}
+
+double sgr_ref_e2m1_to_double(uint8_t c) { return e2m1_to_double(c); }
 
 int sgr_ref_mutant(void) { return SGR_REF_MUTANT; }

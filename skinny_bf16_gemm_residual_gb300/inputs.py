@@ -162,3 +162,74 @@ def random_scales(n: int, seed: int, lo_exp: int = -12, hi_exp: int = 2) -> torc
     expo = torch.randint(lo_exp, hi_exp + 1, (n,), generator=g).to(torch.float64)
     frac = torch.randint(0, 1 << 23, (n,), generator=g).to(torch.float64)
     return ((1.0 + frac / float(1 << 23)) * torch.pow(2.0, expo)).to(torch.float32)
+
+
+@dataclass
+class ProblemW4:
+    """An NVFP4 weight problem: A [M,K] BF16; Wq4 [N,K/2] bytes (torch.uint8),
+    each holding two E2M1 codes (element 2i in the low nibble); bs
+    [N,ceil(K/16)] E4M3 block scales (torch.uint8); gs the tensor's float32
+    scale; R [M,N] BF16 (all CPU)."""
+
+    A: torch.Tensor
+    Wq4: torch.Tensor
+    bs: torch.Tensor
+    gs: float
+    R: torch.Tensor
+    seed: int
+
+    @property
+    def M(self) -> int:
+        return self.A.shape[0]
+
+    @property
+    def N(self) -> int:
+        return self.Wq4.shape[0]
+
+    @property
+    def K(self) -> int:
+        return self.A.shape[1]
+
+
+E2M1_MAX = 6.0
+_E2M1_LEVELS = torch.tensor([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], dtype=torch.float32)
+
+
+def make_problem_w4(M: int, N: int = N_LATENT_MOE, K: int = K_LATENT_MOE, seed: int = 0) -> ProblemW4:
+    """A, R ~ N(0,1) BF16 and NVFP4 weights of a W ~ N(0,1)/sqrt(K) (K even).
+
+    Draw order A, W, R as in ``make_problem``.  Quantisation of the float32 W
+    in blocks of 16 consecutive elements of a row: gs = max|W| / (6 * 448)
+    (1 for an all-zero W); each block's scale is torch's float32 ->
+    float8_e4m3fn cast of max|block| / (6 gs); each element's code is the
+    E2M1 value nearest to w / (scale gs) (the lower one on a tie), with the
+    sign of w: the NVFP4 weight quantisation that produces such operands."""
+    if K % 2:
+        raise ValueError("K must be even for packed 4-bit codes")
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    A = torch.randn((M, K), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    W = torch.randn((N, K), generator=g, dtype=torch.float32) * (1.0 / math.sqrt(K) if K > 0 else 1.0)
+    R = torch.randn((M, N), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    nb = (K + 15) // 16
+    Wp = torch.zeros((N, nb * 16), dtype=torch.float32)
+    Wp[:, :K] = W
+    amax = Wp.abs().reshape(N, nb, 16).amax(dim=2)
+    top = float(amax.max()) if amax.numel() else 0.0
+    gs = float(torch.tensor(top / (E2M1_MAX * E4M3_MAX) if top > 0 else 1.0, dtype=torch.float32))
+    bs = (amax / (E2M1_MAX * gs)).to(torch.float8_e4m3fn)
+    sval = bs.to(torch.float32).repeat_interleave(16, dim=1)[:, :K] * gs
+    x = torch.where(sval > 0, W / torch.where(sval > 0, sval, torch.ones_like(sval)), torch.zeros_like(W))
+    idx = (x.abs()[..., None] - _E2M1_LEVELS).abs().argmin(dim=-1)  # first (lower) level on a tie
+    codes = (idx | torch.where(x < 0, 8, 0)).to(torch.uint8)
+    Wq4 = (codes[:, 0::2] | (codes[:, 1::2] << 4)).to(torch.uint8)
+    return ProblemW4(A, Wq4.contiguous(), bs.view(torch.uint8).contiguous(), gs, R, seed)
+
+
+def random_e2m1_bytes(shape, seed: int) -> torch.Tensor:
+    """Uniformly random bytes (torch.uint8, CPU): two random E2M1 codes each,
+    every sign, exponent and fraction (zero, the subnormal 0.5 and -0 included)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    return torch.randint(0, 256, shape, generator=g, dtype=torch.int64).to(torch.uint8)
+

@@ -474,6 +474,180 @@ def check_w8_sample_matches_full(orc):
     _eq(orc.sample_w8(p.A, p.Wq, p.scale, p.R, ms, ns), full[ms, ns], "w8 sample")
 
 
+# ------------------------------------------------------------ NVFP4 pins
+def e2m1_value(code: int) -> Fraction:
+    """Exact value of a 4-bit E2M1 code from its fields (OCP MX v1.0 FP4)."""
+    s, e, f = (code >> 3) & 1, (code >> 1) & 3, code & 1
+    mag = Fraction(f, 2) if e == 0 else (1 + Fraction(f, 2)) * Fraction(2) ** (e - 1)
+    return -mag if s else mag
+
+
+def load_e2m1_fixture():
+    rows = []
+    with open(os.path.join(GOLDEN, "e2m1_codes.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                c, v = line.split()
+                rows.append((int(c, 16), float.fromhex(v)))
+    return rows
+
+
+def w4_codes(Wq4: np.ndarray) -> np.ndarray:
+    """[N, K/2] packed bytes -> [N, K] 4-bit codes (element 2i = low nibble)."""
+    out = np.empty((Wq4.shape[0], 2 * Wq4.shape[1]), dtype=np.uint8)
+    out[:, 0::2] = Wq4 & 15
+    out[:, 1::2] = Wq4 >> 4
+    return out
+
+
+def exact_reference_w4(A: np.ndarray, Wq4: np.ndarray, bs: np.ndarray, gs: float, R: np.ndarray) -> np.ndarray:
+    """Brute force in exact rationals:
+    Y[m,n] = rne(gs * sum_k A[m,k] e2m1(code[n,k]) e4m3(bs[n,k//16]) + R[m,n])."""
+    M, K = A.shape
+    N = Wq4.shape[0]
+    codes = w4_codes(Wq4)
+    out = np.empty((M, N), dtype=np.uint16)
+    g = Fraction(float(np.float32(gs)))
+    for m in range(M):
+        for n in range(N):
+            s = sum((bf16_value(int(A[m, k])) * e2m1_value(int(codes[n, k])) * e4m3_value(int(bs[n, k // 16]))
+                     for k in range(K)), Fraction(0))
+            out[m, n] = rne_bf16_exact(g * s + bf16_value(int(R[m, n])))
+    return out
+
+
+def load_crafted_w4_fixture():
+    cases, cur = [], None
+    with open(os.path.join(GOLDEN, "crafted_w4.txt")) as f:
+        for raw in f:
+            line = raw.strip()
+            if not line or line.startswith("#"):
+                continue
+            if line.startswith("case "):
+                cur = {"name": line[5:].split(":", 1)[0]}
+                cases.append(cur)
+            elif ":" not in line:
+                cur["M"], cur["N"], cur["K"] = (int(v) for v in line.split())
+            else:
+                key, vals = line.split(":", 1)
+                vals = vals.split()
+                if key == "Y":
+                    cur["Y"] = np.array([int(v, 16) for v in vals], dtype=np.uint16)
+                elif key in ("Wq4", "bs"):
+                    cur[key] = np.array([int(v, 16) for v in vals], dtype=np.uint8)
+                elif key == "gs":
+                    cur["gs"] = float(np.float32(float.fromhex(vals[0])))
+                else:
+                    f32 = np.array([float.fromhex(v) for v in vals], dtype=np.float32)
+                    cur[key] = bits(torch.from_numpy(f32).to(torch.bfloat16))
+    for c in cases:
+        c["A"] = c["A"].reshape(c["M"], c["K"])
+        c["Wq4"] = c["Wq4"].reshape(c["N"], c["K"] // 2)
+        c["bs"] = c["bs"].reshape(c["N"], (c["K"] + 15) // 16)
+        c["R"] = c["R"].reshape(c["M"], c["N"])
+        c["Y"] = c["Y"].reshape(c["M"], c["N"])
+    return cases
+
+
+def check_e2m1_fixture(orc):
+    rows = load_e2m1_fixture()
+    assert [c for c, _ in rows] == list(range(16)), "the fixture lists every 4-bit code"
+    got = orc.e2m1_to_double(np.array([c for c, _ in rows], dtype=np.uint8))
+    want = np.array([v for _, v in rows])
+    if not _same_float(got, want):
+        raise AssertionError(f"E2M1 fixture mismatch: {list(zip(got, want))}")
+    field = np.array([np.copysign(float(abs(e2m1_value(c))), -1.0 if c & 8 else 1.0) for c in range(16)])
+    if not _same_float(got, field):
+        raise AssertionError("E2M1 decode differs from the field formula")
+
+
+def check_w4_crafted_fixture(orc):
+    for c in load_crafted_w4_fixture():
+        _eq(orc.gemm_residual_w4(c["A"], c["Wq4"], c["bs"], c["gs"], c["R"], threads=1), c["Y"],
+            f"crafted w4 case {c['name']}")
+        _eq(exact_reference_w4(c["A"], c["Wq4"], c["bs"], c["gs"], c["R"]), c["Y"],
+            f"crafted w4 case {c['name']} (exact rationals)")
+
+
+def check_w4_brute_force_exact(orc):
+    """Tiny shapes with every code, random non-NaN block scales of both signs,
+    a random tensor scale, and K not a multiple of 16 (a partial last block):
+    oracle == exact rationals."""
+    for (M, N, K, seed) in ((2, 3, 32, 1), (1, 2, 48, 2), (3, 2, 16, 3), (2, 4, 2, 4), (1, 3, 38, 5)):
+        A = bits(inputs.random_bf16_bits((M, K), seed + 700, lo_exp=-6, hi_exp=4))
+        Wq4 = inputs.random_e2m1_bytes((N, K // 2), seed + 710).numpy()
+        bs = inputs.random_e4m3_codes((N, (K + 15) // 16), seed + 720).numpy()
+        gs = float(inputs.random_scales(1, seed + 730, lo_exp=-4, hi_exp=4)[0])
+        R = bits(inputs.random_bf16_bits((M, N), seed + 740, lo_exp=-6, hi_exp=6))
+        _eq(orc.gemm_residual_w4(A, Wq4, bs, gs, R, threads=2), exact_reference_w4(A, Wq4, bs, gs, R),
+            f"w4 brute force {M}x{N}x{K}")
+
+
+def _w4_decoded_bf16(Wq4: np.ndarray, bs: np.ndarray, gs: float) -> np.ndarray:
+    """e2m1(code) * e4m3(block scale) * gs as BF16 bits, built with torch's
+    float8_e4m3fn conversion and a table of the 16 E2M1 values; the caller
+    picks scales that keep every product exact in BF16."""
+    table = torch.tensor([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0, -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0],
+                         dtype=torch.float64)
+    codes = torch.from_numpy(w4_codes(Wq4).astype(np.int64))
+    K = codes.shape[1]
+    sc = torch.from_numpy(bs).view(torch.float8_e4m3fn).to(torch.float64)
+    sc_k = sc.repeat_interleave(16, dim=1)[:, :K]
+    Wf = table[codes] * sc_k * float(gs)
+    Wb = Wf.to(torch.float32).to(torch.bfloat16)
+    assert torch.equal(Wb.to(torch.float64), Wf), "decoded weights not exact in BF16"
+    return bits(Wb)
+
+
+def check_w4_unit_scales_is_bf16_gemm(orc):
+    """All block scales 1 and gs = 1: every E2M1 value is a BF16 value, so the
+    NVFP4 variant equals the pinned BF16 operation on the decoded weights."""
+    M, N, K = 4, 21, 160
+    A = bits(inputs.random_bf16_bits((M, K), 761, lo_exp=-4, hi_exp=4))
+    R = bits(inputs.random_bf16_bits((M, N), 762, lo_exp=-2, hi_exp=6))
+    Wq4 = inputs.random_e2m1_bytes((N, K // 2), 763).numpy()
+    bs = np.full((N, K // 16), 0x38, dtype=np.uint8)
+    _eq(orc.gemm_residual_w4(A, Wq4, bs, 1.0, R), orc.gemm_residual(A, _w4_decoded_bf16(Wq4, bs, 1.0), R),
+        "w4 unit scales")
+
+
+def check_w4_block_scales_as_bf16_gemm(orc):
+    """Power-of-two block scales (different per block and row) and a
+    power-of-two gs: equals the BF16 operation on e2m1 * scale * gs, which
+    pins the block indexing (k // 16) and the nibble order independently."""
+    M, N, K = 3, 12, 96
+    A = bits(inputs.random_bf16_bits((M, K), 771, lo_exp=-4, hi_exp=4))
+    R = bits(inputs.random_bf16_bits((M, N), 772))
+    Wq4 = inputs.random_e2m1_bytes((N, K // 2), 773).numpy()
+    g = torch.Generator().manual_seed(774)
+    e = torch.randint(-6, 7, (N, K // 16), generator=g)
+    bs = torch.pow(2.0, e.to(torch.float64)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    gs = 0.25
+    _eq(orc.gemm_residual_w4(A, Wq4, bs, gs, R), orc.gemm_residual(A, _w4_decoded_bf16(Wq4, bs, gs), R),
+        "w4 block scales")
+
+
+def check_w4_strided_rows(orc):
+    M, N, K = 2, 3, 32
+    A = bits(inputs.random_bf16_bits((M, 2 * K), 781))
+    Wq4 = inputs.random_e2m1_bytes((N, K), 782).numpy()            # row stride K bytes, codes in the second half
+    bs = inputs.random_e4m3_codes((N, 4), 783).numpy()             # row stride 4, scales in columns 2-3
+    R = bits(inputs.random_bf16_bits((M, 2 * N), 784))
+    a_v, w_v, b_v, r_v = A[:, K:], Wq4[:, K // 2:], bs[:, 2:], R[:, N:]
+    want = exact_reference_w4(np.ascontiguousarray(a_v), np.ascontiguousarray(w_v), np.ascontiguousarray(b_v),
+                              1.5, np.ascontiguousarray(r_v))
+    _eq(orc.gemm_residual_w4(a_v, w_v, b_v, 1.5, r_v), want, "w4 strided operands")
+
+
+def check_w4_sample_matches_full(orc):
+    p = inputs.make_problem_w4(3, N=40, K=64, seed=95)
+    full = orc.gemm_residual_w4(p.A, p.Wq4, p.bs, p.gs, p.R)
+    ms = np.array([0, 2, 1, 2, 0])
+    ns = np.array([0, 39, 17, 3, 21])
+    _eq(orc.sample_w4(p.A, p.Wq4, p.bs, p.gs, p.R, ms, ns), full[ms, ns], "w4 sample")
+
+
 ALL_CHECKS = [
     check_rounding_fixture,
     check_rounding_vs_exact_bisection,
@@ -495,4 +669,11 @@ ALL_CHECKS = [
     check_w8_power_of_two_scales,
     check_w8_strided_rows,
     check_w8_sample_matches_full,
+    check_e2m1_fixture,
+    check_w4_crafted_fixture,
+    check_w4_brute_force_exact,
+    check_w4_unit_scales_is_bf16_gemm,
+    check_w4_block_scales_as_bf16_gemm,
+    check_w4_strided_rows,
+    check_w4_sample_matches_full,
 ]

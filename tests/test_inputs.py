@@ -96,3 +96,45 @@ def test_wide_exponent_and_integer_generators_are_exact():
     assert torch.equal(x.to(torch.bfloat16).double(), x)
     i = inputs.integer_bf16((128, 64), -5, 9, seed=5).double()
     assert torch.equal(i, torch.round(i)) and int(i.min()) == -5 and int(i.max()) == 9
+
+
+def _w4_dequantised(q) -> torch.Tensor:
+    """e2m1(code) * e4m3(block scale) * gs from the fields (float64, [N, K])."""
+    lo, hi = (q.Wq4 & 15).long(), (q.Wq4 >> 4).long()
+    codes = torch.stack((lo, hi), dim=2).reshape(q.Wq4.shape[0], -1)
+    mag = torch.tensor([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], dtype=torch.float64)[codes & 7]
+    val = torch.where(codes >= 8, -mag, mag)
+    sc = q.bs.view(torch.float8_e4m3fn).double().repeat_interleave(16, dim=1)[:, :codes.shape[1]]
+    return val * sc * q.gs
+
+
+def test_nvfp4_problem_shares_the_bf16_draws():
+    """Draw order A, W, R as in the BF16 problem; the dequantised NVFP4 weights
+    are W to within half an E2M1 step of the block's scale (the largest step
+    is 2, between 4 and 6) plus the E4M3 rounding of that scale."""
+    p, q = inputs.make_problem(3, 64, 256, seed=5), inputs.make_problem_w4(3, 64, 256, seed=5)
+    assert same(p.A, q.A) and same(p.R, q.R)
+    deq = _w4_dequantised(q)
+    W = p.W.double()
+    blk = q.bs.view(torch.float8_e4m3fn).double().repeat_interleave(16, dim=1) * q.gs
+    bound = blk * 1.0 + W.abs() * (2.0 ** -3 + 2.0 ** -8)
+    assert bool(((deq - W).abs() <= bound).all())
+    cos = float((deq * W).sum() / (deq.norm() * W.norm()))
+    assert cos > 0.99
+
+
+def test_nvfp4_problem_layout_and_range():
+    q = inputs.make_problem_w4(2, 32, 512, seed=9)
+    assert q.Wq4.dtype == torch.uint8 and q.Wq4.shape == (32, 256)
+    assert q.bs.dtype == torch.uint8 and q.bs.shape == (32, 32)
+    assert not bool(((q.bs & 0x7F) == 0x7F).any()) and not bool((q.bs >= 0x80).any())  # finite, positive scales
+    assert q.gs > 0
+    codes = torch.cat(((q.Wq4 & 15), (q.Wq4 >> 4)))
+    assert len(set(torch.unique(codes).tolist())) >= 14  # both signs of every magnitude (up to +-0)
+    with pytest.raises(ValueError):
+        inputs.make_problem_w4(1, 8, 15, seed=0)  # odd K cannot be packed
+
+
+def test_random_e2m1_bytes_cover_every_code_pair():
+    b = inputs.random_e2m1_bytes((64, 256), seed=4)
+    assert b.dtype == torch.uint8 and set(torch.unique(b).tolist()) == set(range(256))
