@@ -617,6 +617,7 @@ def run_ours(args):
     chain = None if (args.skip_chain or rank != 0) else run_chain(sgr, device, stream)
     grouped = None if (args.skip_grouped or rank != 0) else run_grouped(sgr, device, stream)
     w8 = None if (args.skip_w8 or rank != 0) else run_w8(sgr, device, stream, peaks)
+    w4 = None if (args.skip_w4 or rank != 0) else run_w4(sgr, device, stream, peaks)
 
     if rank != 0:
         return 0
@@ -677,6 +678,7 @@ def run_ours(args):
         "chain": chain,
         "grouped": grouped,
         "w8": w8,
+        "w4": w4,
         "gpu_launches": repeats * args.steps * launches_per_step,
         "clocks": clk,
         "peaks": {"hbm_gbs": peaks["hbm_gbs"], "bf16_tflops": peaks["bf16_tflops"],
@@ -799,6 +801,48 @@ def run_w8(sgr, device, stream, peaks: dict, m_list=(1, 2, 4, 16), copies: int =
                     "M <= 4, the widening row-slab kernel above)"}
 
 
+def run_w4(sgr, device, stream, peaks: dict, m_list=(1, 2, 4, 16), copies: int = 8, replays: int = 50,
+           repeats: int = 9):
+    """NVFP4 weight leg: the same projection with E2M1 codes, one E4M3 scale
+    per 16 elements and an FP32 tensor scale (skinny_gemm_residual_w4).  Per
+    M, one CUDA graph of `copies` calls over distinct weight copies (8 x 14.5
+    MB, more than L2), PDL on.  Bytes per call = N*K/2 (codes) + N*K/16
+    (block scales) + 2MK + 4MN, times the kernel's passes of 4 tokens for the
+    weight part (each pass streams the weights)."""
+    import torch
+
+    from skinny_bf16_gemm_residual_gb300 import inputs
+
+    qs = [inputs.make_problem_w4(1, N_DIM, K_DIM, seed=7100 + c) for c in range(copies)]
+    Wq4 = [q.Wq4.to(device) for q in qs]
+    Bs = [q.bs.to(device) for q in qs]
+    rows = []
+    for M in m_list:
+        A = inputs.make_rows(M, K_DIM, seed=8100 + M).to(device)
+        R = inputs.make_rows(M, N_DIM, seed=9100 + M).to(device)
+        Y = torch.empty((M, N_DIM), dtype=torch.bfloat16, device=device)
+        calls = [lambda c=c: sgr.skinny_gemm_residual_w4(A, Wq4[c], Bs[c], qs[c].gs, R, Y, stream=stream)
+                 for c in range(copies)]
+        g = capture(calls, stream)
+        with torch.cuda.stream(stream):
+            for _ in range(5):
+                g.replay()
+        stream.synchronize()
+        us = summarize([t / copies for t in time_graph(g, stream, replays, repeats)])["median_us"]
+        del g
+        passes = (M + 3) // 4
+        wbytes = N_DIM * K_DIM // 2 + N_DIM * K_DIM // 16
+        nbytes = wbytes + 2 * M * K_DIM + 4 * M * N_DIM
+        gbs = nbytes / (us * 1e-6) / 1e9
+        rows.append({"m": M, "kernel": "simt_skinny_kernel<nvfp4>", "passes": passes, "us": us, "bytes": nbytes,
+                     "bytes_streamed": passes * wbytes + 2 * M * K_DIM + 4 * M * N_DIM, "gbs": gbs,
+                     "frac_of_hbm_peak": gbs / peaks["hbm_gbs"] if peaks.get("hbm_gbs") else None})
+    return {"per_m": rows,
+            "note": "NVFP4 weights (E2M1 codes, E4M3 scale per 16 elements, FP32 tensor scale), BF16 A/R/Y; graph "
+                    "of 8 calls over distinct weight copies; CUDA-core kernel, 4 tokens per pass; gbs counts each "
+                    "weight byte once (bytes_streamed counts every pass)"}
+
+
 def run_e2e(sgr, per_m, Ws, m_list, device, stream, steps: int):
     """Each step: one host->device copy of the step's inputs (A for every M,
     R for every call) from a pinned host buffer, the public call for every
@@ -901,6 +945,7 @@ def main(argv=None):
     ap.add_argument("--skip-chain", action="store_true", help="skip the 8-layer dependent chain leg")
     ap.add_argument("--skip-grouped", action="store_true", help="skip the mixture-of-experts grouped leg")
     ap.add_argument("--skip-w8", action="store_true", help="skip the FP8-weight leg")
+    ap.add_argument("--skip-w4", action="store_true", help="skip the NVFP4-weight leg")
     ap.add_argument("--skip-sweeps", action="store_true",
                     help="skip the transition (M = 32-128) and compute-bound (M = 256-1024) legs")
     ap.add_argument("--skip-cublas", action="store_true", help="skip the cuBLAS addmm rows of the per-M leg")

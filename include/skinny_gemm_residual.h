@@ -80,7 +80,7 @@
 extern "C" {
 #endif
 
-#define SGR_ABI_VERSION 8
+#define SGR_ABI_VERSION 9
 
 typedef enum {
   SGR_OK = 0,
@@ -342,6 +342,55 @@ int skinny_gemm_residual_w8(const void* A, int64_t lda, const void* Wq, int64_t 
 int sgr_validate_w8(const void* A, int64_t lda, const void* Wq, int64_t ldw,
                     const float* scale, const void* R, int64_t ldr, const void* Y,
                     int64_t ldy, int M, int N, int K);
+
+/*
+ * NVFP4 weights:
+ *
+ *     Y[m,n] = bf16( gs * sum_k A[m,k] * e2m1(Wq4[n,k]) * e4m3(bs[n,k/16]) + R[m,n] )
+ *
+ * with FP32 accumulation and one round-to-nearest-even: the NVFP4 weight
+ * format the bitsandbytes "QLORA-2" page builds GEMM targets for (its
+ * CMakeLists NVFP4 sm100 entries), read as the published layout: 4-bit E2M1
+ * codes (OCP MX FP4: sign, 2 exponent bits with bias 1, 1 fraction bit;
+ * magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6), two per byte with element 2i in the
+ * low nibble, one E4M3 scale per 16 consecutive elements of a row, and one
+ * FP32 scale gs for the whole tensor.  The weight bytes read per call are a
+ * quarter of the BF16 entry points' plus the block scales (1/16 of them).
+ *
+ *     A      [M, K]          BF16, row stride lda >= K (elements, multiple of 8)
+ *     Wq4    [N, K/2]        bytes of two E2M1 codes, row stride ldw >= K/2 bytes, a multiple of 16
+ *     bs     [N, ceil(K/16)] E4M3 block scales (one byte each, no NaN code), row stride ldbs bytes, a
+ *                            multiple of 16 and >= ceil(K/16) rounded up to 16: each row is read in
+ *                            16-byte units, padding included, so the buffer must hold that many bytes
+ *                            from the start of every row (the last row too)
+ *     gs     FP32 tensor scale (by value)
+ *     R, Y   [M, N]          BF16, row strides ldr, ldy >= N (multiples of 8)
+ *
+ * K a multiple of 32 (whole 32-code vectors) and at most 7168 (else
+ * SGR_ERR_UNSUPPORTED); M <= 256 (decode-sized batches; the kernel handles 4
+ * token rows per pass and runs ceil(M/4) passes, each streaming the
+ * weights).  Device pointers,
+ * ownership, asynchrony, PDL (Wq4 and bs are read before the dependency
+ * wait, like W), graph capture and errors as for skinny_gemm_residual_ex; in
+ * addition SGR_ERR_ALIGN for ldw or ldbs not a multiple of 16 or a
+ * misaligned Wq4 or bs, SGR_ERR_UNSUPPORTED for K not a multiple of 32, and
+ * SGR_ERR_ALIAS when Y overlaps Wq4 or bs.  `cfg` may be NULL; the kernel is
+ * the CUDA-core streaming kernel (SGR_PATH_SIMT or SGR_PATH_AUTO; cfg may set
+ * ctas_per_sm, rows_per_stage = weight rows per ring stage, stages).  Codes
+ * are converted to FP16 and multiplied by their block scale in FP16, which
+ * is exact (at most 6 significant bits, magnitudes 2^-10 .. 2688), then
+ * accumulated in FP32; the epilogue computes fmaf(sum, gs, R) and rounds once.
+ * Returns an sgr_status.
+ */
+int skinny_gemm_residual_w4(const void* A, int64_t lda, const void* Wq4, int64_t ldw,
+                            const void* bs, int64_t ldbs, float gs, const void* R, int64_t ldr,
+                            void* Y, int64_t ldy, int M, int N, int K, const sgr_config* cfg,
+                            unsigned flags, void* stream);
+
+/* Host-only argument check of skinny_gemm_residual_w4 (its exact rules). */
+int sgr_validate_w4(const void* A, int64_t lda, const void* Wq4, int64_t ldw, const void* bs,
+                    int64_t ldbs, const void* R, int64_t ldr, const void* Y, int64_t ldy,
+                    int M, int N, int K);
 
 /*
  * Self-test of the failure path of the kernels' bounded waits: on the

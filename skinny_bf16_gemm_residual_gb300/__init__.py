@@ -57,6 +57,9 @@ from .binding import (  # noqa: F401
     skinny_gemm_residual_w8,
     skinny_gemm_residual_w8_ptr,
     sgr_validate_w8_ptr,
+    skinny_gemm_residual_w4,
+    skinny_gemm_residual_w4_ptr,
+    sgr_validate_w4_ptr,
     sgr_selftest_wait_timeout,
     sgr_selftest_streamk_abort,
 )

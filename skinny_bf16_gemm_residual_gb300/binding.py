@@ -14,7 +14,7 @@ import threading
 
 from . import build as _build
 
-ABI_VERSION = 8  # must equal SGR_ABI_VERSION of the loaded library
+ABI_VERSION = 9  # must equal SGR_ABI_VERSION of the loaded library
 
 SGR_OK = 0
 SGR_ERR_NULL = 1
@@ -84,6 +84,8 @@ EXPORTS = (
     "skinny_gemm_residual_grouped",
     "skinny_gemm_residual_w8",
     "sgr_validate_w8",
+    "skinny_gemm_residual_w4",
+    "sgr_validate_w4",
     "sgr_selftest_wait_timeout",
     "sgr_selftest_streamk_abort",
 )
@@ -127,6 +129,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.skinny_gemm_residual_w8.argtypes = [vp, i64, vp, i64, fp, vp, i64, vp, i64, I, I, I,
                                                 ctypes.POINTER(sgr_config), U, vp]
         lib.sgr_validate_w8.argtypes = [vp, i64, vp, i64, fp, vp, i64, vp, i64, I, I, I]
+        lib.skinny_gemm_residual_w4.argtypes = [vp, i64, vp, i64, vp, i64, ctypes.c_float, vp, i64, vp, i64,
+                                                I, I, I, ctypes.POINTER(sgr_config), U, vp]
+        lib.sgr_validate_w4.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, vp, i64, I, I, I]
         lib.sgr_selftest_wait_timeout.argtypes = [U, ctypes.POINTER(ctypes.c_uint)]
         lib.sgr_selftest_streamk_abort.argtypes = [vp, vp, vp, vp, I, I, I, I, ctypes.POINTER(ctypes.c_uint)]
         for name in EXPORTS:
@@ -403,6 +408,65 @@ def skinny_gemm_residual_w8(A, Wq, scale, R, Y=None, flags: int = 0, stream=None
                                          _stream_handle(stream, dev))
     if rc != SGR_OK:
         raise SgrError(rc, "skinny_gemm_residual_w8")
+    return Y
+
+
+def sgr_validate_w4_ptr(A: int, lda: int, Wq4: int, ldw: int, bs: int, ldbs: int, R: int, ldr: int, Y: int,
+                        ldy: int, M: int, N: int, K: int) -> int:
+    """Host-only argument check of the NVFP4-weight entry point (no GPU needed)."""
+    return load().sgr_validate_w4(A, lda, Wq4, ldw, bs, ldbs, R, ldr, Y, ldy, M, N, K)
+
+
+def skinny_gemm_residual_w4_ptr(A: int, lda: int, Wq4: int, ldw: int, bs: int, ldbs: int, gs: float, R: int,
+                                ldr: int, Y: int, ldy: int, M: int, N: int, K: int, cfg: sgr_config | None,
+                                flags: int, stream: int) -> int:
+    """NVFP4-weight entry point on raw device addresses; returns the status."""
+    return load().skinny_gemm_residual_w4(A, lda, Wq4, ldw, bs, ldbs, float(gs), R, ldr, Y, ldy, M, N, K,
+                                          ctypes.byref(cfg) if cfg is not None else None, flags, stream)
+
+
+def skinny_gemm_residual_w4(A, Wq4, bs, gs: float, R, Y=None, flags: int = 0, stream=None,
+                            config: sgr_config | None = None):
+    """Y = bf16(gs * A . (e2m1(Wq4) * e4m3(bs))^T + R).
+
+    A [M,K], R and Y [M,N]: CUDA bf16 with unit inner stride (row strides
+    allowed).  Wq4 [N,K/2]: CUDA torch.uint8, two E2M1 codes per byte
+    (element 2i in the low nibble), unit inner stride, row stride a multiple
+    of 16 bytes.  bs [N,ceil(K/16)]: CUDA torch.uint8 or float8_e4m3fn block
+    scales, unit inner stride, row stride a multiple of 16 bytes and at least
+    ceil(K/16) rounded up to 16 (rows are read in 16-byte units).  gs: the
+    tensor's scale (a float).  Returns Y."""
+    import torch
+
+    for t, n in ((A, "A"), (R, "R")):
+        _check_tensor(t, n)
+    if Wq4.dtype != torch.uint8:
+        raise TypeError(f"Wq4 must be torch.uint8, got {Wq4.dtype}")
+    if bs.dtype not in (torch.uint8, torch.float8_e4m3fn):
+        raise TypeError(f"bs must be torch.uint8 or torch.float8_e4m3fn, got {bs.dtype}")
+    for t, n in ((Wq4, "Wq4"), (bs, "bs")):
+        if not t.is_cuda or t.dim() != 2 or (t.shape[1] > 1 and t.stride(1) != 1):
+            raise ValueError(f"{n} must be a 2-D CUDA tensor with unit inner stride")
+    if Y is None:
+        Y = torch.empty(R.shape, dtype=R.dtype, device=R.device)
+    _check_tensor(Y, "Y")
+    M, K = A.shape
+    N = Wq4.shape[0]
+    if (K % 2 or Wq4.shape[1] != K // 2 or tuple(bs.shape) != (N, (K + 15) // 16) or tuple(R.shape) != (M, N)
+            or tuple(Y.shape) != (M, N)):
+        raise ValueError(f"shape mismatch A{tuple(A.shape)} Wq4{tuple(Wq4.shape)} bs{tuple(bs.shape)} "
+                         f"R{tuple(R.shape)} Y{tuple(Y.shape)}")
+    padded = ((K + 15) // 16 + 15) // 16 * 16
+    ldbs = bs.stride(0) if N > 1 else padded
+    if K > 0 and N > 0 and bs.untyped_storage().nbytes() - bs.storage_offset() < (N - 1) * ldbs + padded:
+        raise ValueError("bs rows are read in 16-byte units: the buffer must hold the padding of the last row")
+    dev = _common_device((A, Wq4, bs, R, Y))
+    with torch.cuda.device(dev):
+        rc = skinny_gemm_residual_w4_ptr(A.data_ptr(), _ld(A), Wq4.data_ptr(), _ld(Wq4), bs.data_ptr(), ldbs,
+                                         float(gs), R.data_ptr(), _ld(R), Y.data_ptr(), _ld(Y), M, N, K, config,
+                                         flags, _stream_handle(stream, dev))
+    if rc != SGR_OK:
+        raise SgrError(rc, "skinny_gemm_residual_w4")
     return Y
 
 

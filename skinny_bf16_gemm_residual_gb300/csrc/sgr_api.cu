@@ -101,9 +101,9 @@ SimtFn simt_fn(int mt, int vpt) {
 template <int MT>
 SimtFn simt_w8_fn_vpt(int vpt) {
   switch (vpt) {
-    case 1: return sgr::simt_skinny_kernel<MT, 1, true>;
-    case 2: return sgr::simt_skinny_kernel<MT, 2, true>;
-    case 4: return sgr::simt_skinny_kernel<MT, 4, true>;
+    case 1: return sgr::simt_skinny_kernel<MT, 1, sgr::kWfE4m3>;
+    case 2: return sgr::simt_skinny_kernel<MT, 2, sgr::kWfE4m3>;
+    case 4: return sgr::simt_skinny_kernel<MT, 4, sgr::kWfE4m3>;
     default: return nullptr;
   }
 }
@@ -116,6 +116,27 @@ SimtFn simt_w8_fn(int mt, int vpt) {
     case 8: return simt_w8_fn_vpt<8>(vpt);
     default: return nullptr;
   }
+}
+
+// NVFP4-weight instantiations: at most 4 token rows per pass and one 32-code
+// vector per thread and row (K <= 7168), the register budget in which they
+// build without spills.
+constexpr int kW4PassM = 4;
+
+SimtFn simt_w4_fn(int mt, int vpt) {
+  if (vpt != 1) return nullptr;
+  switch (mt) {
+    case 1: return sgr::simt_skinny_kernel<1, 1, sgr::kWfNvfp4>;
+    case 2: return sgr::simt_skinny_kernel<2, 1, sgr::kWfNvfp4>;
+    case 4: return sgr::simt_skinny_kernel<4, 1, sgr::kWfNvfp4>;
+    default: return nullptr;
+  }
+}
+
+// 32-code vectors per row slice: K a multiple of 32, K <= 224 * 32.
+int simt_w4_vpt(int K) {
+  if (K % 32 != 0) return 0;
+  return K / 32 <= sgr::kSimtConsumers ? 1 : 0;
 }
 
 // 16-code vectors per row slice: K a multiple of 16, K <= 224 * 16 * 4.
@@ -223,6 +244,9 @@ int init_device(int dev) {
           ok = SGR_ERR_DEVICE;
         if (ok == SGR_OK && mt <= 8 &&
             sgr::set_kernel_smem_attrs(reinterpret_cast<const void*>(simt_w8_fn(mt, v))) != cudaSuccess)
+          ok = SGR_ERR_DEVICE;
+        if (ok == SGR_OK && mt <= kW4PassM && v == 1 &&
+            sgr::set_kernel_smem_attrs(reinterpret_cast<const void*>(simt_w4_fn(mt, v))) != cudaSuccess)
           ok = SGR_ERR_DEVICE;
       }
     if (ok == SGR_OK && sgr::tc_init_device(sms, &st.ws) != cudaSuccess) ok = SGR_ERR_DEVICE;
@@ -764,6 +788,164 @@ int run_w8(const void* A, long long lda, const void* Wq, long long ldw, const fl
                         (flags & SGR_FLAG_NO_PDL) == 0, stream);
 }
 
+// ------------------------------------------------------------ NVFP4 weights
+// Argument rules of skinny_gemm_residual_w4: those of the BF16 entry points
+// for A, R and Y; K a multiple of 32; Wq4 is [N, K/2] bytes with row stride
+// ldw (>= K/2, a multiple of 16, 16-byte aligned base); bs is
+// [N, ceil(K/16)] E4M3 block scales with row stride ldbs (a multiple of 16,
+// >= ceil(K/16) rounded up to 16: every row is read in 16-byte units,
+// padding included, so the buffer holds N rows of ldbs bytes or at least
+// (N - 1) ldbs + that many), 16-byte aligned base.
+long long w4_scale_row_bytes(int K) { return sgr::simt_w4_scale_bytes(K); }
+
+int validate_w4(const void* A, long long lda, const void* Wq4, long long ldw, const void* bs, long long ldbs,
+                const void* R, long long ldr, const void* Y, long long ldy, int M, int N, int K) {
+  if (M < 0 || N < 0 || K < 0) return SGR_ERR_SHAPE;
+  if (M == 0 || N == 0) return SGR_OK;
+  if (M > kMaxM || N > kMaxN || K > kMaxK) return SGR_ERR_UNSUPPORTED;
+  if (N % 8 != 0 || K % 8 != 0) return SGR_ERR_SHAPE;
+  if (!R || !Y) return SGR_ERR_NULL;
+  if (K > 0 && (!A || !Wq4 || !bs)) return SGR_ERR_NULL;
+  if (ldr < N || ldy < N) return SGR_ERR_SHAPE;
+  if (K > 0 && (lda < K || ldw < K / 2 || ldbs < w4_scale_row_bytes(K))) return SGR_ERR_SHAPE;
+  if (ldr > kMaxLd || ldy > kMaxLd || (K > 0 && (lda > kMaxLd || ldw > kMaxLd || ldbs > kMaxLd)))
+    return SGR_ERR_UNSUPPORTED;
+  if (ldr % 8 != 0 || ldy % 8 != 0 || (K > 0 && (lda % 8 != 0 || ldw % 16 != 0 || ldbs % 16 != 0)))
+    return SGR_ERR_ALIGN;
+  if (!aligned16(R) || !aligned16(Y)) return SGR_ERR_ALIGN;
+  if (K > 0 && (!aligned16(A) || !aligned16(Wq4) || !aligned16(bs))) return SGR_ERR_ALIGN;
+  if (K % 32 != 0) return SGR_ERR_UNSUPPORTED;  // whole 32-code vectors
+  const Extent ey = extent(Y, M, ldy, N);
+  if (K > 0) {
+    if (overlap(ey, extent(A, M, lda, K))) return SGR_ERR_ALIAS;
+    const uintptr_t wb = reinterpret_cast<uintptr_t>(Wq4);
+    if (overlap(ey, Extent{wb, wb + static_cast<uintptr_t>((long long)(N - 1) * ldw + K / 2)})) return SGR_ERR_ALIAS;
+    const uintptr_t sb = reinterpret_cast<uintptr_t>(bs);
+    if (overlap(ey, Extent{sb, sb + static_cast<uintptr_t>((long long)(N - 1) * ldbs + w4_scale_row_bytes(K))}))
+      return SGR_ERR_ALIAS;
+  }
+  const bool in_place = (Y == R) && (ldy == ldr);
+  if (!in_place && overlap(ey, extent(R, M, ldr, N))) return SGR_ERR_ALIAS;
+  return SGR_OK;
+}
+
+// CUDA-core NVFP4 configuration, the fastest measured at N = 7168, K = 3584
+// (graph of 8 calls over distinct weight copies): ring stages of four
+// records; two CTAs per SM with two stages for 1-2 tokens (10.5 / 12.1 us),
+// one CTA with eight stages for 3-4 tokens (23.7 us), where the FMAs and the
+// conversions, not the bytes, set the pace.
+void default_simt_w4_config(int M, sgr_config* c) {
+  std::memset(c, 0, sizeof *c);
+  c->path = SGR_PATH_SIMT;
+  c->ctas_per_sm = M <= 2 ? 2 : 1;
+  c->rows_per_stage = 4;
+  c->stages = M <= 2 ? 2 : 8;
+}
+
+size_t simt_w4_smem_bytes(int stages, int rows_per_stage, int K) {
+  return sgr::simt_ring_offset(stages) + (size_t)stages * rows_per_stage * sgr::simt_w4_record_bytes(K);
+}
+
+int resolve_config_w4(int M, int K, const sgr_config* in, sgr_config* out) {
+  const int path = in ? in->path : SGR_PATH_AUTO;
+  if (path != SGR_PATH_AUTO && path != SGR_PATH_SIMT) return SGR_ERR_UNSUPPORTED;
+  if (!simt_w4_vpt(K)) return SGR_ERR_UNSUPPORTED;
+  default_simt_w4_config(M < kW4PassM ? M : kW4PassM, out);
+  if (in) {
+    for (int r : in->reserved)
+      if (r != 0) return SGR_ERR_UNSUPPORTED;
+    if (in->tile_n || in->k_split || in->k_blocks_per_stage || in->token_tile || in->prefetch_stages)
+      return SGR_ERR_UNSUPPORTED;
+    if (in->ctas_per_sm) out->ctas_per_sm = in->ctas_per_sm;
+    if (in->rows_per_stage) out->rows_per_stage = in->rows_per_stage;
+    if (in->stages) out->stages = in->stages;
+  }
+  if (out->ctas_per_sm < 1 || out->ctas_per_sm > 8 || out->stages < 2 || out->stages > 16) return SGR_ERR_UNSUPPORTED;
+  if (out->rows_per_stage < 1 || out->rows_per_stage > 64) return SGR_ERR_UNSUPPORTED;
+  if (simt_w4_smem_bytes(out->stages, out->rows_per_stage, K) > (size_t)kMaxDynSmem) return SGR_ERR_UNSUPPORTED;
+  return SGR_OK;
+}
+
+// One pass over at most kW4PassM token rows.
+int launch_simt_w4(const sgr_config& c, int sms, unsigned* err, const void* A, long long lda, const void* Wq4,
+                   long long ldw, const void* bs, long long ldbs, float gs, const void* R, long long ldr, void* Y,
+                   long long ldy, int M, int N, int K, unsigned flags, cudaStream_t stream) {
+  SimtFn fn = simt_w4_fn(simt_mt(M), simt_w4_vpt(K));
+  if (!fn) return SGR_ERR_UNSUPPORTED;
+  sgr::SimtParams p;
+  std::memset(&p, 0, sizeof p);
+  p.A = static_cast<const __nv_bfloat16*>(A);
+  p.Wq = static_cast<const uint8_t*>(Wq4);
+  p.bs = static_cast<const uint8_t*>(bs);
+  p.ldw = ldw;
+  p.ldbs = ldbs;
+  p.gs = gs;
+  p.R = static_cast<const __nv_bfloat16*>(R);
+  p.Y = static_cast<__nv_bfloat16*>(Y);
+  p.lda = lda;
+  p.ldr = ldr;
+  p.ldy = ldy;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.rows_per_stage = c.rows_per_stage;
+  p.stages = c.stages;
+  p.err = err;
+  long long grid = (long long)sms * c.ctas_per_sm;
+  if (grid > N) grid = N;
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3((unsigned)grid, 1, 1);
+  lc.blockDim = dim3(sgr::kSimtThreads, 1, 1);
+  lc.dynamicSmemBytes = simt_w4_smem_bytes(c.stages, c.rows_per_stage, K);
+  lc.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = (flags & SGR_FLAG_NO_PDL) ? 0 : 1;
+  if (cudaLaunchKernelEx(&lc, fn, p) != cudaSuccess) {
+    cudaGetLastError();
+    return SGR_ERR_LAUNCH;
+  }
+  return SGR_OK;
+}
+
+constexpr int kW4MaxM = 256;  // decode-sized batches: at most 64 passes of 4 tokens
+
+int run_w4(const void* A, long long lda, const void* Wq4, long long ldw, const void* bs, long long ldbs, float gs,
+           const void* R, long long ldr, void* Y, long long ldy, int M, int N, int K, const sgr_config* cfg,
+           unsigned flags, void* stream_ptr) {
+  int rc = validate_w4(A, lda, Wq4, ldw, bs, ldbs, R, ldr, Y, ldy, M, N, K);
+  if (rc != SGR_OK) return rc;
+  if (M == 0 || N == 0) return SGR_OK;
+  if (M > kW4MaxM) return SGR_ERR_UNSUPPORTED;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  if (K == 0) {  // empty sum: Y = R
+    if (Y == R) return SGR_OK;
+    if (cudaMemcpy2DAsync(Y, (size_t)ldy * 2, R, (size_t)ldr * 2, (size_t)N * 2, (size_t)M,
+                          cudaMemcpyDeviceToDevice, stream) != cudaSuccess) {
+      cudaGetLastError();
+      return SGR_ERR_LAUNCH;
+    }
+    return SGR_OK;
+  }
+  sgr_config c;  // resolved before any device work: a refused configuration needs no GPU
+  if ((rc = resolve_config_w4(M, K, cfg, &c)) != SGR_OK) return rc;
+  int dev;
+  if ((rc = current_device(&dev)) != SGR_OK) return rc;
+  if ((rc = init_device(dev)) != SGR_OK) return rc;
+  DeviceState& st = g_dev[dev];
+  // Passes of at most kW4PassM token rows (each streams the weights again).
+  for (int m0 = 0; m0 < M; m0 += kW4PassM) {
+    const int mp = M - m0 < kW4PassM ? M - m0 : kW4PassM;
+    rc = launch_simt_w4(c, st.sms, st.err, static_cast<const __nv_bfloat16*>(A) + (size_t)m0 * lda, lda, Wq4, ldw,
+                        bs, ldbs, gs, static_cast<const __nv_bfloat16*>(R) + (size_t)m0 * ldr, ldr,
+                        static_cast<__nv_bfloat16*>(Y) + (size_t)m0 * ldy, ldy, mp, N, K, flags, stream);
+    if (rc != SGR_OK) return rc;
+  }
+  return SGR_OK;
+}
+
 // ------------------------------------------------------------ wait self-test
 // One thread waits on an mbarrier that nothing arrives on, with a limit of
 // `limit_ns` nanoseconds of %globaltimer instead of the kernels' one second,
@@ -1113,6 +1295,17 @@ int skinny_gemm_residual_w8(const void* A, int64_t lda, const void* Wq, int64_t 
 int sgr_validate_w8(const void* A, int64_t lda, const void* Wq, int64_t ldw, const float* scale, const void* R,
                     int64_t ldr, const void* Y, int64_t ldy, int M, int N, int K) {
   return validate_w8(A, lda, Wq, ldw, scale, R, ldr, Y, ldy, M, N, K);
+}
+
+int skinny_gemm_residual_w4(const void* A, int64_t lda, const void* Wq4, int64_t ldw, const void* bs, int64_t ldbs,
+                            float gs, const void* R, int64_t ldr, void* Y, int64_t ldy, int M, int N, int K,
+                            const sgr_config* cfg, unsigned flags, void* stream) {
+  return run_w4(A, lda, Wq4, ldw, bs, ldbs, gs, R, ldr, Y, ldy, M, N, K, cfg, flags, stream);
+}
+
+int sgr_validate_w4(const void* A, int64_t lda, const void* Wq4, int64_t ldw, const void* bs, int64_t ldbs,
+                    const void* R, int64_t ldr, const void* Y, int64_t ldy, int M, int N, int K) {
+  return validate_w4(A, lda, Wq4, ldw, bs, ldbs, R, ldr, Y, ldy, M, N, K);
 }
 
 int sgr_selftest_wait_timeout(unsigned limit_us, unsigned* code) { return run_selftest_wait(limit_us, code); }

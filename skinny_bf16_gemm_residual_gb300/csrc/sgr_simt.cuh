@@ -32,6 +32,15 @@
 // the bytes), each 16-byte vector holds 16 codes, which are widened exactly
 // in registers (sgr_e4m3.cuh) before the FP32 FMAs, and the epilogue computes
 // fmaf(sum, scale[n] * 2^8, R) with one rounding.
+//
+// The NVFP4 instantiation streams 4-bit E2M1 codes (two per byte, element 2i
+// in the low nibble) with one E4M3 scale per 16 elements of a row and one
+// FP32 scale for the tensor.  Each ring record is a row's K/2 code bytes
+// followed by its block scales (padded to 16 bytes); each 16-byte vector
+// holds 32 codes, converted two at a time to FP16 by the hardware conversion
+// and multiplied by their block scale in FP16 (exact: 2 x 4 significant bits,
+// magnitudes 2^-10 .. 2688), then widened to FP32 for the FMAs; the epilogue
+// computes fmaf(sum, gs, R) with one rounding.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -46,11 +55,22 @@ constexpr int kSimtConsumers = kSimtConsumerWarps * 32;  // 224 threads
 constexpr int kSimtThreads = kSimtConsumers + 32;        // + one producer warp
 constexpr int kSimtRPrefetch = 4;  // reduction batches whose residuals are loaded early
 
+// Weight formats of the kernel (template parameter WF).
+enum : int { kWfBf16 = 0, kWfE4m3 = 1, kWfNvfp4 = 2 };
+
+// Bytes of one NVFP4 ring record: a row's K/2 code bytes, then its ceil(K/16)
+// block scales padded to 16 bytes (K a multiple of 32).
+__host__ __device__ constexpr uint32_t simt_w4_scale_bytes(int K) { return (uint32_t)(((K + 15) / 16 + 15) / 16 * 16); }
+__host__ __device__ constexpr uint32_t simt_w4_record_bytes(int K) { return (uint32_t)(K / 2) + simt_w4_scale_bytes(K); }
+
 struct SimtParams {
   const __nv_bfloat16* A;  // [M, K], row stride lda (elements)
   const __nv_bfloat16* W;  // [N, K], contiguous rows (BF16 weights)
-  const uint8_t* Wq;       // [N, K], contiguous rows of E4M3 codes (W8 only)
-  const float* scale;      // [N] per-column scales (W8 only)
+  const uint8_t* Wq;       // E4M3: [N, K] contiguous rows of codes; NVFP4: [N, K/2] bytes, row stride ldw
+  const float* scale;      // [N] per-column scales (E4M3 only)
+  const uint8_t* bs;       // NVFP4: [N, ceil(K/16)] E4M3 block scales, row stride ldbs bytes
+  long long ldw, ldbs;     // NVFP4 row strides (bytes, multiples of 16)
+  float gs;                // NVFP4 tensor scale
   const __nv_bfloat16* R;  // [M, N], row stride ldr
   __nv_bfloat16* Y;        // [M, N], row stride ldy
   long long lda, ldr, ldy;
@@ -91,13 +111,30 @@ __device__ __forceinline__ float transpose_reduce32(float (&x)[32], int lane) {
   return x[0];
 }
 
+// Eight E2M1 codes (the nibbles of x, element 0 in the lowest) to four FP16
+// pairs, two codes per conversion (the byte's low nibble to the low half).
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t x, uint32_t (&h)[4]) {
+  asm("{\n\t.reg .b8 c0, c1, c2, c3;\n\t"
+      "mov.b32 {c0, c1, c2, c3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, c0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, c1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, c2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, c3;\n\t}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(x));
+}
+
 // MT: rows of A handled (M <= MT, rows >= M masked); VPT: 16-byte K vectors
-// per consumer thread (K <= 224 * EPV * VPT); W8: E4M3 codes + scales.
-template <int MT, int VPT, bool W8 = false>
-__global__ void __launch_bounds__(kSimtThreads, (MT <= 2 ? 3 : (MT <= 4 ? 2 : 1)))
+// per consumer thread (K <= 224 * EPV * VPT); WF: weight format (BF16, E4M3
+// codes + per-column scales, NVFP4 codes + block scales + tensor scale).
+template <int MT, int VPT, int WF = kWfBf16>
+__global__ void __launch_bounds__(kSimtThreads,
+                                  (WF == kWfNvfp4 ? (MT <= 2 ? 2 : 1) : (MT <= 2 ? 3 : (MT <= 4 ? 2 : 1))))
     simt_skinny_kernel(const SimtParams p) {
+  constexpr bool W8 = WF == kWfE4m3;
+  constexpr bool W4 = WF == kWfNvfp4;
   constexpr int B = 32 / MT;                      // rows per reduction batch
-  constexpr int EPV = W8 ? 16 : 8;                // weight elements per 16-byte vector
+  constexpr int EPV = W4 ? 32 : (W8 ? 16 : 8);    // weight elements per 16-byte vector
   constexpr bool kPackedA = MT * VPT * EPV > 64;  // keep A as bf16x2 when large
   extern __shared__ __align__(128) unsigned char smem[];
 
@@ -115,7 +152,7 @@ __global__ void __launch_bounds__(kSimtThreads, (MT <= 2 ? 3 : (MT <= 4 ? 2 : 1)
   const int n1 = (int)((long long)p.N * (c + 1) / G);
   const int nrows = n1 - n0;
   const int nstages = (nrows + RS - 1) / RS;
-  const int KV = W8 ? (p.K >> 4) : (p.K >> 3);
+  const int KV = W4 ? (p.K >> 5) : (W8 ? (p.K >> 4) : (p.K >> 3));
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -134,9 +171,13 @@ __global__ void __launch_bounds__(kSimtThreads, (MT <= 2 ? 3 : (MT <= 4 ? 2 : 1)
     // ---------------- producer: stream this CTA's W slab through the ring
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
-      const uint32_t row_bytes = (uint32_t)p.K * (W8 ? 1u : 2u);
+      const uint32_t row_bytes = W4 ? simt_w4_record_bytes(p.K) : (uint32_t)p.K * (W8 ? 1u : 2u);
       const char* wbase = (W8 ? reinterpret_cast<const char*>(p.Wq) : reinterpret_cast<const char*>(p.W)) +
                           (size_t)n0 * row_bytes;
+      // NVFP4: each record is gathered from the code row and the scale row.
+      const char* cbase = reinterpret_cast<const char*>(p.Wq) + (W4 ? (size_t)n0 * (size_t)p.ldw : 0);
+      const char* sbase = reinterpret_cast<const char*>(p.bs) + (W4 ? (size_t)n0 * (size_t)p.ldbs : 0);
+      const uint32_t code_bytes = (uint32_t)(p.K / 2), scale_bytes = simt_w4_scale_bytes(p.K);
       // Ring position kept by increments: no integer division on the
       // per-stage path of this single issuing thread.
       int issued = 0;
@@ -155,7 +196,18 @@ __global__ void __launch_bounds__(kSimtThreads, (MT <= 2 ? 3 : (MT <= 4 ? 2 : 1)
         const uint32_t bytes = left < RS ? (uint32_t)left * row_bytes : stage_bytes;
         const uint32_t fb = smem_u32(&full[slot]);
         mbar_arrive_expect_tx(fb, bytes);
-        bulk_g2s(dst, src, bytes, fb, pol);
+        if constexpr (W4) {
+          const int rows = left < RS ? left : RS;
+          for (int r = 0; r < rows; ++r) {
+            const uint32_t d = dst + (uint32_t)r * row_bytes;
+            bulk_g2s(d, cbase, code_bytes, fb, pol);
+            bulk_g2s(d + code_bytes, sbase, scale_bytes, fb, pol);
+            cbase += p.ldw;
+            sbase += p.ldbs;
+          }
+        } else {
+          bulk_g2s(dst, src, bytes, fb, pol);
+        }
         issued = s + 1;
         left -= RS;
         src += stage_bytes;
@@ -209,7 +261,7 @@ __global__ void __launch_bounds__(kSimtThreads, (MT <= 2 ? 3 : (MT <= 4 ? 2 : 1)
   // on memory (warp 0 stores; lane l handles output l of each batch).
   constexpr int kB = 32 / MT;
   float rpre[kSimtRPrefetch];
-  float spre[W8 ? kSimtRPrefetch : 1];  // scales * 2^8 of the same outputs (W8)
+  float spre[W8 ? kSimtRPrefetch : 1];  // scales * 2^8 of the same outputs (E4M3)
 #pragma unroll
   for (int b = 0; b < kSimtRPrefetch; ++b) {
     const int j = lane / MT, m = lane % MT, row = b * kB + j;
@@ -225,7 +277,8 @@ __global__ void __launch_bounds__(kSimtThreads, (MT <= 2 ? 3 : (MT <= 4 ? 2 : 1)
   int slot = 0, rr = 0;   // ring slot of the current stage, row within the stage
   uint32_t phase = 0;     // parity of the current stage's fill of that slot
   const uint32_t ring_base = smem_u32(ring);
-  const uint32_t row_bytes = (uint32_t)p.K * (W8 ? 1u : 2u);
+  const uint32_t row_bytes = W4 ? simt_w4_record_bytes(p.K) : (uint32_t)p.K * (W8 ? 1u : 2u);
+  const uint32_t code_bytes = (uint32_t)(p.K / 2);  // NVFP4: block scales follow the codes
   uint32_t row_addr = ring_base;
   for (int base = 0; base < nrows; base += B, ++bi) {
     float acc[32];
@@ -245,6 +298,47 @@ __global__ void __launch_bounds__(kSimtThreads, (MT <= 2 ? 3 : (MT <= 4 ? 2 : 1)
             const int vid = threadIdx.x + v * kSimtConsumers;
             if (vid < KV) {
               const uint4 q = lds128(row_addr + (uint32_t)vid * 16u);
+              if constexpr (W4) {
+                // Block scales of codes [0, 16) and [16, 32) of this vector, as FP16.
+                uint16_t sc2;
+                asm volatile("ld.shared.u16 %0, [%1];" : "=h"(sc2) : "r"(row_addr + code_bytes + (uint32_t)vid * 2u));
+                uint32_t s16, s0, s1;
+                asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(s16) : "h"(sc2));
+                asm("prmt.b32 %0, %1, %1, 0x1010;" : "=r"(s0) : "r"(s16));  // {scale 0, scale 0}
+                asm("prmt.b32 %0, %1, %1, 0x3232;" : "=r"(s1) : "r"(s16));  // {scale 1, scale 1}
+                const uint32_t x[4] = {q.x, q.y, q.z, q.w};
+                // One 8-code word at a time: decode, then its FMAs for every token.
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  uint32_t hx[4];
+                  e2m1x8_to_f16x2(x[i], hx);
+                  float w8[8];
+#pragma unroll
+                  for (int b = 0; b < 4; ++b) {
+                    uint32_t h = hx[b];
+                    asm("mul.rn.f16x2 %0, %0, %1;" : "+r"(h) : "r"(i < 2 ? s0 : s1));  // exact
+                    asm("{\n\t.reg .b16 l, u;\n\tmov.b32 {l, u}, %2;\n\t"
+                        "cvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, u;\n\t}"
+                        : "=f"(w8[2 * b]), "=f"(w8[2 * b + 1]) : "r"(h));
+                  }
+#pragma unroll
+                  for (int m = 0; m < MT; ++m) {
+                    float t = acc[j * MT + m];
+                    if constexpr (kPackedA) {
+#pragma unroll
+                      for (int e = 0; e < 4; ++e) {
+                        t = fmaf(bf16lo(ap[m][v][4 * i + e]), w8[2 * e], t);
+                        t = fmaf(bf16hi(ap[m][v][4 * i + e]), w8[2 * e + 1], t);
+                      }
+                    } else {
+#pragma unroll
+                      for (int e = 0; e < 8; ++e) t = fmaf(af[m][v][8 * i + e], w8[e], t);
+                    }
+                    acc[j * MT + m] = t;
+                  }
+                }
+              } else {
+              float w[EPV];
               uint32_t wp[EPV / 2];  // weights as BF16 pairs
               if constexpr (W8) {
                 const uint32_t x[4] = {q.x, q.y, q.z, q.w};
@@ -256,7 +350,6 @@ __global__ void __launch_bounds__(kSimtThreads, (MT <= 2 ? 3 : (MT <= 4 ? 2 : 1)
               } else {
                 wp[0] = q.x; wp[1] = q.y; wp[2] = q.z; wp[3] = q.w;
               }
-              float w[EPV];
 #pragma unroll
               for (int i = 0; i < EPV / 2; ++i) {
                 w[2 * i] = bf16lo(wp[i]);
@@ -276,6 +369,7 @@ __global__ void __launch_bounds__(kSimtThreads, (MT <= 2 ? 3 : (MT <= 4 ? 2 : 1)
                   for (int e = 0; e < EPV; ++e) t = fmaf(af[m][v][e], w[e], t);
                 }
                 acc[j * MT + m] = t;
+              }
               }
             }
           }
@@ -321,6 +415,8 @@ __global__ void __launch_bounds__(kSimtThreads, (MT <= 2 ? 3 : (MT <= 4 ? 2 : 1)
             if (k == bi) sc = spre[k];
           if (bi >= kSimtRPrefetch) sc = p.scale[n] * kE4m3Unscale;
           p.Y[(size_t)m * p.ldy + n] = __float2bfloat16_rn(fmaf(total, sc, r));
+        } else if constexpr (W4) {
+          p.Y[(size_t)m * p.ldy + n] = __float2bfloat16_rn(fmaf(total, p.gs, r));
         } else {
           p.Y[(size_t)m * p.ldy + n] = __float2bfloat16_rn(total + r);
         }

@@ -193,6 +193,7 @@ class ProblemW4:
 
 E2M1_MAX = 6.0
 _E2M1_LEVELS = torch.tensor([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], dtype=torch.float32)
+_E2M1_MIDPOINTS = (_E2M1_LEVELS[1:] + _E2M1_LEVELS[:-1]) / 2
 
 
 def make_problem_w4(M: int, N: int = N_LATENT_MOE, K: int = K_LATENT_MOE, seed: int = 0) -> ProblemW4:
@@ -220,7 +221,9 @@ def make_problem_w4(M: int, N: int = N_LATENT_MOE, K: int = K_LATENT_MOE, seed: 
     bs = (amax / (E2M1_MAX * gs)).to(torch.float8_e4m3fn)
     sval = bs.to(torch.float32).repeat_interleave(16, dim=1)[:, :K] * gs
     x = torch.where(sval > 0, W / torch.where(sval > 0, sval, torch.ones_like(sval)), torch.zeros_like(W))
-    idx = (x.abs()[..., None] - _E2M1_LEVELS).abs().argmin(dim=-1)  # first (lower) level on a tie
+    # Nearest level: the number of level midpoints strictly below |x| (the
+    # lower level on a tie).
+    idx = torch.searchsorted(_E2M1_MIDPOINTS, x.abs().contiguous(), right=False)
     codes = (idx | torch.where(x < 0, 8, 0)).to(torch.uint8)
     Wq4 = (codes[:, 0::2] | (codes[:, 1::2] << 4)).to(torch.uint8)
     return ProblemW4(A, Wq4.contiguous(), bs.view(torch.uint8).contiguous(), gs, R, seed)

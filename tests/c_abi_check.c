@@ -44,6 +44,15 @@ int main(void) {
          "validate_w8 code stride");
   expect(sgr_validate_w8(A, K, W, K, NULL, R, N, Y, N, M, N, K), SGR_ERR_NULL, "validate_w8 null scale");
 
+  expect(sgr_validate_w4(A, K, W, K / 2, S, K / 16, R, N, Y, N, M, N, K), SGR_OK, "validate_w4 ok");
+  expect(sgr_validate_w4(A, K, W, K / 2 + 8, S, K / 16, R, N, Y, N, M, N, K), SGR_ERR_ALIGN,
+         "validate_w4 code stride");
+  expect(sgr_validate_w4(A, K, W, K / 2, NULL, K / 16, R, N, Y, N, M, N, K), SGR_ERR_NULL,
+         "validate_w4 null block scales");
+  expect(skinny_gemm_residual_w4(NULL, K, NULL, K / 2, NULL, K / 16, 1.0f, NULL, N, NULL, N, 0, N, K, NULL, 0u,
+                                 NULL),
+         SGR_OK, "w4 M = 0 no-op");
+
   /* Empty problems and empty groups return before touching a device. */
   expect(skinny_gemm_residual(NULL, NULL, NULL, NULL, 0, N, K, NULL), SGR_OK, "M = 0 no-op");
   expect(skinny_gemm_residual_grouped(NULL, 0, N, K, NULL, 0u, NULL), SGR_OK, "no groups");

@@ -294,3 +294,59 @@ def test_w8_config_rejections_need_no_device():
                                              cfg, 0, 0)
     assert rc == sgr.SGR_OK  # M = 0: nothing to do, nothing checked further
     assert lib.sgr_validate_w8(None, 3584, None, 3584, None, None, 7168, None, 7168, 4, 7168, 3584) == sgr.SGR_ERR_NULL
+
+
+# ------------------------------------------------------------ NVFP4-weight entry point (host-side checks only)
+B_ = BASE + (5 << 32)
+
+
+def v4(A=A_, lda=3584, Wq4=W_, ldw=1792, bs=B_, ldbs=224, R=R_, ldr=7168, Y=Y_, ldy=7168, M=4, N=7168, K=3584):
+    return sgr.sgr_validate_w4_ptr(A, lda, Wq4, ldw, bs, ldbs, R, ldr, Y, ldy, M, N, K)
+
+
+def test_validate_w4_accepts_good_arguments():
+    assert v4() == sgr.SGR_OK
+    assert v4(M=256, ldw=1808, ldbs=240) == sgr.SGR_OK   # padded code and scale rows (multiples of 16 bytes)
+    assert v4(Y=R_) == sgr.SGR_OK                         # in-place residual
+    assert v4(M=0, A=0, Wq4=0, bs=0, R=0, Y=0) == sgr.SGR_OK
+    assert v4(K=0, A=0, Wq4=0, bs=0) == sgr.SGR_OK        # empty sum: Y = R
+    assert v4(K=1056, lda=1056, ldw=528, ldbs=80) == sgr.SGR_OK  # 66 scales per row, read as 80 bytes
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(M=-1), sgr.SGR_ERR_SHAPE),
+    (dict(K=3580, lda=3584), sgr.SGR_ERR_SHAPE),          # K not a multiple of 8
+    (dict(K=3592, lda=3592, ldw=1808, ldbs=240), sgr.SGR_ERR_UNSUPPORTED),  # K not a multiple of 32
+    (dict(Wq4=0), sgr.SGR_ERR_NULL),
+    (dict(bs=0), sgr.SGR_ERR_NULL),
+    (dict(ldw=1776), sgr.SGR_ERR_SHAPE),                  # fewer than K/2 bytes per code row
+    (dict(K=1056, lda=1056, ldw=528, ldbs=66), sgr.SGR_ERR_SHAPE),  # scale rows not padded to 16 bytes
+    (dict(ldw=1800), sgr.SGR_ERR_ALIGN),                  # row stride not a multiple of 16 bytes
+    (dict(ldbs=232), sgr.SGR_ERR_ALIGN),
+    (dict(Wq4=W_ + 8), sgr.SGR_ERR_ALIGN),
+    (dict(bs=B_ + 4), sgr.SGR_ERR_ALIGN),
+    (dict(Y=W_ + 4096), sgr.SGR_ERR_ALIAS),               # Y inside the codes
+    (dict(Y=B_ + 4096), sgr.SGR_ERR_ALIAS),               # Y inside the scales
+    (dict(Y=A_), sgr.SGR_ERR_ALIAS),
+    (dict(Y=R_ + 16), sgr.SGR_ERR_ALIAS),
+    (dict(ldbs=(1 << 36) + 16), sgr.SGR_ERR_UNSUPPORTED),
+])
+def test_validate_w4_rejects(kw, status):
+    assert v4(**kw) == status
+
+
+def test_w4_config_and_size_rejections_need_no_device():
+    """A tensor-core path, tile-only fields, M above 256 or K above 7168 are
+    refused before any launch (M = 0 is a no-op whatever the configuration)."""
+    lib = sgr.load()
+    cfg = sgr.make_config(path=sgr.SGR_PATH_TILE)
+    assert binding.skinny_gemm_residual_w4_ptr(A_, 3584, W_, 1792, B_, 224, 1.0, R_, 7168, Y_, 7168, 0, 7168, 3584,
+                                               cfg, 0, 0) == sgr.SGR_OK
+    assert lib.sgr_validate_w4(None, 3584, None, 1792, None, 224, None, 7168, None, 7168, 4, 7168, 3584) == \
+        sgr.SGR_ERR_NULL
+    call = lambda M, K, c: binding.skinny_gemm_residual_w4_ptr(A_, K, W_, K // 2, B_, ((K // 16 + 15) // 16) * 16, 1.0,
+                                                                R_, 7168, Y_, 7168, M, 7168, K, c, 0, 0)
+    assert call(4, 3584, cfg) == sgr.SGR_ERR_UNSUPPORTED                          # tile path
+    assert call(4, 3584, sgr.make_config(k_split=2)) == sgr.SGR_ERR_UNSUPPORTED   # tile-only field
+    assert call(257, 3584, None) == sgr.SGR_ERR_UNSUPPORTED                       # more than 256 tokens
+    assert call(4, 7200, None) == sgr.SGR_ERR_UNSUPPORTED                         # K above 7168
