@@ -807,8 +807,7 @@ def run_w4(sgr, device, stream, peaks: dict, m_list=(1, 2, 4, 16), copies: int =
     per 16 elements and an FP32 tensor scale (skinny_gemm_residual_w4).  Per
     M, one CUDA graph of `copies` calls over distinct weight copies (8 x 14.5
     MB, more than L2), PDL on.  Bytes per call = N*K/2 (codes) + N*K/16
-    (block scales) + 2MK + 4MN, times the kernel's passes of 4 tokens for the
-    weight part (each pass streams the weights)."""
+    (block scales) + 2MK + 4MN."""
     import torch
 
     from skinny_bf16_gemm_residual_gb300 import inputs
@@ -830,17 +829,18 @@ def run_w4(sgr, device, stream, peaks: dict, m_list=(1, 2, 4, 16), copies: int =
         stream.synchronize()
         us = summarize([t / copies for t in time_graph(g, stream, replays, repeats)])["median_us"]
         del g
-        passes = (M + 3) // 4
+        passes = (M + 3) // 4 if M <= 1 else (M + 127) // 128  # CUDA-core kernel: 4 tokens per pass
         wbytes = N_DIM * K_DIM // 2 + N_DIM * K_DIM // 16
         nbytes = wbytes + 2 * M * K_DIM + 4 * M * N_DIM
         gbs = nbytes / (us * 1e-6) / 1e9
-        rows.append({"m": M, "kernel": "simt_skinny_kernel<nvfp4>", "passes": passes, "us": us, "bytes": nbytes,
+        rows.append({"m": M, "kernel": "simt_skinny_kernel<nvfp4>" if M <= 1 else "w8_rows_kernel<nvfp4>",
+                     "passes": passes, "us": us, "bytes": nbytes,
                      "bytes_streamed": passes * wbytes + 2 * M * K_DIM + 4 * M * N_DIM, "gbs": gbs,
                      "frac_of_hbm_peak": gbs / peaks["hbm_gbs"] if peaks.get("hbm_gbs") else None})
     return {"per_m": rows,
             "note": "NVFP4 weights (E2M1 codes, E4M3 scale per 16 elements, FP32 tensor scale), BF16 A/R/Y; graph "
-                    "of 8 calls over distinct weight copies; CUDA-core kernel, 4 tokens per pass; gbs counts each "
-                    "weight byte once (bytes_streamed counts every pass)"}
+                    "of 8 calls over distinct weight copies; the library's choice: CUDA-core kernel for M = 1, "
+                    "tensor-core widening kernel above; gbs counts each weight byte once"}
 
 
 def run_e2e(sgr, per_m, Ws, m_list, device, stream, steps: int):

@@ -102,8 +102,8 @@ typedef enum {
 #define SGR_PATH_TC 2      /* tcgen05 kernel, persistent stream-K with split-K fixup */
 #define SGR_PATH_TC_ROWS 3 /* tcgen05 kernel, one contiguous W row slab per CTA (M <= 256) */
 #define SGR_PATH_TILE 4    /* tcgen05 kernel, 128-token x tile_n output tiles (large M) */
-#define SGR_PATH_W8 5      /* tcgen05 row-slab kernel for FP8 weights (skinny_gemm_residual_w8 only, M <= 256);
-                              skinny_gemm_residual_w8 also takes SGR_PATH_SIMT (CUDA-core kernel, M <= 8) */
+#define SGR_PATH_W8 5      /* tcgen05 row-slab kernel for low-bit weights, widened on chip (skinny_gemm_residual_w8
+                              and _w4 only, M <= 256); both also take SGR_PATH_SIMT (CUDA-core kernel) */
 #define SGR_PATH_PAIR 6    /* tcgen05 tile kernel on 2-CTA clusters (cta_group::2), 256-token x tile_n tiles (large M) */
 #define SGR_PATH_W8S 7     /* FP8 weights on the FP8 tensor-core path (kind::f8f6f4), activations split exactly into
                               two E4M3 parts (skinny_gemm_residual_w8 only, M <= 16) */
@@ -366,21 +366,26 @@ int sgr_validate_w8(const void* A, int64_t lda, const void* Wq, int64_t ldw,
  *     gs     FP32 tensor scale (by value)
  *     R, Y   [M, N]          BF16, row strides ldr, ldy >= N (multiples of 8)
  *
- * K a multiple of 32 (whole 32-code vectors) and at most 7168 (else
- * SGR_ERR_UNSUPPORTED); M <= 256 (decode-sized batches; the kernel handles 4
- * token rows per pass and runs ceil(M/4) passes, each streaming the
- * weights).  Device pointers,
+ * M <= 256 (decode-sized batches), N and K multiples of 8.  Device pointers,
  * ownership, asynchrony, PDL (Wq4 and bs are read before the dependency
  * wait, like W), graph capture and errors as for skinny_gemm_residual_ex; in
  * addition SGR_ERR_ALIGN for ldw or ldbs not a multiple of 16 or a
- * misaligned Wq4 or bs, SGR_ERR_UNSUPPORTED for K not a multiple of 32, and
- * SGR_ERR_ALIAS when Y overlaps Wq4 or bs.  `cfg` may be NULL; the kernel is
- * the CUDA-core streaming kernel (SGR_PATH_SIMT or SGR_PATH_AUTO; cfg may set
- * ctas_per_sm, rows_per_stage = weight rows per ring stage, stages).  Codes
- * are converted to FP16 and multiplied by their block scale in FP16, which
- * is exact (at most 6 significant bits, magnitudes 2^-10 .. 2688), then
- * accumulated in FP32; the epilogue computes fmaf(sum, gs, R) and rounds once.
- * Returns an sgr_status.
+ * misaligned Wq4 or bs, and SGR_ERR_ALIAS when Y overlaps Wq4 or bs.  `cfg`
+ * may be NULL (library choice).  Two kernels, both exact in the conversion
+ * (a code times its block scale has at most 6 significant bits and lies in
+ * [2^-10, 2688], so FP16 and BF16 hold it exactly) and accumulating in FP32:
+ * SGR_PATH_W8, the tensor-core row-slab kernel (one launch per 128 tokens;
+ * the codes are converted to BF16 times their block scale on chip and fed to
+ * BF16 MMAs from tensor memory; cfg may set stages = depth of the code ring
+ * 2..16, prefetch_stages = depth of the activation ring 2..8,
+ * k_blocks_per_stage = 64-wide K blocks per stage, 4 or 8, token_tile, and
+ * rows_per_stage = W rows per CTA), and SGR_PATH_SIMT, the CUDA-core kernel
+ * (K a multiple of 32 and at most 7168; 4 token rows per pass, ceil(M/4)
+ * passes, each streaming the weights; cfg may set ctas_per_sm,
+ * rows_per_stage = weight rows per ring stage, stages).  SGR_PATH_AUTO takes
+ * the CUDA-core kernel for M = 1 where it can run, else the tensor-core
+ * kernel.  The epilogue computes fmaf(sum, gs, R) and rounds once.  Returns
+ * an sgr_status.
  */
 int skinny_gemm_residual_w4(const void* A, int64_t lda, const void* Wq4, int64_t ldw,
                             const void* bs, int64_t ldbs, float gs, const void* R, int64_t ldr,

@@ -814,7 +814,6 @@ int validate_w4(const void* A, long long lda, const void* Wq4, long long ldw, co
     return SGR_ERR_ALIGN;
   if (!aligned16(R) || !aligned16(Y)) return SGR_ERR_ALIGN;
   if (K > 0 && (!aligned16(A) || !aligned16(Wq4) || !aligned16(bs))) return SGR_ERR_ALIGN;
-  if (K % 32 != 0) return SGR_ERR_UNSUPPORTED;  // whole 32-code vectors
   const Extent ey = extent(Y, M, ldy, N);
   if (K > 0) {
     if (overlap(ey, extent(A, M, lda, K))) return SGR_ERR_ALIAS;
@@ -846,24 +845,62 @@ size_t simt_w4_smem_bytes(int stages, int rows_per_stage, int K) {
   return sgr::simt_ring_offset(stages) + (size_t)stages * rows_per_stage * sgr::simt_w4_record_bytes(K);
 }
 
-int resolve_config_w4(int M, int K, const sgr_config* in, sgr_config* out) {
-  const int path = in ? in->path : SGR_PATH_AUTO;
-  if (path != SGR_PATH_AUTO && path != SGR_PATH_SIMT) return SGR_ERR_UNSUPPORTED;
-  if (!simt_w4_vpt(K)) return SGR_ERR_UNSUPPORTED;
-  default_simt_w4_config(M < kW4PassM ? M : kW4PassM, out);
+// The library takes the CUDA-core kernel up to this many tokens where it can
+// run (K a multiple of 32, at most 7168), the tensor-core widening kernel
+// otherwise (measured at N = 7168, K = 3584, graph of 8 calls: 10.5 against
+// 11.1 us at M = 1; 12.1 against 11.2 at M = 2; the tensor-core kernel flat
+// at 11.1-11.5 us up to M = 16, the CUDA-core one 23.7 / 46.7 / 92.9 us at
+// M = 4 / 8 / 16).
+constexpr int kW4SimtMaxM = 1;
+// Tokens per launch of the tensor-core NVFP4 kernel: its activation ring of
+// two 4-block stages holds at most 128 token rows in shared memory.
+constexpr int kW4TcPassM = 128;
+
+// The path of an NVFP4 call, decided without a device: SGR_PATH_SIMT or
+// SGR_PATH_W8 (the tensor-core widening kernel); 0 when refused.
+int w4_path(int M, int K, const sgr_config* in) {
+  int path = in ? in->path : SGR_PATH_AUTO;
   if (in) {
     for (int r : in->reserved)
-      if (r != 0) return SGR_ERR_UNSUPPORTED;
-    if (in->tile_n || in->k_split || in->k_blocks_per_stage || in->token_tile || in->prefetch_stages)
-      return SGR_ERR_UNSUPPORTED;
+      if (r != 0) return 0;
+    if (in->tile_n || in->k_split) return 0;
+  }
+  if (path == SGR_PATH_AUTO) path = (M <= kW4SimtMaxM && simt_w4_vpt(K)) ? SGR_PATH_SIMT : SGR_PATH_W8;
+  if (path == SGR_PATH_SIMT && !simt_w4_vpt(K)) return 0;
+  return (path == SGR_PATH_SIMT || path == SGR_PATH_W8) ? path : 0;
+}
+
+int resolve_config_w4(int sms, int M, int N, int K, const sgr_config* in, sgr_config* out) {
+  const int path = w4_path(M, K, in);
+  if (!path) return SGR_ERR_UNSUPPORTED;
+  if (path == SGR_PATH_SIMT) {
+    default_simt_w4_config(M < kW4PassM ? M : kW4PassM, out);
+    if (in) {
+      if (in->k_blocks_per_stage || in->token_tile || in->prefetch_stages) return SGR_ERR_UNSUPPORTED;
+      if (in->ctas_per_sm) out->ctas_per_sm = in->ctas_per_sm;
+      if (in->rows_per_stage) out->rows_per_stage = in->rows_per_stage;
+      if (in->stages) out->stages = in->stages;
+    }
+    if (out->ctas_per_sm < 1 || out->ctas_per_sm > 8 || out->stages < 2 || out->stages > 16) return SGR_ERR_UNSUPPORTED;
+    if (out->rows_per_stage < 1 || out->rows_per_stage > 64) return SGR_ERR_UNSUPPORTED;
+    if (simt_w4_smem_bytes(out->stages, out->rows_per_stage, K) > (size_t)kMaxDynSmem) return SGR_ERR_UNSUPPORTED;
+    return SGR_OK;
+  }
+  M = M < kW4TcPassM ? M : kW4TcPassM;  // one pass
+  if (!sgr::w8_supported(sms, M, N, K)) return SGR_ERR_UNSUPPORTED;
+  sgr::w8_default_config(sms, M, N, K, out, true);
+  if (in) {
     if (in->ctas_per_sm) out->ctas_per_sm = in->ctas_per_sm;
     if (in->rows_per_stage) out->rows_per_stage = in->rows_per_stage;
     if (in->stages) out->stages = in->stages;
+    if (in->k_blocks_per_stage) out->k_blocks_per_stage = in->k_blocks_per_stage;
+    if (in->token_tile) out->token_tile = in->token_tile;
+    if (in->prefetch_stages) out->prefetch_stages = in->prefetch_stages;
   }
-  if (out->ctas_per_sm < 1 || out->ctas_per_sm > 8 || out->stages < 2 || out->stages > 16) return SGR_ERR_UNSUPPORTED;
-  if (out->rows_per_stage < 1 || out->rows_per_stage > 64) return SGR_ERR_UNSUPPORTED;
-  if (simt_w4_smem_bytes(out->stages, out->rows_per_stage, K) > (size_t)kMaxDynSmem) return SGR_ERR_UNSUPPORTED;
-  return SGR_OK;
+  sgr::W8Params p;
+  int grid = 0;
+  size_t smem = 0;
+  return sgr::w8_plan(*out, sms, M, N, K, &p, &grid, &smem, true);
 }
 
 // One pass over at most kW4PassM token rows.
@@ -929,12 +966,27 @@ int run_w4(const void* A, long long lda, const void* Wq4, long long ldw, const v
     }
     return SGR_OK;
   }
-  sgr_config c;  // resolved before any device work: a refused configuration needs no GPU
-  if ((rc = resolve_config_w4(M, K, cfg, &c)) != SGR_OK) return rc;
+  if (!w4_path(M, K, cfg)) return SGR_ERR_UNSUPPORTED;  // refused before any device work
   int dev;
   if ((rc = current_device(&dev)) != SGR_OK) return rc;
   if ((rc = init_device(dev)) != SGR_OK) return rc;
   DeviceState& st = g_dev[dev];
+  sgr_config c;
+  if ((rc = resolve_config_w4(st.sms, M, N, K, cfg, &c)) != SGR_OK) return rc;
+  if (c.path == SGR_PATH_W8) {
+    // Passes of at most kW4TcPassM token rows (one for M <= 128).
+    for (int m0 = 0; m0 < M; m0 += kW4TcPassM) {
+      const int mp = M - m0 < kW4TcPassM ? M - m0 : kW4TcPassM;
+      sgr_config cp = c;
+      if (mp < M && (!cfg || !cfg->token_tile)) cp.token_tile = (mp + 15) / 16 * 16;
+      rc = sgr::w4_launch(cp, st.sms, st.err, static_cast<const __nv_bfloat16*>(A) + (size_t)m0 * lda, lda, Wq4,
+                          ldw, bs, ldbs, gs, static_cast<const __nv_bfloat16*>(R) + (size_t)m0 * ldr, ldr,
+                          static_cast<__nv_bfloat16*>(Y) + (size_t)m0 * ldy, ldy, mp, N, K,
+                          (flags & SGR_FLAG_NO_PDL) == 0, stream);
+      if (rc != SGR_OK) return rc;
+    }
+    return SGR_OK;
+  }
   // Passes of at most kW4PassM token rows (each streams the weights again).
   for (int m0 = 0; m0 < M; m0 += kW4PassM) {
     const int mp = M - m0 < kW4PassM ? M - m0 : kW4PassM;
@@ -1205,7 +1257,7 @@ int sgr_kernel_resources(int device, int path, int M, int N, int K, int* regs, i
     *smem_bytes = (int)smem;
     *threads = sgr::kRowsThreads;
   } else if (c.path == SGR_PATH_W8) {
-    if (cudaFuncGetAttributes(&fa, sgr::w8_rows_kernel) != cudaSuccess) {
+    if (cudaFuncGetAttributes(&fa, sgr::w8_rows_kernel<false>) != cudaSuccess) {
       cudaGetLastError();
       return SGR_ERR_DEVICE;
     }

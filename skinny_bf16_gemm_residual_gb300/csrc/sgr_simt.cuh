@@ -111,19 +111,6 @@ __device__ __forceinline__ float transpose_reduce32(float (&x)[32], int lane) {
   return x[0];
 }
 
-// Eight E2M1 codes (the nibbles of x, element 0 in the lowest) to four FP16
-// pairs, two codes per conversion (the byte's low nibble to the low half).
-__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t x, uint32_t (&h)[4]) {
-  asm("{\n\t.reg .b8 c0, c1, c2, c3;\n\t"
-      "mov.b32 {c0, c1, c2, c3}, %4;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %0, c0;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %1, c1;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %2, c2;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %3, c3;\n\t}"
-      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
-      : "r"(x));
-}
-
 // MT: rows of A handled (M <= MT, rows >= M masked); VPT: 16-byte K vectors
 // per consumer thread (K <= 224 * EPV * VPT); WF: weight format (BF16, E4M3
 // codes + per-column scales, NVFP4 codes + block scales + tensor scale).
@@ -302,10 +289,8 @@ __global__ void __launch_bounds__(kSimtThreads,
                 // Block scales of codes [0, 16) and [16, 32) of this vector, as FP16.
                 uint16_t sc2;
                 asm volatile("ld.shared.u16 %0, [%1];" : "=h"(sc2) : "r"(row_addr + code_bytes + (uint32_t)vid * 2u));
-                uint32_t s16, s0, s1;
-                asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(s16) : "h"(sc2));
-                asm("prmt.b32 %0, %1, %1, 0x1010;" : "=r"(s0) : "r"(s16));  // {scale 0, scale 0}
-                asm("prmt.b32 %0, %1, %1, 0x3232;" : "=r"(s1) : "r"(s16));  // {scale 1, scale 1}
+                uint32_t s0, s1;
+                e4m3x2_block_scales_f16(sc2, s0, s1);
                 const uint32_t x[4] = {q.x, q.y, q.z, q.w};
                 // One 8-code word at a time: decode, then its FMAs for every token.
 #pragma unroll

@@ -28,6 +28,15 @@
 // (0x7F, 0xFF) are outside the supported domain: a saturating quantiser never
 // writes them, and the kernel reads them as +-480.
 //
+// The NVFP4 instantiation (FP4 = true) runs the same pipeline on 4-bit E2M1
+// codes (two per byte, element 2i in the low nibble) with one E4M3 scale per
+// 16 elements and one FP32 tensor scale: a 128-byte box row holds 256 codes
+// (four 64-wide K blocks); each stage also brings the RB rows' block scales of
+// its K range (a small unswizzled box, counted on the same barrier); a
+// converter lane widens its 32 codes with the hardware E2M1 -> FP16
+// conversion, multiplies each pair by its block scale in FP16 and rounds to
+// BF16, all exact (sgr_e4m3.cuh); the epilogue multiplies by the tensor scale.
+//
 // Warp roles (352 threads): warp 0 lane 0 streams the weight codes with TMA
 // into their own ring, released by the converters (the codes do not depend on
 // the preceding kernel, so they stream from the start); warp 10 lane 0 loads
@@ -63,14 +72,15 @@ constexpr int kW8MaxWins = 8;     // MMA windows per stage (kbps / groups)
 struct W8Params {
   const __nv_bfloat16* R;
   __nv_bfloat16* Y;
-  const float* scale;
+  const float* scale;  // E4M3: per-column scales (NVFP4: unused)
+  float gs;            // NVFP4: tensor scale
   long long ldr, ldy;
   unsigned* err;
   int M, N, K;
   int RB;          // W rows per CTA (multiple of 8, <= 128)
   int NT;          // token tile = MMA N per group (multiple of 16, >= M)
   int k_stages;    // ceil(K / (64 * kbps))
-  int kbps;        // 64-wide K blocks per stage (even)
+  int kbps;        // 64-wide K blocks per stage (even; NVFP4: 4 or 8)
   int stages;      // depth of the weight-code ring
   int a_stages;    // depth of the activation ring
   int groups;      // K blocks packed into one MMA window (1, 2 or 4)
@@ -81,11 +91,21 @@ struct W8Params {
 };
 
 __host__ __device__ inline uint32_t w8_wstage_bytes(int kbps, int rb) { return (uint32_t)(kbps / 2) * rb * 128u; }
+// NVFP4 stage: kbps/4 code boxes (RB rows x 256 codes), then the RB rows'
+// block scales (kbps * 4 bytes each), rounded up to keep the next stage's
+// swizzled boxes 1024-byte aligned.
+__host__ __device__ inline uint32_t w4_scale_off(int kbps, int rb) { return (uint32_t)(kbps / 4) * rb * 128u; }
+__host__ __device__ inline uint32_t w4_wstage_bytes(int kbps, int rb) {
+  return (w4_scale_off(kbps, rb) + (uint32_t)rb * kbps * 4u + 1023u) & ~1023u;
+}
+__host__ __device__ inline uint32_t wring_stage_bytes(bool fp4, int kbps, int rb) {
+  return fp4 ? w4_wstage_bytes(kbps, rb) : w8_wstage_bytes(kbps, rb);
+}
 __host__ __device__ inline uint32_t w8_astage_bytes(int kbps, int nt) { return (uint32_t)kbps * nt * 128u; }
 __host__ __device__ inline uint32_t w8_rtile_bytes(int rb, int nt) { return ((uint32_t)rb * nt * 2u + 1023u) & ~1023u; }
 
-__host__ __device__ inline size_t w8_smem_bytes(int stages, int a_stages, int kbps, int rb, int nt) {
-  return 1024 /* alignment slack */ + 1024 /* barriers */ + (size_t)stages * w8_wstage_bytes(kbps, rb) +
+__host__ __device__ inline size_t w8_smem_bytes(int stages, int a_stages, int kbps, int rb, int nt, bool fp4 = false) {
+  return 1024 /* alignment slack */ + 1024 /* barriers */ + (size_t)stages * wring_stage_bytes(fp4, kbps, rb) +
          (size_t)a_stages * w8_astage_bytes(kbps, nt) + w8_rtile_bytes(rb, nt);
 }
 
@@ -99,9 +119,12 @@ __device__ __forceinline__ void w8_widen32(const uint32_t (&x)[8], uint32_t (&o)
   }
 }
 
+// tmS: the NVFP4 block scales (unused, any map, for E4M3).
+template <bool FP4>
 __global__ void __launch_bounds__(kW8Threads, 2)
     w8_rows_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA,
-                   const __grid_constant__ CUtensorMap tmR, const W8Params p) {
+                   const __grid_constant__ CUtensorMap tmR, const __grid_constant__ CUtensorMap tmS,
+                   const W8Params p) {
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -118,9 +141,11 @@ __global__ void __launch_bounds__(kW8Threads, 2)
   uint64_t* rfull = drain + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rfull + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  const uint32_t wbox = (uint32_t)p.RB * 128u;  // one weight box: RB rows x 128 codes
+  const uint32_t wbox = (uint32_t)p.RB * 128u;  // one weight box: RB rows x 128 bytes (128 or 256 codes)
   const uint32_t ablk = (uint32_t)p.NT * 128u;  // one activation box: NT rows x 64 BF16
-  const uint32_t w_stage = w8_wstage_bytes(p.kbps, p.RB);
+  const uint32_t w_stage = wring_stage_bytes(FP4, p.kbps, p.RB);
+  const uint32_t sc_off = w4_scale_off(p.kbps, p.RB);           // NVFP4: block scales within a stage
+  const uint32_t sc_row = (uint32_t)p.kbps * 4u;                 // NVFP4: block-scale bytes per row and stage
   const uint32_t a_stage = w8_astage_bytes(p.kbps, p.NT);
   const uint32_t w_ring = base + 1024;
   const uint32_t a_ring = w_ring + (uint32_t)S * w_stage;
@@ -163,6 +188,7 @@ __global__ void __launch_bounds__(kW8Threads, 2)
     prefetch_tmap(&tmW);
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmR);
+    if (FP4) prefetch_tmap(&tmS);
   }
   tc_fence_before();
   __syncthreads();
@@ -186,10 +212,18 @@ __global__ void __launch_bounds__(kW8Threads, 2)
           break;
         }
         const uint32_t wb = smem_u32(&wfull[slot]);
-        mbar_arrive_expect_tx(wb, w_stage);
-        for (int j = 0; j < p.kbps / 2; ++j)
-          tma_load_2d(w_ring + (uint32_t)slot * w_stage + (uint32_t)j * wbox, &tmW, (s * p.kbps + 2 * j) * kTcKBlock,
-                      n0, wb, pol_w);
+        const uint32_t st = w_ring + (uint32_t)slot * w_stage;
+        if constexpr (FP4) {
+          // kbps/4 boxes of 256 codes (128 bytes) per row, then the block scales.
+          mbar_arrive_expect_tx(wb, sc_off + (uint32_t)p.RB * sc_row);
+          for (int j = 0; j < p.kbps / 4; ++j)
+            tma_load_2d(st + (uint32_t)j * wbox, &tmW, (s * p.kbps + 4 * j) * (kTcKBlock / 2), n0, wb, pol_w);
+          tma_load_2d(st + sc_off, &tmS, s * p.kbps * 4, n0, wb, pol_w);
+        } else {
+          mbar_arrive_expect_tx(wb, w_stage);
+          for (int j = 0; j < p.kbps / 2; ++j)
+            tma_load_2d(st + (uint32_t)j * wbox, &tmW, (s * p.kbps + 2 * j) * kTcKBlock, n0, wb, pol_w);
+        }
         issued = s + 1;
         if (++slot == S) {
           slot = 0;
@@ -293,7 +327,7 @@ __global__ void __launch_bounds__(kW8Threads, 2)
     const bool epi = half == 0;
     // Scale of the output column this lane may own (a weight: readable before the dependency wait).
     const bool owner = epi && L < p.RB && n0 + L < p.N;
-    const float sc = owner ? p.scale[n0 + L] * kE4m3Unscale : 0.f;
+    const float sc = owner ? (FP4 ? p.gs : p.scale[n0 + L] * kE4m3Unscale) : 0.f;
     if (q * 32 < G * p.RB) {  // warp-uniform: the quarter holds rows of the window
       int g = L / p.RB, r = L - g * p.RB;
       if (g >= G) {  // lanes past the window duplicate a real row (their TMEM rows are never read)
@@ -314,18 +348,33 @@ __global__ void __launch_bounds__(kW8Threads, 2)
         if (!ok) break;
         // Windows are read and widened two at a time (independent work for
         // the scheduler to overlap) and stored into this stage's slot.
-        const uint32_t ws = w_ring + (uint32_t)slot * w_stage + row_off;
+        const uint32_t wst = w_ring + (uint32_t)slot * w_stage;
+        const uint32_t ws = wst + row_off;
         for (int w0 = 0; w0 < wins; w0 += 2) {
           uint32_t o[2][16];
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
             const int kb = (w0 + u < wins ? w0 + u : w0) * G + g;  // K block of this lane within the stage
-            const uint32_t c0 = (uint32_t)((kb & 1) * 4 + half * 2);  // first 16-byte chunk of the row
-            const uint32_t rowp = ws + (uint32_t)(kb >> 1) * wbox;
-            const uint4 v0 = lds128(rowp + ((c0 ^ swz) << 4));
-            const uint4 v1 = lds128(rowp + (((c0 + 1u) ^ swz) << 4));
-            const uint32_t x[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-            w8_widen32(x, o[u]);
+            if constexpr (FP4) {
+              // 32 codes = one 16-byte chunk of the 128-byte row of box kb/4,
+              // and their two block scales.
+              const uint32_t c = (uint32_t)((kb & 3) * 2 + half);
+              const uint4 v = lds128(ws + (uint32_t)(kb >> 2) * wbox + ((c ^ swz) << 4));
+              uint16_t sc2;
+              asm volatile("ld.shared.u16 %0, [%1];"
+                           : "=h"(sc2)
+                           : "r"(wst + sc_off + (uint32_t)r * sc_row + (uint32_t)kb * 4u + (uint32_t)half * 2u));
+              uint32_t s0, s1;
+              e4m3x2_block_scales_f16(sc2, s0, s1);
+              w4_widen32(v, s0, s1, o[u]);
+            } else {
+              const uint32_t c0 = (uint32_t)((kb & 1) * 4 + half * 2);  // first 16-byte chunk of the row
+              const uint32_t rowp = ws + (uint32_t)(kb >> 1) * wbox;
+              const uint4 v0 = lds128(rowp + ((c0 ^ swz) << 4));
+              const uint4 v1 = lds128(rowp + (((c0 + 1u) ^ swz) << 4));
+              const uint32_t x[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+              w8_widen32(x, o[u]);
+            }
           }
           if (w0 + 2 >= wins) {  // the stage's codes are all in registers
             __syncwarp();
@@ -470,7 +519,7 @@ __global__ void __launch_bounds__(kW8Threads, 2)
             const int rr = item % p.RB, c16 = item / p.RB;
             const int n = n0 + rr;
             if (n >= p.N) continue;
-            const float scn = p.scale[n] * kE4m3Unscale;
+            const float scn = FP4 ? p.gs : p.scale[n] * kE4m3Unscale;
             float acc[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) acc[i] = 0.f;
@@ -525,6 +574,21 @@ inline bool make_tmap_u8(CUtensorMap* m, const void* ptr, long long rows, long l
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A byte matrix [rows, cols] (row stride ld bytes) in boxes of box_rows x
+// box_cols bytes without swizzle (the NVFP4 block scales: read per row).
+inline bool make_tmap_u8_plain(CUtensorMap* m, const void* ptr, long long rows, long long cols, long long ld,
+                               int box_rows, int box_cols) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld};
+  cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // The same over BF16 [rows, cols] (row stride ld elements), no swizzle: the
 // residual tile is read row by row from shared memory.
 inline bool make_tmap_plain_bf16(CUtensorMap* m, const void* ptr, long long rows, long long cols, long long ld,
@@ -559,7 +623,7 @@ inline bool w8_supported(int sms, int M, int N, int K) {
 // few large stages beat deep rings of small ones (10.8 us against 13.3 us
 // for four K blocks per stage with a six-deep ring): every stage costs a
 // hand-off between the converter warps and the MMA thread.
-inline void w8_default_config(int sms, int M, int N, int K, sgr_config* c) {
+inline void w8_default_config(int sms, int M, int N, int K, sgr_config* c, bool fp4 = false) {
   (void)K;
   std::memset(c, 0, sizeof *c);
   c->path = SGR_PATH_W8;
@@ -569,9 +633,9 @@ inline void w8_default_config(int sms, int M, int N, int K, sgr_config* c) {
   c->prefetch_stages = 2;
   const int rb = w8_rows_per_cta(sms, N);
   const size_t budget = 110u * 1024u;
-  c->k_blocks_per_stage = 2;
-  for (int kb = 8; kb >= 2; kb /= 2)
-    if (w8_smem_bytes(2, 2, kb, rb, c->token_tile) <= budget) {
+  c->k_blocks_per_stage = fp4 ? 4 : 2;
+  for (int kb = 8; kb >= (fp4 ? 4 : 2); kb /= 2)
+    if (w8_smem_bytes(2, 2, kb, rb, c->token_tile, fp4) <= budget) {
       c->k_blocks_per_stage = kb;
       return;
     }
@@ -579,20 +643,22 @@ inline void w8_default_config(int sms, int M, int N, int K, sgr_config* c) {
 
 // stages = depth of the weight-code ring, prefetch_stages = depth of the
 // activation ring (0: 2).
-inline int w8_plan(const sgr_config& c, int sms, int M, int N, int K, W8Params* p, int* grid, size_t* smem) {
+inline int w8_plan(const sgr_config& c, int sms, int M, int N, int K, W8Params* p, int* grid, size_t* smem,
+                   bool fp4 = false) {
   if (!w8_supported(sms, M, N, K)) return SGR_ERR_UNSUPPORTED;
   if (c.path != SGR_PATH_AUTO && c.path != SGR_PATH_W8) return SGR_ERR_UNSUPPORTED;
   const int nt = c.token_tile;
   if (nt < 16 || nt > kW8MaxTokens || nt % 16 != 0 || nt < M) return SGR_ERR_UNSUPPORTED;
   const int kb = c.k_blocks_per_stage;
   if (kb < 2 || kb > 8 || kb % 2 != 0) return SGR_ERR_UNSUPPORTED;
+  if (fp4 && kb % 4 != 0) return SGR_ERR_UNSUPPORTED;  // whole 256-code boxes; 16-byte block-scale boxes
   if (c.ctas_per_sm != 1) return SGR_ERR_UNSUPPORTED;
   if (c.stages < 2 || c.stages > kW8MaxStages) return SGR_ERR_UNSUPPORTED;
   const int sa = c.prefetch_stages > 0 ? c.prefetch_stages : 2;
   if (sa < 2 || sa > kW8MaxAStages) return SGR_ERR_UNSUPPORTED;
   const int rb = c.rows_per_stage > 0 ? c.rows_per_stage : w8_rows_per_cta(sms, N);
   if (rb % 8 != 0 || rb > kTcTileRows) return SGR_ERR_UNSUPPORTED;
-  const size_t sm = w8_smem_bytes(c.stages, sa, kb, rb, nt);
+  const size_t sm = w8_smem_bytes(c.stages, sa, kb, rb, nt, fp4);
   if (sm > 232448) return SGR_ERR_UNSUPPORTED;
   p->M = M;
   p->N = N;
@@ -610,7 +676,7 @@ inline int w8_plan(const sgr_config& c, int sms, int M, int N, int K, W8Params* 
       break;
     }
   // The general epilogue stages [groups][RB][NT+4] floats in the drained rings.
-  const size_t rings = (size_t)c.stages * w8_wstage_bytes(kb, rb) + (size_t)sa * w8_astage_bytes(kb, nt);
+  const size_t rings = (size_t)c.stages * wring_stage_bytes(fp4, kb, rb) + (size_t)sa * w8_astage_bytes(kb, nt);
   while (p->groups > 1 && (size_t)p->groups * rb * (nt + 4) * 4 > rings) p->groups /= 2;
   if ((size_t)p->groups * rb * (nt + 4) * 4 > rings) return SGR_ERR_UNSUPPORTED;
   if (kb / p->groups > kW8MaxWins) return SGR_ERR_UNSUPPORTED;
@@ -630,7 +696,11 @@ inline int w8_plan(const sgr_config& c, int sms, int M, int N, int K, W8Params* 
   return SGR_OK;
 }
 
-inline cudaError_t w8_init_device() { return set_kernel_smem_attrs(reinterpret_cast<const void*>(w8_rows_kernel)); }
+inline cudaError_t w8_init_device() {
+  cudaError_t e = set_kernel_smem_attrs(reinterpret_cast<const void*>(w8_rows_kernel<false>));
+  if (e == cudaSuccess) e = set_kernel_smem_attrs(reinterpret_cast<const void*>(w8_rows_kernel<true>));
+  return e;
+}
 
 inline int w8_launch(const sgr_config& c, int sms, unsigned* err, const void* A, long long lda, const void* Wq,
                      long long ldw, const float* scale, const void* R, long long ldr, void* Y, long long ldy, int M,
@@ -660,7 +730,46 @@ inline int w8_launch(const sgr_config& c, int sms, unsigned* err, const void* A,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
   lc.numAttrs = pdl ? 1 : 0;
-  if (cudaLaunchKernelEx(&lc, w8_rows_kernel, tmW, tmA, tmR, p) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&lc, w8_rows_kernel<false>, tmW, tmA, tmR, tmW, p) != cudaSuccess) {
+    cudaGetLastError();
+    return SGR_ERR_LAUNCH;
+  }
+  return SGR_OK;
+}
+
+// NVFP4 weights on the same kernel: Wq4 [N, K/2] bytes (row stride ldw), bs
+// [N, ceil(K/16)] E4M3 block scales (row stride ldbs), tensor scale gs.
+inline int w4_launch(const sgr_config& c, int sms, unsigned* err, const void* A, long long lda, const void* Wq4,
+                     long long ldw, const void* bs, long long ldbs, float gs, const void* R, long long ldr, void* Y,
+                     long long ldy, int M, int N, int K, bool pdl, cudaStream_t stream) {
+  W8Params p;
+  int grid = 0;
+  size_t smem = 0;
+  int rc = w8_plan(c, sms, M, N, K, &p, &grid, &smem, true);
+  if (rc != SGR_OK) return rc;
+  CUtensorMap tmW, tmA, tmR, tmS;
+  if (!detail::make_tmap_u8(&tmW, Wq4, N, K / 2, ldw, p.RB, 2 * kTcKBlock)) return SGR_ERR_LAUNCH;
+  if (!detail::make_tmap(&tmA, A, M, K, lda, p.NT, kTcKBlock)) return SGR_ERR_LAUNCH;
+  if (!detail::make_tmap_plain_bf16(&tmR, R, M, N, ldr, p.NT, p.RB)) return SGR_ERR_LAUNCH;
+  if (!detail::make_tmap_u8_plain(&tmS, bs, N, (K + 15) / 16, ldbs, p.RB, p.kbps * 4)) return SGR_ERR_LAUNCH;
+  p.R = static_cast<const __nv_bfloat16*>(R);
+  p.Y = static_cast<__nv_bfloat16*>(Y);
+  p.scale = nullptr;
+  p.gs = gs;
+  p.ldr = ldr;
+  p.ldy = ldy;
+  p.err = err;
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3((unsigned)grid, 1, 1);
+  lc.blockDim = dim3(kW8Threads, 1, 1);
+  lc.dynamicSmemBytes = smem;
+  lc.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = pdl ? 1 : 0;
+  if (cudaLaunchKernelEx(&lc, w8_rows_kernel<true>, tmW, tmA, tmR, tmS, p) != cudaSuccess) {
     cudaGetLastError();
     return SGR_ERR_LAUNCH;
   }

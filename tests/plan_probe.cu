@@ -56,18 +56,21 @@ int main() {
               c.stages = st;
               c.prefetch_stages = sa;
               c.token_tile = nt;
-              sgr::W8Params p;
-              int grid = 0;
-              size_t smem = 0;
-              if (sgr::w8_plan(c, sms, M, N, K, &p, &grid, &smem) != SGR_OK) continue;
-              std::printf("{\"kind\": \"w8\", \"M\": %d, \"N\": %d, \"K\": %d, \"RB\": %d, \"NT\": %d, \"G\": %d, "
-                          "\"kbps\": %d, \"stages\": %d, \"a_stages\": %d, \"k_stages\": %d, \"slots\": %d, "
-                          "\"acc_cols\": %d, \"tmem_cols\": %d, \"conv_warps\": %d, \"grid\": %d, \"smem\": %zu, "
-                          "\"rtile\": %u, \"w_ring\": %zu, \"a_ring\": %zu}\n",
-                          M, N, K, p.RB, p.NT, p.groups, p.kbps, p.stages, p.a_stages, p.k_stages, p.slots,
-                          p.acc_cols, p.tmem_cols, p.conv_warps, grid, smem, sgr::w8_rtile_bytes(p.RB, p.NT),
-                          (size_t)p.stages * sgr::w8_wstage_bytes(p.kbps, p.RB),
-                          (size_t)p.a_stages * sgr::w8_astage_bytes(p.kbps, p.NT));
+              for (int fp4 = 0; fp4 <= 1; ++fp4) {
+                sgr::W8Params p;
+                int grid = 0;
+                size_t smem = 0;
+                if (sgr::w8_plan(c, sms, M, N, K, &p, &grid, &smem, fp4 != 0) != SGR_OK) continue;
+                std::printf("{\"kind\": \"w8\", \"fp4\": %d, \"M\": %d, \"N\": %d, \"K\": %d, \"RB\": %d, \"NT\": %d, "
+                            "\"G\": %d, \"kbps\": %d, \"stages\": %d, \"a_stages\": %d, \"k_stages\": %d, "
+                            "\"slots\": %d, \"acc_cols\": %d, \"tmem_cols\": %d, \"conv_warps\": %d, \"grid\": %d, "
+                            "\"smem\": %zu, \"rtile\": %u, \"w_stage\": %u, \"w_ring\": %zu, \"a_ring\": %zu}\n",
+                            fp4, M, N, K, p.RB, p.NT, p.groups, p.kbps, p.stages, p.a_stages, p.k_stages, p.slots,
+                            p.acc_cols, p.tmem_cols, p.conv_warps, grid, smem, sgr::w8_rtile_bytes(p.RB, p.NT),
+                            sgr::wring_stage_bytes(fp4 != 0, p.kbps, p.RB),
+                            (size_t)p.stages * sgr::wring_stage_bytes(fp4 != 0, p.kbps, p.RB),
+                            (size_t)p.a_stages * sgr::w8_astage_bytes(p.kbps, p.NT));
+              }
             }
       // tile kernel
       for (int tn : {64, 128, 192, 256})

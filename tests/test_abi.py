@@ -311,12 +311,12 @@ def test_validate_w4_accepts_good_arguments():
     assert v4(M=0, A=0, Wq4=0, bs=0, R=0, Y=0) == sgr.SGR_OK
     assert v4(K=0, A=0, Wq4=0, bs=0) == sgr.SGR_OK        # empty sum: Y = R
     assert v4(K=1056, lda=1056, ldw=528, ldbs=80) == sgr.SGR_OK  # 66 scales per row, read as 80 bytes
+    assert v4(K=3592, lda=3592, ldw=1808, ldbs=240) == sgr.SGR_OK  # K not a multiple of 32: tensor-core kernel
 
 
 @pytest.mark.parametrize("kw,status", [
     (dict(M=-1), sgr.SGR_ERR_SHAPE),
     (dict(K=3580, lda=3584), sgr.SGR_ERR_SHAPE),          # K not a multiple of 8
-    (dict(K=3592, lda=3592, ldw=1808, ldbs=240), sgr.SGR_ERR_UNSUPPORTED),  # K not a multiple of 32
     (dict(Wq4=0), sgr.SGR_ERR_NULL),
     (dict(bs=0), sgr.SGR_ERR_NULL),
     (dict(ldw=1776), sgr.SGR_ERR_SHAPE),                  # fewer than K/2 bytes per code row
@@ -336,17 +336,21 @@ def test_validate_w4_rejects(kw, status):
 
 
 def test_w4_config_and_size_rejections_need_no_device():
-    """A tensor-core path, tile-only fields, M above 256 or K above 7168 are
-    refused before any launch (M = 0 is a no-op whatever the configuration)."""
+    """A tile path, tile-only fields, M above 256, or a K the CUDA-core kernel
+    cannot take on that path are refused before any launch (M = 0 is a no-op
+    whatever the configuration)."""
     lib = sgr.load()
     cfg = sgr.make_config(path=sgr.SGR_PATH_TILE)
     assert binding.skinny_gemm_residual_w4_ptr(A_, 3584, W_, 1792, B_, 224, 1.0, R_, 7168, Y_, 7168, 0, 7168, 3584,
                                                cfg, 0, 0) == sgr.SGR_OK
     assert lib.sgr_validate_w4(None, 3584, None, 1792, None, 224, None, 7168, None, 7168, 4, 7168, 3584) == \
         sgr.SGR_ERR_NULL
-    call = lambda M, K, c: binding.skinny_gemm_residual_w4_ptr(A_, K, W_, K // 2, B_, ((K // 16 + 15) // 16) * 16, 1.0,
-                                                                R_, 7168, Y_, 7168, M, 7168, K, c, 0, 0)
+    call = lambda M, K, c: binding.skinny_gemm_residual_w4_ptr(A_, K, W_, (K // 2 + 15) // 16 * 16, B_,
+                                                                ((K + 15) // 16 + 15) // 16 * 16, 1.0, R_, 7168, Y_,
+                                                                7168, M, 7168, K, c, 0, 0)
     assert call(4, 3584, cfg) == sgr.SGR_ERR_UNSUPPORTED                          # tile path
     assert call(4, 3584, sgr.make_config(k_split=2)) == sgr.SGR_ERR_UNSUPPORTED   # tile-only field
     assert call(257, 3584, None) == sgr.SGR_ERR_UNSUPPORTED                       # more than 256 tokens
-    assert call(4, 7200, None) == sgr.SGR_ERR_UNSUPPORTED                         # K above 7168
+    simt = sgr.make_config(path=sgr.SGR_PATH_SIMT)
+    assert call(1, 7200, simt) == sgr.SGR_ERR_UNSUPPORTED                         # CUDA-core kernel: K <= 7168
+    assert call(1, 3592, simt) == sgr.SGR_ERR_UNSUPPORTED                         # and whole 32-code vectors

@@ -17,6 +17,7 @@ pytestmark = pytest.mark.gpu
 
 N_FULL, K_FULL = inputs.N_LATENT_MOE, inputs.K_LATENT_MOE
 SIMT = sgr.SGR_PATH_SIMT
+TC = sgr.SGR_PATH_W8  # the tensor-core widening kernel
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -44,8 +45,19 @@ def scales_on_device(bs: torch.Tensor) -> torch.Tensor:
     return buf[:, :nb]
 
 
+def codes_on_device(Wq4: torch.Tensor) -> torch.Tensor:
+    """Codes on the GPU, rows padded to a multiple of 16 bytes when K/2 is
+    not (the row stride must be, the row length need not)."""
+    N, half = Wq4.shape
+    if half % 16 == 0:
+        return Wq4.cuda()
+    buf = torch.zeros((N, (half + 15) // 16 * 16), dtype=torch.uint8, device="cuda")
+    buf[:, :half].copy_(Wq4)
+    return buf[:, :half]
+
+
 def run(p, **cfg):
-    A, Wq4, bs, R = p.A.cuda(), p.Wq4.cuda(), scales_on_device(p.bs), p.R.cuda()
+    A, Wq4, bs, R = p.A.cuda(), codes_on_device(p.Wq4), scales_on_device(p.bs), p.R.cuda()
     Y = torch.full_like(R, float("nan"))
     sgr.skinny_gemm_residual_w4(A, Wq4, bs, p.gs, R, Y, config=sgr.make_config(**cfg) if cfg else None)
     torch.cuda.synchronize()
@@ -114,6 +126,50 @@ W4_CONFIGS = [
 def test_w4_configs(cfg, M):
     p = inputs.make_problem_w4(M, 2056, 1024, seed=31 + M)
     compare(run(p, **cfg), ref(p), f"w4 M={M} {cfg}")
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 8, 16])
+def test_w4_both_kernels_full_size(M):
+    """The CUDA-core and tensor-core kernels, forced, at the latent-MoE
+    shape: every element of each against the oracle."""
+    p = inputs.make_problem_w4(M, N_FULL, K_FULL, seed=200 + M)
+    want = ref(p)
+    compare(run(p, path=SIMT), want, f"w4 simt M={M}")
+    compare(run(p, path=TC), want, f"w4 tensor core M={M}")
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 8, 8), (3, 520, 1000), (5, 776, 72), (17, 1024, 2056), (40, 2056, 3584),
+                                   (64, 1024, 1024), (100, 264, 3600), (256, 1032, 512)])
+def test_w4_tensor_core_ragged_and_wide(M, N, K):
+    """The tensor-core kernel on shapes the CUDA-core kernel cannot take (K
+    not a multiple of 32, padded code rows) and at 17-256 tokens in one
+    launch (token tiles of 32-256)."""
+    p = inputs.make_problem_w4(M, N, K, seed=M * 3 + N + K)
+    compare(run(p, path=TC), ref(p), f"w4 tc {M}x{N}x{K}")
+
+
+TC_CONFIGS = [
+    dict(path=TC, k_blocks_per_stage=4, stages=2),
+    dict(path=TC, k_blocks_per_stage=4, stages=6, prefetch_stages=4),
+    dict(path=TC, k_blocks_per_stage=8, stages=2),
+    dict(path=TC, k_blocks_per_stage=8, stages=3, prefetch_stages=3),
+    dict(path=TC, k_blocks_per_stage=8, stages=2, rows_per_stage=32),
+    dict(path=TC, k_blocks_per_stage=4, stages=4, token_tile=32),
+]
+
+
+@pytest.mark.parametrize("cfg", TC_CONFIGS, ids=lambda c: "-".join(f"{k}{v}" for k, v in c.items() if k != "path"))
+@pytest.mark.parametrize("M", [1, 7, 16])
+def test_w4_tensor_core_configs(cfg, M):
+    p = inputs.make_problem_w4(M, 2056, 1032, seed=41 + M)
+    compare(run(p, **cfg), ref(p), f"w4 tc M={M} {cfg}")
+
+
+def test_w4_tensor_core_every_code_and_subnormal_scales():
+    p = codes_problem(6, 512, 1024, seed=43)
+    compare(run(p, path=TC), ref(p), "w4 tc codes")
+    q = codes_problem(3, 512, 1024, seed=44, scale_mask=0x07)
+    compare(run(q, path=TC), ref(q), "w4 tc subnormal scales")
 
 
 def test_w4_integer_inputs_exact():
@@ -221,11 +277,17 @@ def test_w4_rejects():
     p = inputs.make_problem_w4(2, 256, 1024, seed=2)
     A, Wq4, bs, R = p.A.cuda(), p.Wq4.cuda(), scales_on_device(p.bs), p.R.cuda()
     for cfg in (dict(path=sgr.SGR_PATH_TILE), dict(path=sgr.SGR_PATH_W8S), dict(path=SIMT, stages=1),
-                dict(path=SIMT, rows_per_stage=65), dict(path=SIMT, ctas_per_sm=9), dict(k_split=2)):
+                dict(path=SIMT, rows_per_stage=65), dict(path=SIMT, ctas_per_sm=9), dict(k_split=2),
+                dict(path=TC, k_blocks_per_stage=2), dict(path=TC, k_blocks_per_stage=6), dict(path=TC, stages=17),
+                dict(path=TC, ctas_per_sm=2), dict(path=TC, token_tile=8)):
         with pytest.raises(sgr.SgrError) as e:
             sgr.skinny_gemm_residual_w4(A, Wq4, bs, p.gs, R, config=sgr.make_config(**cfg))
         assert e.value.status == sgr.SGR_ERR_UNSUPPORTED, cfg
     q = inputs.make_problem_w4(1, 64, 48, seed=3)  # K = 48: not whole 32-code vectors
     with pytest.raises(sgr.SgrError) as e:
-        sgr.skinny_gemm_residual_w4(q.A.cuda(), q.Wq4.cuda(), scales_on_device(q.bs), q.gs, q.R.cuda())
-    assert e.value.status in (sgr.SGR_ERR_UNSUPPORTED, sgr.SGR_ERR_ALIGN)
+        sgr.skinny_gemm_residual_w4(q.A.cuda(), codes_on_device(q.Wq4), scales_on_device(q.bs), q.gs, q.R.cuda(),
+                                    config=sgr.make_config(path=SIMT))
+    assert e.value.status == sgr.SGR_ERR_UNSUPPORTED
+    y = sgr.skinny_gemm_residual_w4(q.A.cuda(), codes_on_device(q.Wq4), scales_on_device(q.bs), q.gs, q.R.cuda())
+    torch.cuda.synchronize()  # the library's choice takes the tensor-core kernel there
+    compare(bits(y), ref(q), "w4 K = 48 (automatic path)")

@@ -60,11 +60,18 @@ def test_row_slab_plans(plans):
 
 def test_fp8_row_slab_plans(plans):
     rows = [p for p in plans if p["kind"] == "w8"]
-    assert len(rows) > 100
+    assert len(rows) > 100 and sum(p["fp4"] for p in rows) > 50
     for p in rows:
         assert p["smem"] <= SMEM_LIMIT, p
         assert p["G"] * p["RB"] <= 128 and p["G"] * p["NT"] <= 256, p
         assert p["kbps"] % 2 == 0 and p["kbps"] % p["G"] == 0, p
+        if p["fp4"]:
+            # 256-code boxes (kbps/4 per stage) and the RB rows' block scales (kbps * 4 bytes each)
+            # inside the stage, whose size keeps the next stage's boxes 1024-byte aligned
+            assert p["kbps"] % 4 == 0, p
+            assert p["w_stage"] % 1024 == 0 and p["w_stage"] >= p["kbps"] // 4 * p["RB"] * 128 + p["RB"] * p["kbps"] * 4, p
+        else:
+            assert p["w_stage"] == p["kbps"] // 2 * p["RB"] * 128, p
         wins = p["kbps"] // p["G"]
         assert p["tmem_cols"] in (256, 512), p
         assert p["acc_cols"] >= p["G"] * p["NT"], p
