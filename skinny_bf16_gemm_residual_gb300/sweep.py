@@ -9,9 +9,11 @@ The per-M table compiled into the library is generated from these rows by
 ``gen_table.py``.  The paths ``w8`` (widening tensor-core FP8-weight kernel), ``w8s`` (FP8
 tensor-core kernel with split activations) and
 ``w8simt`` (CUDA-core FP8-weight kernel) time ``skinny_gemm_residual_w8`` over
-rotating copies of per-column-quantised E4M3 weights; their rows (backend
-``w8`` / ``w8_simt``) are for choosing that entry point's defaults and are
-not part of the BF16 table.
+rotating copies of per-column-quantised E4M3 weights; ``w4`` (tensor-core
+widening kernel) and ``w4simt`` (CUDA-core kernel) time
+``skinny_gemm_residual_w4`` over rotating copies of NVFP4-quantised weights.
+Their rows are for choosing those entry points' defaults and are not part of
+the BF16 table.
 
     python -m skinny_bf16_gemm_residual_gb300.sweep --m 1 2 4 8 16 --output sweep.jsonl
     python -m skinny_bf16_gemm_residual_gb300.sweep --paths w8,w8simt --copies 8 --output sweep_w8.jsonl
@@ -46,6 +48,28 @@ def candidate_configs_w8s(M: int, grid: str) -> list[dict]:
             if grid == "small" and st > 4:
                 continue
             out.append(dict(path=sgr.SGR_PATH_W8S, k_blocks_per_stage=kb, stages=st))
+    return out
+
+
+def candidate_configs_w4(simt: bool, M: int, K: int, grid: str) -> list[dict]:
+    """Launch configurations of the NVFP4-weight kernels (the library refuses
+    what does not fit)."""
+    out = []
+    if simt:
+        if K % 32 or K > 7168:
+            return []
+        for cps in (1, 2, 3):
+            for rps in (1, 2, 4):
+                for st in (2, 4, 8):
+                    if grid == "small" and st == 8:
+                        continue
+                    out.append(dict(path=sgr.SGR_PATH_SIMT, ctas_per_sm=cps, rows_per_stage=rps, stages=st))
+        return out
+    for kb in (4, 8):
+        for st in (2, 3, 4, 6):
+            if grid == "small" and st > 4:
+                continue
+            out.append(dict(path=sgr.SGR_PATH_W8, k_blocks_per_stage=kb, stages=st))
     return out
 
 
@@ -179,7 +203,12 @@ def build_row(M: int, N: int, K: int, backend: str, cfg: dict, copies: int, meta
         return row
     st = summarize(samples)
     row.update(st)
-    nbytes = (N * K + 4 * N + 2 * M * K + 4 * M * N) if backend.startswith("w8") else 2 * (N * K + M * K + 2 * M * N)
+    if backend.startswith("w8"):
+        nbytes = N * K + 4 * N + 2 * M * K + 4 * M * N
+    elif backend.startswith("w4"):
+        nbytes = N * K // 2 + N * ((K + 15) // 16) + 2 * M * K + 4 * M * N
+    else:
+        nbytes = 2 * (N * K + M * K + 2 * M * N)
     sec = st["median_us"] * 1e-6
     row["gbs"] = nbytes / sec / 1e9
     row["tflops"] = 2.0 * M * N * K / sec / 1e12
@@ -306,12 +335,17 @@ def main(argv=None):
     out = open_output(args.output, args.resume) if args.output else None
     paths = {"simt": sgr.SGR_PATH_SIMT, "tc": sgr.SGR_PATH_TC, "rows": sgr.SGR_PATH_TC_ROWS,
              "tile": sgr.SGR_PATH_TILE, "pair": sgr.SGR_PATH_PAIR, "w8": sgr.SGR_PATH_W8, "w8simt": sgr.SGR_PATH_SIMT,
-             "w8s": sgr.SGR_PATH_W8S}
+             "w8s": sgr.SGR_PATH_W8S, "w4": sgr.SGR_PATH_W8, "w4simt": sgr.SGR_PATH_SIMT}
     fp8 = [name for name in args.paths.split(",") if name in ("w8", "w8simt", "w8s")]
     if fp8:  # per-column-quantised E4M3 copies of the same weights
         q = [inputs.make_problem_w8(1, N, K, seed=s) for s in range(args.copies)]
         Wqs = [x.Wq.to(dev) for x in q]
         Scs = [x.scale.to(dev) for x in q]
+    if any(name in ("w4", "w4simt") for name in args.paths.split(",")):  # NVFP4-quantised copies
+        q4 = [inputs.make_problem_w4(1, N, K, seed=s) for s in range(args.copies)]
+        W4s = [x.Wq4.to(dev) for x in q4]
+        B4s = [x.bs.to(dev) for x in q4]
+        G4s = [x.gs for x in q4]
     for M in args.m:
         A = inputs.make_rows(M, K, seed=10_000 + M).to(dev)
         Rs = [inputs.make_rows(M, N, seed=20_000 + 100 * M + s).to(dev) for s in range(args.copies)]
@@ -330,15 +364,18 @@ def main(argv=None):
             record("cublas_addmm", {}, graph_samples(launch, args.copies, stream, args.repeats, args.replays))
         for name in args.paths.split(","):
             w8 = name in ("w8", "w8simt", "w8s")
+            w4 = name in ("w4", "w4simt")
             if args.config:
                 cands = [dict(json.loads(c), path=paths[name]) for c in args.config]
+            elif w4:
+                cands = candidate_configs_w4(name == "w4simt", M, K, args.grid)
             elif name == "w8s":
                 cands = candidate_configs_w8s(M, args.grid)
             elif w8:
                 cands = candidate_configs_w8(name == "w8simt", M, K, args.grid)
             else:
                 cands = candidate_configs(paths[name], M, K, args.grid)
-            backend = {"w8": "w8", "w8simt": "w8_simt", "w8s": "w8s"}.get(name, name)
+            backend = {"w8": "w8", "w8simt": "w8_simt", "w8s": "w8s", "w4": "w4", "w4simt": "w4_simt"}.get(name, name)
             for cfg in cands:
                 if row_key(M, N, K, backend, cfg) in done:
                     continue
@@ -346,6 +383,9 @@ def main(argv=None):
                 if w8:
                     launch = lambda i, c=c: sgr.skinny_gemm_residual_w8(A, Wqs[i], Scs[i], Rs[i], Ys[i], stream=stream,
                                                                        config=c)
+                elif w4:
+                    launch = lambda i, c=c: sgr.skinny_gemm_residual_w4(A, W4s[i], B4s[i], G4s[i], Rs[i], Ys[i],
+                                                                       stream=stream, config=c)
                 else:
                     launch = lambda i, c=c: sgr.skinny_gemm_residual_ex(A, Ws[i], Rs[i], Ys[i], stream=stream,
                                                                         config=c)
