@@ -620,7 +620,10 @@ inline bool tile_supported(int M, int N, int K) {
   return M >= 1 && N >= 8 && K >= 8 && N % 8 == 0 && K % 8 == 0;
 }
 
-// Tile width and K split.  With the K split over 2-CTA clusters (one tile per
+// Tile width and K split.  The default split is the 2-way one: 3- and 4-way
+// splits (explicit configurations) measured slower at N = 7168 and M <= 128,
+// their exchange of partial sums growing with the ranks faster than their K
+// loops shrink.  With the K split over 2-CTA clusters (one tile per
 // cluster, so it needs 2 x tiles <= SMs) the smallest width in {128, 192}
 // that fits is taken while the problem has at most two 128-token tiles;
 // otherwise the NT in {192, 256, 128, 64} with the least work per SM (waves
