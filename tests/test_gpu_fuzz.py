@@ -67,11 +67,11 @@ def test_fuzz_bf16(seed):
     compare(bits(Y), oracle_full(p.A, p.W, p.R), f"fuzz bf16 seed={seed} M={M} N={N} K={K} path={path}")
 
 
-@pytest.mark.parametrize("seed", range(24))
+@pytest.mark.parametrize("seed", range(32))
 def test_fuzz_w8(seed):
     rng, M, N, K = case(500 + seed)
     K = (K + 15) // 16 * 16 if seed % 2 else K  # half the cases have K a multiple of 16
-    path = (sgr.SGR_PATH_AUTO, sgr.SGR_PATH_W8, sgr.SGR_PATH_SIMT)[seed % 3]
+    path = (sgr.SGR_PATH_AUTO, sgr.SGR_PATH_W8, sgr.SGR_PATH_SIMT, sgr.SGR_PATH_W8S)[seed % 4]
     p = inputs.make_problem_w8(M, N, K, seed=2000 + seed)
     if seed % 4 == 0:  # codes of every kind and random scales
         p = inputs.ProblemW8(p.A, inputs.random_e4m3_codes((N, K), 3000 + seed),
@@ -92,3 +92,41 @@ def test_fuzz_w8(seed):
     torch.cuda.synchronize()
     want = oracle.load().gemm_residual_w8(p.A, p.Wq, p.scale, p.R)
     compare(bits(Y), want, f"fuzz w8 seed={seed} M={M} N={N} K={K} path={path}")
+
+
+@pytest.mark.parametrize("seed", range(32))
+def test_fuzz_w4(seed):
+    """NVFP4 weights: random shapes (K a multiple of 32 in half the cases),
+    padded code and scale rows, random codes and block scales in a quarter
+    of the cases, in place or not, on the library's choice or a forced kernel."""
+    rng, M, N, K = case(700 + seed)
+    K = (K + 31) // 32 * 32 if seed % 2 else K
+    path = (sgr.SGR_PATH_AUTO, sgr.SGR_PATH_W8, sgr.SGR_PATH_SIMT)[seed % 3]
+    p = inputs.make_problem_w4(M, N, K, seed=5000 + seed)
+    if seed % 4 == 0:  # every code pair, random positive block scales, a random tensor scale
+        bs = inputs.random_e4m3_codes((N, (K + 15) // 16), 6000 + seed) & 0x7F
+        bs = torch.where(bs == 0x7F, bs - 1, bs)
+        p = inputs.ProblemW4(p.A, inputs.random_e2m1_bytes((N, K // 2), 7000 + seed), bs,
+                             float(inputs.random_scales(1, 8000 + seed, lo_exp=-8, hi_exp=-4)[0]), p.R, p.seed)
+    half, nb = K // 2, (K + 15) // 16
+    wpad = 16 * int(rng.integers(0, 3)) + ((-half) % 16)
+    Wbuf = torch.zeros((N, half + wpad), dtype=torch.uint8, device="cuda")
+    Wq4 = Wbuf[:, :half]
+    Wq4.copy_(p.Wq4)
+    spad = 16 * int(rng.integers(0, 3)) + ((-nb) % 16)
+    Sbuf = torch.zeros((N, nb + spad), dtype=torch.uint8, device="cuda")
+    bs = Sbuf[:, :nb]
+    bs.copy_(p.bs)
+    A = padded(p.A, int(rng.integers(0, 4)) * 8)
+    R = padded(p.R, int(rng.integers(0, 4)) * 8)
+    Y = R if bool(rng.integers(0, 2)) else None
+    cfg = None if path == sgr.SGR_PATH_AUTO else sgr.make_config(path=path)
+    try:
+        Y = sgr.skinny_gemm_residual_w4(A, Wq4, bs, p.gs, R, Y, config=cfg)
+    except sgr.SgrError as e:
+        assert path != sgr.SGR_PATH_AUTO and e.status == sgr.SGR_ERR_UNSUPPORTED, (M, N, K, path, e)
+        return
+    torch.cuda.synchronize()
+    want = oracle.load().gemm_residual_w4(p.A, p.Wq4, p.bs, p.gs, p.R)
+    compare(bits(Y), want, f"fuzz w4 seed={seed} M={M} N={N} K={K} path={path}")
+
