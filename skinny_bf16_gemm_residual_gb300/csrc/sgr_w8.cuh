@@ -632,10 +632,14 @@ inline void w8_default_config(int sms, int M, int N, int K, sgr_config* c, bool 
   c->stages = 2;
   c->prefetch_stages = 2;
   const int rb = w8_rows_per_cta(sms, N);
+  // NVFP4 above 8 tokens: 32-row slabs (four packed K blocks fill the 128-row
+  // window, every tensor-memory lane quarter converts; measured at N = 7168,
+  // K = 3584, M = 16: 11.1 against 11.4 us; slower at M <= 8).
+  if (fp4 && M > 8 && (N + 31) / 32 <= 2 * sms) c->rows_per_stage = 32;
   const size_t budget = 110u * 1024u;
   c->k_blocks_per_stage = fp4 ? 4 : 2;
   for (int kb = 8; kb >= (fp4 ? 4 : 2); kb /= 2)
-    if (w8_smem_bytes(2, 2, kb, rb, c->token_tile, fp4) <= budget) {
+    if (w8_smem_bytes(2, 2, kb, c->rows_per_stage > 0 ? c->rows_per_stage : rb, c->token_tile, fp4) <= budget) {
       c->k_blocks_per_stage = kb;
       return;
     }
