@@ -329,7 +329,7 @@ int skinny_gemm_residual_grouped(const sgr_group* groups, int num_groups, int N,
  * are represented with an absolute error below 2^-21 times that magnitude
  * (so a row whose values span more than 2^13 can differ from the exact
  * result by up to sum_k |scale[n] e4m3(Wq[n,k])| * 2^-21 * max_k |A[m,k]|).
- * SGR_PATH_AUTO takes SGR_PATH_W8S for M <= 4 where it can run, else the
+ * SGR_PATH_AUTO takes SGR_PATH_W8S for M <= 8 where it can run, else the
  * CUDA-core kernel for M = 1 where it can run, else the tensor-core row-slab
  * kernel.  Returns an sgr_status.
  */

@@ -672,11 +672,12 @@ bool simt_w8_supported(int M, int K, long long ldw) {
 constexpr int kW8SimtMaxM = 1;
 
 // The FP8 tensor-core path with split activations up to this many tokens
-// (measured at N = 7168, K = 3584, graph of 8 calls: 9.2 / 9.4 / 9.8 us at
-// M = 1 / 2 / 4 against 10.8 us for the widening kernel; even at M = 8; the
-// widening kernel ahead at M = 16, where converting all of A in every CTA
-// costs more than it saves).
-constexpr int kW8sAutoMaxM = 4;
+// (measured at N = 7168, K = 3584, graph of 8 calls over distinct code
+// copies: 8.2-8.7 us at M = 1-4 and 9.8-10.0 us at M = 5-8 against 10.8 us
+// for the widening kernel; the widening kernel ahead at M = 12-16, 10.9-11.0
+// against 11.9-12.2 us, where converting all of A in every CTA costs more
+// than it saves).
+constexpr int kW8sAutoMaxM = 8;
 
 // CUDA-core FP8 configuration: ring stages of two code rows, 4 stages,
 // CTAs per SM by token count (the register footprint grows with M).
@@ -1270,7 +1271,8 @@ int sgr_kernel_resources(int device, int path, int M, int N, int K, int* regs, i
     *smem_bytes = (int)smem;
     *threads = sgr::kW8Threads;
   } else if (c.path == SGR_PATH_W8S) {
-    if (cudaFuncGetAttributes(&fa, sgr::w8s_kernel) != cudaSuccess) {
+    if (cudaFuncGetAttributes(&fa, sgr::w8s_in_regs(M, K) ? sgr::w8s_kernel<true> : sgr::w8s_kernel<false>) !=
+        cudaSuccess) {
       cudaGetLastError();
       return SGR_ERR_DEVICE;
     }

@@ -29,10 +29,23 @@
 // CTA the next call's CTA fits on the same SM, so with programmatic dependent
 // launch it streams its weights while this one finishes.
 //
-// Warp roles (192 threads): warp 0 lane 0 issues TMA (W for the first stages
-// before griddepcontrol.wait, A after it); warp 1 owns TMEM and lane 0 issues
-// the MMAs; warps 2-5 are the epilogue: they load their residual values while
-// the MMAs run, then tcgen05.ld the accumulator, add, round once and store.
+// Warp roles (224 threads): warp 0 lane 0 issues TMA (W for the first stages
+// before griddepcontrol.wait, A after it); warp 1 owns TMEM and its lane 0
+// issues the MMAs, or, with two issuers, the even MMA windows of every stage
+// while lane 0 of warp 6 issues the odd ones into a second accumulator (one
+// thread issues a small-N MMA only every ~75 cycles, which left the last
+// stage's MMAs exposed after its weights landed; the epilogue adds the two
+// accumulators in a fixed order); warps 2-5 are the epilogue: they load their
+// residual values while the MMAs run, then tcgen05.ld the accumulator, add,
+// round once and store.
+//
+// Warm-up pass: the first run of a code path in a CTA costs ~0.7 us more
+// than the next (measured with the weight stream saturating L2: instruction
+// and parameter fetches wait behind it), and the epilogue runs once, on the
+// critical path after the last weights land.  So the decode epilogue runs its
+// instructions twice: first while the MMAs are still running, against tensor-
+// memory columns no MMA writes, a scratch word of shared memory and stores
+// predicated off, then for real.
 //
 // For up to 16 tokens the epilogue is one TMEM load, one shared-memory
 // hand-over of group 1's partial sums and the stores, with the residuals and
@@ -58,7 +71,7 @@
 
 namespace sgr {
 
-constexpr int kRowsThreads = 192;
+constexpr int kRowsThreads = 224;
 constexpr int kRowsMaxTokens = 256;
 constexpr int kRowsPrefetchTokens = 16;  // residual values held in registers before the MMAs end
 constexpr uint32_t kRowsSlack = kTcTileRows * 128u;  // MMA window over-read past the ring
@@ -76,8 +89,14 @@ struct RowsParams {
   int stages;    // ring depth
   int groups;    // K blocks packed into one MMA along its diagonal (1, 2 or 4)
   int prefetch;  // W stages requested before griddepcontrol.wait (1..stages)
+  int issuers;   // MMA-issuing threads (1 or 2), each into its own accumulator
   int tmem_cols;
 };
+
+// Scratch bytes of the decode epilogue's warm-up pass: the end of the
+// 1024-byte barrier region (at most 32 stages: 2 x 32 + 2 barriers, the TMEM
+// address and the abort flag end below byte 544).
+constexpr uint32_t kRowsWarmScratch = 960;
 
 __host__ __device__ inline uint32_t rows_stage_bytes(int kbps, int rb, int nt) {
   return (uint32_t)kbps * ((uint32_t)rb * 128u + (uint32_t)nt * 128u);
@@ -237,10 +256,10 @@ __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
-      mbar_init(smem_u32(&empty[s]), 1);
+      mbar_init(smem_u32(&empty[s]), (uint32_t)p.issuers);  // one commit per issuer and stage
     }
-    mbar_init(smem_u32(acc_full), 1);
-    mbar_init(smem_u32(drain), 1);
+    mbar_init(smem_u32(acc_full), (uint32_t)p.issuers);
+    mbar_init(smem_u32(drain), (uint32_t)p.issuers);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -319,9 +338,13 @@ __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, 
           break;
         }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+  } else if (warp == 1 || warp == 6) {
+    // ----------------------------------------------------------- MMA issuers
+    const int iss = warp == 6 ? 1 : 0;
+    if (lane == 0 && iss < p.issuers) {
+      // Issuer i takes MMA windows i, i + issuers, ... of every stage into
+      // accumulator i (G * NT columns each).
+      const uint32_t dacc = tmem + (uint32_t)(iss * p.groups * p.NT);
       const uint32_t idesc = idesc_bf16_f32(kTcTileRows, p.groups * p.NT);
       // Descriptors differ only in their start-address field (address >> 4):
       // build the ring bases once and add offsets.
@@ -337,11 +360,11 @@ __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, 
           break;
         }
         tc_fence_after();
-        for (int j = 0; j < p.kbps; j += p.groups) {
+        for (int j = iss * p.groups; j < p.kbps; j += p.issuers * p.groups) {
 #pragma unroll
           for (int kk = 0; kk < kTcKBlock / 16; ++kk) {
-            const bool first = (s == 0) && (j == 0) && (kk == 0);
-            mma_bf16(tmem, wd + ((j * wblk + kk * 32u) >> 4), ad + ((j * ablk + kk * 32u) >> 4), idesc,
+            const bool first = (s == 0) && (j == iss * p.groups) && (kk == 0);
+            mma_bf16(dacc, wd + ((j * wblk + kk * 32u) >> 4), ad + ((j * ablk + kk * 32u) >> 4), idesc,
                      first ? 0u : 1u);
           }
         }
@@ -384,59 +407,77 @@ __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, 
 #pragma unroll
       for (int m = 0; m < kRowsPrefetchTokens; ++m)
         res[m] = (owner && m < io.M) ? __bfloat162float(io.R[(size_t)m * io.ldr + n0 + L]) : 0.f;
-      bool ok = mbar_wait_or_abort(smem_u32(acc_full), 0, abort_flag);
-      if (!ok) {
-        if (!*abort_flag) report_error(p.err, kErrWaitMma);
-        *abort_flag = 1;
-      }
-      ok = __all_sync(0xffffffffu, ok);
-      tc_fence_after();
-      float v[16];
+      // Pass 0 warms the code below while the MMAs run; pass 1 is the real
+      // one.  The pass number goes through an opaque move so that the
+      // compiler keeps one copy of the loop body for both passes.
+#pragma unroll 1
+      for (int pass = 0; pass < 2; ++pass) {
+        int passv;
+        asm volatile("mov.b32 %0, %1;" : "=r"(passv) : "r"(pass));
+        const bool real = passv != 0;
+        bool ok = true;
+        if (real) {
+          ok = mbar_wait_or_abort(smem_u32(acc_full), 0, abort_flag);
+          if (!ok) {
+            if (!*abort_flag) report_error(p.err, kErrWaitMma);
+            *abort_flag = 1;
+          }
+          ok = __all_sync(0xffffffffu, ok);
+        }
+        tc_fence_after();
+        float v[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) v[i] = 0.f;
-      if (ok && q * 32 < G * p.RB) {  // warp-uniform: this warp holds rows of the MMA window in use
-        const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16);
-        if (G == 1 || (q + 1) * 32 <= p.RB) {
-          tmem_ld16(taddr, v);  // group-0 columns only
-        } else if (q * 32 >= p.RB) {
-          tmem_ld16(taddr + 16u, v);  // group-1 columns only
-        } else {
-          float v1[16];
-          tmem_ld16(taddr, v);
-          tmem_ld16(taddr + 16u, v1);
-          if (L >= p.RB) {
+        for (int i = 0; i < 16; ++i) v[i] = 0.f;
+        if (ok && q * 32 < G * p.RB) {  // warp-uniform: this warp holds rows of the MMA window in use
+          // Accumulator i at columns [i C, (i + 1) C), C = G * 16; pass 0
+          // reads the columns after them, which no MMA writes.
+          const uint32_t C = (uint32_t)(G * kRowsPrefetchTokens);
+          const uint32_t taddr =
+              tmem + ((uint32_t)(q * 32) << 16) + (real ? 0u : (uint32_t)p.issuers * C);
+          const bool two = p.issuers == 2;
+          if (G == 1 || (q + 1) * 32 <= p.RB) {
+            tmem_ld16_sum(taddr, C, two, v);  // group-0 columns only
+          } else if (q * 32 >= p.RB) {
+            tmem_ld16_sum(taddr + 16u, C, two, v);  // group-1 columns only
+          } else {
+            float v1[16];
+            tmem_ld16_sum(taddr, C, two, v);
+            tmem_ld16_sum(taddr + 16u, C, two, v1);
+            if (L >= p.RB) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = v1[i];
+              for (int i = 0; i < 16; ++i) v[i] = v1[i];
+            }
           }
         }
-      }
-      if (ok && helper) {
+        const uint32_t x = real ? xch : base + kRowsWarmScratch;
+        if (ok && helper) {
 #pragma unroll
-        for (int i = 0; i < 16; i += 4)
-          asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(xch + (uint32_t)i * 4u), "f"(v[i]),
-                       "f"(v[i + 1]), "f"(v[i + 2]), "f"(v[i + 3])
-                       : "memory");
-      }
-      named_bar_sync(1, 128);
-      if (ok && owner) {
-        if (G == 2) {
-#pragma unroll
-          for (int i = 0; i < 16; i += 4) {
-            float a0, a1, a2, a3;
-            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                         : "=f"(a0), "=f"(a1), "=f"(a2), "=f"(a3)
-                         : "r"(xch + (uint32_t)i * 4u)
+          for (int i = 0; i < 16; i += 4)
+            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(x + (uint32_t)i * 4u), "f"(v[i]),
+                         "f"(v[i + 1]), "f"(v[i + 2]), "f"(v[i + 3])
                          : "memory");
-            v[i] += a0;
-            v[i + 1] += a1;
-            v[i + 2] += a2;
-            v[i + 3] += a3;
-          }
         }
-        __nv_bfloat16* yp = io.Y + n0 + L;
+        named_bar_sync(1, 128);
+        if (ok && owner) {
+          if (G == 2) {
 #pragma unroll
-        for (int m = 0; m < kRowsPrefetchTokens; ++m)
-          if (m < io.M) yp[(size_t)m * io.ldy] = __float2bfloat16_rn(v[m] + res[m]);
+            for (int i = 0; i < 16; i += 4) {
+              float a0, a1, a2, a3;
+              asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                           : "=f"(a0), "=f"(a1), "=f"(a2), "=f"(a3)
+                           : "r"(x + (uint32_t)i * 4u)
+                           : "memory");
+              v[i] += a0;
+              v[i + 1] += a1;
+              v[i + 2] += a2;
+              v[i + 3] += a3;
+            }
+          }
+          __nv_bfloat16* yp = io.Y + n0 + L;
+#pragma unroll
+          for (int m = 0; m < kRowsPrefetchTokens; ++m)
+            st_global_bf16_if(yp + (size_t)m * io.ldy, __float2bfloat16_rn(v[m] + res[m]), real && m < io.M);
+        }
       }
     } else if (p.NT == 32 && p.groups <= 2 && p.groups * p.RB <= kTcTileRows) {
       rows_epilogue_wide<32>(p, io, n0, tmem, w_ring, acc_full, abort_flag, q, lane);
@@ -653,7 +694,9 @@ __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, 
   }
 }
 
-__global__ void __launch_bounds__(kRowsThreads, 1)
+// Two CTAs per SM where their shared memory allows (the register budget is
+// sized for it; the default configuration of untabulated shapes relies on it).
+__global__ void __launch_bounds__(kRowsThreads, 2)
     rows_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA,
                        const RowsParams p) {
   const RowsIO io{&tmW, &tmA, p.R, p.Y, p.ldr, p.ldy, p.M};
@@ -688,7 +731,7 @@ struct RowsGroupList {
   int count;
 };
 
-__global__ void __launch_bounds__(kRowsThreads, 1)
+__global__ void __launch_bounds__(kRowsThreads, 2)
     rows_grouped_kernel(const __grid_constant__ RowsGroupList list, const RowsParams p) {
   const int e = (int)blockIdx.x % list.count;
   const int slab = (int)blockIdx.x / list.count;
@@ -770,7 +813,13 @@ inline int rows_plan(const sgr_config& c, int sms, int M, int N, int K, RowsPara
     p->groups /= 2;
   if (rows_stage_floats(p->groups, rb, nt) * 4 > (size_t)c.stages * rows_stage_bytes(c.k_blocks_per_stage, rb, nt))
     return SGR_ERR_UNSUPPORTED;
-  p->tmem_cols = detail::pow2_at_least(p->groups * nt);
+  // Two MMA issuers where the 16-token decode epilogue (which adds the two
+  // accumulators) serves the tile and every stage has at least two windows;
+  // that epilogue also reserves as many columns again for its warm-up pass.
+  const bool decode_epi = nt == kRowsPrefetchTokens && p->groups <= 2 && p->groups * rb <= kTcTileRows;
+  p->issuers = decode_epi && c.k_blocks_per_stage >= 2 * p->groups ? 2 : 1;
+  const int acc_cols = p->issuers * p->groups * nt;
+  p->tmem_cols = detail::pow2_at_least(decode_epi ? 2 * acc_cols : acc_cols);
   *grid = (N + rb - 1) / rb;
   *smem = sm;
   return SGR_OK;

@@ -28,15 +28,20 @@
 // With K = 32 codes per instruction this is a quarter of the MMAs per weight
 // byte of the BF16 kernel.
 //
-// Roles (320 threads).  Warp 0 lane 0 streams the weight codes with TMA into
+// Roles (352 threads).  Warp 0 lane 0 streams the weight codes with TMA into
 // a ring (they do not depend on the preceding kernel, so they stream from the
-// CTA's start).  Warps 2-9 wait for the preceding kernel, read A once into
-// registers (the threads of a token split its K range), find each token's
-// scale, then write the split activation operand into shared memory stage by
-// stage in K order, announcing each stage on its own barrier; token rows past
-// M are only zero-filled.  Warp 1 owns tensor memory; its lane 0 issues the
-// MMAs of a stage once its codes have landed and its activations are
-// written.  Warps 2-5 then run the epilogue.
+// CTA's start).  Warps 2-9 zero the operand, wait for the preceding kernel,
+// read A once (the threads of a token split its K range), find each token's
+// scale, then write the split activation operand into shared memory in K
+// order, announcing each stage on its own barrier (with A held in registers:
+// stage 0 first, then all others at once).  Warp 1 owns tensor memory; its
+// lane 0 issues the MMAs of a stage once its codes have landed and its
+// activations are written -- with two issuers, the even windows, while lane
+// 0 of warp 10 issues the odd ones into a second accumulator (a small-N MMA
+// occupies its issuing thread for ~75 cycles); the epilogue adds the two in
+// a fixed order.  Warps 2-5 then run the epilogue.  With A held in
+// registers the epilogue runs a warm-up pass over its instructions while the
+// MMAs finish (see the epilogue).
 //
 // The conversion runs on every CTA (each needs all of A), on the conversion
 // pipe: per value one packed FP32 -> FP16 conversion share and three packed
@@ -56,7 +61,7 @@
 
 namespace sgr {
 
-constexpr int kW8sThreads = 320;      // warp 0 codes, warp 1 MMA, warps 2-9 activations (2-5 epilogue)
+constexpr int kW8sThreads = 352;      // warp 0 codes, warps 1 and 10 MMA, warps 2-9 activations (2-5 epilogue)
 constexpr int kW8sConvThreads = 256;  // activation converters
 constexpr int kW8sKBlock = 128;       // codes per 128-byte swizzled row
 constexpr int kW8sMaxStages = 8;
@@ -79,20 +84,39 @@ struct W8sParams {
   int k_stages;  // ceil(kb / kbps)
   int stages;    // weight ring depth
   int groups;    // K blocks per MMA window (1, 2 or 4)
+  int issuers;   // MMA-issuing threads (1 or 2), each into its own accumulator
   int tmem_cols;
 };
 
 __host__ __device__ inline uint32_t w8s_wstage_bytes(int kbps, int rb) { return (uint32_t)kbps * rb * 128u; }
 __host__ __device__ inline uint32_t w8s_bblock_bytes(int nt) { return 2u * nt * 128u; }
 
-// Shared memory: alignment slack, barrier region, weight ring, activation
-// operand, and room for the last MMA window's over-read past the ring when
-// the operand behind it is shorter than that.
+// Bytes after the weight ring that the kernel's MMAs may read: the
+// activation operand, or the last MMA window's over-read past the ring when
+// that is longer.
+__host__ __device__ inline uint32_t w8s_operand_span(int kbp, int nt, int rb) {
+  const uint32_t act = (uint32_t)kbp * w8s_bblock_bytes(nt);
+  const uint32_t over = (uint32_t)(kTcTileRows - rb) * 128u;
+  return act > over ? act : over;
+}
+
+constexpr uint32_t kW8sScratchBytes = 256;  // epilogue warm-up pass, after the operand span
+
+// Whether each converter thread's share of its token row fits the registers
+// (kW8sStageVec 16-byte vectors; all 256 threads over the next power of two
+// >= M tokens): then A is read once into registers, the conversion ends well
+// before the MMAs, and the kernel instance with the epilogue warm-up runs.
+__host__ __device__ inline bool w8s_in_regs(int M, int K) {
+  const int mp = M <= 1 ? 1 : (M <= 2 ? 2 : (M <= 4 ? 4 : (M <= 8 ? 8 : 16)));
+  const int tpt = kW8sConvThreads / mp;
+  return (K / 8 + tpt - 1) / tpt <= kW8sStageVec;
+}
+
+// Shared memory: alignment slack, barrier region, weight ring, operand span,
+// scratch.
 __host__ __device__ inline size_t w8s_smem_bytes(int stages, int kbps, int rb, int nt, int kbp) {
   const size_t ring = (size_t)stages * w8s_wstage_bytes(kbps, rb);
-  const size_t act = (size_t)kbp * w8s_bblock_bytes(nt);
-  const size_t over = (size_t)(kTcTileRows - rb) * 128u;
-  return 1024 + 1024 + ring + act + (over > act ? over - act : 0);
+  return 1024 + 1024 + ring + w8s_operand_span(kbp, nt, rb) + kW8sScratchBytes;
 }
 
 // Four floats -> four E4M3 codes (round to nearest even, saturating), byte i
@@ -170,6 +194,9 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int m, int n) {
   return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
+// kWarmEpi: the epilogue's warm-up pass (the instance for w8s_in_regs(M, K);
+// the other instance has no trace of it).
+template <bool kWarmEpi>
 __global__ void __launch_bounds__(kW8sThreads, 1)
     w8s_kernel(const __grid_constant__ CUtensorMap tmW, const W8sParams p) {
   extern __shared__ unsigned char smem_raw[];
@@ -199,11 +226,11 @@ __global__ void __launch_bounds__(kW8sThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(smem_u32(&wfull[s]), 1);
-      mbar_init(smem_u32(&wempty[s]), 1);
+      mbar_init(smem_u32(&wempty[s]), (uint32_t)p.issuers);  // one commit per issuer and stage
     }
     for (int k = 0; k < p.k_stages; ++k) mbar_init(smem_u32(&bready[k]), 1);
-    mbar_init(smem_u32(acc_full), 1);
-    mbar_init(smem_u32(drain), 1);
+    mbar_init(smem_u32(acc_full), (uint32_t)p.issuers);
+    mbar_init(smem_u32(drain), (uint32_t)p.issuers);
     for (int t = 0; t < kW8sMaxTokens; ++t) tok_mag[t] = 0u;
     *abort_flag = 0;
     fence_mbar_init();
@@ -253,9 +280,13 @@ __global__ void __launch_bounds__(kW8sThreads, 1)
         ok = mbar_wait(smem_u32(&wfull[t % S]), (t / S) & 1);
       if (!ok) report_error(p.err, kErrDrain);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+  } else if (warp == 1 || warp == 10) {
+    // ----------------------------------------------------------- MMA issuers
+    // Issuer i takes MMA windows i, i + issuers, ... of every stage into
+    // accumulator i (G * 2 NT columns each).
+    const int iss = warp == 10 ? 1 : 0;
+    if (lane == 0 && iss < p.issuers) {
+      const uint32_t dacc = tmem + (uint32_t)(iss * G * 2 * p.NT);
       const uint32_t idesc = idesc_e4m3_f32(kTcTileRows, G * 2 * p.NT);
       const uint64_t wdesc0 = smem_desc_sw128(w_ring);
       const uint64_t bdesc0 = smem_desc_sw128(b_buf);
@@ -271,12 +302,12 @@ __global__ void __launch_bounds__(kW8sThreads, 1)
         }
         tc_fence_after();
         const int j0 = s * p.kbps;
-        for (int w = 0; w < p.kbps && j0 + w < p.kb; w += G) {  // windows starting inside K
+        for (int w = iss * G; w < p.kbps && j0 + w < p.kb; w += p.issuers * G) {  // windows starting inside K
           const uint64_t wd = wdesc0 + (((uint32_t)slot * w_stage + (uint32_t)w * wbox) >> 4);
           const uint64_t bd = bdesc0 + (((uint32_t)(j0 + w) * bblk) >> 4);
 #pragma unroll
           for (int kk = 0; kk < kW8sKBlock / 32; ++kk) {
-            mma_e4m3(tmem, wd + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, first ? 0u : 1u);
+            mma_e4m3(dacc, wd + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, first ? 0u : 1u);
             first = false;
           }
         }
@@ -297,8 +328,15 @@ __global__ void __launch_bounds__(kW8sThreads, 1)
     }
   } else {
     // ------------------------------------------------ activation converters
-    pdl_wait();  // A and R may come from the preceding kernel; Y may be read by it
     const int ct = threadIdx.x - 64;  // 0 .. 255
+    // The operand starts as zeros everywhere (rows of tokens M .. NT-1, the
+    // tail of a ragged last block, the padding block of the last MMA
+    // window): this CTA's own shared memory, so before the dependency wait.
+    {
+      const uint32_t z1 = b_buf + (uint32_t)p.kbp * bblk;
+      for (uint32_t a = b_buf + (uint32_t)ct * 16u; a < z1; a += (uint32_t)kW8sConvThreads * 16u)
+        asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
+    }
     // Threads per token: all 256 over the next power of two >= M tokens.
     const int mp = p.M <= 1 ? 1 : (p.M <= 2 ? 2 : (p.M <= 4 ? 4 : (p.M <= 8 ? 8 : 16)));
     const int tpt = kW8sConvThreads / mp;
@@ -306,85 +344,46 @@ __global__ void __launch_bounds__(kW8sThreads, 1)
     const int nvec = p.K / 8;  // 16-byte vectors per token row
     const bool row_ok = t < p.M;
     const __nv_bfloat16* arow = p.A + (size_t)(row_ok ? t : 0) * p.lda;
-    // Rows of tokens M .. NT-1 (hi and lo) hold zeros in every block.
-    if (p.M < p.NT) {
-      const int zrows = p.NT - p.M;  // per part
-      const int per_blk = 2 * zrows * 8;  // 16-byte chunks per block
-      for (int i = ct; i < p.kbp * per_blk; i += kW8sConvThreads) {
-        const int j = i / per_blk, rem = i % per_blk;
-        const int row = (rem / 8) < zrows ? p.M + rem / 8 : p.NT + p.M + (rem / 8 - zrows);
-        const uint32_t a = b_buf + (uint32_t)j * bblk + (uint32_t)row * 128u + (uint32_t)(rem % 8) * 16u;
-        asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
-      }
-    }
     // When a thread's share of its token row is at most kW8sStageVec vectors
     // (M <= 4 at K = 3584), the max pass keeps them in registers (cur[i] =
-    // vector part + i tpt) and the stage loop converts them from there;
-    // otherwise the stage loop reads each stage's vectors again, one stage
-    // ahead.  (Reading them again puts one memory round trip per stage on the
-    // converters' path, which then paces the MMAs and the weight ring.)
-    const int nreg = (nvec + tpt - 1) / tpt;
-    const bool in_regs = nreg <= kW8sStageVec;  // the same in every thread: depends on M and K only
-    uint4 cur[kW8sStageVec], nxt[kW8sStageVec];
-    uint32_t mag = 0;  // largest |A[t,k]| of this thread as a BF16 magnitude pattern
-    if (in_regs) {
-#pragma unroll
-      for (int i = 0; i < kW8sStageVec; ++i) {
-        const int v = part + i * tpt;
-        cur[i] = (row_ok && v < nvec) ? *reinterpret_cast<const uint4*>(arow + (size_t)v * 8) : make_uint4(0u, 0u, 0u, 0u);
-      }
-#pragma unroll
-      for (int i = 0; i < kW8sStageVec; ++i) {
-        const uint32_t w4[4] = {cur[i].x, cur[i].y, cur[i].z, cur[i].w};
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          const uint32_t lo = w4[h] & 0x7FFFu, hi = (w4[h] >> 16) & 0x7FFFu;
-          mag = lo > mag ? lo : mag;
-          mag = hi > mag ? hi : mag;
-        }
-      }
-    } else if (row_ok) {
-#pragma unroll 4
-      for (int v = part; v < nvec; v += tpt) {
-        const uint4 a = *reinterpret_cast<const uint4*>(arow + (size_t)v * 8);
-        const uint32_t w4[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          const uint32_t lo = w4[h] & 0x7FFFu, hi = (w4[h] >> 16) & 0x7FFFu;
-          mag = lo > mag ? lo : mag;
-          mag = hi > mag ? hi : mag;
-        }
-      }
-    }
-    // The token's threads: a lane group of one warp (tpt <= 32) or whole warps.
-    for (int o = (tpt < 32 ? tpt : 32) / 2; o > 0; o >>= 1) {
-      const uint32_t other = __shfl_xor_sync(0xffffffffu, mag, o);
-      mag = other > mag ? other : mag;
-    }
-    if ((lane & ((tpt < 32 ? tpt : 32) - 1)) == 0) atomicMax(&tok_mag[t], mag);
-    named_bar_sync(2, kW8sConvThreads);
-    mag = tok_mag[t];
-    // Scale exponent: max |b| in [2^7, 2^8) (for a zero or subnormal maximum
-    // the largest scale keeps everything representable).
-    const int ex = (int)(mag >> 7);  // biased exponent of the maximum
-    int k = ex == 0 ? 126 : 134 - ex;
-    k = k < -120 ? -120 : (k > 126 ? 126 : k);
-    if (part == 0) tok_k[t] = k;
-    const float sc = exp2i(k);
-    // Zero the operand's blocks beyond K (a ragged last block and the padding
-    // block of the last MMA window) before the valid codes are written.
-    const int kb_full = p.K / kW8sKBlock;
-    {
-      const uint32_t z0 = b_buf + (uint32_t)kb_full * bblk, z1 = b_buf + (uint32_t)p.kbp * bblk;
-      for (uint32_t a = z0 + (uint32_t)ct * 16u; a < z1; a += (uint32_t)kW8sConvThreads * 16u)
-        asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
-    }
-    named_bar_sync(2, kW8sConvThreads);
-    // Stage by stage (kbps blocks of 128 codes = kbps * 16 vectors), in K
-    // order: from the registers of the max pass, or read again (from L2) with
-    // the next stage's vectors requested while this one is converted.
-    const int vps = p.kbps * (kW8sKBlock / 8);  // vectors per stage
+    // vector part + i tpt) and converts them from there; otherwise the stage
+    // loop reads each stage's vectors again, one stage ahead.  (Reading them
+    // again puts one memory round trip per stage on the converters' path,
+    // which then paces the MMAs and the weight ring.)
+    const bool in_regs = w8s_in_regs(p.M, p.K);  // the same in every thread
+    const int vps = p.kbps * (kW8sKBlock / 8);  // vectors per stage (kbps blocks of 128 codes)
     const int voff = ((part % tpt) + tpt) % tpt;
+    uint4 cur[kW8sStageVec], nxt[kW8sStageVec];
+    float sc = 1.f;
+    // The token's largest |A[t,k]| (a BF16 magnitude pattern, this thread's
+    // share in `mag`) over its threads -- a lane group of one warp (tpt <=
+    // 32) or whole warps -- and from it the scale exponent: max |b| in
+    // [2^7, 2^8) (for a zero or subnormal maximum the largest scale keeps
+    // everything representable), published in tok_k for the epilogue.
+    auto token_scale = [&](uint32_t mag) {
+      for (int o = (tpt < 32 ? tpt : 32) / 2; o > 0; o >>= 1) {
+        const uint32_t other = __shfl_xor_sync(0xffffffffu, mag, o);
+        mag = other > mag ? other : mag;
+      }
+      if ((lane & ((tpt < 32 ? tpt : 32) - 1)) == 0) atomicMax(&tok_mag[t], mag);
+      named_bar_sync(2, kW8sConvThreads);
+      mag = tok_mag[t];
+      const int ex = (int)(mag >> 7);  // biased exponent of the maximum
+      int k = ex == 0 ? 126 : 134 - ex;
+      k = k < -120 ? -120 : (k > 126 ? 126 : k);
+      if (part == 0) tok_k[t] = k;
+      sc = exp2i(k);
+    };
+    auto max_mag = [](const uint4& a, uint32_t mag) {
+      const uint32_t w4[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const uint32_t lo = w4[h] & 0x7FFFu, hi = (w4[h] >> 16) & 0x7FFFu;
+        mag = lo > mag ? lo : mag;
+        mag = hi > mag ? hi : mag;
+      }
+      return mag;
+    };
     // Split one 16-byte vector (8 activations of token t at K = 8 v) into its
     // hi and lo E4M3 parts and store both into the operand's block.
     auto convert_store = [&](const uint4& a, int v) {
@@ -428,9 +427,22 @@ __global__ void __launch_bounds__(kW8sThreads, 1)
       }
     };
     if (in_regs) {
-      for (int st = 0; st < KS; ++st) {
-        const int v0 = st * vps;
-        const int v1 = v0 + vps < nvec ? v0 + vps : nvec;
+      pdl_wait();  // A and R may come from the preceding kernel; Y may be read by it
+      uint32_t mag = 0;
+#pragma unroll
+      for (int i = 0; i < kW8sStageVec; ++i) {
+        const int v = part + i * tpt;
+        cur[i] = (row_ok && v < nvec) ? *reinterpret_cast<const uint4*>(arow + (size_t)v * 8)
+                                      : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int i = 0; i < kW8sStageVec; ++i) mag = max_mag(cur[i], mag);
+      token_scale(mag);
+      // Stage 0 first (the first MMAs wait for it), then all the others
+      // (one barrier each: the conversion of a whole stage is short here).
+      for (int ph = 0; ph < 2; ++ph) {
+        const int v0 = ph == 0 ? 0 : vps;
+        const int v1 = ph == 0 ? (vps < nvec ? vps : nvec) : nvec;
         if (row_ok) {
 #pragma unroll
           for (int i = 0; i < kW8sStageVec; ++i) {
@@ -440,9 +452,24 @@ __global__ void __launch_bounds__(kW8sThreads, 1)
         }
         fence_proxy_async_smem();  // the generic-proxy writes become visible to the tensor core
         named_bar_sync(2, kW8sConvThreads);
-        if (ct == 0) mbar_arrive(smem_u32(&bready[st]));
+        if (ct == 0) {
+          if (ph == 0) {
+            mbar_arrive(smem_u32(&bready[0]));
+          } else {
+            for (int st = 1; st < KS; ++st) mbar_arrive(smem_u32(&bready[st]));
+          }
+        }
       }
     } else {
+      pdl_wait();  // A and R may come from the preceding kernel; Y may be read by it
+      uint32_t mag = 0;
+      if (row_ok) {
+#pragma unroll 4
+        for (int v = part; v < nvec; v += tpt) mag = max_mag(*reinterpret_cast<const uint4*>(arow + (size_t)v * 8), mag);
+      }
+      token_scale(mag);
+      // Stage by stage in K order, each stage's vectors read again (from L2)
+      // with the next stage's requested while this one is converted.
       load_stage(0, cur);
       for (int st = 0; st < KS; ++st) {
         load_stage(st + 1, nxt);
@@ -470,6 +497,13 @@ __global__ void __launch_bounds__(kW8sThreads, 1)
       // Thread on TMEM lane L = g RB + r (g < G) holds window group g's sums
       // for W row n0 + r; groups 1 .. G-1 hand theirs to group 0's thread
       // through the drained weight ring, which adds them in group order.
+      // With A held in registers the conversion ends microseconds before the
+      // accumulator is ready, and the epilogue first runs a warm-up pass over
+      // its own instructions in that time (tensor-memory columns no MMA
+      // writes, a scratch area past the operand, stores predicated off): the
+      // first run of a code path in a CTA costs ~0.7 us more than the next
+      // while the weight stream saturates L2.  Otherwise (the conversion
+      // ends close to the MMAs) it runs once.
       const int q = warp & 3;
       const int L = q * 32 + lane;
       const int g = L / p.RB;
@@ -482,69 +516,85 @@ __global__ void __launch_bounds__(kW8sThreads, 1)
       for (int m = 0; m < kW8sMaxTokens; ++m)
         res[m] = (owner && m < p.M) ? __bfloat162float(p.R[(size_t)m * p.ldr + n0 + r]) : 0.f;
       const float wscale = owner ? p.scale[n0 + r] : 0.f;
-      bool ok = mbar_wait_sleepy_or_abort(smem_u32(acc_full), 0, abort_flag);
-      if (!ok) {
-        if (!*abort_flag) report_error(p.err, kErrWaitMma);
-        *abort_flag = 1;
-      }
-      ok = __all_sync(0xffffffffu, ok);
-      tc_fence_after();
-      float v[kW8sMaxTokens];
-#pragma unroll
-      for (int m = 0; m < kW8sMaxTokens; ++m) v[m] = 0.f;
-      if (ok && q * 32 < G * p.RB) {  // warp-uniform: this warp holds rows of the MMA window in use
-        const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16);
-        const int glo = (q * 32) / p.RB;
-        const int ghi = min(G - 1, (q * 32 + 31) / p.RB);
-        for (int gg = glo; gg <= ghi; ++gg) {
-          // columns [2 NT gg, 2 NT gg + NT): hi part, then NT columns of the lo part
-          float hi16[16], lo16[16];
-          if (NT == 16) {
-            tmem_ld16(taddr + (uint32_t)(gg * 32), hi16);  // warp-collective
-            tmem_ld16(taddr + (uint32_t)(gg * 32 + 16), lo16);
-          } else {
-            tmem_ld16(taddr + (uint32_t)(gg * 16), hi16);  // 8 hi then 8 lo columns
-#pragma unroll
-            for (int m = 0; m < 8; ++m) lo16[m] = hi16[8 + m];
-          }
-          if (gg == g) {
-#pragma unroll
-            for (int m = 0; m < kW8sMaxTokens; ++m)
-              if (m < NT) v[m] = hi16[m] + lo16[m] * 0.0625f;
-          }
-        }
-      }
       const uint32_t xch0 = w_ring + (uint32_t)(helper || owner ? r : 0) * 80u;  // 16 floats + pad per row
       const uint32_t xstep = (uint32_t)p.RB * 80u;
-      if (ok && helper) {
-        const uint32_t dst = xch0 + (uint32_t)(g - 1) * xstep;
+      const uint32_t scratch = b_buf + (uint32_t)w8s_operand_span(p.kbp, p.NT, p.RB);
+#pragma unroll 1
+      for (int pass = kWarmEpi ? 0 : 1; pass < 2; ++pass) {
+        int passv;  // opaque to the compiler: one copy of the loop body serves both passes
+        asm volatile("mov.b32 %0, %1;" : "=r"(passv) : "r"(pass));
+        const bool real = passv != 0;
+        bool ok = true;
+        if (real) {
+          ok = mbar_wait_sleepy_or_abort(smem_u32(acc_full), 0, abort_flag);
+          if (!ok) {
+            if (!*abort_flag) report_error(p.err, kErrWaitMma);
+            *abort_flag = 1;
+          }
+          ok = __all_sync(0xffffffffu, ok);
+        }
+        tc_fence_after();
+        float v[kW8sMaxTokens];
 #pragma unroll
-        for (int m = 0; m < kW8sMaxTokens; m += 4)
-          asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(dst + (uint32_t)m * 4u), "f"(v[m]),
-                       "f"(v[m + 1]), "f"(v[m + 2]), "f"(v[m + 3])
-                       : "memory");
-      }
-      named_bar_sync(1, 128);
-      if (ok && owner) {
-        for (int gg = 1; gg < G; ++gg) {
-          const uint32_t src = xch0 + (uint32_t)(gg - 1) * xstep;
+        for (int m = 0; m < kW8sMaxTokens; ++m) v[m] = 0.f;
+        if (ok && q * 32 < G * p.RB) {  // warp-uniform: this warp holds rows of the MMA window in use
+          // Accumulator i (one per MMA issuer) at columns [i C, (i + 1) C).
+          const uint32_t C = (uint32_t)(G * 2 * NT);
+          const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (real ? 0u : (uint32_t)p.issuers * C);
+          const bool two = p.issuers == 2;
+          const int glo = (q * 32) / p.RB;
+          const int ghi = min(G - 1, (q * 32 + 31) / p.RB);
+          for (int gg = glo; gg <= ghi; ++gg) {
+            // columns [2 NT gg, 2 NT gg + NT): hi part, then NT columns of the lo part
+            float hi16[16], lo16[16];
+            if (NT == 16) {
+              tmem_ld16_sum(taddr + (uint32_t)(gg * 32), C, two, hi16);  // warp-collective
+              tmem_ld16_sum(taddr + (uint32_t)(gg * 32 + 16), C, two, lo16);
+            } else {
+              tmem_ld16_sum(taddr + (uint32_t)(gg * 16), C, two, hi16);  // 8 hi then 8 lo columns
 #pragma unroll
-          for (int m = 0; m < kW8sMaxTokens; m += 4) {
-            float a0, a1, a2, a3;
-            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                         : "=f"(a0), "=f"(a1), "=f"(a2), "=f"(a3)
-                         : "r"(src + (uint32_t)m * 4u)
-                         : "memory");
-            v[m] += a0;
-            v[m + 1] += a1;
-            v[m + 2] += a2;
-            v[m + 3] += a3;
+              for (int m = 0; m < 8; ++m) lo16[m] = hi16[8 + m];
+            }
+            if (gg == g) {
+#pragma unroll
+              for (int m = 0; m < kW8sMaxTokens; ++m)
+                if (m < NT) v[m] = hi16[m] + lo16[m] * 0.0625f;
+            }
           }
         }
-        __nv_bfloat16* yp = p.Y + n0 + r;
+        const uint32_t x0 = real ? xch0 : scratch;
+        const uint32_t xs = real ? xstep : 0u;
+        if (ok && helper) {
+          const uint32_t dst = x0 + (uint32_t)(g - 1) * xs;
 #pragma unroll
-        for (int m = 0; m < kW8sMaxTokens; ++m)
-          if (m < p.M) yp[(size_t)m * p.ldy] = __float2bfloat16_rn(fmaf(v[m] * exp2i(-tok_k[m]), wscale, res[m]));
+          for (int m = 0; m < kW8sMaxTokens; m += 4)
+            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(dst + (uint32_t)m * 4u), "f"(v[m]),
+                         "f"(v[m + 1]), "f"(v[m + 2]), "f"(v[m + 3])
+                         : "memory");
+        }
+        named_bar_sync(1, 128);
+        if (ok && owner) {
+          for (int gg = 1; gg < G; ++gg) {
+            const uint32_t src = x0 + (uint32_t)(gg - 1) * xs;
+#pragma unroll
+            for (int m = 0; m < kW8sMaxTokens; m += 4) {
+              float a0, a1, a2, a3;
+              asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                           : "=f"(a0), "=f"(a1), "=f"(a2), "=f"(a3)
+                           : "r"(src + (uint32_t)m * 4u)
+                           : "memory");
+              v[m] += a0;
+              v[m + 1] += a1;
+              v[m + 2] += a2;
+              v[m + 3] += a3;
+            }
+          }
+          __nv_bfloat16* yp = p.Y + n0 + r;
+#pragma unroll
+          for (int m = 0; m < kW8sMaxTokens; ++m)
+            st_global_bf16_if(yp + (size_t)m * p.ldy,
+                              __float2bfloat16_rn(fmaf(v[m] * exp2i(-tok_k[m]), wscale, res[m])), real && m < p.M);
+        }
       }
     }
   }
@@ -578,15 +628,23 @@ inline void w8s_default_config(int sms, int M, int N, int K, sgr_config* c) {
   c->token_tile = M <= 8 ? 8 : 16;
   const int rb = w8_rows_per_cta(sms, N);
   const int kb = (K + kW8sKBlock - 1) / kW8sKBlock;
-  // Three stages of four 128-code blocks (measured at N = 7168, K = 3584:
-  // ahead of a four-deep ring at 1-4 tokens), fewer if shared memory is short.
-  c->k_blocks_per_stage = 4;
+  // Measured at N = 7168, K = 3584 (graph of calls over distinct code
+  // copies): with A in registers (up to 4 tokens) four stages of four
+  // 128-code blocks (8.2-8.7 us, ahead of 3 or 5-7 stages and of 2 x 8);
+  // above, where each stage's activations are read again, two stages of
+  // eight (9.8-10.0 us at 5-8 tokens, ahead of 3-4 x 4).  Shallower rings
+  // where shared memory is short.
+  const bool regs = w8s_in_regs(M, K);
+  const int want_kbps = regs ? 4 : 8, want_stages = regs ? 4 : 2;
+  c->k_blocks_per_stage = 2;
   c->stages = 2;
-  for (int st = 3; st >= 2; --st)
-    if (w8s_smem_bytes(st, 4, rb, c->token_tile, kb + 4) <= 232448) {
-      c->stages = st;
-      break;
-    }
+  for (int kbps = want_kbps; kbps >= 2; kbps /= 2)
+    for (int st = want_stages; st >= 2; --st)
+      if (w8s_smem_bytes(st, kbps, rb, c->token_tile, kb + 4) <= 232448) {
+        c->k_blocks_per_stage = kbps;
+        c->stages = st;
+        return;
+      }
 }
 
 inline int w8s_plan(const sgr_config& c, int sms, int M, int N, int K, long long ldw, W8sParams* p, int* grid,
@@ -629,13 +687,21 @@ inline int w8s_plan(const sgr_config& c, int sms, int M, int N, int K, long long
   p->k_stages = (kb + kbps - 1) / kbps;
   p->stages = c.stages;
   p->groups = groups;
-  p->tmem_cols = detail::pow2_at_least(groups * 2 * nt);
+  // Two MMA issuers when every stage has two or more windows and the second
+  // issuer has one in the first stage (otherwise its accumulator would stay
+  // unwritten); the epilogue's warm-up pass reads as many columns again.
+  p->issuers = kbps >= 2 * groups && kb > groups ? 2 : 1;
+  p->tmem_cols = detail::pow2_at_least(2 * p->issuers * groups * 2 * nt);
   *grid = (N + rb - 1) / rb;
   *smem = sm;
   return SGR_OK;
 }
 
-inline cudaError_t w8s_init_device() { return set_kernel_smem_attrs(reinterpret_cast<const void*>(w8s_kernel)); }
+inline cudaError_t w8s_init_device() {
+  cudaError_t e = set_kernel_smem_attrs(reinterpret_cast<const void*>(w8s_kernel<true>));
+  if (e == cudaSuccess) e = set_kernel_smem_attrs(reinterpret_cast<const void*>(w8s_kernel<false>));
+  return e;
+}
 
 inline int w8s_launch(const sgr_config& c, int sms, unsigned* err, const void* A, long long lda, const void* Wq,
                       long long ldw, const float* scale, const void* R, long long ldr, void* Y, long long ldy, int M,
@@ -665,7 +731,7 @@ inline int w8s_launch(const sgr_config& c, int sms, unsigned* err, const void* A
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
   lc.numAttrs = pdl ? 1 : 0;
-  if (cudaLaunchKernelEx(&lc, w8s_kernel, tmW, p) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&lc, w8s_in_regs(M, K) ? w8s_kernel<true> : w8s_kernel<false>, tmW, p) != cudaSuccess) {
     cudaGetLastError();
     return SGR_ERR_LAUNCH;
   }

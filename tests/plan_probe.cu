@@ -1,11 +1,12 @@
 // Host-only driver for tests/test_plans.py: runs the launch planners of the
-// row-slab, FP8 row-slab and tile kernels over a grid of shapes and launch
+// row-slab, FP8 row-slab, FP8 split-activation and tile kernels over a grid of shapes and launch
 // configurations and prints one JSON object per accepted plan.  No CUDA call
 // is made; the kernels' headers are included for their host planners only.
 #include <cstdio>
 
 #include "sgr_rows.cuh"
 #include "sgr_w8.cuh"
+#include "sgr_w8s.cuh"
 #include "sgr_gemm.cuh"
 #include "sgr_pair.cuh"
 
@@ -39,9 +40,9 @@ int main() {
             const size_t w_ring = (size_t)st * kb * p.RB * 128, a_ring = (size_t)st * kb * p.NT * 128;
             std::printf("{\"kind\": \"rows\", \"M\": %d, \"N\": %d, \"K\": %d, \"RB\": %d, \"NT\": %d, \"G\": %d, "
                         "\"kbps\": %d, \"stages\": %d, \"prefetch\": %d, \"k_stages\": %d, \"tmem_cols\": %d, "
-                        "\"grid\": %d, \"smem\": %zu, \"w_ring\": %zu, \"a_ring\": %zu}\n",
-                        M, N, K, p.RB, p.NT, p.groups, p.kbps, p.stages, p.prefetch, p.k_stages, p.tmem_cols, grid,
-                        smem, w_ring, a_ring);
+                        "\"issuers\": %d, \"grid\": %d, \"smem\": %zu, \"w_ring\": %zu, \"a_ring\": %zu}\n",
+                        M, N, K, p.RB, p.NT, p.groups, p.kbps, p.stages, p.prefetch, p.k_stages, p.tmem_cols,
+                        p.issuers, grid, smem, w_ring, a_ring);
           }
       // FP8 row-slab kernel
       for (int rb : {0, 8, 24, 32, 64, 128})
@@ -71,6 +72,30 @@ int main() {
                             (size_t)p.stages * sgr::wring_stage_bytes(fp4 != 0, p.kbps, p.RB),
                             (size_t)p.a_stages * sgr::w8_astage_bytes(p.kbps, p.NT));
               }
+            }
+      // FP8 split-activation kernel (up to 16 tokens)
+      if (M <= sgr::kW8sMaxTokens)
+        for (int rb : {0, 24, 32, 48, 64})
+          for (int kb : {1, 2, 4, 8})
+            for (int st : {2, 3, 4, 7, 8}) {
+              sgr_config c = {};
+              c.path = SGR_PATH_W8S;
+              c.ctas_per_sm = 1;
+              c.rows_per_stage = rb;
+              c.k_blocks_per_stage = kb;
+              c.stages = st;
+              c.token_tile = M <= 8 ? 8 : 16;
+              sgr::W8sParams p;
+              int grid = 0;
+              size_t smem = 0;
+              if (sgr::w8s_plan(c, sms, M, N, K, K, &p, &grid, &smem) != SGR_OK) continue;
+              std::printf("{\"kind\": \"w8s\", \"M\": %d, \"N\": %d, \"K\": %d, \"RB\": %d, \"NT\": %d, \"G\": %d, "
+                          "\"kbps\": %d, \"stages\": %d, \"k_stages\": %d, \"kb\": %d, \"kbp\": %d, "
+                          "\"issuers\": %d, \"tmem_cols\": %d, \"grid\": %d, \"smem\": %zu, \"ring\": %zu, "
+                          "\"span\": %u}\n",
+                          M, N, K, p.RB, p.NT, p.groups, p.kbps, p.stages, p.k_stages, p.kb, p.kbp, p.issuers,
+                          p.tmem_cols, grid, smem, (size_t)p.stages * sgr::w8s_wstage_bytes(p.kbps, p.RB),
+                          sgr::w8s_operand_span(p.kbp, p.NT, p.RB));
             }
       // tile kernel
       for (int tn : {64, 128, 192, 256})

@@ -29,7 +29,7 @@ def test_default_config_auto_matches_selected_path(M):
 # local (stack) bytes per thread: none, except a 16-byte local array in the
 # stream-K kernel (no register spills anywhere).
 @pytest.mark.parametrize("path,M,threads,local", [
-    (sgr.SGR_PATH_TC_ROWS, 4, 192, 0), (sgr.SGR_PATH_TILE, 1024, 192, 0), (sgr.SGR_PATH_SIMT, 4, 256, 0),
+    (sgr.SGR_PATH_TC_ROWS, 4, 224, 0), (sgr.SGR_PATH_TILE, 1024, 192, 0), (sgr.SGR_PATH_SIMT, 4, 256, 0),
     (sgr.SGR_PATH_TC, 8, None, 16), (sgr.SGR_PATH_W8, 4, 352, 0)])
 def test_kernel_resources(path, M, threads, local):
     r = sgr.sgr_kernel_resources(M, N, K, path=path)
@@ -39,6 +39,8 @@ def test_kernel_resources(path, M, threads, local):
     if threads is not None:
         assert r["threads"] == threads
     assert r["registers_per_thread"] * r["threads"] <= 65536
+    if path == sgr.SGR_PATH_TC_ROWS:  # two CTAs per SM where shared memory allows
+        assert 2 * r["registers_per_thread"] * r["threads"] <= 65536
 
 
 def test_fp8_default_config():

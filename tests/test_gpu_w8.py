@@ -327,6 +327,15 @@ def test_w8_auto_small_m_matches_tensor_core_path():
     compare(run(p, path=sgr.SGR_PATH_SIMT), want, "w8 CUDA-core M=1")
 
 
+@pytest.mark.parametrize("M", [3, 6, 12])
+def test_w8_auto_matches_oracle(M):
+    """AUTO at token counts served by the split-activation kernel's two
+    instances (3: A in registers; 6: A read per stage) and by the widening
+    kernel (12)."""
+    p = inputs.make_problem_w8(M, N_FULL, K_FULL, seed=60 + M)
+    compare(run(p), ref(p), f"w8 auto M={M}")
+
+
 def test_w8_simt_rejects():
     p = inputs.make_problem_w8(9, 256, 256, seed=3)
     with pytest.raises(sgr.SgrError) as e:  # more than 8 tokens

@@ -81,7 +81,7 @@ def test_w8s_every_kind_of_code(M, N, K):
     compare(run(p), ref(p), f"w8s codes {M}x{N}x{K}")
 
 
-@pytest.mark.parametrize("M", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 6, 8, 16])
 @pytest.mark.parametrize("seed", [0, 1, 2, 3])
 def test_w8s_full_size_m_sweep(M, seed):
     p = inputs.make_problem_w8(M, N_FULL, K_FULL, seed=seed)
@@ -165,6 +165,16 @@ def test_w8s_integer_inputs_exact():
                                 config=sgr.make_config(path=W8S))
     torch.cuda.synchronize()
     assert np.array_equal(bits(Y), bits(want.to(torch.bfloat16)))
+
+
+@pytest.mark.parametrize("M,kbps,stages,nt", [(1, 4, 4, 8), (4, 4, 4, 8), (5, 8, 2, 8), (8, 8, 2, 8), (9, 8, 2, 16),
+                                               (16, 8, 2, 16)])
+def test_w8s_default_configs(M, kbps, stages, nt):
+    """The measured defaults at the latent-MoE shape: four stages of four
+    128-code blocks while A fits the converters' registers (up to 4 tokens),
+    two stages of eight above."""
+    c = sgr.sgr_default_config(M, N_FULL, K_FULL, path=W8S)
+    assert (c.path, c.k_blocks_per_stage, c.stages, c.token_tile) == (W8S, kbps, stages, nt)
 
 
 W8S_CONFIGS = [

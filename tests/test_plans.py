@@ -41,13 +41,20 @@ def test_row_slab_plans(plans):
         assert p["G"] * p["RB"] <= 128 and p["G"] * p["NT"] <= 256, p            # one MMA window
         assert p["kbps"] % p["G"] == 0, p
         assert p["NT"] >= p["M"] and p["NT"] % 16 == 0, p
-        assert p["tmem_cols"] >= p["G"] * p["NT"] and p["tmem_cols"] <= 512, p
+        decode_epi = p["NT"] == 16 and p["G"] <= 2
+        # two MMA issuers (alternate windows, own accumulators) only under the
+        # 16-token epilogue that adds them, with two or more windows a stage
+        assert p["issuers"] == (2 if decode_epi and p["kbps"] >= 2 * p["G"] else 1), p
+        acc_cols = p["issuers"] * p["G"] * p["NT"]
+        # that epilogue's warm-up pass reads as many columns again, unwritten
+        assert p["tmem_cols"] >= (2 if decode_epi else 1) * acc_cols and p["tmem_cols"] <= 512, p
         assert p["grid"] * p["RB"] >= p["N"] > (p["grid"] - 1) * p["RB"], p      # every row, no empty CTA
         assert p["k_stages"] * p["kbps"] * 64 >= p["K"], p
         assert 1 <= p["prefetch"] <= p["stages"], p
         # landing and slot-free barriers per stage, accumulator and drain
         # barriers, the TMEM address and the abort flag
-        assert (2 * p["stages"] + 2) * 8 + 8 <= 1024, p
+        # (below the warm-up pass's scratch at byte 960 of the region)
+        assert (2 * p["stages"] + 2) * 8 + 8 <= 960, p
         drained = p["w_ring"] + p["a_ring"]
         # hand-over buffers of the epilogues live in the drained rings
         if p["NT"] == 16 and p["G"] <= 2:
@@ -127,6 +134,27 @@ def test_pair_plans(plans):
         assert (2 * p["stages"] + 5) * 8 + 8 <= 1024, p                         # barrier region
         # the even CTA arms each stage with both CTAs' bytes: within the tx-count range
         assert 2 * p["stage_bytes"] < 2 ** 20, p
+
+
+def test_fp8_split_plans(plans):
+    rows = [p for p in plans if p["kind"] == "w8s"]
+    assert len(rows) > 50 and {p["issuers"] for p in rows} == {1, 2}
+    for p in rows:
+        assert p["smem"] <= SMEM_LIMIT, p
+        # alignment slack, barrier region, weight ring, operand span, warm-up scratch
+        assert p["smem"] == 2048 + p["ring"] + p["span"] + 256, p
+        assert p["span"] >= p["kbp"] * 2 * p["NT"] * 128 and p["span"] >= (128 - p["RB"]) * 128, p
+        assert p["G"] * p["RB"] <= 128 and p["G"] * 2 * p["NT"] <= 256 and p["kbps"] % p["G"] == 0, p
+        assert p["kbp"] % p["G"] == 0 and p["kb"] <= p["kbp"] < p["kb"] + p["G"], p
+        assert p["k_stages"] * p["kbps"] >= p["kb"] and p["kb"] * 128 >= p["K"], p
+        # a second MMA issuer needs two windows a stage and one in the first stage
+        assert p["issuers"] == (2 if p["kbps"] >= 2 * p["G"] and p["kb"] > p["G"] else 1), p
+        # one accumulator per issuer, as many columns again for the warm-up pass
+        acc = p["issuers"] * p["G"] * 2 * p["NT"]
+        assert 2 * acc <= p["tmem_cols"] <= 512 and p["tmem_cols"] & (p["tmem_cols"] - 1) == 0, p
+        assert (2 * p["stages"] + p["k_stages"] + 2) * 8 + 8 <= 896, p       # barriers below the token words
+        assert (p["G"] - 1) * p["RB"] * 80 <= p["ring"], p                   # epilogue hand-over in the drained ring
+        assert p["grid"] * p["RB"] >= p["N"] > (p["grid"] - 1) * p["RB"], p
 
 
 def test_large_ends_are_planned_or_refused(plans):
