@@ -104,12 +104,12 @@ def load_peaks():
 # stays valid while these files are unchanged.
 KERNEL_SOURCES = {
     "simt_skinny_kernel": ("sgr_simt.cuh", "sgr_ptx.cuh"),
-    "rows_skinny_kernel": ("sgr_rows.cuh", "sgr_tc.cuh", "sgr_ptx.cuh"),
+    "rows_skinny_kernel": ("sgr_rows.cuh", "sgr_epi.cuh", "sgr_tc.cuh", "sgr_ptx.cuh"),
     "tc_skinny_kernel": ("sgr_tc.cuh", "sgr_ptx.cuh"),
     "tile_gemm_kernel": ("sgr_gemm.cuh", "sgr_tc.cuh", "sgr_ptx.cuh"),
     "pair_gemm_kernel": ("sgr_pair.cuh", "sgr_gemm.cuh", "sgr_tc.cuh", "sgr_ptx.cuh"),
     "w8_rows_kernel": ("sgr_w8.cuh", "sgr_tc.cuh", "sgr_ptx.cuh"),
-    "w8s_kernel": ("sgr_w8s.cuh", "sgr_w8.cuh", "sgr_tc.cuh", "sgr_ptx.cuh"),
+    "w8s_kernel": ("sgr_w8s.cuh", "sgr_epi.cuh", "sgr_w8.cuh", "sgr_tc.cuh", "sgr_ptx.cuh"),
 }
 
 

@@ -129,28 +129,6 @@ __device__ __forceinline__ bool mbar_wait_sleepy_or_abort(uint32_t bar, uint32_t
   }
 }
 
-// 16 accumulator columns at taddr, plus the same columns of the second
-// accumulator (C columns further) when there are two issuers, added in that
-// order.  Warp-collective.
-__device__ __forceinline__ void tmem_ld16_sum(uint32_t taddr, uint32_t C, bool two, float (&v)[16]) {
-  tmem_ld16(taddr, v);
-  if (two) {
-    float w[16];
-    tmem_ld16(taddr + C, w);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] += w[i];
-  }
-}
-
-// Store one BF16 value if `pred`; the store instruction is executed either
-// way (predicated off, it touches no memory), so a warm-up pass fetches it.
-__device__ __forceinline__ void st_global_bf16_if(__nv_bfloat16* ptr, __nv_bfloat16 x, bool pred) {
-  asm volatile(
-      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t@q st.global.b16 [%0], %1;\n\t}" ::"l"(ptr),
-      "h"(__bfloat16_as_ushort(x)), "r"((int)pred)
-      : "memory");
-}
-
 // 16 accumulator columns summed over the chains, chain 0 first (fixed order).
 __device__ __forceinline__ void tc_ld_chains(uint32_t taddr, int nt, int chains, float (&v)[16]) {
   tmem_ld16(taddr, v);

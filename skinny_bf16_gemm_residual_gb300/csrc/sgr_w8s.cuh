@@ -55,6 +55,7 @@
 #include <cuda_runtime.h>
 
 #include "sgr_ptx.cuh"
+#include "sgr_epi.cuh"
 #include "sgr_tc.cuh"
 #include "sgr_w8.cuh"
 #include "skinny_gemm_residual.h"
