@@ -1249,14 +1249,16 @@ int sgr_kernel_resources(int device, int path, int M, int N, int K, int* regs, i
     int sms = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
     if (sgr::rows_plan(c, sms, M, N, K, &rp, &grid, &smem) != SGR_OK) return SGR_ERR_UNSUPPORTED;
-    const void* fn = (rp.NT == 64 && rp.groups <= 2) ? reinterpret_cast<const void*>(sgr::rows_skinny64_kernel)
-                                                     : reinterpret_cast<const void*>(sgr::rows_skinny_kernel);
+    const int mode = sgr::rows_epi_mode(rp.NT, rp.groups);
+    const void* fn = mode == sgr::kRowsEpi16   ? reinterpret_cast<const void*>(sgr::rows_skinny_kernel<sgr::kRowsEpi16>)
+                     : mode == sgr::kRowsEpi64 ? reinterpret_cast<const void*>(sgr::rows_skinny_kernel<sgr::kRowsEpi64>)
+                                               : reinterpret_cast<const void*>(sgr::rows_skinny_kernel<sgr::kRowsEpiWide>);
     if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) {
       cudaGetLastError();
       return SGR_ERR_DEVICE;
     }
     *smem_bytes = (int)smem;
-    *threads = sgr::kRowsThreads;
+    *threads = sgr::rows_threads(mode);
   } else if (c.path == SGR_PATH_W8) {
     if (cudaFuncGetAttributes(&fa, sgr::w8_rows_kernel<false>) != cudaSuccess) {
       cudaGetLastError();

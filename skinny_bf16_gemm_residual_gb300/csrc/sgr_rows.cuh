@@ -29,15 +29,19 @@
 // CTA the next call's CTA fits on the same SM, so with programmatic dependent
 // launch it streams its weights while this one finishes.
 //
-// Warp roles (224 threads): warp 0 lane 0 issues TMA (W for the first stages
-// before griddepcontrol.wait, A after it); warp 1 owns TMEM and its lane 0
-// issues the MMAs, or, with two issuers, the even MMA windows of every stage
-// while lane 0 of warp 6 issues the odd ones into a second accumulator (one
-// thread issues a small-N MMA only every ~75 cycles, which left the last
-// stage's MMAs exposed after its weights landed; the epilogue adds the two
-// accumulators in a fixed order); warps 2-5 are the epilogue: they load their
-// residual values while the MMAs run, then tcgen05.ld the accumulator, add,
-// round once and store.
+// Warp roles: warp 0 lane 0 issues TMA (W for the first stages before
+// griddepcontrol.wait, A after it); warp 1 owns TMEM and its lane 0 issues
+// the MMAs, or, with two issuers (16-token tiles, 224 threads), the even MMA
+// windows of every stage while lane 0 of warp 6 issues the odd ones into a
+// second accumulator (one thread issues a small-N MMA only every ~75 cycles,
+// which left the last stage's MMAs exposed after its weights landed; the
+// epilogue adds the two accumulators in a fixed order); warps 2-5 are the
+// epilogue: they load their residual values while the MMAs run, then
+// tcgen05.ld the accumulator, add, round once and store.
+//
+// One kernel instance per epilogue family (16-token tiles with 224 threads;
+// 32- and 48-token tiles and the general form; 64-token tiles), each
+// compiled with only its own epilogue code and issuer count.
 //
 // Warm-up pass: the first run of a code path in a CTA costs ~0.7 us more
 // than the next (measured with the weight stream saturating L2: instruction
@@ -54,9 +58,8 @@
 // packed groups on separate barriers, to start the last stage's MMAs early,
 // measured slower).  Token tiles of 32, 48 and 64 use the same register form
 // with the accumulator loaded in 16-column pieces (rows_epilogue_wide; the
-// 64-token form in its own kernel instance, rows_skinny64_kernel, because of
-// its register count); only larger tiles stage partial sums through shared
-// memory.
+// 64-token form in its own kernel instance because of its register count);
+// only larger tiles stage partial sums through shared memory.
 #pragma once
 
 #include <cstring>
@@ -72,7 +75,12 @@
 
 namespace sgr {
 
-constexpr int kRowsThreads = 224;
+// Epilogue families (kernel instances) and their block sizes.
+enum RowsEpi : int { kRowsEpi16 = 0, kRowsEpiWide = 1, kRowsEpi64 = 2 };
+__host__ __device__ constexpr int rows_threads(int mode) { return mode == kRowsEpi16 ? 224 : 192; }
+__host__ __device__ inline int rows_epi_mode(int nt, int groups) {
+  return nt == 16 ? kRowsEpi16 : (nt == 64 && groups <= 2 ? kRowsEpi64 : kRowsEpiWide);
+}
 constexpr int kRowsMaxTokens = 256;
 constexpr int kRowsPrefetchTokens = 16;  // residual values held in registers before the MMAs end
 constexpr uint32_t kRowsSlack = kTcTileRows * 128u;  // MMA window over-read past the ring
@@ -224,12 +232,13 @@ __device__ __forceinline__ void rows_epilogue_wide(const RowsParams& p, const Ro
   }
 }
 
-// One CTA: the RB-row slab of W starting at row n0 of the problem `io`.
-// kWide64: include the 64-token register epilogue (more registers per
-// thread: only the kernel instance launched for 64-token tiles has it, so
-// that the others keep two CTAs per SM where their shared memory allows).
-template <bool kWide64>
+// One CTA: the RB-row slab of W starting at row n0 of the problem `io`, with
+// the epilogue family kMode (the 64-token register epilogue needs more
+// registers per thread: only its own instance has it, so that the others
+// keep two CTAs per SM where their shared memory allows).
+template <int kMode>
 __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, int n0) {
+  const int issuers = kMode == kRowsEpi16 ? p.issuers : 1;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -257,10 +266,10 @@ __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
-      mbar_init(smem_u32(&empty[s]), (uint32_t)p.issuers);  // one commit per issuer and stage
+      mbar_init(smem_u32(&empty[s]), (uint32_t)issuers);  // one commit per issuer and stage
     }
-    mbar_init(smem_u32(acc_full), (uint32_t)p.issuers);
-    mbar_init(smem_u32(drain), (uint32_t)p.issuers);
+    mbar_init(smem_u32(acc_full), (uint32_t)issuers);
+    mbar_init(smem_u32(drain), (uint32_t)issuers);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -341,19 +350,28 @@ __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, 
     }
   } else if (warp == 1 || warp == 6) {
     // ----------------------------------------------------------- MMA issuers
-    const int iss = warp == 6 ? 1 : 0;
-    if (lane == 0 && iss < p.issuers) {
+    const int iss = kMode == kRowsEpi16 && warp == 6 ? 1 : 0;
+    if (lane == 0 && iss < issuers) {
       // Issuer i takes MMA windows i, i + issuers, ... of every stage into
-      // accumulator i (G * NT columns each).
+      // accumulator i (G * NT columns each).  This thread's issue rate bounds
+      // the kernel at 32-64 tokens, so its loop carries no index arithmetic
+      // per MMA: window descriptors advance by a fixed step, and the
+      // accumulate flag is a register the first MMA clears (recomputing the
+      // first-window test and the offsets per MMA measured ~1.5 us slower
+      // per call there).
       const uint32_t dacc = tmem + (uint32_t)(iss * p.groups * p.NT);
       const uint32_t idesc = idesc_bf16_f32(kTcTileRows, p.groups * p.NT);
       // Descriptors differ only in their start-address field (address >> 4):
       // build the ring bases once and add offsets.
       const uint64_t wdesc0 = smem_desc_sw128(w_ring);
       const uint64_t adesc0 = smem_desc_sw128(a_ring);
+      const int j0 = iss * p.groups, jstep = issuers * p.groups;
+      const uint64_t wfirst = (uint64_t)((uint32_t)j0 * wblk >> 4), afirst = (uint64_t)((uint32_t)j0 * ablk >> 4);
+      const uint64_t wwin = (uint64_t)((uint32_t)jstep * wblk >> 4), awin = (uint64_t)((uint32_t)jstep * ablk >> 4);
       bool ok = true;
       int slot = 0;
       uint32_t par = 0;  // ring round parity of `slot`
+      uint32_t accum = 0;
       uint64_t wd = wdesc0, ad = adesc0;
       for (int s = 0; s < KS; ++s) {
         if (!mbar_wait_or_abort(smem_u32(&full[slot]), par, abort_flag)) {
@@ -361,13 +379,15 @@ __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, 
           break;
         }
         tc_fence_after();
-        for (int j = iss * p.groups; j < p.kbps; j += p.issuers * p.groups) {
+        uint64_t wj = wd + wfirst, aj = ad + afirst;
+        for (int j = j0; j < p.kbps; j += jstep) {
 #pragma unroll
           for (int kk = 0; kk < kTcKBlock / 16; ++kk) {
-            const bool first = (s == 0) && (j == iss * p.groups) && (kk == 0);
-            mma_bf16(dacc, wd + ((j * wblk + kk * 32u) >> 4), ad + ((j * ablk + kk * 32u) >> 4), idesc,
-                     first ? 0u : 1u);
+            mma_bf16(dacc, wj + (uint64_t)(kk * 2), aj + (uint64_t)(kk * 2), idesc, accum);  // K step: 32 bytes
+            accum = 1u;
           }
+          wj += wwin;
+          aj += awin;
         }
         mma_commit(smem_u32(&empty[slot]));
         wd += w_stage >> 4;
@@ -392,7 +412,7 @@ __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, 
     // ------------------------------------------------------------ epilogue
     pdl_wait();  // R may come from the preceding kernel; Y may be read by it
     const int q = warp & 3;       // TMEM lane quarter this warp may access
-    if (p.NT == kRowsPrefetchTokens && p.groups <= 2 && p.groups * p.RB <= kTcTileRows) {
+    if (kMode == kRowsEpi16 && p.NT == kRowsPrefetchTokens && p.groups <= 2 && p.groups * p.RB <= kTcTileRows) {
       // Decode epilogue (at most 16 tokens, at most two packed groups): the
       // thread on TMEM lane r < RB owns output column n0 + r and holds group
       // 0's partial sums; the thread on lane RB + r holds group 1's and hands
@@ -434,8 +454,8 @@ __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, 
           // reads the columns after them, which no MMA writes.
           const uint32_t C = (uint32_t)(G * kRowsPrefetchTokens);
           const uint32_t taddr =
-              tmem + ((uint32_t)(q * 32) << 16) + (real ? 0u : (uint32_t)p.issuers * C);
-          const bool two = p.issuers == 2;
+              tmem + ((uint32_t)(q * 32) << 16) + (real ? 0u : (uint32_t)issuers * C);
+          const bool two = issuers == 2;
           if (G == 1 || (q + 1) * 32 <= p.RB) {
             tmem_ld16_sum(taddr, C, two, v);  // group-0 columns only
           } else if (q * 32 >= p.RB) {
@@ -480,13 +500,13 @@ __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, 
             st_global_bf16_if(yp + (size_t)m * io.ldy, __float2bfloat16_rn(v[m] + res[m]), real && m < io.M);
         }
       }
-    } else if (p.NT == 32 && p.groups <= 2 && p.groups * p.RB <= kTcTileRows) {
+    } else if (kMode == kRowsEpiWide && p.NT == 32 && p.groups <= 2 && p.groups * p.RB <= kTcTileRows) {
       rows_epilogue_wide<32>(p, io, n0, tmem, w_ring, acc_full, abort_flag, q, lane);
-    } else if (p.NT == 48 && p.groups <= 2 && p.groups * p.RB <= kTcTileRows) {
+    } else if (kMode == kRowsEpiWide && p.NT == 48 && p.groups <= 2 && p.groups * p.RB <= kTcTileRows) {
       rows_epilogue_wide<48>(p, io, n0, tmem, w_ring, acc_full, abort_flag, q, lane);
-    } else if (kWide64 && p.NT == 64 && p.groups <= 2 && p.groups * p.RB <= kTcTileRows) {
+    } else if (kMode == kRowsEpi64 && p.NT == 64 && p.groups <= 2 && p.groups * p.RB <= kTcTileRows) {
       rows_epilogue_wide<64>(p, io, n0, tmem, w_ring, acc_full, abort_flag, q, lane);
-    } else if (p.NT == kRowsPrefetchTokens && p.groups == 4 && p.RB == 32) {
+    } else if (kMode == kRowsEpi16 && p.NT == kRowsPrefetchTokens && p.groups == 4 && p.RB == 32) {
       // 32-row slabs, four packed groups: warp quarter q holds group q whole.
       // Warps 1-3 hand their partial sums to warp 0's lanes (one output
       // column each) through shared memory; warp 0 adds them in group order.
@@ -537,7 +557,7 @@ __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, 
         for (int m = 0; m < kRowsPrefetchTokens; ++m)
           if (m < io.M) yp[(size_t)m * io.ldy] = __float2bfloat16_rn(v[m] + res[m]);
       }
-    } else if (p.NT == kRowsPrefetchTokens && p.groups * p.RB <= kTcTileRows) {
+    } else if (kMode == kRowsEpi16 && p.NT == kRowsPrefetchTokens && p.groups * p.RB <= kTcTileRows) {
       // The same for three or four packed groups (short slabs, e.g. 24 rows
       // when N = 3584): lane g*RB + r (g = 1 .. G-1) hands group g's partial
       // sums to the owner of row r, who adds them in g order.  Kept apart
@@ -696,20 +716,14 @@ __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, 
 }
 
 // Two CTAs per SM where their shared memory allows (the register budget is
-// sized for it; the default configuration of untabulated shapes relies on it).
-__global__ void __launch_bounds__(kRowsThreads, 2)
+// sized for it; the default configuration of untabulated shapes relies on
+// it), except for the 64-token instance.
+template <int kMode>
+__global__ void __launch_bounds__(rows_threads(kMode), kMode == kRowsEpi64 ? 1 : 2)
     rows_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA,
                        const RowsParams p) {
   const RowsIO io{&tmW, &tmA, p.R, p.Y, p.ldr, p.ldy, p.M};
-  rows_run<false>(p, io, (int)blockIdx.x * p.RB);
-}
-
-// The same for 64-token tiles (33 <= M <= 64), with the 64-token epilogue.
-__global__ void __launch_bounds__(kRowsThreads, 1)
-    rows_skinny64_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA,
-                         const RowsParams p) {
-  const RowsIO io{&tmW, &tmA, p.R, p.Y, p.ldr, p.ldy, p.M};
-  rows_run<true>(p, io, (int)blockIdx.x * p.RB);
+  rows_run<kMode>(p, io, (int)blockIdx.x * p.RB);
 }
 
 // Grouped launch: several independent problems with the same N and K and
@@ -732,13 +746,15 @@ struct RowsGroupList {
   int count;
 };
 
-__global__ void __launch_bounds__(kRowsThreads, 2)
+// kMode: kRowsEpi16 for 16-token tiles, else kRowsEpiWide.
+template <int kMode>
+__global__ void __launch_bounds__(rows_threads(kMode), 2)
     rows_grouped_kernel(const __grid_constant__ RowsGroupList list, const RowsParams p) {
   const int e = (int)blockIdx.x % list.count;
   const int slab = (int)blockIdx.x / list.count;
   const RowsGroup& g = list.g[e];
   const RowsIO io{&g.tmW, &g.tmA, g.R, g.Y, g.ldr, g.ldy, g.M};
-  rows_run<false>(p, io, slab * p.RB);
+  rows_run<kMode>(p, io, slab * p.RB);
 }
 
 // ------------------------------------------------------------------ host side
@@ -827,9 +843,11 @@ inline int rows_plan(const sgr_config& c, int sms, int M, int N, int K, RowsPara
 }
 
 inline cudaError_t rows_init_device() {
-  cudaError_t e = set_kernel_smem_attrs(reinterpret_cast<const void*>(rows_skinny_kernel));
-  if (e == cudaSuccess) e = set_kernel_smem_attrs(reinterpret_cast<const void*>(rows_skinny64_kernel));
-  if (e == cudaSuccess) e = set_kernel_smem_attrs(reinterpret_cast<const void*>(rows_grouped_kernel));
+  cudaError_t e = set_kernel_smem_attrs(reinterpret_cast<const void*>(rows_skinny_kernel<kRowsEpi16>));
+  if (e == cudaSuccess) e = set_kernel_smem_attrs(reinterpret_cast<const void*>(rows_skinny_kernel<kRowsEpiWide>));
+  if (e == cudaSuccess) e = set_kernel_smem_attrs(reinterpret_cast<const void*>(rows_skinny_kernel<kRowsEpi64>));
+  if (e == cudaSuccess) e = set_kernel_smem_attrs(reinterpret_cast<const void*>(rows_grouped_kernel<kRowsEpi16>));
+  if (e == cudaSuccess) e = set_kernel_smem_attrs(reinterpret_cast<const void*>(rows_grouped_kernel<kRowsEpiWide>));
   return e;
 }
 
@@ -851,7 +869,8 @@ inline int rows_launch(const sgr_config& c, int sms, unsigned* err, const void* 
   p.err = err;
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3((unsigned)grid, 1, 1);
-  lc.blockDim = dim3(kRowsThreads, 1, 1);
+  const int mode = rows_epi_mode(p.NT, p.groups);
+  lc.blockDim = dim3(rows_threads(mode), 1, 1);
   lc.dynamicSmemBytes = smem;
   lc.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -859,8 +878,9 @@ inline int rows_launch(const sgr_config& c, int sms, unsigned* err, const void* 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
   lc.numAttrs = pdl ? 1 : 0;
-  const bool wide64 = p.NT == 64 && p.groups <= 2;
-  if (cudaLaunchKernelEx(&lc, wide64 ? rows_skinny64_kernel : rows_skinny_kernel, tmW, tmA, p) != cudaSuccess) {
+  auto fn = mode == kRowsEpi16 ? rows_skinny_kernel<kRowsEpi16>
+                               : (mode == kRowsEpi64 ? rows_skinny_kernel<kRowsEpi64> : rows_skinny_kernel<kRowsEpiWide>);
+  if (cudaLaunchKernelEx(&lc, fn, tmW, tmA, p) != cudaSuccess) {
     cudaGetLastError();
     return SGR_ERR_LAUNCH;
   }
@@ -907,7 +927,8 @@ inline int rows_grouped_launch(const sgr_config& c, int sms, unsigned* err, cons
   }
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3((unsigned)(grid * count), 1, 1);
-  lc.blockDim = dim3(kRowsThreads, 1, 1);
+  const int mode = p.NT == 16 ? kRowsEpi16 : kRowsEpiWide;  // 64-token tiles take the general epilogue here
+  lc.blockDim = dim3(rows_threads(mode), 1, 1);
   lc.dynamicSmemBytes = smem;
   lc.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -915,7 +936,8 @@ inline int rows_grouped_launch(const sgr_config& c, int sms, unsigned* err, cons
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
   lc.numAttrs = pdl ? 1 : 0;
-  if (cudaLaunchKernelEx(&lc, rows_grouped_kernel, list, p) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&lc, mode == kRowsEpi16 ? rows_grouped_kernel<kRowsEpi16> : rows_grouped_kernel<kRowsEpiWide>,
+                         list, p) != cudaSuccess) {
     cudaGetLastError();
     return SGR_ERR_LAUNCH;
   }

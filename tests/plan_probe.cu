@@ -40,9 +40,11 @@ int main() {
             const size_t w_ring = (size_t)st * kb * p.RB * 128, a_ring = (size_t)st * kb * p.NT * 128;
             std::printf("{\"kind\": \"rows\", \"M\": %d, \"N\": %d, \"K\": %d, \"RB\": %d, \"NT\": %d, \"G\": %d, "
                         "\"kbps\": %d, \"stages\": %d, \"prefetch\": %d, \"k_stages\": %d, \"tmem_cols\": %d, "
-                        "\"issuers\": %d, \"grid\": %d, \"smem\": %zu, \"w_ring\": %zu, \"a_ring\": %zu}\n",
+                        "\"issuers\": %d, \"mode\": %d, \"threads\": %d, \"grid\": %d, \"smem\": %zu, \"w_ring\": %zu, "
+                        "\"a_ring\": %zu}\n",
                         M, N, K, p.RB, p.NT, p.groups, p.kbps, p.stages, p.prefetch, p.k_stages, p.tmem_cols,
-                        p.issuers, grid, smem, w_ring, a_ring);
+                        p.issuers, sgr::rows_epi_mode(p.NT, p.groups), sgr::rows_threads(sgr::rows_epi_mode(p.NT, p.groups)),
+                        grid, smem, w_ring, a_ring);
           }
       // FP8 row-slab kernel
       for (int rb : {0, 8, 24, 32, 64, 128})

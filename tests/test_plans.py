@@ -45,6 +45,10 @@ def test_row_slab_plans(plans):
         # two MMA issuers (alternate windows, own accumulators) only under the
         # 16-token epilogue that adds them, with two or more windows a stage
         assert p["issuers"] == (2 if decode_epi and p["kbps"] >= 2 * p["G"] else 1), p
+        # kernel instance by epilogue family: 16-token tiles (224 threads, the
+        # only one with a second issuer), 64-token register form, the rest
+        assert p["mode"] == (0 if p["NT"] == 16 else (2 if p["NT"] == 64 and p["G"] <= 2 else 1)), p
+        assert p["threads"] == (224 if p["mode"] == 0 else 192), p
         acc_cols = p["issuers"] * p["G"] * p["NT"]
         # that epilogue's warm-up pass reads as many columns again, unwritten
         assert p["tmem_cols"] >= (2 if decode_epi else 1) * acc_cols and p["tmem_cols"] <= 512, p
