@@ -302,6 +302,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       uint32_t par = 0;
       uint64_t doff = 0;  // slot * stage_bytes >> 4 (descriptor start-address units)
       const uint64_t dstep = stage_bytes >> 4;
+      const uint64_t a_win = (uint64_t)(a_box >> 4), w_win = (uint64_t)(w_box >> 4);  // one K block
       for (int i = 0; i < my_tiles && ok; ++i) {
         const int buf = i & 1;
         if (i >= 2 && !mbar_wait_cluster(smem_u32(&acc_empty[buf]), ((i >> 1) - 1) & 1, abort_flag)) {
@@ -310,18 +311,24 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         }
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(buf * NT);
+        uint32_t accum = 0;
         for (int ks = 0; ks < KS; ++ks) {
           if (!mbar_wait_or_abort(smem_u32(&full[slot]), par, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
+          // No index arithmetic per MMA: descriptors advance by fixed steps
+          // and the accumulate flag is a register the tile's first MMA clears.
+          uint64_t aj = adesc0 + doff, wj = wdesc0 + doff;
           for (int j = 0; j < KP; ++j) {
-            const uint64_t ao = doff + (uint64_t)((j * a_box) >> 4), wo = doff + (uint64_t)((j * w_box) >> 4);
 #pragma unroll
-            for (int kk = 0; kk < kTcKBlock / 16; ++kk)
-              mma_bf16_pair(d, adesc0 + ao + (uint64_t)(kk * 2), wdesc0 + wo + (uint64_t)(kk * 2), idesc,
-                            (ks | j | kk) != 0 ? 1u : 0u);
+            for (int kk = 0; kk < kTcKBlock / 16; ++kk) {
+              mma_bf16_pair(d, aj + (uint64_t)(kk * 2), wj + (uint64_t)(kk * 2), idesc, accum);  // K step: 32 bytes
+              accum = 1u;
+            }
+            aj += a_win;
+            wj += w_win;
           }
           mma_commit_pair(smem_u32(&empty[slot]));
           mma_commit_pair(map_to_rank(smem_u32(&empty[slot]), peer));

@@ -280,6 +280,8 @@ __global__ void __launch_bounds__(kW8Threads, 2)
       int slot = 0, ts = 0;
       uint32_t par = 0, tpar = 0;
       uint64_t ad = adesc0;
+      uint32_t accum = 0;
+      const uint64_t a_win = (uint64_t)((uint32_t)G * ablk >> 4);  // activations of one MMA window
       const uint32_t tstage = (uint32_t)wins * kW8SlotCols;  // TMEM columns of one widened stage
       for (int s = 0; s < KS; ++s) {
         if (!mbar_wait_or_abort(smem_u32(&afull[slot]), par, abort_flag) ||
@@ -288,14 +290,19 @@ __global__ void __launch_bounds__(kW8Threads, 2)
           break;
         }
         tc_fence_after();
-        const uint32_t wa = wslot0 + (uint32_t)ts * tstage;
+        // No index arithmetic per MMA: operand addresses advance by fixed
+        // steps and the accumulate flag is a register the first MMA clears.
+        uint32_t wa = wslot0 + (uint32_t)ts * tstage;
+        uint64_t aw = ad;
         for (int w = 0; w < wins; ++w) {
 #pragma unroll
           for (int kk = 0; kk < kTcKBlock / 16; ++kk) {
-            const bool first = (s == 0) && (w == 0) && (kk == 0);
-            mma_bf16_tmem_a(tmem, wa + (uint32_t)(w * kW8SlotCols + kk * 8),
-                            ad + (((uint32_t)(w * G) * ablk + kk * 32u) >> 4), idesc, first ? 0u : 1u);
+            // K step: 8 TMEM columns of widened codes, 32 bytes of activations
+            mma_bf16_tmem_a(tmem, wa + (uint32_t)(kk * 8), aw + (uint64_t)(kk * 2), idesc, accum);
+            accum = 1u;
           }
+          wa += (uint32_t)kW8SlotCols;
+          aw += a_win;
         }
         mma_commit(smem_u32(&tfree[ts]));
         mma_commit(smem_u32(&aempty[slot]));

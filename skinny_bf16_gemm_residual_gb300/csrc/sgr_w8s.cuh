@@ -291,10 +291,18 @@ __global__ void __launch_bounds__(kW8sThreads, 1)
       const uint32_t idesc = idesc_e4m3_f32(kTcTileRows, G * 2 * p.NT);
       const uint64_t wdesc0 = smem_desc_sw128(w_ring);
       const uint64_t bdesc0 = smem_desc_sw128(b_buf);
+      // No index arithmetic per MMA: descriptors advance by fixed steps and
+      // the accumulate flag is a register the first MMA clears.
+      const int w0 = iss * G, wstep = p.issuers * G;
+      const uint64_t w_win = (uint64_t)((uint32_t)wstep * wbox >> 4), b_win = (uint64_t)((uint32_t)wstep * bblk >> 4);
+      const uint64_t w_first = (uint64_t)((uint32_t)w0 * wbox >> 4);
       bool ok = true;
       int slot = 0;
       uint32_t par = 0;
-      bool first = true;
+      uint32_t accum = 0;
+      uint64_t wstage = wdesc0;                                        // this slot's first code box
+      uint64_t bstage = bdesc0 + (uint64_t)((uint32_t)w0 * bblk >> 4);  // this issuer's first window in stage s
+      const uint64_t b_stage = (uint64_t)((uint32_t)p.kbps * bblk >> 4);
       for (int s = 0; s < KS && ok; ++s) {
         if (!mbar_wait_or_abort(smem_u32(&wfull[slot]), par, abort_flag) ||
             !mbar_wait_or_abort(smem_u32(&bready[s]), 0, abort_flag)) {
@@ -302,20 +310,24 @@ __global__ void __launch_bounds__(kW8sThreads, 1)
           break;
         }
         tc_fence_after();
-        const int j0 = s * p.kbps;
-        for (int w = iss * G; w < p.kbps && j0 + w < p.kb; w += p.issuers * G) {  // windows starting inside K
-          const uint64_t wd = wdesc0 + (((uint32_t)slot * w_stage + (uint32_t)w * wbox) >> 4);
-          const uint64_t bd = bdesc0 + (((uint32_t)(j0 + w) * bblk) >> 4);
+        const int wend = p.kb - s * p.kbps < p.kbps ? p.kb - s * p.kbps : p.kbps;  // windows starting inside K
+        uint64_t wd = wstage + w_first, bd = bstage;
+        for (int w = w0; w < wend; w += wstep) {
 #pragma unroll
           for (int kk = 0; kk < kW8sKBlock / 32; ++kk) {
-            mma_e4m3(dacc, wd + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, first ? 0u : 1u);
-            first = false;
+            mma_e4m3(dacc, wd + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, accum);  // K step: 32 bytes
+            accum = 1u;
           }
+          wd += w_win;
+          bd += b_win;
         }
         mma_commit(smem_u32(&wempty[slot]));
+        bstage += b_stage;
+        wstage += w_stage >> 4;
         if (++slot == S) {
           slot = 0;
           par ^= 1u;
+          wstage = wdesc0;
         }
       }
       if (ok) {
