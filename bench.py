@@ -792,13 +792,13 @@ def run_w8(sgr, device, stream, peaks: dict, m_list=(1, 2, 4, 16), copies: int =
         del g
         nbytes = N_DIM * K_DIM + 4 * N_DIM + 2 * M * K_DIM + 4 * M * N_DIM
         gbs = nbytes / (us * 1e-6) / 1e9
-        rows.append({"m": M, "kernel": "w8s_kernel" if M <= 4 else "w8_rows_kernel",
+        rows.append({"m": M, "kernel": "w8s_kernel" if M <= 8 else "w8_rows_kernel",
                      "us": us, "bytes": nbytes, "gbs": gbs,
                      "frac_of_hbm_peak": gbs / peaks["hbm_gbs"] if peaks.get("hbm_gbs") else None})
     return {"per_m": rows,
             "note": "FP8 E4M3 weights + FP32 per-column scale, BF16 A/R/Y; graph of 8 calls over distinct weight "
                     "copies; the library's own kernel choice (FP8 tensor-core kernel with split activations for "
-                    "M <= 4, the widening row-slab kernel above)"}
+                    "M <= 8, the widening row-slab kernel above)"}
 
 
 def run_w4(sgr, device, stream, peaks: dict, m_list=(1, 2, 4, 16), copies: int = 8, replays: int = 50,
