@@ -39,9 +39,10 @@
 // epilogue: they load their residual values while the MMAs run, then
 // tcgen05.ld the accumulator, add, round once and store.
 //
-// One kernel instance per epilogue family (16-token tiles with 224 threads;
-// 32- and 48-token tiles and the general form; 64-token tiles), each
-// compiled with only its own epilogue code and issuer count.
+// One kernel instance per epilogue family (16-token tiles with one or two
+// packed groups, and with three or four, both with 224 threads; 32- and
+// 48-token tiles and the general form; 64-token tiles), each compiled with
+// only its own epilogue code and issuer count.
 //
 // Warm-up pass: the first run of a code path in a CTA costs ~0.7 us more
 // than the next (measured with the weight stream saturating L2: instruction
@@ -76,10 +77,16 @@
 namespace sgr {
 
 // Epilogue families (kernel instances) and their block sizes.
-enum RowsEpi : int { kRowsEpi16 = 0, kRowsEpiWide = 1, kRowsEpi64 = 2 };
-__host__ __device__ constexpr int rows_threads(int mode) { return mode == kRowsEpi16 ? 224 : 192; }
+// kRowsEpi16: 16-token tiles with one or two packed groups; kRowsEpi16G4:
+// 16-token tiles with three or four (short slabs); both with a second MMA
+// issuer (224 threads).  The two are separate instances so that each keeps
+// its register budget for two CTAs per SM without spills.
+enum RowsEpi : int { kRowsEpi16 = 0, kRowsEpiWide = 1, kRowsEpi64 = 2, kRowsEpi16G4 = 3 };
+__host__ __device__ constexpr bool rows_two_issuer_mode(int mode) { return mode == 0 || mode == 3; }
+__host__ __device__ constexpr int rows_threads(int mode) { return rows_two_issuer_mode(mode) ? 224 : 192; }
 __host__ __device__ inline int rows_epi_mode(int nt, int groups) {
-  return nt == 16 ? kRowsEpi16 : (nt == 64 && groups <= 2 ? kRowsEpi64 : kRowsEpiWide);
+  return nt == 16 ? (groups <= 2 ? kRowsEpi16 : kRowsEpi16G4)
+                  : (nt == 64 && groups <= 2 ? kRowsEpi64 : kRowsEpiWide);
 }
 constexpr int kRowsMaxTokens = 256;
 constexpr int kRowsPrefetchTokens = 16;  // residual values held in registers before the MMAs end
@@ -238,7 +245,7 @@ __device__ __forceinline__ void rows_epilogue_wide(const RowsParams& p, const Ro
 // keep two CTAs per SM where their shared memory allows).
 template <int kMode>
 __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, int n0) {
-  const int issuers = kMode == kRowsEpi16 ? p.issuers : 1;
+  const int issuers = rows_two_issuer_mode(kMode) ? p.issuers : 1;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -350,7 +357,7 @@ __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, 
     }
   } else if (warp == 1 || warp == 6) {
     // ----------------------------------------------------------- MMA issuers
-    const int iss = kMode == kRowsEpi16 && warp == 6 ? 1 : 0;
+    const int iss = rows_two_issuer_mode(kMode) && warp == 6 ? 1 : 0;
     if (lane == 0 && iss < issuers) {
       // Issuer i takes MMA windows i, i + issuers, ... of every stage into
       // accumulator i (G * NT columns each).  This thread's issue rate bounds
@@ -424,10 +431,16 @@ __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, 
       const bool helper = G == 2 && L >= p.RB && L < 2 * p.RB;
       const int r = owner ? L : L - p.RB;
       const uint32_t xch = w_ring + (uint32_t)(helper || owner ? r : 0) * 80u;  // drained ring: 16 floats + pad per row
-      float res[kRowsPrefetchTokens];
+      uint32_t res2[kRowsPrefetchTokens / 2];  // residuals as BF16 pairs (half the registers)
+      {
+        const unsigned short* rp = reinterpret_cast<const unsigned short*>(io.R) + n0 + L;
 #pragma unroll
-      for (int m = 0; m < kRowsPrefetchTokens; ++m)
-        res[m] = (owner && m < io.M) ? __bfloat162float(io.R[(size_t)m * io.ldr + n0 + L]) : 0.f;
+        for (int m = 0; m < kRowsPrefetchTokens; m += 2) {
+          const uint32_t lo = (owner && m < io.M) ? rp[(size_t)m * io.ldr] : 0u;
+          const uint32_t hi = (owner && m + 1 < io.M) ? rp[(size_t)(m + 1) * io.ldr] : 0u;
+          res2[m / 2] = lo | (hi << 16);
+        }
+      }
       // Pass 0 warms the code below while the MMAs run; pass 1 is the real
       // one.  The pass number goes through an opaque move so that the
       // compiler keeps one copy of the loop body for both passes.
@@ -497,7 +510,9 @@ __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, 
           __nv_bfloat16* yp = io.Y + n0 + L;
 #pragma unroll
           for (int m = 0; m < kRowsPrefetchTokens; ++m)
-            st_global_bf16_if(yp + (size_t)m * io.ldy, __float2bfloat16_rn(v[m] + res[m]), real && m < io.M);
+            st_global_bf16_if(yp + (size_t)m * io.ldy,
+                              __float2bfloat16_rn(v[m] + ((m & 1) ? bf16hi(res2[m / 2]) : bf16lo(res2[m / 2]))),
+                              real && m < io.M);
         }
       }
     } else if (kMode == kRowsEpiWide && p.NT == 32 && p.groups <= 2 && p.groups * p.RB <= kTcTileRows) {
@@ -506,63 +521,85 @@ __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, 
       rows_epilogue_wide<48>(p, io, n0, tmem, w_ring, acc_full, abort_flag, q, lane);
     } else if (kMode == kRowsEpi64 && p.NT == 64 && p.groups <= 2 && p.groups * p.RB <= kTcTileRows) {
       rows_epilogue_wide<64>(p, io, n0, tmem, w_ring, acc_full, abort_flag, q, lane);
-    } else if (kMode == kRowsEpi16 && p.NT == kRowsPrefetchTokens && p.groups == 4 && p.RB == 32) {
+    } else if (kMode == kRowsEpi16G4 && p.NT == kRowsPrefetchTokens && p.groups == 4 && p.RB == 32) {
       // 32-row slabs, four packed groups: warp quarter q holds group q whole.
       // Warps 1-3 hand their partial sums to warp 0's lanes (one output
       // column each) through shared memory; warp 0 adds them in group order.
+      // A warm-up pass first, as in the two-group form above.
       const bool owner = q == 0 && n0 + lane < p.N;
       const uint32_t xch = w_ring + (uint32_t)lane * 80u;  // drained ring: [3][32] rows of 16 floats + pad
-      float res[kRowsPrefetchTokens];
+      uint32_t res2[kRowsPrefetchTokens / 2];  // residuals as BF16 pairs (half the registers)
+      {
+        const unsigned short* rp = reinterpret_cast<const unsigned short*>(io.R) + n0 + lane;
 #pragma unroll
-      for (int m = 0; m < kRowsPrefetchTokens; ++m)
-        res[m] = (owner && m < io.M) ? __bfloat162float(io.R[(size_t)m * io.ldr + n0 + lane]) : 0.f;
-      bool ok = mbar_wait_or_abort(smem_u32(acc_full), 0, abort_flag);
-      if (!ok) {
-        if (!*abort_flag) report_error(p.err, kErrWaitMma);
-        *abort_flag = 1;
-      }
-      ok = __all_sync(0xffffffffu, ok);
-      tc_fence_after();
-      float v[16];
-      if (ok) {
-        tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(q * 16), v);
-        if (q > 0) {
-          const uint32_t dst = xch + (uint32_t)(q - 1) * 32u * 80u;
-#pragma unroll
-          for (int i = 0; i < 16; i += 4)
-            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(dst + (uint32_t)i * 4u), "f"(v[i]),
-                         "f"(v[i + 1]), "f"(v[i + 2]), "f"(v[i + 3])
-                         : "memory");
+        for (int m = 0; m < kRowsPrefetchTokens; m += 2) {
+          const uint32_t lo = (owner && m < io.M) ? rp[(size_t)m * io.ldr] : 0u;
+          const uint32_t hi = (owner && m + 1 < io.M) ? rp[(size_t)(m + 1) * io.ldr] : 0u;
+          res2[m / 2] = lo | (hi << 16);
         }
       }
-      named_bar_sync(1, 128);
-      if (ok && owner) {
+      const uint32_t C = (uint32_t)(p.groups * kRowsPrefetchTokens);  // columns of one accumulator
+#pragma unroll 1
+      for (int pass = 0; pass < 2; ++pass) {
+        int passv;  // opaque to the compiler: one copy of the loop body serves both passes
+        asm volatile("mov.b32 %0, %1;" : "=r"(passv) : "r"(pass));
+        const bool real = passv != 0;
+        bool ok = true;
+        if (real) {
+          ok = mbar_wait_or_abort(smem_u32(acc_full), 0, abort_flag);
+          if (!ok) {
+            if (!*abort_flag) report_error(p.err, kErrWaitMma);
+            *abort_flag = 1;
+          }
+          ok = __all_sync(0xffffffffu, ok);
+        }
+        tc_fence_after();
+        const uint32_t x = real ? xch : base + kRowsWarmScratch;
+        const uint32_t xs = real ? 32u * 80u : 0u;
+        float v[16];
+        if (ok) {
+          tmem_ld16_sum(tmem + ((uint32_t)(q * 32) << 16) + (real ? 0u : (uint32_t)issuers * C) + (uint32_t)(q * 16),
+                        C, issuers == 2, v);
+          if (q > 0) {
+            const uint32_t dst = x + (uint32_t)(q - 1) * xs;
 #pragma unroll
-        for (int gg = 0; gg < 3; ++gg) {
-#pragma unroll
-          for (int i = 0; i < 16; i += 4) {
-            float a0, a1, a2, a3;
-            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                         : "=f"(a0), "=f"(a1), "=f"(a2), "=f"(a3)
-                         : "r"(xch + (uint32_t)gg * 32u * 80u + (uint32_t)i * 4u)
-                         : "memory");
-            v[i] += a0;
-            v[i + 1] += a1;
-            v[i + 2] += a2;
-            v[i + 3] += a3;
+            for (int i = 0; i < 16; i += 4)
+              asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(dst + (uint32_t)i * 4u), "f"(v[i]),
+                           "f"(v[i + 1]), "f"(v[i + 2]), "f"(v[i + 3])
+                           : "memory");
           }
         }
-        __nv_bfloat16* yp = io.Y + n0 + lane;
+        named_bar_sync(1, 128);
+        if (ok && owner) {
 #pragma unroll
-        for (int m = 0; m < kRowsPrefetchTokens; ++m)
-          if (m < io.M) yp[(size_t)m * io.ldy] = __float2bfloat16_rn(v[m] + res[m]);
+          for (int gg = 0; gg < 3; ++gg) {
+#pragma unroll
+            for (int i = 0; i < 16; i += 4) {
+              float a0, a1, a2, a3;
+              asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                           : "=f"(a0), "=f"(a1), "=f"(a2), "=f"(a3)
+                           : "r"(x + (uint32_t)gg * xs + (uint32_t)i * 4u)
+                           : "memory");
+              v[i] += a0;
+              v[i + 1] += a1;
+              v[i + 2] += a2;
+              v[i + 3] += a3;
+            }
+          }
+          __nv_bfloat16* yp = io.Y + n0 + lane;
+#pragma unroll
+          for (int m = 0; m < kRowsPrefetchTokens; ++m)
+            st_global_bf16_if(yp + (size_t)m * io.ldy,
+                              __float2bfloat16_rn(v[m] + ((m & 1) ? bf16hi(res2[m / 2]) : bf16lo(res2[m / 2]))),
+                              real && m < io.M);
+        }
       }
-    } else if (kMode == kRowsEpi16 && p.NT == kRowsPrefetchTokens && p.groups * p.RB <= kTcTileRows) {
+    } else if (kMode == kRowsEpi16G4 && p.NT == kRowsPrefetchTokens && p.groups * p.RB <= kTcTileRows) {
       // The same for three or four packed groups (short slabs, e.g. 24 rows
       // when N = 3584): lane g*RB + r (g = 1 .. G-1) hands group g's partial
       // sums to the owner of row r, who adds them in g order.  Kept apart
       // from the two-group version above, which measured ~0.3 us faster per
-      // call than this loop form with G = 2.
+      // call than this loop form with G = 2.  A warm-up pass first, as there.
       const int L = q * 32 + lane;
       const int G = p.groups;
       const int g = L / p.RB;  // packed group of this lane (>= G: unused lane)
@@ -572,64 +609,91 @@ __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, 
       // drained ring: [G-1][RB] rows of 16 floats + 4 pad
       const uint32_t xch0 = w_ring + (uint32_t)r * 80u;
       const uint32_t xstep = (uint32_t)p.RB * 80u;
-      float res[kRowsPrefetchTokens];
+      uint32_t res2[kRowsPrefetchTokens / 2];  // residuals as BF16 pairs (half the registers)
+      {
+        const unsigned short* rp = reinterpret_cast<const unsigned short*>(io.R) + n0 + r;
 #pragma unroll
-      for (int m = 0; m < kRowsPrefetchTokens; ++m)
-        res[m] = (owner && m < io.M) ? __bfloat162float(io.R[(size_t)m * io.ldr + n0 + r]) : 0.f;
-      bool ok = mbar_wait_or_abort(smem_u32(acc_full), 0, abort_flag);
-      if (!ok) {
-        if (!*abort_flag) report_error(p.err, kErrWaitMma);
-        *abort_flag = 1;
-      }
-      ok = __all_sync(0xffffffffu, ok);
-      tc_fence_after();
-      float v[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) v[i] = 0.f;
-      if (ok && q * 32 < G * p.RB) {  // warp-uniform: this warp holds rows of the MMA window in use
-        // The warp's lanes hold groups glo .. ghi: load their columns
-        // (16 per group) and keep this lane's.
-        const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16);
-        const int glo = (q * 32) / p.RB;
-        const int ghi = min(G - 1, (q * 32 + 31) / p.RB);
-        for (int gg = glo; gg <= ghi; ++gg) {
-          float w[16];
-          tmem_ld16(taddr + (uint32_t)(gg * 16), w);  // warp-collective
-          if (gg == g) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = w[i];
-          }
+        for (int m = 0; m < kRowsPrefetchTokens; m += 2) {
+          const uint32_t lo = (owner && m < io.M) ? rp[(size_t)m * io.ldr] : 0u;
+          const uint32_t hi = (owner && m + 1 < io.M) ? rp[(size_t)(m + 1) * io.ldr] : 0u;
+          res2[m / 2] = lo | (hi << 16);
         }
       }
-      if (ok && helper) {
-        const uint32_t dst = xch0 + (uint32_t)(g - 1) * xstep;
+      const uint32_t C = (uint32_t)(G * kRowsPrefetchTokens);  // columns of one accumulator
+#pragma unroll 1
+      for (int pass = 0; pass < 2; ++pass) {
+        int passv;  // opaque to the compiler: one copy of the loop body serves both passes
+        asm volatile("mov.b32 %0, %1;" : "=r"(passv) : "r"(pass));
+        const bool real = passv != 0;
+        bool ok = true;
+        if (real) {
+          ok = mbar_wait_or_abort(smem_u32(acc_full), 0, abort_flag);
+          if (!ok) {
+            if (!*abort_flag) report_error(p.err, kErrWaitMma);
+            *abort_flag = 1;
+          }
+          ok = __all_sync(0xffffffffu, ok);
+        }
+        tc_fence_after();
+        float v[16];
 #pragma unroll
-        for (int i = 0; i < 16; i += 4)
-          asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(dst + (uint32_t)i * 4u), "f"(v[i]),
-                       "f"(v[i + 1]), "f"(v[i + 2]), "f"(v[i + 3])
-                       : "memory");
-      }
-      named_bar_sync(1, 128);
-      if (ok && owner) {
-        for (int gg = 1; gg < G; ++gg) {
-          const uint32_t src = xch0 + (uint32_t)(gg - 1) * xstep;
+        for (int i = 0; i < 16; ++i) v[i] = 0.f;
+        if (ok && q * 32 < G * p.RB) {  // warp-uniform: this warp holds rows of the MMA window in use
+          // The warp's lanes hold groups glo .. ghi: load their columns
+          // (16 per group) and keep this lane's.
+          const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (real ? 0u : (uint32_t)issuers * C);
+          const int glo = (q * 32) / p.RB;
+          const int ghi = min(G - 1, (q * 32 + 31) / p.RB);
+          for (int gg = glo; gg <= ghi; ++gg) {
+            float w[16];
+            tmem_ld16(taddr + (uint32_t)(gg * 16), w);  // warp-collective
+            if (gg == g) {
 #pragma unroll
-          for (int i = 0; i < 16; i += 4) {
-            float a0, a1, a2, a3;
-            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                         : "=f"(a0), "=f"(a1), "=f"(a2), "=f"(a3)
-                         : "r"(src + (uint32_t)i * 4u)
+              for (int i = 0; i < 16; ++i) v[i] = w[i];
+            }
+            if (issuers == 2) {  // the second accumulator, added after the first
+              tmem_ld16(taddr + C + (uint32_t)(gg * 16), w);
+              if (gg == g) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] += w[i];
+              }
+            }
+          }
+        }
+        const uint32_t x0 = real ? xch0 : base + kRowsWarmScratch;
+        const uint32_t xs = real ? xstep : 0u;
+        if (ok && helper) {
+          const uint32_t dst = x0 + (uint32_t)(g - 1) * xs;
+#pragma unroll
+          for (int i = 0; i < 16; i += 4)
+            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(dst + (uint32_t)i * 4u), "f"(v[i]),
+                         "f"(v[i + 1]), "f"(v[i + 2]), "f"(v[i + 3])
                          : "memory");
-            v[i] += a0;
-            v[i + 1] += a1;
-            v[i + 2] += a2;
-            v[i + 3] += a3;
-          }
         }
-        __nv_bfloat16* yp = io.Y + n0 + r;
+        named_bar_sync(1, 128);
+        if (ok && owner) {
+          for (int gg = 1; gg < G; ++gg) {
+            const uint32_t src = x0 + (uint32_t)(gg - 1) * xs;
 #pragma unroll
-        for (int m = 0; m < kRowsPrefetchTokens; ++m)
-          if (m < io.M) yp[(size_t)m * io.ldy] = __float2bfloat16_rn(v[m] + res[m]);
+            for (int i = 0; i < 16; i += 4) {
+              float a0, a1, a2, a3;
+              asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                           : "=f"(a0), "=f"(a1), "=f"(a2), "=f"(a3)
+                           : "r"(src + (uint32_t)i * 4u)
+                           : "memory");
+              v[i] += a0;
+              v[i + 1] += a1;
+              v[i + 2] += a2;
+              v[i + 3] += a3;
+            }
+          }
+          __nv_bfloat16* yp = io.Y + n0 + r;
+#pragma unroll
+          for (int m = 0; m < kRowsPrefetchTokens; ++m)
+            st_global_bf16_if(yp + (size_t)m * io.ldy,
+                              __float2bfloat16_rn(v[m] + ((m & 1) ? bf16hi(res2[m / 2]) : bf16lo(res2[m / 2]))),
+                              real && m < io.M);
+        }
       }
     } else {
       const int etid = threadIdx.x - 64;
@@ -746,7 +810,7 @@ struct RowsGroupList {
   int count;
 };
 
-// kMode: kRowsEpi16 for 16-token tiles, else kRowsEpiWide.
+// kMode: the 16-token families for 16-token tiles, else kRowsEpiWide.
 template <int kMode>
 __global__ void __launch_bounds__(rows_threads(kMode), 2)
     rows_grouped_kernel(const __grid_constant__ RowsGroupList list, const RowsParams p) {
@@ -830,10 +894,10 @@ inline int rows_plan(const sgr_config& c, int sms, int M, int N, int K, RowsPara
     p->groups /= 2;
   if (rows_stage_floats(p->groups, rb, nt) * 4 > (size_t)c.stages * rows_stage_bytes(c.k_blocks_per_stage, rb, nt))
     return SGR_ERR_UNSUPPORTED;
-  // Two MMA issuers where the 16-token decode epilogue (which adds the two
+  // Two MMA issuers where a 16-token epilogue (which adds the two
   // accumulators) serves the tile and every stage has at least two windows;
-  // that epilogue also reserves as many columns again for its warm-up pass.
-  const bool decode_epi = nt == kRowsPrefetchTokens && p->groups <= 2 && p->groups * rb <= kTcTileRows;
+  // those epilogues also reserve as many columns again for their warm-up pass.
+  const bool decode_epi = nt == kRowsPrefetchTokens && p->groups * rb <= kTcTileRows;
   p->issuers = decode_epi && c.k_blocks_per_stage >= 2 * p->groups ? 2 : 1;
   const int acc_cols = p->issuers * p->groups * nt;
   p->tmem_cols = detail::pow2_at_least(decode_epi ? 2 * acc_cols : acc_cols);
@@ -844,9 +908,11 @@ inline int rows_plan(const sgr_config& c, int sms, int M, int N, int K, RowsPara
 
 inline cudaError_t rows_init_device() {
   cudaError_t e = set_kernel_smem_attrs(reinterpret_cast<const void*>(rows_skinny_kernel<kRowsEpi16>));
+  if (e == cudaSuccess) e = set_kernel_smem_attrs(reinterpret_cast<const void*>(rows_skinny_kernel<kRowsEpi16G4>));
   if (e == cudaSuccess) e = set_kernel_smem_attrs(reinterpret_cast<const void*>(rows_skinny_kernel<kRowsEpiWide>));
   if (e == cudaSuccess) e = set_kernel_smem_attrs(reinterpret_cast<const void*>(rows_skinny_kernel<kRowsEpi64>));
   if (e == cudaSuccess) e = set_kernel_smem_attrs(reinterpret_cast<const void*>(rows_grouped_kernel<kRowsEpi16>));
+  if (e == cudaSuccess) e = set_kernel_smem_attrs(reinterpret_cast<const void*>(rows_grouped_kernel<kRowsEpi16G4>));
   if (e == cudaSuccess) e = set_kernel_smem_attrs(reinterpret_cast<const void*>(rows_grouped_kernel<kRowsEpiWide>));
   return e;
 }
@@ -878,8 +944,10 @@ inline int rows_launch(const sgr_config& c, int sms, unsigned* err, const void* 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
   lc.numAttrs = pdl ? 1 : 0;
-  auto fn = mode == kRowsEpi16 ? rows_skinny_kernel<kRowsEpi16>
-                               : (mode == kRowsEpi64 ? rows_skinny_kernel<kRowsEpi64> : rows_skinny_kernel<kRowsEpiWide>);
+  auto fn = mode == kRowsEpi16     ? rows_skinny_kernel<kRowsEpi16>
+            : mode == kRowsEpi16G4 ? rows_skinny_kernel<kRowsEpi16G4>
+            : mode == kRowsEpi64   ? rows_skinny_kernel<kRowsEpi64>
+                                   : rows_skinny_kernel<kRowsEpiWide>;
   if (cudaLaunchKernelEx(&lc, fn, tmW, tmA, p) != cudaSuccess) {
     cudaGetLastError();
     return SGR_ERR_LAUNCH;
@@ -927,7 +995,7 @@ inline int rows_grouped_launch(const sgr_config& c, int sms, unsigned* err, cons
   }
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3((unsigned)(grid * count), 1, 1);
-  const int mode = p.NT == 16 ? kRowsEpi16 : kRowsEpiWide;  // 64-token tiles take the general epilogue here
+  const int mode = p.NT == 16 ? rows_epi_mode(p.NT, p.groups) : kRowsEpiWide;  // 64-token tiles: the general epilogue
   lc.blockDim = dim3(rows_threads(mode), 1, 1);
   lc.dynamicSmemBytes = smem;
   lc.stream = stream;
@@ -936,8 +1004,10 @@ inline int rows_grouped_launch(const sgr_config& c, int sms, unsigned* err, cons
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
   lc.numAttrs = pdl ? 1 : 0;
-  if (cudaLaunchKernelEx(&lc, mode == kRowsEpi16 ? rows_grouped_kernel<kRowsEpi16> : rows_grouped_kernel<kRowsEpiWide>,
-                         list, p) != cudaSuccess) {
+  auto fn = mode == kRowsEpi16     ? rows_grouped_kernel<kRowsEpi16>
+            : mode == kRowsEpi16G4 ? rows_grouped_kernel<kRowsEpi16G4>
+                                   : rows_grouped_kernel<kRowsEpiWide>;
+  if (cudaLaunchKernelEx(&lc, fn, list, p) != cudaSuccess) {
     cudaGetLastError();
     return SGR_ERR_LAUNCH;
   }

@@ -41,14 +41,16 @@ def test_row_slab_plans(plans):
         assert p["G"] * p["RB"] <= 128 and p["G"] * p["NT"] <= 256, p            # one MMA window
         assert p["kbps"] % p["G"] == 0, p
         assert p["NT"] >= p["M"] and p["NT"] % 16 == 0, p
-        decode_epi = p["NT"] == 16 and p["G"] <= 2
+        decode_epi = p["NT"] == 16 and p["G"] * p["RB"] <= 128
         # two MMA issuers (alternate windows, own accumulators) only under the
-        # 16-token epilogue that adds them, with two or more windows a stage
+        # 16-token epilogues that add them, with two or more windows a stage
         assert p["issuers"] == (2 if decode_epi and p["kbps"] >= 2 * p["G"] else 1), p
-        # kernel instance by epilogue family: 16-token tiles (224 threads, the
-        # only one with a second issuer), 64-token register form, the rest
-        assert p["mode"] == (0 if p["NT"] == 16 else (2 if p["NT"] == 64 and p["G"] <= 2 else 1)), p
-        assert p["threads"] == (224 if p["mode"] == 0 else 192), p
+        # kernel instance by epilogue family: 16-token tiles with up to two
+        # and with three or four packed groups (224 threads, the only ones with
+        # a second issuer), 64-token register form, the rest
+        want_mode = (0 if p["G"] <= 2 else 3) if p["NT"] == 16 else (2 if p["NT"] == 64 and p["G"] <= 2 else 1)
+        assert p["mode"] == want_mode, p
+        assert p["threads"] == (224 if p["mode"] in (0, 3) else 192), p
         acc_cols = p["issuers"] * p["G"] * p["NT"]
         # that epilogue's warm-up pass reads as many columns again, unwritten
         assert p["tmem_cols"] >= (2 if decode_epi else 1) * acc_cols and p["tmem_cols"] <= 512, p
