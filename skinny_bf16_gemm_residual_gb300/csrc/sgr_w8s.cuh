@@ -195,9 +195,11 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int m, int n) {
   return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
-// kWarmEpi: the epilogue's warm-up pass (the instance for w8s_in_regs(M, K);
-// the other instance has no trace of it).
-template <bool kWarmEpi>
+// kInRegs = w8s_in_regs(M, K): the instance with the register form of the
+// converters and the epilogue's warm-up pass; the other instance has the
+// per-stage form and no warm-up.  Each carries only its own code (the first
+// run of a code path in a CTA is paid in instruction fetches).
+template <bool kInRegs>
 __global__ void __launch_bounds__(kW8sThreads, 1)
     w8s_kernel(const __grid_constant__ CUtensorMap tmW, const W8sParams p) {
   extern __shared__ unsigned char smem_raw[];
@@ -363,7 +365,7 @@ __global__ void __launch_bounds__(kW8sThreads, 1)
     // loop reads each stage's vectors again, one stage ahead.  (Reading them
     // again puts one memory round trip per stage on the converters' path,
     // which then paces the MMAs and the weight ring.)
-    const bool in_regs = w8s_in_regs(p.M, p.K);  // the same in every thread
+    constexpr bool in_regs = kInRegs;  // the host launched the instance for w8s_in_regs(M, K)
     const int vps = p.kbps * (kW8sKBlock / 8);  // vectors per stage (kbps blocks of 128 codes)
     const int voff = ((part % tpt) + tpt) % tpt;
     uint4 cur[kW8sStageVec], nxt[kW8sStageVec];
@@ -439,7 +441,7 @@ __global__ void __launch_bounds__(kW8sThreads, 1)
                                               : make_uint4(0u, 0u, 0u, 0u);
       }
     };
-    if (in_regs) {
+    if constexpr (in_regs) {
       pdl_wait();  // A and R may come from the preceding kernel; Y may be read by it
       uint32_t mag = 0;
 #pragma unroll
@@ -533,7 +535,7 @@ __global__ void __launch_bounds__(kW8sThreads, 1)
       const uint32_t xstep = (uint32_t)p.RB * 80u;
       const uint32_t scratch = b_buf + (uint32_t)w8s_operand_span(p.kbp, p.NT, p.RB);
 #pragma unroll 1
-      for (int pass = kWarmEpi ? 0 : 1; pass < 2; ++pass) {
+      for (int pass = kInRegs ? 0 : 1; pass < 2; ++pass) {
         int passv;  // opaque to the compiler: one copy of the loop body serves both passes
         asm volatile("mov.b32 %0, %1;" : "=r"(passv) : "r"(pass));
         const bool real = passv != 0;
