@@ -1261,16 +1261,17 @@ int sgr_kernel_resources(int device, int path, int M, int N, int K, int* regs, i
     *smem_bytes = (int)smem;
     *threads = sgr::rows_threads(mode);
   } else if (c.path == SGR_PATH_W8) {
-    if (cudaFuncGetAttributes(&fa, sgr::w8_rows_kernel<false>) != cudaSuccess) {
-      cudaGetLastError();
-      return SGR_ERR_DEVICE;
-    }
     sgr::W8Params wp;
     int grid = 0;
     size_t smem = 0;
     int sms = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
     if (sgr::w8_plan(c, sms, M, N, K, &wp, &grid, &smem) != SGR_OK) return SGR_ERR_UNSUPPORTED;
+    if (cudaFuncGetAttributes(&fa, sgr::w8_decode_epi(wp) ? sgr::w8_rows_kernel<false, true>
+                                                          : sgr::w8_rows_kernel<false, false>) != cudaSuccess) {
+      cudaGetLastError();
+      return SGR_ERR_DEVICE;
+    }
     *smem_bytes = (int)smem;
     *threads = sgr::kW8Threads;
   } else if (c.path == SGR_PATH_W8S) {

@@ -119,8 +119,14 @@ __device__ __forceinline__ void w8_widen32(const uint32_t (&x)[8], uint32_t (&o)
   }
 }
 
-// tmS: the NVFP4 block scales (unused, any map, for E4M3).
-template <bool FP4>
+// The 16-token epilogue form serves the plan.
+__host__ __device__ inline bool w8_decode_epi(const W8Params& p) { return p.NT == 16 && p.groups <= 2; }
+
+// tmS: the NVFP4 block scales (unused, any map, for E4M3).  kDecode: the
+// 16-token epilogue with at most two packed groups (w8_decode_epi), else the
+// general one; each instance carries only its own epilogue code (the first
+// run of a code path in a CTA is paid in instruction fetches).
+template <bool FP4, bool kDecode>
 __global__ void __launch_bounds__(kW8Threads, 2)
     w8_rows_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmR, const __grid_constant__ CUtensorMap tmS,
@@ -441,7 +447,7 @@ __global__ void __launch_bounds__(kW8Threads, 2)
       tc_fence_after();
       pdl_wait();  // Y may be read by the preceding kernel (already satisfied: the residual tile came after it)
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16);
-      if (p.NT == 16 && G <= 2) {
+      if constexpr (kDecode) {
         // Decode form: the thread on lane r < RB owns output column n0 + r
         // and holds group 0's sums; the thread on lane RB + r holds group
         // 1's and hands them over through the drained weight ring.
@@ -708,8 +714,10 @@ inline int w8_plan(const sgr_config& c, int sms, int M, int N, int K, W8Params* 
 }
 
 inline cudaError_t w8_init_device() {
-  cudaError_t e = set_kernel_smem_attrs(reinterpret_cast<const void*>(w8_rows_kernel<false>));
-  if (e == cudaSuccess) e = set_kernel_smem_attrs(reinterpret_cast<const void*>(w8_rows_kernel<true>));
+  cudaError_t e = set_kernel_smem_attrs(reinterpret_cast<const void*>(w8_rows_kernel<false, false>));
+  if (e == cudaSuccess) e = set_kernel_smem_attrs(reinterpret_cast<const void*>(w8_rows_kernel<false, true>));
+  if (e == cudaSuccess) e = set_kernel_smem_attrs(reinterpret_cast<const void*>(w8_rows_kernel<true, false>));
+  if (e == cudaSuccess) e = set_kernel_smem_attrs(reinterpret_cast<const void*>(w8_rows_kernel<true, true>));
   return e;
 }
 
@@ -741,7 +749,8 @@ inline int w8_launch(const sgr_config& c, int sms, unsigned* err, const void* A,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
   lc.numAttrs = pdl ? 1 : 0;
-  if (cudaLaunchKernelEx(&lc, w8_rows_kernel<false>, tmW, tmA, tmR, tmW, p) != cudaSuccess) {
+  auto fn = w8_decode_epi(p) ? w8_rows_kernel<false, true> : w8_rows_kernel<false, false>;
+  if (cudaLaunchKernelEx(&lc, fn, tmW, tmA, tmR, tmW, p) != cudaSuccess) {
     cudaGetLastError();
     return SGR_ERR_LAUNCH;
   }
@@ -780,7 +789,8 @@ inline int w4_launch(const sgr_config& c, int sms, unsigned* err, const void* A,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
   lc.numAttrs = pdl ? 1 : 0;
-  if (cudaLaunchKernelEx(&lc, w8_rows_kernel<true>, tmW, tmA, tmR, tmS, p) != cudaSuccess) {
+  auto fn = w8_decode_epi(p) ? w8_rows_kernel<true, true> : w8_rows_kernel<true, false>;
+  if (cudaLaunchKernelEx(&lc, fn, tmW, tmA, tmR, tmS, p) != cudaSuccess) {
     cudaGetLastError();
     return SGR_ERR_LAUNCH;
   }
