@@ -419,7 +419,9 @@ __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, 
     // ------------------------------------------------------------ epilogue
     pdl_wait();  // R may come from the preceding kernel; Y may be read by it
     const int q = warp & 3;       // TMEM lane quarter this warp may access
-    if (kMode == kRowsEpi16 && p.NT == kRowsPrefetchTokens && p.groups <= 2 && p.groups * p.RB <= kTcTileRows) {
+    // Each instance compiles only its own forms: the 16-token ones always
+    // apply to their instance (the planner packs G * RB <= 128 rows).
+    if constexpr (kMode == kRowsEpi16) {
       // Decode epilogue (at most 16 tokens, at most two packed groups): the
       // thread on TMEM lane r < RB owns output column n0 + r and holds group
       // 0's partial sums; the thread on lane RB + r holds group 1's and hands
@@ -594,7 +596,7 @@ __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, 
                               real && m < io.M);
         }
       }
-    } else if (kMode == kRowsEpi16G4 && p.NT == kRowsPrefetchTokens && p.groups * p.RB <= kTcTileRows) {
+    } else if constexpr (kMode == kRowsEpi16G4) {
       // The same for three or four packed groups (short slabs, e.g. 24 rows
       // when N = 3584): lane g*RB + r (g = 1 .. G-1) hands group g's partial
       // sums to the owner of row r, who adds them in g order.  Kept apart
