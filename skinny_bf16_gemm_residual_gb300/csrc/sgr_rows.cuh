@@ -126,9 +126,15 @@ __host__ __device__ inline uint32_t rows_tail_slack(int stages, int kbps, int rb
   return over > a_ring ? over - a_ring : 0u;
 }
 
+// Scratch of the 17-64-token epilogues' warm-up pass, after the rings and
+// the MMA window's over-read slack (no MMA reads it); the 16-token epilogues
+// use the end of the barrier region instead.
+constexpr uint32_t kRowsWideScratch = 512;
+
 __host__ __device__ inline size_t rows_smem_bytes(int stages, int kbps, int rb, int nt) {
   return 1024 /* alignment slack */ + 1024 /* barriers */ +
-         (size_t)stages * rows_stage_bytes(kbps, rb, nt) + rows_tail_slack(stages, kbps, rb, nt);
+         (size_t)stages * rows_stage_bytes(kbps, rb, nt) + rows_tail_slack(stages, kbps, rb, nt) +
+         (nt > 16 ? kRowsWideScratch : 0);
 }
 
 // Shared-memory staging for the epilogue's sum over packed groups:
@@ -153,12 +159,15 @@ struct RowsIO {
 // owns output column n0 + r, lane RB + r holds group 1's partial sums and
 // hands them over through the drained ring), with T accumulator columns per
 // group loaded in 16-column pieces and the residuals of all T token rows
-// loaded into registers before the accumulator is ready.  Called by the four
-// epilogue warps (q: TMEM lane quarter of the warp).
-template <int T>
+// loaded into registers before the accumulator is ready.  Like the 16-token
+// epilogue it first runs a warm-up pass over its instructions while the MMAs
+// run (tensor-memory columns after the accumulator, which no MMA writes, the
+// exchange in `scratch`, stores predicated off; kWarm false skips it).
+// Called by the four epilogue warps (q: TMEM lane quarter of the warp).
+template <int T, bool kWarm>
 __device__ __forceinline__ void rows_epilogue_wide(const RowsParams& p, const RowsIO& io, int n0, uint32_t tmem,
-                                                   uint32_t w_ring, uint64_t* acc_full, volatile int* abort_flag,
-                                                   int q, int lane) {
+                                                   uint32_t w_ring, uint32_t scratch, uint64_t* acc_full,
+                                                   volatile int* abort_flag, int q, int lane) {
   constexpr int C = T / 16;
   const int L = q * 32 + lane;
   const int G = p.groups;
@@ -175,75 +184,85 @@ __device__ __forceinline__ void rows_epilogue_wide(const RowsParams& p, const Ro
     const uint32_t hi = (owner && m + 1 < io.M) ? rp[(size_t)(m + 1) * io.ldr] : 0u;
     res2[m / 2] = lo | (hi << 16);
   }
-  bool ok = mbar_wait_or_abort(smem_u32(acc_full), 0, abort_flag);
-  if (!ok) {
-    if (!*abort_flag) report_error(p.err, kErrWaitMma);
-    *abort_flag = 1;
-  }
-  ok = __all_sync(0xffffffffu, ok);
-  tc_fence_after();
-  float v[T];
+#pragma unroll 1
+  for (int pass = kWarm ? 0 : 1; pass < 2; ++pass) {
+    int passv;  // opaque to the compiler: one copy of the loop body serves both passes
+    asm volatile("mov.b32 %0, %1;" : "=r"(passv) : "r"(pass));
+    const bool real = passv != 0;
+    bool ok = true;
+    if (real) {
+      ok = mbar_wait_or_abort(smem_u32(acc_full), 0, abort_flag);
+      if (!ok) {
+        if (!*abort_flag) report_error(p.err, kErrWaitMma);
+        *abort_flag = 1;
+      }
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    tc_fence_after();
+    float v[T];
 #pragma unroll
-  for (int i = 0; i < T; ++i) v[i] = 0.f;
-  if (ok && q * 32 < G * p.RB) {  // warp-uniform: this warp holds rows of the MMA window in use
-    const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16);
-    // Columns [0, T) hold group 0's diagonal block, [T, 2T) group 1's.
-    const bool straddle = G == 2 && q * 32 < p.RB && (q + 1) * 32 > p.RB;
-    const uint32_t col0 = (G == 2 && q * 32 >= p.RB) ? (uint32_t)T : 0u;
+    for (int i = 0; i < T; ++i) v[i] = 0.f;
+    if (ok && q * 32 < G * p.RB) {  // warp-uniform: this warp holds rows of the MMA window in use
+      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (real ? 0u : (uint32_t)(G * T));
+      // Columns [0, T) hold group 0's diagonal block, [T, 2T) group 1's.
+      const bool straddle = G == 2 && q * 32 < p.RB && (q + 1) * 32 > p.RB;
+      const uint32_t col0 = (G == 2 && q * 32 >= p.RB) ? (uint32_t)T : 0u;
 #pragma unroll
-    for (int c = 0; c < C; ++c) {
-      float a[16];
-      tmem_ld16(taddr + col0 + (uint32_t)(16 * c), a);  // warp-collective
-      if (straddle) {
-        float b[16];
-        tmem_ld16(taddr + (uint32_t)(T + 16 * c), b);
-        if (L >= p.RB) {
+      for (int c = 0; c < C; ++c) {
+        float a[16];
+        tmem_ld16(taddr + col0 + (uint32_t)(16 * c), a);  // warp-collective
+        if (straddle) {
+          float b[16];
+          tmem_ld16(taddr + (uint32_t)(T + 16 * c), b);
+          if (L >= p.RB) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) a[i] = b[i];
+            for (int i = 0; i < 16; ++i) a[i] = b[i];
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[16 * c + i] = a[i];
+      }
+    }
+    const uint32_t x = real ? xch : scratch;
+    if (ok && helper) {
+#pragma unroll
+      for (int i = 0; i < T; i += 4)
+        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(x + (uint32_t)i * 4u), "f"(v[i]),
+                     "f"(v[i + 1]), "f"(v[i + 2]), "f"(v[i + 3])
+                     : "memory");
+    }
+    named_bar_sync(1, 128);
+    if (ok && owner) {
+      if (G == 2) {
+#pragma unroll
+        for (int i = 0; i < T; i += 4) {
+          float a0, a1, a2, a3;
+          asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                       : "=f"(a0), "=f"(a1), "=f"(a2), "=f"(a3)
+                       : "r"(x + (uint32_t)i * 4u)
+                       : "memory");
+          v[i] += a0;
+          v[i + 1] += a1;
+          v[i + 2] += a2;
+          v[i + 3] += a3;
         }
       }
+      __nv_bfloat16* yp = io.Y + n0 + L;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) v[16 * c + i] = a[i];
-    }
-  }
-  if (ok && helper) {
-#pragma unroll
-    for (int i = 0; i < T; i += 4)
-      asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(xch + (uint32_t)i * 4u), "f"(v[i]), "f"(v[i + 1]),
-                   "f"(v[i + 2]), "f"(v[i + 3])
-                   : "memory");
-  }
-  named_bar_sync(1, 128);
-  if (ok && owner) {
-    if (G == 2) {
-#pragma unroll
-      for (int i = 0; i < T; i += 4) {
-        float a0, a1, a2, a3;
-        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                     : "=f"(a0), "=f"(a1), "=f"(a2), "=f"(a3)
-                     : "r"(xch + (uint32_t)i * 4u)
-                     : "memory");
-        v[i] += a0;
-        v[i + 1] += a1;
-        v[i + 2] += a2;
-        v[i + 3] += a3;
-      }
-    }
-    __nv_bfloat16* yp = io.Y + n0 + L;
-#pragma unroll
-    for (int m = 0; m < T; ++m)
-      if (m < io.M) {
+      for (int m = 0; m < T; ++m) {
         const float rm = (m & 1) ? bf16hi(res2[m / 2]) : bf16lo(res2[m / 2]);
-        yp[(size_t)m * io.ldy] = __float2bfloat16_rn(v[m] + rm);
+        st_global_bf16_if(yp + (size_t)m * io.ldy, __float2bfloat16_rn(v[m] + rm), real && m < io.M);
       }
+    }
   }
 }
 
 // One CTA: the RB-row slab of W starting at row n0 of the problem `io`, with
 // the epilogue family kMode (the 64-token register epilogue needs more
 // registers per thread: only its own instance has it, so that the others
-// keep two CTAs per SM where their shared memory allows).
-template <int kMode>
+// keep two CTAs per SM where their shared memory allows); kWideWarm: the
+// 17-64-token register epilogues run their warm-up pass.
+template <int kMode, bool kWideWarm>
 __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, int n0) {
   const int issuers = rows_two_issuer_mode(kMode) ? p.issuers : 1;
   extern __shared__ unsigned char smem_raw[];
@@ -264,6 +283,8 @@ __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, 
   const uint32_t stage_bytes = w_stage + a_stage;  // bytes one stage brings in
   const uint32_t w_ring = base + 1024;                         // [stages][kbps] W boxes
   const uint32_t a_ring = w_ring + (uint32_t)S * w_stage;      // [stages][kbps] A boxes
+  const uint32_t wide_scratch =  // after the A ring and the MMA window's over-read slack
+      a_ring + (uint32_t)S * a_stage + rows_tail_slack(S, p.kbps, p.RB, p.NT);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int KS = p.k_stages;
@@ -518,11 +539,11 @@ __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, 
         }
       }
     } else if (kMode == kRowsEpiWide && p.NT == 32 && p.groups <= 2 && p.groups * p.RB <= kTcTileRows) {
-      rows_epilogue_wide<32>(p, io, n0, tmem, w_ring, acc_full, abort_flag, q, lane);
+      rows_epilogue_wide<32, kWideWarm>(p, io, n0, tmem, w_ring, wide_scratch, acc_full, abort_flag, q, lane);
     } else if (kMode == kRowsEpiWide && p.NT == 48 && p.groups <= 2 && p.groups * p.RB <= kTcTileRows) {
-      rows_epilogue_wide<48>(p, io, n0, tmem, w_ring, acc_full, abort_flag, q, lane);
+      rows_epilogue_wide<48, kWideWarm>(p, io, n0, tmem, w_ring, wide_scratch, acc_full, abort_flag, q, lane);
     } else if (kMode == kRowsEpi64 && p.NT == 64 && p.groups <= 2 && p.groups * p.RB <= kTcTileRows) {
-      rows_epilogue_wide<64>(p, io, n0, tmem, w_ring, acc_full, abort_flag, q, lane);
+      rows_epilogue_wide<64, kWideWarm>(p, io, n0, tmem, w_ring, wide_scratch, acc_full, abort_flag, q, lane);
     } else if (kMode == kRowsEpi16G4 && p.NT == kRowsPrefetchTokens && p.groups == 4 && p.RB == 32) {
       // 32-row slabs, four packed groups: warp quarter q holds group q whole.
       // Warps 1-3 hand their partial sums to warp 0's lanes (one output
@@ -789,7 +810,7 @@ __global__ void __launch_bounds__(rows_threads(kMode), kMode == kRowsEpi64 ? 1 :
     rows_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA,
                        const RowsParams p) {
   const RowsIO io{&tmW, &tmA, p.R, p.Y, p.ldr, p.ldy, p.M};
-  rows_run<kMode>(p, io, (int)blockIdx.x * p.RB);
+  rows_run<kMode, true>(p, io, (int)blockIdx.x * p.RB);
 }
 
 // Grouped launch: several independent problems with the same N and K and
@@ -812,7 +833,9 @@ struct RowsGroupList {
   int count;
 };
 
-// kMode: the 16-token families for 16-token tiles, else kRowsEpiWide.
+// kMode: the 16-token families for 16-token tiles, else kRowsEpiWide (whose
+// 32/48-token epilogue here runs without its warm-up pass, which would cost
+// this kernel register spills).
 template <int kMode>
 __global__ void __launch_bounds__(rows_threads(kMode), 2)
     rows_grouped_kernel(const __grid_constant__ RowsGroupList list, const RowsParams p) {
@@ -820,7 +843,7 @@ __global__ void __launch_bounds__(rows_threads(kMode), 2)
   const int slab = (int)blockIdx.x / list.count;
   const RowsGroup& g = list.g[e];
   const RowsIO io{&g.tmW, &g.tmA, g.R, g.Y, g.ldr, g.ldy, g.M};
-  rows_run<kMode>(p, io, slab * p.RB);
+  rows_run<kMode, false>(p, io, slab * p.RB);
 }
 
 // ------------------------------------------------------------------ host side
@@ -902,7 +925,9 @@ inline int rows_plan(const sgr_config& c, int sms, int M, int N, int K, RowsPara
   const bool decode_epi = nt == kRowsPrefetchTokens && p->groups * rb <= kTcTileRows;
   p->issuers = decode_epi && c.k_blocks_per_stage >= 2 * p->groups ? 2 : 1;
   const int acc_cols = p->issuers * p->groups * nt;
-  p->tmem_cols = detail::pow2_at_least(decode_epi ? 2 * acc_cols : acc_cols);
+  // The 17-64-token register epilogues (at most two groups) warm up too.
+  const bool wide_epi = (nt == 32 || nt == 48 || nt == 64) && p->groups <= 2 && p->groups * rb <= kTcTileRows;
+  p->tmem_cols = detail::pow2_at_least(decode_epi || wide_epi ? 2 * acc_cols : acc_cols);
   *grid = (N + rb - 1) / rb;
   *smem = sm;
   return SGR_OK;

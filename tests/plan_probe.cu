@@ -41,10 +41,10 @@ int main() {
             std::printf("{\"kind\": \"rows\", \"M\": %d, \"N\": %d, \"K\": %d, \"RB\": %d, \"NT\": %d, \"G\": %d, "
                         "\"kbps\": %d, \"stages\": %d, \"prefetch\": %d, \"k_stages\": %d, \"tmem_cols\": %d, "
                         "\"issuers\": %d, \"mode\": %d, \"threads\": %d, \"grid\": %d, \"smem\": %zu, \"w_ring\": %zu, "
-                        "\"a_ring\": %zu}\n",
+                        "\"a_ring\": %zu, \"slack\": %u}\n",
                         M, N, K, p.RB, p.NT, p.groups, p.kbps, p.stages, p.prefetch, p.k_stages, p.tmem_cols,
                         p.issuers, sgr::rows_epi_mode(p.NT, p.groups), sgr::rows_threads(sgr::rows_epi_mode(p.NT, p.groups)),
-                        grid, smem, w_ring, a_ring);
+                        grid, smem, w_ring, a_ring, (unsigned)sgr::rows_tail_slack(p.stages, p.kbps, p.RB, p.NT));
           }
       // FP8 row-slab kernel
       for (int rb : {0, 8, 24, 32, 64, 128})

@@ -52,8 +52,16 @@ def test_row_slab_plans(plans):
         assert p["mode"] == want_mode, p
         assert p["threads"] == (224 if p["mode"] in (0, 3) else 192), p
         acc_cols = p["issuers"] * p["G"] * p["NT"]
-        # that epilogue's warm-up pass reads as many columns again, unwritten
-        assert p["tmem_cols"] >= (2 if decode_epi else 1) * acc_cols and p["tmem_cols"] <= 512, p
+        # the register epilogues' warm-up pass (16 tokens, and 32-64 tokens in
+        # at most two groups) reads as many columns again, unwritten
+        warm_epi = decode_epi or (p["NT"] in (32, 48, 64) and p["G"] <= 2 and p["G"] * p["RB"] <= 128)
+        assert p["tmem_cols"] >= (2 if warm_epi else 1) * acc_cols and p["tmem_cols"] <= 512, p
+        # alignment slack and barrier region, the rings, the MMA window's
+        # over-read slack, and the 32-64-token warm-up pass's 512-byte scratch
+        # (its exchange: up to NT + 4 floats)
+        assert p["smem"] == 2048 + p["w_ring"] + p["a_ring"] + p["slack"] + (512 if p["NT"] > 16 else 0), p
+        if warm_epi:
+            assert (p["NT"] + 4) * 4 <= 512, p
         assert p["grid"] * p["RB"] >= p["N"] > (p["grid"] - 1) * p["RB"], p      # every row, no empty CTA
         assert p["k_stages"] * p["kbps"] * 64 >= p["K"], p
         assert 1 <= p["prefetch"] <= p["stages"], p
