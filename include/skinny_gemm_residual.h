@@ -144,7 +144,10 @@ typedef struct {
   int tile_n;             /* TILE: W rows per output tile (MMA N): 64, 128, 192 or 256;
                              PAIR: W rows per 256-token tile: 64, 96, 128, 192 or 256 */
   int k_split;            /* TILE: 1, or S = 2, 3, 4 = K split over an S-CTA cluster (one tile per cluster, all
-                             clusters resident at once); tile_n 64/128/192 for S = 2, 192 for 3, 128/192/256 for 4 */
+                             clusters resident at once); tile_n 64/128/192 for S = 2, 192 for 3, 128/192/256 for 4;
+                             TC_ROWS: 0 or 1, or 2 = each W slab on a 2-CTA cluster, one CTA per half of K, the
+                             partial sums added in the epilogue through distributed shared memory (token tiles of
+                             16-64 with at most two K blocks per MMA) */
   int reserved[2];        /* must be zero */
 } sgr_config;
 

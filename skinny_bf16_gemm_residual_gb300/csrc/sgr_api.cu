@@ -362,6 +362,7 @@ int resolve_config(int dev_sms, int M, int N, int K, const sgr_config* in, sgr_c
       if (path == SGR_PATH_TC_ROWS || tiled) out->prefetch_stages = e->prefetch_stages;
       if (tiled && e->tile_n) out->tile_n = e->tile_n;
       if (path == SGR_PATH_TILE) out->k_split = e->k_split > 0 ? e->k_split : 1;
+      if (path == SGR_PATH_TC_ROWS && e->k_split == 2) out->k_split = 2;
     }
   }
   if (in) {

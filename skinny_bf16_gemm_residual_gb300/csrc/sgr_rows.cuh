@@ -8,6 +8,12 @@
 // kernel) every CTA owns a contiguous slab of RB whole rows of W, RB =
 // ceil(N / SMs) rounded up to 8 (48 for N = 7168 on 152 SMs), so no output
 // element is split across CTAs: no workspace, no counters, no fixup tail.
+// (Except under the 2-CTA K split, k_split = 2, for long K with few rows per
+// SM, as in the down-projection N = 3584, K = 7168: each slab goes to a
+// 2-CTA cluster whose rank r streams the r-th half of K, i.e. 48-row slabs of
+// half of K instead of 24-row slabs of all of it, and the epilogue adds the
+// peer's partial sums read through distributed shared memory; rank 0
+// finishes the slab's first RB / 2 columns, rank 1 the others.)
 // The slab is streamed once with 2-D TMA boxes of RB rows x 64 K into a
 // shared-memory ring and multiplied on the tensor core with
 // tcgen05.mma M=128 (W rows) x N=G*NT (tokens) x K=16.
@@ -47,8 +53,8 @@
 // Warm-up pass: the first run of a code path in a CTA costs ~0.7 us more
 // than the next (measured with the weight stream saturating L2: instruction
 // and parameter fetches wait behind it), and the epilogue runs once, on the
-// critical path after the last weights land.  So the decode epilogue runs its
-// instructions twice: first while the MMAs are still running, against tensor-
+// critical path after the last weights land.  So the 16- to 64-token
+// epilogues run their instructions twice: first while the MMAs are still running, against tensor-
 // memory columns no MMA writes, a scratch word of shared memory and stores
 // predicated off, then for real.
 //
@@ -107,11 +113,12 @@ struct RowsParams {
   int prefetch;  // W stages requested before griddepcontrol.wait (1..stages)
   int issuers;   // MMA-issuing threads (1 or 2), each into its own accumulator
   int tmem_cols;
+  int ksplit;    // 1, or 2: K split over a 2-CTA cluster (rank r takes K blocks from r k_stages kbps on)
 };
 
 // Scratch bytes of the decode epilogue's warm-up pass: the end of the
-// 1024-byte barrier region (at most 32 stages: 2 x 32 + 2 barriers, the TMEM
-// address and the abort flag end below byte 544).
+// 1024-byte barrier region (at most 32 stages: 2 x 32 + 3 barriers, the TMEM
+// address and the abort flag end at byte 544).
 constexpr uint32_t kRowsWarmScratch = 960;
 
 __host__ __device__ inline uint32_t rows_stage_bytes(int kbps, int rb, int nt) {
@@ -154,6 +161,52 @@ struct RowsIO {
   int M;
 };
 
+// Bytes per row of the epilogues' hand-over buffers in the drained ring: the
+// group-1 partial sums at rows [0, RB), and under the 2-CTA K split the
+// partial sums the peer finishes at rows [RB, 2 RB).
+__host__ __device__ inline uint32_t rows_xch_stride(int nt) { return nt == 16 ? 80u : (uint32_t)(nt + 4) * 4u; }
+
+// 2-CTA K split: owner thread L of either rank holds that rank's partial sums
+// v[0..T) of output column n0 + L; rank 0 finishes the columns L < RB / 2,
+// rank 1 the others.  A thread whose column the peer finishes leaves its
+// partial sums in its own drained ring at `xo`; every epilogue thread then
+// arrives once on the peer's `ready` barrier (releasing those writes at
+// cluster scope) and waits for the peer's 128 arrivals on its own; a
+// finishing thread adds the peer's partial sums, read at the same offset of
+// the peer's shared memory (the sum of two terms is the same in either
+// order).  Returns false after a timed-out wait (reported).
+template <int T>
+__device__ __forceinline__ bool rows_pair_exchange(float (&v)[T], bool has, bool fin, uint32_t xo, uint64_t* ready,
+                                                   uint32_t rank, volatile int* abort_flag, unsigned* err) {
+  if (has && !fin) {
+#pragma unroll
+    for (int i = 0; i < T; i += 4)
+      asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(xo + (uint32_t)i * 4u), "f"(v[i]), "f"(v[i + 1]),
+                   "f"(v[i + 2]), "f"(v[i + 3])
+                   : "memory");
+  }
+  mbar_arrive_remote(map_to_rank(smem_u32(ready), rank ^ 1u));
+  bool got = mbar_wait_cluster(smem_u32(ready), 0, abort_flag);
+  got = __all_sync(0xffffffffu, got);
+  if (!got) {
+    if (!*abort_flag) report_error(err, kErrWaitFixup);
+    *abort_flag = 1;
+    return false;
+  }
+  if (has && fin) {
+    const uint32_t src = map_to_rank(xo, rank ^ 1u);
+#pragma unroll
+    for (int i = 0; i < T; i += 4) {
+      const float4 o = ld_cluster_f32x4(src + (uint32_t)i * 4u);
+      v[i] += o.x;
+      v[i + 1] += o.y;
+      v[i + 2] += o.z;
+      v[i + 3] += o.w;
+    }
+  }
+  return true;
+}
+
 // Epilogue for 17..64 tokens (token tile T = 32, 48 or 64) with at most two
 // packed groups: the ownership of the 16-token decode epilogue (lane r < RB
 // owns output column n0 + r, lane RB + r holds group 1's partial sums and
@@ -163,25 +216,32 @@ struct RowsIO {
 // epilogue it first runs a warm-up pass over its instructions while the MMAs
 // run (tensor-memory columns after the accumulator, which no MMA writes, the
 // exchange in `scratch`, stores predicated off; kWarm false skips it).
-// Called by the four epilogue warps (q: TMEM lane quarter of the warp).
+// Under the 2-CTA K split the partial sums are completed by
+// rows_pair_exchange before the residual add.  Called by the
+// four epilogue warps (q: TMEM lane quarter of the warp).
 template <int T, bool kWarm>
 __device__ __forceinline__ void rows_epilogue_wide(const RowsParams& p, const RowsIO& io, int n0, uint32_t tmem,
                                                    uint32_t w_ring, uint32_t scratch, uint64_t* acc_full,
-                                                   volatile int* abort_flag, int q, int lane) {
+                                                   uint64_t* ready, volatile int* abort_flag, int q, int lane) {
   constexpr int C = T / 16;
   const int L = q * 32 + lane;
   const int G = p.groups;
   const bool owner = L < p.RB && n0 + L < p.N;
+  // Under the K split this rank stores column n0 + L only if fin (the rank is
+  // read again where needed rather than held through the epilogue).
+  const bool split = p.ksplit == 2;
+  const bool fin = !split || ((L < p.RB / 2) == (cluster_ctarank() == 0u));
   const bool helper = G == 2 && L >= p.RB && L < 2 * p.RB;
   const int r = owner ? L : L - p.RB;
-  const uint32_t xch = w_ring + (uint32_t)(helper || owner ? r : 0) * (uint32_t)((T + 4) * 4);  // T floats + pad per row
+  const uint32_t stride = rows_xch_stride(T);  // T floats + pad per row
+  const uint32_t xch = w_ring + (uint32_t)(helper || owner ? r : 0) * stride;
   // Residuals kept as BF16 pairs (half the registers of FP32 values).
   const unsigned short* rp = reinterpret_cast<const unsigned short*>(io.R) + n0 + L;
   uint32_t res2[T / 2];
 #pragma unroll
   for (int m = 0; m < T; m += 2) {
-    const uint32_t lo = (owner && m < io.M) ? rp[(size_t)m * io.ldr] : 0u;
-    const uint32_t hi = (owner && m + 1 < io.M) ? rp[(size_t)(m + 1) * io.ldr] : 0u;
+    const uint32_t lo = (owner && fin && m < io.M) ? rp[(size_t)m * io.ldr] : 0u;
+    const uint32_t hi = (owner && fin && m + 1 < io.M) ? rp[(size_t)(m + 1) * io.ldr] : 0u;
     res2[m / 2] = lo | (hi << 16);
   }
 #pragma unroll 1
@@ -232,21 +292,25 @@ __device__ __forceinline__ void rows_epilogue_wide(const RowsParams& p, const Ro
                      : "memory");
     }
     named_bar_sync(1, 128);
-    if (ok && owner) {
-      if (G == 2) {
+    if (ok && owner && G == 2) {
 #pragma unroll
-        for (int i = 0; i < T; i += 4) {
-          float a0, a1, a2, a3;
-          asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                       : "=f"(a0), "=f"(a1), "=f"(a2), "=f"(a3)
-                       : "r"(x + (uint32_t)i * 4u)
-                       : "memory");
-          v[i] += a0;
-          v[i + 1] += a1;
-          v[i + 2] += a2;
-          v[i + 3] += a3;
-        }
+      for (int i = 0; i < T; i += 4) {
+        float a0, a1, a2, a3;
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(a0), "=f"(a1), "=f"(a2), "=f"(a3)
+                     : "r"(x + (uint32_t)i * 4u)
+                     : "memory");
+        v[i] += a0;
+        v[i + 1] += a1;
+        v[i + 2] += a2;
+        v[i + 3] += a3;
       }
+    }
+    if (split && real)
+      ok = rows_pair_exchange<T>(v, ok && owner, fin, xch + (uint32_t)p.RB * stride, ready, cluster_ctarank(),
+                                 abort_flag, p.err) &&
+           ok;
+    if (ok && owner && fin) {
       __nv_bfloat16* yp = io.Y + n0 + L;
 #pragma unroll
       for (int m = 0; m < T; ++m) {
@@ -274,8 +338,11 @@ __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, 
   uint64_t* empty = full + S;                         // [S]
   uint64_t* acc_full = empty + S;                     // [1]
   uint64_t* drain = acc_full + 1;                     // [1]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* ready = drain + 1;                        // [1] the K-split peer's partial sums
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ready + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const bool split = p.ksplit == 2;
+  const uint32_t rank = split ? cluster_ctarank() : 0u;
   const uint32_t wblk = (uint32_t)p.RB * 128u;   // bytes of one W box (RB rows x 128 B)
   const uint32_t ablk = (uint32_t)p.NT * 128u;   // bytes of one A box
   const uint32_t w_stage = (uint32_t)p.kbps * wblk;
@@ -298,6 +365,7 @@ __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, 
     }
     mbar_init(smem_u32(acc_full), (uint32_t)issuers);
     mbar_init(smem_u32(drain), (uint32_t)issuers);
+    mbar_init(smem_u32(ready), 128u);  // the peer's four epilogue warps
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -314,6 +382,10 @@ __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, 
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Under the K split the peer's barriers must exist before the first remote
+  // arrive: every thread arrives here, and waits for this phase before its
+  // first remote access (the epilogue warps) or at the end (the others).
+  if (split) cluster_arrive();
   pdl_launch_dependents();  // the dependent grid still waits for our completion before reading
 
   if (warp == 0) {
@@ -325,18 +397,21 @@ __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, 
       // slot left free lets weights keep streaming while A (needed by the
       // first MMA) is fetched after the wait.
       const int pre = KS < p.prefetch ? KS : p.prefetch;
+      // This rank's first K element (rank 1 of a K split may start or run
+      // past K: those boxes are zero-filled and add nothing).
+      const int kbase = (int)rank * KS * p.kbps * kTcKBlock;
       for (int s = 0; s < pre; ++s) {
         const uint32_t fb = smem_u32(&full[s]);
         mbar_arrive_expect_tx(fb, stage_bytes);
         const uint32_t ws = w_ring + (uint32_t)s * w_stage;
         for (int j = 0; j < p.kbps; ++j)
-          tma_load_2d(ws + (uint32_t)j * wblk, tmW, (s * p.kbps + j) * kTcKBlock, n0, fb, pol_w);
+          tma_load_2d(ws + (uint32_t)j * wblk, tmW, kbase + (s * p.kbps + j) * kTcKBlock, n0, fb, pol_w);
       }
       pdl_wait();
       for (int s = 0; s < pre; ++s) {
         const uint32_t as = a_ring + (uint32_t)s * a_stage;
         for (int j = 0; j < p.kbps; ++j)
-          tma_load_2d(as + (uint32_t)j * ablk, tmA, (s * p.kbps + j) * kTcKBlock, 0,
+          tma_load_2d(as + (uint32_t)j * ablk, tmA, kbase + (s * p.kbps + j) * kTcKBlock, 0,
                       smem_u32(&full[s]), pol_a);
       }
       // Ring position kept by increments: no integer division on the
@@ -345,7 +420,7 @@ __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, 
       int slot = pre == S ? 0 : pre;
       uint32_t par = pre == S ? 1u : 0u;  // ring round parity of `slot`
       uint32_t ws = w_ring + (uint32_t)slot * w_stage, as = a_ring + (uint32_t)slot * a_stage;
-      int kx = pre * p.kbps * kTcKBlock;
+      int kx = kbase + pre * p.kbps * kTcKBlock;
       const int kstep = p.kbps * kTcKBlock;
       for (int s = pre; s < KS; ++s) {
         if (s >= S && !mbar_wait_or_abort(smem_u32(&empty[slot]), par ^ 1u, abort_flag)) {
@@ -438,6 +513,7 @@ __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, 
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    if (split) cluster_wait();  // the peer's barriers exist (the CTAs of a cluster start together)
     pdl_wait();  // R may come from the preceding kernel; Y may be read by it
     const int q = warp & 3;       // TMEM lane quarter this warp may access
     // Each instance compiles only its own forms: the 16-token ones always
@@ -451,6 +527,7 @@ __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, 
       const int L = q * 32 + lane;
       const int G = p.groups;
       const bool owner = L < p.RB && n0 + L < p.N;
+      const bool fin = !split || ((L < p.RB / 2) == (rank == 0u));  // this rank stores column n0 + L
       const bool helper = G == 2 && L >= p.RB && L < 2 * p.RB;
       const int r = owner ? L : L - p.RB;
       const uint32_t xch = w_ring + (uint32_t)(helper || owner ? r : 0) * 80u;  // drained ring: 16 floats + pad per row
@@ -459,8 +536,8 @@ __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, 
         const unsigned short* rp = reinterpret_cast<const unsigned short*>(io.R) + n0 + L;
 #pragma unroll
         for (int m = 0; m < kRowsPrefetchTokens; m += 2) {
-          const uint32_t lo = (owner && m < io.M) ? rp[(size_t)m * io.ldr] : 0u;
-          const uint32_t hi = (owner && m + 1 < io.M) ? rp[(size_t)(m + 1) * io.ldr] : 0u;
+          const uint32_t lo = (owner && fin && m < io.M) ? rp[(size_t)m * io.ldr] : 0u;
+          const uint32_t hi = (owner && fin && m + 1 < io.M) ? rp[(size_t)(m + 1) * io.ldr] : 0u;
           res2[m / 2] = lo | (hi << 16);
         }
       }
@@ -515,21 +592,25 @@ __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, 
                          : "memory");
         }
         named_bar_sync(1, 128);
-        if (ok && owner) {
-          if (G == 2) {
+        if (ok && owner && G == 2) {
 #pragma unroll
-            for (int i = 0; i < 16; i += 4) {
-              float a0, a1, a2, a3;
-              asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                           : "=f"(a0), "=f"(a1), "=f"(a2), "=f"(a3)
-                           : "r"(x + (uint32_t)i * 4u)
-                           : "memory");
-              v[i] += a0;
-              v[i + 1] += a1;
-              v[i + 2] += a2;
-              v[i + 3] += a3;
-            }
+          for (int i = 0; i < 16; i += 4) {
+            float a0, a1, a2, a3;
+            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(a0), "=f"(a1), "=f"(a2), "=f"(a3)
+                         : "r"(x + (uint32_t)i * 4u)
+                         : "memory");
+            v[i] += a0;
+            v[i + 1] += a1;
+            v[i + 2] += a2;
+            v[i + 3] += a3;
           }
+        }
+        if (split && real)
+          ok = rows_pair_exchange<16>(v, ok && owner, fin, xch + (uint32_t)p.RB * 80u, ready, rank, abort_flag,
+                                      p.err) &&
+               ok;
+        if (ok && owner && fin) {
           __nv_bfloat16* yp = io.Y + n0 + L;
 #pragma unroll
           for (int m = 0; m < kRowsPrefetchTokens; ++m)
@@ -539,11 +620,14 @@ __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, 
         }
       }
     } else if (kMode == kRowsEpiWide && p.NT == 32 && p.groups <= 2 && p.groups * p.RB <= kTcTileRows) {
-      rows_epilogue_wide<32, kWideWarm>(p, io, n0, tmem, w_ring, wide_scratch, acc_full, abort_flag, q, lane);
+      rows_epilogue_wide<32, kWideWarm>(p, io, n0, tmem, w_ring, wide_scratch, acc_full, ready, abort_flag, q,
+                                          lane);
     } else if (kMode == kRowsEpiWide && p.NT == 48 && p.groups <= 2 && p.groups * p.RB <= kTcTileRows) {
-      rows_epilogue_wide<48, kWideWarm>(p, io, n0, tmem, w_ring, wide_scratch, acc_full, abort_flag, q, lane);
+      rows_epilogue_wide<48, kWideWarm>(p, io, n0, tmem, w_ring, wide_scratch, acc_full, ready, abort_flag, q,
+                                          lane);
     } else if (kMode == kRowsEpi64 && p.NT == 64 && p.groups <= 2 && p.groups * p.RB <= kTcTileRows) {
-      rows_epilogue_wide<64, kWideWarm>(p, io, n0, tmem, w_ring, wide_scratch, acc_full, abort_flag, q, lane);
+      rows_epilogue_wide<64, kWideWarm>(p, io, n0, tmem, w_ring, wide_scratch, acc_full, ready, abort_flag, q,
+                                          lane);
     } else if (kMode == kRowsEpi16G4 && p.NT == kRowsPrefetchTokens && p.groups == 4 && p.RB == 32) {
       // 32-row slabs, four packed groups: warp quarter q holds group q whole.
       // Warps 1-3 hand their partial sums to warp 0's lanes (one output
@@ -800,6 +884,12 @@ __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, 
     tc_fence_after();
     tmem_dealloc(tmem, (uint32_t)p.tmem_cols);
   }
+  if (split) {
+    // The producer and MMA warps close the start-up phase; then no CTA
+    // leaves while its peer may still read its shared memory.
+    if (warp == 0 || warp == 1 || warp == 6) cluster_wait();
+    cluster_sync_all();
+  }
 }
 
 // Two CTAs per SM where their shared memory allows (the register budget is
@@ -810,7 +900,7 @@ __global__ void __launch_bounds__(rows_threads(kMode), kMode == kRowsEpi64 ? 1 :
     rows_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA,
                        const RowsParams p) {
   const RowsIO io{&tmW, &tmA, p.R, p.Y, p.ldr, p.ldy, p.M};
-  rows_run<kMode, true>(p, io, (int)blockIdx.x * p.RB);
+  rows_run<kMode, true>(p, io, (int)(blockIdx.x / (unsigned)p.ksplit) * p.RB);  // a K-split pair shares its slab
 }
 
 // Grouped launch: several independent problems with the same N and K and
@@ -887,10 +977,13 @@ inline int rows_plan(const sgr_config& c, int sms, int M, int N, int K, RowsPara
   if (c.k_blocks_per_stage < 1 || c.k_blocks_per_stage > 8) return SGR_ERR_UNSUPPORTED;
   if (c.ctas_per_sm != 1) return SGR_ERR_UNSUPPORTED;
   if (c.stages < 2 || c.stages > 32) return SGR_ERR_UNSUPPORTED;
-  // W rows per CTA: N / SMs rounded up to 8 unless the configuration names a
+  if (c.k_split < 0 || c.k_split > 2) return SGR_ERR_UNSUPPORTED;
+  const int ks = c.k_split == 2 ? 2 : 1;
+  // W rows per CTA: N / SMs rounded up to 8 (N / (SMs / 2) under the K
+  // split, whose two CTAs share a slab) unless the configuration names a
   // slab height (rows_per_stage; e.g. 32 rows: 224 CTAs for N = 7168, two per
   // SM, four K blocks per MMA).
-  const int rb = c.rows_per_stage > 0 ? c.rows_per_stage : rows_per_cta(sms, N);
+  const int rb = c.rows_per_stage > 0 ? c.rows_per_stage : rows_per_cta(sms / ks > 0 ? sms / ks : 1, N);
   if (rb % 8 != 0 || rb > kTcTileRows) return SGR_ERR_UNSUPPORTED;
   const size_t sm = rows_smem_bytes(c.stages, c.k_blocks_per_stage, rb, nt);
   if (sm > 232448) return SGR_ERR_UNSUPPORTED;
@@ -900,7 +993,8 @@ inline int rows_plan(const sgr_config& c, int sms, int M, int N, int K, RowsPara
   p->K = K;
   p->RB = rb;
   p->NT = nt;
-  p->k_stages = (K + kstage_elems - 1) / kstage_elems;
+  p->ksplit = ks;
+  p->k_stages = (K + ks * kstage_elems - 1) / (ks * kstage_elems);  // per rank
   p->kbps = c.k_blocks_per_stage;
   p->stages = c.stages;
   p->prefetch = c.prefetch_stages > 0 ? c.prefetch_stages : (c.stages > 2 ? c.stages - 1 : c.stages);
@@ -908,8 +1002,9 @@ inline int rows_plan(const sgr_config& c, int sms, int M, int N, int K, RowsPara
   // Diagonal packing: as many consecutive K blocks per MMA as fit in the
   // 128-row window and the 256-column N limit, dividing the stage's blocks,
   // with room to stage the epilogue's partial sums in the drained ring.
+  // (At most two under the K split, whose epilogues take at most two.)
   p->groups = 1;
-  for (int gcount = 4; gcount >= 2; gcount /= 2)
+  for (int gcount = ks == 2 ? 2 : 4; gcount >= 2; gcount /= 2)
     if (gcount * rb <= kTcTileRows && gcount * nt <= 256 && c.k_blocks_per_stage % gcount == 0) {
       p->groups = gcount;
       break;
@@ -928,7 +1023,13 @@ inline int rows_plan(const sgr_config& c, int sms, int M, int N, int K, RowsPara
   // The 17-64-token register epilogues (at most two groups) warm up too.
   const bool wide_epi = (nt == 32 || nt == 48 || nt == 64) && p->groups <= 2 && p->groups * rb <= kTcTileRows;
   p->tmem_cols = detail::pow2_at_least(decode_epi || wide_epi ? 2 * acc_cols : acc_cols);
-  *grid = (N + rb - 1) / rb;
+  // The K split completes its partial sums in the 16-64-token register
+  // epilogues (at most two groups), whose hand-over buffers then take two
+  // rows per W row in the drained ring.
+  if (ks == 2 && (!(decode_epi || wide_epi) || p->groups > 2 ||
+                  (size_t)2 * rb * rows_xch_stride(nt) > (size_t)c.stages * rows_stage_bytes(c.k_blocks_per_stage, rb, nt)))
+    return SGR_ERR_UNSUPPORTED;
+  *grid = ks * ((N + rb - 1) / rb);
   *smem = sm;
   return SGR_OK;
 }
@@ -966,11 +1067,22 @@ inline int rows_launch(const sgr_config& c, int sms, unsigned* err, const void* 
   lc.blockDim = dim3(rows_threads(mode), 1, 1);
   lc.dynamicSmemBytes = smem;
   lc.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  unsigned n_attr = 0;
+  if (pdl) {
+    attr[n_attr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n_attr].val.programmaticStreamSerializationAllowed = 1;
+    ++n_attr;
+  }
+  if (p.ksplit == 2) {  // the two CTAs of a slab form a cluster
+    attr[n_attr].id = cudaLaunchAttributeClusterDimension;
+    attr[n_attr].val.clusterDim.x = 2;
+    attr[n_attr].val.clusterDim.y = 1;
+    attr[n_attr].val.clusterDim.z = 1;
+    ++n_attr;
+  }
   lc.attrs = attr;
-  lc.numAttrs = pdl ? 1 : 0;
+  lc.numAttrs = n_attr;
   auto fn = mode == kRowsEpi16     ? rows_skinny_kernel<kRowsEpi16>
             : mode == kRowsEpi16G4 ? rows_skinny_kernel<kRowsEpi16G4>
             : mode == kRowsEpi64   ? rows_skinny_kernel<kRowsEpi64>
@@ -1006,6 +1118,7 @@ inline int rows_grouped_launch(const sgr_config& c, int sms, unsigned* err, cons
   size_t smem = 0;
   int rc = rows_plan(c, sms, m_max, N, K, &p, &grid, &smem);
   if (rc != SGR_OK) return rc;
+  if (p.ksplit != 1) return SGR_ERR_UNSUPPORTED;  // one CTA per slab and problem
   p.err = err;
   RowsGroupList list;
   std::memset(&list, 0, sizeof list);

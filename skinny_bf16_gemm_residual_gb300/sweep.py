@@ -131,6 +131,16 @@ def candidate_configs(path: int, M: int, K: int, grid: str) -> list[dict]:
                     for pf in sorted({st, max(1, st - 1), max(1, st - 2)}):
                         out.append(dict(path=path, ctas_per_sm=1, k_blocks_per_stage=kb, stages=st,
                                         prefetch_stages=pf, rows_per_stage=cfg_rb))
+        # 2-CTA K split (a slab per cluster, each CTA half of K): slabs of
+        # N / (SMs / 2) rows, 16-64-token tiles
+        if nt <= 64:
+            for kb in (4, 8):
+                for st in (2, 3, 4, 5, 6):
+                    if grid == "small" and st not in (2, 3, 4):
+                        continue
+                    for pf in sorted({st, max(1, st - 1), max(1, st - 2)}):
+                        out.append(dict(path=path, ctas_per_sm=1, k_blocks_per_stage=kb, stages=st,
+                                        prefetch_stages=pf, rows_per_stage=0, k_split=2))
     elif path == sgr.SGR_PATH_TILE:
         if M < 32:
             return []

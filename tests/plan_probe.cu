@@ -23,6 +23,7 @@ int main() {
     for (int M : Ms) {
       const int nt = (M + 15) / 16 * 16;
       // row-slab kernel
+      for (int ksp : {0, 2})
       for (int rb : {0, 8, 24, 32, 48, 64, 128})
         for (int kb : {1, 2, 4, 8})
           for (int st : {2, 3, 4, 6, 8}) {
@@ -33,6 +34,7 @@ int main() {
             c.k_blocks_per_stage = kb;
             c.stages = st;
             c.token_tile = nt;
+            c.k_split = ksp;
             sgr::RowsParams p;
             int grid = 0;
             size_t smem = 0;
@@ -41,10 +43,10 @@ int main() {
             std::printf("{\"kind\": \"rows\", \"M\": %d, \"N\": %d, \"K\": %d, \"RB\": %d, \"NT\": %d, \"G\": %d, "
                         "\"kbps\": %d, \"stages\": %d, \"prefetch\": %d, \"k_stages\": %d, \"tmem_cols\": %d, "
                         "\"issuers\": %d, \"mode\": %d, \"threads\": %d, \"grid\": %d, \"smem\": %zu, \"w_ring\": %zu, "
-                        "\"a_ring\": %zu, \"slack\": %u}\n",
+                        "\"a_ring\": %zu, \"slack\": %u, \"ksplit\": %d}\n",
                         M, N, K, p.RB, p.NT, p.groups, p.kbps, p.stages, p.prefetch, p.k_stages, p.tmem_cols,
                         p.issuers, sgr::rows_epi_mode(p.NT, p.groups), sgr::rows_threads(sgr::rows_epi_mode(p.NT, p.groups)),
-                        grid, smem, w_ring, a_ring, (unsigned)sgr::rows_tail_slack(p.stages, p.kbps, p.RB, p.NT));
+                        grid, smem, w_ring, a_ring, (unsigned)sgr::rows_tail_slack(p.stages, p.kbps, p.RB, p.NT), p.ksplit);
           }
       // FP8 row-slab kernel
       for (int rb : {0, 8, 24, 32, 64, 128})

@@ -34,7 +34,7 @@ def plans(tmp_path_factory):
 
 def test_row_slab_plans(plans):
     rows = [p for p in plans if p["kind"] == "rows"]
-    assert len(rows) > 100
+    assert len(rows) > 100 and sum(p["ksplit"] == 2 for p in rows) > 50
     for p in rows:
         assert p["smem"] <= SMEM_LIMIT, p
         assert p["RB"] % 8 == 0 and p["RB"] <= 128, p
@@ -62,13 +62,24 @@ def test_row_slab_plans(plans):
         assert p["smem"] == 2048 + p["w_ring"] + p["a_ring"] + p["slack"] + (512 if p["NT"] > 16 else 0), p
         if warm_epi:
             assert (p["NT"] + 4) * 4 <= 512, p
-        assert p["grid"] * p["RB"] >= p["N"] > (p["grid"] - 1) * p["RB"], p      # every row, no empty CTA
-        assert p["k_stages"] * p["kbps"] * 64 >= p["K"], p
+        ks = p["ksplit"]
+        slabs = p["grid"] // ks
+        assert p["grid"] % ks == 0, p                                            # whole clusters
+        assert slabs * p["RB"] >= p["N"] > (slabs - 1) * p["RB"], p             # every row, no empty slab
+        assert ks * p["k_stages"] * p["kbps"] * 64 >= p["K"], p                  # both ranks cover K
+        assert ks == 1 or (p["k_stages"] - 1) * p["kbps"] * 64 < p["K"], p      # rank 0 starts inside K
+        if ks == 2:
+            # the split's partial sums are completed in the 16-64-token
+            # register epilogues (at most two groups), with two hand-over rows
+            # per W row in the drained ring
+            assert warm_epi and p["G"] <= 2 and p["mode"] in (0, 1, 2), p
+            assert 2 * p["RB"] * (80 if p["NT"] == 16 else (p["NT"] + 4) * 4) <= p["w_ring"] + p["a_ring"], p
         assert 1 <= p["prefetch"] <= p["stages"], p
         # landing and slot-free barriers per stage, accumulator and drain
         # barriers, the TMEM address and the abort flag
-        # (below the warm-up pass's scratch at byte 960 of the region)
-        assert (2 * p["stages"] + 2) * 8 + 8 <= 960, p
+        # and the K split's hand-over barrier (below the warm-up pass's
+        # scratch at byte 960 of the region)
+        assert (2 * p["stages"] + 3) * 8 + 8 <= 960, p
         drained = p["w_ring"] + p["a_ring"]
         # hand-over buffers of the epilogues live in the drained rings
         if p["NT"] == 16 and p["G"] <= 2:
