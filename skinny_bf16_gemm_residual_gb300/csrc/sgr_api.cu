@@ -1251,10 +1251,7 @@ int sgr_kernel_resources(int device, int path, int M, int N, int K, int* regs, i
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
     if (sgr::rows_plan(c, sms, M, N, K, &rp, &grid, &smem) != SGR_OK) return SGR_ERR_UNSUPPORTED;
     const int mode = sgr::rows_epi_mode(rp.NT, rp.groups);
-    const void* fn = mode == sgr::kRowsEpi16     ? reinterpret_cast<const void*>(sgr::rows_skinny_kernel<sgr::kRowsEpi16>)
-                     : mode == sgr::kRowsEpi16G4 ? reinterpret_cast<const void*>(sgr::rows_skinny_kernel<sgr::kRowsEpi16G4>)
-                     : mode == sgr::kRowsEpi64   ? reinterpret_cast<const void*>(sgr::rows_skinny_kernel<sgr::kRowsEpi64>)
-                                                 : reinterpret_cast<const void*>(sgr::rows_skinny_kernel<sgr::kRowsEpiWide>);
+    const void* fn = sgr::rows_kernel_fn(mode, rp.ksplit == 2);
     if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) {
       cudaGetLastError();
       return SGR_ERR_DEVICE;

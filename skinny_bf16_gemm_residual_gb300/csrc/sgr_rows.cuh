@@ -216,10 +216,10 @@ __device__ __forceinline__ bool rows_pair_exchange(float (&v)[T], bool has, bool
 // epilogue it first runs a warm-up pass over its instructions while the MMAs
 // run (tensor-memory columns after the accumulator, which no MMA writes, the
 // exchange in `scratch`, stores predicated off; kWarm false skips it).
-// Under the 2-CTA K split the partial sums are completed by
+// Under the 2-CTA K split (kSplit) the partial sums are completed by
 // rows_pair_exchange before the residual add.  Called by the
 // four epilogue warps (q: TMEM lane quarter of the warp).
-template <int T, bool kWarm>
+template <int T, bool kWarm, bool kSplit>
 __device__ __forceinline__ void rows_epilogue_wide(const RowsParams& p, const RowsIO& io, int n0, uint32_t tmem,
                                                    uint32_t w_ring, uint32_t scratch, uint64_t* acc_full,
                                                    uint64_t* ready, volatile int* abort_flag, int q, int lane) {
@@ -229,8 +229,9 @@ __device__ __forceinline__ void rows_epilogue_wide(const RowsParams& p, const Ro
   const bool owner = L < p.RB && n0 + L < p.N;
   // Under the K split this rank stores column n0 + L only if fin (the rank is
   // read again where needed rather than held through the epilogue).
-  const bool split = p.ksplit == 2;
-  const bool fin = !split || ((L < p.RB / 2) == (cluster_ctarank() == 0u));
+  constexpr bool split = kSplit;
+  bool fin = true;
+  if constexpr (kSplit) fin = (L < p.RB / 2) == (cluster_ctarank() == 0u);
   const bool helper = G == 2 && L >= p.RB && L < 2 * p.RB;
   const int r = owner ? L : L - p.RB;
   const uint32_t stride = rows_xch_stride(T);  // T floats + pad per row
@@ -306,8 +307,9 @@ __device__ __forceinline__ void rows_epilogue_wide(const RowsParams& p, const Ro
         v[i + 3] += a3;
       }
     }
-    if (split && real)
-      ok = rows_pair_exchange<T>(v, ok && owner, fin, xch + (uint32_t)p.RB * stride, ready, cluster_ctarank(),
+    if constexpr (split)
+      if (real)
+        ok = rows_pair_exchange<T>(v, ok && owner, fin, xch + (uint32_t)p.RB * stride, ready, cluster_ctarank(),
                                  abort_flag, p.err) &&
            ok;
     if (ok && owner && fin) {
@@ -325,8 +327,10 @@ __device__ __forceinline__ void rows_epilogue_wide(const RowsParams& p, const Ro
 // the epilogue family kMode (the 64-token register epilogue needs more
 // registers per thread: only its own instance has it, so that the others
 // keep two CTAs per SM where their shared memory allows); kWideWarm: the
-// 17-64-token register epilogues run their warm-up pass.
-template <int kMode, bool kWideWarm>
+// 17-64-token register epilogues run their warm-up pass; kSplit: the 2-CTA
+// K split (p.ksplit == 2), in instances of its own so that the others carry
+// none of its code.
+template <int kMode, bool kWideWarm, bool kSplit>
 __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, int n0) {
   const int issuers = rows_two_issuer_mode(kMode) ? p.issuers : 1;
   extern __shared__ unsigned char smem_raw[];
@@ -341,7 +345,7 @@ __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, 
   uint64_t* ready = drain + 1;                        // [1] the K-split peer's partial sums
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ready + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  const bool split = p.ksplit == 2;
+  constexpr bool split = kSplit;  // p.ksplit == 2 (its own kernel instances)
   const uint32_t rank = split ? cluster_ctarank() : 0u;
   const uint32_t wblk = (uint32_t)p.RB * 128u;   // bytes of one W box (RB rows x 128 B)
   const uint32_t ablk = (uint32_t)p.NT * 128u;   // bytes of one A box
@@ -365,7 +369,7 @@ __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, 
     }
     mbar_init(smem_u32(acc_full), (uint32_t)issuers);
     mbar_init(smem_u32(drain), (uint32_t)issuers);
-    mbar_init(smem_u32(ready), 128u);  // the peer's four epilogue warps
+    if (split) mbar_init(smem_u32(ready), 128u);  // the peer's four epilogue warps
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -606,8 +610,9 @@ __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, 
             v[i + 3] += a3;
           }
         }
-        if (split && real)
-          ok = rows_pair_exchange<16>(v, ok && owner, fin, xch + (uint32_t)p.RB * 80u, ready, rank, abort_flag,
+        if constexpr (split)
+          if (real)
+            ok = rows_pair_exchange<16>(v, ok && owner, fin, xch + (uint32_t)p.RB * 80u, ready, rank, abort_flag,
                                       p.err) &&
                ok;
         if (ok && owner && fin) {
@@ -620,13 +625,13 @@ __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, 
         }
       }
     } else if (kMode == kRowsEpiWide && p.NT == 32 && p.groups <= 2 && p.groups * p.RB <= kTcTileRows) {
-      rows_epilogue_wide<32, kWideWarm>(p, io, n0, tmem, w_ring, wide_scratch, acc_full, ready, abort_flag, q,
+      rows_epilogue_wide<32, kWideWarm, kSplit>(p, io, n0, tmem, w_ring, wide_scratch, acc_full, ready, abort_flag, q,
                                           lane);
     } else if (kMode == kRowsEpiWide && p.NT == 48 && p.groups <= 2 && p.groups * p.RB <= kTcTileRows) {
-      rows_epilogue_wide<48, kWideWarm>(p, io, n0, tmem, w_ring, wide_scratch, acc_full, ready, abort_flag, q,
+      rows_epilogue_wide<48, kWideWarm, kSplit>(p, io, n0, tmem, w_ring, wide_scratch, acc_full, ready, abort_flag, q,
                                           lane);
     } else if (kMode == kRowsEpi64 && p.NT == 64 && p.groups <= 2 && p.groups * p.RB <= kTcTileRows) {
-      rows_epilogue_wide<64, kWideWarm>(p, io, n0, tmem, w_ring, wide_scratch, acc_full, ready, abort_flag, q,
+      rows_epilogue_wide<64, kWideWarm, kSplit>(p, io, n0, tmem, w_ring, wide_scratch, acc_full, ready, abort_flag, q,
                                           lane);
     } else if (kMode == kRowsEpi16G4 && p.NT == kRowsPrefetchTokens && p.groups == 4 && p.RB == 32) {
       // 32-row slabs, four packed groups: warp quarter q holds group q whole.
@@ -895,12 +900,25 @@ __device__ __forceinline__ void rows_run(const RowsParams& p, const RowsIO& io, 
 // Two CTAs per SM where their shared memory allows (the register budget is
 // sized for it; the default configuration of untabulated shapes relies on
 // it), except for the 64-token instance.
-template <int kMode>
+template <int kMode, bool kSplit>
 __global__ void __launch_bounds__(rows_threads(kMode), kMode == kRowsEpi64 ? 1 : 2)
     rows_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA,
                        const RowsParams p) {
   const RowsIO io{&tmW, &tmA, p.R, p.Y, p.ldr, p.ldy, p.M};
-  rows_run<kMode, true>(p, io, (int)(blockIdx.x / (unsigned)p.ksplit) * p.RB);  // a K-split pair shares its slab
+  rows_run<kMode, true, kSplit>(p, io, (int)(blockIdx.x / (kSplit ? 2u : 1u)) * p.RB);  // a K-split pair shares its slab
+}
+
+// The instance for an epilogue family and K split (the 16-token form with
+// three or four groups has no K-split instance).
+inline const void* rows_kernel_fn(int mode, bool split) {
+  if (split)
+    return mode == kRowsEpi16   ? reinterpret_cast<const void*>(rows_skinny_kernel<kRowsEpi16, true>)
+           : mode == kRowsEpi64 ? reinterpret_cast<const void*>(rows_skinny_kernel<kRowsEpi64, true>)
+                                : reinterpret_cast<const void*>(rows_skinny_kernel<kRowsEpiWide, true>);
+  return mode == kRowsEpi16     ? reinterpret_cast<const void*>(rows_skinny_kernel<kRowsEpi16, false>)
+         : mode == kRowsEpi16G4 ? reinterpret_cast<const void*>(rows_skinny_kernel<kRowsEpi16G4, false>)
+         : mode == kRowsEpi64   ? reinterpret_cast<const void*>(rows_skinny_kernel<kRowsEpi64, false>)
+                                : reinterpret_cast<const void*>(rows_skinny_kernel<kRowsEpiWide, false>);
 }
 
 // Grouped launch: several independent problems with the same N and K and
@@ -933,7 +951,7 @@ __global__ void __launch_bounds__(rows_threads(kMode), 2)
   const int slab = (int)blockIdx.x / list.count;
   const RowsGroup& g = list.g[e];
   const RowsIO io{&g.tmW, &g.tmA, g.R, g.Y, g.ldr, g.ldy, g.M};
-  rows_run<kMode, false>(p, io, slab * p.RB);
+  rows_run<kMode, false, false>(p, io, slab * p.RB);
 }
 
 // ------------------------------------------------------------------ host side
@@ -1035,10 +1053,10 @@ inline int rows_plan(const sgr_config& c, int sms, int M, int N, int K, RowsPara
 }
 
 inline cudaError_t rows_init_device() {
-  cudaError_t e = set_kernel_smem_attrs(reinterpret_cast<const void*>(rows_skinny_kernel<kRowsEpi16>));
-  if (e == cudaSuccess) e = set_kernel_smem_attrs(reinterpret_cast<const void*>(rows_skinny_kernel<kRowsEpi16G4>));
-  if (e == cudaSuccess) e = set_kernel_smem_attrs(reinterpret_cast<const void*>(rows_skinny_kernel<kRowsEpiWide>));
-  if (e == cudaSuccess) e = set_kernel_smem_attrs(reinterpret_cast<const void*>(rows_skinny_kernel<kRowsEpi64>));
+  cudaError_t e = cudaSuccess;
+  for (int split = 0; split < 2; ++split)
+    for (int mode : {kRowsEpi16, kRowsEpi16G4, kRowsEpiWide, kRowsEpi64})
+      if (e == cudaSuccess) e = set_kernel_smem_attrs(rows_kernel_fn(mode, split != 0));
   if (e == cudaSuccess) e = set_kernel_smem_attrs(reinterpret_cast<const void*>(rows_grouped_kernel<kRowsEpi16>));
   if (e == cudaSuccess) e = set_kernel_smem_attrs(reinterpret_cast<const void*>(rows_grouped_kernel<kRowsEpi16G4>));
   if (e == cudaSuccess) e = set_kernel_smem_attrs(reinterpret_cast<const void*>(rows_grouped_kernel<kRowsEpiWide>));
@@ -1083,10 +1101,13 @@ inline int rows_launch(const sgr_config& c, int sms, unsigned* err, const void* 
   }
   lc.attrs = attr;
   lc.numAttrs = n_attr;
-  auto fn = mode == kRowsEpi16     ? rows_skinny_kernel<kRowsEpi16>
-            : mode == kRowsEpi16G4 ? rows_skinny_kernel<kRowsEpi16G4>
-            : mode == kRowsEpi64   ? rows_skinny_kernel<kRowsEpi64>
-                                   : rows_skinny_kernel<kRowsEpiWide>;
+  auto fn = p.ksplit == 2 ? (mode == kRowsEpi16   ? rows_skinny_kernel<kRowsEpi16, true>
+                             : mode == kRowsEpi64 ? rows_skinny_kernel<kRowsEpi64, true>
+                                                  : rows_skinny_kernel<kRowsEpiWide, true>)
+                          : (mode == kRowsEpi16     ? rows_skinny_kernel<kRowsEpi16, false>
+                             : mode == kRowsEpi16G4 ? rows_skinny_kernel<kRowsEpi16G4, false>
+                             : mode == kRowsEpi64   ? rows_skinny_kernel<kRowsEpi64, false>
+                                                    : rows_skinny_kernel<kRowsEpiWide, false>);
   if (cudaLaunchKernelEx(&lc, fn, tmW, tmA, p) != cudaSuccess) {
     cudaGetLastError();
     return SGR_ERR_LAUNCH;
