@@ -67,6 +67,31 @@ def test_fuzz_bf16(seed):
     compare(bits(Y), oracle_full(p.A, p.W, p.R), f"fuzz bf16 seed={seed} M={M} N={N} K={K} path={path}")
 
 
+@pytest.mark.parametrize("seed", range(24))
+def test_fuzz_rows_ksplit(seed):
+    """The row slab with the 2-CTA K split on seeded random shapes (1-64
+    tokens, K up to 8 192), ring shapes, row strides and in-place outputs."""
+    rng = np.random.default_rng(5000 + seed)
+    M = int(rng.integers(1, 65))
+    N = int(rng.integers(1, 600)) * 8
+    K = int(rng.integers(1, 1025)) * 8
+    kb = int(rng.choice([1, 2, 4, 8]))
+    st = int(rng.integers(2, 7))
+    p = inputs.make_problem(M, N, K, seed=6000 + seed)
+    A = padded(p.A, int(rng.integers(0, 4)) * 8)
+    R = padded(p.R, int(rng.integers(0, 4)) * 8)
+    in_place = bool(rng.integers(0, 2))
+    Y = R if in_place else padded(torch.zeros_like(p.R), int(rng.integers(0, 4)) * 8)
+    cfg = sgr.make_config(path=sgr.SGR_PATH_TC_ROWS, k_split=2, k_blocks_per_stage=kb, stages=st)
+    try:
+        sgr.skinny_gemm_residual_ex(A, p.W.cuda(), R, Y, config=cfg)
+    except sgr.SgrError as e:  # a ring too large for shared memory, or too small for the hand-over
+        assert e.status == sgr.SGR_ERR_UNSUPPORTED, (M, N, K, kb, st, e)
+        return
+    torch.cuda.synchronize()
+    compare(bits(Y), oracle_full(p.A, p.W, p.R), f"fuzz k-split seed={seed} M={M} N={N} K={K} kb={kb} st={st}")
+
+
 @pytest.mark.parametrize("seed", range(32))
 def test_fuzz_w8(seed):
     rng, M, N, K = case(500 + seed)
