@@ -61,12 +61,13 @@ def test_parity_full_size_every_element(M, seed):
     assert m["cosine"] > 0.999
 
 
-# The down-projection of the same block (K = 7168 -> N = 3584): the row slab
-# holds 24 weight rows per CTA there, so four K blocks share one MMA.
+# The down-projection of the same block (K = 7168 -> N = 3584): through the
+# library's choice, the row slab with the 2-CTA K split (48-row slabs, one CTA
+# per half of K) up to 64 tokens, each table entry and the M between them.
 N_DOWN, K_DOWN = 3584, 7168
 
 
-@pytest.mark.parametrize("M", [1, 2, 4, 8, 16, 32, 64, 128])
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 8, 16, 24, 32, 40, 48, 64, 100, 128])
 def test_parity_down_projection_every_element(M):
     p = inputs.make_problem(M, N_DOWN, K_DOWN, seed=500 + M)
     m = compare(run_gpu(p), oracle_full(p.A, p.W, p.R), f"down M={M}")
