@@ -618,6 +618,8 @@ def run_ours(args):
     grouped = None if (args.skip_grouped or rank != 0) else run_grouped(sgr, device, stream)
     w8 = None if (args.skip_w8 or rank != 0) else run_w8(sgr, device, stream, peaks)
     w4 = None if (args.skip_w4 or rank != 0) else run_w4(sgr, device, stream, peaks)
+    down = None if (args.skip_down or rank != 0 or (N_DIM, K_DIM) != (7168, 3584)) else run_down(
+        sgr, device, stream, peaks)
 
     if rank != 0:
         return 0
@@ -679,6 +681,7 @@ def run_ours(args):
         "grouped": grouped,
         "w8": w8,
         "w4": w4,
+        "down_projection": down,
         "gpu_launches": repeats * args.steps * launches_per_step,
         "clocks": clk,
         "peaks": {"hbm_gbs": peaks["hbm_gbs"], "bf16_tflops": peaks["bf16_tflops"],
@@ -799,6 +802,37 @@ def run_w8(sgr, device, stream, peaks: dict, m_list=(1, 2, 4, 16), copies: int =
             "note": "FP8 E4M3 weights + FP32 per-column scale, BF16 A/R/Y; graph of 8 calls over distinct weight "
                     "copies; the library's own kernel choice (FP8 tensor-core kernel with split activations for "
                     "M <= 8, the widening row-slab kernel above)"}
+
+
+def run_down(sgr, device, stream, peaks: dict, m_list=(1, 4, 16, 32, 64), replays: int = 50, repeats: int = 9):
+    """The block's other projection, K = 7168 -> N = 3584 (the down-projection),
+    when the headline runs the up-projection: per M, the library's own choice
+    (the row slab with the 2-CTA K split up to 64 tokens) and cuBLAS `addmm`,
+    each as one CUDA graph of COPIES calls over distinct weight copies (4 x
+    51 MB, more than L2), PDL on."""
+    import torch
+
+    from skinny_bf16_gemm_residual_gb300 import inputs
+
+    N, K = K_DIM, N_DIM
+    Ws = [inputs.make_weights(N, K, seed=11_000 + c).to(device) for c in range(COPIES)]
+    rows = []
+    for M in m_list:
+        A = inputs.make_rows(M, K, seed=12_000 + M).to(device)
+        Rs = [inputs.make_rows(M, N, seed=13_000 + 100 * M + c).to(device) for c in range(COPIES)]
+        Ys = [torch.empty((M, N), dtype=torch.bfloat16, device=device) for _ in range(COPIES)]
+        ours = time_calls([lambda c=c: sgr.skinny_gemm_residual(A, Ws[c], Rs[c], Ys[c], stream=stream)
+                           for c in range(COPIES)], stream, replays, repeats)
+        ref = time_calls(addmm_calls(A, Ws, Rs, Ys, stream), stream, replays, repeats)
+        gbs = alg_bytes(M, N, K) / (ours["median_us"] * 1e-6) / 1e9
+        rows.append({"m": M, "path": PATH_NAMES.get(sgr.sgr_select_path(M, N, K), "?"),
+                     "us": ours["median_us"], "p10_us": ours["p10_us"], "p90_us": ours["p90_us"],
+                     "gbs": gbs, "frac_of_hbm_peak": gbs / peaks["hbm_gbs"],
+                     "cublas_addmm_us": ref["median_us"]})
+    del Ws
+    return {"n": N, "k": K, "per_m": rows,
+            "note": "down-projection of the same block; graph of 4 calls over distinct weight copies; "
+                    "the library's choice and cuBLAS addmm under the same protocol"}
 
 
 def run_w4(sgr, device, stream, peaks: dict, m_list=(1, 2, 4, 16), copies: int = 8, replays: int = 50,
@@ -946,6 +980,7 @@ def main(argv=None):
     ap.add_argument("--skip-grouped", action="store_true", help="skip the mixture-of-experts grouped leg")
     ap.add_argument("--skip-w8", action="store_true", help="skip the FP8-weight leg")
     ap.add_argument("--skip-w4", action="store_true", help="skip the NVFP4-weight leg")
+    ap.add_argument("--skip-down", action="store_true", help="skip the down-projection (N 3584, K 7168) leg")
     ap.add_argument("--skip-sweeps", action="store_true",
                     help="skip the transition (M = 32-128) and compute-bound (M = 256-1024) legs")
     ap.add_argument("--skip-cublas", action="store_true", help="skip the cuBLAS addmm rows of the per-M leg")
