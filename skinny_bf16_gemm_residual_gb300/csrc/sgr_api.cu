@@ -362,7 +362,7 @@ int resolve_config(int dev_sms, int M, int N, int K, const sgr_config* in, sgr_c
       if (path == SGR_PATH_TC_ROWS || tiled) out->prefetch_stages = e->prefetch_stages;
       if (tiled && e->tile_n) out->tile_n = e->tile_n;
       if (path == SGR_PATH_TILE) out->k_split = e->k_split > 0 ? e->k_split : 1;
-      if (path == SGR_PATH_TC_ROWS && e->k_split == 2) out->k_split = 2;
+      if (path == SGR_PATH_TC_ROWS) out->k_split = e->k_split == 2 ? 2 : 0;  // as measured
     }
   }
   if (in) {
@@ -1136,6 +1136,8 @@ int run_grouped(const sgr_group* groups, int num_groups, int N, int K, const sgr
   in.path = SGR_PATH_TC_ROWS;
   sgr_config c;
   if ((rc = resolve_config(st.sms, m_max, N, K, &in, &c)) != SGR_OK) return rc;
+  // One CTA per slab and problem: no K split unless asked for (then refused).
+  if (in.k_split == 0) c.k_split = 0;
   // Active groups in launches of up to 32.
   sgr::RowsGroupArgs batch[sgr::kRowsMaxGroups];
   int n = 0;

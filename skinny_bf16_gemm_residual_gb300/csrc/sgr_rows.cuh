@@ -965,26 +965,41 @@ inline bool rows_supported(int sms, int M, int N, int K) {
          rows_per_cta(sms, N) <= kTcTileRows;
 }
 
+inline int rows_plan(const sgr_config& c, int sms, int M, int N, int K, RowsParams* p, int* grid, size_t* smem);
+
 // Default: 4 K blocks per stage and the deepest ring (up to 4 stages) that
 // keeps the CTA at or under ~110 KB of shared memory, so that the next call's
 // CTA can be resident on the same SM; smaller stages if even 2 do not fit.
+// Slabs of at most 32 rows over a long K (K >= 4096) take the 2-CTA K split
+// with the same ring: measured on GB300 at 1-64 tokens, N x K = 1024 x 4096,
+// 2048 x 8192, 2560 x 10240, 4096 x 14336 ran in 0.54-0.76 of the unsplit
+// time; 48-row slabs (7168 x 2048) ran slower split.
 inline void rows_default_config(int sms, int M, int N, int K, sgr_config* c) {
-  (void)K;
   c->path = SGR_PATH_TC_ROWS;
   c->ctas_per_sm = 1;
   c->token_tile = (M + 15) / 16 * 16;
   c->rows_per_stage = 0;
+  c->k_split = 0;
   const int rb = rows_per_cta(sms, N);
   const size_t budget = 110u * 1024u;
-  for (int kb = 4; kb >= 1; kb /= 2)
-    for (int st = 4; st >= 2; --st)
+  c->k_blocks_per_stage = 1;
+  c->stages = 2;
+  bool found = false;
+  for (int kb = 4; kb >= 1 && !found; kb /= 2)
+    for (int st = 4; st >= 2 && !found; --st)
       if (rows_smem_bytes(st, kb, rb, c->token_tile) <= budget) {
         c->k_blocks_per_stage = kb;
         c->stages = st;
-        return;
+        found = true;
       }
-  c->k_blocks_per_stage = 1;
-  c->stages = 2;
+  if (rb <= 32 && K >= 4096 && c->token_tile <= 64) {
+    sgr_config s = *c;
+    s.k_split = 2;
+    RowsParams p;
+    int grid = 0;
+    size_t smem = 0;
+    if (rows_plan(s, sms, M, N, K, &p, &grid, &smem) == SGR_OK) c->k_split = 2;
+  }
 }
 
 inline int rows_plan(const sgr_config& c, int sms, int M, int N, int K, RowsParams* p, int* grid,

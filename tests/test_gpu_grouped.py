@@ -46,7 +46,7 @@ def test_grouped_full_size(counts):
     check(counts, N_FULL, K_FULL, seed=sum(counts))
 
 
-@pytest.mark.parametrize("N,K", [(1000, 264), (304, 8), (3584, 7168), (2056, 1800)])
+@pytest.mark.parametrize("N,K", [(1000, 264), (304, 8), (3584, 7168), (2056, 1800), (2048, 8192)])
 def test_grouped_small_and_other_shapes(N, K):
     check([3, 0, 16, 1, 7], N, K, seed=N + K)
 

@@ -171,3 +171,29 @@ def test_split_rejects_unsupported_forms():
         sgr.skinny_gemm_residual_grouped([(q.A.cuda(), q.W.cuda(), q.R.cuda(), None)],
                                          config=sgr.make_config(path=ROWS, k_split=2, token_tile=16))
     assert e.value.status == sgr.SGR_ERR_UNSUPPORTED
+
+
+# Untabulated shapes whose default configuration takes the split (slabs of at
+# most 32 rows over K >= 4096), through the library's own choice.
+AUTO_SPLIT = [(1, 2048, 8192), (16, 2048, 8192), (40, 2560, 10240), (64, 1024, 4096), (7, 4096, 14336),
+              (33, 1000, 4104)]
+
+
+@pytest.mark.parametrize("M,N,K", AUTO_SPLIT)
+def test_split_default_configuration_every_element(M, N, K):
+    c = sgr.sgr_default_config(M, N, K)
+    assert (c.path, c.k_split) == (ROWS, 2), (c.path, c.k_split)
+    p = inputs.make_problem(M, N, K, seed=800 + M + N)
+    Y = sgr.skinny_gemm_residual(p.A.cuda(), p.W.cuda(), p.R.cuda())
+    torch.cuda.synchronize()
+    compare(bits(Y), oracle_full(p.A, p.W, p.R), f"split default {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K,split", [(16, 7168, 3584, 0), (16, 3584, 7168, 2), (64, 3584, 7168, 2),
+                                         (16, 7168, 2048, 0), (16, 2048, 2048, 0)])
+def test_split_default_choice(M, N, K, split):
+    """The measured table (up- and down-projection) and the default rule for
+    other shapes: 48-row slabs and short K stay unsplit."""
+    c = sgr.sgr_default_config(M, N, K)
+    assert (c.k_split == 2) == (split == 2), (M, N, K, c.path, c.k_split)
+
