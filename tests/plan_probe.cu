@@ -145,5 +145,23 @@ int main() {
           }
     }
   }
+  // Default row-slab configurations (the K-split rule among them).
+  const int dNKs[][2] = {{7168, 3584}, {3584, 7168}, {2048, 8192}, {1024, 4096}, {7168, 2048}, {2048, 2048},
+                         {4096, 14336}, {4864, 4096}, {4872, 4096}, {8, 65536}, {2560, 10240}};
+  for (auto& nk : dNKs)
+    for (int M : {1, 16, 17, 40, 64, 65, 128}) {
+      const int N = nk[0], K = nk[1];
+      if (!sgr::rows_supported(sms, M, N, K)) continue;
+      sgr_config c = {};
+      sgr::rows_default_config(sms, M, N, K, &c);
+      sgr::RowsParams p;
+      int grid = 0;
+      size_t smem = 0;
+      const int rc = sgr::rows_plan(c, sms, M, N, K, &p, &grid, &smem);
+      std::printf("{\"kind\": \"rows_default\", \"M\": %d, \"N\": %d, \"K\": %d, \"k_split\": %d, \"kbps\": %d, "
+                  "\"stages\": %d, \"token_tile\": %d, \"plan_ok\": %d, \"RB\": %d}\n",
+                  M, N, K, c.k_split, c.k_blocks_per_stage, c.stages, c.token_tile, rc == SGR_OK ? 1 : 0,
+                  rc == SGR_OK ? p.RB : 0);
+    }
   return 0;
 }

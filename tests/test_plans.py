@@ -191,3 +191,21 @@ def test_large_ends_are_planned_or_refused(plans):
     assert kinds(N=131072) == {"tile", "pair"}
     assert kinds(M=1024) == {"tile", "pair"}
     assert {"rows", "w8", "tile"} <= kinds(K=65536, M=256)
+
+
+def test_row_slab_default_configurations(plans):
+    """The default configuration of shapes without a table entry: a plan the
+    kernel accepts, and the 2-CTA K split exactly for slabs of at most 32 rows
+    over K >= 4096 at up to 64 tokens (where the split plan fits)."""
+    rows = [p for p in plans if p["kind"] == "rows_default"]
+    assert len(rows) > 40
+    for p in rows:
+        assert p["plan_ok"] == 1, p
+        rb = -(-p["N"] // 152)
+        rb = -(-rb // 8) * 8
+        want = rb <= 32 and p["K"] >= 4096 and p["token_tile"] <= 64
+        assert (p["k_split"] == 2) == want, p
+        if want:  # the split's slab: N / 76 rows rounded up to 8
+            assert p["RB"] == -(-(-(-p["N"] // 76)) // 8) * 8, p
+    assert any(p["k_split"] == 2 for p in rows) and any(p["k_split"] == 0 for p in rows)
+
