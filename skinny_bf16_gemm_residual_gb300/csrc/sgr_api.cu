@@ -1136,8 +1136,8 @@ int run_grouped(const sgr_group* groups, int num_groups, int N, int K, const sgr
   in.path = SGR_PATH_TC_ROWS;
   sgr_config c;
   if ((rc = resolve_config(st.sms, m_max, N, K, &in, &c)) != SGR_OK) return rc;
-  // One CTA per slab and problem: no K split unless asked for (then refused).
-  if (in.k_split == 0) c.k_split = 0;
+  // The default's K split where the grouped kernel has it (16-48-token tiles).
+  if (in.k_split == 0 && c.token_tile > 48) c.k_split = 0;
   // Active groups in launches of up to 32.
   sgr::RowsGroupArgs batch[sgr::kRowsMaxGroups];
   int n = 0;

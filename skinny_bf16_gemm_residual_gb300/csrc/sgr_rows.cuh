@@ -943,15 +943,17 @@ struct RowsGroupList {
 
 // kMode: the 16-token families for 16-token tiles, else kRowsEpiWide (whose
 // 32/48-token epilogue here runs without its warm-up pass, which would cost
-// this kernel register spills).
-template <int kMode>
+// this kernel register spills).  kSplit: the 2-CTA K split, the two CTAs of a
+// cluster on the same slab of the same problem (16-48-token tiles).
+template <int kMode, bool kSplit>
 __global__ void __launch_bounds__(rows_threads(kMode), 2)
     rows_grouped_kernel(const __grid_constant__ RowsGroupList list, const RowsParams p) {
-  const int e = (int)blockIdx.x % list.count;
-  const int slab = (int)blockIdx.x / list.count;
+  const int unit = (int)blockIdx.x / (kSplit ? 2 : 1);
+  const int e = unit % list.count;
+  const int slab = unit / list.count;
   const RowsGroup& g = list.g[e];
   const RowsIO io{&g.tmW, &g.tmA, g.R, g.Y, g.ldr, g.ldy, g.M};
-  rows_run<kMode, false, false>(p, io, slab * p.RB);
+  rows_run<kMode, false, kSplit>(p, io, slab * p.RB);
 }
 
 // ------------------------------------------------------------------ host side
@@ -1072,9 +1074,11 @@ inline cudaError_t rows_init_device() {
   for (int split = 0; split < 2; ++split)
     for (int mode : {kRowsEpi16, kRowsEpi16G4, kRowsEpiWide, kRowsEpi64})
       if (e == cudaSuccess) e = set_kernel_smem_attrs(rows_kernel_fn(mode, split != 0));
-  if (e == cudaSuccess) e = set_kernel_smem_attrs(reinterpret_cast<const void*>(rows_grouped_kernel<kRowsEpi16>));
-  if (e == cudaSuccess) e = set_kernel_smem_attrs(reinterpret_cast<const void*>(rows_grouped_kernel<kRowsEpi16G4>));
-  if (e == cudaSuccess) e = set_kernel_smem_attrs(reinterpret_cast<const void*>(rows_grouped_kernel<kRowsEpiWide>));
+  if (e == cudaSuccess) e = set_kernel_smem_attrs(reinterpret_cast<const void*>(rows_grouped_kernel<kRowsEpi16, false>));
+  if (e == cudaSuccess) e = set_kernel_smem_attrs(reinterpret_cast<const void*>(rows_grouped_kernel<kRowsEpi16G4, false>));
+  if (e == cudaSuccess) e = set_kernel_smem_attrs(reinterpret_cast<const void*>(rows_grouped_kernel<kRowsEpiWide, false>));
+  if (e == cudaSuccess) e = set_kernel_smem_attrs(reinterpret_cast<const void*>(rows_grouped_kernel<kRowsEpi16, true>));
+  if (e == cudaSuccess) e = set_kernel_smem_attrs(reinterpret_cast<const void*>(rows_grouped_kernel<kRowsEpiWide, true>));
   return e;
 }
 
@@ -1154,7 +1158,9 @@ inline int rows_grouped_launch(const sgr_config& c, int sms, unsigned* err, cons
   size_t smem = 0;
   int rc = rows_plan(c, sms, m_max, N, K, &p, &grid, &smem);
   if (rc != SGR_OK) return rc;
-  if (p.ksplit != 1) return SGR_ERR_UNSUPPORTED;  // one CTA per slab and problem
+  // Under the K split only the 16-48-token epilogues (the 64-token tile runs
+  // the general epilogue here, which does not complete split sums).
+  if (p.ksplit == 2 && p.NT > 48) return SGR_ERR_UNSUPPORTED;
   p.err = err;
   RowsGroupList list;
   std::memset(&list, 0, sizeof list);
@@ -1175,14 +1181,27 @@ inline int rows_grouped_launch(const sgr_config& c, int sms, unsigned* err, cons
   lc.blockDim = dim3(rows_threads(mode), 1, 1);
   lc.dynamicSmemBytes = smem;
   lc.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  unsigned n_attr = 0;
+  if (pdl) {
+    attr[n_attr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n_attr].val.programmaticStreamSerializationAllowed = 1;
+    ++n_attr;
+  }
+  if (p.ksplit == 2) {  // the two CTAs of a slab form a cluster
+    attr[n_attr].id = cudaLaunchAttributeClusterDimension;
+    attr[n_attr].val.clusterDim.x = 2;
+    attr[n_attr].val.clusterDim.y = 1;
+    attr[n_attr].val.clusterDim.z = 1;
+    ++n_attr;
+  }
   lc.attrs = attr;
-  lc.numAttrs = pdl ? 1 : 0;
-  auto fn = mode == kRowsEpi16     ? rows_grouped_kernel<kRowsEpi16>
-            : mode == kRowsEpi16G4 ? rows_grouped_kernel<kRowsEpi16G4>
-                                   : rows_grouped_kernel<kRowsEpiWide>;
+  lc.numAttrs = n_attr;
+  auto fn = p.ksplit == 2 ? (mode == kRowsEpi16 ? rows_grouped_kernel<kRowsEpi16, true>
+                                                : rows_grouped_kernel<kRowsEpiWide, true>)
+                          : (mode == kRowsEpi16     ? rows_grouped_kernel<kRowsEpi16, false>
+                             : mode == kRowsEpi16G4 ? rows_grouped_kernel<kRowsEpi16G4, false>
+                                                    : rows_grouped_kernel<kRowsEpiWide, false>);
   if (cudaLaunchKernelEx(&lc, fn, list, p) != cudaSuccess) {
     cudaGetLastError();
     return SGR_ERR_LAUNCH;

@@ -167,10 +167,29 @@ def test_split_rejects_unsupported_forms():
             sgr.skinny_gemm_residual_ex(A, W, R, config=sgr.make_config(path=ROWS, **cfg))
         assert e.value.status == sgr.SGR_ERR_UNSUPPORTED, cfg
     q = inputs.make_problem(4, 2048, 1024, seed=2)
-    with pytest.raises(sgr.SgrError) as e:
+    with pytest.raises(sgr.SgrError) as e:  # the grouped kernel's 64-token tile has no split form
         sgr.skinny_gemm_residual_grouped([(q.A.cuda(), q.W.cuda(), q.R.cuda(), None)],
-                                         config=sgr.make_config(path=ROWS, k_split=2, token_tile=16))
+                                         config=sgr.make_config(path=ROWS, k_split=2, token_tile=64))
     assert e.value.status == sgr.SGR_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("nt,kb,st,counts", [(16, 8, 3, [1, 5, 0, 16]), (48, 4, 4, [33, 2, 48])])
+def test_split_grouped_matches_oracle_and_separate_calls(nt, kb, st, counts):
+    """The grouped launch with the K split (a cluster per slab and problem):
+    every element against the oracle, and the same bits as separate calls
+    with the same configuration."""
+    probs = [inputs.make_problem(m, N_DOWN, K_DOWN, seed=900 + 13 * i + m) for i, m in enumerate(counts)]
+    dev = [(p.A.cuda(), p.W.cuda(), p.R.cuda(), None) for p in probs]
+    cfg = sgr.make_config(path=ROWS, k_split=2, token_tile=nt, k_blocks_per_stage=kb, stages=st)
+    ys = sgr.skinny_gemm_residual_grouped(dev, config=cfg)
+    torch.cuda.synchronize()
+    for i, (p, y) in enumerate(zip(probs, ys)):
+        if p.A.shape[0] == 0:
+            continue
+        compare(bits(y), oracle_full(p.A, p.W, p.R), f"grouped split expert {i} M={p.A.shape[0]}")
+        sep = sgr.skinny_gemm_residual_ex(dev[i][0], dev[i][1], dev[i][2], config=cfg)
+        torch.cuda.synchronize()
+        assert np.array_equal(bits(sep), bits(y)), i
 
 
 # Untabulated shapes whose default configuration takes the split (slabs of at
